@@ -1,0 +1,18 @@
+"""GB300-native sparse MoE FFN layer: routing, grouping, grouped SwiGLU, combine.
+
+The compute path is the C-ABI library ``libsparse_moe_ffn.so`` built from
+``csrc/`` for sm_103a; ``binding`` wraps it with the same entry-point names.
+There is no CPU fallback: every call fails loudly when the library is missing.
+"""
+from .inputs import CONFIGS, MoEShape, make_inputs, to_device  # noqa: F401
+
+
+def __getattr__(name):
+    # the binding is imported on first use so that the input generators work on
+    # machines without the CUDA library
+    if name in ("moe_route", "moe_align", "moe_forward", "moe_status_string",
+                "moe_align_workspace_bytes", "moe_forward_workspace_bytes",
+                "moe_read_device_status", "binding", "MoEError"):
+        from . import binding
+        return binding if name == "binding" else getattr(binding, name)
+    raise AttributeError(name)
