@@ -1,0 +1,436 @@
+"""Benchmark of the sparse MoE FFN layer (one step = one whole moe_forward:
+routing, grouping, grouped gate/up + SiLU, grouped down + weight, combine).
+
+    python bench.py [--config decode] [--steps K] [--warmup W] [--gpus N]
+    python bench.py --impl reference ...     # the fp64 CPU oracle, timed
+
+Prints ONE JSON line (rank 0).  Under torchrun every rank runs an independent
+replica of the same per-GPU workload (the layer has no cross-GPU step), and
+the value is the tokens of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_moe_ffn_gb300.inputs import CONFIGS, MoEShape, make_inputs, to_device  # noqa: E402
+
+METRIC = "MoE-layer tokens/s & TFLOPS (decode: % HBM roofline; prefill: % bf16 peak)"
+UNIT = "tokens/s"
+WORKLOADS = {
+    "tiny": "tiny MoE layer: N=16, H=64, E=6, top-2, I=128, norm_topk_prob=True",
+    "decode": "Qwen3-30B-A3B-shaped MoE decode: N=64, H=2048, E=128, top-8, I=768, "
+              "norm_topk_prob=True",
+    "prefill": "Qwen3-30B-A3B-shaped MoE prefill: N=8192, H=2048, E=128, top-8, I=768, "
+               "norm_topk_prob=True",
+    "talker": "talker-style MoE with shared expert: N=2048, H=2048, E=64, top-6, I=768, "
+              "I_s=2048, norm_topk_prob=False",
+    "skewed": "skewed-routing stress: N=16384, H=2048, E=128, top-8, I=768, 8 hot experts",
+}
+BOUND = {"tiny": "hbm", "decode": "hbm", "talker": "hbm", "prefill": "tensor", "skewed": "tensor"}
+STAGES = ("route", "align", "gate_up", "down", "shared", "combine")
+SOURCES = {"route": "router.cu", "align": "align.cu", "gate_up": "grouped_gemm.cu",
+           "down": "grouped_gemm.cu", "shared": "grouped_gemm.cu", "combine": "combine.cu"}
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+
+
+# ------------------------------------------------------------------ helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"])}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash(stage):
+    h = hashlib.sha256()
+    for f in sorted({SOURCES[stage], "ptx.cuh", "kernels.cuh"}):
+        with open(os.path.join(ROOT, "sparse_moe_ffn_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(stage, config):
+    """DRAM bytes per launch from a committed ncu capture, if it was taken on
+    the current source of that kernel (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(f"{config}/{stage}")
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_hash") != source_hash(stage):
+        return None
+    return rec.get("bytes_per_launch")
+
+
+def algorithmic_work(shape: MoEShape, touched: int):
+    """Per-stage algorithmic bytes and FLOPs of one layer call (padding rows,
+    re-reads and the act/ypair intermediates are overheads, not work)."""
+    N, H, E, k, I, Is = shape.N, shape.H, shape.E, shape.k, shape.I, shape.I_s
+    P = N * k
+    b = {
+        "route": E * H * 2 + N * H * 2 + P * 8,
+        "align": P * 4 + P * 4,
+        "gate_up": touched * 2 * I * H * 2 + N * H * 2 + P * I * 2,
+        "down": touched * H * I * 2 + P * I * 2 + P * H * 2 + P * 4,
+        "shared": (3 * Is * H * 2 + N * H * 2 + 2 * N * Is * 2 + N * H * 2) if Is else 0,
+        "combine": P * H * 2 + N * H * 2 + (N * H * 2 if Is else 0),
+    }
+    f = {
+        "route": 2 * N * H * (E + (1 if Is else 0)),
+        "align": 0,
+        "gate_up": 4 * H * I * P,
+        "down": 2 * H * I * P,
+        "shared": 6 * H * Is * N if Is else 0,
+        "combine": 0,
+    }
+    layer_flops = 2 * N * H * E + 6 * H * I * P + (N * (6 * H * Is + 2 * H) if Is else 0)
+    layer_bytes = (touched * 3 * H * I * 2 + E * H * 2 + ((3 * H * Is * 2 + 2 * H) if Is else 0)
+                   + 2 * N * H * 2 + P * 8)
+    return b, f, layer_flops, layer_bytes
+
+
+class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons (read only)."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.4)  # nvidia-smi start-up
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return []
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [ln.strip().split(", ") for ln in self.file if ln.strip()]
+        self.file.close()
+        os.unlink(self.file.name)
+        return rows
+
+    @staticmethod
+    def summarize(rows, t0, t1):
+        import datetime
+        def ts(s):
+            try:
+                return datetime.datetime.strptime(s, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                return None
+        parsed = []
+        for r in rows:
+            if len(r) < 10:
+                continue
+            t = ts(r[0])
+            try:
+                sm, smax = float(r[2]), float(r[3])
+            except ValueError:
+                continue
+            parsed.append((t, sm, smax, r[6:10]))
+        if not parsed:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        inside = [p for p in parsed if p[0] is not None and t0 - 0.03 <= p[0] <= t1 + 0.03]
+        use = inside or parsed
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for p in use for i, v in enumerate(p[3])
+                          if v.strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(p[1] for p in use),
+                "sm_max_mhz": max(p[2] for p in use), "reasons": reasons,
+                "samples": len(use), "window": "timed region" if inside else "around the run"}
+
+
+# --------------------------------------------------------------- distributed
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int, device) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------- CPU oracle leg
+
+def oracle_bits(cpu_inputs):
+    import oracle
+    return {n: oracle.bf16_bits(t.to(torch.bfloat16)) for n, t in cpu_inputs.items()}
+
+
+def time_oracle(shape, bits, target_s: float):
+    """Tokens/s of the fp64 oracle on a bounded sample of the workload: whole
+    passes over the first min(N, 64) tokens until target_s has elapsed."""
+    import numpy as np
+    import oracle
+    rows = np.arange(min(shape.N, 64), dtype=np.int64)
+    threads = oracle.hardware_threads()
+    done, t0 = 0, time.perf_counter()
+    while True:
+        oracle.moe_forward(bits, shape.k, shape.norm_topk_prob, rows=rows, nthreads=threads)
+        done += len(rows)
+        el = time.perf_counter() - t0
+        if el >= target_s:
+            break
+    return done / el, threads, done, el
+
+
+# ----------------------------------------------------------------- our arm
+
+def run_ours(args, world, rank, local):
+    from sparse_moe_ffn_gb300 import binding
+
+    shape = CONFIGS[args.config]
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    cpu = make_inputs(shape, seed=args.seed)
+    d = to_device(cpu, device)
+    shared = {n: d[n] for n in binding.SHARED_KEYS} if shape.I_s else None
+    ws = binding.alloc_workspace(shape.N, shape.H, shape.E, shape.I, shape.k, shape.I_s, device)
+    out = torch.empty((shape.N, shape.H), dtype=torch.bfloat16, device=device)
+
+    def step():
+        binding.moe_forward(d["x"], d["router"], d["w_gate"], d["w_up"], d["w_down"], shape.k,
+                            shape.norm_topk_prob, shared, out=out, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    status = binding.moe_read_device_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {status}: {binding.moe_status_string(status)}")
+
+    nst = len(STAGES) + 1
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    sampler.start()
+    launches0 = binding.moe_kernel_launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record()
+    for i in range(args.steps):
+        binding.set_stage_events(ev[i])
+        step()
+    end.record()
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world)
+    binding.set_stage_events(None)
+    launches = binding.moe_kernel_launch_count() - launches0
+    clocks = ClockSampler.summarize(sampler.stop(), t0, t1)
+    ms = start.elapsed_time(end)
+    ms_max = max_over_ranks(ms, world, device)
+    stage_ms = {s: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
+                for j, s in enumerate(STAGES)}
+
+    touched = int((binding.workspace_views(ws, shape.N, shape.H, shape.E, shape.I, shape.k,
+                                           shape.I_s)["counts"] > 0).sum().item())
+    sbytes, sflops, layer_flops, layer_bytes = algorithmic_work(shape, touched)
+    ms_step = ms_max / args.steps
+    value = shape.N * args.steps * world / (ms_max / 1e3)
+    tflops = layer_flops * args.steps * world / (ms_max / 1e3) / 1e12
+
+    # roofline of the dominant kernel (largest share of the step)
+    dom = max(("route", "gate_up", "down", "shared", "combine"), key=lambda s: stage_ms[s])
+    peaks, peak_src = load_peaks()
+    bound = BOUND[args.config]
+    if bound == "tensor" and sflops[dom] == 0:
+        bound = "hbm"
+    if bound == "hbm":
+        achieved = sbytes[dom] / (stage_ms[dom] / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s"}
+    else:
+        achieved = sflops[dom] / (stage_ms[dom] / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    roof.update(frac=round(achieved / roof["peak"], 4), traffic=measured_traffic(dom, args.config),
+                kernel=dom, peak_source=f"{peak_src} (MEASURED_PEAKS.json)" if peak_src ==
+                "measured" else "fallback", algorithmic_per_launch=(
+                    sbytes[dom] if roof["bound"] == "hbm" else sflops[dom]))
+
+    # end to end through the public call with host buffers
+    x_host = cpu["x"].to(torch.bfloat16).pin_memory()
+    out_host = torch.empty((shape.N, shape.H), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(d["x"])
+    weights = {n: t for n, t in d.items() if n != "x"}
+
+    def e2e_step():
+        binding.moe_forward_from_host(x_host, out_host, x_dev, out, weights, shape.k,
+                                      shape.norm_topk_prob, ws)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    barrier(world)
+    torch.cuda.synchronize()
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record()
+    for _ in range(args.steps):
+        e2e_step()
+    e2.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(s2.elapsed_time(e2), world, device)
+    e2e = {"value": round(shape.N * args.steps * world / (e2e_ms / 1e3), 1), "unit": UNIT,
+           "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
+           "d2h_bytes_per_step": out_host.numel() * out_host.element_size()}
+
+    cpu_base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tps, threads, rows, el = time_oracle(shape, oracle_bits(cpu), args.cpu_seconds)
+        cpu_base = {"value": round(tps, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
+                    "sample": f"fp64 C oracle, {rows} token rows (repeated passes over the "
+                              f"first {min(shape.N, 64)} tokens of the same inputs), "
+                              f"{el:.1f} s wall on {threads} threads"}
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights, random init)",
+        "config": {"workload": WORKLOADS[args.config], "N": shape.N, "H": shape.H,
+                   "E": shape.E, "k": shape.k, "I": shape.I, "I_s": shape.I_s,
+                   "norm_topk_prob": shape.norm_topk_prob, "seed": args.seed,
+                   "l2": "inputs larger than L2 (expert weights "
+                         f"{3 * shape.E * shape.H * shape.I * 2 / 1e9:.2f} GB > 129 MB)"
+                         if shape.E * shape.H * shape.I * 6 > 129e6 else
+                         "inputs smaller than L2 (not flushed: latency-bound case)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "tflops": round(tflops, 2),
+        "stage_ms": {s: round(v, 5) for s, v in stage_ms.items()},
+        "experts_touched": touched,
+        "roofline": roof,
+        "cpu_baseline": cpu_base,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------ reference arm
+
+def run_reference(args, world, rank):
+    """The fp64 CPU oracle as the reference arm (host cores, bounded samples)."""
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    shape = CONFIGS[args.config]
+    bits = oracle_bits(make_inputs(shape, seed=args.seed))
+    threads = oracle.hardware_threads()
+    # size each step's sample so that W + K steps take about two minutes
+    probe = np.arange(min(shape.N, threads), dtype=np.int64)
+    t = time.perf_counter()
+    oracle.moe_forward(bits, shape.k, shape.norm_topk_prob, rows=probe, nthreads=threads)
+    per_row = (time.perf_counter() - t) / len(probe)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n_rows = int(max(1, min(shape.N, budget / max(per_row, 1e-9))))
+    rows = np.arange(n_rows, dtype=np.int64)
+    for _ in range(args.warmup):
+        oracle.moe_forward(bits, shape.k, shape.norm_topk_prob, rows=rows, nthreads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.moe_forward(bits, shape.k, shape.norm_topk_prob, rows=rows, nthreads=threads)
+    el = time.perf_counter() - t0
+    value = n_rows * args.steps / el
+    sample = (f"each step: the first {n_rows} of the {shape.N} tokens of the workload, fp64 C "
+              f"oracle on {threads} threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOADS[args.config], "N": shape.N, "H": shape.H, "E": shape.E,
+                   "k": shape.k, "I": shape.I, "I_s": shape.I_s, "seed": args.seed},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="decode", choices=sorted(CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        from sparse_moe_ffn_gb300 import build as lib_build
+        lib_build.build()
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

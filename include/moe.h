@@ -1,0 +1,227 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) sparse MoE FFN layer library
+ * (libsparse_moe_ffn.so).
+ *
+ * The layer is the one defined on the page "M03 · Sparse MoE: routing,
+ * per-expert grouped compute, shared expert" (nano-vllm-omni drills), problem
+ * overview:
+ *
+ *   logits = x @ router^T                     [N, E]
+ *   probs  = softmax(logits) over all E (fp32)
+ *   w, ids = topk(probs, k)                   descending
+ *   if norm_topk_prob: w = w / sum(w)
+ *   out[n] = sum_j w[n,j] * Expert_{ids[n,j]}(x[n]),
+ *   Expert(h) = (silu(h Wg^T) * (h Wu^T)) Wd^T
+ *   talker only: out += sigmoid(x @ g^T) * SharedMLP(x)   (scalar gate per token)
+ *
+ * computed the "serving way" of that page: the N*k (token, slot) pairs are
+ * grouped by expert (stable order, counts, prefix offsets, padded to the GEMM
+ * block as FusedMoE's moe_align_block_size does), each expert runs one
+ * grouped SwiGLU over its gathered tokens, and the weighted results are
+ * accumulated back to every token.
+ *
+ * Conventions shared by every entry point
+ *   - All tensors are dense, row-major, on the current CUDA device, unless a
+ *     parameter says "host".  bf16 data is passed as moe_bf16_t (the raw
+ *     IEEE bfloat16 bit pattern).  Pointers to bf16 matrices must be 16-byte
+ *     aligned; H and I must be multiples of 8 (16-byte rows for TMA).
+ *   - The caller owns every buffer, including the workspace.  The library
+ *     never allocates, frees or synchronises (except moe_read_device_status),
+ *     and keeps no state between calls: calls on different streams with
+ *     different workspaces may run concurrently.
+ *   - Work is enqueued asynchronously on `stream`.  A call returns MOE_OK once
+ *     its kernels are enqueued; device-side failures (a bounded wait that ran
+ *     out, an out-of-range expert id given to moe_align) are recorded in the
+ *     workspace's status word and read with moe_read_device_status.
+ *   - Argument errors return at once and enqueue nothing.  N = 0 is a no-op
+ *     that returns MOE_OK.
+ *   - Routing ties (equal probabilities) go to the lower expert index; slot j
+ *     of a token holds its j-th largest probability.
+ */
+#ifndef SPARSE_MOE_FFN_MOE_H
+#define SPARSE_MOE_FFN_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* IEEE bfloat16 bit pattern. */
+typedef uint16_t moe_bf16_t;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,          /* null pointer, bad size, k > E, misalignment */
+    MOE_ERR_WORKSPACE_TOO_SMALL = 2,  /* workspace_bytes below the *_workspace_bytes value */
+    MOE_ERR_UNSUPPORTED = 3,          /* valid but outside this build's limits (E > 256 ...) */
+    MOE_ERR_CUDA = 4,                 /* a CUDA runtime/driver call failed */
+    MOE_ERR_DEVICE_CHECK = 5,         /* a kernel found a bad value (e.g. expert id >= E) */
+    MOE_ERR_DEVICE_TIMEOUT = 6        /* a kernel's bounded wait ran out; it stopped early */
+} moe_status_t;
+
+/* GEMM row block used by moe_forward: every expert segment is padded to it. */
+#define MOE_BLOCK_M 128
+/* Largest expert count the fused router supports (its MMA tile is <= 256 wide). */
+#define MOE_MAX_EXPERTS 256
+
+/* Static description of a status code.  Never NULL. */
+const char *moe_status_string(moe_status_t status);
+
+/* Detail of the last error returned on the calling thread ("" if none). */
+const char *moe_last_error(void);
+
+/* -------------------------------------------------------------------------
+ * moe_route -- the routing block of the M03 problem overview (logits, fp32
+ * softmax over all E experts, top-k, optional norm_topk_prob renorm), plus
+ * the talker's scalar shared-expert gate sigmoid(x . g).  Also the router of
+ * the Nano-vLLM notes' Qwen3MoeSparseMoeBlock (softmax in fp32, topk, renorm).
+ *
+ *   x            [N, H] bf16
+ *   router       [E, H] bf16
+ *   shared_gate  [1, H] bf16 or NULL
+ *   topk_w       [N, k] fp32 out: routing weights (renormalised iff
+ *                norm_topk_prob != 0)
+ *   topk_ids     [N, k] int32 out: expert ids, slot 0 = largest probability
+ *   topk_w_bf16  [N, k] bf16 out or NULL: topk_w rounded to nearest even
+ *                (the pages return weights in x's dtype)
+ *   shared_gamma [N]    fp32 out: sigmoid(x . g); required iff shared_gate
+ *   workspace    >= moe_route_workspace_bytes() bytes, or NULL (then device
+ *                failures are not recorded)
+ * Limits: 1 <= k <= E <= 256 (E <= 248 with a shared gate), H % 8 == 0.
+ * ---------------------------------------------------------------------- */
+size_t moe_route_workspace_bytes(void);
+moe_status_t moe_route(const moe_bf16_t *x, const moe_bf16_t *router,
+                       const moe_bf16_t *shared_gate, int64_t N, int H, int E,
+                       int k, int norm_topk_prob, float *topk_w,
+                       int32_t *topk_ids, moe_bf16_t *topk_w_bf16,
+                       float *shared_gamma, void *workspace,
+                       size_t workspace_bytes, cudaStream_t stream);
+
+/* -------------------------------------------------------------------------
+ * moe_align -- the grouping bookkeeping of the M03 walk-through (flatten the
+ * pairs p = n*k + j row-major, stable sort by expert, per-expert counts,
+ * prefix-sum segment starts), padded to block_m rows per expert segment as
+ * FusedMoE's moe_align_block_size (named in the M03 shape-trace section).
+ *
+ *   topk_ids     [N, k] int32 in, each in [0, E)
+ *   sorted_pair  [cap] int32 out, cap = moe_align_capacity(N, k, E, block_m):
+ *                expert e's pairs in ascending p start at
+ *                pad_off[e] = sum_{e'<e} round_up(counts[e'], block_m), followed
+ *                by the sentinel N*k up to the next multiple of block_m.
+ *                Slots >= *num_padded are left unspecified.
+ *   block_expert [cap / block_m] int32 out: owner expert of each row block
+ *                (entries >= *num_padded / block_m unspecified)
+ *   counts       [E] int32 out: pairs per expert (sum = N*k)
+ *   offsets      [E+1] int32 out: exclusive prefix sum of counts
+ *   num_padded   [1] int32 out: pad_off[E]
+ *   workspace    >= moe_align_workspace_bytes(...) bytes (scratch + status)
+ * An id outside [0, E) is skipped and records MOE_ERR_DEVICE_CHECK.
+ * Limits: 1 <= E <= 1024, 1 <= block_m <= 1024, N*k + E*block_m < 2^31.
+ * ---------------------------------------------------------------------- */
+int64_t moe_align_capacity(int64_t N, int k, int E, int block_m);
+size_t moe_align_workspace_bytes(int64_t N, int k, int E, int block_m);
+moe_status_t moe_align(const int32_t *topk_ids, int64_t N, int k, int E,
+                       int block_m, int32_t *sorted_pair, int32_t *block_expert,
+                       int32_t *counts, int32_t *offsets, int32_t *num_padded,
+                       void *workspace, size_t workspace_bytes,
+                       cudaStream_t stream);
+
+/* -------------------------------------------------------------------------
+ * moe_forward -- the whole layer (M03 problem overview and its "serving way";
+ * the shared expert of the same page and of the talker MoE block in the
+ * vLLM Qwen3.5 walkthrough, section "2.5B Sparse MoE").
+ *
+ *   x                 [N, H] bf16
+ *   router            [E, H] bf16
+ *   w_gate, w_up      [E, I, H] bf16
+ *   w_down            [E, H, I] bf16
+ *   shared_gate_proj  [I_s, H] bf16 \
+ *   shared_up_proj    [I_s, H] bf16  | all four NULL: no shared expert
+ *   shared_down_proj  [H, I_s] bf16  | (I_s ignored); all four set: shared
+ *   shared_gate       [1, H]   bf16 /  expert with I_s >= 8, I_s % 8 == 0
+ *   out               [N, H] bf16 out (may not alias any input)
+ *   workspace         >= moe_forward_workspace_bytes(...) bytes, 256-byte
+ *                     aligned; holds the routing, grouping and intermediate
+ *                     activations (layout: moe_forward_layout)
+ * Precision: bf16 inputs, fp32 routing and accumulation, the gate/up
+ * activation silu(g)*u and each pair's weighted down projection are rounded
+ * to bf16 once, the k contributions (and the shared expert) are summed in
+ * fp32 in slot order, and out is rounded to bf16.  The result does not depend
+ * on the other tokens of the batch, and is bitwise reproducible.
+ * Limits: as moe_route, plus I % 8 == 0, N*k + E*128 < 2^31.
+ * ---------------------------------------------------------------------- */
+size_t moe_forward_workspace_bytes(int64_t N, int H, int E, int I, int k, int I_s);
+moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router,
+                         const moe_bf16_t *w_gate, const moe_bf16_t *w_up,
+                         const moe_bf16_t *w_down,
+                         const moe_bf16_t *shared_gate_proj,
+                         const moe_bf16_t *shared_up_proj,
+                         const moe_bf16_t *shared_down_proj,
+                         const moe_bf16_t *shared_gate, int64_t N, int H, int E,
+                         int I, int I_s, int k, int norm_topk_prob,
+                         moe_bf16_t *out, void *workspace,
+                         size_t workspace_bytes, cudaStream_t stream);
+
+/* Byte offsets of moe_forward's workspace sub-buffers (for inspecting the
+ * intermediate results; every offset is 256-byte aligned). */
+typedef struct {
+    size_t status;        /* int32 device status word (a moe_status_t)       */
+    size_t topk_w;        /* fp32 [N, k]                                      */
+    size_t topk_ids;      /* int32 [N, k]                                     */
+    size_t gamma;         /* fp32 [N] (shared expert only)                    */
+    size_t counts;        /* int32 [E]                                        */
+    size_t offsets;       /* int32 [E+1]                                      */
+    size_t pad_offsets;   /* int32 [E+1]                                      */
+    size_t num_padded;    /* int32 [1]                                        */
+    size_t align_scratch; /* int32 [chunks, E]                                */
+    size_t sorted_pair;   /* int32 [capacity]                                 */
+    size_t block_expert;  /* int32 [capacity / 128]                           */
+    size_t act;           /* bf16 [capacity, I]   silu(x Wg^T) * (x Wu^T)     */
+    size_t ypair;         /* bf16 [N*k, H]        w * Expert(x), per pair     */
+    size_t act_shared;    /* bf16 [round_up(N,128), I_s] (shared only)        */
+    size_t y_shared;      /* bf16 [N, H]  gamma * SharedMLP(x) (shared only)  */
+    size_t total;         /* = moe_forward_workspace_bytes                    */
+    int64_t capacity;     /* moe_align_capacity(N, k, E, 128)                 */
+} moe_forward_layout_t;
+
+moe_status_t moe_forward_layout(int64_t N, int H, int E, int I, int k, int I_s,
+                                moe_forward_layout_t *layout);
+
+/* Waits for `stream`, then returns the status word kept in `workspace` by the
+ * last moe_route / moe_align / moe_forward call that used it (MOE_OK if no
+ * kernel recorded a failure).  The only synchronising entry point. */
+moe_status_t moe_read_device_status(const void *workspace, cudaStream_t stream);
+
+/* -------------------------------------------------------------------------
+ * Instrumentation
+ * ---------------------------------------------------------------------- */
+
+/* Stages of moe_forward, in launch order. */
+enum {
+    MOE_STAGE_ROUTE = 0,
+    MOE_STAGE_ALIGN = 1,
+    MOE_STAGE_GATE_UP = 2,
+    MOE_STAGE_DOWN = 3,
+    MOE_STAGE_SHARED = 4, /* shared expert gate/up + down (empty without one) */
+    MOE_STAGE_COMBINE = 5,
+    MOE_NUM_STAGES = 6
+};
+
+/* Total number of kernels this library has launched in the process. */
+uint64_t moe_kernel_launch_count(void);
+
+/* Ask the next moe_forward calls on this thread to record events[i] (created
+ * by the caller with timing enabled) on their stream before stage i, and
+ * events[MOE_NUM_STAGES] after the last stage.  n_events must be
+ * MOE_NUM_STAGES + 1, or 0 with events NULL to stop recording. */
+moe_status_t moe_set_stage_events(cudaEvent_t *events, int n_events);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPARSE_MOE_FFN_MOE_H */

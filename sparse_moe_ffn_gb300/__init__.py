@@ -4,15 +4,18 @@ The compute path is the C-ABI library ``libsparse_moe_ffn.so`` built from
 ``csrc/`` for sm_103a; ``binding`` wraps it with the same entry-point names.
 There is no CPU fallback: every call fails loudly when the library is missing.
 """
+import importlib
+
 from .inputs import CONFIGS, MoEShape, make_inputs, to_device  # noqa: F401
+
+_BINDING_NAMES = ("moe_route", "moe_route_raw", "moe_align", "moe_forward",
+                  "moe_status_string", "moe_forward_workspace_bytes", "moe_forward_layout",
+                  "moe_read_device_status", "alloc_workspace", "MoEError")
 
 
 def __getattr__(name):
     # the binding is imported on first use so that the input generators work on
     # machines without the CUDA library
-    if name in ("moe_route", "moe_align", "moe_forward", "moe_status_string",
-                "moe_align_workspace_bytes", "moe_forward_workspace_bytes",
-                "moe_read_device_status", "binding", "MoEError"):
-        from . import binding
-        return binding if name == "binding" else getattr(binding, name)
+    if name in _BINDING_NAMES:
+        return getattr(importlib.import_module(".binding", __name__), name)
     raise AttributeError(name)

@@ -1,0 +1,262 @@
+"""ctypes binding of libsparse_moe_ffn.so, with the same entry-point names as
+include/moe.h.  Argument marshalling only: torch tensors supply device
+pointers and the current stream; every step of the layer runs in the
+library's CUDA kernels.  There is no fallback: a missing library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB
+
+MOE_OK = 0
+MOE_BLOCK_M = 128
+MOE_NUM_STAGES = 6
+STAGE_NAMES = ("route", "align", "gate_up", "down", "shared", "combine")
+SHARED_KEYS = ("shared_gate_proj", "shared_up_proj", "shared_down_proj", "shared_gate")
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{message} (status {status})")
+        self.status = status
+
+
+class _Layout(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_size_t) for name in (
+        "status", "topk_w", "topk_ids", "gamma", "counts", "offsets", "pad_offsets",
+        "num_padded", "align_scratch", "sorted_pair", "block_expert", "act", "ypair",
+        "act_shared", "y_shared", "total")] + [("capacity", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB):
+        raise RuntimeError(f"{LIB} is missing: build it first (python -m sparse_moe_ffn_gb300.build)")
+    L = ctypes.CDLL(LIB)
+    P, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    sig = {
+        "moe_status_string": ([i32], ctypes.c_char_p),
+        "moe_last_error": ([], ctypes.c_char_p),
+        "moe_route_workspace_bytes": ([], sz),
+        "moe_route": ([P, P, P, i64, i32, i32, i32, i32, P, P, P, P, P, sz, P], i32),
+        "moe_align_capacity": ([i64, i32, i32, i32], i64),
+        "moe_align_workspace_bytes": ([i64, i32, i32, i32], sz),
+        "moe_align": ([P, i64, i32, i32, i32, P, P, P, P, P, P, sz, P], i32),
+        "moe_forward_workspace_bytes": ([i64, i32, i32, i32, i32, i32], sz),
+        "moe_forward": ([P] * 9 + [i64, i32, i32, i32, i32, i32, i32, P, P, sz, P], i32),
+        "moe_forward_layout": ([i64, i32, i32, i32, i32, i32, ctypes.POINTER(_Layout)], i32),
+        "moe_read_device_status": ([P, P], i32),
+        "moe_kernel_launch_count": ([], ctypes.c_uint64),
+        "moe_set_stage_events": ([P, i32], i32),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = L
+    return L
+
+
+def _check(status: int, what: str) -> None:
+    if status != MOE_OK:
+        L = lib()
+        detail = L.moe_last_error().decode()
+        raise MoEError(status, f"{what}: {L.moe_status_string(status).decode()}"
+                               + (f" -- {detail}" if detail else ""))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _bf16(t, name, shape=None):
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+def moe_status_string(status: int) -> str:
+    return lib().moe_status_string(status).decode()
+
+
+def moe_kernel_launch_count() -> int:
+    return int(lib().moe_kernel_launch_count())
+
+
+def moe_route_raw(x, router, k: int, norm_topk_prob: bool, shared_gate=None,
+                  want_bf16: bool = False):
+    """Routing in the library's own types: (topk_w fp32 [N,k], topk_ids int32
+    [N,k], gamma fp32 [N] or None, topk_w_bf16 or None)."""
+    N, H = x.shape
+    E = router.shape[0]
+    _bf16(x, "x")
+    _bf16(router, "router", (E, H))
+    if shared_gate is not None:
+        _bf16(shared_gate, "shared_gate", (1, H))
+    dev = x.device
+    w = torch.empty((N, k), dtype=torch.float32, device=dev)
+    ids = torch.empty((N, k), dtype=torch.int32, device=dev)
+    wb = torch.empty((N, k), dtype=torch.bfloat16, device=dev) if want_bf16 else None
+    gamma = torch.empty(N, dtype=torch.float32, device=dev) if shared_gate is not None else None
+    ws = torch.empty(lib().moe_route_workspace_bytes(), dtype=torch.uint8, device=dev)
+    _check(lib().moe_route(_ptr(x), _ptr(router), _ptr(shared_gate), N, H, E, k,
+                           int(bool(norm_topk_prob)), _ptr(w), _ptr(ids), _ptr(wb), _ptr(gamma),
+                           _ptr(ws), ws.numel(), _stream()), "moe_route")
+    return w, ids, gamma, wb
+
+
+def moe_route(x, router, k: int, norm_topk_prob: bool = True):
+    """The pages' route(): (weights in x.dtype, ids int64), each [N, k]."""
+    _, ids, _, wb = moe_route_raw(x, router, k, norm_topk_prob, want_bf16=True)
+    return wb, ids.long()
+
+
+def moe_align(topk_ids, E: int, block_m: int = MOE_BLOCK_M):
+    """Grouping of the pairs by expert; returns a dict of CUDA tensors."""
+    if topk_ids.dtype != torch.int32 or not topk_ids.is_cuda or not topk_ids.is_contiguous():
+        raise ValueError("topk_ids must be a contiguous int32 CUDA tensor")
+    N, k = topk_ids.shape
+    L = lib()
+    cap = int(L.moe_align_capacity(N, k, E, block_m))
+    dev = topk_ids.device
+    sp = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)
+    be = torch.empty(max(cap // block_m, 1), dtype=torch.int32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    npad = torch.empty(1, dtype=torch.int32, device=dev)
+    wsb = int(L.moe_align_workspace_bytes(N, k, E, block_m))
+    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+    _check(L.moe_align(_ptr(topk_ids), N, k, E, block_m, _ptr(sp), _ptr(be), _ptr(counts),
+                       _ptr(offsets), _ptr(npad), _ptr(ws), wsb, _stream()), "moe_align")
+    return {"sorted_pair": sp, "block_expert": be, "counts": counts, "offsets": offsets,
+            "num_padded": npad, "capacity": cap, "workspace": ws}
+
+
+def moe_forward_layout(N, H, E, I, k, I_s=0) -> dict:
+    lay = _Layout()
+    _check(lib().moe_forward_layout(N, H, E, I, k, I_s, ctypes.byref(lay)), "moe_forward_layout")
+    return {name: getattr(lay, name) for name, _ in _Layout._fields_}
+
+
+def moe_forward_workspace_bytes(N, H, E, I, k, I_s=0) -> int:
+    return int(lib().moe_forward_workspace_bytes(N, H, E, I, k, I_s))
+
+
+def alloc_workspace(N, H, E, I, k, I_s=0, device="cuda"):
+    """A workspace tensor for moe_forward (the caller owns it and may reuse it)."""
+    return torch.empty(max(moe_forward_workspace_bytes(N, H, E, I, k, I_s), 256),
+                       dtype=torch.uint8, device=device)
+
+
+def moe_forward(x, router, w_gate, w_up, w_down, k: int, norm_topk_prob: bool = True,
+                shared=None, out=None, workspace=None):
+    """The whole layer.  ``shared`` is None or a dict with shared_gate_proj,
+    shared_up_proj, shared_down_proj and shared_gate.  Returns out [N, H] bf16."""
+    N, H = x.shape
+    E, I, _ = w_gate.shape
+    _bf16(x, "x")
+    _bf16(router, "router", (E, H))
+    _bf16(w_gate, "w_gate", (E, I, H))
+    _bf16(w_up, "w_up", (E, I, H))
+    _bf16(w_down, "w_down", (E, H, I))
+    sp = [None] * 4
+    I_s = 0
+    if shared is not None:
+        sp = [shared[n] for n in SHARED_KEYS]
+        I_s = sp[0].shape[0]
+        _bf16(sp[0], "shared_gate_proj", (I_s, H))
+        _bf16(sp[1], "shared_up_proj", (I_s, H))
+        _bf16(sp[2], "shared_down_proj", (H, I_s))
+        _bf16(sp[3], "shared_gate", (1, H))
+    if out is None:
+        out = torch.empty((N, H), dtype=torch.bfloat16, device=x.device)
+    _bf16(out, "out", (N, H))
+    if workspace is None:
+        workspace = alloc_workspace(N, H, E, I, k, I_s, x.device)
+    _check(lib().moe_forward(_ptr(x), _ptr(router), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
+                             *[_ptr(t) for t in sp], N, H, E, I, I_s, k,
+                             int(bool(norm_topk_prob)), _ptr(out), _ptr(workspace),
+                             workspace.numel(), _stream()), "moe_forward")
+    return out
+
+
+def moe_forward_from_host(x_host, out_host, x_dev, out_dev, weights: dict, k: int,
+                          norm_topk_prob: bool, workspace):
+    """End-to-end call with host buffers: copy x (pinned host) to the device,
+    run the layer, copy the result back to pinned host memory, all on the
+    current stream.  Weights stay resident on the device."""
+    x_dev.copy_(x_host, non_blocking=True)
+    shared = {n: weights[n] for n in SHARED_KEYS} if "shared_gate" in weights else None
+    moe_forward(x_dev, weights["router"], weights["w_gate"], weights["w_up"], weights["w_down"],
+                k, norm_topk_prob, shared, out=out_dev, workspace=workspace)
+    out_host.copy_(out_dev, non_blocking=True)
+    return out_host
+
+
+def workspace_views(workspace, N, H, E, I, k, I_s=0) -> dict:
+    """Typed views of moe_forward's intermediate buffers inside ``workspace``."""
+    lay = moe_forward_layout(N, H, E, I, k, I_s)
+    cap = lay["capacity"]
+    P = N * k
+    base = workspace
+
+    def view(off, dtype, shape):
+        n = 1
+        for s in shape:
+            n *= s
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        return base[off:off + nbytes].view(dtype).view(shape)
+
+    v = {
+        "status": view(lay["status"], torch.int32, (1,)),
+        "topk_w": view(lay["topk_w"], torch.float32, (N, k)),
+        "topk_ids": view(lay["topk_ids"], torch.int32, (N, k)),
+        "counts": view(lay["counts"], torch.int32, (E,)),
+        "offsets": view(lay["offsets"], torch.int32, (E + 1,)),
+        "pad_offsets": view(lay["pad_offsets"], torch.int32, (E + 1,)),
+        "num_padded": view(lay["num_padded"], torch.int32, (1,)),
+        "sorted_pair": view(lay["sorted_pair"], torch.int32, (cap,)),
+        "block_expert": view(lay["block_expert"], torch.int32, (cap // MOE_BLOCK_M,)),
+        "act": view(lay["act"], torch.bfloat16, (cap, I)),
+        "ypair": view(lay["ypair"], torch.bfloat16, (P, H)),
+    }
+    if I_s:
+        rows_s = -(-N // MOE_BLOCK_M) * MOE_BLOCK_M
+        v["gamma"] = view(lay["gamma"], torch.float32, (N,))
+        v["act_shared"] = view(lay["act_shared"], torch.bfloat16, (rows_s, I_s))
+        v["y_shared"] = view(lay["y_shared"], torch.bfloat16, (N, H))
+    return v
+
+
+def moe_read_device_status(workspace) -> int:
+    """Synchronise the current stream and return the workspace's status word."""
+    return int(lib().moe_read_device_status(_ptr(workspace), _stream()))
+
+
+def set_stage_events(events) -> None:
+    """Record the given torch.cuda.Event objects around the stages of the next
+    moe_forward calls on this thread (None to stop)."""
+    L = lib()
+    if events is None:
+        _check(L.moe_set_stage_events(None, 0), "moe_set_stage_events")
+        return
+    if len(events) != MOE_NUM_STAGES + 1:
+        raise ValueError(f"need {MOE_NUM_STAGES + 1} events")
+    arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    _check(L.moe_set_stage_events(arr, len(events)), "moe_set_stage_events")

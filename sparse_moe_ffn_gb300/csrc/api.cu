@@ -1,0 +1,540 @@
+// api.cu -- the C ABI of libsparse_moe_ffn (declared in include/moe.h):
+// argument checks, workspace carving, TMA tensor maps and kernel launches.
+// Host code only; it allocates nothing, frees nothing and synchronises
+// nothing (except moe_read_device_status).
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "kernels.cuh"
+#include "moe.h"
+
+using namespace moe;
+
+namespace {
+
+thread_local std::string g_last_error;
+thread_local cudaEvent_t g_stage_events[MOE_NUM_STAGES + 1];
+thread_local bool g_stage_events_on = false;
+std::atomic<uint64_t> g_launches{0};
+
+moe_status_t fail(moe_status_t s, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+moe_status_t cuda_fail(cudaError_t e, const char *what) {
+    return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define MOE_CUDA(call, what)                                   \
+    do {                                                       \
+        cudaError_t e_ = (call);                               \
+        if (e_ != cudaSuccess) return cuda_fail(e_, (what));   \
+    } while (0)
+
+constexpr size_t kAlign = 256;
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+int64_t round_up64(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// --------------------------------------------------------------- tensor maps
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// bf16 matrix [rows, cols] (row stride `ld` elements), 128-byte swizzled box
+// of box_rows x box_cols (box_cols * 2 <= 128).  Out-of-range elements read 0.
+moe_status_t make_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows,
+                      uint64_t ld, uint32_t box_cols, uint32_t box_rows, const char *what) {
+    auto fn = encode_tiled();
+    if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {ld * 2};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(MOE_ERR_CUDA, "tensor map for %s rejected (CUresult %d)", what,
+                    static_cast<int>(r));
+    return MOE_OK;
+}
+
+int num_sms_of_current_device() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (cache[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = n > 0 ? n : 148;
+    }
+    return cache[dev];
+}
+
+void record_stage(int i, cudaStream_t s) {
+    if (g_stage_events_on) cudaEventRecord(g_stage_events[i], s);
+}
+
+// ------------------------------------------------------------------ layouts
+
+int align_chunks(int64_t P) { return static_cast<int>((P + kAlignChunk - 1) / kAlignChunk); }
+
+int router_e_pad(int E, bool shared) {
+    const int e8 = (E + 7) / 8 * 8;
+    const int cols = shared ? e8 + 8 : E;
+    return (cols < 16 ? 16 : (cols + 15) / 16 * 16);
+}
+
+moe_status_t check_route_args(const void *x, const void *router, const void *shared_gate,
+                              int64_t N, int H, int E, int k, float *topk_w, int32_t *topk_ids,
+                              float *gamma) {
+    if (N < 0) return fail(MOE_ERR_INVALID_ARG, "N must be >= 0 (got %lld)", (long long)N);
+    if (H < 8 || H % 8) return fail(MOE_ERR_INVALID_ARG, "H must be a positive multiple of 8 (got %d)", H);
+    if (E < 1) return fail(MOE_ERR_INVALID_ARG, "E must be >= 1 (got %d)", E);
+    if (k < 1 || k > E) return fail(MOE_ERR_INVALID_ARG, "k must be in [1, E] (k=%d, E=%d)", k, E);
+    if (router_e_pad(E, shared_gate != nullptr) > MOE_MAX_EXPERTS)
+        return fail(MOE_ERR_UNSUPPORTED, "E=%d exceeds the fused router's limit", E);
+    if (N == 0) return MOE_OK;
+    if (!x || !router || !topk_w || !topk_ids)
+        return fail(MOE_ERR_INVALID_ARG, "x, router, topk_w and topk_ids must be non-null");
+    if (shared_gate && !gamma)
+        return fail(MOE_ERR_INVALID_ARG, "shared_gamma must be given with shared_gate");
+    if (!aligned16(x) || !aligned16(router) || (shared_gate && !aligned16(shared_gate)))
+        return fail(MOE_ERR_INVALID_ARG, "bf16 matrices must be 16-byte aligned");
+    if (N > (int64_t(1) << 31) / k)
+        return fail(MOE_ERR_UNSUPPORTED, "N*k must stay below 2^31");
+    return MOE_OK;
+}
+
+moe_status_t enqueue_route(const moe_bf16_t *x, const moe_bf16_t *router,
+                           const moe_bf16_t *shared_gate, int64_t N, int H, int E, int k,
+                           int norm, float *topk_w, int32_t *topk_ids, moe_bf16_t *topk_w_bf16,
+                           float *gamma, int32_t *status, cudaStream_t stream) {
+    const bool shared = shared_gate != nullptr;
+    RouterArgs ra;
+    ra.N = N;
+    ra.H = H;
+    ra.E = E;
+    ra.k = k;
+    ra.norm = norm ? 1 : 0;
+    ra.e_pad = router_e_pad(E, shared);
+    ra.gamma_col = shared ? (E + 7) / 8 * 8 : -1;
+    ra.topk_w = topk_w;
+    ra.topk_ids = topk_ids;
+    ra.topk_w_bf16 = topk_w_bf16;
+    ra.gamma = gamma;
+    ra.status = status;
+    CUtensorMap tm_x, tm_r, tm_g;
+    moe_status_t st;
+    if ((st = make_map(&tm_x, x, H, N, H, kBlockK, kBlockM, "x")) != MOE_OK) return st;
+    if ((st = make_map(&tm_r, router, H, E, H, kBlockK, E, "router")) != MOE_OK) return st;
+    if (shared) {
+        if ((st = make_map(&tm_g, shared_gate, H, 1, H, kBlockK, 8, "shared_gate")) != MOE_OK)
+            return st;
+    } else {
+        tm_g = tm_r;  // unused placeholder
+    }
+    MOE_CUDA(launch_router(tm_x, tm_r, tm_g, ra, stream), "router kernel launch");
+    g_launches += 1;
+    return MOE_OK;
+}
+
+struct AlignBuffers {
+    int32_t *sorted_pair, *block_expert, *counts, *offsets, *pad_offsets, *num_padded, *scratch;
+    int32_t *status;
+};
+
+moe_status_t enqueue_align(const int32_t *ids, int64_t N, int k, int E, int block_m,
+                           const AlignBuffers &b, cudaStream_t stream) {
+    AlignArgs aa;
+    aa.ids = ids;
+    aa.P = N * k;
+    aa.E = E;
+    aa.block_m = block_m;
+    aa.chunk = kAlignChunk;
+    aa.nchunks = align_chunks(aa.P);
+    aa.chunk_counts = b.scratch;
+    aa.counts = b.counts;
+    aa.offsets = b.offsets;
+    aa.pad_offsets = b.pad_offsets;
+    aa.num_padded = b.num_padded;
+    aa.sorted_pair = b.sorted_pair;
+    aa.block_expert = b.block_expert;
+    aa.status = b.status;
+    int launches = 0;
+    cudaError_t e = launch_align(aa, stream, &launches);
+    g_launches += launches;
+    if (e != cudaSuccess) return cuda_fail(e, "align kernel launch");
+    return MOE_OK;
+}
+
+moe_status_t forward_layout(int64_t N, int H, int E, int I, int k, int I_s,
+                            moe_forward_layout_t *L) {
+    const int64_t P = N * k;
+    const bool shared = I_s > 0;
+    const int64_t cap = moe_align_capacity(N, k, E, kBlockM);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = round_up(off + bytes, kAlign);
+        return at;
+    };
+    L->status = take(4);
+    L->topk_w = take(sizeof(float) * P);
+    L->topk_ids = take(sizeof(int32_t) * P);
+    L->gamma = take(shared ? sizeof(float) * N : 0);
+    L->counts = take(sizeof(int32_t) * E);
+    L->offsets = take(sizeof(int32_t) * (E + 1));
+    L->pad_offsets = take(sizeof(int32_t) * (E + 1));
+    L->num_padded = take(sizeof(int32_t));
+    L->align_scratch = take(sizeof(int32_t) * static_cast<size_t>(align_chunks(P)) * E);
+    L->sorted_pair = take(sizeof(int32_t) * cap);
+    L->block_expert = take(sizeof(int32_t) * (cap / kBlockM));
+    L->act = take(2 * static_cast<size_t>(cap) * I);
+    L->ypair = take(2 * static_cast<size_t>(P) * H);
+    L->act_shared = take(shared ? 2 * static_cast<size_t>(round_up64(N, kBlockM)) * I_s : 0);
+    L->y_shared = take(shared ? 2 * static_cast<size_t>(N) * H : 0);
+    L->total = off;
+    L->capacity = cap;
+    return MOE_OK;
+}
+
+}  // namespace
+
+// =========================================================================
+extern "C" {
+
+const char *moe_status_string(moe_status_t s) {
+    switch (s) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case MOE_ERR_UNSUPPORTED: return "unsupported size";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_DEVICE_CHECK: return "device-side check failed (bad input value)";
+        case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+const char *moe_last_error(void) { return g_last_error.c_str(); }
+
+uint64_t moe_kernel_launch_count(void) { return g_launches.load(); }
+
+moe_status_t moe_set_stage_events(cudaEvent_t *events, int n_events) {
+    if (n_events == 0 && events == nullptr) {
+        g_stage_events_on = false;
+        return MOE_OK;
+    }
+    if (!events || n_events != MOE_NUM_STAGES + 1)
+        return fail(MOE_ERR_INVALID_ARG, "need %d events", MOE_NUM_STAGES + 1);
+    for (int i = 0; i <= MOE_NUM_STAGES; ++i) g_stage_events[i] = events[i];
+    g_stage_events_on = true;
+    return MOE_OK;
+}
+
+size_t moe_route_workspace_bytes(void) { return kAlign; }
+
+moe_status_t moe_route(const moe_bf16_t *x, const moe_bf16_t *router,
+                       const moe_bf16_t *shared_gate, int64_t N, int H, int E, int k,
+                       int norm_topk_prob, float *topk_w, int32_t *topk_ids,
+                       moe_bf16_t *topk_w_bf16, float *shared_gamma, void *workspace,
+                       size_t workspace_bytes, cudaStream_t stream) {
+    g_last_error.clear();
+    moe_status_t st = check_route_args(x, router, shared_gate, N, H, E, k, topk_w, topk_ids,
+                                       shared_gamma);
+    if (st != MOE_OK || N == 0) return st;
+    if (workspace && workspace_bytes < moe_route_workspace_bytes())
+        return fail(MOE_ERR_WORKSPACE_TOO_SMALL, "route workspace needs %zu bytes",
+                    moe_route_workspace_bytes());
+    int32_t *status = static_cast<int32_t *>(workspace);
+    if (status) MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int32_t), stream), "status reset");
+    return enqueue_route(x, router, shared_gate, N, H, E, k, norm_topk_prob, topk_w, topk_ids,
+                         topk_w_bf16, shared_gamma, status, stream);
+}
+
+int64_t moe_align_capacity(int64_t N, int k, int E, int block_m) {
+    if (N < 0 || k < 1 || E < 1 || block_m < 1) return 0;
+    return round_up64(N * k + static_cast<int64_t>(E) * (block_m - 1), block_m);
+}
+
+size_t moe_align_workspace_bytes(int64_t N, int k, int E, int block_m) {
+    if (N < 0 || k < 1 || E < 1 || block_m < 1) return 0;
+    return kAlign + round_up(sizeof(int32_t) * (E + 1), kAlign) +
+           round_up(sizeof(int32_t) * static_cast<size_t>(align_chunks(N * k)) * E, kAlign);
+}
+
+moe_status_t moe_align(const int32_t *topk_ids, int64_t N, int k, int E, int block_m,
+                       int32_t *sorted_pair, int32_t *block_expert, int32_t *counts,
+                       int32_t *offsets, int32_t *num_padded, void *workspace,
+                       size_t workspace_bytes, cudaStream_t stream) {
+    g_last_error.clear();
+    if (N < 0 || k < 1 || E < 1 || block_m < 1)
+        return fail(MOE_ERR_INVALID_ARG, "need N >= 0, k >= 1, E >= 1, block_m >= 1");
+    if (E > 1024 || block_m > 1024)
+        return fail(MOE_ERR_UNSUPPORTED, "E and block_m must be <= 1024");
+    if (N * k + static_cast<int64_t>(E) * block_m >= (int64_t(1) << 31))
+        return fail(MOE_ERR_UNSUPPORTED, "N*k + E*block_m must stay below 2^31");
+    if (N == 0) return MOE_OK;
+    if (!topk_ids || !sorted_pair || !block_expert || !counts || !offsets || !num_padded ||
+        !workspace)
+        return fail(MOE_ERR_INVALID_ARG, "every moe_align pointer must be non-null");
+    const size_t need = moe_align_workspace_bytes(N, k, E, block_m);
+    if (workspace_bytes < need)
+        return fail(MOE_ERR_WORKSPACE_TOO_SMALL, "align workspace needs %zu bytes, got %zu", need,
+                    workspace_bytes);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    AlignBuffers b;
+    b.status = reinterpret_cast<int32_t *>(ws);
+    b.pad_offsets = reinterpret_cast<int32_t *>(ws + kAlign);
+    b.scratch = reinterpret_cast<int32_t *>(ws + kAlign + round_up(sizeof(int32_t) * (E + 1), kAlign));
+    b.sorted_pair = sorted_pair;
+    b.block_expert = block_expert;
+    b.counts = counts;
+    b.offsets = offsets;
+    b.num_padded = num_padded;
+    MOE_CUDA(cudaMemsetAsync(b.status, 0, sizeof(int32_t), stream), "status reset");
+    return enqueue_align(topk_ids, N, k, E, block_m, b, stream);
+}
+
+moe_status_t moe_forward_layout(int64_t N, int H, int E, int I, int k, int I_s,
+                                moe_forward_layout_t *layout) {
+    if (!layout) return fail(MOE_ERR_INVALID_ARG, "layout must be non-null");
+    if (N < 0 || H < 1 || E < 1 || I < 1 || k < 1 || I_s < 0)
+        return fail(MOE_ERR_INVALID_ARG, "bad sizes");
+    return forward_layout(N, H, E, I, k, I_s, layout);
+}
+
+size_t moe_forward_workspace_bytes(int64_t N, int H, int E, int I, int k, int I_s) {
+    moe_forward_layout_t L;
+    if (N < 0 || H < 1 || E < 1 || I < 1 || k < 1 || I_s < 0) return 0;
+    forward_layout(N, H, E, I, k, I_s, &L);
+    return L.total;
+}
+
+moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const moe_bf16_t *w_gate,
+                         const moe_bf16_t *w_up, const moe_bf16_t *w_down,
+                         const moe_bf16_t *shared_gate_proj, const moe_bf16_t *shared_up_proj,
+                         const moe_bf16_t *shared_down_proj, const moe_bf16_t *shared_gate,
+                         int64_t N, int H, int E, int I, int I_s, int k, int norm_topk_prob,
+                         moe_bf16_t *out, void *workspace, size_t workspace_bytes,
+                         cudaStream_t stream) {
+    g_last_error.clear();
+    const int nshared = (shared_gate_proj != nullptr) + (shared_up_proj != nullptr) +
+                        (shared_down_proj != nullptr) + (shared_gate != nullptr);
+    if (nshared != 0 && nshared != 4)
+        return fail(MOE_ERR_INVALID_ARG,
+                    "give all four shared-expert tensors or none (got %d of 4)", nshared);
+    const bool shared = nshared == 4;
+    if (!shared) I_s = 0;
+    if (shared && (I_s < 8 || I_s % 8))
+        return fail(MOE_ERR_INVALID_ARG, "I_s must be a positive multiple of 8 (got %d)", I_s);
+    if (I < 8 || I % 8) return fail(MOE_ERR_INVALID_ARG, "I must be a positive multiple of 8 (got %d)", I);
+    float dummy_gamma;
+    int32_t dummy_ids;
+    moe_status_t st = check_route_args(x, router, shared ? shared_gate : nullptr, N, H, E, k,
+                                       reinterpret_cast<float *>(&dummy_gamma), &dummy_ids,
+                                       &dummy_gamma);
+    if (st != MOE_OK || N == 0) return st;
+    if (!w_gate || !w_up || !w_down || !out || !workspace)
+        return fail(MOE_ERR_INVALID_ARG, "w_gate, w_up, w_down, out and workspace must be non-null");
+    if (!aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) || !aligned16(out) ||
+        (shared && (!aligned16(shared_gate_proj) || !aligned16(shared_up_proj) ||
+                    !aligned16(shared_down_proj))))
+        return fail(MOE_ERR_INVALID_ARG, "bf16 matrices must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
+        return fail(MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    if (N * k + static_cast<int64_t>(E) * kBlockM >= (int64_t(1) << 31))
+        return fail(MOE_ERR_UNSUPPORTED, "N*k + E*128 must stay below 2^31");
+    moe_forward_layout_t L;
+    forward_layout(N, H, E, I, k, I_s, &L);
+    if (workspace_bytes < L.total)
+        return fail(MOE_ERR_WORKSPACE_TOO_SMALL, "forward workspace needs %zu bytes, got %zu",
+                    L.total, workspace_bytes);
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    auto at = [&](size_t off) { return ws + off; };
+    int32_t *status = reinterpret_cast<int32_t *>(at(L.status));
+    float *topk_w = reinterpret_cast<float *>(at(L.topk_w));
+    int32_t *topk_ids = reinterpret_cast<int32_t *>(at(L.topk_ids));
+    float *gamma = shared ? reinterpret_cast<float *>(at(L.gamma)) : nullptr;
+    uint16_t *act = reinterpret_cast<uint16_t *>(at(L.act));
+    uint16_t *ypair = reinterpret_cast<uint16_t *>(at(L.ypair));
+    const int64_t P = N * k;
+    const int64_t cap = L.capacity;
+    const int sms = num_sms_of_current_device();
+
+    MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int32_t), stream), "status reset");
+
+    // K1: routing
+    record_stage(MOE_STAGE_ROUTE, stream);
+    st = enqueue_route(x, router, shared ? shared_gate : nullptr, N, H, E, k, norm_topk_prob,
+                       topk_w, topk_ids, nullptr, gamma, status, stream);
+    if (st != MOE_OK) return st;
+
+    // K2: grouping
+    record_stage(MOE_STAGE_ALIGN, stream);
+    AlignBuffers b;
+    b.sorted_pair = reinterpret_cast<int32_t *>(at(L.sorted_pair));
+    b.block_expert = reinterpret_cast<int32_t *>(at(L.block_expert));
+    b.counts = reinterpret_cast<int32_t *>(at(L.counts));
+    b.offsets = reinterpret_cast<int32_t *>(at(L.offsets));
+    b.pad_offsets = reinterpret_cast<int32_t *>(at(L.pad_offsets));
+    b.num_padded = reinterpret_cast<int32_t *>(at(L.num_padded));
+    b.scratch = reinterpret_cast<int32_t *>(at(L.align_scratch));
+    b.status = status;
+    st = enqueue_align(topk_ids, N, k, E, kBlockM, b, stream);
+    if (st != MOE_OK) return st;
+
+    // K3: gathered gate/up GEMM + silu * up
+    record_stage(MOE_STAGE_GATE_UP, stream);
+    CUtensorMap tm_xrows, tm_wg, tm_wu, tm_act, tm_wd;
+    if ((st = make_map(&tm_xrows, x, H, N, H, kBlockK, 1, "x rows")) != MOE_OK) return st;
+    if ((st = make_map(&tm_wg, w_gate, H, static_cast<uint64_t>(E) * I, H, kBlockK,
+                       gemm_block_n(kGateUp), "w_gate")) != MOE_OK)
+        return st;
+    if ((st = make_map(&tm_wu, w_up, H, static_cast<uint64_t>(E) * I, H, kBlockK,
+                       gemm_block_n(kGateUp), "w_up")) != MOE_OK)
+        return st;
+    GemmArgs g;
+    g.sorted_pair = b.sorted_pair;
+    g.block_expert = b.block_expert;
+    g.num_padded = b.num_padded;
+    g.num_rows_host = cap;
+    g.q_limit = P;
+    g.k_div = k;
+    g.K = H;
+    g.n_out = I;
+    g.w_rows = I;
+    g.out = act;
+    g.out_ld = I;
+    g.scale = nullptr;
+    g.status = status;
+    {
+        const int nt = (I + gemm_block_n(kGateUp) - 1) / gemm_block_n(kGateUp);
+        g.max_tiles = static_cast<int>(cap / kBlockM) * nt;
+        g.grid = g.max_tiles < sms ? g.max_tiles : sms;
+    }
+    MOE_CUDA(launch_gemm(kGateUp, tm_xrows, tm_wg, tm_wu, g, stream), "gate/up kernel launch");
+    g_launches += 1;
+
+    // K4: down GEMM * routing weight, one row per pair
+    record_stage(MOE_STAGE_DOWN, stream);
+    if ((st = make_map(&tm_act, act, I, cap, I, kBlockK, 1, "act rows")) != MOE_OK) return st;
+    if ((st = make_map(&tm_wd, w_down, I, static_cast<uint64_t>(E) * H, I, kBlockK,
+                       gemm_block_n(kDown), "w_down")) != MOE_OK)
+        return st;
+    g.k_div = 1;
+    g.K = I;
+    g.n_out = H;
+    g.w_rows = H;
+    g.out = ypair;
+    g.out_ld = H;
+    g.scale = topk_w;
+    {
+        const int nt = (H + gemm_block_n(kDown) - 1) / gemm_block_n(kDown);
+        g.max_tiles = static_cast<int>(cap / kBlockM) * nt;
+        g.grid = g.max_tiles < sms ? g.max_tiles : sms;
+    }
+    MOE_CUDA(launch_gemm(kDown, tm_act, tm_wd, tm_wd, g, stream), "down kernel launch");
+    g_launches += 1;
+
+    // shared expert: one dense group over all N tokens, weight sigmoid(x . g)
+    record_stage(MOE_STAGE_SHARED, stream);
+    uint16_t *y_shared = nullptr;
+    if (shared) {
+        uint16_t *act_s = reinterpret_cast<uint16_t *>(at(L.act_shared));
+        y_shared = reinterpret_cast<uint16_t *>(at(L.y_shared));
+        const int64_t rows_s = round_up64(N, kBlockM);
+        CUtensorMap tm_sg, tm_su, tm_acts, tm_sd;
+        if ((st = make_map(&tm_sg, shared_gate_proj, H, I_s, H, kBlockK, gemm_block_n(kGateUp),
+                           "shared_gate_proj")) != MOE_OK)
+            return st;
+        if ((st = make_map(&tm_su, shared_up_proj, H, I_s, H, kBlockK, gemm_block_n(kGateUp),
+                           "shared_up_proj")) != MOE_OK)
+            return st;
+        if ((st = make_map(&tm_acts, act_s, I_s, rows_s, I_s, kBlockK, 1, "shared act rows")) !=
+            MOE_OK)
+            return st;
+        if ((st = make_map(&tm_sd, shared_down_proj, I_s, H, I_s, kBlockK, gemm_block_n(kDown),
+                           "shared_down_proj")) != MOE_OK)
+            return st;
+        GemmArgs s;
+        s.sorted_pair = nullptr;
+        s.block_expert = nullptr;
+        s.num_padded = nullptr;
+        s.num_rows_host = N;
+        s.q_limit = N;
+        s.k_div = 1;
+        s.K = H;
+        s.n_out = I_s;
+        s.w_rows = I_s;
+        s.out = act_s;
+        s.out_ld = I_s;
+        s.scale = nullptr;
+        s.status = status;
+        {
+            const int nt = (I_s + gemm_block_n(kGateUp) - 1) / gemm_block_n(kGateUp);
+            s.max_tiles = static_cast<int>(rows_s / kBlockM) * nt;
+            s.grid = s.max_tiles < sms ? s.max_tiles : sms;
+        }
+        MOE_CUDA(launch_gemm(kGateUp, tm_xrows, tm_sg, tm_su, s, stream),
+                 "shared gate/up kernel launch");
+        s.K = I_s;
+        s.n_out = H;
+        s.w_rows = H;
+        s.out = y_shared;
+        s.out_ld = H;
+        s.scale = gamma;
+        {
+            const int nt = (H + gemm_block_n(kDown) - 1) / gemm_block_n(kDown);
+            s.max_tiles = static_cast<int>(rows_s / kBlockM) * nt;
+            s.grid = s.max_tiles < sms ? s.max_tiles : sms;
+        }
+        MOE_CUDA(launch_gemm(kDown, tm_acts, tm_sd, tm_sd, s, stream),
+                 "shared down kernel launch");
+        g_launches += 2;
+    }
+
+    // K5: out[n] = sum_j ypair[n*k + j] (+ shared)
+    record_stage(MOE_STAGE_COMBINE, stream);
+    MOE_CUDA(launch_combine(ypair, y_shared, N, H, k, out, sms, stream), "combine kernel launch");
+    g_launches += 1;
+    record_stage(MOE_NUM_STAGES, stream);
+    return MOE_OK;
+}
+
+moe_status_t moe_read_device_status(const void *workspace, cudaStream_t stream) {
+    if (!workspace) return fail(MOE_ERR_INVALID_ARG, "workspace must be non-null");
+    MOE_CUDA(cudaStreamSynchronize(stream), "stream synchronize");
+    int32_t v = 0;
+    MOE_CUDA(cudaMemcpy(&v, workspace, sizeof v, cudaMemcpyDeviceToHost), "status read");
+    return static_cast<moe_status_t>(v);
+}
+
+}  // extern "C"

@@ -1,0 +1,324 @@
+// grouped_gemm.cu -- K3 and K4: the per-expert SwiGLU of the M03 "Sparse
+// MoE" drill, Expert(h) = (silu(h Wg^T) * (h Wu^T)) Wd^T, run "the serving
+// way" (each expert once over the tokens routed to it) as grouped GEMMs over
+// the row blocks that moe_align produced (one group per expert; FusedMoE's
+// grouped GEMM as named in the drill's shape-trace section).
+//
+//   K3 (kGateUp): for the 128 rows of block b (expert e = block_expert[b]),
+//       A = x[token(q)] gathered row by row, B0 = Wg[e], B1 = Wu[e];
+//       act[b*128 + r, :] = bf16(silu(A B0^T) * (A B1^T))  (128-column tiles)
+//   K4 (kDown): A = act rows of block b, B0 = Wd[e];
+//       y[q, :] = bf16(w[q] * (A B0^T))                     (256-column tiles)
+//       where w[q] is the routing weight of pair q (or the shared gate).
+// Padding rows (q >= q_limit) are computed by the MMA but never loaded from
+// memory nor stored.
+//
+// Persistent kernel, one CTA per SM, 6 warps:
+//   warp 0    TMA producer: each lane fetches 4 rows of A with one
+//             tile::gather4 copy (skipped when all 4 are padding); lane 0
+//             fetches the weight tile(s) with tiled copies.
+//   warp 1    TMEM allocator and MMA issuer (one thread): 4 x K=16 tcgen05
+//             MMAs per 64-wide K slice into one of two TMEM accumulators.
+//   warps 2-5 epilogue: tcgen05.ld of the 128 x 256 fp32 accumulator (one
+//             row per thread), activation or weight scale, bf16 stores.
+// The two accumulators let the epilogue of tile t overlap the mainloop of
+// tile t+1.  Every wait is bounded (see ptx.cuh).
+#include <cuda_bf16.h>
+
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr int kATileBytes = kBlockM * 128;  // 128 rows x 64 bf16
+constexpr int kBTileBytes = 256 * 128;      // 256 weight rows x 64 bf16
+constexpr int kStageBytes = kATileBytes + kBTileBytes;
+constexpr int kAccCols = 256;               // fp32 columns per accumulator
+constexpr uint32_t kTmemCols = 2 * kAccCols;
+
+struct GemmSmem {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+template <int MODE>
+struct Cfg {
+    static constexpr int BN = MODE == kGateUp ? 128 : 256;  // output columns per tile
+};
+
+__device__ __forceinline__ float silu_times(float g, float u) {
+    return g / (1.f + __expf(-g)) * u;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
+                        const __grid_constant__ CUtensorMap tm_b0,
+                        const __grid_constant__ CUtensorMap tm_b1, const GemmArgs a) {
+    constexpr int BN = Cfg<MODE>::BN;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *tiles = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    GemmSmem *sm = reinterpret_cast<GemmSmem *>(tiles + kStages * kStageBytes);
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&sm->full[s], 1);
+            mbar_init(&sm->empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm->acc_full[i], 1);
+            mbar_init(&sm->acc_empty[i], 4);  // one arrival per epilogue warp
+        }
+        mbar_init(&sm->drain, 1);
+        sm->abort_flag = 0;
+        fence_barrier_init();
+        prefetch_tensor_map(&tm_a);
+        prefetch_tensor_map(&tm_b0);
+        if (MODE == kGateUp) prefetch_tensor_map(&tm_b1);
+    }
+    if (warp == 1) {
+        tmem_alloc(&sm->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = sm->tmem_base;
+    volatile int *abort_flag = &sm->abort_flag;
+
+    const int64_t rows = a.num_padded ? static_cast<int64_t>(*a.num_padded) : a.num_rows_host;
+    const int num_blocks = static_cast<int>((rows + kBlockM - 1) / kBlockM);
+    const int n_tiles = (a.n_out + BN - 1) / BN;
+    const int total_tiles = min(num_blocks * n_tiles, a.max_tiles);
+    const int nk = (a.K + kBlockK - 1) / kBlockK;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (warp)
+        int g = 0;  // K slices issued by this CTA so far
+        bool failed = false;
+        for (int tile = blockIdx.x; tile < total_tiles && !failed; tile += gridDim.x) {
+            const int blk = tile / n_tiles;
+            const int nt = tile % n_tiles;
+            const int expert = a.block_expert ? a.block_expert[blk] : 0;
+            // rows 4*lane .. 4*lane+3 of this block
+            int src[4];
+            bool any = false;
+            int first_valid = -1;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int64_t row = static_cast<int64_t>(blk) * kBlockM + lane * 4 + i;
+                const int64_t q = a.sorted_pair ? a.sorted_pair[row] : row;
+                const bool v = q >= 0 && q < a.q_limit;
+                src[i] = !v ? -1 : (MODE == kGateUp ? static_cast<int>(q / a.k_div)
+                                                    : static_cast<int>(row));
+                if (v && first_valid < 0) first_valid = src[i];
+                any |= v;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (src[i] < 0) src[i] = first_valid;  // a real row; its result is dropped
+            const uint32_t groups = __popc(__ballot_sync(0xffffffffu, any));
+            const uint32_t b_bytes = MODE == kGateUp ? 2 * BN * 128 : BN * 128;
+            const uint32_t tx = groups * 4 * 128 + b_bytes;
+            const int brow = static_cast<int>(static_cast<int64_t>(expert) * a.w_rows) + nt * BN;
+            for (int kc = 0; kc < nk; ++kc, ++g) {
+                const int s = g % kStages;
+                const uint32_t use = g / kStages;
+                bool ok = true;
+                if (lane == 0 && use > 0) ok = mbar_wait(&sm->empty[s], (use - 1) & 1, abort_flag);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) {
+                    if (lane == 0) {
+                        record_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
+                        *abort_flag = 1;
+                    }
+                    failed = true;
+                    break;
+                }
+                uint8_t *st = tiles + s * kStageBytes;
+                if (lane == 0) mbar_arrive_expect_tx(&sm->full[s], tx);
+                __syncwarp();
+                if (any)
+                    tma_gather4(st + lane * 512, &tm_a, &sm->full[s], kc * kBlockK, src[0],
+                                src[1], src[2], src[3]);
+                if (lane == 0) {
+                    tma_load_2d(st + kATileBytes, &tm_b0, &sm->full[s], kc * kBlockK, brow);
+                    if (MODE == kGateUp)
+                        tma_load_2d(st + kATileBytes + BN * 128, &tm_b1, &sm->full[s],
+                                    kc * kBlockK, brow);
+                }
+            }
+        }
+        // drain: wait until the last copy issued into every stage has landed
+        if (lane == 0)
+            for (int i = (g > kStages ? g - kStages : 0); i < g; ++i)
+                mbar_wait(&sm->full[i % kStages], (i / kStages) & 1, abort_flag);
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (1 thread)
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, BN);
+            int g = 0, it = 0;
+            bool failed = false;
+            for (int tile = blockIdx.x; tile < total_tiles && !failed; tile += gridDim.x, ++it) {
+                const int acc = it & 1;
+                const uint32_t use = it >> 1;
+                if (use > 0 && !mbar_wait(&sm->acc_empty[acc], (use - 1) & 1, abort_flag)) {
+                    failed = true;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d = tmem + acc * kAccCols;
+                for (int kc = 0; kc < nk; ++kc, ++g) {
+                    const int s = g % kStages;
+                    if (!mbar_wait(&sm->full[s], (g / kStages) & 1, abort_flag)) {
+                        failed = true;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint8_t *st = tiles + s * kStageBytes;
+                    const uint64_t da = sw128_kmajor_desc(smem_addr(st));
+                    const uint64_t db = sw128_kmajor_desc(smem_addr(st + kATileBytes));
+#pragma unroll
+                    for (int kk = 0; kk < kBlockK / 16; ++kk) {
+                        const uint32_t accumulate = (kc | kk) != 0;
+                        mma_bf16(d, da + 2 * kk, db + 2 * kk, idesc, accumulate);
+                        if (MODE == kGateUp) {
+                            const uint64_t db1 =
+                                sw128_kmajor_desc(smem_addr(st + kATileBytes + BN * 128));
+                            mma_bf16(d + BN, da + 2 * kk, db1 + 2 * kk, idesc, accumulate);
+                        }
+                    }
+                    mma_commit(&sm->empty[s]);
+                }
+                if (!failed) mma_commit(&sm->acc_full[acc]);
+            }
+            if (failed) {
+                record_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
+                *abort_flag = 1;
+            }
+            mma_commit(&sm->drain);
+            mbar_wait(&sm->drain, 0, abort_flag);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue (4 warps)
+        const int quarter = warp % 4;               // TMEM lanes this warp may read
+        const int row = quarter * 32 + lane;        // tile row = TMEM lane
+        int it = 0;
+        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
+            const int acc = it & 1;
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait(&sm->acc_full[acc], (it >> 1) & 1, abort_flag);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) {
+                    record_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            tc_fence_after_sync();
+            const int blk = tile / n_tiles;
+            const int nt = tile % n_tiles;
+            const int64_t grow = static_cast<int64_t>(blk) * kBlockM + row;
+            const int64_t q = a.sorted_pair ? a.sorted_pair[grow] : grow;
+            const bool valid = q >= 0 && q < a.q_limit;
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kAccCols;
+            const int col0 = nt * BN;
+            if (MODE == kGateUp) {
+                uint16_t *dst = a.out + grow * a.out_ld + col0;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    float gv[32], uv[32];
+                    tmem_load32(taddr + c * 32, gv);
+                    tmem_load32(taddr + BN + c * 32, uv);
+                    tmem_load_wait();
+                    if (valid) {
+#pragma unroll
+                        for (int v8 = 0; v8 < 4; ++v8) {
+                            const int col = col0 + c * 32 + v8 * 8;
+                            if (col + 8 <= a.n_out) {
+                                uint4 pk;
+                                pk.x = pack_bf16x2(silu_times(gv[v8 * 8 + 0], uv[v8 * 8 + 0]),
+                                                   silu_times(gv[v8 * 8 + 1], uv[v8 * 8 + 1]));
+                                pk.y = pack_bf16x2(silu_times(gv[v8 * 8 + 2], uv[v8 * 8 + 2]),
+                                                   silu_times(gv[v8 * 8 + 3], uv[v8 * 8 + 3]));
+                                pk.z = pack_bf16x2(silu_times(gv[v8 * 8 + 4], uv[v8 * 8 + 4]),
+                                                   silu_times(gv[v8 * 8 + 5], uv[v8 * 8 + 5]));
+                                pk.w = pack_bf16x2(silu_times(gv[v8 * 8 + 6], uv[v8 * 8 + 6]),
+                                                   silu_times(gv[v8 * 8 + 7], uv[v8 * 8 + 7]));
+                                *reinterpret_cast<uint4 *>(dst + c * 32 + v8 * 8) = pk;
+                            }
+                        }
+                    }
+                }
+            } else {
+                const float w = valid ? a.scale[q] : 0.f;
+                uint16_t *dst = a.out + (valid ? q : 0) * a.out_ld + col0;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    float yv[32];
+                    tmem_load32(taddr + c * 32, yv);
+                    tmem_load_wait();
+                    if (valid) {
+#pragma unroll
+                        for (int v8 = 0; v8 < 4; ++v8) {
+                            const int col = col0 + c * 32 + v8 * 8;
+                            if (col + 8 <= a.n_out) {
+                                uint4 pk;
+                                pk.x = pack_bf16x2(w * yv[v8 * 8 + 0], w * yv[v8 * 8 + 1]);
+                                pk.y = pack_bf16x2(w * yv[v8 * 8 + 2], w * yv[v8 * 8 + 3]);
+                                pk.z = pack_bf16x2(w * yv[v8 * 8 + 4], w * yv[v8 * 8 + 5]);
+                                pk.w = pack_bf16x2(w * yv[v8 * 8 + 6], w * yv[v8 * 8 + 7]);
+                                *reinterpret_cast<uint4 *>(dst + c * 32 + v8 * 8) = pk;
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm->acc_empty[acc]);
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+int gemm_block_n(GemmMode mode) { return mode == kGateUp ? Cfg<kGateUp>::BN : Cfg<kDown>::BN; }
+
+size_t gemm_smem_bytes() { return 1024 + kStages * kStageBytes + sizeof(GemmSmem); }
+
+cudaError_t launch_gemm(GemmMode mode, const CUtensorMap &tm_a, const CUtensorMap &tm_b0,
+                        const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s) {
+    const size_t smem = gemm_smem_bytes();
+    auto kern = mode == kGateUp ? grouped_gemm_kernel<kGateUp> : grouped_gemm_kernel<kDown>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    kern<<<a.grid, kThreads, smem, s>>>(tm_a, tm_b0, tm_b1, a);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

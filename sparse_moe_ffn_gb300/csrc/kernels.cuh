@@ -1,0 +1,85 @@
+// kernels.cuh -- parameter blocks and host-side launchers of the kernels of
+// libsparse_moe_ffn (router, align, grouped GEMMs, combine).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+constexpr int kBlockM = MOE_BLOCK_M;  // GEMM row block (tokens / pairs per tile)
+constexpr int kBlockK = 64;           // 64 bf16 = one 128-byte swizzle row
+
+// ------------------------------------------------------------------ router
+
+struct RouterArgs {
+    int64_t N;
+    int H, E, k, norm;
+    int e_pad;      // MMA N: columns of the logits tile (multiple of 16, <= 256)
+    int gamma_col;  // column holding x . g, or -1 without a shared gate
+    float *topk_w;
+    int32_t *topk_ids;
+    uint16_t *topk_w_bf16;
+    float *gamma;
+    int32_t *status;
+};
+
+size_t router_smem_bytes(int e_pad);
+cudaError_t launch_router(const CUtensorMap &tm_x, const CUtensorMap &tm_router,
+                          const CUtensorMap &tm_gate, const RouterArgs &a, cudaStream_t s);
+
+// ------------------------------------------------------------------- align
+
+struct AlignArgs {
+    const int32_t *ids;
+    int64_t P;       // pairs N*k
+    int E, block_m;
+    int chunk;       // pairs per CTA in the count / scatter kernels
+    int nchunks;
+    int32_t *chunk_counts;  // [nchunks, E], becomes the per-chunk base in place
+    int32_t *counts, *offsets, *pad_offsets, *num_padded;
+    int32_t *sorted_pair, *block_expert;
+    int32_t *status;
+};
+
+constexpr int kAlignChunk = 2048;
+cudaError_t launch_align(const AlignArgs &a, cudaStream_t s, int *launches);
+
+// ------------------------------------------------------------ grouped GEMM
+
+enum GemmMode { kGateUp = 0, kDown = 1 };
+
+struct GemmArgs {
+    // row map: tile row r of block b holds q = sorted_pair[b*128 + r] (or
+    // b*128 + r when sorted_pair is null); the row is real iff q < q_limit
+    const int32_t *sorted_pair;
+    const int32_t *block_expert;  // null: every block belongs to expert 0
+    const int32_t *num_padded;    // device row count; null: use num_rows_host
+    int64_t num_rows_host;
+    int64_t q_limit;
+    int k_div;          // gate/up: the A row gathered for q is q / k_div
+    int K;              // reduction length (H for gate/up, I for down)
+    int n_out;          // output columns (I for gate/up, H for down)
+    int64_t w_rows;     // weight rows per expert (I or H)
+    uint16_t *out;      // act [rows, I] (gate/up) or y [q_limit, H] (down)
+    int64_t out_ld;
+    const float *scale; // down: per-q weight
+    int32_t *status;
+    int max_tiles;      // upper bound on tiles (sizes the persistent grid)
+    int grid;           // persistent CTAs
+};
+
+size_t gemm_smem_bytes();
+cudaError_t launch_gemm(GemmMode mode, const CUtensorMap &tm_a, const CUtensorMap &tm_b0,
+                        const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s);
+int gemm_block_n(GemmMode mode);
+
+// ----------------------------------------------------------------- combine
+
+cudaError_t launch_combine(const uint16_t *ypair, const uint16_t *yshared, int64_t N, int H,
+                           int k, uint16_t *out, int num_sms, cudaStream_t s);
+
+}  // namespace moe

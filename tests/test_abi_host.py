@@ -1,0 +1,102 @@
+"""The C ABI on the host, without a GPU: the library builds and loads, exports
+every entry point include/moe.h declares, sizes workspaces consistently, and
+rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_moe_ffn_gb300 import binding
+from sparse_moe_ffn_gb300 import build as lib_build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "moe.h")
+OK, INVALID, SMALL, UNSUPPORTED = 0, 1, 2, 3
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation fails first
+
+
+@pytest.fixture(scope="module")
+def L():
+    lib_build.build()
+    return binding.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_symbols_are_exported(L):
+    names = declared_functions()
+    assert len(names) >= 12, names
+    for name in names:
+        assert hasattr(L, name), f"{name} declared in moe.h but not exported"
+
+
+def test_status_strings(L):
+    for code in range(7):
+        assert L.moe_status_string(code)
+    assert L.moe_status_string(99) == b"unknown status"
+
+
+def test_layout_is_consistent(L):
+    for args in [(64, 2048, 128, 768, 8, 0), (2048, 2048, 64, 768, 6, 2048), (16, 64, 6, 128, 2, 0)]:
+        lay = binding.moe_forward_layout(*args)
+        assert lay["total"] == binding.moe_forward_workspace_bytes(*args)
+        offs = [v for k, v in lay.items() if k not in ("total", "capacity")]
+        assert all(o % 256 == 0 for o in offs)
+        N, H, E, I, k, _ = args
+        cap = lay["capacity"]
+        assert cap == L.moe_align_capacity(N, k, E, 128)
+        assert lay["ypair"] >= lay["act"] + 2 * cap * I
+        assert lay["total"] >= lay["ypair"] + 2 * N * k * H
+
+
+def _fwd(L, N=64, H=2048, E=128, I=768, I_s=0, k=8, ws_bytes=None, shared=(None,) * 4,
+         x=FAKE, ws=FAKE * 16):
+    if ws_bytes is None:
+        ws_bytes = L.moe_forward_workspace_bytes(N, H, E, I, k, I_s)
+    return L.moe_forward(x, FAKE, FAKE, FAKE, FAKE, *shared, N, H, E, I, I_s, k, 1, FAKE,
+                         ws, ws_bytes, None)
+
+
+def test_forward_argument_errors(L):
+    assert _fwd(L, k=0) == INVALID
+    assert _fwd(L, k=129) == INVALID
+    assert _fwd(L, H=2044) == INVALID
+    assert _fwd(L, I=770) == INVALID
+    assert _fwd(L, N=-1) == INVALID
+    assert _fwd(L, x=None) == INVALID
+    assert _fwd(L, x=FAKE + 2) == INVALID          # misaligned bf16 matrix
+    assert _fwd(L, ws=FAKE + 64) == INVALID        # workspace not 256-byte aligned
+    assert _fwd(L, E=300, k=8) == UNSUPPORTED
+    assert _fwd(L, shared=(FAKE, None, None, None), I_s=64) == INVALID
+    assert _fwd(L, shared=(FAKE,) * 4, I_s=60) == INVALID
+    assert _fwd(L, E=256, shared=(FAKE,) * 4, I_s=64) == UNSUPPORTED
+    need = L.moe_forward_workspace_bytes(64, 2048, 128, 768, 8, 0)
+    assert _fwd(L, ws_bytes=need - 1) == SMALL
+    assert b"needs" in L.moe_last_error()
+    assert _fwd(L, N=0) == OK                      # no-op, nothing launched
+
+
+def test_route_and_align_argument_errors(L):
+    P = FAKE
+    assert L.moe_route(P, P, None, 16, 64, 6, 7, 1, P, P, None, None, None, 0, None) == INVALID
+    assert L.moe_route(P, P, P, 16, 64, 6, 2, 1, P, P, None, None, None, 0, None) == INVALID
+    assert L.moe_route(P, P, None, 16, 60, 6, 2, 1, P, P, None, None, None, 0, None) == INVALID
+    assert L.moe_route(P, P, None, 16, 64, 6, 2, 1, P, P, None, None, P, 1, None) == SMALL
+    assert L.moe_route(P, P, None, 0, 64, 6, 2, 1, P, P, None, None, None, 0, None) == OK
+    need = L.moe_align_workspace_bytes(100, 2, 8, 16)
+    assert L.moe_align(P, 100, 2, 8, 16, P, P, P, P, P, P, need - 1, None) == SMALL
+    assert L.moe_align(P, 100, 2, 8, 0, P, P, P, P, P, P, need, None) == INVALID
+    assert L.moe_align(P, 100, 2, 2000, 16, P, P, P, P, P, P, need, None) == UNSUPPORTED
+    assert L.moe_align(None, 100, 2, 8, 16, P, P, P, P, P, P, need, None) == INVALID
+    assert L.moe_align_capacity(3, 2, 5, 4) == 24  # round_up(6 + 5*3, 4)
+
+
+def test_stage_events_argument_check(L):
+    assert L.moe_set_stage_events(None, 0) == OK
+    arr = (ctypes.c_void_p * 3)()
+    assert L.moe_set_stage_events(arr, 3) == INVALID

@@ -1,0 +1,203 @@
+"""GPU parity: every kernel of the layer against the fp64 oracle, through the
+C ABI (ctypes binding).  Routing and grouping are compared bit for bit,
+outputs within the tolerance stated in gpu_cases.py."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_cases import (WEIGHT_ATOL, assert_close, error_stats, prepare, prepared, run_forward,
+                       sample_rows, shared_of)
+from sparse_moe_ffn_gb300 import binding
+from sparse_moe_ffn_gb300.inputs import MoEShape
+
+pytestmark = pytest.mark.gpu
+
+ALL = ["tiny", "decode", "prefill", "talker", "skewed"]
+SAMPLED_ROWS = 192
+
+
+# ----------------------------------------------------------------- routing
+
+@pytest.mark.parametrize("name", ALL)
+def test_route_matches_oracle(name):
+    shape, dev, bits = prepared(name)
+    sg = dev.get("shared_gate")
+    w, ids, gamma, wb = binding.moe_route_raw(dev["x"], dev["router"], shape.k,
+                                              shape.norm_topk_prob, shared_gate=sg,
+                                              want_bf16=True)
+    logits, _, w_ref, ids_ref = oracle.route(bits["x"], bits["router"], shape.k,
+                                             shape.norm_topk_prob)
+    got_ids = ids.cpu().numpy()
+    assert np.array_equal(got_ids, ids_ref), \
+        f"{name}: {np.sum(got_ids != ids_ref)} ids differ"
+    werr = np.abs(w.cpu().numpy() - w_ref).max()
+    assert werr <= WEIGHT_ATOL, f"{name}: routing weight error {werr:.3e}"
+    # exported bf16 weights are the fp32 weights rounded to nearest even
+    assert torch.equal(wb, w.to(torch.bfloat16))
+    if sg is not None:
+        g_ref = 1.0 / (1.0 + np.exp(-(oracle.widen(bits["x"]) @ oracle.widen(bits["shared_gate"]).T)[:, 0]))
+        gerr = np.abs(gamma.cpu().numpy() - g_ref).max()
+        assert gerr <= WEIGHT_ATOL, f"{name}: shared gate error {gerr:.3e}"
+    # the page's route(): weights in x.dtype, ids int64
+    wt, it = binding.moe_route(dev["x"], dev["router"], shape.k, shape.norm_topk_prob)
+    assert wt.dtype == dev["x"].dtype and it.dtype == torch.int64
+    assert np.array_equal(it.cpu().numpy(), ids_ref)
+
+
+def test_route_sums():
+    """Renormalised weights sum to 1; unrenormalised ones to less than 1."""
+    shape, dev, _ = prepared("decode")
+    w, _, _, _ = binding.moe_route_raw(dev["x"], dev["router"], shape.k, True)
+    assert torch.allclose(w.sum(1), torch.ones(shape.N, device="cuda"), atol=1e-6)
+    w, _, _, _ = binding.moe_route_raw(dev["x"], dev["router"], shape.k, False)
+    assert bool((w.sum(1) < 1.0).all())
+
+
+# ---------------------------------------------------------------- grouping
+
+def _align_vs_oracle(ids_np, E, block_m):
+    ids = torch.from_numpy(np.ascontiguousarray(ids_np, dtype=np.int32)).cuda()
+    r = binding.moe_align(ids, E, block_m)
+    torch.cuda.synchronize()
+    ref = oracle.align(ids_np, E, block_m)
+    npad = int(r["num_padded"].item())
+    assert npad == ref["num_padded"]
+    assert np.array_equal(r["counts"].cpu().numpy(), ref["counts"])
+    assert np.array_equal(r["offsets"].cpu().numpy(), ref["offsets"])
+    assert np.array_equal(r["sorted_pair"][:npad].cpu().numpy(), ref["sorted_pair"])
+    assert np.array_equal(r["block_expert"][:npad // block_m].cpu().numpy(),
+                          ref["block_expert"])
+    assert binding.moe_read_device_status(r["workspace"]) == 0
+
+
+@pytest.mark.parametrize("name", ALL)
+def test_align_matches_oracle(name):
+    shape, dev, bits = prepared(name)
+    _, _, _, ids = oracle.route(bits["x"], bits["router"], shape.k, shape.norm_topk_prob)
+    _align_vs_oracle(ids, shape.E, 128)
+
+
+@pytest.mark.parametrize("N,k,E,block_m", [(1, 1, 1, 1), (3, 2, 5, 4), (1000, 8, 64, 16),
+                                           (5000, 4, 1024, 128), (70000, 2, 3, 1),
+                                           (513, 8, 128, 128), (4096, 8, 256, 64)])
+def test_align_random(N, k, E, block_m):
+    rng = np.random.default_rng(N + E)
+    ids = rng.integers(0, E, size=(N, k)).astype(np.int32)
+    if E > 4:
+        ids[ids == 3] = 4  # an expert with no pairs
+    _align_vs_oracle(ids, E, block_m)
+
+
+def test_align_flags_bad_ids():
+    """An id outside [0, E) is skipped and recorded in the status word."""
+    ids = torch.tensor([[0, 1], [7, 2]], dtype=torch.int32, device="cuda")
+    r = binding.moe_align(ids, 4, 8)
+    assert binding.moe_read_device_status(r["workspace"]) == 5  # MOE_ERR_DEVICE_CHECK
+
+
+# ------------------------------------------------------------ whole layer
+
+@pytest.mark.parametrize("name", ALL)
+def test_forward_matches_oracle(name):
+    shape, dev, bits = prepared(name)
+    out, ws = run_forward(shape, dev)
+    rows = sample_rows(shape.N, SAMPLED_ROWS)
+    ref = oracle.moe_forward(bits, shape.k, shape.norm_topk_prob, rows=rows)
+    assert_close(out[torch.from_numpy(rows).cuda()], ref, name)
+    # the stages inside the workspace: routing and grouping bit-exact
+    v = binding.workspace_views(ws, shape.N, shape.H, shape.E, shape.I, shape.k, shape.I_s)
+    _, _, _, ids_ref = oracle.route(bits["x"], bits["router"], shape.k, shape.norm_topk_prob)
+    assert np.array_equal(v["topk_ids"].cpu().numpy(), ids_ref)
+    al = oracle.align(ids_ref, shape.E, 128)
+    npad = int(v["num_padded"].item())
+    assert npad == al["num_padded"]
+    assert np.array_equal(v["counts"].cpu().numpy(), al["counts"])
+    assert np.array_equal(v["sorted_pair"][:npad].cpu().numpy(), al["sorted_pair"])
+
+
+def test_pair_outputs_decode():
+    """K3 + K4 per pair: ypair[p] = w_p * Expert_{e_p}(x_n) for sampled pairs,
+    the expert evaluated by the oracle as a one-expert layer."""
+    shape, dev, bits = prepared("decode")
+    out, ws = run_forward(shape, dev)
+    v = binding.workspace_views(ws, shape.N, shape.H, shape.E, shape.I, shape.k)
+    ids = v["topk_ids"].cpu().numpy()
+    w = v["topk_w"].cpu().numpy()
+    ypair = v["ypair"].float().cpu().numpy()
+    rng = np.random.default_rng(1)
+    got, ref = [], []
+    for p in rng.choice(shape.N * shape.k, size=24, replace=False):
+        n, j = divmod(int(p), shape.k)
+        e = int(ids[n, j])
+        one = {"x": bits["x"][n:n + 1], "router": bits["router"][:1],
+               "w_gate": bits["w_gate"][e:e + 1], "w_up": bits["w_up"][e:e + 1],
+               "w_down": bits["w_down"][e:e + 1]}
+        ref.append(w[n, j] * oracle.moe_forward(one, 1, True)[0])
+        got.append(ypair[p])
+    assert_close(np.array(got), np.array(ref), "ypair")
+
+
+EDGE = [
+    # name, N, H, E, k, I, I_s, norm
+    ("ragged", 300, 256, 16, 4, 192, 0, True),
+    ("one-token", 1, 128, 8, 2, 64, 0, True),
+    ("tile-plus-one", 129, 64, 8, 2, 128, 0, False),
+    ("k-equals-E", 40, 64, 4, 4, 64, 0, True),
+    ("dense-E1-k1", 77, 128, 1, 1, 96, 0, True),
+    ("odd-E-shared", 50, 64, 6, 2, 128, 64, False),
+    ("ragged-H-I", 200, 200, 10, 3, 72, 40, True),
+    ("wide-E", 256, 128, 256, 8, 64, 0, True),
+    ("E248-shared", 64, 64, 248, 4, 32, 16, False),
+]
+
+
+@pytest.mark.parametrize("case", EDGE, ids=[c[0] for c in EDGE])
+def test_forward_edge_shapes(case):
+    name, N, H, E, k, I, I_s, norm = case
+    shape, dev, bits = prepare(MoEShape(name, N=N, H=H, E=E, k=k, I=I, I_s=I_s,
+                                        norm_topk_prob=norm), seed=3)
+    out, _ = run_forward(shape, dev)
+    ref = oracle.moe_forward(bits, k, norm)
+    assert_close(out, ref, name)
+
+
+def test_batch_invariance_skewed():
+    """A token computed alone equals the same token inside the skewed batch,
+    bit for bit (routing, grouping position and GEMM order do not depend on
+    the rest of the batch)."""
+    shape, dev, _ = prepared("skewed")
+    out, _ = run_forward(shape, dev)
+    for i in (0, 1, 4097, shape.N - 1):
+        one, _ = run_forward(shape, dev, x=dev["x"][i:i + 1].contiguous())
+        assert torch.equal(one[0], out[i]), f"row {i} differs"
+    w_all, ids_all, _, _ = binding.moe_route_raw(dev["x"], dev["router"], shape.k, True)
+    w_one, ids_one, _, _ = binding.moe_route_raw(dev["x"][5:6].contiguous(), dev["router"],
+                                                 shape.k, True)
+    assert torch.equal(ids_all[5], ids_one[0]) and torch.equal(w_all[5], w_one[0])
+
+
+def test_repeatable_and_status_clean():
+    shape, dev, _ = prepared("talker")
+    a, ws = run_forward(shape, dev)
+    b, _ = run_forward(shape, dev, workspace=ws)
+    assert torch.equal(a, b)
+
+
+def test_zero_tokens_is_a_noop():
+    shape, dev, _ = prepared("tiny")
+    x = dev["x"][:0]
+    out = binding.moe_forward(x, dev["router"], dev["w_gate"], dev["w_up"], dev["w_down"],
+                              shape.k, True)
+    assert out.shape == (0, shape.H)
+
+
+def test_error_summary_is_reported(capsys):
+    """Print the measured error figures of every configuration (information)."""
+    for name in ALL:
+        shape, dev, bits = prepared(name)
+        out, _ = run_forward(shape, dev)
+        rows = sample_rows(shape.N, 64)
+        ref = oracle.moe_forward(bits, shape.k, shape.norm_topk_prob, rows=rows)
+        mx, rms, mean_rel = error_stats(out[torch.from_numpy(rows).cuda()], ref)
+        print(f"{name}: max|err|/rms = {mx / rms:.3e}, mean rel err = {mean_rel:.3e}")
