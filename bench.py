@@ -246,15 +246,27 @@ def run_ours(args, world, rank, local):
         binding.moe_forward(d["x"], d["router"], d["w_gate"], d["w_up"], d["w_down"], shape.k,
                             shape.norm_topk_prob, shared, out=out, workspace=ws)
 
-    for _ in range(args.warmup):
+    # warm-up; the last warm-up step records every stage boundary to find the
+    # dominant kernel, whose launches the timed steps then bracket with events
+    nst = len(STAGES) + 1
+    probe = [torch.cuda.Event(enable_timing=True) for _ in range(nst)]
+    for i in range(args.warmup):
+        if i == args.warmup - 1:
+            binding.set_stage_events(probe)
         step()
+    binding.set_stage_events(None)
     torch.cuda.synchronize()
     status = binding.moe_read_device_status(ws)
     if status != 0:
         raise RuntimeError(f"device status {status}: {binding.moe_status_string(status)}")
+    probe_ms = {s: probe[j].elapsed_time(probe[j + 1]) for j, s in enumerate(STAGES)}
+    dom = max(("route", "gate_up", "down", "shared", "combine"), key=lambda s: probe_ms[s])
+    j_dom = STAGES.index(dom)
 
-    nst = len(STAGES) + 1
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)] for _ in range(args.steps)]
+    ev = [[None] * nst for _ in range(args.steps)]
+    for i in range(args.steps):
+        ev[i][j_dom] = torch.cuda.Event(enable_timing=True)
+        ev[i][j_dom + 1] = torch.cuda.Event(enable_timing=True)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(device.index if device.index is not None else 0)
     sampler.start()
@@ -275,8 +287,8 @@ def run_ours(args, world, rank, local):
     clocks = ClockSampler.summarize(sampler.stop(), t0, t1)
     ms = start.elapsed_time(end)
     ms_max = max_over_ranks(ms, world, device)
-    stage_ms = {s: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
-                for j, s in enumerate(STAGES)}
+    dom_ms = statistics.mean(ev[i][j_dom].elapsed_time(ev[i][j_dom + 1])
+                             for i in range(args.steps))
 
     touched = int((binding.workspace_views(ws, shape.N, shape.H, shape.E, shape.I, shape.k,
                                            shape.I_s)["counts"] > 0).sum().item())
@@ -286,21 +298,20 @@ def run_ours(args, world, rank, local):
     tflops = layer_flops * args.steps * world / (ms_max / 1e3) / 1e12
 
     # roofline of the dominant kernel (largest share of the step)
-    dom = max(("route", "gate_up", "down", "shared", "combine"), key=lambda s: stage_ms[s])
     peaks, peak_src = load_peaks()
     bound = BOUND[args.config]
     if bound == "tensor" and sflops[dom] == 0:
         bound = "hbm"
     if bound == "hbm":
-        achieved = sbytes[dom] / (stage_ms[dom] / 1e3) / 1e9
+        achieved = sbytes[dom] / (dom_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s"}
     else:
-        achieved = sflops[dom] / (stage_ms[dom] / 1e3) / 1e12
+        achieved = sflops[dom] / (dom_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s"}
     roof.update(frac=round(achieved / roof["peak"], 4), traffic=measured_traffic(dom, args.config),
-                kernel=dom, peak_source=f"{peak_src} (MEASURED_PEAKS.json)" if peak_src ==
+                kernel=dom, kernel_ms=round(dom_ms, 5), peak_source=f"{peak_src} (MEASURED_PEAKS.json)" if peak_src ==
                 "measured" else "fallback", algorithmic_per_launch=(
                     sbytes[dom] if roof["bound"] == "hbm" else sflops[dom]))
 
@@ -352,7 +363,7 @@ def run_ours(args, world, rank, local):
                          "inputs smaller than L2 (not flushed: latency-bound case)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "tflops": round(tflops, 2),
-        "stage_ms": {s: round(v, 5) for s, v in stage_ms.items()},
+        "stage_ms_warmup_probe": {s: round(v, 5) for s, v in probe_ms.items()},
         "experts_touched": touched,
         "roofline": roof,
         "cpu_baseline": cpu_base,

@@ -147,11 +147,14 @@ moe_status_t moe_align(const int32_t *topk_ids, int64_t N, int k, int E,
  *   workspace         >= moe_forward_workspace_bytes(...) bytes, 256-byte
  *                     aligned; holds the routing, grouping and intermediate
  *                     activations (layout: moe_forward_layout)
- * Precision: bf16 inputs, fp32 routing and accumulation, the gate/up
- * activation silu(g)*u and each pair's weighted down projection are rounded
- * to bf16 once, the k contributions (and the shared expert) are summed in
- * fp32 in slot order, and out is rounded to bf16.  The result does not depend
- * on the other tokens of the batch, and is bitwise reproducible.
+ * Precision: bf16 inputs, fp32 routing and accumulation; the gate/up
+ * activation a = silu(g)*u is kept as the bf16 pair (hi, lo = a - hi), both
+ * fed to the down GEMM (about 16 significant bits); each pair's weighted down projection (and the gated shared expert) is
+ * stored in fp16 (same bytes as bf16, 8x finer rounding); the k
+ * contributions and the shared term are summed in fp32 in slot order, and
+ * out is rounded to bf16 once.  A pair output beyond the fp16 range
+ * (|w * Expert(x)| > 65504) records MOE_ERR_DEVICE_CHECK.  The result does
+ * not depend on the other tokens of the batch and is bitwise reproducible.
  * Limits: as moe_route, plus I % 8 == 0, N*k + E*128 < 2^31.
  * ---------------------------------------------------------------------- */
 size_t moe_forward_workspace_bytes(int64_t N, int H, int E, int I, int k, int I_s);
@@ -180,10 +183,12 @@ typedef struct {
     size_t align_scratch; /* int32 [chunks, E]                                */
     size_t sorted_pair;   /* int32 [capacity]                                 */
     size_t block_expert;  /* int32 [capacity / 128]                           */
-    size_t act;           /* bf16 [capacity, I]   silu(x Wg^T) * (x Wu^T)     */
-    size_t ypair;         /* bf16 [N*k, H]        w * Expert(x), per pair     */
-    size_t act_shared;    /* bf16 [round_up(N,128), I_s] (shared only)        */
-    size_t y_shared;      /* bf16 [N, H]  gamma * SharedMLP(x) (shared only)  */
+    size_t act;           /* bf16 [capacity, I]   a_hi = bf16(a), a = silu(x Wg^T) * (x Wu^T) */
+    size_t act_lo;        /* bf16 [capacity, I]   a_lo = bf16(a - a_hi)       */
+    size_t ypair;         /* fp16 [N*k, H]        w * Expert(x), per pair     */
+    size_t act_shared;    /* bf16 [round_up(N,128), I_s] hi (shared only)     */
+    size_t act_shared_lo; /* bf16 [round_up(N,128), I_s] lo (shared only)     */
+    size_t y_shared;      /* fp16 [N, H]  gamma * SharedMLP(x) (shared only)  */
     size_t total;         /* = moe_forward_workspace_bytes                    */
     int64_t capacity;     /* moe_align_capacity(N, k, E, 128)                 */
 } moe_forward_layout_t;
@@ -216,8 +221,8 @@ uint64_t moe_kernel_launch_count(void);
 
 /* Ask the next moe_forward calls on this thread to record events[i] (created
  * by the caller with timing enabled) on their stream before stage i, and
- * events[MOE_NUM_STAGES] after the last stage.  n_events must be
- * MOE_NUM_STAGES + 1, or 0 with events NULL to stop recording. */
+ * events[MOE_NUM_STAGES] after the last stage; NULL entries are skipped.
+ * n_events must be MOE_NUM_STAGES + 1, or 0 with events NULL to stop. */
 moe_status_t moe_set_stage_events(cudaEvent_t *events, int n_events);
 
 #ifdef __cplusplus

@@ -28,8 +28,8 @@ class MoEError(RuntimeError):
 class _Layout(ctypes.Structure):
     _fields_ = [(name, ctypes.c_size_t) for name in (
         "status", "topk_w", "topk_ids", "gamma", "counts", "offsets", "pad_offsets",
-        "num_padded", "align_scratch", "sorted_pair", "block_expert", "act", "ypair",
-        "act_shared", "y_shared", "total")] + [("capacity", ctypes.c_int64)]
+        "num_padded", "align_scratch", "sorted_pair", "block_expert", "act", "act_lo", "ypair",
+        "act_shared", "act_shared_lo", "y_shared", "total")] + [("capacity", ctypes.c_int64)]
 
 
 _lib = None
@@ -234,13 +234,15 @@ def workspace_views(workspace, N, H, E, I, k, I_s=0) -> dict:
         "sorted_pair": view(lay["sorted_pair"], torch.int32, (cap,)),
         "block_expert": view(lay["block_expert"], torch.int32, (cap // MOE_BLOCK_M,)),
         "act": view(lay["act"], torch.bfloat16, (cap, I)),
-        "ypair": view(lay["ypair"], torch.bfloat16, (P, H)),
+        "act_lo": view(lay["act_lo"], torch.bfloat16, (cap, I)),
+        "ypair": view(lay["ypair"], torch.float16, (P, H)),
     }
     if I_s:
         rows_s = -(-N // MOE_BLOCK_M) * MOE_BLOCK_M
         v["gamma"] = view(lay["gamma"], torch.float32, (N,))
         v["act_shared"] = view(lay["act_shared"], torch.bfloat16, (rows_s, I_s))
-        v["y_shared"] = view(lay["y_shared"], torch.bfloat16, (N, H))
+        v["act_shared_lo"] = view(lay["act_shared_lo"], torch.bfloat16, (rows_s, I_s))
+        v["y_shared"] = view(lay["y_shared"], torch.float16, (N, H))
     return v
 
 
@@ -250,13 +252,17 @@ def moe_read_device_status(workspace) -> int:
 
 
 def set_stage_events(events) -> None:
-    """Record the given torch.cuda.Event objects around the stages of the next
-    moe_forward calls on this thread (None to stop)."""
+    """Record the given torch.cuda.Event objects (None entries skipped) around
+    the stages of the next moe_forward calls on this thread (None to stop)."""
     L = lib()
     if events is None:
         _check(L.moe_set_stage_events(None, 0), "moe_set_stage_events")
         return
     if len(events) != MOE_NUM_STAGES + 1:
         raise ValueError(f"need {MOE_NUM_STAGES + 1} events")
-    arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    for e in events:
+        if e is not None and not e.cuda_event:  # torch creates it on first record
+            e.record()
+    arr = (ctypes.c_void_p * len(events))(
+        *[ctypes.c_void_p(e.cuda_event if e is not None else None) for e in events])
     _check(L.moe_set_stage_events(arr, len(events)), "moe_set_stage_events")

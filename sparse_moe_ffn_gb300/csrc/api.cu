@@ -96,8 +96,11 @@ int num_sms_of_current_device() {
     return cache[dev];
 }
 
-void record_stage(int i, cudaStream_t s) {
-    if (g_stage_events_on) cudaEventRecord(g_stage_events[i], s);
+moe_status_t record_stage(int i, cudaStream_t s) {
+    if (!g_stage_events_on || g_stage_events[i] == nullptr) return MOE_OK;
+    cudaError_t e = cudaEventRecord(g_stage_events[i], s);
+    if (e != cudaSuccess) return cuda_fail(e, "stage event record");
+    return MOE_OK;
 }
 
 // ------------------------------------------------------------------ layouts
@@ -216,9 +219,11 @@ moe_status_t forward_layout(int64_t N, int H, int E, int I, int k, int I_s,
     L->sorted_pair = take(sizeof(int32_t) * cap);
     L->block_expert = take(sizeof(int32_t) * (cap / kBlockM));
     L->act = take(2 * static_cast<size_t>(cap) * I);
-    L->ypair = take(2 * static_cast<size_t>(P) * H);
+    L->act_lo = take(2 * static_cast<size_t>(cap) * I);
+    L->ypair = take(2 * static_cast<size_t>(P) * H);  // fp16
     L->act_shared = take(shared ? 2 * static_cast<size_t>(round_up64(N, kBlockM)) * I_s : 0);
-    L->y_shared = take(shared ? 2 * static_cast<size_t>(N) * H : 0);
+    L->act_shared_lo = take(shared ? 2 * static_cast<size_t>(round_up64(N, kBlockM)) * I_s : 0);
+    L->y_shared = take(shared ? 2 * static_cast<size_t>(N) * H : 0);  // fp16
     L->total = off;
     L->capacity = cap;
     return MOE_OK;
@@ -384,6 +389,7 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
     int32_t *topk_ids = reinterpret_cast<int32_t *>(at(L.topk_ids));
     float *gamma = shared ? reinterpret_cast<float *>(at(L.gamma)) : nullptr;
     uint16_t *act = reinterpret_cast<uint16_t *>(at(L.act));
+    uint16_t *act_lo = reinterpret_cast<uint16_t *>(at(L.act_lo));
     uint16_t *ypair = reinterpret_cast<uint16_t *>(at(L.ypair));
     const int64_t P = N * k;
     const int64_t cap = L.capacity;
@@ -392,13 +398,13 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
     MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int32_t), stream), "status reset");
 
     // K1: routing
-    record_stage(MOE_STAGE_ROUTE, stream);
+    if ((st = record_stage(MOE_STAGE_ROUTE, stream)) != MOE_OK) return st;
     st = enqueue_route(x, router, shared ? shared_gate : nullptr, N, H, E, k, norm_topk_prob,
                        topk_w, topk_ids, nullptr, gamma, status, stream);
     if (st != MOE_OK) return st;
 
     // K2: grouping
-    record_stage(MOE_STAGE_ALIGN, stream);
+    if ((st = record_stage(MOE_STAGE_ALIGN, stream)) != MOE_OK) return st;
     AlignBuffers b;
     b.sorted_pair = reinterpret_cast<int32_t *>(at(L.sorted_pair));
     b.block_expert = reinterpret_cast<int32_t *>(at(L.block_expert));
@@ -412,8 +418,8 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
     if (st != MOE_OK) return st;
 
     // K3: gathered gate/up GEMM + silu * up
-    record_stage(MOE_STAGE_GATE_UP, stream);
-    CUtensorMap tm_xrows, tm_wg, tm_wu, tm_act, tm_wd;
+    if ((st = record_stage(MOE_STAGE_GATE_UP, stream)) != MOE_OK) return st;
+    CUtensorMap tm_xrows, tm_wg, tm_wu, tm_act, tm_act_lo, tm_wd;
     if ((st = make_map(&tm_xrows, x, H, N, H, kBlockK, 1, "x rows")) != MOE_OK) return st;
     if ((st = make_map(&tm_wg, w_gate, H, static_cast<uint64_t>(E) * I, H, kBlockK,
                        gemm_block_n(kGateUp), "w_gate")) != MOE_OK)
@@ -432,6 +438,7 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
     g.n_out = I;
     g.w_rows = I;
     g.out = act;
+    g.out_lo = act_lo;
     g.out_ld = I;
     g.scale = nullptr;
     g.status = status;
@@ -440,12 +447,15 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
         g.max_tiles = static_cast<int>(cap / kBlockM) * nt;
         g.grid = g.max_tiles < sms ? g.max_tiles : sms;
     }
-    MOE_CUDA(launch_gemm(kGateUp, tm_xrows, tm_wg, tm_wu, g, stream), "gate/up kernel launch");
+    MOE_CUDA(launch_gemm(kGateUp, tm_xrows, tm_xrows, tm_wg, tm_wu, g, stream),
+             "gate/up kernel launch");
     g_launches += 1;
 
     // K4: down GEMM * routing weight, one row per pair
-    record_stage(MOE_STAGE_DOWN, stream);
+    if ((st = record_stage(MOE_STAGE_DOWN, stream)) != MOE_OK) return st;
     if ((st = make_map(&tm_act, act, I, cap, I, kBlockK, 1, "act rows")) != MOE_OK) return st;
+    if ((st = make_map(&tm_act_lo, act_lo, I, cap, I, kBlockK, 1, "act_lo rows")) != MOE_OK)
+        return st;
     if ((st = make_map(&tm_wd, w_down, I, static_cast<uint64_t>(E) * H, I, kBlockK,
                        gemm_block_n(kDown), "w_down")) != MOE_OK)
         return st;
@@ -454,6 +464,7 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
     g.n_out = H;
     g.w_rows = H;
     g.out = ypair;
+    g.out_lo = nullptr;
     g.out_ld = H;
     g.scale = topk_w;
     {
@@ -461,17 +472,19 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
         g.max_tiles = static_cast<int>(cap / kBlockM) * nt;
         g.grid = g.max_tiles < sms ? g.max_tiles : sms;
     }
-    MOE_CUDA(launch_gemm(kDown, tm_act, tm_wd, tm_wd, g, stream), "down kernel launch");
+    MOE_CUDA(launch_gemm(kDown, tm_act, tm_act_lo, tm_wd, tm_wd, g, stream),
+             "down kernel launch");
     g_launches += 1;
 
     // shared expert: one dense group over all N tokens, weight sigmoid(x . g)
-    record_stage(MOE_STAGE_SHARED, stream);
+    if ((st = record_stage(MOE_STAGE_SHARED, stream)) != MOE_OK) return st;
     uint16_t *y_shared = nullptr;
     if (shared) {
         uint16_t *act_s = reinterpret_cast<uint16_t *>(at(L.act_shared));
+        uint16_t *act_s_lo = reinterpret_cast<uint16_t *>(at(L.act_shared_lo));
         y_shared = reinterpret_cast<uint16_t *>(at(L.y_shared));
         const int64_t rows_s = round_up64(N, kBlockM);
-        CUtensorMap tm_sg, tm_su, tm_acts, tm_sd;
+        CUtensorMap tm_sg, tm_su, tm_acts, tm_acts_lo, tm_sd;
         if ((st = make_map(&tm_sg, shared_gate_proj, H, I_s, H, kBlockK, gemm_block_n(kGateUp),
                            "shared_gate_proj")) != MOE_OK)
             return st;
@@ -480,6 +493,9 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
             return st;
         if ((st = make_map(&tm_acts, act_s, I_s, rows_s, I_s, kBlockK, 1, "shared act rows")) !=
             MOE_OK)
+            return st;
+        if ((st = make_map(&tm_acts_lo, act_s_lo, I_s, rows_s, I_s, kBlockK, 1,
+                           "shared act_lo rows")) != MOE_OK)
             return st;
         if ((st = make_map(&tm_sd, shared_down_proj, I_s, H, I_s, kBlockK, gemm_block_n(kDown),
                            "shared_down_proj")) != MOE_OK)
@@ -495,6 +511,7 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
         s.n_out = I_s;
         s.w_rows = I_s;
         s.out = act_s;
+        s.out_lo = act_s_lo;
         s.out_ld = I_s;
         s.scale = nullptr;
         s.status = status;
@@ -503,12 +520,13 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
             s.max_tiles = static_cast<int>(rows_s / kBlockM) * nt;
             s.grid = s.max_tiles < sms ? s.max_tiles : sms;
         }
-        MOE_CUDA(launch_gemm(kGateUp, tm_xrows, tm_sg, tm_su, s, stream),
+        MOE_CUDA(launch_gemm(kGateUp, tm_xrows, tm_xrows, tm_sg, tm_su, s, stream),
                  "shared gate/up kernel launch");
         s.K = I_s;
         s.n_out = H;
         s.w_rows = H;
         s.out = y_shared;
+        s.out_lo = nullptr;
         s.out_ld = H;
         s.scale = gamma;
         {
@@ -516,16 +534,16 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
             s.max_tiles = static_cast<int>(rows_s / kBlockM) * nt;
             s.grid = s.max_tiles < sms ? s.max_tiles : sms;
         }
-        MOE_CUDA(launch_gemm(kDown, tm_acts, tm_sd, tm_sd, s, stream),
+        MOE_CUDA(launch_gemm(kDown, tm_acts, tm_acts_lo, tm_sd, tm_sd, s, stream),
                  "shared down kernel launch");
         g_launches += 2;
     }
 
     // K5: out[n] = sum_j ypair[n*k + j] (+ shared)
-    record_stage(MOE_STAGE_COMBINE, stream);
+    if ((st = record_stage(MOE_STAGE_COMBINE, stream)) != MOE_OK) return st;
     MOE_CUDA(launch_combine(ypair, y_shared, N, H, k, out, sms, stream), "combine kernel launch");
     g_launches += 1;
-    record_stage(MOE_NUM_STAGES, stream);
+    if ((st = record_stage(MOE_NUM_STAGES, stream)) != MOE_OK) return st;
     return MOE_OK;
 }
 

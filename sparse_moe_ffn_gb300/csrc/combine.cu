@@ -4,11 +4,12 @@
 // y * w)": each token receives the sum of all k contributions, never just the
 // last one written) done without atomics: the down-projection epilogue stored
 // w * Expert(x) of pair p = n*k + j at row p of ypair, so token n's k
-// contributions are the k consecutive rows n*k .. n*k+k-1.  They are summed
-// in slot order in fp32, the shared-expert term gamma * SharedMLP(x) (same
+// contributions are the k consecutive fp16 rows n*k .. n*k+k-1.  They are
+// summed in slot order in fp32, the shared-expert term gamma * SharedMLP(x) (same
 // page, talker line) is added last, and the result is rounded to bf16 once.
 // Bandwidth bound: one thread per 8 output columns, 16-byte loads and stores.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "kernels.cuh"
 #include "ptx.cuh"
@@ -19,11 +20,11 @@ namespace {
 
 constexpr int kCombineThreads = 256;
 
-__device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4 &v) {
-    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v);
+__device__ __forceinline__ void add_f16x8(float (&acc)[8], const uint4 &v) {
+    const __half2 *h = reinterpret_cast<const __half2 *>(&v);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(h[i]);
+        const float2 f = __half22float2(h[i]);
         acc[2 * i] += f.x;
         acc[2 * i + 1] += f.y;
     }
@@ -41,9 +42,9 @@ __global__ void __launch_bounds__(kCombineThreads)
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         const uint16_t *src = ypair + n * k * static_cast<int64_t>(H) + col;
         for (int j = 0; j < k; ++j)
-            add_bf16x8(acc, *reinterpret_cast<const uint4 *>(src + static_cast<int64_t>(j) * H));
+            add_f16x8(acc, *reinterpret_cast<const uint4 *>(src + static_cast<int64_t>(j) * H));
         if (yshared)
-            add_bf16x8(acc, *reinterpret_cast<const uint4 *>(yshared + n * H + col));
+            add_f16x8(acc, *reinterpret_cast<const uint4 *>(yshared + n * H + col));
         uint4 pk;
         pk.x = pack_bf16x2(acc[0], acc[1]);
         pk.y = pack_bf16x2(acc[2], acc[3]);

@@ -6,10 +6,18 @@
 //
 //   K3 (kGateUp): for the 128 rows of block b (expert e = block_expert[b]),
 //       A = x[token(q)] gathered row by row, B0 = Wg[e], B1 = Wu[e];
-//       act[b*128 + r, :] = bf16(silu(A B0^T) * (A B1^T))  (128-column tiles)
-//   K4 (kDown): A = act rows of block b, B0 = Wd[e];
-//       y[q, :] = bf16(w[q] * (A B0^T))                     (256-column tiles)
+//       a = silu(A B0^T) * (A B1^T) in fp32 (128-column tiles), stored as
+//       the pair act_hi = bf16(a), act_lo = bf16(a - act_hi)
+//   K4 (kDown): A = act_hi and act_lo rows of block b, B0 = Wd[e];
+//       y[q, :] = fp16(w[q] * (act_hi B0^T + act_lo B0^T))  (256-column tiles)
 //       where w[q] is the routing weight of pair q (or the shared gate).
+//       Both MMAs accumulate into the same TMEM tile, so the activation
+//       reaches the down projection with ~16 significant bits instead of
+//       bf16's 8 (a bf16 activation alone costs ~1.6e-3 relative error per
+//       pair, more than the layer's output tolerance leaves over the final
+//       bf16 rounding).  The per-pair results are stored in fp16: the same
+//       bytes as bf16 with an 8x finer rounding step.  |y| > 65504 records
+//       MOE_ERR_DEVICE_CHECK.
 // Padding rows (q >= q_limit) are computed by the MMA but never loaded from
 // memory nor stored.
 //
@@ -20,7 +28,7 @@
 //   warp 1    TMEM allocator and MMA issuer (one thread): 4 x K=16 tcgen05
 //             MMAs per 64-wide K slice into one of two TMEM accumulators.
 //   warps 2-5 epilogue: tcgen05.ld of the 128 x 256 fp32 accumulator (one
-//             row per thread), activation or weight scale, bf16 stores.
+//             row per thread), activation or weight scale, 16-byte stores.
 // The two accumulators let the epilogue of tile t overlap the mainloop of
 // tile t+1.  Every wait is bounded (see ptx.cuh).
 #include <cuda_bf16.h>
@@ -32,17 +40,16 @@ namespace moe {
 
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kMaxStages = 4;
 constexpr int kThreads = 192;
 constexpr int kATileBytes = kBlockM * 128;  // 128 rows x 64 bf16
-constexpr int kBTileBytes = 256 * 128;      // 256 weight rows x 64 bf16
-constexpr int kStageBytes = kATileBytes + kBTileBytes;
 constexpr int kAccCols = 256;               // fp32 columns per accumulator
 constexpr uint32_t kTmemCols = 2 * kAccCols;
+constexpr float kF16Max = 65504.f;
 
 struct GemmSmem {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t drain;
@@ -50,21 +57,41 @@ struct GemmSmem {
     int abort_flag;
 };
 
+// Per-mode tile shape: BN output columns per tile, A_TILES activation tiles
+// (the gathered x, or act_hi + act_lo) and B_TILES weight tiles per K slice.
 template <int MODE>
 struct Cfg {
-    static constexpr int BN = MODE == kGateUp ? 128 : 256;  // output columns per tile
+    static constexpr int BN = MODE == kGateUp ? 128 : 256;
+    static constexpr int A_TILES = MODE == kGateUp ? 1 : 2;
+    static constexpr int B_TILES = MODE == kGateUp ? 2 : 1;
+    static constexpr int B_BYTES = B_TILES * BN * 128;
+    static constexpr int STAGE_BYTES = A_TILES * kATileBytes + B_BYTES;
+    static constexpr int STAGES = MODE == kGateUp ? 4 : 3;  // 192 KB of tiles either way
 };
 
 __device__ __forceinline__ float silu_times(float g, float u) {
     return g / (1.f + __expf(-g)) * u;
 }
 
+// a -> (hi, lo) with hi = bf16(a) and lo = bf16(a - hi), two values at a time
+__device__ __forceinline__ void split_bf16x2(float a0, float a1, uint32_t &hi, uint32_t &lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a0, a1);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(a0 - hf.x, a1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
+                        const __grid_constant__ CUtensorMap tm_a_lo,
                         const __grid_constant__ CUtensorMap tm_b0,
                         const __grid_constant__ CUtensorMap tm_b1, const GemmArgs a) {
     constexpr int BN = Cfg<MODE>::BN;
+    constexpr int kStages = Cfg<MODE>::STAGES;
+    constexpr int kStageBytes = Cfg<MODE>::STAGE_BYTES;
+    constexpr int kBOffset = Cfg<MODE>::A_TILES * kATileBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *tiles = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -88,6 +115,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensor_map(&tm_a);
         prefetch_tensor_map(&tm_b0);
         if (MODE == kGateUp) prefetch_tensor_map(&tm_b1);
+        if (MODE == kDown) prefetch_tensor_map(&tm_a_lo);
     }
     if (warp == 1) {
         tmem_alloc(&sm->tmem_base, kTmemCols);
@@ -131,8 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 4; ++i)
                 if (src[i] < 0) src[i] = first_valid;  // a real row; its result is dropped
             const uint32_t groups = __popc(__ballot_sync(0xffffffffu, any));
-            const uint32_t b_bytes = MODE == kGateUp ? 2 * BN * 128 : BN * 128;
-            const uint32_t tx = groups * 4 * 128 + b_bytes;
+            const uint32_t tx = groups * 512 * Cfg<MODE>::A_TILES + Cfg<MODE>::B_BYTES;
             const int brow = static_cast<int>(static_cast<int64_t>(expert) * a.w_rows) + nt * BN;
             for (int kc = 0; kc < nk; ++kc, ++g) {
                 const int s = g % kStages;
@@ -151,13 +178,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t *st = tiles + s * kStageBytes;
                 if (lane == 0) mbar_arrive_expect_tx(&sm->full[s], tx);
                 __syncwarp();
-                if (any)
+                if (any) {
                     tma_gather4(st + lane * 512, &tm_a, &sm->full[s], kc * kBlockK, src[0],
                                 src[1], src[2], src[3]);
+                    if (MODE == kDown)
+                        tma_gather4(st + kATileBytes + lane * 512, &tm_a_lo, &sm->full[s],
+                                    kc * kBlockK, src[0], src[1], src[2], src[3]);
+                }
                 if (lane == 0) {
-                    tma_load_2d(st + kATileBytes, &tm_b0, &sm->full[s], kc * kBlockK, brow);
+                    tma_load_2d(st + kBOffset, &tm_b0, &sm->full[s], kc * kBlockK, brow);
                     if (MODE == kGateUp)
-                        tma_load_2d(st + kATileBytes + BN * 128, &tm_b1, &sm->full[s],
+                        tma_load_2d(st + kBOffset + BN * 128, &tm_b1, &sm->full[s],
                                     kc * kBlockK, brow);
                 }
             }
@@ -191,15 +222,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after_sync();
                     const uint8_t *st = tiles + s * kStageBytes;
                     const uint64_t da = sw128_kmajor_desc(smem_addr(st));
-                    const uint64_t db = sw128_kmajor_desc(smem_addr(st + kATileBytes));
+                    const uint64_t db = sw128_kmajor_desc(smem_addr(st + kBOffset));
 #pragma unroll
                     for (int kk = 0; kk < kBlockK / 16; ++kk) {
                         const uint32_t accumulate = (kc | kk) != 0;
                         mma_bf16(d, da + 2 * kk, db + 2 * kk, idesc, accumulate);
                         if (MODE == kGateUp) {
                             const uint64_t db1 =
-                                sw128_kmajor_desc(smem_addr(st + kATileBytes + BN * 128));
+                                sw128_kmajor_desc(smem_addr(st + kBOffset + BN * 128));
                             mma_bf16(d + BN, da + 2 * kk, db1 + 2 * kk, idesc, accumulate);
+                        } else {
+                            const uint64_t da_lo = sw128_kmajor_desc(smem_addr(st + kATileBytes));
+                            mma_bf16(d, da_lo + 2 * kk, db + 2 * kk, idesc, 1u);
                         }
                     }
                     mma_commit(&sm->empty[s]);
@@ -241,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int col0 = nt * BN;
             if (MODE == kGateUp) {
                 uint16_t *dst = a.out + grow * a.out_ld + col0;
+                uint16_t *dst_lo = a.out_lo + grow * a.out_ld + col0;
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     float gv[32], uv[32];
@@ -252,16 +287,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int v8 = 0; v8 < 4; ++v8) {
                             const int col = col0 + c * 32 + v8 * 8;
                             if (col + 8 <= a.n_out) {
-                                uint4 pk;
-                                pk.x = pack_bf16x2(silu_times(gv[v8 * 8 + 0], uv[v8 * 8 + 0]),
-                                                   silu_times(gv[v8 * 8 + 1], uv[v8 * 8 + 1]));
-                                pk.y = pack_bf16x2(silu_times(gv[v8 * 8 + 2], uv[v8 * 8 + 2]),
-                                                   silu_times(gv[v8 * 8 + 3], uv[v8 * 8 + 3]));
-                                pk.z = pack_bf16x2(silu_times(gv[v8 * 8 + 4], uv[v8 * 8 + 4]),
-                                                   silu_times(gv[v8 * 8 + 5], uv[v8 * 8 + 5]));
-                                pk.w = pack_bf16x2(silu_times(gv[v8 * 8 + 6], uv[v8 * 8 + 6]),
-                                                   silu_times(gv[v8 * 8 + 7], uv[v8 * 8 + 7]));
-                                *reinterpret_cast<uint4 *>(dst + c * 32 + v8 * 8) = pk;
+                                uint32_t hi[4], lo[4];
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const float a0 = silu_times(gv[v8 * 8 + 2 * i], uv[v8 * 8 + 2 * i]);
+                                    const float a1 = silu_times(gv[v8 * 8 + 2 * i + 1],
+                                                                uv[v8 * 8 + 2 * i + 1]);
+                                    split_bf16x2(a0, a1, hi[i], lo[i]);
+                                }
+                                *reinterpret_cast<uint4 *>(dst + c * 32 + v8 * 8) =
+                                    make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                                *reinterpret_cast<uint4 *>(dst_lo + c * 32 + v8 * 8) =
+                                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
                             }
                         }
                     }
@@ -269,6 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 const float w = valid ? a.scale[q] : 0.f;
                 uint16_t *dst = a.out + (valid ? q : 0) * a.out_ld + col0;
+                float vmax = 0.f;
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     float yv[32];
@@ -279,16 +317,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int v8 = 0; v8 < 4; ++v8) {
                             const int col = col0 + c * 32 + v8 * 8;
                             if (col + 8 <= a.n_out) {
+                                float t[8];
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    t[i] = w * yv[v8 * 8 + i];
+                                    vmax = fmaxf(vmax, fabsf(t[i]));
+                                }
                                 uint4 pk;
-                                pk.x = pack_bf16x2(w * yv[v8 * 8 + 0], w * yv[v8 * 8 + 1]);
-                                pk.y = pack_bf16x2(w * yv[v8 * 8 + 2], w * yv[v8 * 8 + 3]);
-                                pk.z = pack_bf16x2(w * yv[v8 * 8 + 4], w * yv[v8 * 8 + 5]);
-                                pk.w = pack_bf16x2(w * yv[v8 * 8 + 6], w * yv[v8 * 8 + 7]);
+                                pk.x = pack_f16x2(t[0], t[1]);
+                                pk.y = pack_f16x2(t[2], t[3]);
+                                pk.z = pack_f16x2(t[4], t[5]);
+                                pk.w = pack_f16x2(t[6], t[7]);
                                 *reinterpret_cast<uint4 *>(dst + c * 32 + v8 * 8) = pk;
                             }
                         }
                     }
                 }
+                // fp16 keeps 11 significant bits; a value past its range is
+                // reported rather than silently turned into infinity
+                if (!(vmax <= kF16Max)) record_status(a.status, MOE_ERR_DEVICE_CHECK);
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -308,16 +355,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int gemm_block_n(GemmMode mode) { return mode == kGateUp ? Cfg<kGateUp>::BN : Cfg<kDown>::BN; }
 
-size_t gemm_smem_bytes() { return 1024 + kStages * kStageBytes + sizeof(GemmSmem); }
+size_t gemm_smem_bytes(GemmMode mode) {
+    const size_t tiles = mode == kGateUp
+                             ? Cfg<kGateUp>::STAGES * Cfg<kGateUp>::STAGE_BYTES
+                             : Cfg<kDown>::STAGES * Cfg<kDown>::STAGE_BYTES;
+    return 1024 + tiles + sizeof(GemmSmem);
+}
 
-cudaError_t launch_gemm(GemmMode mode, const CUtensorMap &tm_a, const CUtensorMap &tm_b0,
-                        const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s) {
-    const size_t smem = gemm_smem_bytes();
+cudaError_t launch_gemm(GemmMode mode, const CUtensorMap &tm_a, const CUtensorMap &tm_a_lo,
+                        const CUtensorMap &tm_b0, const CUtensorMap &tm_b1, const GemmArgs &a,
+                        cudaStream_t s) {
+    const size_t smem = gemm_smem_bytes(mode);
     auto kern = mode == kGateUp ? grouped_gemm_kernel<kGateUp> : grouped_gemm_kernel<kDown>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    kern<<<a.grid, kThreads, smem, s>>>(tm_a, tm_b0, tm_b1, a);
+    kern<<<a.grid, kThreads, smem, s>>>(tm_a, tm_a_lo, tm_b0, tm_b1, a);
     return cudaGetLastError();
 }
 

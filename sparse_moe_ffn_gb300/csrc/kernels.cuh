@@ -64,7 +64,8 @@ struct GemmArgs {
     int K;              // reduction length (H for gate/up, I for down)
     int n_out;          // output columns (I for gate/up, H for down)
     int64_t w_rows;     // weight rows per expert (I or H)
-    uint16_t *out;      // act [rows, I] (gate/up) or y [q_limit, H] (down)
+    uint16_t *out;      // act_hi [rows, I] (gate/up) or fp16 y [q_limit, H] (down)
+    uint16_t *out_lo;   // act_lo [rows, I] (gate/up only)
     int64_t out_ld;
     const float *scale; // down: per-q weight
     int32_t *status;
@@ -72,9 +73,12 @@ struct GemmArgs {
     int grid;           // persistent CTAs
 };
 
-size_t gemm_smem_bytes();
-cudaError_t launch_gemm(GemmMode mode, const CUtensorMap &tm_a, const CUtensorMap &tm_b0,
-                        const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s);
+size_t gemm_smem_bytes(GemmMode mode);
+// tm_a: A rows (x or act_hi); tm_a_lo: act_lo rows (down only); tm_b0/tm_b1:
+// weight rows (Wg/Wu for gate/up, Wd for down)
+cudaError_t launch_gemm(GemmMode mode, const CUtensorMap &tm_a, const CUtensorMap &tm_a_lo,
+                        const CUtensorMap &tm_b0, const CUtensorMap &tm_b1, const GemmArgs &a,
+                        cudaStream_t s);
 int gemm_block_n(GemmMode mode);
 
 // ----------------------------------------------------------------- combine
