@@ -58,6 +58,7 @@ def lib():
         "moe_read_device_status": ([P, P], i32),
         "moe_kernel_launch_count": ([], ctypes.c_uint64),
         "moe_set_stage_events": ([P, i32], i32),
+        "moe_selftest_wait_timeout": ([P, sz, ctypes.c_uint64, P], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -244,6 +245,12 @@ def workspace_views(workspace, N, H, E, I, k, I_s=0) -> dict:
         v["act_shared_lo"] = view(lay["act_shared_lo"], torch.bfloat16, (rows_s, I_s))
         v["y_shared"] = view(lay["y_shared"], torch.float16, (N, H))
     return v
+
+
+def moe_selftest_wait_timeout(workspace, limit_ns: int) -> None:
+    """Enqueue the device wait-timeout self-check (see moe.h)."""
+    _check(lib().moe_selftest_wait_timeout(_ptr(workspace), workspace.numel(), int(limit_ns),
+                                           _stream()), "moe_selftest_wait_timeout")
 
 
 def moe_read_device_status(workspace) -> int:

@@ -547,6 +547,20 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
     return MOE_OK;
 }
 
+moe_status_t moe_selftest_wait_timeout(void *workspace, size_t workspace_bytes,
+                                       uint64_t limit_ns, cudaStream_t stream) {
+    g_last_error.clear();
+    if (!workspace || workspace_bytes < sizeof(int32_t))
+        return fail(MOE_ERR_INVALID_ARG, "need a workspace of at least 4 bytes");
+    if (limit_ns == 0 || limit_ns > 10000000000ull)
+        return fail(MOE_ERR_INVALID_ARG, "limit_ns must be in (0, 10 s]");
+    int32_t *status = static_cast<int32_t *>(workspace);
+    MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int32_t), stream), "status reset");
+    MOE_CUDA(launch_wait_timeout_probe(status, limit_ns, stream), "self-test kernel launch");
+    g_launches += 1;
+    return MOE_OK;
+}
+
 moe_status_t moe_read_device_status(const void *workspace, cudaStream_t stream) {
     if (!workspace) return fail(MOE_ERR_INVALID_ARG, "workspace must be non-null");
     MOE_CUDA(cudaStreamSynchronize(stream), "stream synchronize");

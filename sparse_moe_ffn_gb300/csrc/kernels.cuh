@@ -86,4 +86,8 @@ int gemm_block_n(GemmMode mode);
 cudaError_t launch_combine(const uint16_t *ypair, const uint16_t *yshared, int64_t N, int H,
                            int k, uint16_t *out, int num_sms, cudaStream_t s);
 
+// ---------------------------------------------------------------- selftest
+
+cudaError_t launch_wait_timeout_probe(int32_t *status, uint64_t limit_ns, cudaStream_t s);
+
 }  // namespace moe

@@ -59,16 +59,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Returns false if
-// `abort_flag` became non-zero or the time limit passed.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
-                                          volatile int *abort_flag) {
+// `abort_flag` became non-zero or `limit_ns` passed.
+__device__ __forceinline__ bool mbar_wait_ns(uint64_t *bar, uint32_t parity,
+                                             volatile int *abort_flag, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+        if (global_timer_ns() - t0 > limit_ns) return false;
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          volatile int *abort_flag) {
+    return mbar_wait_ns(bar, parity, abort_flag, kWaitTimeoutNs);
 }
 
 // -------------------------------------------------------------------- TMA

@@ -1,0 +1,49 @@
+"""bench.py's multi-rank logic on CPU: two gloo ranks, replicas of the same
+per-GPU workload with no data-path collective; the step time is the max over
+ranks and only rank 0 runs the reference arm."""
+import os
+import socket
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        bench.barrier(world)
+        slowest = bench.max_over_ranks(10.0 + rank, world, "cpu")
+
+        class A:  # the reference arm on a non-zero rank does no work
+            config, seed, steps, warmup = "tiny", 0, 1, 3
+        if rank != 0:
+            bench.run_reference(A, world, rank)
+        q.put((rank, slowest))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_take_the_max():
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+    assert all(p.exitcode == 0 for p in procs), [p.exitcode for p in procs]
+    got = dict(q.get(timeout=5) for _ in range(world))
+    assert got == {0: 11.0, 1: 11.0}
