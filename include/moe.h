@@ -183,6 +183,7 @@ typedef struct {
     size_t align_scratch; /* int32 [chunks, E]                                */
     size_t sorted_pair;   /* int32 [capacity]                                 */
     size_t block_expert;  /* int32 [capacity / 128]                           */
+    size_t x_sorted;      /* bf16 [capacity, H]   x rows in expert order (dense blocks) */
     size_t act;           /* bf16 [capacity, I]   a_hi = bf16(a), a = silu(x Wg^T) * (x Wu^T) */
     size_t act_lo;        /* bf16 [capacity, I]   a_lo = bf16(a - a_hi)       */
     size_t ypair;         /* fp16 [N*k, H]        w * Expert(x), per pair     */

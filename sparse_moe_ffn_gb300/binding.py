@@ -28,7 +28,8 @@ class MoEError(RuntimeError):
 class _Layout(ctypes.Structure):
     _fields_ = [(name, ctypes.c_size_t) for name in (
         "status", "topk_w", "topk_ids", "gamma", "counts", "offsets", "pad_offsets",
-        "num_padded", "align_scratch", "sorted_pair", "block_expert", "act", "act_lo", "ypair",
+        "num_padded", "align_scratch", "sorted_pair", "block_expert", "x_sorted", "act", "act_lo",
+        "ypair",
         "act_shared", "act_shared_lo", "y_shared", "total")] + [("capacity", ctypes.c_int64)]
 
 
@@ -234,6 +235,7 @@ def workspace_views(workspace, N, H, E, I, k, I_s=0) -> dict:
         "num_padded": view(lay["num_padded"], torch.int32, (1,)),
         "sorted_pair": view(lay["sorted_pair"], torch.int32, (cap,)),
         "block_expert": view(lay["block_expert"], torch.int32, (cap // MOE_BLOCK_M,)),
+        "x_sorted": view(lay["x_sorted"], torch.bfloat16, (cap, H)),
         "act": view(lay["act"], torch.bfloat16, (cap, I)),
         "act_lo": view(lay["act_lo"], torch.bfloat16, (cap, I)),
         "ypair": view(lay["ypair"], torch.float16, (P, H)),

@@ -218,6 +218,7 @@ moe_status_t forward_layout(int64_t N, int H, int E, int I, int k, int I_s,
     L->align_scratch = take(sizeof(int32_t) * static_cast<size_t>(align_chunks(P)) * E);
     L->sorted_pair = take(sizeof(int32_t) * cap);
     L->block_expert = take(sizeof(int32_t) * (cap / kBlockM));
+    L->x_sorted = take(2 * static_cast<size_t>(cap) * H);
     L->act = take(2 * static_cast<size_t>(cap) * I);
     L->act_lo = take(2 * static_cast<size_t>(cap) * I);
     L->ypair = take(2 * static_cast<size_t>(P) * H);  // fp16
@@ -388,6 +389,7 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
     float *topk_w = reinterpret_cast<float *>(at(L.topk_w));
     int32_t *topk_ids = reinterpret_cast<int32_t *>(at(L.topk_ids));
     float *gamma = shared ? reinterpret_cast<float *>(at(L.gamma)) : nullptr;
+    uint16_t *x_sorted = reinterpret_cast<uint16_t *>(at(L.x_sorted));
     uint16_t *act = reinterpret_cast<uint16_t *>(at(L.act));
     uint16_t *act_lo = reinterpret_cast<uint16_t *>(at(L.act_lo));
     uint16_t *ypair = reinterpret_cast<uint16_t *>(at(L.ypair));
@@ -419,8 +421,11 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
 
     // K3: gathered gate/up GEMM + silu * up
     if ((st = record_stage(MOE_STAGE_GATE_UP, stream)) != MOE_OK) return st;
-    CUtensorMap tm_xrows, tm_wg, tm_wu, tm_act, tm_act_lo, tm_wd;
+    CUtensorMap tm_xrows, tm_xsorted, tm_wg, tm_wu, tm_act, tm_act_lo, tm_act_box, tm_act_lo_box,
+        tm_wd;
     if ((st = make_map(&tm_xrows, x, H, N, H, kBlockK, 1, "x rows")) != MOE_OK) return st;
+    if ((st = make_map(&tm_xsorted, x_sorted, H, cap, H, kBlockK, kBlockM, "x_sorted")) != MOE_OK)
+        return st;
     if ((st = make_map(&tm_wg, w_gate, H, static_cast<uint64_t>(E) * I, H, kBlockK,
                        gemm_block_n(kGateUp), "w_gate")) != MOE_OK)
         return st;
@@ -447,14 +452,20 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
         g.max_tiles = static_cast<int>(cap / kBlockM) * nt;
         g.grid = g.max_tiles < sms ? g.max_tiles : sms;
     }
-    MOE_CUDA(launch_gemm(kGateUp, tm_xrows, tm_xrows, tm_wg, tm_wu, g, stream),
+    MOE_CUDA(launch_gather_rows(x, H, k, b.sorted_pair, b.num_padded, P, cap, x_sorted, sms, stream),
+             "gather kernel launch");
+    MOE_CUDA(launch_gemm(kGateUp, tm_xrows, tm_xrows, tm_xsorted, tm_xsorted, tm_wg, tm_wu, g,
+                         stream),
              "gate/up kernel launch");
-    g_launches += 1;
+    g_launches += 2;
 
     // K4: down GEMM * routing weight, one row per pair
     if ((st = record_stage(MOE_STAGE_DOWN, stream)) != MOE_OK) return st;
     if ((st = make_map(&tm_act, act, I, cap, I, kBlockK, 1, "act rows")) != MOE_OK) return st;
     if ((st = make_map(&tm_act_lo, act_lo, I, cap, I, kBlockK, 1, "act_lo rows")) != MOE_OK)
+        return st;
+    if ((st = make_map(&tm_act_box, act, I, cap, I, kBlockK, kBlockM, "act")) != MOE_OK) return st;
+    if ((st = make_map(&tm_act_lo_box, act_lo, I, cap, I, kBlockK, kBlockM, "act_lo")) != MOE_OK)
         return st;
     if ((st = make_map(&tm_wd, w_down, I, static_cast<uint64_t>(E) * H, I, kBlockK,
                        gemm_block_n(kDown), "w_down")) != MOE_OK)
@@ -472,7 +483,8 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
         g.max_tiles = static_cast<int>(cap / kBlockM) * nt;
         g.grid = g.max_tiles < sms ? g.max_tiles : sms;
     }
-    MOE_CUDA(launch_gemm(kDown, tm_act, tm_act_lo, tm_wd, tm_wd, g, stream),
+    MOE_CUDA(launch_gemm(kDown, tm_act, tm_act_lo, tm_act_box, tm_act_lo_box, tm_wd, tm_wd, g,
+                         stream),
              "down kernel launch");
     g_launches += 1;
 
@@ -484,17 +496,18 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
         uint16_t *act_s_lo = reinterpret_cast<uint16_t *>(at(L.act_shared_lo));
         y_shared = reinterpret_cast<uint16_t *>(at(L.y_shared));
         const int64_t rows_s = round_up64(N, kBlockM);
-        CUtensorMap tm_sg, tm_su, tm_acts, tm_acts_lo, tm_sd;
+        CUtensorMap tm_sg, tm_su, tm_acts, tm_acts_lo, tm_sd, tm_xbox;
+        if ((st = make_map(&tm_xbox, x, H, N, H, kBlockK, kBlockM, "x")) != MOE_OK) return st;
         if ((st = make_map(&tm_sg, shared_gate_proj, H, I_s, H, kBlockK, gemm_block_n(kGateUp),
                            "shared_gate_proj")) != MOE_OK)
             return st;
         if ((st = make_map(&tm_su, shared_up_proj, H, I_s, H, kBlockK, gemm_block_n(kGateUp),
                            "shared_up_proj")) != MOE_OK)
             return st;
-        if ((st = make_map(&tm_acts, act_s, I_s, rows_s, I_s, kBlockK, 1, "shared act rows")) !=
-            MOE_OK)
+        if ((st = make_map(&tm_acts, act_s, I_s, rows_s, I_s, kBlockK, kBlockM,
+                           "shared act rows")) != MOE_OK)
             return st;
-        if ((st = make_map(&tm_acts_lo, act_s_lo, I_s, rows_s, I_s, kBlockK, 1,
+        if ((st = make_map(&tm_acts_lo, act_s_lo, I_s, rows_s, I_s, kBlockK, kBlockM,
                            "shared act_lo rows")) != MOE_OK)
             return st;
         if ((st = make_map(&tm_sd, shared_down_proj, I_s, H, I_s, kBlockK, gemm_block_n(kDown),
@@ -520,7 +533,7 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
             s.max_tiles = static_cast<int>(rows_s / kBlockM) * nt;
             s.grid = s.max_tiles < sms ? s.max_tiles : sms;
         }
-        MOE_CUDA(launch_gemm(kGateUp, tm_xrows, tm_xrows, tm_sg, tm_su, s, stream),
+        MOE_CUDA(launch_gemm(kGateUp, tm_xbox, tm_xbox, tm_xbox, tm_xbox, tm_sg, tm_su, s, stream),
                  "shared gate/up kernel launch");
         s.K = I_s;
         s.n_out = H;
@@ -534,7 +547,8 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
             s.max_tiles = static_cast<int>(rows_s / kBlockM) * nt;
             s.grid = s.max_tiles < sms ? s.max_tiles : sms;
         }
-        MOE_CUDA(launch_gemm(kDown, tm_acts, tm_acts_lo, tm_sd, tm_sd, s, stream),
+        MOE_CUDA(launch_gemm(kDown, tm_acts, tm_acts_lo, tm_acts, tm_acts_lo, tm_sd, tm_sd, s,
+                         stream),
                  "shared down kernel launch");
         g_launches += 2;
     }

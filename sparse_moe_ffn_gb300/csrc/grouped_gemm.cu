@@ -21,10 +21,21 @@
 // Padding rows (q >= q_limit) are computed by the MMA but never loaded from
 // memory nor stored.
 //
+// A rows come in one of two ways, chosen per block:
+//   dense  (more than kSparseRows real rows): one tiled 128-row TMA box per A
+//          operand per K slice, from rows that are contiguous in memory (x
+//          rows copied into expert order by gather_rows_kernel, act rows, or x
+//          itself for the shared expert);
+//   sparse (at most kSparseRows real rows, e.g. decode): each lane fetches 4
+//          rows with one tile::gather4 copy, skipped when all 4 are padding,
+//          so padding rows are never read.  A gather4 copy costs the TMA unit
+//          far more than a box (32 of them per K slice ran the gate/up GEMM
+//          2.6x slower at prefill), hence only for blocks that are mostly
+//          padding.
+//
 // Persistent kernel, one CTA per SM, 6 warps:
-//   warp 0    TMA producer: each lane fetches 4 rows of A with one
-//             tile::gather4 copy (skipped when all 4 are padding); lane 0
-//             fetches the weight tile(s) with tiled copies.
+//   warp 0    TMA producer: A rows (box or gather4), then lane 0 fetches the
+//             weight tile(s) with tiled copies.
 //   warp 1    TMEM allocator and MMA issuer (one thread): 4 x K=16 tcgen05
 //             MMAs per 64-wide K slice into one of two TMEM accumulators.
 //   warps 2-5 epilogue: tcgen05.ld of the 128 x 256 fp32 accumulator (one
@@ -46,6 +57,7 @@ constexpr int kATileBytes = kBlockM * 128;  // 128 rows x 64 bf16
 constexpr int kAccCols = 256;               // fp32 columns per accumulator
 constexpr uint32_t kTmemCols = 2 * kAccCols;
 constexpr float kF16Max = 65504.f;
+constexpr int kSparseRows = 32;             // blocks with at most this many real rows gather
 
 struct GemmSmem {
     uint64_t full[kMaxStages];
@@ -86,6 +98,8 @@ template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                         const __grid_constant__ CUtensorMap tm_a_lo,
+                        const __grid_constant__ CUtensorMap tm_a_box,
+                        const __grid_constant__ CUtensorMap tm_a_lo_box,
                         const __grid_constant__ CUtensorMap tm_b0,
                         const __grid_constant__ CUtensorMap tm_b1, const GemmArgs a) {
     constexpr int BN = Cfg<MODE>::BN;
@@ -116,6 +130,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensor_map(&tm_b0);
         if (MODE == kGateUp) prefetch_tensor_map(&tm_b1);
         if (MODE == kDown) prefetch_tensor_map(&tm_a_lo);
+        prefetch_tensor_map(&tm_a_box);
+        if (MODE == kDown) prefetch_tensor_map(&tm_a_lo_box);
     }
     if (warp == 1) {
         tmem_alloc(&sm->tmem_base, kTmemCols);
@@ -141,25 +157,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int blk = tile / n_tiles;
             const int nt = tile % n_tiles;
             const int expert = a.block_expert ? a.block_expert[blk] : 0;
-            // rows 4*lane .. 4*lane+3 of this block
+            // dense: the block has more than kSparseRows real rows (real rows
+            // come first in a block, so looking at row kSparseRows suffices)
+            bool dense = true;
+            if (a.sorted_pair) {
+                const int64_t probe = a.sorted_pair[static_cast<int64_t>(blk) * kBlockM + kSparseRows];
+                dense = probe >= 0 && probe < a.q_limit;
+            }
+            // sparse: rows 4*lane .. 4*lane+3 of this block
             int src[4];
             bool any = false;
             int first_valid = -1;
+            if (!dense) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int64_t row = static_cast<int64_t>(blk) * kBlockM + lane * 4 + i;
-                const int64_t q = a.sorted_pair ? a.sorted_pair[row] : row;
-                const bool v = q >= 0 && q < a.q_limit;
-                src[i] = !v ? -1 : (MODE == kGateUp ? static_cast<int>(q / a.k_div)
-                                                    : static_cast<int>(row));
-                if (v && first_valid < 0) first_valid = src[i];
-                any |= v;
+                for (int i = 0; i < 4; ++i) {
+                    const int64_t row = static_cast<int64_t>(blk) * kBlockM + lane * 4 + i;
+                    const int64_t q = a.sorted_pair[row];
+                    const bool v = q >= 0 && q < a.q_limit;
+                    src[i] = !v ? -1 : (MODE == kGateUp ? static_cast<int>(q / a.k_div)
+                                                        : static_cast<int>(row));
+                    if (v && first_valid < 0) first_valid = src[i];
+                    any |= v;
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (src[i] < 0) src[i] = first_valid;  // a real row; its result is dropped
             }
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                if (src[i] < 0) src[i] = first_valid;  // a real row; its result is dropped
-            const uint32_t groups = __popc(__ballot_sync(0xffffffffu, any));
-            const uint32_t tx = groups * 512 * Cfg<MODE>::A_TILES + Cfg<MODE>::B_BYTES;
+            const uint32_t groups = dense ? 0u : __popc(__ballot_sync(0xffffffffu, any));
+            const uint32_t a_bytes = dense ? kATileBytes : groups * 512;
+            const uint32_t tx = a_bytes * Cfg<MODE>::A_TILES + Cfg<MODE>::B_BYTES;
+            const int arow = blk * kBlockM;
             const int brow = static_cast<int>(static_cast<int64_t>(expert) * a.w_rows) + nt * BN;
             for (int kc = 0; kc < nk; ++kc, ++g) {
                 const int s = g % kStages;
@@ -178,7 +205,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t *st = tiles + s * kStageBytes;
                 if (lane == 0) mbar_arrive_expect_tx(&sm->full[s], tx);
                 __syncwarp();
-                if (any) {
+                if (dense) {
+                    if (lane == 0) {
+                        tma_load_2d(st, &tm_a_box, &sm->full[s], kc * kBlockK, arow);
+                        if (MODE == kDown)
+                            tma_load_2d(st + kATileBytes, &tm_a_lo_box, &sm->full[s],
+                                        kc * kBlockK, arow);
+                    }
+                } else if (any) {
                     tma_gather4(st + lane * 512, &tm_a, &sm->full[s], kc * kBlockK, src[0],
                                 src[1], src[2], src[3]);
                     if (MODE == kDown)
@@ -351,7 +385,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// x_sorted[s, :] = x[sorted_pair[s] / k, :] for the real rows s of dense
+// blocks (the A operand of the gate/up GEMM in expert order); one warp per
+// row, 16-byte loads and stores.
+__global__ void __launch_bounds__(256)
+    gather_rows_kernel(const uint16_t *__restrict__ x, int H, int k,
+                       const int32_t *__restrict__ sorted_pair,
+                       const int32_t *__restrict__ num_padded, int64_t P, int64_t cap,
+                       uint16_t *__restrict__ x_sorted) {
+    const int lane = threadIdx.x % 32;
+    const int64_t rows = min(static_cast<int64_t>(*num_padded), cap);
+    for (int64_t s = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32; s < rows;
+         s += static_cast<int64_t>(gridDim.x) * blockDim.x / 32) {
+        const int64_t probe = sorted_pair[s / kBlockM * kBlockM + kSparseRows];
+        if (probe < 0 || probe >= P) continue;  // sparse block: its rows are gathered by TMA
+        const int64_t q = sorted_pair[s];
+        if (q < 0 || q >= P) continue;          // padding row
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + (q / k) * H);
+        uint4 *dst = reinterpret_cast<uint4 *>(x_sorted + s * H);
+        for (int c = lane; c < H / 8; c += 32) dst[c] = src[c];
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_gather_rows(const uint16_t *x, int H, int k, const int32_t *sorted_pair,
+                               const int32_t *num_padded, int64_t P, int64_t cap,
+                               uint16_t *x_sorted, int num_sms, cudaStream_t s) {
+    int64_t blocks = (cap * 32 + 255) / 256;
+    const int64_t limit = static_cast<int64_t>(num_sms) * 8;
+    if (blocks > limit) blocks = limit;
+    gather_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(x, H, k, sorted_pair,
+                                                                    num_padded, P, cap, x_sorted);
+    return cudaGetLastError();
+}
 
 int gemm_block_n(GemmMode mode) { return mode == kGateUp ? Cfg<kGateUp>::BN : Cfg<kDown>::BN; }
 
@@ -363,6 +430,7 @@ size_t gemm_smem_bytes(GemmMode mode) {
 }
 
 cudaError_t launch_gemm(GemmMode mode, const CUtensorMap &tm_a, const CUtensorMap &tm_a_lo,
+                        const CUtensorMap &tm_a_box, const CUtensorMap &tm_a_lo_box,
                         const CUtensorMap &tm_b0, const CUtensorMap &tm_b1, const GemmArgs &a,
                         cudaStream_t s) {
     const size_t smem = gemm_smem_bytes(mode);
@@ -370,7 +438,7 @@ cudaError_t launch_gemm(GemmMode mode, const CUtensorMap &tm_a, const CUtensorMa
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    kern<<<a.grid, kThreads, smem, s>>>(tm_a, tm_a_lo, tm_b0, tm_b1, a);
+    kern<<<a.grid, kThreads, smem, s>>>(tm_a, tm_a_lo, tm_a_box, tm_a_lo_box, tm_b0, tm_b1, a);
     return cudaGetLastError();
 }
 

@@ -74,11 +74,18 @@ struct GemmArgs {
 };
 
 size_t gemm_smem_bytes(GemmMode mode);
-// tm_a: A rows (x or act_hi); tm_a_lo: act_lo rows (down only); tm_b0/tm_b1:
-// weight rows (Wg/Wu for gate/up, Wd for down)
+// tm_a / tm_a_lo: 1-row boxes for gather4 of sparse blocks (x or act_hi;
+// act_lo, down only); tm_a_box / tm_a_lo_box: 128-row boxes over rows that
+// are contiguous per block (x_sorted or x for gate/up; act_hi / act_lo for
+// down); tm_b0/tm_b1: weight rows (Wg/Wu for gate/up, Wd for down)
 cudaError_t launch_gemm(GemmMode mode, const CUtensorMap &tm_a, const CUtensorMap &tm_a_lo,
+                        const CUtensorMap &tm_a_box, const CUtensorMap &tm_a_lo_box,
                         const CUtensorMap &tm_b0, const CUtensorMap &tm_b1, const GemmArgs &a,
                         cudaStream_t s);
+// x rows of dense blocks copied into expert order (x_sorted [cap, H])
+cudaError_t launch_gather_rows(const uint16_t *x, int H, int k, const int32_t *sorted_pair,
+                               const int32_t *num_padded, int64_t P, int64_t cap,
+                               uint16_t *x_sorted, int num_sms, cudaStream_t s);
 int gemm_block_n(GemmMode mode);
 
 // ----------------------------------------------------------------- combine
