@@ -8,13 +8,16 @@
 // to the GEMM row block, padding slots hold the sentinel P = N*k, and every
 // row block records its expert.  Experts with no pairs own no block.
 //
-// Three deterministic passes, none of which uses atomics to order outputs:
+// Large P: three deterministic passes, none of which uses atomics to order
+// outputs:
 //   count:   CTA c histograms pairs [c*chunk, (c+1)*chunk) in shared memory
 //   scan:    one CTA: per-expert exclusive scan over chunks (in place),
-//            counts, offsets, padded offsets, block owners, sentinels
+//            counts, offsets, padded offsets, then block owners and the
+//            sentinel in every padded slot (coalesced, all threads)
 //   scatter: CTA c ranks each of its pairs among the same-expert pairs before
 //            it (warp match + per-warp tallies), so pair p lands at
 //            pad_off[e] + #{p' < p : expert(p') = e}: a stable order.
+// Small P (decode): the same steps inside one 1024-thread CTA, one launch.
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -25,10 +28,14 @@ namespace {
 constexpr int kAlignThreads = 256;
 constexpr int kAlignWarps = kAlignThreads / 32;
 constexpr int kScanThreads = 1024;
+constexpr int kSmallPairs = 4096;  // single-CTA path up to this many pairs
+constexpr int kSmallMaxE = 256;
 
 __global__ void __launch_bounds__(kAlignThreads)
     align_count_kernel(const int32_t *__restrict__ ids, int64_t P, int E, int chunk,
                        int32_t *__restrict__ chunk_counts, int32_t *status) {
+    griddep_launch_dependents();
+    griddep_wait();
     extern __shared__ int32_t hist[];
     for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
     __syncthreads();
@@ -36,7 +43,7 @@ __global__ void __launch_bounds__(kAlignThreads)
     const int64_t end = min(P, start + chunk);
     bool bad = false;
     for (int64_t p = start + threadIdx.x; p < end; p += blockDim.x) {
-        const int e = ids[p];
+        const int e = __ldcg(ids + p);
         if (e < 0 || e >= E) {
             bad = true;
             continue;
@@ -77,11 +84,33 @@ __device__ int32_t block_exclusive_scan(int32_t v, int32_t *warp_sums, int32_t *
     return r;
 }
 
+// Expert owning padded slot `slot`: the last e with pad_off[e] <= slot
+// (experts without pairs share their successor's offset and own nothing).
+__device__ __forceinline__ int owner_of(const int32_t *pad_off, int E, int64_t slot) {
+    int lo = 0, hi = E;  // answer in [lo, hi)
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) / 2;
+        if (pad_off[mid] <= slot) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+// every padded slot gets the sentinel P, every row block its owner expert
+__device__ void fill_padded(const int32_t *pad_off_smem, int E, int block_m, int32_t num_padded,
+                            int64_t P, int32_t *sorted_pair, int32_t *block_expert) {
+    for (int32_t i = threadIdx.x; i < num_padded; i += blockDim.x)
+        sorted_pair[i] = static_cast<int32_t>(P);
+    for (int32_t b = threadIdx.x; b < num_padded / block_m; b += blockDim.x)
+        block_expert[b] = owner_of(pad_off_smem, E, static_cast<int64_t>(b) * block_m);
+}
+
 __global__ void __launch_bounds__(kScanThreads)
     align_scan_kernel(int32_t *__restrict__ chunk_counts, int nchunks, int E, int block_m,
                       int64_t P, int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
                       int32_t *__restrict__ pad_offsets, int32_t *__restrict__ num_padded,
                       int32_t *__restrict__ block_expert, int32_t *__restrict__ sorted_pair) {
+    griddep_launch_dependents();
+    griddep_wait();
     __shared__ int32_t warp_sums[32];
     __shared__ int32_t total;
     const int e = threadIdx.x;
@@ -90,7 +119,7 @@ __global__ void __launch_bounds__(kScanThreads)
         // per-expert exclusive scan over chunks, in place: count -> base
         for (int c = 0; c < nchunks; ++c) {
             int32_t *slot = chunk_counts + static_cast<int64_t>(c) * E + e;
-            const int32_t v = *slot;
+            const int32_t v = __ldcg(slot);
             *slot = cnt;
             cnt += v;
         }
@@ -98,18 +127,23 @@ __global__ void __launch_bounds__(kScanThreads)
     const int32_t seg = (cnt + block_m - 1) / block_m * block_m;
     const int32_t off = block_exclusive_scan(cnt, warp_sums, &total);
     const int32_t pad = block_exclusive_scan(seg, warp_sums, &total);
+    __shared__ int32_t pad_smem[1024 + 1];
+    __shared__ int32_t npad;
     if (e < E) {
         counts[e] = cnt;
         offsets[e] = off;
         pad_offsets[e] = pad;
+        pad_smem[e] = pad;
         if (e == E - 1) {
             offsets[E] = off + cnt;
             pad_offsets[E] = pad + seg;
             *num_padded = pad + seg;
+            npad = pad + seg;
         }
-        for (int32_t b = pad / block_m; b < (pad + seg) / block_m; ++b) block_expert[b] = e;
-        for (int32_t i = pad + cnt; i < pad + seg; ++i) sorted_pair[i] = static_cast<int32_t>(P);
     }
+    __syncthreads();
+    // the scatter kernel overwrites the real slots after this kernel ends
+    fill_padded(pad_smem, E, block_m, npad, P, sorted_pair, block_expert);
 }
 
 __global__ void __launch_bounds__(kAlignThreads)
@@ -117,6 +151,8 @@ __global__ void __launch_bounds__(kAlignThreads)
                          const int32_t *__restrict__ chunk_base,
                          const int32_t *__restrict__ pad_offsets,
                          int32_t *__restrict__ sorted_pair) {
+    griddep_launch_dependents();
+    griddep_wait();
     extern __shared__ int32_t sh[];
     int32_t *running = sh;                 // [E] next destination of each expert
     int32_t *warp_cnt = sh + E;            // [kAlignWarps][E]
@@ -124,13 +160,14 @@ __global__ void __launch_bounds__(kAlignThreads)
     const int64_t start = static_cast<int64_t>(blockIdx.x) * chunk;
     const int64_t end = min(P, start + chunk);
     for (int e = threadIdx.x; e < E; e += blockDim.x)
-        running[e] = pad_offsets[e] + chunk_base[static_cast<int64_t>(blockIdx.x) * E + e];
+        running[e] = __ldcg(pad_offsets + e) +
+                     __ldcg(chunk_base + static_cast<int64_t>(blockIdx.x) * E + e);
     for (int i = threadIdx.x; i < kAlignWarps * E; i += blockDim.x) warp_cnt[i] = 0;
     __syncthreads();
     const uint32_t lanes_below = (1u << lane) - 1u;
     for (int64_t base = start; base < end; base += blockDim.x) {
         const int64_t p = base + threadIdx.x;
-        int e = p < end ? ids[p] : -1;
+        int e = p < end ? __ldcg(ids + p) : -1;
         const bool valid = e >= 0 && e < E;
         // lanes that are not real pairs get keys no real expert can match
         const uint32_t peers = __match_any_sync(0xffffffffu, valid ? e : E + lane);
@@ -155,18 +192,102 @@ __global__ void __launch_bounds__(kAlignThreads)
     }
 }
 
+// The whole grouping in one CTA (P <= kSmallPairs, E <= 256).
+__global__ void __launch_bounds__(kScanThreads)
+    align_small_kernel(const int32_t *__restrict__ ids, int64_t P, int E, int block_m,
+                       int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+                       int32_t *__restrict__ pad_offsets, int32_t *__restrict__ num_padded,
+                       int32_t *__restrict__ sorted_pair, int32_t *__restrict__ block_expert,
+                       int32_t *status) {
+    griddep_launch_dependents();
+    griddep_wait();
+    __shared__ int32_t hist[kSmallMaxE];
+    __shared__ int32_t pad_smem[kSmallMaxE + 1];
+    __shared__ int32_t running[kSmallMaxE];
+    __shared__ int32_t warp_cnt[kScanThreads / 32][kSmallMaxE];
+    __shared__ int32_t warp_sums[32];
+    __shared__ int32_t total, npad;
+    const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+    for (int i = threadIdx.x; i < kSmallMaxE; i += blockDim.x) hist[i] = 0;
+    for (int i = threadIdx.x; i < (kScanThreads / 32) * kSmallMaxE; i += blockDim.x)
+        (&warp_cnt[0][0])[i] = 0;
+    __syncthreads();
+    bool bad = false;
+    for (int64_t p = threadIdx.x; p < P; p += blockDim.x) {
+        const int e = __ldcg(ids + p);
+        if (e < 0 || e >= E) {
+            bad = true;
+            continue;
+        }
+        atomicAdd(&hist[e], 1);
+    }
+    if (bad) record_status(status, MOE_ERR_DEVICE_CHECK);
+    __syncthreads();
+    const int e = threadIdx.x;
+    const int32_t cnt = e < E ? hist[e] : 0;
+    const int32_t seg = (cnt + block_m - 1) / block_m * block_m;
+    const int32_t off = block_exclusive_scan(cnt, warp_sums, &total);
+    const int32_t pad = block_exclusive_scan(seg, warp_sums, &total);
+    if (e < E) {
+        counts[e] = cnt;
+        offsets[e] = off;
+        pad_offsets[e] = pad;
+        pad_smem[e] = pad;
+        running[e] = pad;
+        if (e == E - 1) {
+            offsets[E] = off + cnt;
+            pad_offsets[E] = pad + seg;
+            *num_padded = pad + seg;
+            npad = pad + seg;
+        }
+    }
+    __syncthreads();
+    fill_padded(pad_smem, E, block_m, npad, P, sorted_pair, block_expert);
+    __syncthreads();  // sentinels first, then the real pairs over them
+    const uint32_t lanes_below = (1u << lane) - 1u;
+    for (int64_t base = 0; base < P; base += blockDim.x) {
+        const int64_t p = base + threadIdx.x;
+        const int pe = p < P ? __ldcg(ids + p) : -1;
+        const bool valid = pe >= 0 && pe < E;
+        const uint32_t peers = __match_any_sync(0xffffffffu, valid ? pe : E + lane);
+        const int rank_in_warp = __popc(peers & lanes_below);
+        if (valid && rank_in_warp == 0) warp_cnt[warp][pe] = __popc(peers);
+        __syncthreads();
+        if (valid) {
+            int32_t before = 0;
+            for (int w = 0; w < warp; ++w) before += warp_cnt[w][pe];
+            sorted_pair[running[pe] + before + rank_in_warp] = static_cast<int32_t>(p);
+        }
+        __syncthreads();
+        if (threadIdx.x < E) {
+            int32_t tot = 0;
+            for (int w = 0; w < kScanThreads / 32; ++w) {
+                tot += warp_cnt[w][threadIdx.x];
+                warp_cnt[w][threadIdx.x] = 0;
+            }
+            running[threadIdx.x] += tot;
+        }
+        __syncthreads();
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_align(const AlignArgs &a, cudaStream_t s, int *launches) {
+    if (a.P <= kSmallPairs && a.E <= kSmallMaxE) {
+        *launches += 1;
+        return launch_pdl(align_small_kernel, dim3(1), dim3(kScanThreads), 0, s, 1, a.ids, a.P,
+                          a.E, a.block_m, a.counts, a.offsets, a.pad_offsets, a.num_padded,
+                          a.sorted_pair, a.block_expert, a.status);
+    }
     const size_t count_smem = sizeof(int32_t) * a.E;
-    align_count_kernel<<<a.nchunks, kAlignThreads, count_smem, s>>>(a.ids, a.P, a.E, a.chunk,
-                                                                     a.chunk_counts, a.status);
-    cudaError_t err = cudaGetLastError();
+    cudaError_t err = launch_pdl(align_count_kernel, dim3(a.nchunks), dim3(kAlignThreads),
+                                 count_smem, s, 1, a.ids, a.P, a.E, a.chunk, a.chunk_counts,
+                                 a.status);
     if (err != cudaSuccess) return err;
-    align_scan_kernel<<<1, kScanThreads, 0, s>>>(a.chunk_counts, a.nchunks, a.E, a.block_m,
-                                                 a.P, a.counts, a.offsets, a.pad_offsets,
-                                                 a.num_padded, a.block_expert, a.sorted_pair);
-    err = cudaGetLastError();
+    err = launch_pdl(align_scan_kernel, dim3(1), dim3(kScanThreads), 0, s, 1, a.chunk_counts,
+                     a.nchunks, a.E, a.block_m, a.P, a.counts, a.offsets, a.pad_offsets,
+                     a.num_padded, a.block_expert, a.sorted_pair);
     if (err != cudaSuccess) return err;
     const size_t scatter_smem = sizeof(int32_t) * (a.E + kAlignWarps * a.E);
     if (scatter_smem > 48 * 1024) {
@@ -175,10 +296,11 @@ cudaError_t launch_align(const AlignArgs &a, cudaStream_t s, int *launches) {
                                    static_cast<int>(scatter_smem));
         if (err != cudaSuccess) return err;
     }
-    align_scatter_kernel<<<a.nchunks, kAlignThreads, scatter_smem, s>>>(
-        a.ids, a.P, a.E, a.chunk, a.chunk_counts, a.pad_offsets, a.sorted_pair);
     *launches += 3;
-    return cudaGetLastError();
+    return launch_pdl(align_scatter_kernel, dim3(a.nchunks), dim3(kAlignThreads), scatter_smem,
+                      s, 1, a.ids, a.P, a.E, a.chunk,
+                      static_cast<const int32_t *>(a.chunk_counts),
+                      static_cast<const int32_t *>(a.pad_offsets), a.sorted_pair);
 }
 
 }  // namespace moe

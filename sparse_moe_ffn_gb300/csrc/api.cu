@@ -137,7 +137,8 @@ moe_status_t check_route_args(const void *x, const void *router, const void *sha
 moe_status_t enqueue_route(const moe_bf16_t *x, const moe_bf16_t *router,
                            const moe_bf16_t *shared_gate, int64_t N, int H, int E, int k,
                            int norm, float *topk_w, int32_t *topk_ids, moe_bf16_t *topk_w_bf16,
-                           float *gamma, int32_t *status, cudaStream_t stream) {
+                           float *gamma, int32_t *status, bool reset_status,
+                           cudaStream_t stream) {
     const bool shared = shared_gate != nullptr;
     RouterArgs ra;
     ra.N = N;
@@ -147,6 +148,8 @@ moe_status_t enqueue_route(const moe_bf16_t *x, const moe_bf16_t *router,
     ra.norm = norm ? 1 : 0;
     ra.e_pad = router_e_pad(E, shared);
     ra.gamma_col = shared ? (E + 7) / 8 * 8 : -1;
+    ra.split = router_split(H);
+    ra.reset_status = reset_status ? 1 : 0;
     ra.topk_w = topk_w;
     ra.topk_ids = topk_ids;
     ra.topk_w_bf16 = topk_w_bf16;
@@ -281,7 +284,7 @@ moe_status_t moe_route(const moe_bf16_t *x, const moe_bf16_t *router,
     int32_t *status = static_cast<int32_t *>(workspace);
     if (status) MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int32_t), stream), "status reset");
     return enqueue_route(x, router, shared_gate, N, H, E, k, norm_topk_prob, topk_w, topk_ids,
-                         topk_w_bf16, shared_gamma, status, stream);
+                         topk_w_bf16, shared_gamma, status, false, stream);
 }
 
 int64_t moe_align_capacity(int64_t N, int k, int E, int block_m) {
@@ -397,12 +400,11 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
     const int64_t cap = L.capacity;
     const int sms = num_sms_of_current_device();
 
-    MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int32_t), stream), "status reset");
-
-    // K1: routing
+    // K1: routing (its first CTA also clears the status word, so that no
+    // memset node breaks the chain of programmatically serialized launches)
     if ((st = record_stage(MOE_STAGE_ROUTE, stream)) != MOE_OK) return st;
     st = enqueue_route(x, router, shared ? shared_gate : nullptr, N, H, E, k, norm_topk_prob,
-                       topk_w, topk_ids, nullptr, gamma, status, stream);
+                       topk_w, topk_ids, nullptr, gamma, status, true, stream);
     if (st != MOE_OK) return st;
 
     // K2: grouping

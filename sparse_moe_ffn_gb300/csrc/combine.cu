@@ -33,6 +33,8 @@ __device__ __forceinline__ void add_f16x8(float (&acc)[8], const uint4 &v) {
 __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(const uint16_t *__restrict__ ypair, const uint16_t *__restrict__ yshared,
                    int64_t N, int H, int k, uint16_t *__restrict__ out) {
+    griddep_launch_dependents();
+    griddep_wait();
     const int groups = H / 8;
     const int64_t total = N * groups;
     for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
@@ -42,9 +44,9 @@ __global__ void __launch_bounds__(kCombineThreads)
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         const uint16_t *src = ypair + n * k * static_cast<int64_t>(H) + col;
         for (int j = 0; j < k; ++j)
-            add_f16x8(acc, *reinterpret_cast<const uint4 *>(src + static_cast<int64_t>(j) * H));
+            add_f16x8(acc, __ldcg(reinterpret_cast<const uint4 *>(src + static_cast<int64_t>(j) * H)));
         if (yshared)
-            add_f16x8(acc, *reinterpret_cast<const uint4 *>(yshared + n * H + col));
+            add_f16x8(acc, __ldcg(reinterpret_cast<const uint4 *>(yshared + n * H + col)));
         uint4 pk;
         pk.x = pack_bf16x2(acc[0], acc[1]);
         pk.y = pack_bf16x2(acc[2], acc[3]);
@@ -62,9 +64,8 @@ cudaError_t launch_combine(const uint16_t *ypair, const uint16_t *yshared, int64
     int64_t blocks = (total + kCombineThreads - 1) / kCombineThreads;
     const int64_t cap = static_cast<int64_t>(num_sms) * 16;
     if (blocks > cap) blocks = cap;
-    combine_kernel<<<static_cast<unsigned>(blocks), kCombineThreads, 0, s>>>(ypair, yshared, N,
-                                                                           H, k, out);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kCombineThreads),
+                      0, s, 1, ypair, yshared, N, H, k, out);
 }
 
 }  // namespace moe

@@ -142,8 +142,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem = sm->tmem_base;
     volatile int *abort_flag = &sm->abort_flag;
+    griddep_launch_dependents();
+    griddep_wait();  // the block list and A rows come from earlier kernels
 
-    const int64_t rows = a.num_padded ? static_cast<int64_t>(*a.num_padded) : a.num_rows_host;
+    const int64_t rows = a.num_padded ? static_cast<int64_t>(__ldcg(a.num_padded)) : a.num_rows_host;
     const int num_blocks = static_cast<int>((rows + kBlockM - 1) / kBlockM);
     const int n_tiles = (a.n_out + BN - 1) / BN;
     const int total_tiles = min(num_blocks * n_tiles, a.max_tiles);
@@ -156,12 +158,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int tile = blockIdx.x; tile < total_tiles && !failed; tile += gridDim.x) {
             const int blk = tile / n_tiles;
             const int nt = tile % n_tiles;
-            const int expert = a.block_expert ? a.block_expert[blk] : 0;
+            const int expert = a.block_expert ? __ldcg(a.block_expert + blk) : 0;
             // dense: the block has more than kSparseRows real rows (real rows
             // come first in a block, so looking at row kSparseRows suffices)
             bool dense = true;
             if (a.sorted_pair) {
-                const int64_t probe = a.sorted_pair[static_cast<int64_t>(blk) * kBlockM + kSparseRows];
+                const int64_t probe =
+                    __ldcg(a.sorted_pair + static_cast<int64_t>(blk) * kBlockM + kSparseRows);
                 dense = probe >= 0 && probe < a.q_limit;
             }
             // sparse: rows 4*lane .. 4*lane+3 of this block
@@ -172,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int64_t row = static_cast<int64_t>(blk) * kBlockM + lane * 4 + i;
-                    const int64_t q = a.sorted_pair[row];
+                    const int64_t q = __ldcg(a.sorted_pair + row);
                     const bool v = q >= 0 && q < a.q_limit;
                     src[i] = !v ? -1 : (MODE == kGateUp ? static_cast<int>(q / a.k_div)
                                                         : static_cast<int>(row));
@@ -303,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int blk = tile / n_tiles;
             const int nt = tile % n_tiles;
             const int64_t grow = static_cast<int64_t>(blk) * kBlockM + row;
-            const int64_t q = a.sorted_pair ? a.sorted_pair[grow] : grow;
+            const int64_t q = a.sorted_pair ? __ldcg(a.sorted_pair + grow) : grow;
             const bool valid = q >= 0 && q < a.q_limit;
             const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kAccCols;
             const int col0 = nt * BN;
@@ -338,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             } else {
-                const float w = valid ? a.scale[q] : 0.f;
+                const float w = valid ? __ldcg(a.scale + q) : 0.f;
                 uint16_t *dst = a.out + (valid ? q : 0) * a.out_ld + col0;
                 float vmax = 0.f;
 #pragma unroll 1
@@ -393,17 +396,19 @@ __global__ void __launch_bounds__(256)
                        const int32_t *__restrict__ sorted_pair,
                        const int32_t *__restrict__ num_padded, int64_t P, int64_t cap,
                        uint16_t *__restrict__ x_sorted) {
+    griddep_launch_dependents();
+    griddep_wait();
     const int lane = threadIdx.x % 32;
-    const int64_t rows = min(static_cast<int64_t>(*num_padded), cap);
+    const int64_t rows = min(static_cast<int64_t>(__ldcg(num_padded)), cap);
     for (int64_t s = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32; s < rows;
          s += static_cast<int64_t>(gridDim.x) * blockDim.x / 32) {
-        const int64_t probe = sorted_pair[s / kBlockM * kBlockM + kSparseRows];
+        const int64_t probe = __ldcg(sorted_pair + s / kBlockM * kBlockM + kSparseRows);
         if (probe < 0 || probe >= P) continue;  // sparse block: its rows are gathered by TMA
-        const int64_t q = sorted_pair[s];
+        const int64_t q = __ldcg(sorted_pair + s);
         if (q < 0 || q >= P) continue;          // padding row
         const uint4 *src = reinterpret_cast<const uint4 *>(x + (q / k) * H);
         uint4 *dst = reinterpret_cast<uint4 *>(x_sorted + s * H);
-        for (int c = lane; c < H / 8; c += 32) dst[c] = src[c];
+        for (int c = lane; c < H / 8; c += 32) dst[c] = __ldcg(src + c);
     }
 }
 
@@ -415,9 +420,8 @@ cudaError_t launch_gather_rows(const uint16_t *x, int H, int k, const int32_t *s
     int64_t blocks = (cap * 32 + 255) / 256;
     const int64_t limit = static_cast<int64_t>(num_sms) * 8;
     if (blocks > limit) blocks = limit;
-    gather_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(x, H, k, sorted_pair,
-                                                                    num_padded, P, cap, x_sorted);
-    return cudaGetLastError();
+    return launch_pdl(gather_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, 1,
+                      x, H, k, sorted_pair, num_padded, P, cap, x_sorted);
 }
 
 int gemm_block_n(GemmMode mode) { return mode == kGateUp ? Cfg<kGateUp>::BN : Cfg<kDown>::BN; }
@@ -438,8 +442,8 @@ cudaError_t launch_gemm(GemmMode mode, const CUtensorMap &tm_a, const CUtensorMa
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    kern<<<a.grid, kThreads, smem, s>>>(tm_a, tm_a_lo, tm_a_box, tm_a_lo_box, tm_b0, tm_b1, a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(a.grid), dim3(kThreads), smem, s, 1, tm_a, tm_a_lo, tm_a_box,
+                      tm_a_lo_box, tm_b0, tm_b1, a);
 }
 
 }  // namespace moe

@@ -6,9 +6,39 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "moe.h"
 
 namespace moe {
+
+// Launches `kernel` with programmatic stream serialization (the kernel may be
+// scheduled while its predecessor finishes; it calls griddep_wait before
+// touching memory) and, when cluster_x > 1, as clusters of cluster_x CTAs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, unsigned cluster_x, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (cluster_x > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster_x;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 constexpr int kBlockM = MOE_BLOCK_M;  // GEMM row block (tokens / pairs per tile)
 constexpr int kBlockK = 64;           // 64 bf16 = one 128-byte swizzle row
@@ -20,6 +50,8 @@ struct RouterArgs {
     int H, E, k, norm;
     int e_pad;      // MMA N: columns of the logits tile (multiple of 16, <= 256)
     int gamma_col;  // column holding x . g, or -1 without a shared gate
+    int split;      // CTAs per cluster along H (router_split(H))
+    int reset_status;  // CTA 0 clears *status first (the layer's first kernel)
     float *topk_w;
     int32_t *topk_ids;
     uint16_t *topk_w_bf16;
@@ -27,7 +59,8 @@ struct RouterArgs {
     int32_t *status;
 };
 
-size_t router_smem_bytes(int e_pad);
+int router_split(int H);  // 1, 2, 4 or 8: depends on H only (batch invariance)
+size_t router_smem_bytes(int e_pad, int k);
 cudaError_t launch_router(const CUtensorMap &tm_x, const CUtensorMap &tm_router,
                           const CUtensorMap &tm_gate, const RouterArgs &a, cudaStream_t s);
 

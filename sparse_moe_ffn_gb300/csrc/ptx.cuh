@@ -205,6 +205,25 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
            | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
+// ------------------------------------------- programmatic dependent launch
+
+// Blocks until the grids this one depends on have completed and their memory
+// is visible; a no-op for launches without programmatic serialization.
+// Because a dependent grid can be resident before its predecessor finishes,
+// every kernel here reads data written by an earlier kernel of the chain
+// either through TMA or with ld.global.cg (__ldcg), never through the
+// non-coherent / L1 path: without that, a second layer call in a process was
+// seen to read stale row indices after this wait.
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next kernel in the stream be scheduled (it still waits in
+// griddep_wait for this grid to finish before touching memory).
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------ misc helpers
 
 __device__ __forceinline__ void record_status(int32_t *status, int32_t code) {

@@ -7,14 +7,18 @@
 // (the pages return them in x's dtype) and ids as int32.  The shared gate is
 // sigmoid(x . g), one scalar per token (same page, shared-expert line).
 //
-// One CTA owns 128 tokens.  The logits tile [128 x e_pad] is one tcgen05 MMA
-// chain: x rows are the A operand (M = 128 tokens), router rows are B (N =
-// e_pad experts, plus g in column gamma_col), K = H streamed through a 4-stage
-// TMA pipeline in 64-wide slices.  The fp32 accumulator sits in TMEM with
-// token r in lane r, so the epilogue thread of lane r owns its whole logit
-// row: max, sum of exponentials and the k arg-max rounds need no cross-thread
-// reduction at all.  The reduction order over H is the same for every token
-// and every N, which makes routing batch invariant bit for bit.
+// A cluster of `split` CTAs (1, 2, 4 or 8, chosen from H alone) owns 128
+// tokens; CTA c of the cluster takes the c-th slice of H.  Each CTA streams x
+// [128 x 64] and router [e_pad x 64] slices through a TMA ring into one
+// tcgen05 MMA chain (M = 128 tokens, N = e_pad experts, plus g in column
+// gamma_col), so its TMEM holds the partial logits of its H slice.  The
+// partial tile is copied to the CTA's own shared memory; after a cluster
+// barrier, CTA c reduces token rows [16c, 16c + 16) (in 16-row passes when
+// split < 8), 8 lanes per row and 4 rows per warp: the `split` partial rows
+// are read through distributed shared memory in rank order with coalesced
+// 16-byte loads, and the 8 lanes run the softmax, the k arg-max rounds and the
+// renormalisation with shuffle reductions.  Every reduction order depends
+// on H and E only, never on N: routing is batch invariant bit for bit.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -28,6 +32,9 @@ namespace {
 constexpr int kRouterStages = 4;
 constexpr int kRouterThreads = 128;
 constexpr int kATileBytes = kBlockM * 128;  // 128 tokens x 64 bf16
+constexpr int kLanesPerRow = 8;                           // lanes sharing one token row
+constexpr int kRowsPerPass = kRouterThreads / kLanesPerRow;  // 16 rows per pass
+constexpr int kMaxPerLane = MOE_MAX_EXPERTS / kLanesPerRow;  // 32 logits per lane
 
 struct RouterSmem {
     uint64_t full[kRouterStages];
@@ -42,6 +49,43 @@ __device__ __forceinline__ float finite_or_neg_inf(float v) {
     return (v != v) ? -INFINITY : v;  // NaN never wins a comparison
 }
 
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Shared-memory address of `local` in cluster CTA `rank`.  The loads below
+// are volatile (so they stay after the cluster barrier) but carry no memory
+// clobber, so that many of them are in flight at once.
+__device__ __forceinline__ uint32_t dsmem_addr(const void *local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
+    return remote;
+}
+
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+// the larger of two (logit, expert) keys: larger logit, then lower expert;
+// an expert of -1 means "none"
+__device__ __forceinline__ void key_max(float &v, int &e, float ov, int oe) {
+    if (oe >= 0 && (e < 0 || ov > v || (ov == v && oe < e))) {
+        v = ov;
+        e = oe;
+    }
+}
+
 __global__ void __launch_bounds__(kRouterThreads, 1)
     router_kernel(const __grid_constant__ CUtensorMap tm_x,
                   const __grid_constant__ CUtensorMap tm_router,
@@ -51,12 +95,21 @@ __global__ void __launch_bounds__(kRouterThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int b_tile_bytes = a.e_pad * 128;
     const int stage_bytes = kATileBytes + b_tile_bytes;
-    RouterSmem *sm = reinterpret_cast<RouterSmem *>(tiles + kRouterStages * stage_bytes);
+    const int ring_bytes = kRouterStages * stage_bytes;
+    const int part_bytes = kBlockM * (a.e_pad + 4) * 4 + kRowsPerPass * a.k * 8;
+    RouterSmem *sm = reinterpret_cast<RouterSmem *>(
+        tiles + (ring_bytes > part_bytes ? ring_bytes : part_bytes));
+    float *partial = reinterpret_cast<float *>(tiles);  // reuses the ring once it is idle
+    const int ld = a.e_pad + 4;                          // row stride of the partial tile
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kBlockM;
+    const uint32_t crank = cluster_rank();
+    const int64_t n0 = static_cast<int64_t>(blockIdx.y) * kBlockM;
     const int nk = (a.H + kBlockK - 1) / kBlockK;
+    const int kc0 = static_cast<int>(crank) * nk / a.split;
+    const int kc1 = static_cast<int>(crank + 1) * nk / a.split;
+    const int my_nk = kc1 - kc0;  // >= 1 because split <= nk
     const uint32_t tmem_cols = a.e_pad <= 32 ? 32 : (a.e_pad <= 64 ? 64 : (a.e_pad <= 128 ? 128 : 256));
 
     if (threadIdx.x == 0) {
@@ -81,40 +134,44 @@ __global__ void __launch_bounds__(kRouterThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem = sm->tmem_base;
     volatile int *abort_flag = &sm->abort_flag;
+    griddep_launch_dependents();
+    griddep_wait();  // x may come from the previous kernel in the stream
+    if (a.reset_status && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0 && a.status)
+        *a.status = 0;
 
     if (warp == 0) {
-        // ---------------- TMA producer
+        // ---------------- TMA producer: this CTA's slice of H
         if (lane == 0) {
             const uint32_t tx = kATileBytes + a.E * 128 + (a.gamma_col >= 0 ? 8 * 128 : 0);
-            int kc = 0;
-            for (; kc < nk; ++kc) {
-                const int s = kc % kRouterStages;
-                const uint32_t use = kc / kRouterStages;
+            int i = 0;
+            for (; i < my_nk; ++i) {
+                const int s = i % kRouterStages;
+                const uint32_t use = i / kRouterStages;
                 if (use > 0 && !mbar_wait(&sm->empty[s], (use - 1) & 1, abort_flag)) {
                     record_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
                     *abort_flag = 1;
                     break;
                 }
                 uint8_t *st = tiles + s * stage_bytes;
+                const int kcol = (kc0 + i) * kBlockK;
                 mbar_arrive_expect_tx(&sm->full[s], tx);
-                tma_load_2d(st, &tm_x, &sm->full[s], kc * kBlockK, static_cast<int>(n0));
-                tma_load_2d(st + kATileBytes, &tm_router, &sm->full[s], kc * kBlockK, 0);
+                tma_load_2d(st, &tm_x, &sm->full[s], kcol, static_cast<int>(n0));
+                tma_load_2d(st + kATileBytes, &tm_router, &sm->full[s], kcol, 0);
                 if (a.gamma_col >= 0)
                     tma_load_2d(st + kATileBytes + a.gamma_col * 128, &tm_gate, &sm->full[s],
-                                kc * kBlockK, 0);
+                                kcol, 0);
             }
-            // drain: wait for the last load issued to every stage
-            for (int i = (kc > kRouterStages ? kc - kRouterStages : 0); i < kc; ++i)
-                mbar_wait(&sm->full[i % kRouterStages], (i / kRouterStages) & 1, abort_flag);
+            for (int j = (i > kRouterStages ? i - kRouterStages : 0); j < i; ++j)
+                mbar_wait(&sm->full[j % kRouterStages], (j / kRouterStages) & 1, abort_flag);
         }
         __syncwarp();
     } else if (warp == 1) {
         // ---------------- MMA issuer
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16_f32(kBlockM, a.e_pad);
-            for (int kc = 0; kc < nk; ++kc) {
-                const int s = kc % kRouterStages;
-                if (!mbar_wait(&sm->full[s], (kc / kRouterStages) & 1, abort_flag)) {
+            for (int i = 0; i < my_nk; ++i) {
+                const int s = i % kRouterStages;
+                if (!mbar_wait(&sm->full[s], (i / kRouterStages) & 1, abort_flag)) {
                     record_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
                     *abort_flag = 1;
                     break;
@@ -125,7 +182,7 @@ __global__ void __launch_bounds__(kRouterThreads, 1)
                 const uint64_t db = sw128_kmajor_desc(smem_addr(st + kATileBytes));
 #pragma unroll
                 for (int kk = 0; kk < kBlockK / 16; ++kk)
-                    mma_bf16(tmem, da + 2 * kk, db + 2 * kk, idesc, (kc | kk) != 0);
+                    mma_bf16(tmem, da + 2 * kk, db + 2 * kk, idesc, (i | kk) != 0);
                 mma_commit(&sm->empty[s]);
             }
             mma_commit(&sm->acc_full);
@@ -135,92 +192,137 @@ __global__ void __launch_bounds__(kRouterThreads, 1)
         __syncwarp();
     }
 
-    // ---------------- epilogue: every thread owns one token row (TMEM lane)
+    // ---------------- phase 1: partial logits TMEM -> own shared memory
     const bool ok = mbar_wait(&sm->acc_full, 0, abort_flag);
     __syncwarp();
     if (!ok) {
         record_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
         *abort_flag = 1;
-    } else {
-        tc_fence_after_sync();
-        const int row = warp * 32 + lane;
-        const int64_t n = n0 + row;
-        const bool live = n < a.N;
+    }
+    tc_fence_after_sync();
+    __syncthreads();  // every stage is consumed: the ring may be overwritten
+    {
+        const int row = warp * 32 + lane;  // TMEM lane
         const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        const int nchunk = (a.E + 31) / 32;
-
-        float mx = -INFINITY;
-        for (int c = 0; c < nchunk; ++c) {
+        for (int c = 0; c < (a.e_pad + 31) / 32; ++c) {
             float v[32];
             tmem_load32(trow + c * 32, v);
             tmem_load_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-                if (c * 32 + i < a.E) mx = fmaxf(mx, finite_or_neg_inf(v[i]));
-        }
-        float den = 0.f;
-        for (int c = 0; c < nchunk; ++c) {
-            float v[32];
-            tmem_load32(trow + c * 32, v);
-            tmem_load_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                if (c * 32 + i < a.E) den += expf(finite_or_neg_inf(v[i]) - mx);
-        }
-        // top-k: round j takes the largest (logit, lower index first) key that
-        // comes strictly after the key taken in round j-1.  exp is monotone,
-        // so this is the top-k of the probabilities.
-        float prev_v = INFINITY;
-        int prev_i = -1;
-        float wsum = 0.f;
-        float *w_row = a.topk_w + n * a.k;
-        int32_t *id_row = a.topk_ids + n * a.k;
-        for (int j = 0; j < a.k; ++j) {
-            float best_v = -INFINITY;
-            int best_i = -1;
-            for (int c = 0; c < nchunk; ++c) {
-                float v[32];
-                tmem_load32(trow + c * 32, v);
-                tmem_load_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int e = c * 32 + i;
-                    const float x = finite_or_neg_inf(v[i]);
-                    const bool after_prev = (x < prev_v) || (x == prev_v && e > prev_i);
-                    if (e < a.E && after_prev && (best_i < 0 || x > best_v)) {
-                        best_v = x;
-                        best_i = e;
-                    }
-                }
-            }
-            const float p = expf(best_v - mx) / den;
-            wsum += p;
-            if (live) {
-                w_row[j] = p;
-                id_row[j] = best_i;
-            }
-            prev_v = best_v;
-            prev_i = best_i;
-        }
-        if (live) {
-            const float inv = a.norm ? 1.f / wsum : 1.f;
-            for (int j = 0; j < a.k; ++j) {
-                const float w = a.norm ? w_row[j] * inv : w_row[j];
-                if (a.norm) w_row[j] = w;
-                if (a.topk_w_bf16) {
-                    __nv_bfloat16 h = __float2bfloat16_rn(w);
-                    a.topk_w_bf16[n * a.k + j] = *reinterpret_cast<uint16_t *>(&h);
-                }
-            }
-        }
-        if (a.gamma_col >= 0) {
-            const float lg = tmem_load1(trow + a.gamma_col);
-            tmem_load_wait();
-            if (live) a.gamma[n] = 1.f / (1.f + expf(-lg));
+            for (int i = 0; i < 32; i += 4)
+                if (c * 32 + i < a.e_pad)
+                    *reinterpret_cast<float4 *>(&partial[row * ld + c * 32 + i]) =
+                        ok ? make_float4(v[i], v[i + 1], v[i + 2], v[i + 3])
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
     tc_fence_before_sync();
-    __syncthreads();
+    cluster_sync();  // all partial tiles of the cluster are in place
+
+    // ---------------- phase 2: reduce over the cluster, then route
+    // 8 lanes per token row, 4 rows per warp, 16 rows per pass.  Lane `sub`
+    // owns the float4 column groups 32i + 4*sub (i < e_pad/32), so each 8-lane
+    // group reads 128 contiguous bytes of a partial row per load.  The
+    // `split` partials are summed in rank order.
+    const int sub = lane % kLanesPerRow;
+    const int rows_per_cta = kBlockM / a.split;
+    const int groups = (a.e_pad + 31) / 32;
+    float *slot_w = partial + kBlockM * ld;                              // [16][k]
+    int32_t *slot_e = reinterpret_cast<int32_t *>(slot_w + kRowsPerPass * a.k);  // [16][k]
+    for (int base = 0; base < rows_per_cta; base += kRowsPerPass) {
+        const int rl = warp * (32 / kLanesPerRow) + lane / kLanesPerRow;  // row in pass
+        const int row = static_cast<int>(crank) * rows_per_cta + base + rl;
+        const int64_t n = n0 + row;
+        const bool live = n < a.N;
+        float lg[kMaxPerLane];
+#pragma unroll
+        for (int j = 0; j < kMaxPerLane; ++j) lg[j] = 0.f;
+        for (int r = 0; r < a.split; ++r) {
+            const uint32_t src = dsmem_addr(&partial[row * ld + 4 * sub], static_cast<uint32_t>(r));
+            float4 t[kMaxPerLane / 4];
+#pragma unroll
+            for (int i = 0; i < kMaxPerLane / 4; ++i)
+                if (i < groups && 32 * i + 4 * sub < a.e_pad) t[i] = ld_dsmem_f4(src + 128 * i);
+#pragma unroll
+            for (int i = 0; i < kMaxPerLane / 4; ++i)
+                if (i < groups && 32 * i + 4 * sub < a.e_pad) {
+                    lg[4 * i + 0] += t[i].x;
+                    lg[4 * i + 1] += t[i].y;
+                    lg[4 * i + 2] += t[i].z;
+                    lg[4 * i + 3] += t[i].w;
+                }
+        }
+        // the shared gate logit lives in one lane's columns
+        if (a.gamma_col >= 0 && live && (a.gamma_col % 32) / 4 == sub) {
+            const int jg = 4 * (a.gamma_col / 32) + a.gamma_col % 4;
+            float lgate = 0.f;
+#pragma unroll
+            for (int j = 0; j < kMaxPerLane; ++j)
+                if (j == jg) lgate = lg[j];
+            a.gamma[n] = 1.f / (1.f + expf(-lgate));
+        }
+#pragma unroll
+        for (int j = 0; j < kMaxPerLane; ++j) {
+            const int e = 32 * (j / 4) + 4 * sub + j % 4;
+            lg[j] = e < a.E ? finite_or_neg_inf(lg[j]) : -INFINITY;
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < kMaxPerLane; ++j) mx = fmaxf(mx, lg[j]);
+#pragma unroll
+        for (int d = kLanesPerRow / 2; d > 0; d >>= 1)
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d, kLanesPerRow));
+        float den = 0.f;
+#pragma unroll
+        for (int j = 0; j < kMaxPerLane; ++j) {
+            const int e = 32 * (j / 4) + 4 * sub + j % 4;
+            if (e < a.E) den += expf(lg[j] - mx);
+        }
+#pragma unroll
+        for (int d = kLanesPerRow / 2; d > 0; d >>= 1)
+            den += __shfl_xor_sync(0xffffffffu, den, d, kLanesPerRow);
+        // k arg-max rounds; exp is monotone, so this is the top-k of the
+        // probabilities
+        uint32_t taken = 0;
+        float wsum = 0.f;
+        for (int r = 0; r < a.k; ++r) {
+            float bv = -INFINITY;
+            int be = -1;
+#pragma unroll
+            for (int j = 0; j < kMaxPerLane; ++j) {
+                const int e = 32 * (j / 4) + 4 * sub + j % 4;
+                if (e < a.E && !((taken >> j) & 1u)) key_max(bv, be, lg[j], e);
+            }
+#pragma unroll
+            for (int d = kLanesPerRow / 2; d > 0; d >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, d, kLanesPerRow);
+                const int oe = __shfl_xor_sync(0xffffffffu, be, d, kLanesPerRow);
+                key_max(bv, be, ov, oe);
+            }
+            if ((be % 32) / 4 == sub) taken |= 1u << (4 * (be / 32) + be % 4);
+            const float p = expf(bv - mx) / den;
+            wsum += p;
+            if (sub == 0) {
+                slot_w[rl * a.k + r] = p;
+                slot_e[rl * a.k + r] = be;
+            }
+        }
+        __syncwarp();
+        if (live) {
+            const float inv = a.norm ? 1.f / wsum : 1.f;
+            for (int r = sub; r < a.k; r += kLanesPerRow) {
+                const float w = slot_w[rl * a.k + r] * inv;
+                a.topk_w[n * a.k + r] = w;
+                a.topk_ids[n * a.k + r] = slot_e[rl * a.k + r];
+                if (a.topk_w_bf16) {
+                    __nv_bfloat16 h = __float2bfloat16_rn(w);
+                    a.topk_w_bf16[n * a.k + r] = *reinterpret_cast<uint16_t *>(&h);
+                }
+            }
+        }
+        __syncwarp();
+    }
+    cluster_sync();  // no CTA leaves while a peer may still read its partial tile
     if (warp == 0) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, tmem_cols);
@@ -229,21 +331,30 @@ __global__ void __launch_bounds__(kRouterThreads, 1)
 
 }  // namespace
 
-size_t router_smem_bytes(int e_pad) {
-    return 1024 + static_cast<size_t>(kRouterStages) * (kATileBytes + e_pad * 128) +
-           sizeof(RouterSmem);
+int router_split(int H) {
+    const int nk = (H + kBlockK - 1) / kBlockK;
+    return nk >= 8 ? 8 : (nk >= 4 ? 4 : (nk >= 2 ? 2 : 1));
+}
+
+size_t router_smem_bytes(int e_pad, int k) {
+    const size_t ring = static_cast<size_t>(kRouterStages) * (kATileBytes + e_pad * 128);
+    // the partial tile, then the slot results of one 16-row pass
+    const size_t part = static_cast<size_t>(kBlockM) * (e_pad + 4) * sizeof(float) +
+                        static_cast<size_t>(kRowsPerPass) * k * 8;
+    return 1024 + (ring > part ? ring : part) + sizeof(RouterSmem);
 }
 
 cudaError_t launch_router(const CUtensorMap &tm_x, const CUtensorMap &tm_router,
                           const CUtensorMap &tm_gate, const RouterArgs &a, cudaStream_t s) {
-    const size_t smem = router_smem_bytes(a.e_pad);
+    const size_t smem = router_smem_bytes(a.e_pad, a.k);
     cudaError_t err = cudaFuncSetAttribute(router_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    const unsigned grid = static_cast<unsigned>((a.N + kBlockM - 1) / kBlockM);
-    router_kernel<<<grid, kRouterThreads, smem, s>>>(tm_x, tm_router, tm_gate, a);
-    return cudaGetLastError();
+    const dim3 grid(static_cast<unsigned>(a.split),
+                    static_cast<unsigned>((a.N + kBlockM - 1) / kBlockM), 1);
+    return launch_pdl(router_kernel, grid, dim3(kRouterThreads), smem, s,
+                      static_cast<unsigned>(a.split), tm_x, tm_router, tm_gate, a);
 }
 
 }  // namespace moe

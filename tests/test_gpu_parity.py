@@ -184,6 +184,28 @@ def test_repeatable_and_status_clean():
     assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("name", ["talker", "skewed", "prefill"])
+def test_repeated_calls_with_fresh_workspaces(name):
+    """Back-to-back layer calls (kernels chained by programmatic dependent
+    launch), each with a newly allocated workspace, give bit-identical
+    outputs: no kernel reads a stale copy of its predecessor's results."""
+    shape, dev, _ = prepared(name)
+    first, _ = run_forward(shape, dev)
+    for _ in range(3):
+        again, _ = run_forward(shape, dev)
+        assert torch.equal(first, again)
+    # and calls queued without a synchronisation in between
+    outs = []
+    for _ in range(3):
+        ws = binding.alloc_workspace(shape.N, shape.H, shape.E, shape.I, shape.k, shape.I_s)
+        outs.append(binding.moe_forward(dev["x"], dev["router"], dev["w_gate"], dev["w_up"],
+                                        dev["w_down"], shape.k, shape.norm_topk_prob,
+                                        shared_of(shape, dev), workspace=ws))
+    torch.cuda.synchronize()
+    for o in outs:
+        assert torch.equal(first, o)
+
+
 def test_zero_tokens_is_a_noop():
     shape, dev, _ = prepared("tiny")
     x = dev["x"][:0]
