@@ -131,6 +131,35 @@ moe_status_t moe_align(const int32_t *topk_ids, int64_t N, int k, int E,
                        cudaStream_t stream);
 
 /* -------------------------------------------------------------------------
+ * moe_align_noalloc -- moe_align without a caller-provided workspace, for
+ * callers that cannot allocate device memory (no counterpart on the pages:
+ * it exists for integration, not for the method).  Code being captured into
+ * a CUDA graph may not call cudaMalloc, plugin-style hosts give a kernel
+ * only its input and output buffers, and latency-critical paths must avoid an
+ * allocator's locks and implicit synchronisation; such callers pass only
+ * topk_ids and the outputs of moe_align.
+ *
+ * The scratch lives in a static device array of
+ * MOE_ALIGN_NOALLOC_SCRATCH_BYTES (1 MiB) that every GPU loading the library
+ * holds until exit.  Sizes whose moe_align_workspace_bytes(N, k, E, block_m)
+ * exceed it return MOE_ERR_UNSUPPORTED (for E = 128 that is above ~4M pairs).
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current): make that first call
+ * before any stream capture.  Every call shares the array, so calls whose
+ * work overlaps on the GPU (other streams, other host threads) race; the
+ * array needs no clearing between calls.  device_status (nullable, int32 on
+ * the device) receives the call's status word (MOE_ERR_DEVICE_CHECK for an
+ * id outside [0, E)) by an asynchronous copy on `stream`.
+ * Arguments and outputs are those of moe_align.  Allocates nothing.
+ * ---------------------------------------------------------------------- */
+#define MOE_ALIGN_NOALLOC_SCRATCH_BYTES (1u << 20)
+moe_status_t moe_align_noalloc(const int32_t *topk_ids, int64_t N, int k, int E,
+                               int block_m, int32_t *sorted_pair,
+                               int32_t *block_expert, int32_t *counts,
+                               int32_t *offsets, int32_t *num_padded,
+                               int32_t *device_status, cudaStream_t stream);
+
+/* -------------------------------------------------------------------------
  * moe_forward -- the whole layer (M03 problem overview and its "serving way";
  * the shared expert of the same page and of the talker MoE block in the
  * vLLM Qwen3.5 walkthrough, section "2.5B Sparse MoE").

@@ -60,6 +60,7 @@ def lib():
         "moe_kernel_launch_count": ([], ctypes.c_uint64),
         "moe_set_stage_events": ([P, i32], i32),
         "moe_selftest_wait_timeout": ([P, sz, ctypes.c_uint64, P], i32),
+        "moe_align_noalloc": ([P, i64, i32, i32, i32, P, P, P, P, P, P, P], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -148,6 +149,29 @@ def moe_align(topk_ids, E: int, block_m: int = MOE_BLOCK_M):
                        _ptr(offsets), _ptr(npad), _ptr(ws), wsb, _stream()), "moe_align")
     return {"sorted_pair": sp, "block_expert": be, "counts": counts, "offsets": offsets,
             "num_padded": npad, "capacity": cap, "workspace": ws}
+
+
+def moe_align_noalloc(topk_ids, E: int, block_m: int = MOE_BLOCK_M):
+    """moe_align for callers that cannot allocate scratch (see moe.h): the
+    library's static device array serves as the workspace.  Returns the same
+    dict as moe_align, with "status" (int32 [1]) in place of "workspace"."""
+    if topk_ids.dtype != torch.int32 or not topk_ids.is_cuda or not topk_ids.is_contiguous():
+        raise ValueError("topk_ids must be a contiguous int32 CUDA tensor")
+    N, k = topk_ids.shape
+    L = lib()
+    cap = int(L.moe_align_capacity(N, k, E, block_m))
+    dev = topk_ids.device
+    sp = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)
+    be = torch.empty(max(cap // block_m, 1), dtype=torch.int32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    npad = torch.empty(1, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    _check(L.moe_align_noalloc(_ptr(topk_ids), N, k, E, block_m, _ptr(sp), _ptr(be),
+                               _ptr(counts), _ptr(offsets), _ptr(npad), _ptr(status), _stream()),
+           "moe_align_noalloc")
+    return {"sorted_pair": sp, "block_expert": be, "counts": counts, "offsets": offsets,
+            "num_padded": npad, "capacity": cap, "status": status}
 
 
 def moe_forward_layout(N, H, E, I, k, I_s=0) -> dict:

@@ -235,6 +235,8 @@ moe_status_t forward_layout(int64_t N, int H, int E, int I, int k, int I_s,
 
 }  // namespace
 
+void moe::set_last_error(const char *msg) { g_last_error = msg; }
+
 // =========================================================================
 extern "C" {
 

@@ -126,6 +126,9 @@ int gemm_block_n(GemmMode mode);
 cudaError_t launch_combine(const uint16_t *ypair, const uint16_t *yshared, int64_t N, int H,
                            int k, uint16_t *out, int num_sms, cudaStream_t s);
 
+// Sets the message moe_last_error() returns on this thread.
+void set_last_error(const char *msg);
+
 // ---------------------------------------------------------------- selftest
 
 cudaError_t launch_wait_timeout_probe(int32_t *status, uint64_t limit_ns, cudaStream_t s);
