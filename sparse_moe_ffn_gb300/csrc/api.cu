@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -102,6 +103,44 @@ moe_status_t record_stage(int i, cudaStream_t s) {
     if (e != cudaSuccess) return cuda_fail(e, "stage event record");
     return MOE_OK;
 }
+
+// ------------------------------------------------------------ tile choice
+
+// Expected number of 128-row blocks after grouping P pairs over E experts
+// (near-uniform routing): touched experts times blocks per touched expert.
+double expected_blocks(int64_t P, int E) {
+    const double touched = E * (1.0 - std::exp(-static_cast<double>(P) / E));
+    if (touched < 1.0) return 1.0;
+    const double per = static_cast<double>(P) / touched;
+    return touched * (per <= kBlockM ? 1.0 : per / kBlockM + 0.5);
+}
+
+// Fraction of SM time lost to the last, partial wave of `tiles` tiles.
+double wave_loss(double tiles, int sms) {
+    const double waves = tiles / sms;
+    return std::ceil(waves) / waves - 1.0;
+}
+
+// Wave loss averaged over +-3% around the expected block count (the real
+// count is only known on the device, and the loss jumps at wave boundaries).
+double mean_wave_loss(double blocks, int tiles_per_block, int sms) {
+    double sum = 0.0;
+    for (double f : {0.97, 0.985, 1.0, 1.015, 1.03})
+        sum += wave_loss(blocks * f * tiles_per_block, sms);
+    return sum / 5.0;
+}
+
+// Gate/up tile width: the one losing less SM time to wave quantisation; when
+// blocks are dense (compute bound) 96 must win by 3 points to be taken,
+// since wider tiles reuse each A tile over more columns.
+int choose_gate_up_bn(double blocks, double rows_per_expert, int I, int sms) {
+    const double l128 = mean_wave_loss(blocks, (I + 127) / 128, sms);
+    const double l96 = mean_wave_loss(blocks, (I + 95) / 96, sms);
+    const double margin = rows_per_expert >= kBlockM ? 0.03 : 0.0;
+    return l96 + margin < l128 ? 96 : 128;
+}
+
+constexpr int kDownBN = 256;
 
 // ------------------------------------------------------------------ layouts
 
@@ -430,11 +469,12 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
     if ((st = make_map(&tm_xrows, x, H, N, H, kBlockK, 1, "x rows")) != MOE_OK) return st;
     if ((st = make_map(&tm_xsorted, x_sorted, H, cap, H, kBlockK, kBlockM, "x_sorted")) != MOE_OK)
         return st;
-    if ((st = make_map(&tm_wg, w_gate, H, static_cast<uint64_t>(E) * I, H, kBlockK,
-                       gemm_block_n(kGateUp), "w_gate")) != MOE_OK)
+    const int bn_gu = choose_gate_up_bn(expected_blocks(P, E), static_cast<double>(P) / E, I, sms);
+    if ((st = make_map(&tm_wg, w_gate, H, static_cast<uint64_t>(E) * I, H, kBlockK, bn_gu,
+                       "w_gate")) != MOE_OK)
         return st;
-    if ((st = make_map(&tm_wu, w_up, H, static_cast<uint64_t>(E) * I, H, kBlockK,
-                       gemm_block_n(kGateUp), "w_up")) != MOE_OK)
+    if ((st = make_map(&tm_wu, w_up, H, static_cast<uint64_t>(E) * I, H, kBlockK, bn_gu,
+                       "w_up")) != MOE_OK)
         return st;
     GemmArgs g;
     g.sorted_pair = b.sorted_pair;
@@ -452,14 +492,14 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
     g.scale = nullptr;
     g.status = status;
     {
-        const int nt = (I + gemm_block_n(kGateUp) - 1) / gemm_block_n(kGateUp);
+        const int nt = (I + bn_gu - 1) / bn_gu;
         g.max_tiles = static_cast<int>(cap / kBlockM) * nt;
         g.grid = g.max_tiles < sms ? g.max_tiles : sms;
     }
     MOE_CUDA(launch_gather_rows(x, H, k, b.sorted_pair, b.num_padded, P, cap, x_sorted, sms, stream),
              "gather kernel launch");
-    MOE_CUDA(launch_gemm(kGateUp, tm_xrows, tm_xrows, tm_xsorted, tm_xsorted, tm_wg, tm_wu, g,
-                         stream),
+    MOE_CUDA(launch_gemm(kGateUp, bn_gu, tm_xrows, tm_xrows, tm_xsorted, tm_xsorted, tm_wg,
+                         tm_wu, g, stream),
              "gate/up kernel launch");
     g_launches += 2;
 
@@ -471,8 +511,8 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
     if ((st = make_map(&tm_act_box, act, I, cap, I, kBlockK, kBlockM, "act")) != MOE_OK) return st;
     if ((st = make_map(&tm_act_lo_box, act_lo, I, cap, I, kBlockK, kBlockM, "act_lo")) != MOE_OK)
         return st;
-    if ((st = make_map(&tm_wd, w_down, I, static_cast<uint64_t>(E) * H, I, kBlockK,
-                       gemm_block_n(kDown), "w_down")) != MOE_OK)
+    if ((st = make_map(&tm_wd, w_down, I, static_cast<uint64_t>(E) * H, I, kBlockK, kDownBN,
+                       "w_down")) != MOE_OK)
         return st;
     g.k_div = 1;
     g.K = I;
@@ -483,12 +523,12 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
     g.out_ld = H;
     g.scale = topk_w;
     {
-        const int nt = (H + gemm_block_n(kDown) - 1) / gemm_block_n(kDown);
+        const int nt = (H + kDownBN - 1) / kDownBN;
         g.max_tiles = static_cast<int>(cap / kBlockM) * nt;
         g.grid = g.max_tiles < sms ? g.max_tiles : sms;
     }
-    MOE_CUDA(launch_gemm(kDown, tm_act, tm_act_lo, tm_act_box, tm_act_lo_box, tm_wd, tm_wd, g,
-                         stream),
+    MOE_CUDA(launch_gemm(kDown, kDownBN, tm_act, tm_act_lo, tm_act_box, tm_act_lo_box, tm_wd,
+                         tm_wd, g, stream),
              "down kernel launch");
     g_launches += 1;
 
@@ -501,11 +541,13 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
         y_shared = reinterpret_cast<uint16_t *>(at(L.y_shared));
         const int64_t rows_s = round_up64(N, kBlockM);
         CUtensorMap tm_sg, tm_su, tm_acts, tm_acts_lo, tm_sd, tm_xbox;
+        const int bn_s = choose_gate_up_bn(static_cast<double>(rows_s / kBlockM),
+                                           static_cast<double>(N), I_s, sms);
         if ((st = make_map(&tm_xbox, x, H, N, H, kBlockK, kBlockM, "x")) != MOE_OK) return st;
-        if ((st = make_map(&tm_sg, shared_gate_proj, H, I_s, H, kBlockK, gemm_block_n(kGateUp),
+        if ((st = make_map(&tm_sg, shared_gate_proj, H, I_s, H, kBlockK, bn_s,
                            "shared_gate_proj")) != MOE_OK)
             return st;
-        if ((st = make_map(&tm_su, shared_up_proj, H, I_s, H, kBlockK, gemm_block_n(kGateUp),
+        if ((st = make_map(&tm_su, shared_up_proj, H, I_s, H, kBlockK, bn_s,
                            "shared_up_proj")) != MOE_OK)
             return st;
         if ((st = make_map(&tm_acts, act_s, I_s, rows_s, I_s, kBlockK, kBlockM,
@@ -514,7 +556,7 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
         if ((st = make_map(&tm_acts_lo, act_s_lo, I_s, rows_s, I_s, kBlockK, kBlockM,
                            "shared act_lo rows")) != MOE_OK)
             return st;
-        if ((st = make_map(&tm_sd, shared_down_proj, I_s, H, I_s, kBlockK, gemm_block_n(kDown),
+        if ((st = make_map(&tm_sd, shared_down_proj, I_s, H, I_s, kBlockK, kDownBN,
                            "shared_down_proj")) != MOE_OK)
             return st;
         GemmArgs s;
@@ -533,11 +575,12 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
         s.scale = nullptr;
         s.status = status;
         {
-            const int nt = (I_s + gemm_block_n(kGateUp) - 1) / gemm_block_n(kGateUp);
+            const int nt = (I_s + bn_s - 1) / bn_s;
             s.max_tiles = static_cast<int>(rows_s / kBlockM) * nt;
             s.grid = s.max_tiles < sms ? s.max_tiles : sms;
         }
-        MOE_CUDA(launch_gemm(kGateUp, tm_xbox, tm_xbox, tm_xbox, tm_xbox, tm_sg, tm_su, s, stream),
+        MOE_CUDA(launch_gemm(kGateUp, bn_s, tm_xbox, tm_xbox, tm_xbox, tm_xbox, tm_sg, tm_su, s,
+                             stream),
                  "shared gate/up kernel launch");
         s.K = I_s;
         s.n_out = H;
@@ -547,12 +590,12 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
         s.out_ld = H;
         s.scale = gamma;
         {
-            const int nt = (H + gemm_block_n(kDown) - 1) / gemm_block_n(kDown);
+            const int nt = (H + kDownBN - 1) / kDownBN;
             s.max_tiles = static_cast<int>(rows_s / kBlockM) * nt;
             s.grid = s.max_tiles < sms ? s.max_tiles : sms;
         }
-        MOE_CUDA(launch_gemm(kDown, tm_acts, tm_acts_lo, tm_acts, tm_acts_lo, tm_sd, tm_sd, s,
-                         stream),
+        MOE_CUDA(launch_gemm(kDown, kDownBN, tm_acts, tm_acts_lo, tm_acts, tm_acts_lo, tm_sd,
+                             tm_sd, s, stream),
                  "shared down kernel launch");
         g_launches += 2;
     }

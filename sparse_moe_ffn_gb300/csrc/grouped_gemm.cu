@@ -51,7 +51,7 @@ namespace moe {
 
 namespace {
 
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 6;
 constexpr int kThreads = 192;
 constexpr int kATileBytes = kBlockM * 128;  // 128 rows x 64 bf16
 constexpr int kAccCols = 256;               // fp32 columns per accumulator
@@ -69,16 +69,19 @@ struct GemmSmem {
     int abort_flag;
 };
 
-// Per-mode tile shape: BN output columns per tile, A_TILES activation tiles
-// (the gathered x, or act_hi + act_lo) and B_TILES weight tiles per K slice.
-template <int MODE>
+// Tile shape: BN output columns per tile (gate/up: BN gate + BN up
+// columns), A_TILES activation tiles (the gathered x, or act_hi + act_lo) and
+// B_TILES weight tiles per K slice; as many stages as fit in ~200 KB.
+template <int MODE, int BN_>
 struct Cfg {
-    static constexpr int BN = MODE == kGateUp ? 128 : 256;
+    static constexpr int BN = BN_;
     static constexpr int A_TILES = MODE == kGateUp ? 1 : 2;
     static constexpr int B_TILES = MODE == kGateUp ? 2 : 1;
     static constexpr int B_BYTES = B_TILES * BN * 128;
     static constexpr int STAGE_BYTES = A_TILES * kATileBytes + B_BYTES;
-    static constexpr int STAGES = MODE == kGateUp ? 4 : 3;  // 192 KB of tiles either way
+    static constexpr int STAGES = (200 * 1024 / STAGE_BYTES) < kMaxStages
+                                      ? (200 * 1024 / STAGE_BYTES) : kMaxStages;
+    static_assert(B_TILES * BN <= kAccCols, "accumulator wider than its TMEM slot");
 };
 
 __device__ __forceinline__ float silu_times(float g, float u) {
@@ -94,7 +97,7 @@ __device__ __forceinline__ void split_bf16x2(float a0, float a1, uint32_t &hi, u
     lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
-template <int MODE>
+template <int MODE, int BN_>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                         const __grid_constant__ CUtensorMap tm_a_lo,
@@ -102,10 +105,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap tm_a_lo_box,
                         const __grid_constant__ CUtensorMap tm_b0,
                         const __grid_constant__ CUtensorMap tm_b1, const GemmArgs a) {
-    constexpr int BN = Cfg<MODE>::BN;
-    constexpr int kStages = Cfg<MODE>::STAGES;
-    constexpr int kStageBytes = Cfg<MODE>::STAGE_BYTES;
-    constexpr int kBOffset = Cfg<MODE>::A_TILES * kATileBytes;
+    using C = Cfg<MODE, BN_>;
+    constexpr int BN = C::BN;
+    constexpr int kStages = C::STAGES;
+    constexpr int kStageBytes = C::STAGE_BYTES;
+    constexpr int kBOffset = C::A_TILES * kATileBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *tiles = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -188,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const uint32_t groups = dense ? 0u : __popc(__ballot_sync(0xffffffffu, any));
             const uint32_t a_bytes = dense ? kATileBytes : groups * 512;
-            const uint32_t tx = a_bytes * Cfg<MODE>::A_TILES + Cfg<MODE>::B_BYTES;
+            const uint32_t tx = a_bytes * C::A_TILES + C::B_BYTES;
             const int arow = blk * kBlockM;
             const int brow = static_cast<int>(static_cast<int64_t>(expert) * a.w_rows) + nt * BN;
             for (int kc = 0; kc < nk; ++kc, ++g) {
@@ -424,26 +428,36 @@ cudaError_t launch_gather_rows(const uint16_t *x, int H, int k, const int32_t *s
                       x, H, k, sorted_pair, num_padded, P, cap, x_sorted);
 }
 
-int gemm_block_n(GemmMode mode) { return mode == kGateUp ? Cfg<kGateUp>::BN : Cfg<kDown>::BN; }
-
-size_t gemm_smem_bytes(GemmMode mode) {
-    const size_t tiles = mode == kGateUp
-                             ? Cfg<kGateUp>::STAGES * Cfg<kGateUp>::STAGE_BYTES
-                             : Cfg<kDown>::STAGES * Cfg<kDown>::STAGE_BYTES;
-    return 1024 + tiles + sizeof(GemmSmem);
-}
-
-cudaError_t launch_gemm(GemmMode mode, const CUtensorMap &tm_a, const CUtensorMap &tm_a_lo,
-                        const CUtensorMap &tm_a_box, const CUtensorMap &tm_a_lo_box,
-                        const CUtensorMap &tm_b0, const CUtensorMap &tm_b1, const GemmArgs &a,
-                        cudaStream_t s) {
-    const size_t smem = gemm_smem_bytes(mode);
-    auto kern = mode == kGateUp ? grouped_gemm_kernel<kGateUp> : grouped_gemm_kernel<kDown>;
+template <int MODE, int BN>
+cudaError_t launch_one(const CUtensorMap &tm_a, const CUtensorMap &tm_a_lo,
+                       const CUtensorMap &tm_a_box, const CUtensorMap &tm_a_lo_box,
+                       const CUtensorMap &tm_b0, const CUtensorMap &tm_b1, const GemmArgs &a,
+                       cudaStream_t s) {
+    using C = Cfg<MODE, BN>;
+    const size_t smem = 1024 + static_cast<size_t>(C::STAGES) * C::STAGE_BYTES + sizeof(GemmSmem);
+    auto kern = grouped_gemm_kernel<MODE, BN>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
     return launch_pdl(kern, dim3(a.grid), dim3(kThreads), smem, s, 1, tm_a, tm_a_lo, tm_a_box,
                       tm_a_lo_box, tm_b0, tm_b1, a);
+}
+
+bool gemm_block_n_supported(GemmMode mode, int bn) {
+    return mode == kGateUp ? (bn == 96 || bn == 128) : (bn == 256);
+}
+
+cudaError_t launch_gemm(GemmMode mode, int bn, const CUtensorMap &tm_a,
+                        const CUtensorMap &tm_a_lo, const CUtensorMap &tm_a_box,
+                        const CUtensorMap &tm_a_lo_box, const CUtensorMap &tm_b0,
+                        const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s) {
+    if (mode == kGateUp && bn == 96)
+        return launch_one<kGateUp, 96>(tm_a, tm_a_lo, tm_a_box, tm_a_lo_box, tm_b0, tm_b1, a, s);
+    if (mode == kGateUp && bn == 128)
+        return launch_one<kGateUp, 128>(tm_a, tm_a_lo, tm_a_box, tm_a_lo_box, tm_b0, tm_b1, a, s);
+    if (mode == kDown && bn == 256)
+        return launch_one<kDown, 256>(tm_a, tm_a_lo, tm_a_box, tm_a_lo_box, tm_b0, tm_b1, a, s);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace moe

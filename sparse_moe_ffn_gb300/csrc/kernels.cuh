@@ -106,20 +106,22 @@ struct GemmArgs {
     int grid;           // persistent CTAs
 };
 
-size_t gemm_smem_bytes(GemmMode mode);
+// Tile widths: gate/up 96 or 128 columns (of each of gate and up), down 256.
+// The width changes no output element's arithmetic, only the tile count.
+bool gemm_block_n_supported(GemmMode mode, int bn);
 // tm_a / tm_a_lo: 1-row boxes for gather4 of sparse blocks (x or act_hi;
 // act_lo, down only); tm_a_box / tm_a_lo_box: 128-row boxes over rows that
 // are contiguous per block (x_sorted or x for gate/up; act_hi / act_lo for
-// down); tm_b0/tm_b1: weight rows (Wg/Wu for gate/up, Wd for down)
-cudaError_t launch_gemm(GemmMode mode, const CUtensorMap &tm_a, const CUtensorMap &tm_a_lo,
-                        const CUtensorMap &tm_a_box, const CUtensorMap &tm_a_lo_box,
-                        const CUtensorMap &tm_b0, const CUtensorMap &tm_b1, const GemmArgs &a,
-                        cudaStream_t s);
+// down); tm_b0/tm_b1: weight rows (Wg/Wu for gate/up, Wd for down), boxes of
+// bn rows
+cudaError_t launch_gemm(GemmMode mode, int bn, const CUtensorMap &tm_a,
+                        const CUtensorMap &tm_a_lo, const CUtensorMap &tm_a_box,
+                        const CUtensorMap &tm_a_lo_box, const CUtensorMap &tm_b0,
+                        const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s);
 // x rows of dense blocks copied into expert order (x_sorted [cap, H])
 cudaError_t launch_gather_rows(const uint16_t *x, int H, int k, const int32_t *sorted_pair,
                                const int32_t *num_padded, int64_t P, int64_t cap,
                                uint16_t *x_sorted, int num_sms, cudaStream_t s);
-int gemm_block_n(GemmMode mode);
 
 // ----------------------------------------------------------------- combine
 
