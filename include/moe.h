@@ -198,6 +198,23 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router,
                          moe_bf16_t *out, void *workspace,
                          size_t workspace_bytes, cudaStream_t stream);
 
+/* -------------------------------------------------------------------------
+ * moe_dense_mlp -- the dense SwiGLU MLP of the non-MoE layers (Qwen3MLP of
+ * the Nano-vLLM notes, used for mlp_only_layers; section 2.5A of the
+ * Qwen3.5 walkthrough): out = (silu(x Wg^T) * (x Wu^T)) Wd^T, the layer with
+ * E = k = 1, run on the same grouped GEMM kernels as one dense group.
+ *
+ *   x [N, H], w_gate / w_up [I, H], w_down [H, I], out [N, H]: bf16
+ *   workspace >= moe_dense_mlp_workspace_bytes(N, H, I), 256-byte aligned
+ * Precision as moe_forward.  Limits: H % 8 == 0, I % 8 == 0.
+ * ---------------------------------------------------------------------- */
+size_t moe_dense_mlp_workspace_bytes(int64_t N, int H, int I);
+moe_status_t moe_dense_mlp(const moe_bf16_t *x, const moe_bf16_t *w_gate,
+                           const moe_bf16_t *w_up, const moe_bf16_t *w_down,
+                           int64_t N, int H, int I, moe_bf16_t *out,
+                           void *workspace, size_t workspace_bytes,
+                           cudaStream_t stream);
+
 /* Byte offsets of moe_forward's workspace sub-buffers (for inspecting the
  * intermediate results; every offset is 256-byte aligned). */
 typedef struct {

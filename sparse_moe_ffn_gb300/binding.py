@@ -61,6 +61,8 @@ def lib():
         "moe_set_stage_events": ([P, i32], i32),
         "moe_selftest_wait_timeout": ([P, sz, ctypes.c_uint64, P], i32),
         "moe_align_noalloc": ([P, i64, i32, i32, i32, P, P, P, P, P, P, P], i32),
+        "moe_dense_mlp_workspace_bytes": ([i64, i32, i32], sz),
+        "moe_dense_mlp": ([P, P, P, P, i64, i32, i32, P, P, sz, P], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -222,6 +224,26 @@ def moe_forward(x, router, w_gate, w_up, w_down, k: int, norm_topk_prob: bool = 
     return out
 
 
+def moe_dense_mlp(x, w_gate, w_up, w_down, out=None, workspace=None):
+    """Dense SwiGLU MLP (silu(x Wg^T) * (x Wu^T)) Wd^T on the grouped GEMM kernels."""
+    N, H = x.shape
+    I = w_gate.shape[0]
+    _bf16(x, "x")
+    _bf16(w_gate, "w_gate", (I, H))
+    _bf16(w_up, "w_up", (I, H))
+    _bf16(w_down, "w_down", (H, I))
+    if out is None:
+        out = torch.empty((N, H), dtype=torch.bfloat16, device=x.device)
+    _bf16(out, "out", (N, H))
+    L = lib()
+    if workspace is None:
+        workspace = torch.empty(max(int(L.moe_dense_mlp_workspace_bytes(N, H, I)), 256),
+                                dtype=torch.uint8, device=x.device)
+    _check(L.moe_dense_mlp(_ptr(x), _ptr(w_gate), _ptr(w_up), _ptr(w_down), N, H, I, _ptr(out),
+                           _ptr(workspace), workspace.numel(), _stream()), "moe_dense_mlp")
+    return out
+
+
 def moe_forward_from_host(x_host, out_host, x_dev, out_dev, weights: dict, k: int,
                           norm_topk_prob: bool, workspace):
     """End-to-end call with host buffers: copy x (pinned host) to the device,
@@ -233,6 +255,51 @@ def moe_forward_from_host(x_host, out_host, x_dev, out_dev, weights: dict, k: in
                 k, norm_topk_prob, shared, out=out_dev, workspace=workspace)
     out_host.copy_(out_dev, non_blocking=True)
     return out_host
+
+
+class ForwardGraph:
+    """moe_forward captured once in a CUDA graph for a token bucket of
+    `bucket` rows, then replayed: the serving decode loop's way of removing
+    per-step launch cost.  A batch of n <= bucket tokens is copied into the
+    first n rows of the static input (the rest zero); since every token's
+    result is independent of the others, out[:n] equals an eager call on the
+    n tokens bit for bit."""
+
+    def __init__(self, weights: dict, k: int, norm_topk_prob: bool, bucket: int):
+        dev = weights["router"].device
+        H = weights["router"].shape[1]
+        E, I, _ = weights["w_gate"].shape
+        self.shared = ({n: weights[n] for n in SHARED_KEYS} if "shared_gate" in weights
+                       else None)
+        I_s = self.shared["shared_gate_proj"].shape[0] if self.shared else 0
+        self.w, self.k, self.norm, self.bucket = weights, k, norm_topk_prob, bucket
+        self.x = torch.zeros((bucket, H), dtype=torch.bfloat16, device=dev)
+        self.out = torch.empty((bucket, H), dtype=torch.bfloat16, device=dev)
+        self.ws = alloc_workspace(bucket, H, E, I, k, I_s, dev)
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            for _ in range(2):
+                self._call()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self._call()
+
+    def _call(self):
+        w = self.w
+        moe_forward(self.x, w["router"], w["w_gate"], w["w_up"], w["w_down"], self.k, self.norm,
+                    self.shared, out=self.out, workspace=self.ws)
+
+    def __call__(self, x):
+        n = x.shape[0]
+        if n > self.bucket:
+            raise ValueError(f"{n} tokens exceed the graph's bucket of {self.bucket}")
+        self.x[:n].copy_(x)
+        if n < self.bucket:
+            self.x[n:].zero_()
+        self.graph.replay()
+        return self.out[:n]
 
 
 def workspace_views(workspace, N, H, E, I, k, I_s=0) -> dict:

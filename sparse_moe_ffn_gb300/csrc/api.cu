@@ -608,6 +608,87 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
     return MOE_OK;
 }
 
+// ------------------------------------------------------------ dense MLP
+
+size_t moe_dense_mlp_workspace_bytes(int64_t N, int H, int I) {
+    if (N < 0 || H < 1 || I < 1) return 0;
+    const size_t rows = static_cast<size_t>(round_up64(N, kBlockM));
+    return kAlign + 2 * round_up(2 * rows * I, kAlign) + round_up(2 * static_cast<size_t>(N) * H, kAlign);
+}
+
+moe_status_t moe_dense_mlp(const moe_bf16_t *x, const moe_bf16_t *w_gate, const moe_bf16_t *w_up,
+                           const moe_bf16_t *w_down, int64_t N, int H, int I, moe_bf16_t *out,
+                           void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    g_last_error.clear();
+    if (N < 0) return fail(MOE_ERR_INVALID_ARG, "N must be >= 0");
+    if (H < 8 || H % 8 || I < 8 || I % 8)
+        return fail(MOE_ERR_INVALID_ARG, "H and I must be positive multiples of 8 (H=%d, I=%d)", H, I);
+    if (N == 0) return MOE_OK;
+    if (!x || !w_gate || !w_up || !w_down || !out || !workspace)
+        return fail(MOE_ERR_INVALID_ARG, "every moe_dense_mlp pointer must be non-null");
+    if (!aligned16(x) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
+        !aligned16(out))
+        return fail(MOE_ERR_INVALID_ARG, "bf16 matrices must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
+        return fail(MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    if (N >= (int64_t(1) << 31) - kBlockM) return fail(MOE_ERR_UNSUPPORTED, "N must stay below 2^31");
+    const size_t need = moe_dense_mlp_workspace_bytes(N, H, I);
+    if (workspace_bytes < need)
+        return fail(MOE_ERR_WORKSPACE_TOO_SMALL, "dense MLP workspace needs %zu bytes, got %zu", need,
+                    workspace_bytes);
+    const int64_t rows = round_up64(N, kBlockM);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    int32_t *status = reinterpret_cast<int32_t *>(ws);
+    uint16_t *act = reinterpret_cast<uint16_t *>(ws + kAlign);
+    uint16_t *act_lo = reinterpret_cast<uint16_t *>(ws + kAlign + round_up(2 * rows * I, kAlign));
+    uint16_t *y = reinterpret_cast<uint16_t *>(ws + kAlign + 2 * round_up(2 * rows * I, kAlign));
+    const int sms = num_sms_of_current_device();
+    moe_status_t st;
+    CUtensorMap tm_x, tm_g, tm_u, tm_act, tm_act_lo, tm_d;
+    const int bn = choose_gate_up_bn(static_cast<double>(rows / kBlockM), static_cast<double>(N), I, sms);
+    if ((st = make_map(&tm_x, x, H, N, H, kBlockK, kBlockM, "x")) != MOE_OK) return st;
+    if ((st = make_map(&tm_g, w_gate, H, I, H, kBlockK, bn, "w_gate")) != MOE_OK) return st;
+    if ((st = make_map(&tm_u, w_up, H, I, H, kBlockK, bn, "w_up")) != MOE_OK) return st;
+    if ((st = make_map(&tm_act, act, I, rows, I, kBlockK, kBlockM, "act")) != MOE_OK) return st;
+    if ((st = make_map(&tm_act_lo, act_lo, I, rows, I, kBlockK, kBlockM, "act_lo")) != MOE_OK) return st;
+    if ((st = make_map(&tm_d, w_down, I, H, I, kBlockK, kDownBN, "w_down")) != MOE_OK) return st;
+    MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int32_t), stream), "status reset");
+    // one dense group: every token row, weight 1
+    GemmArgs g = {};
+    g.sorted_pair = nullptr;
+    g.block_expert = nullptr;
+    g.num_padded = nullptr;
+    g.num_rows_host = N;
+    g.q_limit = N;
+    g.k_div = 1;
+    g.K = H;
+    g.n_out = I;
+    g.w_rows = I;
+    g.out = act;
+    g.out_lo = act_lo;
+    g.out_ld = I;
+    g.scale = nullptr;
+    g.status = status;
+    g.max_tiles = static_cast<int>(rows / kBlockM) * ((I + bn - 1) / bn);
+    g.grid = g.max_tiles < sms ? g.max_tiles : sms;
+    MOE_CUDA(launch_gemm(kGateUp, bn, tm_x, tm_x, tm_x, tm_x, tm_g, tm_u, g, stream),
+             "dense gate/up kernel launch");
+    g.K = I;
+    g.n_out = H;
+    g.w_rows = H;
+    g.out = y;
+    g.out_lo = nullptr;
+    g.out_ld = H;
+    g.max_tiles = static_cast<int>(rows / kBlockM) * ((H + kDownBN - 1) / kDownBN);
+    g.grid = g.max_tiles < sms ? g.max_tiles : sms;
+    MOE_CUDA(launch_gemm(kDown, kDownBN, tm_act, tm_act_lo, tm_act, tm_act_lo, tm_d, tm_d, g, stream),
+             "dense down kernel launch");
+    // fp16 rows -> bf16 out (the combine with one slot per token)
+    MOE_CUDA(launch_combine(y, nullptr, N, H, 1, out, sms, stream), "combine kernel launch");
+    g_launches += 3;
+    return MOE_OK;
+}
+
 moe_status_t moe_selftest_wait_timeout(void *workspace, size_t workspace_bytes,
                                        uint64_t limit_ns, cudaStream_t stream) {
     g_last_error.clear();

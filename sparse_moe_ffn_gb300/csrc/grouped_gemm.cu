@@ -345,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             } else {
-                const float w = valid ? __ldcg(a.scale + q) : 0.f;
+                const float w = !valid ? 0.f : (a.scale ? __ldcg(a.scale + q) : 1.f);
                 uint16_t *dst = a.out + (valid ? q : 0) * a.out_ld + col0;
                 float vmax = 0.f;
 #pragma unroll 1

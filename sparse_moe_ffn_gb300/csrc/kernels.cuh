@@ -100,7 +100,7 @@ struct GemmArgs {
     uint16_t *out;      // act_hi [rows, I] (gate/up) or fp16 y [q_limit, H] (down)
     uint16_t *out_lo;   // act_lo [rows, I] (gate/up only)
     int64_t out_ld;
-    const float *scale; // down: per-q weight
+    const float *scale; // down: per-q weight (null: 1)
     int32_t *status;
     int max_tiles;      // upper bound on tiles (sizes the persistent grid)
     int grid;           // persistent CTAs
