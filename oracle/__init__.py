@@ -84,6 +84,8 @@ class Oracle:
         lib.oracle_moe_forward.argtypes = [P] * 9 + [i64, i32, i32, i32, i32, i32, i32,
                                                     P, i64, P, i32]
         lib.oracle_moe_forward.restype = i32
+        lib.oracle_add_rmsnorm.argtypes = [P, P, P, i64, i32, ctypes.c_double, i32, P, P]
+        lib.oracle_add_rmsnorm.restype = i32
         lib.oracle_hardware_threads.argtypes = []
         lib.oracle_hardware_threads.restype = i32
         self.lib = lib
@@ -136,6 +138,20 @@ class Oracle:
             "flat_e": ids.reshape(-1).copy(),
             "flat_tok": np.repeat(np.arange(N, dtype=np.int64), k),
         }
+
+    def add_rmsnorm(self, x, residual, weight, eps: float, gemma: bool = False):
+        """(new residual as bf16 bits [N,H], normed [N,H] fp64)."""
+        x = _u16(x)
+        N, H = x.shape
+        residual = _u16(residual, (N, H))
+        weight = _u16(weight, (H,))
+        res_out = np.zeros((N, H), np.uint16)
+        normed = np.zeros((N, H), np.float64)
+        rc = self.lib.oracle_add_rmsnorm(_ptr(x), _ptr(residual), _ptr(weight), N, H, float(eps),
+                                         int(bool(gemma)), _ptr(res_out), _ptr(normed))
+        if rc != 0:
+            raise ValueError(f"oracle_add_rmsnorm failed with code {rc}")
+        return res_out, normed
 
     def moe_forward(self, w: dict, k: int, norm: bool, rows=None, nthreads: int = 0):
         """out[r] = MoE(x[rows[r]]) in fp64.
@@ -206,3 +222,7 @@ def align(ids, E: int, BM: int):
 
 def moe_forward(w: dict, k: int, norm: bool, rows=None, nthreads: int = 0):
     return default().moe_forward(w, k, norm, rows, nthreads)
+
+
+def add_rmsnorm(x, residual, weight, eps: float, gemma: bool = False):
+    return default().add_rmsnorm(x, residual, weight, eps, gemma)

@@ -252,6 +252,58 @@ done:
     return NULL;
 }
 
+/* ------------------------------------------------------------------------ */
+/* fused residual add + RMSNorm (the decoder layer's step before the MoE)    */
+/* ------------------------------------------------------------------------ */
+
+/* IEEE binary32 -> bf16 bits, round to nearest even (finite inputs). */
+static uint16_t round_to_bf16(double v)
+{
+    float f = (float)v; /* exact for the sums formed below (see caller) */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7FFFu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+/*
+ * Nano-vLLM notes (question 4 on the decoder layer) and the Qwen3.5
+ * walkthrough (section 2.1): hidden = hidden + residual; residual = hidden;
+ * hidden = norm(hidden), with RMSNorm(r) = r / sqrt(mean(r^2) + eps) * w
+ * (Qwen3 tutorial, RMSNorm section) or, when gemma != 0, * (1 + w)
+ * (GemmaRMSNorm, walkthrough section 2.1).  The add happens in the model's
+ * bf16 dtype: r = bf16(x + residual) is the new residual and the norm's input.
+ *   residual_out [N, H] bf16 bits;  normed [N, H] fp64 (before any rounding)
+ */
+int oracle_add_rmsnorm(const uint16_t *x, const uint16_t *residual, const uint16_t *w,
+                       int64_t N, int H, double eps, int gemma, uint16_t *residual_out,
+                       double *normed)
+{
+    if (N < 0 || H < 1 || eps < 0) return 1;
+    double *r = malloc(sizeof(double) * (size_t)H);
+    if (!r) return 2;
+    for (int64_t n = 0; n < N; ++n) {
+        double ss = 0.0;
+        for (int h = 0; h < H; ++h) {
+            /* the sum of two bf16 values is exact in binary32 unless their
+             * exponents differ by more than 16, where the smaller one is far
+             * below half a bf16 ulp and cannot change the rounded result */
+            uint16_t b = round_to_bf16(widen_bf16(x[n * H + h]) + widen_bf16(residual[n * H + h]));
+            residual_out[n * H + h] = b;
+            r[h] = widen_bf16(b);
+            ss += r[h] * r[h];
+        }
+        double inv = 1.0 / sqrt(ss / H + eps);
+        for (int h = 0; h < H; ++h) {
+            double wh = widen_bf16(w[h]);
+            normed[n * H + h] = r[h] * inv * (gemma ? 1.0 + wh : wh);
+        }
+    }
+    free(r);
+    return 0;
+}
+
 int oracle_hardware_threads(void)
 {
     long n = sysconf(_SC_NPROCESSORS_ONLN);

@@ -297,9 +297,31 @@ def check_batch_invariance(orc):
         assert np.array_equal(orc.moe_forward(w, 2, True, rows=[i])[0], full[i])
 
 
+def check_add_rmsnorm(orc):
+    """Residual add in bf16, then RMSNorm: against torch's rms_norm in fp64 on
+    the bf16 sum, a closed form (constant rows) and the Gemma (1 + w) form."""
+    rng = np.random.default_rng(21)
+    N, H, eps = 9, 96, 1e-6
+    x = bits(rng.standard_normal((N, H)))
+    res = bits(rng.standard_normal((N, H)) * 3)
+    w = bits(1 + 0.1 * rng.standard_normal(H))
+    r_bits, normed = orc.add_rmsnorm(x, res, w, eps)
+    r_ref = (torch.from_numpy(widen(x)) + torch.from_numpy(widen(res))).to(torch.bfloat16)
+    assert np.array_equal(r_bits, r_ref.view(torch.int16).numpy().view(np.uint16))
+    want = torch.nn.functional.rms_norm(r_ref.double(), (H,), torch.from_numpy(widen(w)), eps)
+    np.testing.assert_allclose(normed, want.numpy(), rtol=1e-12, atol=1e-14)
+    _, g = orc.add_rmsnorm(x, res, w, eps, gemma=True)
+    want_g = torch.nn.functional.rms_norm(r_ref.double(), (H,), 1 + torch.from_numpy(widen(w)), eps)
+    np.testing.assert_allclose(g, want_g.numpy(), rtol=1e-12, atol=1e-14)
+    # a constant row c normalises to c / sqrt(c^2 + eps) * w
+    c = np.full((1, H), 0.75)
+    _, one = orc.add_rmsnorm(bits(c), bits(np.zeros((1, H))), w, eps)
+    np.testing.assert_allclose(one[0], 0.75 / np.sqrt(0.5625 + eps) * widen(w), rtol=1e-13)
+
+
 ALL_CHECKS = [check_bookkeeping, check_route_io, check_scalar_e2e, check_shared,
               check_shape_trace, check_brute_force, check_closed_forms, check_ties,
-              check_align_vs_numpy, check_batch_invariance]
+              check_align_vs_numpy, check_batch_invariance, check_add_rmsnorm]
 
 
 def failures(orc):

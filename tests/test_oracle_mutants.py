@@ -29,6 +29,10 @@ MUTANTS = [
     ("offsets not accumulated", "offsets[e + 1] = offsets[e] + counts[e];", "offsets[e + 1] = counts[e];"),
     ("wrong padding sentinel", "(i < c) ? order[offsets[e] + i] : (int32_t)P", "(i < c) ? order[offsets[e] + i] : (int32_t)(P - 1)"),
     ("segments not padded", "int64_t seg = (c + BM - 1) / BM * BM;", "int64_t seg = c;"),
+    ("rmsnorm without eps", "double inv = 1.0 / sqrt(ss / H + eps);", "double inv = 1.0 / sqrt(ss / H);"),
+    ("rmsnorm sum not averaged", "double inv = 1.0 / sqrt(ss / H + eps);", "double inv = 1.0 / sqrt(ss + eps);"),
+    ("gemma weight not offset", "(gemma ? 1.0 + wh : wh)", "(gemma ? wh : wh)"),
+    ("residual add dropped", "round_to_bf16(widen_bf16(x[n * H + h]) + widen_bf16(residual[n * H + h]))", "round_to_bf16(widen_bf16(x[n * H + h]))"),
 ]
 
 

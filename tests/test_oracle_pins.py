@@ -64,3 +64,7 @@ def test_pitfall_variants_are_rejected_by_the_pins():
     # equals the renormalised weights, but not the raw ones
     assert np.allclose(top_first, r["weights_norm"], atol=1e-4)
     assert not np.allclose(top_first, r["weights_raw"], atol=1e-2)
+
+
+def test_fused_add_rmsnorm():
+    pins.check_add_rmsnorm(oracle.default())
