@@ -199,6 +199,25 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router,
                          size_t workspace_bytes, cudaStream_t stream);
 
 /* -------------------------------------------------------------------------
+ * moe_add_rmsnorm -- the decoder layer's step that feeds the MoE, in one
+ * kernel (Nano-vLLM notes, question 4 on the decoder layer; Qwen3.5
+ * walkthrough section 2.1): r = x + residual in the model's bf16 dtype;
+ * residual = r; normed = r / sqrt(mean(r^2) + eps) * weight, or
+ * * (1 + weight) when gemma != 0 (GemmaRMSNorm).
+ *
+ *   x        [N, H] bf16 in (the sub-layer's output)
+ *   residual [N, H] bf16 in/out (becomes r)
+ *   weight   [H]    bf16
+ *   normed   [N, H] bf16 out (the MoE's input x; may not alias x or residual)
+ * Precision: the sum of squares in fp32, one bf16 rounding of normed; the
+ * residual equals bf16(x + residual) bit for bit.  Limits: H % 8 == 0.
+ * ---------------------------------------------------------------------- */
+moe_status_t moe_add_rmsnorm(const moe_bf16_t *x, moe_bf16_t *residual,
+                             const moe_bf16_t *weight, int64_t N, int H,
+                             float eps, int gemma, moe_bf16_t *normed,
+                             cudaStream_t stream);
+
+/* -------------------------------------------------------------------------
  * moe_dense_mlp -- the dense SwiGLU MLP of the non-MoE layers (Qwen3MLP of
  * the Nano-vLLM notes, used for mlp_only_layers; section 2.5A of the
  * Qwen3.5 walkthrough): out = (silu(x Wg^T) * (x Wu^T)) Wd^T, the layer with

@@ -62,6 +62,7 @@ def lib():
         "moe_selftest_wait_timeout": ([P, sz, ctypes.c_uint64, P], i32),
         "moe_align_noalloc": ([P, i64, i32, i32, i32, P, P, P, P, P, P, P], i32),
         "moe_dense_mlp_workspace_bytes": ([i64, i32, i32], sz),
+        "moe_add_rmsnorm": ([P, P, P, i64, i32, ctypes.c_float, i32, P, P], i32),
         "moe_dense_mlp": ([P, P, P, P, i64, i32, i32, P, P, sz, P], i32),
     }
     for name, (args, res) in sig.items():
@@ -222,6 +223,20 @@ def moe_forward(x, router, w_gate, w_up, w_down, k: int, norm_topk_prob: bool = 
                              int(bool(norm_topk_prob)), _ptr(out), _ptr(workspace),
                              workspace.numel(), _stream()), "moe_forward")
     return out
+
+
+def moe_add_rmsnorm(x, residual, weight, eps: float = 1e-6, gemma: bool = False, normed=None):
+    """residual <- bf16(x + residual) in place; returns RMSNorm(residual) (bf16)."""
+    N, H = x.shape
+    _bf16(x, "x")
+    _bf16(residual, "residual", (N, H))
+    _bf16(weight, "weight", (H,))
+    if normed is None:
+        normed = torch.empty((N, H), dtype=torch.bfloat16, device=x.device)
+    _bf16(normed, "normed", (N, H))
+    _check(lib().moe_add_rmsnorm(_ptr(x), _ptr(residual), _ptr(weight), N, H, float(eps),
+                                 int(bool(gemma)), _ptr(normed), _stream()), "moe_add_rmsnorm")
+    return normed
 
 
 def moe_dense_mlp(x, w_gate, w_up, w_down, out=None, workspace=None):

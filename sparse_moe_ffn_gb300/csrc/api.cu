@@ -608,6 +608,27 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
     return MOE_OK;
 }
 
+// ----------------------------------------------------- add + RMSNorm
+
+moe_status_t moe_add_rmsnorm(const moe_bf16_t *x, moe_bf16_t *residual, const moe_bf16_t *weight,
+                             int64_t N, int H, float eps, int gemma, moe_bf16_t *normed,
+                             cudaStream_t stream) {
+    g_last_error.clear();
+    if (N < 0) return fail(MOE_ERR_INVALID_ARG, "N must be >= 0");
+    if (H < 8 || H % 8) return fail(MOE_ERR_INVALID_ARG, "H must be a positive multiple of 8 (got %d)", H);
+    if (!(eps >= 0.f)) return fail(MOE_ERR_INVALID_ARG, "eps must be >= 0");
+    if (N == 0) return MOE_OK;
+    if (!x || !residual || !weight || !normed)
+        return fail(MOE_ERR_INVALID_ARG, "x, residual, weight and normed must be non-null");
+    if (!aligned16(x) || !aligned16(residual) || !aligned16(weight) || !aligned16(normed))
+        return fail(MOE_ERR_INVALID_ARG, "bf16 arrays must be 16-byte aligned");
+    MOE_CUDA(launch_add_rmsnorm(x, residual, weight, N, H, eps, gemma ? 1 : 0, normed,
+                                num_sms_of_current_device(), stream),
+             "add+rmsnorm kernel launch");
+    g_launches += 1;
+    return MOE_OK;
+}
+
 // ------------------------------------------------------------ dense MLP
 
 size_t moe_dense_mlp_workspace_bytes(int64_t N, int H, int I) {

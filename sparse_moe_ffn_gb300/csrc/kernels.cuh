@@ -128,6 +128,12 @@ cudaError_t launch_gather_rows(const uint16_t *x, int H, int k, const int32_t *s
 cudaError_t launch_combine(const uint16_t *ypair, const uint16_t *yshared, int64_t N, int H,
                            int k, uint16_t *out, int num_sms, cudaStream_t s);
 
+// ------------------------------------------------- residual add + RMSNorm
+
+cudaError_t launch_add_rmsnorm(const uint16_t *x, uint16_t *residual, const uint16_t *w,
+                               int64_t N, int H, float eps, int gemma, uint16_t *normed,
+                               int num_sms, cudaStream_t s);
+
 // Sets the message moe_last_error() returns on this thread.
 void set_last_error(const char *msg);
 

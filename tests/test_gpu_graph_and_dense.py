@@ -46,3 +46,20 @@ def test_dense_mlp_matches_oracle(N, H, I):
     assert_close(out[torch.from_numpy(rows).cuda()], ref, f"dense N={N}")
     # and it agrees with the layer's own E = k = 1 path bit for bit
     assert torch.equal(out, _eager(shape, dev, dev["x"]))
+
+
+@pytest.mark.parametrize("N,H,gemma", [(64, 2048, False), (8192, 2048, False), (37, 200, True),
+                                       (1, 64, False)])
+def test_add_rmsnorm_matches_oracle(N, H, gemma):
+    rng = np.random.default_rng(N + H)
+    x = torch.from_numpy(rng.standard_normal((N, H)).astype(np.float32)).to(torch.bfloat16)
+    res = torch.from_numpy((3 * rng.standard_normal((N, H))).astype(np.float32)).to(torch.bfloat16)
+    w = torch.from_numpy((1 + 0.1 * rng.standard_normal(H)).astype(np.float32)).to(torch.bfloat16)
+    r_ref, n_ref = oracle.add_rmsnorm(oracle.bf16_bits(x), oracle.bf16_bits(res),
+                                      oracle.bf16_bits(w), 1e-6, gemma)
+    res_d = res.cuda()
+    normed = binding.moe_add_rmsnorm(x.cuda(), res_d, w.cuda(), 1e-6, gemma)
+    assert np.array_equal(oracle.bf16_bits(res_d), r_ref)   # the new residual, bit for bit
+    got = normed.float().cpu().numpy().astype(np.float64)
+    # one bf16 rounding (half an ulp is 2^-9 relative) plus the fp32 sum of squares
+    assert np.all(np.abs(got - n_ref) <= 2.0 ** -8 * np.abs(n_ref) + 1e-30)
