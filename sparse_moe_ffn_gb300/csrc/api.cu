@@ -491,6 +491,8 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
     g.out_ld = I;
     g.scale = nullptr;
     g.status = status;
+    // fewer than a block of pairs per expert: every weight tile is read once
+    g.stream_weights = P < static_cast<int64_t>(E) * kBlockM ? 1 : 0;
     {
         const int nt = (I + bn_gu - 1) / bn_gu;
         g.max_tiles = static_cast<int>(cap / kBlockM) * nt;
@@ -574,6 +576,7 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
         s.out_ld = I_s;
         s.scale = nullptr;
         s.status = status;
+        s.stream_weights = N <= kBlockM ? 1 : 0;
         {
             const int nt = (I_s + bn_s - 1) / bn_s;
             s.max_tiles = static_cast<int>(rows_s / kBlockM) * nt;
@@ -690,6 +693,7 @@ moe_status_t moe_dense_mlp(const moe_bf16_t *x, const moe_bf16_t *w_gate, const 
     g.out_ld = I;
     g.scale = nullptr;
     g.status = status;
+    g.stream_weights = N <= kBlockM ? 1 : 0;
     g.max_tiles = static_cast<int>(rows / kBlockM) * ((I + bn - 1) / bn);
     g.grid = g.max_tiles < sms ? g.max_tiles : sms;
     MOE_CUDA(launch_gemm(kGateUp, bn, tm_x, tm_x, tm_x, tm_x, tm_g, tm_u, g, stream),

@@ -157,6 +157,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (warp)
+        // weight tiles used by one row block each (decode) are streamed with
+        // evict-first so that they do not push the reused data out of L2
+        const uint64_t wpol = a.stream_weights ? l2_policy_evict_first() : 0;
         int g = 0;  // K slices issued by this CTA so far
         bool failed = false;
         for (int tile = blockIdx.x; tile < total_tiles && !failed; tile += gridDim.x) {
@@ -227,10 +230,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     kc * kBlockK, src[0], src[1], src[2], src[3]);
                 }
                 if (lane == 0) {
-                    tma_load_2d(st + kBOffset, &tm_b0, &sm->full[s], kc * kBlockK, brow);
-                    if (MODE == kGateUp)
-                        tma_load_2d(st + kBOffset + BN * 128, &tm_b1, &sm->full[s],
-                                    kc * kBlockK, brow);
+                    if (a.stream_weights) {
+                        tma_load_2d_hint(st + kBOffset, &tm_b0, &sm->full[s], kc * kBlockK, brow,
+                                         wpol);
+                        if (MODE == kGateUp)
+                            tma_load_2d_hint(st + kBOffset + BN * 128, &tm_b1, &sm->full[s],
+                                             kc * kBlockK, brow, wpol);
+                    } else {
+                        tma_load_2d(st + kBOffset, &tm_b0, &sm->full[s], kc * kBlockK, brow);
+                        if (MODE == kGateUp)
+                            tma_load_2d(st + kBOffset + BN * 128, &tm_b1, &sm->full[s],
+                                        kc * kBlockK, brow);
+                    }
                 }
             }
         }

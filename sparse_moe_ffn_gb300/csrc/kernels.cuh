@@ -102,6 +102,7 @@ struct GemmArgs {
     int64_t out_ld;
     const float *scale; // down: per-q weight (null: 1)
     int32_t *status;
+    int stream_weights; // weight tiles read once per call: load them evict-first
     int max_tiles;      // upper bound on tiles (sizes the persistent grid)
     int grid;           // persistent CTAs
 };

@@ -143,6 +143,8 @@ __global__ void __launch_bounds__(kRouterThreads, 1)
         // ---------------- TMA producer: this CTA's slice of H
         if (lane == 0) {
             const uint32_t tx = kATileBytes + a.E * 128 + (a.gamma_col >= 0 ? 8 * 128 : 0);
+            // the router (and gate) rows are re-read by every layer call: keep them in L2
+            const uint64_t keep = l2_policy_evict_last();
             int i = 0;
             for (; i < my_nk; ++i) {
                 const int s = i % kRouterStages;
@@ -156,10 +158,10 @@ __global__ void __launch_bounds__(kRouterThreads, 1)
                 const int kcol = (kc0 + i) * kBlockK;
                 mbar_arrive_expect_tx(&sm->full[s], tx);
                 tma_load_2d(st, &tm_x, &sm->full[s], kcol, static_cast<int>(n0));
-                tma_load_2d(st + kATileBytes, &tm_router, &sm->full[s], kcol, 0);
+                tma_load_2d_hint(st + kATileBytes, &tm_router, &sm->full[s], kcol, 0, keep);
                 if (a.gamma_col >= 0)
-                    tma_load_2d(st + kATileBytes + a.gamma_col * 128, &tm_gate, &sm->full[s],
-                                kcol, 0);
+                    tma_load_2d_hint(st + kATileBytes + a.gamma_col * 128, &tm_gate, &sm->full[s],
+                                     kcol, 0, keep);
             }
             for (int j = (i > kRouterStages ? i - kRouterStages : 0); j < i; ++j)
                 mbar_wait(&sm->full[j % kRouterStages], (j / kRouterStages) & 1, abort_flag);
