@@ -11,13 +11,13 @@
 // tokens; CTA c of the cluster takes the c-th slice of H.  Each CTA streams x
 // [128 x 64] and router [e_pad x 64] slices through a TMA ring into one
 // tcgen05 MMA chain (M = 128 tokens, N = e_pad experts, plus g in column
-// gamma_col), so its TMEM holds the partial logits of its H slice.  The
-// partial tile is copied to the CTA's own shared memory; after a cluster
-// barrier, CTA c reduces token rows [16c, 16c + 16) (in 16-row passes when
-// split < 8), 8 lanes per row and 4 rows per warp: the `split` partial rows
-// are read through distributed shared memory in rank order with coalesced
-// 16-byte loads, and the 8 lanes run the softmax, the k arg-max rounds and the
-// renormalisation with shuffle reductions.  Every reduction order depends
+// gamma_col), so its TMEM holds the partial logits of its H slice.  CTA c
+// reduces token rows [16c, 16c + 16) (all 128 rows, in 16-row passes, when
+// split = 1): every CTA stores its partial rows into the reducing CTA's shared
+// memory with distributed-shared-memory stores, and after a cluster barrier
+// the reducer sums the `split` partial rows in rank order from local memory.
+// 8 lanes per row and 4 rows per warp run the softmax, the k arg-max rounds
+// and the renormalisation with shuffle reductions.  Every reduction order depends
 // on H and E only, never on N: routing is batch invariant bit for bit.
 #include <cuda_bf16.h>
 #include <math.h>
@@ -29,12 +29,12 @@ namespace moe {
 
 namespace {
 
-constexpr int kRouterStages = 4;
+constexpr int kRouterStages = 3;  // ~99 KB per CTA at E = 128: two CTAs per SM
 constexpr int kRouterThreads = 128;
 constexpr int kATileBytes = kBlockM * 128;  // 128 tokens x 64 bf16
 constexpr int kLanesPerRow = 8;                           // lanes sharing one token row
 constexpr int kRowsPerPass = kRouterThreads / kLanesPerRow;  // 16 rows per pass
-constexpr int kMaxPerLane = MOE_MAX_EXPERTS / kLanesPerRow;  // 32 logits per lane
+constexpr int kMaxPerLane = MOE_MAX_EXPERTS / kLanesPerRow;  // 32 logits per lane at most
 
 struct RouterSmem {
     uint64_t full[kRouterStages];
@@ -69,6 +69,12 @@ __device__ __forceinline__ uint32_t dsmem_addr(const void *local, uint32_t rank)
     return remote;
 }
 
+__device__ __forceinline__ void st_dsmem_f4(uint32_t addr, float4 v) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x),
+                 "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
 __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
     float4 v;
     asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
@@ -86,6 +92,9 @@ __device__ __forceinline__ void key_max(float &v, int &e, float ov, int oe) {
     }
 }
 
+// PL: logits per lane (e_pad / 8 rounded up to 4, 16 or 32), a compile-time
+// bound so that the per-round scans cover only the columns that exist.
+template <int PL>
 __global__ void __launch_bounds__(kRouterThreads, 1)
     router_kernel(const __grid_constant__ CUtensorMap tm_x,
                   const __grid_constant__ CUtensorMap tm_router,
@@ -194,7 +203,10 @@ __global__ void __launch_bounds__(kRouterThreads, 1)
         __syncwarp();
     }
 
-    // ---------------- phase 1: partial logits TMEM -> own shared memory
+    // ---------------- phase 1: partial logits -> the shared memory of the CTA
+    // that reduces them.  Token row r belongs to cluster CTA r / rows_per_cta;
+    // each CTA stores its partial row there, into slot [own rank][row], with
+    // remote stores (no round trip), so the reduction reads local memory.
     const bool ok = mbar_wait(&sm->acc_full, 0, abort_flag);
     __syncwarp();
     if (!ok) {
@@ -202,9 +214,14 @@ __global__ void __launch_bounds__(kRouterThreads, 1)
         *abort_flag = 1;
     }
     tc_fence_after_sync();
-    __syncthreads();  // every stage is consumed: the ring may be overwritten
+    const int rows_per_cta = kBlockM / a.split;
+    // every ring of the cluster is idle before any CTA writes into a peer's
+    cluster_sync();
     {
         const int row = warp * 32 + lane;  // TMEM lane
+        const uint32_t owner = static_cast<uint32_t>(row / rows_per_cta);
+        const int slot = static_cast<int>(crank) * rows_per_cta + row % rows_per_cta;
+        const uint32_t dst = dsmem_addr(&partial[slot * ld], owner);
         const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
         for (int c = 0; c < (a.e_pad + 31) / 32; ++c) {
             float v[32];
@@ -213,13 +230,13 @@ __global__ void __launch_bounds__(kRouterThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; i += 4)
                 if (c * 32 + i < a.e_pad)
-                    *reinterpret_cast<float4 *>(&partial[row * ld + c * 32 + i]) =
-                        ok ? make_float4(v[i], v[i + 1], v[i + 2], v[i + 3])
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                    st_dsmem_f4(dst + 4 * (c * 32 + i),
+                                ok ? make_float4(v[i], v[i + 1], v[i + 2], v[i + 3])
+                                   : make_float4(0.f, 0.f, 0.f, 0.f));
         }
     }
     tc_fence_before_sync();
-    cluster_sync();  // all partial tiles of the cluster are in place
+    cluster_sync();  // every partial row has reached its reducer
 
     // ---------------- phase 2: reduce over the cluster, then route
     // 8 lanes per token row, 4 rows per warp, 16 rows per pass.  Lane `sub`
@@ -227,7 +244,6 @@ __global__ void __launch_bounds__(kRouterThreads, 1)
     // group reads 128 contiguous bytes of a partial row per load.  The
     // `split` partials are summed in rank order.
     const int sub = lane % kLanesPerRow;
-    const int rows_per_cta = kBlockM / a.split;
     const int groups = (a.e_pad + 31) / 32;
     float *slot_w = partial + kBlockM * ld;                              // [16][k]
     int32_t *slot_e = reinterpret_cast<int32_t *>(slot_w + kRowsPerPass * a.k);  // [16][k]
@@ -236,17 +252,18 @@ __global__ void __launch_bounds__(kRouterThreads, 1)
         const int row = static_cast<int>(crank) * rows_per_cta + base + rl;
         const int64_t n = n0 + row;
         const bool live = n < a.N;
-        float lg[kMaxPerLane];
+        float lg[PL];
 #pragma unroll
-        for (int j = 0; j < kMaxPerLane; ++j) lg[j] = 0.f;
+        for (int j = 0; j < PL; ++j) lg[j] = 0.f;
         for (int r = 0; r < a.split; ++r) {
-            const uint32_t src = dsmem_addr(&partial[row * ld + 4 * sub], static_cast<uint32_t>(r));
-            float4 t[kMaxPerLane / 4];
+            const float *src = &partial[(r * rows_per_cta + base + rl) * ld + 4 * sub];
+            float4 t[PL / 4];
 #pragma unroll
-            for (int i = 0; i < kMaxPerLane / 4; ++i)
-                if (i < groups && 32 * i + 4 * sub < a.e_pad) t[i] = ld_dsmem_f4(src + 128 * i);
+            for (int i = 0; i < PL / 4; ++i)
+                if (i < groups && 32 * i + 4 * sub < a.e_pad)
+                    t[i] = *reinterpret_cast<const float4 *>(src + 32 * i);
 #pragma unroll
-            for (int i = 0; i < kMaxPerLane / 4; ++i)
+            for (int i = 0; i < PL / 4; ++i)
                 if (i < groups && 32 * i + 4 * sub < a.e_pad) {
                     lg[4 * i + 0] += t[i].x;
                     lg[4 * i + 1] += t[i].y;
@@ -259,24 +276,24 @@ __global__ void __launch_bounds__(kRouterThreads, 1)
             const int jg = 4 * (a.gamma_col / 32) + a.gamma_col % 4;
             float lgate = 0.f;
 #pragma unroll
-            for (int j = 0; j < kMaxPerLane; ++j)
+            for (int j = 0; j < PL; ++j)
                 if (j == jg) lgate = lg[j];
             a.gamma[n] = 1.f / (1.f + expf(-lgate));
         }
 #pragma unroll
-        for (int j = 0; j < kMaxPerLane; ++j) {
+        for (int j = 0; j < PL; ++j) {
             const int e = 32 * (j / 4) + 4 * sub + j % 4;
             lg[j] = e < a.E ? finite_or_neg_inf(lg[j]) : -INFINITY;
         }
         float mx = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < kMaxPerLane; ++j) mx = fmaxf(mx, lg[j]);
+        for (int j = 0; j < PL; ++j) mx = fmaxf(mx, lg[j]);
 #pragma unroll
         for (int d = kLanesPerRow / 2; d > 0; d >>= 1)
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d, kLanesPerRow));
         float den = 0.f;
 #pragma unroll
-        for (int j = 0; j < kMaxPerLane; ++j) {
+        for (int j = 0; j < PL; ++j) {
             const int e = 32 * (j / 4) + 4 * sub + j % 4;
             if (e < a.E) den += expf(lg[j] - mx);
         }
@@ -291,7 +308,7 @@ __global__ void __launch_bounds__(kRouterThreads, 1)
             float bv = -INFINITY;
             int be = -1;
 #pragma unroll
-            for (int j = 0; j < kMaxPerLane; ++j) {
+            for (int j = 0; j < PL; ++j) {
                 const int e = 32 * (j / 4) + 4 * sub + j % 4;
                 if (e < a.E && !((taken >> j) & 1u)) key_max(bv, be, lg[j], e);
             }
@@ -324,7 +341,7 @@ __global__ void __launch_bounds__(kRouterThreads, 1)
         }
         __syncwarp();
     }
-    cluster_sync();  // no CTA leaves while a peer may still read its partial tile
+    __syncthreads();
     if (warp == 0) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, tmem_cols);
@@ -338,6 +355,11 @@ int router_split(int H) {
     return nk >= 8 ? 8 : (nk >= 4 ? 4 : (nk >= 2 ? 2 : 1));
 }
 
+int router_per_lane(int e_pad) {
+    const int pl = (e_pad + kLanesPerRow - 1) / kLanesPerRow;
+    return pl <= 4 ? 4 : (pl <= 16 ? 16 : 32);
+}
+
 size_t router_smem_bytes(int e_pad, int k) {
     const size_t ring = static_cast<size_t>(kRouterStages) * (kATileBytes + e_pad * 128);
     // the partial tile, then the slot results of one 16-row pass
@@ -349,13 +371,14 @@ size_t router_smem_bytes(int e_pad, int k) {
 cudaError_t launch_router(const CUtensorMap &tm_x, const CUtensorMap &tm_router,
                           const CUtensorMap &tm_gate, const RouterArgs &a, cudaStream_t s) {
     const size_t smem = router_smem_bytes(a.e_pad, a.k);
-    cudaError_t err = cudaFuncSetAttribute(router_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const int pl = router_per_lane(a.e_pad);
+    auto kern = pl == 4 ? router_kernel<4> : (pl == 16 ? router_kernel<16> : router_kernel<32>);
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
     const dim3 grid(static_cast<unsigned>(a.split),
                     static_cast<unsigned>((a.N + kBlockM - 1) / kBlockM), 1);
-    return launch_pdl(router_kernel, grid, dim3(kRouterThreads), smem, s,
+    return launch_pdl(kern, grid, dim3(kRouterThreads), smem, s,
                       static_cast<unsigned>(a.split), tm_x, tm_router, tm_gate, a);
 }
 
