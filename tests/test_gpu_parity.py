@@ -162,6 +162,21 @@ def test_forward_edge_shapes(case):
     assert_close(out, ref, name)
 
 
+def test_forward_mixed_sparse_and_dense_row_blocks():
+    """Skewed routing at a small size with top-10: each token takes the 8 hot
+    experts (160 pairs each: one full row block loaded as a tiled box, then a
+    block of exactly 32 rows, gathered) and two of the others (3 to 21 pairs,
+    gathered four rows at a time), all in one call."""
+    shape, dev, bits = prepare(MoEShape("skewed-small", N=160, H=256, E=64, k=10, I=128,
+                                        skew=True), seed=4)
+    out, ws = run_forward(shape, dev)
+    v = binding.workspace_views(ws, shape.N, shape.H, shape.E, shape.I, shape.k)
+    counts = v["counts"].cpu()
+    assert int(counts.max()) > 64 and int(counts[counts > 0].min()) <= 32
+    ref = oracle.moe_forward(bits, shape.k, shape.norm_topk_prob)
+    assert_close(out, ref, shape.name)
+
+
 def test_batch_invariance_skewed():
     """A token computed alone equals the same token inside the skewed batch,
     bit for bit (routing, grouping position and GEMM order do not depend on
