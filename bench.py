@@ -40,8 +40,9 @@ WORKLOADS = {
     "skewed": "skewed-routing stress: N=16384, H=2048, E=128, top-8, I=768, 8 hot experts",
 }
 BOUND = {"tiny": "hbm", "decode": "hbm", "talker": "hbm", "prefill": "tensor", "skewed": "tensor"}
-STAGES = ("route", "align", "gate_up", "down", "shared", "combine")
-SOURCES = {"route": "router.cu", "align": "align.cu", "gate_up": "grouped_gemm.cu",
+STAGES = ("route", "align", "gather", "gate_up", "down", "shared", "combine")
+SOURCES = {"route": "router.cu", "align": "align.cu", "gather": "grouped_gemm.cu",
+           "gate_up": "grouped_gemm.cu",
            "down": "grouped_gemm.cu", "shared": "grouped_gemm.cu", "combine": "combine.cu"}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 
@@ -88,6 +89,7 @@ def algorithmic_work(shape: MoEShape, touched: int):
     b = {
         "route": E * H * 2 + N * H * 2 + P * 8,
         "align": P * 4 + P * 4,
+        "gather": 0,  # x rows copied into expert order: an intermediate, not work
         "gate_up": touched * 2 * I * H * 2 + N * H * 2 + P * I * 2,
         "down": touched * H * I * 2 + P * I * 2 + P * H * 2 + P * 4,
         "shared": (3 * Is * H * 2 + N * H * 2 + 2 * N * Is * 2 + N * H * 2) if Is else 0,
@@ -96,6 +98,7 @@ def algorithmic_work(shape: MoEShape, touched: int):
     f = {
         "route": 2 * N * H * (E + (1 if Is else 0)),
         "align": 0,
+        "gather": 0,
         "gate_up": 4 * H * I * P,
         "down": 2 * H * I * P,
         "shared": 6 * H * Is * N if Is else 0,

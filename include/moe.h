@@ -284,11 +284,12 @@ moe_status_t moe_selftest_wait_timeout(void *workspace, size_t workspace_bytes,
 enum {
     MOE_STAGE_ROUTE = 0,
     MOE_STAGE_ALIGN = 1,
-    MOE_STAGE_GATE_UP = 2,
-    MOE_STAGE_DOWN = 3,
-    MOE_STAGE_SHARED = 4, /* shared expert gate/up + down (empty without one) */
-    MOE_STAGE_COMBINE = 5,
-    MOE_NUM_STAGES = 6
+    MOE_STAGE_GATHER = 2,  /* x rows of full row blocks copied into expert order */
+    MOE_STAGE_GATE_UP = 3,
+    MOE_STAGE_DOWN = 4,
+    MOE_STAGE_SHARED = 5, /* shared expert gate/up + down (empty without one) */
+    MOE_STAGE_COMBINE = 6,
+    MOE_NUM_STAGES = 7
 };
 
 /* Total number of kernels this library has launched in the process. */

@@ -14,8 +14,8 @@ from .build import LIB
 
 MOE_OK = 0
 MOE_BLOCK_M = 128
-MOE_NUM_STAGES = 6
-STAGE_NAMES = ("route", "align", "gate_up", "down", "shared", "combine")
+MOE_NUM_STAGES = 7
+STAGE_NAMES = ("route", "align", "gather", "gate_up", "down", "shared", "combine")
 SHARED_KEYS = ("shared_gate_proj", "shared_up_proj", "shared_down_proj", "shared_gate")
 
 

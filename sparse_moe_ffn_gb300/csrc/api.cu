@@ -463,7 +463,6 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
     if (st != MOE_OK) return st;
 
     // K3: gathered gate/up GEMM + silu * up
-    if ((st = record_stage(MOE_STAGE_GATE_UP, stream)) != MOE_OK) return st;
     CUtensorMap tm_xrows, tm_xsorted, tm_wg, tm_wu, tm_act, tm_act_lo, tm_act_box, tm_act_lo_box,
         tm_wd;
     if ((st = make_map(&tm_xrows, x, H, N, H, kBlockK, 1, "x rows")) != MOE_OK) return st;
@@ -498,8 +497,10 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
         g.max_tiles = static_cast<int>(cap / kBlockM) * nt;
         g.grid = g.max_tiles < sms ? g.max_tiles : sms;
     }
+    if ((st = record_stage(MOE_STAGE_GATHER, stream)) != MOE_OK) return st;
     MOE_CUDA(launch_gather_rows(x, H, k, b.sorted_pair, b.num_padded, P, cap, x_sorted, sms, stream),
              "gather kernel launch");
+    if ((st = record_stage(MOE_STAGE_GATE_UP, stream)) != MOE_OK) return st;
     MOE_CUDA(launch_gemm(kGateUp, bn_gu, tm_xrows, tm_xrows, tm_xsorted, tm_xsorted, tm_wg,
                          tm_wu, g, stream),
              "gate/up kernel launch");

@@ -404,26 +404,47 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // x_sorted[s, :] = x[sorted_pair[s] / k, :] for the real rows s of dense
-// blocks (the A operand of the gate/up GEMM in expert order); one warp per
-// row, 16-byte loads and stores.
-__global__ void __launch_bounds__(256)
+// blocks (the A operand of the gate/up GEMM in expert order).  One CTA per
+// row block (grid-stride): a broadcast load of the block's row kSparseRows
+// decides whether it is dense, so sparse blocks (all of them at decode) cost
+// one load.  Warp w copies rows w, w + 8, ... until the first padding row
+// (real rows come first), four 16-byte loads in flight per lane.  The stores
+// are streaming (evict-first): the GEMM reads each x_sorted row once, while
+// each x row is read k times here and should stay in L2.
+constexpr int kGatherThreads = 256;
+
+__global__ void __launch_bounds__(kGatherThreads)
     gather_rows_kernel(const uint16_t *__restrict__ x, int H, int k,
                        const int32_t *__restrict__ sorted_pair,
                        const int32_t *__restrict__ num_padded, int64_t P, int64_t cap,
                        uint16_t *__restrict__ x_sorted) {
     griddep_launch_dependents();
     griddep_wait();
+    constexpr int kWarps = kGatherThreads / 32;
+    constexpr int kUnroll = 4;
+    const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    const int64_t rows = min(static_cast<int64_t>(__ldcg(num_padded)), cap);
-    for (int64_t s = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32; s < rows;
-         s += static_cast<int64_t>(gridDim.x) * blockDim.x / 32) {
-        const int64_t probe = __ldcg(sorted_pair + s / kBlockM * kBlockM + kSparseRows);
+    const int64_t nblocks = min(static_cast<int64_t>(__ldcg(num_padded)), cap) / kBlockM;
+    const int n16 = H / 8;  // 16-byte pieces per row
+    for (int64_t b = blockIdx.x; b < nblocks; b += gridDim.x) {
+        const int64_t base = b * kBlockM;
+        const int32_t probe = __ldcg(sorted_pair + base + kSparseRows);
         if (probe < 0 || probe >= P) continue;  // sparse block: its rows are gathered by TMA
-        const int64_t q = __ldcg(sorted_pair + s);
-        if (q < 0 || q >= P) continue;          // padding row
-        const uint4 *src = reinterpret_cast<const uint4 *>(x + (q / k) * H);
-        uint4 *dst = reinterpret_cast<uint4 *>(x_sorted + s * H);
-        for (int c = lane; c < H / 8; c += 32) dst[c] = __ldcg(src + c);
+        for (int r = warp; r < kBlockM; r += kWarps) {
+            const int32_t q = __ldcg(sorted_pair + base + r);
+            if (q < 0 || q >= P) break;  // padding from here on
+            const uint4 *src = reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(q / k) * H);
+            uint4 *dst = reinterpret_cast<uint4 *>(x_sorted + (base + r) * H);
+            for (int c0 = lane; c0 < n16; c0 += 32 * kUnroll) {
+                uint4 v[kUnroll];
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u)
+                    if (c0 + 32 * u < n16) v[u] = __ldcg(src + c0 + 32 * u);
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u)
+                    if (c0 + 32 * u < n16) __stcs(dst + c0 + 32 * u, v[u]);
+            }
+        }
     }
 }
 
@@ -432,10 +453,12 @@ __global__ void __launch_bounds__(256)
 cudaError_t launch_gather_rows(const uint16_t *x, int H, int k, const int32_t *sorted_pair,
                                const int32_t *num_padded, int64_t P, int64_t cap,
                                uint16_t *x_sorted, int num_sms, cudaStream_t s) {
-    int64_t blocks = (cap * 32 + 255) / 256;
-    const int64_t limit = static_cast<int64_t>(num_sms) * 8;
+    int64_t blocks = cap / kBlockM;  // one CTA per row block, at most 4 per SM
+    const int64_t limit = static_cast<int64_t>(num_sms) * 4;
     if (blocks > limit) blocks = limit;
-    return launch_pdl(gather_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, 1,
+    if (blocks < 1) blocks = 1;
+    return launch_pdl(gather_rows_kernel, dim3(static_cast<unsigned>(blocks)),
+                      dim3(kGatherThreads), 0, s, 1,
                       x, H, k, sorted_pair, num_padded, P, cap, x_sorted);
 }
 
