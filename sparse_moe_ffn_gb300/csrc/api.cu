@@ -238,6 +238,13 @@ moe_status_t enqueue_align(const int32_t *ids, int64_t N, int k, int E, int bloc
     return MOE_OK;
 }
 
+// The CTA-pair GEMMs pay when experts own at least two row blocks on
+// average (prefill-sized batches): every weight tile then serves 256 rows
+// instead of 128.  Below that, an expert's single block would leave half of
+// every pair idle, and decode-sized batches are bound by streaming weights
+// anyway.
+bool use_pair_tiles(int64_t P, int E) { return P >= 2 * static_cast<int64_t>(kBlockM) * E; }
+
 moe_status_t forward_layout(int64_t N, int H, int E, int I, int k, int I_s,
                             moe_forward_layout_t *L) {
     const int64_t P = N * k;
@@ -475,9 +482,12 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
     if ((st = make_map(&tm_wu, w_up, H, static_cast<uint64_t>(E) * I, H, kBlockK, bn_gu,
                        "w_up")) != MOE_OK)
         return st;
+    const bool pairs = use_pair_tiles(P, E);
     GemmArgs g;
     g.sorted_pair = b.sorted_pair;
     g.block_expert = b.block_expert;
+    g.pad_offsets = b.pad_offsets;
+    g.num_groups = E;
     g.num_padded = b.num_padded;
     g.num_rows_host = cap;
     g.q_limit = P;
@@ -498,12 +508,30 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
         g.grid = g.max_tiles < sms ? g.max_tiles : sms;
     }
     if ((st = record_stage(MOE_STAGE_GATHER, stream)) != MOE_OK) return st;
-    MOE_CUDA(launch_gather_rows(x, H, k, b.sorted_pair, b.num_padded, P, cap, x_sorted, sms, stream),
+    MOE_CUDA(launch_gather_rows(x, H, k, b.sorted_pair, b.num_padded, P, cap, x_sorted,
+                                pairs ? 1 : 0, sms, stream),
              "gather kernel launch");
     if ((st = record_stage(MOE_STAGE_GATE_UP, stream)) != MOE_OK) return st;
-    MOE_CUDA(launch_gemm(kGateUp, bn_gu, tm_xrows, tm_xrows, tm_xsorted, tm_xsorted, tm_wg,
-                         tm_wu, g, stream),
-             "gate/up kernel launch");
+    if (pairs) {
+        const int bn = pair_gemm_block_n(kGateUp);
+        CUtensorMap tm_wg_tile, tm_wu_tile;
+        if ((st = make_map(&tm_wg_tile, w_gate, H, static_cast<uint64_t>(E) * I, H, kBlockK, bn,
+                           "w_gate")) != MOE_OK)
+            return st;
+        if ((st = make_map(&tm_wu_tile, w_up, H, static_cast<uint64_t>(E) * I, H, kBlockK, bn,
+                           "w_up")) != MOE_OK)
+            return st;
+        const int max_pairs = static_cast<int>(cap / kBlockM);  // pairs <= blocks
+        g.max_tiles = max_pairs * ((I + bn - 1) / bn);
+        g.grid = 2 * (g.max_tiles < sms / 2 ? g.max_tiles : sms / 2);
+        MOE_CUDA(launch_pair_gemm(kGateUp, tm_xsorted, tm_xsorted, tm_wg_tile, tm_wu_tile, g,
+                                  stream),
+                 "gate/up kernel launch");
+    } else {
+        MOE_CUDA(launch_gemm(kGateUp, bn_gu, tm_xrows, tm_xrows, tm_xsorted, tm_xsorted, tm_wg,
+                             tm_wu, g, stream),
+                 "gate/up kernel launch");
+    }
     g_launches += 2;
 
     // K4: down GEMM * routing weight, one row per pair
@@ -530,9 +558,22 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
         g.max_tiles = static_cast<int>(cap / kBlockM) * nt;
         g.grid = g.max_tiles < sms ? g.max_tiles : sms;
     }
-    MOE_CUDA(launch_gemm(kDown, kDownBN, tm_act, tm_act_lo, tm_act_box, tm_act_lo_box, tm_wd,
-                         tm_wd, g, stream),
-             "down kernel launch");
+    if (pairs) {
+        const int bn = pair_gemm_block_n(kDown);
+        CUtensorMap tm_wd_half;
+        if ((st = make_map(&tm_wd_half, w_down, I, static_cast<uint64_t>(E) * H, I, kBlockK,
+                           bn / 2, "w_down")) != MOE_OK)
+            return st;
+        g.max_tiles = static_cast<int>(cap / kBlockM) * ((H + bn - 1) / bn);
+        g.grid = 2 * (g.max_tiles < sms / 2 ? g.max_tiles : sms / 2);
+        MOE_CUDA(launch_pair_gemm(kDown, tm_act_box, tm_act_lo_box, tm_wd_half, tm_wd_half, g,
+                                  stream),
+                 "down kernel launch");
+    } else {
+        MOE_CUDA(launch_gemm(kDown, kDownBN, tm_act, tm_act_lo, tm_act_box, tm_act_lo_box, tm_wd,
+                             tm_wd, g, stream),
+                 "down kernel launch");
+    }
     g_launches += 1;
 
     // shared expert: one dense group over all N tokens, weight sigmoid(x . g)
@@ -569,6 +610,8 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
         s.num_rows_host = N;
         s.q_limit = N;
         s.k_div = 1;
+        s.pad_offsets = nullptr;
+        s.num_groups = 0;
         s.K = H;
         s.n_out = I_s;
         s.w_rows = I_s;

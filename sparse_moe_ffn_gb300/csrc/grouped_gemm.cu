@@ -45,6 +45,7 @@
 #include <cuda_bf16.h>
 
 #include "kernels.cuh"
+#include "gemm_common.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -53,11 +54,6 @@ namespace {
 
 constexpr int kMaxStages = 6;
 constexpr int kThreads = 192;
-constexpr int kATileBytes = kBlockM * 128;  // 128 rows x 64 bf16
-constexpr int kAccCols = 256;               // fp32 columns per accumulator
-constexpr uint32_t kTmemCols = 2 * kAccCols;
-constexpr float kF16Max = 65504.f;
-constexpr int kSparseRows = 32;             // blocks with at most this many real rows gather
 
 struct GemmSmem {
     uint64_t full[kMaxStages];
@@ -83,19 +79,6 @@ struct Cfg {
                                       ? (200 * 1024 / STAGE_BYTES) : kMaxStages;
     static_assert(B_TILES * BN <= kAccCols, "accumulator wider than its TMEM slot");
 };
-
-__device__ __forceinline__ float silu_times(float g, float u) {
-    return g / (1.f + __expf(-g)) * u;
-}
-
-// a -> (hi, lo) with hi = bf16(a) and lo = bf16(a - hi), two values at a time
-__device__ __forceinline__ void split_bf16x2(float a0, float a1, uint32_t &hi, uint32_t &lo) {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(a0, a1);
-    const float2 hf = __bfloat1622float2(h);
-    const __nv_bfloat162 l = __floats2bfloat162_rn(a0 - hf.x, a1 - hf.y);
-    hi = *reinterpret_cast<const uint32_t *>(&h);
-    lo = *reinterpret_cast<const uint32_t *>(&l);
-}
 
 template <int MODE, int BN_>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -253,7 +236,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (1 thread)
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, BN);
+            // gate/up: the Wg and Wu tiles sit back to back in shared memory,
+            // so one MMA of N = 2 BN produces [gate | up] in the accumulator
+            constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, MODE == kGateUp ? 2 * BN : BN);
             int g = 0, it = 0;
             bool failed = false;
             for (int tile = blockIdx.x; tile < total_tiles && !failed; tile += gridDim.x, ++it) {
@@ -279,11 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int kk = 0; kk < kBlockK / 16; ++kk) {
                         const uint32_t accumulate = (kc | kk) != 0;
                         mma_bf16(d, da + 2 * kk, db + 2 * kk, idesc, accumulate);
-                        if (MODE == kGateUp) {
-                            const uint64_t db1 =
-                                sw128_kmajor_desc(smem_addr(st + kBOffset + BN * 128));
-                            mma_bf16(d + BN, da + 2 * kk, db1 + 2 * kk, idesc, accumulate);
-                        } else {
+                        if (MODE == kDown) {
                             const uint64_t da_lo = sw128_kmajor_desc(smem_addr(st + kATileBytes));
                             mma_bf16(d, da_lo + 2 * kk, db + 2 * kk, idesc, 1u);
                         }
@@ -318,77 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after_sync();
-            const int blk = tile / n_tiles;
-            const int nt = tile % n_tiles;
-            const int64_t grow = static_cast<int64_t>(blk) * kBlockM + row;
-            const int64_t q = a.sorted_pair ? __ldcg(a.sorted_pair + grow) : grow;
-            const bool valid = q >= 0 && q < a.q_limit;
             const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kAccCols;
-            const int col0 = nt * BN;
-            if (MODE == kGateUp) {
-                uint16_t *dst = a.out + grow * a.out_ld + col0;
-                uint16_t *dst_lo = a.out_lo + grow * a.out_ld + col0;
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    float gv[32], uv[32];
-                    tmem_load32(taddr + c * 32, gv);
-                    tmem_load32(taddr + BN + c * 32, uv);
-                    tmem_load_wait();
-                    if (valid) {
-#pragma unroll
-                        for (int v8 = 0; v8 < 4; ++v8) {
-                            const int col = col0 + c * 32 + v8 * 8;
-                            if (col + 8 <= a.n_out) {
-                                uint32_t hi[4], lo[4];
-#pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    const float a0 = silu_times(gv[v8 * 8 + 2 * i], uv[v8 * 8 + 2 * i]);
-                                    const float a1 = silu_times(gv[v8 * 8 + 2 * i + 1],
-                                                                uv[v8 * 8 + 2 * i + 1]);
-                                    split_bf16x2(a0, a1, hi[i], lo[i]);
-                                }
-                                *reinterpret_cast<uint4 *>(dst + c * 32 + v8 * 8) =
-                                    make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                                *reinterpret_cast<uint4 *>(dst_lo + c * 32 + v8 * 8) =
-                                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                            }
-                        }
-                    }
-                }
-            } else {
-                const float w = !valid ? 0.f : (a.scale ? __ldcg(a.scale + q) : 1.f);
-                uint16_t *dst = a.out + (valid ? q : 0) * a.out_ld + col0;
-                float vmax = 0.f;
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    float yv[32];
-                    tmem_load32(taddr + c * 32, yv);
-                    tmem_load_wait();
-                    if (valid) {
-#pragma unroll
-                        for (int v8 = 0; v8 < 4; ++v8) {
-                            const int col = col0 + c * 32 + v8 * 8;
-                            if (col + 8 <= a.n_out) {
-                                float t[8];
-#pragma unroll
-                                for (int i = 0; i < 8; ++i) {
-                                    t[i] = w * yv[v8 * 8 + i];
-                                    vmax = fmaxf(vmax, fabsf(t[i]));
-                                }
-                                uint4 pk;
-                                pk.x = pack_f16x2(t[0], t[1]);
-                                pk.y = pack_f16x2(t[2], t[3]);
-                                pk.z = pack_f16x2(t[4], t[5]);
-                                pk.w = pack_f16x2(t[6], t[7]);
-                                *reinterpret_cast<uint4 *>(dst + c * 32 + v8 * 8) = pk;
-                            }
-                        }
-                    }
-                }
-                // fp16 keeps 11 significant bits; a value past its range is
-                // reported rather than silently turned into infinity
-                if (!(vmax <= kF16Max)) record_status(a.status, MOE_ERR_DEVICE_CHECK);
-            }
+            store_tile<MODE, BN>(a, taddr, tile / n_tiles, tile % n_tiles, row);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm->acc_empty[acc]);
@@ -404,10 +316,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // x_sorted[s, :] = x[sorted_pair[s] / k, :] for the real rows s of dense
-// blocks (the A operand of the gate/up GEMM in expert order).  One CTA per
-// row block (grid-stride): a broadcast load of the block's row kSparseRows
-// decides whether it is dense, so sparse blocks (all of them at decode) cost
-// one load.  Warp w copies rows w, w + 8, ... until the first padding row
+// blocks, or of every block when all_blocks is set (the CTA-pair kernel loads
+// every block with tiled boxes).  One CTA per row block (grid-stride): a
+// broadcast load of the block's row kSparseRows decides whether it is dense,
+// so sparse blocks (all of them at decode) cost one load.  Warp w copies rows w, w + 8, ... until the first padding row
 // (real rows come first), four 16-byte loads in flight per lane.  The stores
 // are streaming (evict-first): the GEMM reads each x_sorted row once, while
 // each x row is read k times here and should stay in L2.
@@ -417,7 +329,7 @@ __global__ void __launch_bounds__(kGatherThreads)
     gather_rows_kernel(const uint16_t *__restrict__ x, int H, int k,
                        const int32_t *__restrict__ sorted_pair,
                        const int32_t *__restrict__ num_padded, int64_t P, int64_t cap,
-                       uint16_t *__restrict__ x_sorted) {
+                       uint16_t *__restrict__ x_sorted, int all_blocks) {
     griddep_launch_dependents();
     griddep_wait();
     constexpr int kWarps = kGatherThreads / 32;
@@ -428,8 +340,10 @@ __global__ void __launch_bounds__(kGatherThreads)
     const int n16 = H / 8;  // 16-byte pieces per row
     for (int64_t b = blockIdx.x; b < nblocks; b += gridDim.x) {
         const int64_t base = b * kBlockM;
-        const int32_t probe = __ldcg(sorted_pair + base + kSparseRows);
-        if (probe < 0 || probe >= P) continue;  // sparse block: its rows are gathered by TMA
+        if (!all_blocks) {
+            const int32_t probe = __ldcg(sorted_pair + base + kSparseRows);
+            if (probe < 0 || probe >= P) continue;  // sparse block: its rows are gathered by TMA
+        }
         for (int r = warp; r < kBlockM; r += kWarps) {
             const int32_t q = __ldcg(sorted_pair + base + r);
             if (q < 0 || q >= P) break;  // padding from here on
@@ -452,14 +366,14 @@ __global__ void __launch_bounds__(kGatherThreads)
 
 cudaError_t launch_gather_rows(const uint16_t *x, int H, int k, const int32_t *sorted_pair,
                                const int32_t *num_padded, int64_t P, int64_t cap,
-                               uint16_t *x_sorted, int num_sms, cudaStream_t s) {
+                               uint16_t *x_sorted, int all_blocks, int num_sms, cudaStream_t s) {
     int64_t blocks = cap / kBlockM;  // one CTA per row block, at most 4 per SM
     const int64_t limit = static_cast<int64_t>(num_sms) * 4;
     if (blocks > limit) blocks = limit;
     if (blocks < 1) blocks = 1;
     return launch_pdl(gather_rows_kernel, dim3(static_cast<unsigned>(blocks)),
                       dim3(kGatherThreads), 0, s, 1,
-                      x, H, k, sorted_pair, num_padded, P, cap, x_sorted);
+                      x, H, k, sorted_pair, num_padded, P, cap, x_sorted, all_blocks);
 }
 
 template <int MODE, int BN>

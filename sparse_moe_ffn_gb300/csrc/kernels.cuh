@@ -103,6 +103,10 @@ struct GemmArgs {
     const float *scale; // down: per-q weight (null: 1)
     int32_t *status;
     int stream_weights; // weight tiles read once per call: load them evict-first
+    // CTA-pair kernel only: group g (expert) owns padded rows
+    // [pad_offsets[g], pad_offsets[g+1]); null: one group of num_rows_host rows
+    const int32_t *pad_offsets;
+    int num_groups;
     int max_tiles;      // upper bound on tiles (sizes the persistent grid)
     int grid;           // persistent CTAs
 };
@@ -119,10 +123,22 @@ cudaError_t launch_gemm(GemmMode mode, int bn, const CUtensorMap &tm_a,
                         const CUtensorMap &tm_a_lo, const CUtensorMap &tm_a_box,
                         const CUtensorMap &tm_a_lo_box, const CUtensorMap &tm_b0,
                         const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s);
-// x rows of dense blocks copied into expert order (x_sorted [cap, H])
+// x rows copied into expert order (x_sorted [cap, H]): the real rows of dense
+// blocks, or of every block when all_blocks is set
 cudaError_t launch_gather_rows(const uint16_t *x, int H, int k, const int32_t *sorted_pair,
                                const int32_t *num_padded, int64_t P, int64_t cap,
-                               uint16_t *x_sorted, int num_sms, cudaStream_t s);
+                               uint16_t *x_sorted, int all_blocks, int num_sms, cudaStream_t s);
+
+// CTA-pair grouped GEMM (cta_group::2, M = 256 over two row blocks of one
+// group): tm_a / tm_a_lo: 128-row boxes over A rows that are contiguous per
+// block (x_sorted for gate/up; act_hi / act_lo for down); tm_b0 / tm_b1:
+// weight rows, Wg / Wu in boxes of pair_gemm_block_n(kGateUp) rows for
+// gate/up, Wd in boxes of pair_gemm_block_n(kDown) / 2 rows for down.  a.grid
+// must be even (two CTAs per cluster).
+int pair_gemm_block_n(GemmMode mode);
+cudaError_t launch_pair_gemm(GemmMode mode, const CUtensorMap &tm_a, const CUtensorMap &tm_a_lo,
+                             const CUtensorMap &tm_b0, const CUtensorMap &tm_b1,
+                             const GemmArgs &a, cudaStream_t s);
 
 // ----------------------------------------------------------------- combine
 

@@ -149,6 +149,12 @@ EDGE = [
     ("ragged-H-I", 200, 200, 10, 3, 72, 40, True),
     ("wide-E", 256, 128, 256, 8, 64, 0, True),
     ("E248-shared", 64, 64, 248, 4, 32, 16, False),
+    # at least two row blocks per expert: the CTA-pair GEMMs (odd block
+    # counts leave half-empty pairs; ragged H and I give K and N tails)
+    ("pairs-3-blocks", 600, 256, 4, 2, 256, 0, True),
+    ("pairs-ragged-H-I", 700, 200, 5, 3, 200, 0, False),
+    ("pairs-E1-k1", 520, 128, 1, 1, 128, 0, True),
+    ("pairs-shared", 600, 128, 4, 2, 128, 64, True),
 ]
 
 
