@@ -212,14 +212,25 @@ __global__ void __launch_bounds__(kScanThreads)
     for (int i = threadIdx.x; i < (kScanThreads / 32) * kSmallMaxE; i += blockDim.x)
         (&warp_cnt[0][0])[i] = 0;
     __syncthreads();
+    // each thread keeps its (at most kSmallPairs / kScanThreads) ids in
+    // registers for the scatter below: one round trip to memory, not two
+    constexpr int kPerThread = kSmallPairs / kScanThreads;
+    int my_e[kPerThread];
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) {
+        const int64_t p = threadIdx.x + static_cast<int64_t>(i) * kScanThreads;
+        my_e[i] = p < P ? __ldcg(ids + p) : -1;
+    }
     bool bad = false;
-    for (int64_t p = threadIdx.x; p < P; p += blockDim.x) {
-        const int e = __ldcg(ids + p);
-        if (e < 0 || e >= E) {
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) {
+        const int64_t p = threadIdx.x + static_cast<int64_t>(i) * kScanThreads;
+        if (p >= P) continue;
+        if (my_e[i] < 0 || my_e[i] >= E) {
             bad = true;
             continue;
         }
-        atomicAdd(&hist[e], 1);
+        atomicAdd(&hist[my_e[i]], 1);
     }
     if (bad) record_status(status, MOE_ERR_DEVICE_CHECK);
     __syncthreads();
@@ -245,9 +256,12 @@ __global__ void __launch_bounds__(kScanThreads)
     fill_padded(pad_smem, E, block_m, npad, P, sorted_pair, block_expert);
     __syncthreads();  // sentinels first, then the real pairs over them
     const uint32_t lanes_below = (1u << lane) - 1u;
-    for (int64_t base = 0; base < P; base += blockDim.x) {
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) {
+        const int64_t base = static_cast<int64_t>(i) * kScanThreads;
+        if (base >= P) break;  // uniform across the CTA
         const int64_t p = base + threadIdx.x;
-        const int pe = p < P ? __ldcg(ids + p) : -1;
+        const int pe = p < P ? my_e[i] : -1;
         const bool valid = pe >= 0 && pe < E;
         const uint32_t peers = __match_any_sync(0xffffffffu, valid ? pe : E + lane);
         const int rank_in_warp = __popc(peers & lanes_below);

@@ -245,6 +245,11 @@ moe_status_t enqueue_align(const int32_t *ids, int64_t N, int k, int E, int bloc
 // anyway.
 bool use_pair_tiles(int64_t P, int E) { return P >= 2 * static_cast<int64_t>(kBlockM) * E; }
 
+// Fewer than 32 pairs per expert on average (decode-sized batches): most row
+// blocks hold a handful of real rows, and the GEMMs that stage activation
+// rows in 32-row passes keep more weight bytes in flight.
+bool use_sparse_tiles(int64_t P, int E) { return P < 32 * static_cast<int64_t>(E); }
+
 moe_status_t forward_layout(int64_t N, int H, int E, int I, int k, int I_s,
                             moe_forward_layout_t *L) {
     const int64_t P = N * k;
@@ -483,6 +488,7 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
                        "w_up")) != MOE_OK)
         return st;
     const bool pairs = use_pair_tiles(P, E);
+    const bool sparse = !pairs && use_sparse_tiles(P, E);
     GemmArgs g;
     g.sorted_pair = b.sorted_pair;
     g.block_expert = b.block_expert;
@@ -508,11 +514,17 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
         g.grid = g.max_tiles < sms ? g.max_tiles : sms;
     }
     if ((st = record_stage(MOE_STAGE_GATHER, stream)) != MOE_OK) return st;
-    MOE_CUDA(launch_gather_rows(x, H, k, b.sorted_pair, b.num_padded, P, cap, x_sorted,
-                                pairs ? 1 : 0, sms, stream),
-             "gather kernel launch");
+    if (!sparse) {  // the sparse GEMM gathers its x rows itself
+        MOE_CUDA(launch_gather_rows(x, H, k, b.sorted_pair, b.num_padded, P, cap, x_sorted,
+                                    pairs ? 1 : 0, sms, stream),
+                 "gather kernel launch");
+        g_launches += 1;
+    }
     if ((st = record_stage(MOE_STAGE_GATE_UP, stream)) != MOE_OK) return st;
-    if (pairs) {
+    if (sparse) {
+        MOE_CUDA(launch_sparse_gemm(kGateUp, bn_gu, tm_xrows, tm_xrows, tm_wg, tm_wu, g, stream),
+                 "gate/up kernel launch");
+    } else if (pairs) {
         const int bn = pair_gemm_block_n(kGateUp);
         CUtensorMap tm_wg_tile, tm_wu_tile;
         if ((st = make_map(&tm_wg_tile, w_gate, H, static_cast<uint64_t>(E) * I, H, kBlockK, bn,
@@ -532,7 +544,7 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
                              tm_wu, g, stream),
                  "gate/up kernel launch");
     }
-    g_launches += 2;
+    g_launches += 1;
 
     // K4: down GEMM * routing weight, one row per pair
     if ((st = record_stage(MOE_STAGE_DOWN, stream)) != MOE_OK) return st;
@@ -558,7 +570,10 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
         g.max_tiles = static_cast<int>(cap / kBlockM) * nt;
         g.grid = g.max_tiles < sms ? g.max_tiles : sms;
     }
-    if (pairs) {
+    if (sparse) {
+        MOE_CUDA(launch_sparse_gemm(kDown, kDownBN, tm_act, tm_act_lo, tm_wd, tm_wd, g, stream),
+                 "down kernel launch");
+    } else if (pairs) {
         const int bn = pair_gemm_block_n(kDown);
         CUtensorMap tm_wd_half;
         if ((st = make_map(&tm_wd_half, w_down, I, static_cast<uint64_t>(E) * H, I, kBlockK,

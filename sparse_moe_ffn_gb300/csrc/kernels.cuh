@@ -136,6 +136,15 @@ cudaError_t launch_gather_rows(const uint16_t *x, int H, int k, const int32_t *s
 // gate/up, Wd in boxes of pair_gemm_block_n(kDown) / 2 rows for down.  a.grid
 // must be even (two CTAs per cluster).
 int pair_gemm_block_n(GemmMode mode);
+
+// Grouped GEMM for blocks holding few real rows (decode): activation rows in
+// 32-row passes, gathered with tile::gather4 (tm_a / tm_a_lo: 1-row boxes of
+// x rows for gate/up, act_hi / act_lo rows for down), more weight stages in
+// flight; tm_b0 / tm_b1 as for launch_gemm (boxes of bn rows).  Needs the
+// routed block list (sorted_pair, block_expert, num_padded).
+cudaError_t launch_sparse_gemm(GemmMode mode, int bn, const CUtensorMap &tm_a,
+                               const CUtensorMap &tm_a_lo, const CUtensorMap &tm_b0,
+                               const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s);
 cudaError_t launch_pair_gemm(GemmMode mode, const CUtensorMap &tm_a, const CUtensorMap &tm_a_lo,
                              const CUtensorMap &tm_b0, const CUtensorMap &tm_b1,
                              const GemmArgs &a, cudaStream_t s);

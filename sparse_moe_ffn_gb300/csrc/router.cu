@@ -217,8 +217,12 @@ __global__ void __launch_bounds__(kRouterThreads, 1)
     const int rows_per_cta = kBlockM / a.split;
     // every ring of the cluster is idle before any CTA writes into a peer's
     cluster_sync();
-    {
+    // a warp whose 32 token rows are all past N skips the push; inside a
+    // warp the TMEM loads stay warp-wide (tcgen05.ld is a .sync.aligned
+    // collective) and only the stores of rows past N are dropped
+    if (n0 + warp * 32 < a.N) {
         const int row = warp * 32 + lane;  // TMEM lane
+        const bool live_row = n0 + row < a.N;
         const uint32_t owner = static_cast<uint32_t>(row / rows_per_cta);
         const int slot = static_cast<int>(crank) * rows_per_cta + row % rows_per_cta;
         const uint32_t dst = dsmem_addr(&partial[slot * ld], owner);
@@ -229,7 +233,7 @@ __global__ void __launch_bounds__(kRouterThreads, 1)
             tmem_load_wait();
 #pragma unroll
             for (int i = 0; i < 32; i += 4)
-                if (c * 32 + i < a.e_pad)
+                if (live_row && c * 32 + i < a.e_pad)
                     st_dsmem_f4(dst + 4 * (c * 32 + i),
                                 ok ? make_float4(v[i], v[i + 1], v[i + 2], v[i + 3])
                                    : make_float4(0.f, 0.f, 0.f, 0.f));
@@ -248,6 +252,8 @@ __global__ void __launch_bounds__(kRouterThreads, 1)
     float *slot_w = partial + kBlockM * ld;                              // [16][k]
     int32_t *slot_e = reinterpret_cast<int32_t *>(slot_w + kRowsPerPass * a.k);  // [16][k]
     for (int base = 0; base < rows_per_cta; base += kRowsPerPass) {
+        // rows are consecutive tokens: a pass that starts past N has no live row
+        if (n0 + static_cast<int>(crank) * rows_per_cta + base >= a.N) break;
         const int rl = warp * (32 / kLanesPerRow) + lane / kLanesPerRow;  // row in pass
         const int row = static_cast<int>(crank) * rows_per_cta + base + rl;
         const int64_t n = n0 + row;
@@ -291,15 +297,18 @@ __global__ void __launch_bounds__(kRouterThreads, 1)
 #pragma unroll
         for (int d = kLanesPerRow / 2; d > 0; d >>= 1)
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d, kLanesPerRow));
+        // fast exponentials: their relative error (~1e-6 over the logit
+        // range of a softmax) is far below the weights' fp32 budget
         float den = 0.f;
 #pragma unroll
         for (int j = 0; j < PL; ++j) {
             const int e = 32 * (j / 4) + 4 * sub + j % 4;
-            if (e < a.E) den += expf(lg[j] - mx);
+            if (e < a.E) den += __expf(lg[j] - mx);
         }
 #pragma unroll
         for (int d = kLanesPerRow / 2; d > 0; d >>= 1)
             den += __shfl_xor_sync(0xffffffffu, den, d, kLanesPerRow);
+        const float inv_den = 1.f / den;
         // k arg-max rounds; exp is monotone, so this is the top-k of the
         // probabilities
         uint32_t taken = 0;
@@ -319,7 +328,7 @@ __global__ void __launch_bounds__(kRouterThreads, 1)
                 key_max(bv, be, ov, oe);
             }
             if ((be % 32) / 4 == sub) taken |= 1u << (4 * (be / 32) + be % 4);
-            const float p = expf(bv - mx) / den;
+            const float p = __expf(bv - mx) * inv_den;
             wsum += p;
             if (sub == 0) {
                 slot_w[rl * a.k + r] = p;

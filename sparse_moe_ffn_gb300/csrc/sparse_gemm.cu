@@ -1,0 +1,401 @@
+// sparse_gemm.cu -- K3 (gate/up) and K4 (down) for batches whose row blocks
+// hold only a few real rows each (decode: N·k pairs spread over many
+// experts).  Same arithmetic per output element as the other grouped GEMMs
+// (same K order, same epilogue: store_tile in gemm_common.cuh); only the
+// staging differs.
+//
+// Such a GEMM streams every weight tile once and is bound by how many weight
+// bytes each SM keeps in flight.  The activation rows of a block are loaded
+// as 32-row sub-blocks into a 4 KB region per operand (instead of a 16 KB
+// 128-row tile), which leaves room for more weight stages:
+//   gate/up BN = 96: 4 KB + 24 KB per stage, 7 stages (168 KB of weights);
+//   gate/up BN = 128: 4 KB + 32 KB, 5 stages (160 KB);
+//   down BN = 256: 4 + 4 KB + 32 KB, 5 stages (160 KB; 96 KB with 128-row
+//   activation tiles).
+// The MMA is still M = 128: its A operand spans 16 KB from the region's
+// start, so rows 32-127 read whatever follows in the stage; they only feed
+// accumulator rows 32-127, which the epilogue never stores (and TMEM lanes
+// 0-31 belong to the first epilogue warp alone).  A block with more than 32
+// real rows is computed as several 32-row passes over K (rare at decode);
+// real rows come first in a block, so a block with n real rows takes
+// ceil(n / 32) passes.
+//
+// The producer publishes each tile's pass count through a small ring of
+// shared-memory words (full/empty barriers per slot), so that the MMA issuer
+// and the epilogue never wait on a global load.  The next tile's row map
+// and expert are loaded while the current tile's stages are issued.
+//
+// Roles: warp 0 TMA producer (gather4 of the sub-block's real rows, lane 0
+// the weight tile(s)); warp 1 TMEM allocation and MMA issuer; warps 2-5
+// epilogue (warp 4, which owns TMEM lanes 0-31, stores; the others only
+// release the accumulator).  Every wait is bounded.
+#include <cuda_bf16.h>
+
+#include "gemm_common.cuh"
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kSubRows = kSparseRows;          // rows per pass
+constexpr int kSubTileBytes = kSubRows * 128;  // 32 rows x 64 bf16
+constexpr int kSparseMaxStages = 8;
+constexpr int kSparseThreads = 192;
+constexpr int kInfoSlots = 4;
+constexpr int kInfoReaders = 1 + 4;  // MMA warp + four epilogue warps
+
+template <int MODE, int BN_>
+struct SparseCfg {
+    static constexpr int BN = BN_;
+    static constexpr int A_TILES = MODE == kGateUp ? 1 : 2;
+    static constexpr int B_BYTES = (MODE == kGateUp ? 2 : 1) * BN * 128;
+    static constexpr int STAGE_BYTES = A_TILES * kSubTileBytes + B_BYTES;
+    static constexpr int STAGES = (200 * 1024 / STAGE_BYTES) < kSparseMaxStages
+                                      ? (200 * 1024 / STAGE_BYTES) : kSparseMaxStages;
+    // the MMA reads a 16 KB (128-row) A operand from each A region
+    static_assert(STAGE_BYTES >= (A_TILES - 1) * kSubTileBytes + kATileBytes,
+                  "a 128-row A read would leave the stage");
+    static_assert((MODE == kGateUp ? 2 : 1) * BN <= kAccCols, "accumulator too wide");
+};
+
+struct SparseSmem {
+    uint64_t full[kSparseMaxStages];
+    uint64_t empty[kSparseMaxStages];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t info_full[kInfoSlots];
+    uint64_t info_empty[kInfoSlots];
+    uint64_t drain;
+    int info[kInfoSlots];
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+// Consumer side of the tile-info ring: the pass count of local tile j
+// (warp-wide; -1 when the wait gave up).
+__device__ __forceinline__ int read_passes(SparseSmem *sm, int j, int lane,
+                                           volatile int *abort_flag) {
+    int n = -1;
+    if (lane == 0) {
+        const int slot = j % kInfoSlots;
+        if (mbar_wait(&sm->info_full[slot], (j / kInfoSlots) & 1, abort_flag)) {
+            n = *reinterpret_cast<volatile int *>(&sm->info[slot]);
+            mbar_arrive(&sm->info_empty[slot]);
+        }
+    }
+    return __shfl_sync(0xffffffffu, n, 0);
+}
+
+template <int MODE, int BN_>
+__global__ void __launch_bounds__(kSparseThreads, 1)
+    sparse_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
+                       const __grid_constant__ CUtensorMap tm_a_lo,
+                       const __grid_constant__ CUtensorMap tm_b0,
+                       const __grid_constant__ CUtensorMap tm_b1, const GemmArgs a) {
+    using C = SparseCfg<MODE, BN_>;
+    constexpr int BN = C::BN;
+    constexpr int kStages = C::STAGES;
+    constexpr int kStageBytes = C::STAGE_BYTES;
+    constexpr int kBOffset = C::A_TILES * kSubTileBytes;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *tiles = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    SparseSmem *sm = reinterpret_cast<SparseSmem *>(tiles + kStages * kStageBytes);
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&sm->full[s], 1);
+            mbar_init(&sm->empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm->acc_full[i], 1);
+            mbar_init(&sm->acc_empty[i], 4);
+        }
+        for (int i = 0; i < kInfoSlots; ++i) {
+            mbar_init(&sm->info_full[i], 1);
+            mbar_init(&sm->info_empty[i], kInfoReaders);
+        }
+        mbar_init(&sm->drain, 1);
+        sm->abort_flag = 0;
+        fence_barrier_init();
+        prefetch_tensor_map(&tm_a);
+        if (MODE == kDown) prefetch_tensor_map(&tm_a_lo);
+        prefetch_tensor_map(&tm_b0);
+        if (MODE == kGateUp) prefetch_tensor_map(&tm_b1);
+    }
+    if (warp == 1) {
+        tmem_alloc(&sm->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = sm->tmem_base;
+    volatile int *abort_flag = &sm->abort_flag;
+    griddep_launch_dependents();
+    griddep_wait();  // the block list and the A rows come from earlier kernels
+
+    const int64_t rows = static_cast<int64_t>(__ldcg(a.num_padded));
+    const int num_blocks = static_cast<int>((rows + kBlockM - 1) / kBlockM);
+    const int n_tiles = (a.n_out + BN - 1) / BN;
+    const int total_tiles = min(num_blocks * n_tiles, a.max_tiles);
+    const int nk = (a.K + kBlockK - 1) / kBlockK;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (warp)
+        const uint64_t wpol = a.stream_weights ? l2_policy_evict_first() : 0;
+        int g = 0;
+        bool failed = false;
+        // lane l holds rows 4l .. 4l+3 of a block; the next tile's are loaded
+        // while this tile's stages are issued and compared only then
+        int32_t q_next[4] = {-1, -1, -1, -1};
+        int expert_next = 0;
+        if (static_cast<int>(blockIdx.x) < total_tiles) {
+            const int64_t base = static_cast<int64_t>(blockIdx.x / n_tiles) * kBlockM;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) q_next[i] = __ldcg(a.sorted_pair + base + lane * 4 + i);
+            expert_next = __ldcg(a.block_expert + blockIdx.x / n_tiles);
+        }
+        for (int tile = blockIdx.x, j = 0; tile < total_tiles && !failed;
+             tile += gridDim.x, ++j) {
+            const int blk = tile / n_tiles;
+            const int nt = tile % n_tiles;
+            int src[4];
+            bool any = false;
+            int last = 0;  // 1 + highest real row of the block
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int32_t q = q_next[i];
+                const bool v = q >= 0 && q < a.q_limit;
+                src[i] = !v ? -1 : (MODE == kGateUp ? static_cast<int>(q / a.k_div)
+                                                    : blk * kBlockM + lane * 4 + i);
+                any |= v;
+                if (v) last = lane * 4 + i + 1;
+            }
+            const int expert = expert_next;
+            const int next = tile + static_cast<int>(gridDim.x);
+            if (next < total_tiles) {
+                const int64_t base = static_cast<int64_t>(next / n_tiles) * kBlockM;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) q_next[i] = __ldcg(a.sorted_pair + base + lane * 4 + i);
+                expert_next = __ldcg(a.block_expert + next / n_tiles);
+            }
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, d));
+            const int passes = (last + kSubRows - 1) / kSubRows;
+            {
+                bool ok = true;
+                if (lane == 0) {
+                    const int slot = j % kInfoSlots;
+                    if (j >= kInfoSlots)
+                        ok = mbar_wait(&sm->info_empty[slot], ((j / kInfoSlots) - 1) & 1, abort_flag);
+                    if (ok) {
+                        sm->info[slot] = passes;
+                        mbar_arrive(&sm->info_full[slot]);
+                    }
+                }
+                if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                    if (lane == 0) {
+                        record_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
+                        *abort_flag = 1;
+                    }
+                    failed = true;
+                    break;
+                }
+            }
+            // a lane's 4 rows sit in sub-block lane / 8; padding rows copy a
+            // real row of the same group (their results are dropped)
+            int first_valid = -1;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (src[i] >= 0 && first_valid < 0) first_valid = src[i];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (src[i] < 0) src[i] = first_valid;
+            const int brow = static_cast<int>(static_cast<int64_t>(expert) * a.w_rows) + nt * BN;
+            for (int p = 0; p < passes && !failed; ++p) {
+                const bool mine = lane / 8 == p && any;  // lanes 8p .. 8p+7 gather pass p
+                const uint32_t groups = __popc(__ballot_sync(0xffffffffu, mine));
+                const uint32_t tx = C::A_TILES * groups * 512 + C::B_BYTES;
+                for (int kc = 0; kc < nk; ++kc, ++g) {
+                    const int s = g % kStages;
+                    const uint32_t use = g / kStages;
+                    bool ok = true;
+                    if (lane == 0 && use > 0) ok = mbar_wait(&sm->empty[s], (use - 1) & 1, abort_flag);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) {
+                        if (lane == 0) {
+                            record_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
+                            *abort_flag = 1;
+                        }
+                        failed = true;
+                        break;
+                    }
+                    uint8_t *st = tiles + s * kStageBytes;
+                    if (lane == 0) mbar_arrive_expect_tx(&sm->full[s], tx);
+                    __syncwarp();
+                    if (mine) {
+                        const int slot = lane % 8;
+                        tma_gather4(st + slot * 512, &tm_a, &sm->full[s], kc * kBlockK, src[0],
+                                    src[1], src[2], src[3]);
+                        if (MODE == kDown)
+                            tma_gather4(st + kSubTileBytes + slot * 512, &tm_a_lo, &sm->full[s],
+                                        kc * kBlockK, src[0], src[1], src[2], src[3]);
+                    }
+                    if (lane == 0) {
+                        if (a.stream_weights) {
+                            tma_load_2d_hint(st + kBOffset, &tm_b0, &sm->full[s], kc * kBlockK,
+                                             brow, wpol);
+                            if (MODE == kGateUp)
+                                tma_load_2d_hint(st + kBOffset + BN * 128, &tm_b1, &sm->full[s],
+                                                 kc * kBlockK, brow, wpol);
+                        } else {
+                            tma_load_2d(st + kBOffset, &tm_b0, &sm->full[s], kc * kBlockK, brow);
+                            if (MODE == kGateUp)
+                                tma_load_2d(st + kBOffset + BN * 128, &tm_b1, &sm->full[s],
+                                            kc * kBlockK, brow);
+                        }
+                    }
+                }
+            }
+        }
+        if (lane == 0)
+            for (int i = (g > kStages ? g - kStages : 0); i < g; ++i)
+                mbar_wait(&sm->full[i % kStages], (i / kStages) & 1, abort_flag);
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (1 thread)
+        // gate/up: Wg and Wu tiles are adjacent, one MMA of N = 2 BN
+        constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, MODE == kGateUp ? 2 * BN : BN);
+        int g = 0, it = 0;
+        bool failed = false;
+        for (int tile = blockIdx.x, j = 0; tile < total_tiles && !failed; tile += gridDim.x, ++j) {
+            const int passes = read_passes(sm, j, lane, abort_flag);
+            if (passes < 0) {
+                failed = true;
+                break;
+            }
+            for (int p = 0; p < passes && !failed; ++p, ++it) {
+                if (lane == 0) {
+                    const int acc = it & 1;
+                    const uint32_t use = it >> 1;
+                    if (use > 0 && !mbar_wait(&sm->acc_empty[acc], (use - 1) & 1, abort_flag)) {
+                        failed = true;
+                    } else {
+                        tc_fence_after_sync();
+                        const uint32_t d = tmem + acc * kAccCols;
+                        for (int kc = 0; kc < nk; ++kc, ++g) {
+                            const int s = g % kStages;
+                            if (!mbar_wait(&sm->full[s], (g / kStages) & 1, abort_flag)) {
+                                failed = true;
+                                break;
+                            }
+                            tc_fence_after_sync();
+                            const uint8_t *st = tiles + s * kStageBytes;
+                            const uint64_t da = sw128_kmajor_desc(smem_addr(st));
+                            const uint64_t db = sw128_kmajor_desc(smem_addr(st + kBOffset));
+#pragma unroll
+                            for (int kk = 0; kk < kBlockK / 16; ++kk) {
+                                mma_bf16(d, da + 2 * kk, db + 2 * kk, idesc, (kc | kk) != 0);
+                                if (MODE == kDown) {
+                                    const uint64_t da_lo =
+                                        sw128_kmajor_desc(smem_addr(st + kSubTileBytes));
+                                    mma_bf16(d, da_lo + 2 * kk, db + 2 * kk, idesc, 1u);
+                                }
+                            }
+                            mma_commit(&sm->empty[s]);
+                        }
+                        if (!failed) mma_commit(&sm->acc_full[acc]);
+                    }
+                }
+                failed = __shfl_sync(0xffffffffu, failed, 0);
+            }
+        }
+        if (lane == 0) {
+            if (failed) {
+                record_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
+                *abort_flag = 1;
+            }
+            mma_commit(&sm->drain);
+            mbar_wait(&sm->drain, 0, abort_flag);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue (4 warps)
+        const int quarter = warp % 4;  // warp 4 owns TMEM lanes 0-31
+        int it = 0;
+        bool failed = false;
+        for (int tile = blockIdx.x, j = 0; tile < total_tiles && !failed; tile += gridDim.x, ++j) {
+            const int passes = read_passes(sm, j, lane, abort_flag);
+            if (passes < 0) {
+                if (lane == 0) {
+                    record_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            for (int p = 0; p < passes; ++p, ++it) {
+                const int acc = it & 1;
+                bool ok = true;
+                if (lane == 0) ok = mbar_wait(&sm->acc_full[acc], (it >> 1) & 1, abort_flag);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) {
+                    if (lane == 0) {
+                        record_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
+                        *abort_flag = 1;
+                    }
+                    failed = true;
+                    break;
+                }
+                tc_fence_after_sync();
+                if (quarter == 0)
+                    store_tile<MODE, BN>(a, tmem + acc * kAccCols, tile / n_tiles, tile % n_tiles,
+                                         p * kSubRows + lane);
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm->acc_empty[acc]);
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int MODE, int BN>
+cudaError_t launch_sparse_one(const CUtensorMap &tm_a, const CUtensorMap &tm_a_lo,
+                              const CUtensorMap &tm_b0, const CUtensorMap &tm_b1,
+                              const GemmArgs &a, cudaStream_t s) {
+    using C = SparseCfg<MODE, BN>;
+    const size_t smem = 1024 + static_cast<size_t>(C::STAGES) * C::STAGE_BYTES + sizeof(SparseSmem);
+    auto kern = sparse_gemm_kernel<MODE, BN>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    return launch_pdl(kern, dim3(a.grid), dim3(kSparseThreads), smem, s, 1, tm_a, tm_a_lo, tm_b0,
+                      tm_b1, a);
+}
+
+}  // namespace
+
+cudaError_t launch_sparse_gemm(GemmMode mode, int bn, const CUtensorMap &tm_a,
+                               const CUtensorMap &tm_a_lo, const CUtensorMap &tm_b0,
+                               const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s) {
+    if (!a.sorted_pair || !a.block_expert || !a.num_padded) return cudaErrorInvalidValue;
+    if (mode == kGateUp && bn == 96) return launch_sparse_one<kGateUp, 96>(tm_a, tm_a_lo, tm_b0, tm_b1, a, s);
+    if (mode == kGateUp && bn == 128)
+        return launch_sparse_one<kGateUp, 128>(tm_a, tm_a_lo, tm_b0, tm_b1, a, s);
+    if (mode == kDown && bn == 256) return launch_sparse_one<kDown, 256>(tm_a, tm_a_lo, tm_b0, tm_b1, a, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

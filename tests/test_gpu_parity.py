@@ -149,6 +149,9 @@ EDGE = [
     ("ragged-H-I", 200, 200, 10, 3, 72, 40, True),
     ("wide-E", 256, 128, 256, 8, 64, 0, True),
     ("E248-shared", 64, 64, 248, 4, 32, 16, False),
+    # fewer than 32 pairs per expert: the GEMMs with 32-row activation
+    # passes (K tails in both GEMMs, a partial N tile)
+    ("sparse-ragged-H-I", 40, 200, 32, 4, 72, 0, True),
     # at least two row blocks per expert: the CTA-pair GEMMs (odd block
     # counts leave half-empty pairs; ragged H and I give K and N tails)
     ("pairs-3-blocks", 600, 256, 4, 2, 256, 0, True),
