@@ -310,24 +310,39 @@ __global__ void __launch_bounds__(kRouterThreads, 1)
             den += __shfl_xor_sync(0xffffffffu, den, d, kLanesPerRow);
         const float inv_den = 1.f / den;
         // k arg-max rounds; exp is monotone, so this is the top-k of the
-        // probabilities
-        uint32_t taken = 0;
+        // probabilities.  A lane's candidates are reduced as a tournament
+        // (log2(PL) levels of key_max instead of a PL-long dependent chain);
+        // a selected expert's index becomes -1, so it never wins again.
+        int le[PL];
+#pragma unroll
+        for (int j = 0; j < PL; ++j) {
+            const int e = 32 * (j / 4) + 4 * sub + j % 4;
+            le[j] = e < a.E ? e : -1;
+        }
         float wsum = 0.f;
         for (int r = 0; r < a.k; ++r) {
-            float bv = -INFINITY;
-            int be = -1;
+            float tv[PL];
+            int te[PL];
 #pragma unroll
             for (int j = 0; j < PL; ++j) {
-                const int e = 32 * (j / 4) + 4 * sub + j % 4;
-                if (e < a.E && !((taken >> j) & 1u)) key_max(bv, be, lg[j], e);
+                tv[j] = lg[j];
+                te[j] = le[j];
             }
+#pragma unroll
+            for (int w = PL / 2; w > 0; w >>= 1)
+#pragma unroll
+                for (int j = 0; j < w; ++j) key_max(tv[j], te[j], tv[j + w], te[j + w]);
+            float bv = tv[0];
+            int be = te[0];
 #pragma unroll
             for (int d = kLanesPerRow / 2; d > 0; d >>= 1) {
                 const float ov = __shfl_xor_sync(0xffffffffu, bv, d, kLanesPerRow);
                 const int oe = __shfl_xor_sync(0xffffffffu, be, d, kLanesPerRow);
                 key_max(bv, be, ov, oe);
             }
-            if ((be % 32) / 4 == sub) taken |= 1u << (4 * (be / 32) + be % 4);
+#pragma unroll
+            for (int j = 0; j < PL; ++j)
+                if (le[j] == be) le[j] = -1;
             const float p = __expf(bv - mx) * inv_den;
             wsum += p;
             if (sub == 0) {
