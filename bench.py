@@ -41,9 +41,12 @@ WORKLOADS = {
 }
 BOUND = {"tiny": "hbm", "decode": "hbm", "talker": "hbm", "prefill": "tensor", "skewed": "tensor"}
 STAGES = ("route", "align", "gather", "gate_up", "down", "shared", "combine")
-SOURCES = {"route": "router.cu", "align": "align.cu", "gather": "grouped_gemm.cu",
-           "gate_up": "grouped_gemm.cu",
-           "down": "grouped_gemm.cu", "shared": "grouped_gemm.cu", "combine": "combine.cu"}
+# kernel sources behind each stage (the GEMM stages run the one-CTA, the
+# sparse-block or the CTA-pair kernel depending on the batch)
+GEMM_SOURCES = ("grouped_gemm.cu", "sparse_gemm.cu", "pair_gemm.cu", "gemm_common.cuh")
+SOURCES = {"route": ("router.cu",), "align": ("align.cu",), "gather": ("grouped_gemm.cu",),
+           "gate_up": GEMM_SOURCES, "down": GEMM_SOURCES, "shared": GEMM_SOURCES,
+           "combine": ("combine.cu",)}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 
 
@@ -61,7 +64,7 @@ def load_peaks():
 
 def source_hash(stage):
     h = hashlib.sha256()
-    for f in sorted({SOURCES[stage], "ptx.cuh", "kernels.cuh"}):
+    for f in sorted({*SOURCES[stage], "ptx.cuh", "kernels.cuh"}):
         with open(os.path.join(ROOT, "sparse_moe_ffn_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
