@@ -42,13 +42,22 @@ __global__ void __launch_bounds__(kAlignThreads)
     const int64_t start = static_cast<int64_t>(blockIdx.x) * chunk;
     const int64_t end = min(P, start + chunk);
     bool bad = false;
-    for (int64_t p = start + threadIdx.x; p < end; p += blockDim.x) {
-        const int e = __ldcg(ids + p);
-        if (e < 0 || e >= E) {
+    constexpr int kPerThread = kAlignChunk / kAlignThreads;
+    int my_e[kPerThread];
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) {  // every load in flight at once
+        const int64_t p = start + threadIdx.x + static_cast<int64_t>(i) * kAlignThreads;
+        my_e[i] = p < end ? __ldcg(ids + p) : 0;
+    }
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) {
+        const int64_t p = start + threadIdx.x + static_cast<int64_t>(i) * kAlignThreads;
+        if (p >= end) continue;
+        if (my_e[i] < 0 || my_e[i] >= E) {
             bad = true;
             continue;
         }
-        atomicAdd(&hist[e], 1);  // a count: order-free, exact
+        atomicAdd(&hist[my_e[i]], 1);  // a count: order-free, exact
     }
     if (bad) record_status(status, MOE_ERR_DEVICE_CHECK);
     __syncthreads();
@@ -116,12 +125,22 @@ __global__ void __launch_bounds__(kScanThreads)
     const int e = threadIdx.x;
     int32_t cnt = 0;
     if (e < E) {
-        // per-expert exclusive scan over chunks, in place: count -> base
-        for (int c = 0; c < nchunks; ++c) {
-            int32_t *slot = chunk_counts + static_cast<int64_t>(c) * E + e;
-            const int32_t v = __ldcg(slot);
-            *slot = cnt;
-            cnt += v;
+        // per-expert exclusive scan over chunks, in place: count -> base.
+        // kBatch independent loads are issued before their stores, so the
+        // chunks cost nchunks / kBatch round trips to L2, not nchunks
+        constexpr int kBatch = 16;
+        for (int c0 = 0; c0 < nchunks; c0 += kBatch) {
+            int32_t v[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u)
+                v[u] = c0 + u < nchunks ? __ldcg(chunk_counts + static_cast<int64_t>(c0 + u) * E + e)
+                                        : 0;
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u)
+                if (c0 + u < nchunks) {
+                    chunk_counts[static_cast<int64_t>(c0 + u) * E + e] = cnt;
+                    cnt += v[u];
+                }
         }
     }
     const int32_t seg = (cnt + block_m - 1) / block_m * block_m;
@@ -163,11 +182,22 @@ __global__ void __launch_bounds__(kAlignThreads)
         running[e] = __ldcg(pad_offsets + e) +
                      __ldcg(chunk_base + static_cast<int64_t>(blockIdx.x) * E + e);
     for (int i = threadIdx.x; i < kAlignWarps * E; i += blockDim.x) warp_cnt[i] = 0;
+    // the chunk's ids, all loaded up front (one round trip to memory)
+    constexpr int kPerThread = kAlignChunk / kAlignThreads;
+    int my_e[kPerThread];
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) {
+        const int64_t p = start + threadIdx.x + static_cast<int64_t>(i) * kAlignThreads;
+        my_e[i] = p < end ? __ldcg(ids + p) : -1;
+    }
     __syncthreads();
     const uint32_t lanes_below = (1u << lane) - 1u;
-    for (int64_t base = start; base < end; base += blockDim.x) {
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) {
+        const int64_t base = start + static_cast<int64_t>(i) * kAlignThreads;
+        if (base >= end) break;  // uniform across the CTA
         const int64_t p = base + threadIdx.x;
-        int e = p < end ? __ldcg(ids + p) : -1;
+        int e = p < end ? my_e[i] : -1;
         const bool valid = e >= 0 && e < E;
         // lanes that are not real pairs get keys no real expert can match
         const uint32_t peers = __match_any_sync(0xffffffffu, valid ? e : E + lane);
@@ -294,6 +324,8 @@ cudaError_t launch_align(const AlignArgs &a, cudaStream_t s, int *launches) {
                           a.E, a.block_m, a.counts, a.offsets, a.pad_offsets, a.num_padded,
                           a.sorted_pair, a.block_expert, a.status);
     }
+    // the count and scatter kernels hold a chunk's ids in registers
+    if (a.chunk != kAlignChunk) return cudaErrorInvalidValue;
     const size_t count_smem = sizeof(int32_t) * a.E;
     cudaError_t err = launch_pdl(align_count_kernel, dim3(a.nchunks), dim3(kAlignThreads),
                                  count_smem, s, 1, a.ids, a.P, a.E, a.chunk, a.chunk_counts,
