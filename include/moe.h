@@ -199,6 +199,32 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router,
                          size_t workspace_bytes, cudaStream_t stream);
 
 /* -------------------------------------------------------------------------
+ * moe_forward_host -- moe_forward for activations that live in host memory:
+ * the end-to-end call of a loop whose tokens come from the host (the pages
+ * have no counterpart; their layer works on device tensors).  Enqueued on
+ * `stream`: copy x_host -> x_dev, the layer x_dev -> out_dev, copy out_dev ->
+ * out_host.  The result is in out_host once the stream reaches that point.
+ *   x_host, out_host  [N, H] bf16 host memory (pinned for asynchronous copies;
+ *                     pageable memory makes the copies synchronous)
+ *   x_dev, out_dev    [N, H] bf16 device buffers owned by the caller, 16-byte
+ *                     aligned, aliasing no input
+ * Every other argument, limit and error as moe_forward (with x_dev as x and
+ * out_dev as out); all argument errors are returned before anything is
+ * enqueued, plus MOE_ERR_INVALID_ARG for a null host pointer with N > 0.
+ * ---------------------------------------------------------------------- */
+moe_status_t moe_forward_host(const moe_bf16_t *x_host, moe_bf16_t *out_host,
+                              moe_bf16_t *x_dev, moe_bf16_t *out_dev,
+                              const moe_bf16_t *router, const moe_bf16_t *w_gate,
+                              const moe_bf16_t *w_up, const moe_bf16_t *w_down,
+                              const moe_bf16_t *shared_gate_proj,
+                              const moe_bf16_t *shared_up_proj,
+                              const moe_bf16_t *shared_down_proj,
+                              const moe_bf16_t *shared_gate, int64_t N, int H, int E,
+                              int I, int I_s, int k, int norm_topk_prob,
+                              void *workspace, size_t workspace_bytes,
+                              cudaStream_t stream);
+
+/* -------------------------------------------------------------------------
  * moe_add_rmsnorm -- the decoder layer's step that feeds the MoE, in one
  * kernel (Nano-vLLM notes, question 4 on the decoder layer; Qwen3.5
  * walkthrough section 2.1): r = x + residual in the model's bf16 dtype;

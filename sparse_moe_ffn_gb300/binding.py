@@ -55,6 +55,7 @@ def lib():
         "moe_align": ([P, i64, i32, i32, i32, P, P, P, P, P, P, sz, P], i32),
         "moe_forward_workspace_bytes": ([i64, i32, i32, i32, i32, i32], sz),
         "moe_forward": ([P] * 9 + [i64, i32, i32, i32, i32, i32, i32, P, P, sz, P], i32),
+        "moe_forward_host": ([P] * 12 + [i64, i32, i32, i32, i32, i32, i32, P, sz, P], i32),
         "moe_forward_layout": ([i64, i32, i32, i32, i32, i32, ctypes.POINTER(_Layout)], i32),
         "moe_read_device_status": ([P, P], i32),
         "moe_kernel_launch_count": ([], ctypes.c_uint64),
@@ -261,14 +262,29 @@ def moe_dense_mlp(x, w_gate, w_up, w_down, out=None, workspace=None):
 
 def moe_forward_from_host(x_host, out_host, x_dev, out_dev, weights: dict, k: int,
                           norm_topk_prob: bool, workspace):
-    """End-to-end call with host buffers: copy x (pinned host) to the device,
-    run the layer, copy the result back to pinned host memory, all on the
+    """End-to-end call with host buffers through moe_forward_host: x (pinned
+    host) is copied to the device staging buffer x_dev, the layer runs, and
+    the result is copied from out_dev back to pinned host memory, all on the
     current stream.  Weights stay resident on the device."""
-    x_dev.copy_(x_host, non_blocking=True)
-    shared = {n: weights[n] for n in SHARED_KEYS} if "shared_gate" in weights else None
-    moe_forward(x_dev, weights["router"], weights["w_gate"], weights["w_up"], weights["w_down"],
-                k, norm_topk_prob, shared, out=out_dev, workspace=workspace)
-    out_host.copy_(out_dev, non_blocking=True)
+    N, H = x_host.shape
+    E, I, _ = weights["w_gate"].shape
+    if x_host.is_cuda or out_host.is_cuda:
+        raise ValueError("x_host and out_host must be host tensors")
+    if x_host.dtype != torch.bfloat16 or out_host.dtype != torch.bfloat16:
+        raise ValueError("x_host and out_host must be bf16")
+    if not (x_host.is_contiguous() and out_host.is_contiguous()) or out_host.shape != (N, H):
+        raise ValueError("x_host and out_host must be contiguous [N, H]")
+    _bf16(x_dev, "x_dev", (N, H))
+    _bf16(out_dev, "out_dev", (N, H))
+    shared = "shared_gate" in weights
+    sp = [weights[n] if shared else None for n in SHARED_KEYS]
+    I_s = weights["shared_gate_proj"].shape[0] if shared else 0
+    _check(lib().moe_forward_host(x_host.data_ptr(), out_host.data_ptr(), _ptr(x_dev),
+                                  _ptr(out_dev), _ptr(weights["router"]), _ptr(weights["w_gate"]),
+                                  _ptr(weights["w_up"]), _ptr(weights["w_down"]),
+                                  *[_ptr(t) for t in sp], N, H, E, I, I_s, k,
+                                  int(bool(norm_topk_prob)), _ptr(workspace), workspace.numel(),
+                                  _stream()), "moe_forward_host")
     return out_host
 
 

@@ -284,6 +284,53 @@ moe_status_t forward_layout(int64_t N, int H, int E, int I, int k, int I_s,
     return MOE_OK;
 }
 
+// Every argument check of moe_forward, before anything is enqueued; on
+// success *shared_out tells whether the shared expert is present and *L holds
+// the workspace layout.
+moe_status_t check_forward_args(const moe_bf16_t *x, const moe_bf16_t *router,
+                                const moe_bf16_t *w_gate, const moe_bf16_t *w_up,
+                                const moe_bf16_t *w_down, const moe_bf16_t *shared_gate_proj,
+                                const moe_bf16_t *shared_up_proj,
+                                const moe_bf16_t *shared_down_proj, const moe_bf16_t *shared_gate,
+                                int64_t N, int H, int E, int I, int I_s, int k,
+                                const moe_bf16_t *out, const void *workspace,
+                                size_t workspace_bytes, bool *shared_out,
+                                moe_forward_layout_t *L) {
+    const int nshared = (shared_gate_proj != nullptr) + (shared_up_proj != nullptr) +
+                        (shared_down_proj != nullptr) + (shared_gate != nullptr);
+    if (nshared != 0 && nshared != 4)
+        return fail(MOE_ERR_INVALID_ARG,
+                    "give all four shared-expert tensors or none (got %d of 4)", nshared);
+    const bool shared = nshared == 4;
+    *shared_out = shared;
+    if (!shared) I_s = 0;
+    if (shared && (I_s < 8 || I_s % 8))
+        return fail(MOE_ERR_INVALID_ARG, "I_s must be a positive multiple of 8 (got %d)", I_s);
+    if (I < 8 || I % 8) return fail(MOE_ERR_INVALID_ARG, "I must be a positive multiple of 8 (got %d)", I);
+    float dummy_gamma;
+    int32_t dummy_ids;
+    moe_status_t st = check_route_args(x, router, shared ? shared_gate : nullptr, N, H, E, k,
+                                       reinterpret_cast<float *>(&dummy_gamma), &dummy_ids,
+                                       &dummy_gamma);
+    if (st != MOE_OK || N == 0) return st;
+    if (!w_gate || !w_up || !w_down || !out || !workspace)
+        return fail(MOE_ERR_INVALID_ARG, "w_gate, w_up, w_down, out and workspace must be non-null");
+    if (!aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) || !aligned16(out) ||
+        (shared && (!aligned16(shared_gate_proj) || !aligned16(shared_up_proj) ||
+                    !aligned16(shared_down_proj))))
+        return fail(MOE_ERR_INVALID_ARG, "bf16 matrices must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
+        return fail(MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    if (N * k + static_cast<int64_t>(E) * kBlockM >= (int64_t(1) << 31))
+        return fail(MOE_ERR_UNSUPPORTED, "N*k + E*128 must stay below 2^31");
+    forward_layout(N, H, E, I, k, I_s, L);
+    if (workspace_bytes < L->total)
+        return fail(MOE_ERR_WORKSPACE_TOO_SMALL, "forward workspace needs %zu bytes, got %zu",
+                    L->total, workspace_bytes);
+    return MOE_OK;
+}
+
+
 }  // namespace
 
 void moe::set_last_error(const char *msg) { g_last_error = msg; }
@@ -407,37 +454,13 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
                          moe_bf16_t *out, void *workspace, size_t workspace_bytes,
                          cudaStream_t stream) {
     g_last_error.clear();
-    const int nshared = (shared_gate_proj != nullptr) + (shared_up_proj != nullptr) +
-                        (shared_down_proj != nullptr) + (shared_gate != nullptr);
-    if (nshared != 0 && nshared != 4)
-        return fail(MOE_ERR_INVALID_ARG,
-                    "give all four shared-expert tensors or none (got %d of 4)", nshared);
-    const bool shared = nshared == 4;
-    if (!shared) I_s = 0;
-    if (shared && (I_s < 8 || I_s % 8))
-        return fail(MOE_ERR_INVALID_ARG, "I_s must be a positive multiple of 8 (got %d)", I_s);
-    if (I < 8 || I % 8) return fail(MOE_ERR_INVALID_ARG, "I must be a positive multiple of 8 (got %d)", I);
-    float dummy_gamma;
-    int32_t dummy_ids;
-    moe_status_t st = check_route_args(x, router, shared ? shared_gate : nullptr, N, H, E, k,
-                                       reinterpret_cast<float *>(&dummy_gamma), &dummy_ids,
-                                       &dummy_gamma);
-    if (st != MOE_OK || N == 0) return st;
-    if (!w_gate || !w_up || !w_down || !out || !workspace)
-        return fail(MOE_ERR_INVALID_ARG, "w_gate, w_up, w_down, out and workspace must be non-null");
-    if (!aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) || !aligned16(out) ||
-        (shared && (!aligned16(shared_gate_proj) || !aligned16(shared_up_proj) ||
-                    !aligned16(shared_down_proj))))
-        return fail(MOE_ERR_INVALID_ARG, "bf16 matrices must be 16-byte aligned");
-    if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
-        return fail(MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-    if (N * k + static_cast<int64_t>(E) * kBlockM >= (int64_t(1) << 31))
-        return fail(MOE_ERR_UNSUPPORTED, "N*k + E*128 must stay below 2^31");
+    bool shared = false;
     moe_forward_layout_t L;
-    forward_layout(N, H, E, I, k, I_s, &L);
-    if (workspace_bytes < L.total)
-        return fail(MOE_ERR_WORKSPACE_TOO_SMALL, "forward workspace needs %zu bytes, got %zu",
-                    L.total, workspace_bytes);
+    moe_status_t st = check_forward_args(x, router, w_gate, w_up, w_down, shared_gate_proj,
+                                         shared_up_proj, shared_down_proj, shared_gate, N, H, E,
+                                         I, I_s, k, out, workspace, workspace_bytes, &shared, &L);
+    if (st != MOE_OK || N == 0) return st;
+    if (!shared) I_s = 0;
 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     auto at = [&](size_t off) { return ws + off; };
@@ -667,6 +690,35 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
     MOE_CUDA(launch_combine(ypair, y_shared, N, H, k, out, sms, stream), "combine kernel launch");
     g_launches += 1;
     if ((st = record_stage(MOE_NUM_STAGES, stream)) != MOE_OK) return st;
+    return MOE_OK;
+}
+
+moe_status_t moe_forward_host(const moe_bf16_t *x_host, moe_bf16_t *out_host, moe_bf16_t *x_dev,
+                              moe_bf16_t *out_dev, const moe_bf16_t *router,
+                              const moe_bf16_t *w_gate, const moe_bf16_t *w_up,
+                              const moe_bf16_t *w_down, const moe_bf16_t *shared_gate_proj,
+                              const moe_bf16_t *shared_up_proj,
+                              const moe_bf16_t *shared_down_proj, const moe_bf16_t *shared_gate,
+                              int64_t N, int H, int E, int I, int I_s, int k, int norm_topk_prob,
+                              void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    g_last_error.clear();
+    bool shared = false;
+    moe_forward_layout_t L;
+    moe_status_t st = check_forward_args(x_dev, router, w_gate, w_up, w_down, shared_gate_proj,
+                                         shared_up_proj, shared_down_proj, shared_gate, N, H, E,
+                                         I, I_s, k, out_dev, workspace, workspace_bytes, &shared,
+                                         &L);
+    if (st != MOE_OK || N == 0) return st;
+    if (!x_host || !out_host)
+        return fail(MOE_ERR_INVALID_ARG, "x_host and out_host must be non-null");
+    const size_t bytes = static_cast<size_t>(N) * H * sizeof(moe_bf16_t);
+    MOE_CUDA(cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, stream), "input copy");
+    st = moe_forward(x_dev, router, w_gate, w_up, w_down, shared_gate_proj, shared_up_proj,
+                     shared_down_proj, shared_gate, N, H, E, I, I_s, k, norm_topk_prob, out_dev,
+                     workspace, workspace_bytes, stream);
+    if (st != MOE_OK) return st;
+    MOE_CUDA(cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, stream),
+             "output copy");
     return MOE_OK;
 }
 

@@ -81,6 +81,23 @@ def test_forward_argument_errors(L):
     assert _fwd(L, N=0) == OK                      # no-op, nothing launched
 
 
+def _fwd_host(L, N=64, H=2048, E=128, I=768, k=8, x_host=FAKE, out_host=FAKE, x_dev=FAKE,
+              out_dev=FAKE, ws=FAKE * 16):
+    ws_bytes = L.moe_forward_workspace_bytes(N, H, E, I, k, 0)
+    return L.moe_forward_host(x_host, out_host, x_dev, out_dev, FAKE, FAKE, FAKE, FAKE,
+                              None, None, None, None, N, H, E, I, 0, k, 1, ws, ws_bytes, None)
+
+
+def test_forward_host_argument_errors(L):
+    # every check runs before the input copy is enqueued
+    assert _fwd_host(L, x_host=None) == INVALID
+    assert _fwd_host(L, out_host=None) == INVALID
+    assert _fwd_host(L, x_dev=FAKE + 2) == INVALID   # misaligned staging buffer
+    assert _fwd_host(L, out_dev=None) == INVALID
+    assert _fwd_host(L, k=0) == INVALID
+    assert _fwd_host(L, N=0, x_host=None) == OK       # no-op, nothing enqueued
+
+
 def test_route_and_align_argument_errors(L):
     P = FAKE
     assert L.moe_route(P, P, None, 16, 64, 6, 7, 1, P, P, None, None, None, 0, None) == INVALID

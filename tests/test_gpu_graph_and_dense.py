@@ -29,6 +29,23 @@ def test_graph_replay_matches_eager(name):
         assert torch.equal(got, _eager(shape, dev, x)), f"seed {seed}"
 
 
+@pytest.mark.parametrize("name", ["decode", "talker"])
+def test_forward_host_buffers_match_device_call(name):
+    """moe_forward_host (pinned host x in, pinned host out) equals the device
+    call bit for bit."""
+    shape, dev, _ = prepared(name)
+    weights = {n: t for n, t in dev.items() if n != "x"}
+    x_host = dev["x"].cpu().pin_memory()
+    out_host = torch.empty_like(x_host).pin_memory()
+    x_dev, out_dev = torch.empty_like(dev["x"]), torch.empty_like(dev["x"])
+    ws = binding.alloc_workspace(shape.N, shape.H, shape.E, shape.I, shape.k, shape.I_s)
+    binding.moe_forward_from_host(x_host, out_host, x_dev, out_dev, weights, shape.k,
+                                  shape.norm_topk_prob, ws)
+    torch.cuda.synchronize()
+    assert binding.moe_read_device_status(ws) == 0
+    assert torch.equal(out_host, _eager(shape, dev, dev["x"]).cpu())
+
+
 def test_graph_bucket_padding_is_exact():
     shape, dev, _ = prepared("decode")
     weights = {n: t for n, t in dev.items() if n != "x"}
