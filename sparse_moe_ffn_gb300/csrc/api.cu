@@ -664,9 +664,25 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
             s.max_tiles = static_cast<int>(rows_s / kBlockM) * nt;
             s.grid = s.max_tiles < sms ? s.max_tiles : sms;
         }
-        MOE_CUDA(launch_gemm(kGateUp, bn_s, tm_xbox, tm_xbox, tm_xbox, tm_xbox, tm_sg, tm_su, s,
-                             stream),
-                 "shared gate/up kernel launch");
+        // more than one row block: two-CTA tiles over consecutive blocks
+        const bool pairs_s = rows_s >= 2 * kBlockM;
+        if (pairs_s) {
+            const int bn = pair_gemm_block_n(kGateUp);
+            CUtensorMap tm_sg2, tm_su2;
+            if ((st = make_map(&tm_sg2, shared_gate_proj, H, I_s, H, kBlockK, bn,
+                               "shared_gate_proj")) != MOE_OK ||
+                (st = make_map(&tm_su2, shared_up_proj, H, I_s, H, kBlockK, bn,
+                               "shared_up_proj")) != MOE_OK)
+                return st;
+            s.max_tiles = static_cast<int>((rows_s / kBlockM + 1) / 2) * ((I_s + bn - 1) / bn);
+            s.grid = 2 * (s.max_tiles < sms / 2 ? s.max_tiles : sms / 2);
+            MOE_CUDA(launch_pair_gemm(kGateUp, tm_xbox, tm_xbox, tm_sg2, tm_su2, s, stream),
+                     "shared gate/up kernel launch");
+        } else {
+            MOE_CUDA(launch_gemm(kGateUp, bn_s, tm_xbox, tm_xbox, tm_xbox, tm_xbox, tm_sg, tm_su,
+                                 s, stream),
+                     "shared gate/up kernel launch");
+        }
         s.K = I_s;
         s.n_out = H;
         s.w_rows = H;
@@ -679,9 +695,21 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
             s.max_tiles = static_cast<int>(rows_s / kBlockM) * nt;
             s.grid = s.max_tiles < sms ? s.max_tiles : sms;
         }
-        MOE_CUDA(launch_gemm(kDown, kDownBN, tm_acts, tm_acts_lo, tm_acts, tm_acts_lo, tm_sd,
-                             tm_sd, s, stream),
-                 "shared down kernel launch");
+        if (pairs_s) {
+            const int bn = pair_gemm_block_n(kDown);
+            CUtensorMap tm_sd2;
+            if ((st = make_map(&tm_sd2, shared_down_proj, I_s, H, I_s, kBlockK, bn / 2,
+                               "shared_down_proj")) != MOE_OK)
+                return st;
+            s.max_tiles = static_cast<int>((rows_s / kBlockM + 1) / 2) * ((H + bn - 1) / bn);
+            s.grid = 2 * (s.max_tiles < sms / 2 ? s.max_tiles : sms / 2);
+            MOE_CUDA(launch_pair_gemm(kDown, tm_acts, tm_acts_lo, tm_sd2, tm_sd2, s, stream),
+                     "shared down kernel launch");
+        } else {
+            MOE_CUDA(launch_gemm(kDown, kDownBN, tm_acts, tm_acts_lo, tm_acts, tm_acts_lo, tm_sd,
+                                 tm_sd, s, stream),
+                     "shared down kernel launch");
+        }
         g_launches += 2;
     }
 
@@ -807,18 +835,44 @@ moe_status_t moe_dense_mlp(const moe_bf16_t *x, const moe_bf16_t *w_gate, const 
     g.stream_weights = N <= kBlockM ? 1 : 0;
     g.max_tiles = static_cast<int>(rows / kBlockM) * ((I + bn - 1) / bn);
     g.grid = g.max_tiles < sms ? g.max_tiles : sms;
-    MOE_CUDA(launch_gemm(kGateUp, bn, tm_x, tm_x, tm_x, tm_x, tm_g, tm_u, g, stream),
-             "dense gate/up kernel launch");
+    // more than one row block: two-CTA tiles over consecutive blocks
+    const bool pairs = rows >= 2 * kBlockM;
+    if (pairs) {
+        const int bnp = pair_gemm_block_n(kGateUp);
+        CUtensorMap tm_g2, tm_u2;
+        if ((st = make_map(&tm_g2, w_gate, H, I, H, kBlockK, bnp, "w_gate")) != MOE_OK ||
+            (st = make_map(&tm_u2, w_up, H, I, H, kBlockK, bnp, "w_up")) != MOE_OK)
+            return st;
+        g.max_tiles = static_cast<int>((rows / kBlockM + 1) / 2) * ((I + bnp - 1) / bnp);
+        g.grid = 2 * (g.max_tiles < sms / 2 ? g.max_tiles : sms / 2);
+        MOE_CUDA(launch_pair_gemm(kGateUp, tm_x, tm_x, tm_g2, tm_u2, g, stream),
+                 "dense gate/up kernel launch");
+    } else {
+        MOE_CUDA(launch_gemm(kGateUp, bn, tm_x, tm_x, tm_x, tm_x, tm_g, tm_u, g, stream),
+                 "dense gate/up kernel launch");
+    }
     g.K = I;
     g.n_out = H;
     g.w_rows = H;
     g.out = y;
     g.out_lo = nullptr;
     g.out_ld = H;
-    g.max_tiles = static_cast<int>(rows / kBlockM) * ((H + kDownBN - 1) / kDownBN);
-    g.grid = g.max_tiles < sms ? g.max_tiles : sms;
-    MOE_CUDA(launch_gemm(kDown, kDownBN, tm_act, tm_act_lo, tm_act, tm_act_lo, tm_d, tm_d, g, stream),
-             "dense down kernel launch");
+    if (pairs) {
+        const int bnp = pair_gemm_block_n(kDown);
+        CUtensorMap tm_d2;
+        if ((st = make_map(&tm_d2, w_down, I, H, I, kBlockK, bnp / 2, "w_down")) != MOE_OK)
+            return st;
+        g.max_tiles = static_cast<int>((rows / kBlockM + 1) / 2) * ((H + bnp - 1) / bnp);
+        g.grid = 2 * (g.max_tiles < sms / 2 ? g.max_tiles : sms / 2);
+        MOE_CUDA(launch_pair_gemm(kDown, tm_act, tm_act_lo, tm_d2, tm_d2, g, stream),
+                 "dense down kernel launch");
+    } else {
+        g.max_tiles = static_cast<int>(rows / kBlockM) * ((H + kDownBN - 1) / kDownBN);
+        g.grid = g.max_tiles < sms ? g.max_tiles : sms;
+        MOE_CUDA(launch_gemm(kDown, kDownBN, tm_act, tm_act_lo, tm_act, tm_act_lo, tm_d, tm_d, g,
+                             stream),
+                 "dense down kernel launch");
+    }
     // fp16 rows -> bf16 out (the combine with one slot per token)
     MOE_CUDA(launch_combine(y, nullptr, N, H, 1, out, sms, stream), "combine kernel launch");
     g_launches += 3;
