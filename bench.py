@@ -253,7 +253,12 @@ def run_ours(args, world, rank, local):
                             shape.norm_topk_prob, shared, out=out, workspace=ws)
 
     # warm-up; the last warm-up step records every stage boundary to find the
-    # dominant kernel, whose launches the timed steps then bracket with events
+    # dominant kernel.  The timed region runs the K steps with no stage events:
+    # an event recorded between two launches removes the programmatic
+    # dependent-launch overlap of the kernels around it (~15 us per decode
+    # step).  A second pass of K steps then brackets the dominant kernel's
+    # launches with events for the roofline; its duration there is an upper
+    # bound (the launch no longer overlaps its predecessor).
     nst = len(STAGES) + 1
     probe = [torch.cuda.Event(enable_timing=True) for _ in range(nst)]
     for i in range(args.warmup):
@@ -282,17 +287,21 @@ def run_ours(args, world, rank, local):
     t0 = time.time()
     start.record()
     for i in range(args.steps):
-        binding.set_stage_events(ev[i])
         step()
     end.record()
     torch.cuda.synchronize()
     t1 = time.time()
     barrier(world)
-    binding.set_stage_events(None)
     launches = binding.moe_kernel_launch_count() - launches0
     clocks = ClockSampler.summarize(sampler.stop(), t0, t1)
     ms = start.elapsed_time(end)
     ms_max = max_over_ranks(ms, world, device)
+    # roofline pass: the same K steps, the dominant kernel bracketed by events
+    for i in range(args.steps):
+        binding.set_stage_events(ev[i])
+        step()
+    binding.set_stage_events(None)
+    torch.cuda.synchronize()
     dom_ms = statistics.mean(ev[i][j_dom].elapsed_time(ev[i][j_dom + 1])
                              for i in range(args.steps))
 
@@ -319,7 +328,10 @@ def run_ours(args, world, rank, local):
     roof.update(frac=round(achieved / roof["peak"], 4), traffic=measured_traffic(dom, args.config),
                 kernel=dom, kernel_ms=round(dom_ms, 5), peak_source=f"{peak_src} (MEASURED_PEAKS.json)" if peak_src ==
                 "measured" else "fallback", algorithmic_per_launch=(
-                    sbytes[dom] if roof["bound"] == "hbm" else sflops[dom]))
+                    sbytes[dom] if roof["bound"] == "hbm" else sflops[dom]),
+                window=f"second pass of {args.steps} steps after the timed region, CUDA events "
+                       "around the kernel's launch on its stream (the event removes the launch "
+                       "overlap with the previous kernel, so kernel_ms is an upper bound)")
 
     # end to end through the public call with host buffers
     x_host = cpu["x"].to(torch.bfloat16).pin_memory()

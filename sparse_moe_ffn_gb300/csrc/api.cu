@@ -517,6 +517,8 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
     g.block_expert = b.block_expert;
     g.pad_offsets = b.pad_offsets;
     g.num_groups = E;
+    g.expert_tiles = 0;
+    g.w0 = g.w1 = nullptr;
     g.num_padded = b.num_padded;
     g.num_rows_host = cap;
     g.q_limit = P;
@@ -545,8 +547,18 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
     }
     if ((st = record_stage(MOE_STAGE_GATE_UP, stream)) != MOE_OK) return st;
     if (sparse) {
+        if (N <= kBlockM) {
+            // every expert owns at most one row block: tiles indexed by
+            // expert, the first ones' weight rows warmed into L2 during routing
+            g.expert_tiles = 1;
+            g.w0 = w_gate;
+            g.w1 = w_up;
+            g.max_tiles = E * ((I + bn_gu - 1) / bn_gu);
+            g.grid = g.max_tiles < sms ? g.max_tiles : sms;
+        }
         MOE_CUDA(launch_sparse_gemm(kGateUp, bn_gu, tm_xrows, tm_xrows, tm_wg, tm_wu, g, stream),
                  "gate/up kernel launch");
+        g.expert_tiles = 0;
     } else if (pairs) {
         const int bn = pair_gemm_block_n(kGateUp);
         CUtensorMap tm_wg_tile, tm_wu_tile;
@@ -650,6 +662,8 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
         s.k_div = 1;
         s.pad_offsets = nullptr;
         s.num_groups = 0;
+        s.expert_tiles = 0;
+        s.w0 = s.w1 = nullptr;
         s.K = H;
         s.n_out = I_s;
         s.w_rows = I_s;

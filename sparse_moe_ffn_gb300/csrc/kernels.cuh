@@ -107,6 +107,14 @@ struct GemmArgs {
     // [pad_offsets[g], pad_offsets[g+1]); null: one group of num_rows_host rows
     const int32_t *pad_offsets;
     int num_groups;
+    // sparse kernel: tile t = (expert t / n_tiles, N tile t % n_tiles) when set,
+    // for batches where every expert owns at most one row block (N <= 128);
+    // the tile order is then known before routing, and each CTA warms L2 with
+    // its first tile's weight rows (w0, w1: the Wg and Wu bases) while it
+    // waits for the earlier kernels
+    int expert_tiles;
+    const void *w0;
+    const void *w1;
     int max_tiles;      // upper bound on tiles (sizes the persistent grid)
     int grid;           // persistent CTAs
 };

@@ -92,6 +92,12 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// Asks L2 to fetch [src, src + bytes) from memory (bytes: a multiple of 16,
+// src 16-byte aligned); nothing is written to shared memory.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // L2 eviction-priority policies for the cache-hinted copies below.
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;

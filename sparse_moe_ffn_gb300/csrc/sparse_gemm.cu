@@ -60,7 +60,10 @@ struct SparseCfg {
     static_assert((MODE == kGateUp ? 2 : 1) * BN <= kAccCols, "accumulator too wide");
 };
 
+constexpr int kMaxExperts = MOE_MAX_EXPERTS;
+
 struct SparseSmem {
+    int pad[kMaxExperts + 1];  // expert-indexed tiles: padded row offset of each expert
     uint64_t full[kSparseMaxStages];
     uint64_t empty[kSparseMaxStages];
     uint64_t acc_full[2];
@@ -137,13 +140,46 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem = sm->tmem_base;
     volatile int *abort_flag = &sm->abort_flag;
+    const int n_tiles = (a.n_out + BN - 1) / BN;
+    const bool by_expert = a.expert_tiles != 0;
     griddep_launch_dependents();
+    // weights are inputs, not results of earlier kernels: with expert-indexed
+    // tiles the first tile's weight rows are known now, and L2 fetches them
+    // while memory is otherwise idle (routing)
+    // (half of the tile's rows: the same gain as the whole tile in a timed
+    // decode loop, with half the L2 footprint)
+    if (by_expert && threadIdx.x == 0 && static_cast<int>(blockIdx.x) < a.num_groups * n_tiles) {
+        const int64_t e = blockIdx.x / n_tiles;
+        const int64_t r0 = static_cast<int64_t>(blockIdx.x % n_tiles) * BN;
+        const int64_t nrows = min(static_cast<int64_t>(BN), a.w_rows - r0) / 2;
+        const int64_t off = (e * a.w_rows + r0) * a.K * 2;
+        const uint32_t bytes = static_cast<uint32_t>(nrows * a.K * 2);
+        if (bytes > 0) {
+            prefetch_l2_bulk(static_cast<const uint8_t *>(a.w0) + off, bytes);
+            if (MODE == kGateUp) prefetch_l2_bulk(static_cast<const uint8_t *>(a.w1) + off, bytes);
+        }
+    }
     griddep_wait();  // the block list and the A rows come from earlier kernels
 
-    const int64_t rows = static_cast<int64_t>(__ldcg(a.num_padded));
-    const int num_blocks = static_cast<int>((rows + kBlockM - 1) / kBlockM);
-    const int n_tiles = (a.n_out + BN - 1) / BN;
-    const int total_tiles = min(num_blocks * n_tiles, a.max_tiles);
+    int total_tiles;
+    if (by_expert) {
+        for (int i = threadIdx.x; i <= a.num_groups; i += blockDim.x)
+            sm->pad[i] = __ldcg(a.pad_offsets + i);
+        __syncthreads();
+        total_tiles = min(a.num_groups * n_tiles, a.max_tiles);
+    } else {
+        const int64_t rows = static_cast<int64_t>(__ldcg(a.num_padded));
+        total_tiles = min(static_cast<int>((rows + kBlockM - 1) / kBlockM) * n_tiles, a.max_tiles);
+    }
+    // row block of a tile (-1: its expert received no pairs)
+    auto block_of = [&](int tile) -> int {
+        if (!by_expert) return tile / n_tiles;
+        const int e = tile / n_tiles;
+        return sm->pad[e + 1] > sm->pad[e] ? sm->pad[e] / kBlockM : -1;
+    };
+    auto expert_of = [&](int tile) -> int {
+        return by_expert ? tile / n_tiles : __ldcg(a.block_expert + tile / n_tiles);
+    };
     const int nk = (a.K + kBlockK - 1) / kBlockK;
 
     if (warp == 0) {
@@ -156,14 +192,17 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
         int32_t q_next[4] = {-1, -1, -1, -1};
         int expert_next = 0;
         if (static_cast<int>(blockIdx.x) < total_tiles) {
-            const int64_t base = static_cast<int64_t>(blockIdx.x / n_tiles) * kBlockM;
+            const int b0 = block_of(blockIdx.x);
+            if (b0 >= 0) {
+                const int64_t base = static_cast<int64_t>(b0) * kBlockM;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) q_next[i] = __ldcg(a.sorted_pair + base + lane * 4 + i);
-            expert_next = __ldcg(a.block_expert + blockIdx.x / n_tiles);
+                for (int i = 0; i < 4; ++i) q_next[i] = __ldcg(a.sorted_pair + base + lane * 4 + i);
+            }
+            expert_next = expert_of(blockIdx.x);
         }
         for (int tile = blockIdx.x, j = 0; tile < total_tiles && !failed;
              tile += gridDim.x, ++j) {
-            const int blk = tile / n_tiles;
+            const int blk = block_of(tile);
             const int nt = tile % n_tiles;
             int src[4];
             bool any = false;
@@ -180,10 +219,13 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
             const int expert = expert_next;
             const int next = tile + static_cast<int>(gridDim.x);
             if (next < total_tiles) {
-                const int64_t base = static_cast<int64_t>(next / n_tiles) * kBlockM;
+                const int bn = block_of(next);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) q_next[i] = __ldcg(a.sorted_pair + base + lane * 4 + i);
-                expert_next = __ldcg(a.block_expert + next / n_tiles);
+                for (int i = 0; i < 4; ++i)
+                    q_next[i] = bn >= 0 ? __ldcg(a.sorted_pair + static_cast<int64_t>(bn) * kBlockM +
+                                                 lane * 4 + i)
+                                        : -1;
+                expert_next = expert_of(next);
             }
 #pragma unroll
             for (int d = 16; d > 0; d >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, d));
@@ -354,7 +396,7 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
                 }
                 tc_fence_after_sync();
                 if (quarter == 0)
-                    store_tile<MODE, BN>(a, tmem + acc * kAccCols, tile / n_tiles, tile % n_tiles,
+                    store_tile<MODE, BN>(a, tmem + acc * kAccCols, block_of(tile), tile % n_tiles,
                                          p * kSubRows + lane);
                 tc_fence_before_sync();
                 __syncwarp();
