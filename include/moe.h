@@ -199,6 +199,43 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router,
                          size_t workspace_bytes, cudaStream_t stream);
 
 /* -------------------------------------------------------------------------
+ * moe_experts -- the per-expert half of the layer for rows whose expert and
+ * weight are already chosen: the receiving side of expert-parallel dispatch
+ * (M03 drill, level-3 follow-up on splitting experts across devices: the
+ * (token, expert) table drives an all-to-all).  For every row r:
+ *   y[r] = fp16(weights[r] * Expert_{ids[r]}(x_rows[r]))
+ * with the arithmetic of moe_forward's per-pair outputs (grouping by expert,
+ * gate/up with the hi/lo activation, down), so the bits equal the pair rows
+ * moe_forward produces for the same (row, expert, weight).
+ *   x_rows   [R, H] bf16      ids [R] int32 in [0, E)      weights [R] fp32
+ *   w_gate, w_up [E, I, H], w_down [E, H, I] bf16: the experts this call
+ *            serves (a rank's slice of the layer's experts)
+ *   y        [R, H] fp16 out
+ *   workspace >= moe_experts_workspace_bytes(R, H, E, I) bytes, 256-byte
+ *            aligned; its first 4 bytes are the status word
+ *            (moe_read_device_status)
+ * Errors: argument problems before anything is enqueued; ids outside [0, E)
+ * record MOE_ERR_DEVICE_CHECK (their rows are left unwritten).
+ * ---------------------------------------------------------------------- */
+size_t moe_experts_workspace_bytes(int64_t R, int H, int E, int I);
+moe_status_t moe_experts(const moe_bf16_t *x_rows, const int32_t *ids,
+                         const float *weights, int64_t R, int H, int E, int I,
+                         const moe_bf16_t *w_gate, const moe_bf16_t *w_up,
+                         const moe_bf16_t *w_down, uint16_t *y, void *workspace,
+                         size_t workspace_bytes, cudaStream_t stream);
+
+/* -------------------------------------------------------------------------
+ * moe_combine -- the weighted accumulation of the layer (M03 drill: each
+ * token's outputs summed back, index_add_ in the pages' PyTorch form), done
+ * without atomics: out[n] = bf16(sum_{j<k} ypair[n*k + j] (+ yshared[n])),
+ * summed in fp32 in slot order.  ypair [N*k, H] fp16, yshared [N, H] fp16 or
+ * NULL, out [N, H] bf16; 16-byte aligned.  moe_forward ends with the same
+ * kernel.
+ * ---------------------------------------------------------------------- */
+moe_status_t moe_combine(const uint16_t *ypair, const uint16_t *yshared, int64_t N, int H,
+                         int k, moe_bf16_t *out, cudaStream_t stream);
+
+/* -------------------------------------------------------------------------
  * moe_forward_host -- moe_forward for activations that live in host memory:
  * the end-to-end call of a loop whose tokens come from the host (the pages
  * have no counterpart; their layer works on device tensors).  Enqueued on

@@ -56,6 +56,9 @@ def lib():
         "moe_forward_workspace_bytes": ([i64, i32, i32, i32, i32, i32], sz),
         "moe_forward": ([P] * 9 + [i64, i32, i32, i32, i32, i32, i32, P, P, sz, P], i32),
         "moe_forward_host": ([P] * 12 + [i64, i32, i32, i32, i32, i32, i32, P, sz, P], i32),
+        "moe_experts_workspace_bytes": ([i64, i32, i32, i32], sz),
+        "moe_experts": ([P, P, P, i64, i32, i32, i32, P, P, P, P, P, sz, P], i32),
+        "moe_combine": ([P, P, i64, i32, i32, P, P], i32),
         "moe_forward_layout": ([i64, i32, i32, i32, i32, i32, ctypes.POINTER(_Layout)], i32),
         "moe_read_device_status": ([P, P], i32),
         "moe_kernel_launch_count": ([], ctypes.c_uint64),
@@ -257,6 +260,48 @@ def moe_dense_mlp(x, w_gate, w_up, w_down, out=None, workspace=None):
                                 dtype=torch.uint8, device=x.device)
     _check(L.moe_dense_mlp(_ptr(x), _ptr(w_gate), _ptr(w_up), _ptr(w_down), N, H, I, _ptr(out),
                            _ptr(workspace), workspace.numel(), _stream()), "moe_dense_mlp")
+    return out
+
+
+def moe_experts(x_rows, ids, weights, w_gate, w_up, w_down, y=None, workspace=None):
+    """Per-row expert outputs y[r] = fp16(weights[r] * Expert_{ids[r]}(x_rows[r]))
+    ([R, H] fp16): the receiving side of expert-parallel dispatch."""
+    R, H = x_rows.shape
+    E, I, _ = w_gate.shape
+    _bf16(x_rows, "x_rows")
+    _bf16(w_gate, "w_gate", (E, I, H))
+    _bf16(w_up, "w_up", (E, I, H))
+    _bf16(w_down, "w_down", (E, H, I))
+    if ids.dtype != torch.int32 or not ids.is_cuda or tuple(ids.shape) != (R,):
+        raise ValueError("ids must be a CUDA int32 tensor of shape [R]")
+    if weights.dtype != torch.float32 or not weights.is_cuda or tuple(weights.shape) != (R,):
+        raise ValueError("weights must be a CUDA float32 tensor of shape [R]")
+    ids, weights = ids.contiguous(), weights.contiguous()
+    if y is None:
+        y = torch.empty((R, H), dtype=torch.float16, device=x_rows.device)
+    if y.dtype != torch.float16 or tuple(y.shape) != (R, H) or not y.is_contiguous():
+        raise ValueError("y must be a contiguous float16 tensor of shape [R, H]")
+    if workspace is None:
+        workspace = torch.empty(max(lib().moe_experts_workspace_bytes(R, H, E, I), 256),
+                                dtype=torch.uint8, device=x_rows.device)
+    _check(lib().moe_experts(_ptr(x_rows), _ptr(ids), _ptr(weights), R, H, E, I, _ptr(w_gate),
+                             _ptr(w_up), _ptr(w_down), _ptr(y), _ptr(workspace),
+                             workspace.numel(), _stream()), "moe_experts")
+    return y, workspace
+
+
+def moe_combine(ypair, N: int, k: int, yshared=None, out=None):
+    """out[n] = bf16(sum_j ypair[n*k + j] (+ yshared[n])) in fp32, slot order."""
+    H = ypair.shape[1]
+    if ypair.dtype != torch.float16 or tuple(ypair.shape) != (N * k, H) or not ypair.is_contiguous():
+        raise ValueError("ypair must be a contiguous float16 tensor of shape [N*k, H]")
+    if yshared is not None and (yshared.dtype != torch.float16 or tuple(yshared.shape) != (N, H)):
+        raise ValueError("yshared must be float16 of shape [N, H]")
+    if out is None:
+        out = torch.empty((N, H), dtype=torch.bfloat16, device=ypair.device)
+    _bf16(out, "out", (N, H))
+    _check(lib().moe_combine(_ptr(ypair), _ptr(yshared), N, H, k, _ptr(out), _stream()),
+           "moe_combine")
     return out
 
 

@@ -331,6 +331,171 @@ moe_status_t check_forward_args(const moe_bf16_t *x, const moe_bf16_t *router,
 }
 
 
+// Grouping, gate/up and down for N rows with k (expert, weight) slots each:
+// ypair[p] = fp16(weights[p] * Expert_{ids[p]}(x[p / k])), p = n * k + j.
+// The workspace follows moe_forward_layout(N, H, E, I, k, 0); its status word
+// is not reset here.  Records the align .. down stage events.
+moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const float *weights,
+                             int64_t N, int k, int H, int E, int I, const moe_bf16_t *w_gate,
+                             const moe_bf16_t *w_up, const moe_bf16_t *w_down,
+                             const moe_forward_layout_t &L, uint8_t *ws, uint16_t *ypair,
+                             cudaStream_t stream) {
+    moe_status_t st;
+    auto at = [&](size_t off) { return ws + off; };
+    int32_t *status = reinterpret_cast<int32_t *>(at(L.status));
+    uint16_t *x_sorted = reinterpret_cast<uint16_t *>(at(L.x_sorted));
+    uint16_t *act = reinterpret_cast<uint16_t *>(at(L.act));
+    uint16_t *act_lo = reinterpret_cast<uint16_t *>(at(L.act_lo));
+    const int64_t P = N * k;
+    const int64_t cap = L.capacity;
+    const int sms = num_sms_of_current_device();
+
+    // K2: grouping
+    if ((st = record_stage(MOE_STAGE_ALIGN, stream)) != MOE_OK) return st;
+    AlignBuffers b;
+    b.sorted_pair = reinterpret_cast<int32_t *>(at(L.sorted_pair));
+    b.block_expert = reinterpret_cast<int32_t *>(at(L.block_expert));
+    b.counts = reinterpret_cast<int32_t *>(at(L.counts));
+    b.offsets = reinterpret_cast<int32_t *>(at(L.offsets));
+    b.pad_offsets = reinterpret_cast<int32_t *>(at(L.pad_offsets));
+    b.num_padded = reinterpret_cast<int32_t *>(at(L.num_padded));
+    b.scratch = reinterpret_cast<int32_t *>(at(L.align_scratch));
+    b.status = status;
+    st = enqueue_align(ids, N, k, E, kBlockM, b, stream);
+    if (st != MOE_OK) return st;
+
+    // K3: gathered gate/up GEMM + silu * up
+    CUtensorMap tm_xrows, tm_xsorted, tm_wg, tm_wu, tm_act, tm_act_lo, tm_act_box, tm_act_lo_box,
+        tm_wd;
+    if ((st = make_map(&tm_xrows, x, H, N, H, kBlockK, 1, "x rows")) != MOE_OK) return st;
+    if ((st = make_map(&tm_xsorted, x_sorted, H, cap, H, kBlockK, kBlockM, "x_sorted")) != MOE_OK)
+        return st;
+    const int bn_gu = choose_gate_up_bn(expected_blocks(P, E), static_cast<double>(P) / E, I, sms);
+    if ((st = make_map(&tm_wg, w_gate, H, static_cast<uint64_t>(E) * I, H, kBlockK, bn_gu,
+                       "w_gate")) != MOE_OK)
+        return st;
+    if ((st = make_map(&tm_wu, w_up, H, static_cast<uint64_t>(E) * I, H, kBlockK, bn_gu,
+                       "w_up")) != MOE_OK)
+        return st;
+    const bool pairs = use_pair_tiles(P, E);
+    const bool sparse = !pairs && use_sparse_tiles(P, E);
+    GemmArgs g;
+    g.sorted_pair = b.sorted_pair;
+    g.block_expert = b.block_expert;
+    g.pad_offsets = b.pad_offsets;
+    g.num_groups = E;
+    g.expert_tiles = 0;
+    g.w0 = g.w1 = nullptr;
+    g.num_padded = b.num_padded;
+    g.num_rows_host = cap;
+    g.q_limit = P;
+    g.k_div = k;
+    g.K = H;
+    g.n_out = I;
+    g.w_rows = I;
+    g.out = act;
+    g.out_lo = act_lo;
+    g.out_ld = I;
+    g.scale = nullptr;
+    g.status = status;
+    // fewer than a block of pairs per expert: every weight tile is read once
+    g.stream_weights = P < static_cast<int64_t>(E) * kBlockM ? 1 : 0;
+    {
+        const int nt = (I + bn_gu - 1) / bn_gu;
+        g.max_tiles = static_cast<int>(cap / kBlockM) * nt;
+        g.grid = g.max_tiles < sms ? g.max_tiles : sms;
+    }
+    if ((st = record_stage(MOE_STAGE_GATHER, stream)) != MOE_OK) return st;
+    if (!sparse) {  // the sparse GEMM gathers its x rows itself
+        MOE_CUDA(launch_gather_rows(x, H, k, b.sorted_pair, b.num_padded, P, cap, x_sorted,
+                                    pairs ? 1 : 0, sms, stream),
+                 "gather kernel launch");
+        g_launches += 1;
+    }
+    if ((st = record_stage(MOE_STAGE_GATE_UP, stream)) != MOE_OK) return st;
+    if (sparse) {
+        if (N <= kBlockM) {
+            // every expert owns at most one row block: tiles indexed by
+            // expert, the first ones' weight rows warmed into L2 during routing
+            g.expert_tiles = 1;
+            g.w0 = w_gate;
+            g.w1 = w_up;
+            g.max_tiles = E * ((I + bn_gu - 1) / bn_gu);
+            g.grid = g.max_tiles < sms ? g.max_tiles : sms;
+        }
+        MOE_CUDA(launch_sparse_gemm(kGateUp, bn_gu, tm_xrows, tm_xrows, tm_wg, tm_wu, g, stream),
+                 "gate/up kernel launch");
+        g.expert_tiles = 0;
+    } else if (pairs) {
+        const int bn = pair_gemm_block_n(kGateUp);
+        CUtensorMap tm_wg_tile, tm_wu_tile;
+        if ((st = make_map(&tm_wg_tile, w_gate, H, static_cast<uint64_t>(E) * I, H, kBlockK, bn,
+                           "w_gate")) != MOE_OK)
+            return st;
+        if ((st = make_map(&tm_wu_tile, w_up, H, static_cast<uint64_t>(E) * I, H, kBlockK, bn,
+                           "w_up")) != MOE_OK)
+            return st;
+        const int max_pairs = static_cast<int>(cap / kBlockM);  // pairs <= blocks
+        g.max_tiles = max_pairs * ((I + bn - 1) / bn);
+        g.grid = 2 * (g.max_tiles < sms / 2 ? g.max_tiles : sms / 2);
+        MOE_CUDA(launch_pair_gemm(kGateUp, tm_xsorted, tm_xsorted, tm_wg_tile, tm_wu_tile, g,
+                                  stream),
+                 "gate/up kernel launch");
+    } else {
+        MOE_CUDA(launch_gemm(kGateUp, bn_gu, tm_xrows, tm_xrows, tm_xsorted, tm_xsorted, tm_wg,
+                             tm_wu, g, stream),
+                 "gate/up kernel launch");
+    }
+    g_launches += 1;
+
+    // K4: down GEMM * routing weight, one row per pair
+    if ((st = record_stage(MOE_STAGE_DOWN, stream)) != MOE_OK) return st;
+    if ((st = make_map(&tm_act, act, I, cap, I, kBlockK, 1, "act rows")) != MOE_OK) return st;
+    if ((st = make_map(&tm_act_lo, act_lo, I, cap, I, kBlockK, 1, "act_lo rows")) != MOE_OK)
+        return st;
+    if ((st = make_map(&tm_act_box, act, I, cap, I, kBlockK, kBlockM, "act")) != MOE_OK) return st;
+    if ((st = make_map(&tm_act_lo_box, act_lo, I, cap, I, kBlockK, kBlockM, "act_lo")) != MOE_OK)
+        return st;
+    if ((st = make_map(&tm_wd, w_down, I, static_cast<uint64_t>(E) * H, I, kBlockK, kDownBN,
+                       "w_down")) != MOE_OK)
+        return st;
+    g.k_div = 1;
+    g.K = I;
+    g.n_out = H;
+    g.w_rows = H;
+    g.out = ypair;
+    g.out_lo = nullptr;
+    g.out_ld = H;
+    g.scale = weights;
+    {
+        const int nt = (H + kDownBN - 1) / kDownBN;
+        g.max_tiles = static_cast<int>(cap / kBlockM) * nt;
+        g.grid = g.max_tiles < sms ? g.max_tiles : sms;
+    }
+    if (sparse) {
+        MOE_CUDA(launch_sparse_gemm(kDown, kDownBN, tm_act, tm_act_lo, tm_wd, tm_wd, g, stream),
+                 "down kernel launch");
+    } else if (pairs) {
+        const int bn = pair_gemm_block_n(kDown);
+        CUtensorMap tm_wd_half;
+        if ((st = make_map(&tm_wd_half, w_down, I, static_cast<uint64_t>(E) * H, I, kBlockK,
+                           bn / 2, "w_down")) != MOE_OK)
+            return st;
+        g.max_tiles = static_cast<int>(cap / kBlockM) * ((H + bn - 1) / bn);
+        g.grid = 2 * (g.max_tiles < sms / 2 ? g.max_tiles : sms / 2);
+        MOE_CUDA(launch_pair_gemm(kDown, tm_act_box, tm_act_lo_box, tm_wd_half, tm_wd_half, g,
+                                  stream),
+                 "down kernel launch");
+    } else {
+        MOE_CUDA(launch_gemm(kDown, kDownBN, tm_act, tm_act_lo, tm_act_box, tm_act_lo_box, tm_wd,
+                             tm_wd, g, stream),
+                 "down kernel launch");
+    }
+    g_launches += 1;
+
+    return MOE_OK;
+}
+
 }  // namespace
 
 void moe::set_last_error(const char *msg) { g_last_error = msg; }
@@ -468,12 +633,7 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
     float *topk_w = reinterpret_cast<float *>(at(L.topk_w));
     int32_t *topk_ids = reinterpret_cast<int32_t *>(at(L.topk_ids));
     float *gamma = shared ? reinterpret_cast<float *>(at(L.gamma)) : nullptr;
-    uint16_t *x_sorted = reinterpret_cast<uint16_t *>(at(L.x_sorted));
-    uint16_t *act = reinterpret_cast<uint16_t *>(at(L.act));
-    uint16_t *act_lo = reinterpret_cast<uint16_t *>(at(L.act_lo));
     uint16_t *ypair = reinterpret_cast<uint16_t *>(at(L.ypair));
-    const int64_t P = N * k;
-    const int64_t cap = L.capacity;
     const int sms = num_sms_of_current_device();
 
     // K1: routing (its first CTA also clears the status word, so that no
@@ -483,148 +643,10 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
                        topk_w, topk_ids, nullptr, gamma, status, true, stream);
     if (st != MOE_OK) return st;
 
-    // K2: grouping
-    if ((st = record_stage(MOE_STAGE_ALIGN, stream)) != MOE_OK) return st;
-    AlignBuffers b;
-    b.sorted_pair = reinterpret_cast<int32_t *>(at(L.sorted_pair));
-    b.block_expert = reinterpret_cast<int32_t *>(at(L.block_expert));
-    b.counts = reinterpret_cast<int32_t *>(at(L.counts));
-    b.offsets = reinterpret_cast<int32_t *>(at(L.offsets));
-    b.pad_offsets = reinterpret_cast<int32_t *>(at(L.pad_offsets));
-    b.num_padded = reinterpret_cast<int32_t *>(at(L.num_padded));
-    b.scratch = reinterpret_cast<int32_t *>(at(L.align_scratch));
-    b.status = status;
-    st = enqueue_align(topk_ids, N, k, E, kBlockM, b, stream);
-    if (st != MOE_OK) return st;
-
-    // K3: gathered gate/up GEMM + silu * up
-    CUtensorMap tm_xrows, tm_xsorted, tm_wg, tm_wu, tm_act, tm_act_lo, tm_act_box, tm_act_lo_box,
-        tm_wd;
-    if ((st = make_map(&tm_xrows, x, H, N, H, kBlockK, 1, "x rows")) != MOE_OK) return st;
-    if ((st = make_map(&tm_xsorted, x_sorted, H, cap, H, kBlockK, kBlockM, "x_sorted")) != MOE_OK)
+    // K2-K4: grouping, gate/up, down
+    if ((st = enqueue_experts(x, topk_ids, topk_w, N, k, H, E, I, w_gate, w_up, w_down, L, ws,
+                              ypair, stream)) != MOE_OK)
         return st;
-    const int bn_gu = choose_gate_up_bn(expected_blocks(P, E), static_cast<double>(P) / E, I, sms);
-    if ((st = make_map(&tm_wg, w_gate, H, static_cast<uint64_t>(E) * I, H, kBlockK, bn_gu,
-                       "w_gate")) != MOE_OK)
-        return st;
-    if ((st = make_map(&tm_wu, w_up, H, static_cast<uint64_t>(E) * I, H, kBlockK, bn_gu,
-                       "w_up")) != MOE_OK)
-        return st;
-    const bool pairs = use_pair_tiles(P, E);
-    const bool sparse = !pairs && use_sparse_tiles(P, E);
-    GemmArgs g;
-    g.sorted_pair = b.sorted_pair;
-    g.block_expert = b.block_expert;
-    g.pad_offsets = b.pad_offsets;
-    g.num_groups = E;
-    g.expert_tiles = 0;
-    g.w0 = g.w1 = nullptr;
-    g.num_padded = b.num_padded;
-    g.num_rows_host = cap;
-    g.q_limit = P;
-    g.k_div = k;
-    g.K = H;
-    g.n_out = I;
-    g.w_rows = I;
-    g.out = act;
-    g.out_lo = act_lo;
-    g.out_ld = I;
-    g.scale = nullptr;
-    g.status = status;
-    // fewer than a block of pairs per expert: every weight tile is read once
-    g.stream_weights = P < static_cast<int64_t>(E) * kBlockM ? 1 : 0;
-    {
-        const int nt = (I + bn_gu - 1) / bn_gu;
-        g.max_tiles = static_cast<int>(cap / kBlockM) * nt;
-        g.grid = g.max_tiles < sms ? g.max_tiles : sms;
-    }
-    if ((st = record_stage(MOE_STAGE_GATHER, stream)) != MOE_OK) return st;
-    if (!sparse) {  // the sparse GEMM gathers its x rows itself
-        MOE_CUDA(launch_gather_rows(x, H, k, b.sorted_pair, b.num_padded, P, cap, x_sorted,
-                                    pairs ? 1 : 0, sms, stream),
-                 "gather kernel launch");
-        g_launches += 1;
-    }
-    if ((st = record_stage(MOE_STAGE_GATE_UP, stream)) != MOE_OK) return st;
-    if (sparse) {
-        if (N <= kBlockM) {
-            // every expert owns at most one row block: tiles indexed by
-            // expert, the first ones' weight rows warmed into L2 during routing
-            g.expert_tiles = 1;
-            g.w0 = w_gate;
-            g.w1 = w_up;
-            g.max_tiles = E * ((I + bn_gu - 1) / bn_gu);
-            g.grid = g.max_tiles < sms ? g.max_tiles : sms;
-        }
-        MOE_CUDA(launch_sparse_gemm(kGateUp, bn_gu, tm_xrows, tm_xrows, tm_wg, tm_wu, g, stream),
-                 "gate/up kernel launch");
-        g.expert_tiles = 0;
-    } else if (pairs) {
-        const int bn = pair_gemm_block_n(kGateUp);
-        CUtensorMap tm_wg_tile, tm_wu_tile;
-        if ((st = make_map(&tm_wg_tile, w_gate, H, static_cast<uint64_t>(E) * I, H, kBlockK, bn,
-                           "w_gate")) != MOE_OK)
-            return st;
-        if ((st = make_map(&tm_wu_tile, w_up, H, static_cast<uint64_t>(E) * I, H, kBlockK, bn,
-                           "w_up")) != MOE_OK)
-            return st;
-        const int max_pairs = static_cast<int>(cap / kBlockM);  // pairs <= blocks
-        g.max_tiles = max_pairs * ((I + bn - 1) / bn);
-        g.grid = 2 * (g.max_tiles < sms / 2 ? g.max_tiles : sms / 2);
-        MOE_CUDA(launch_pair_gemm(kGateUp, tm_xsorted, tm_xsorted, tm_wg_tile, tm_wu_tile, g,
-                                  stream),
-                 "gate/up kernel launch");
-    } else {
-        MOE_CUDA(launch_gemm(kGateUp, bn_gu, tm_xrows, tm_xrows, tm_xsorted, tm_xsorted, tm_wg,
-                             tm_wu, g, stream),
-                 "gate/up kernel launch");
-    }
-    g_launches += 1;
-
-    // K4: down GEMM * routing weight, one row per pair
-    if ((st = record_stage(MOE_STAGE_DOWN, stream)) != MOE_OK) return st;
-    if ((st = make_map(&tm_act, act, I, cap, I, kBlockK, 1, "act rows")) != MOE_OK) return st;
-    if ((st = make_map(&tm_act_lo, act_lo, I, cap, I, kBlockK, 1, "act_lo rows")) != MOE_OK)
-        return st;
-    if ((st = make_map(&tm_act_box, act, I, cap, I, kBlockK, kBlockM, "act")) != MOE_OK) return st;
-    if ((st = make_map(&tm_act_lo_box, act_lo, I, cap, I, kBlockK, kBlockM, "act_lo")) != MOE_OK)
-        return st;
-    if ((st = make_map(&tm_wd, w_down, I, static_cast<uint64_t>(E) * H, I, kBlockK, kDownBN,
-                       "w_down")) != MOE_OK)
-        return st;
-    g.k_div = 1;
-    g.K = I;
-    g.n_out = H;
-    g.w_rows = H;
-    g.out = ypair;
-    g.out_lo = nullptr;
-    g.out_ld = H;
-    g.scale = topk_w;
-    {
-        const int nt = (H + kDownBN - 1) / kDownBN;
-        g.max_tiles = static_cast<int>(cap / kBlockM) * nt;
-        g.grid = g.max_tiles < sms ? g.max_tiles : sms;
-    }
-    if (sparse) {
-        MOE_CUDA(launch_sparse_gemm(kDown, kDownBN, tm_act, tm_act_lo, tm_wd, tm_wd, g, stream),
-                 "down kernel launch");
-    } else if (pairs) {
-        const int bn = pair_gemm_block_n(kDown);
-        CUtensorMap tm_wd_half;
-        if ((st = make_map(&tm_wd_half, w_down, I, static_cast<uint64_t>(E) * H, I, kBlockK,
-                           bn / 2, "w_down")) != MOE_OK)
-            return st;
-        g.max_tiles = static_cast<int>(cap / kBlockM) * ((H + bn - 1) / bn);
-        g.grid = 2 * (g.max_tiles < sms / 2 ? g.max_tiles : sms / 2);
-        MOE_CUDA(launch_pair_gemm(kDown, tm_act_box, tm_act_lo_box, tm_wd_half, tm_wd_half, g,
-                                  stream),
-                 "down kernel launch");
-    } else {
-        MOE_CUDA(launch_gemm(kDown, kDownBN, tm_act, tm_act_lo, tm_act_box, tm_act_lo_box, tm_wd,
-                             tm_wd, g, stream),
-                 "down kernel launch");
-    }
-    g_launches += 1;
 
     // shared expert: one dense group over all N tokens, weight sigmoid(x . g)
     if ((st = record_stage(MOE_STAGE_SHARED, stream)) != MOE_OK) return st;
@@ -732,6 +754,57 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
     MOE_CUDA(launch_combine(ypair, y_shared, N, H, k, out, sms, stream), "combine kernel launch");
     g_launches += 1;
     if ((st = record_stage(MOE_NUM_STAGES, stream)) != MOE_OK) return st;
+    return MOE_OK;
+}
+
+size_t moe_experts_workspace_bytes(int64_t R, int H, int E, int I) {
+    return moe_forward_workspace_bytes(R, H, E, I, 1, 0);
+}
+
+moe_status_t moe_experts(const moe_bf16_t *x_rows, const int32_t *ids, const float *weights,
+                         int64_t R, int H, int E, int I, const moe_bf16_t *w_gate,
+                         const moe_bf16_t *w_up, const moe_bf16_t *w_down, uint16_t *y,
+                         void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    g_last_error.clear();
+    if (R < 0) return fail(MOE_ERR_INVALID_ARG, "R must be >= 0 (got %lld)", (long long)R);
+    if (H < 8 || H % 8 || I < 8 || I % 8)
+        return fail(MOE_ERR_INVALID_ARG, "H and I must be positive multiples of 8 (H=%d, I=%d)", H, I);
+    if (E < 1 || E > MOE_MAX_EXPERTS)
+        return fail(MOE_ERR_UNSUPPORTED, "E must be in [1, %d] (got %d)", MOE_MAX_EXPERTS, E);
+    if (R == 0) return MOE_OK;
+    if (!x_rows || !ids || !weights || !w_gate || !w_up || !w_down || !y || !workspace)
+        return fail(MOE_ERR_INVALID_ARG, "every moe_experts pointer must be non-null");
+    if (!aligned16(x_rows) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
+        !aligned16(y))
+        return fail(MOE_ERR_INVALID_ARG, "bf16 / fp16 matrices must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
+        return fail(MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    if (R + static_cast<int64_t>(E) * kBlockM >= (int64_t(1) << 31))
+        return fail(MOE_ERR_UNSUPPORTED, "R + E*128 must stay below 2^31");
+    moe_forward_layout_t L;
+    forward_layout(R, H, E, I, 1, 0, &L);
+    if (workspace_bytes < L.total)
+        return fail(MOE_ERR_WORKSPACE_TOO_SMALL, "experts workspace needs %zu bytes, got %zu",
+                    L.total, workspace_bytes);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    MOE_CUDA(cudaMemsetAsync(ws + L.status, 0, sizeof(int32_t), stream), "status reset");
+    return enqueue_experts(x_rows, ids, weights, R, 1, H, E, I, w_gate, w_up, w_down, L, ws, y,
+                           stream);
+}
+
+moe_status_t moe_combine(const uint16_t *ypair, const uint16_t *yshared, int64_t N, int H, int k,
+                         moe_bf16_t *out, cudaStream_t stream) {
+    g_last_error.clear();
+    if (N < 0 || H < 8 || H % 8 || k < 1)
+        return fail(MOE_ERR_INVALID_ARG, "need N >= 0, H a positive multiple of 8, k >= 1");
+    if (N == 0) return MOE_OK;
+    if (!ypair || !out) return fail(MOE_ERR_INVALID_ARG, "ypair and out must be non-null");
+    if (!aligned16(ypair) || !aligned16(out) || (yshared && !aligned16(yshared)))
+        return fail(MOE_ERR_INVALID_ARG, "ypair, yshared and out must be 16-byte aligned");
+    if (N > (int64_t(1) << 31) / k) return fail(MOE_ERR_UNSUPPORTED, "N*k must stay below 2^31");
+    MOE_CUDA(launch_combine(ypair, yshared, N, H, k, out, num_sms_of_current_device(), stream),
+             "combine kernel launch");
+    g_launches += 1;
     return MOE_OK;
 }
 

@@ -34,7 +34,6 @@ constexpr int kRouterThreads = 128;
 constexpr int kATileBytes = kBlockM * 128;  // 128 tokens x 64 bf16
 constexpr int kLanesPerRow = 8;                           // lanes sharing one token row
 constexpr int kRowsPerPass = kRouterThreads / kLanesPerRow;  // 16 rows per pass
-constexpr int kMaxPerLane = MOE_MAX_EXPERTS / kLanesPerRow;  // 32 logits per lane at most
 
 struct RouterSmem {
     uint64_t full[kRouterStages];
@@ -73,14 +72,6 @@ __device__ __forceinline__ void st_dsmem_f4(uint32_t addr, float4 v) {
     asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x),
                  "f"(v.y), "f"(v.z), "f"(v.w)
                  : "memory");
-}
-
-__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr));
-    return v;
 }
 
 // the larger of two (logit, expert) keys: larger logit, then lower expert;

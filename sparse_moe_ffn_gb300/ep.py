@@ -1,0 +1,121 @@
+"""Expert parallelism: the layer's experts split across ranks.  Every rank
+routes its own tokens over all experts and exchanges its (token, slot) pairs
+with the ranks that own the chosen experts.  This is the expert-parallel
+follow-up of the M03 drill's level-3 hints, where the (token, expert) table
+drives an all-to-all dispatch and an all-to-all combine.
+
+Rank r owns experts [r * E_local, (r + 1) * E_local), E_local = ceil(E / R),
+and holds only their weights.  Per layer call, on every rank:
+
+1. route its N tokens over all E experts (moe_route: fp32 weights, ids);
+2. plan: pair p = n*k + j goes to rank ids[p] // E_local.  Pairs are sent
+   grouped by destination rank and in pair order within a rank (a stable
+   sort); the per-rank counts are exchanged first;
+3. dispatch: each pair's token row, its expert id local to the receiving
+   rank and its routing weight travel with one all_to_all each;
+4. the receiving rank runs its experts on the rows it received
+   (moe_experts: y = fp16(w * Expert(x)));
+5. combine: the results travel back with the reverse all_to_all and land in
+   pair order (ypair[p]).  moe_combine then sums each token's k slots in slot
+   order.
+
+Step 4 computes each pair as moe_forward does, and step 5 is moe_forward's
+own combine.  So the output equals moe_forward on the same tokens bit for
+bit, whatever the number of ranks.
+
+Transport: gloo and NCCL both carry int32, so bf16 and fp16 rows travel as
+their bit patterns viewed as int32 (H is even).  With one rank nothing is
+exchanged.  The three compute steps can be replaced (route_fn, experts_fn,
+combine_fn), which is how the exchange logic is tested on CPU ranks.
+"""
+from __future__ import annotations
+
+import torch
+import torch.distributed as dist
+
+
+def ep_plan(ids: torch.Tensor, E: int, world: int):
+    """Destination rank of every pair and the send order.
+
+    Returns (order, dest, send_counts, E_local): ``order`` lists the pair
+    indices p = n*k + j grouped by destination rank (stable within a rank),
+    ``dest[p]`` is the rank owning expert ids[p], ``send_counts[r]`` the
+    number of pairs sent to rank r."""
+    if world < 1:
+        raise ValueError("world must be >= 1")
+    E_local = -(-E // world)
+    flat = ids.reshape(-1).long()
+    if flat.numel() and (int(flat.min()) < 0 or int(flat.max()) >= E):
+        raise ValueError("expert ids must lie in [0, E)")
+    dest = flat // E_local
+    order = torch.sort(dest, stable=True).indices
+    send_counts = torch.bincount(dest, minlength=world)
+    return order, dest, send_counts, E_local
+
+
+def _world(group):
+    if not dist.is_available() or not dist.is_initialized():
+        return 1
+    return dist.get_world_size(group)
+
+
+def _exchange(t: torch.Tensor, send_counts, recv_counts, group):
+    """Rows of ``t`` (int32) sent in blocks of send_counts[r] rows to rank r;
+    returns the rows received, recv_counts[r] from rank r."""
+    out = torch.empty((int(sum(recv_counts)),) + tuple(t.shape[1:]), dtype=t.dtype,
+                      device=t.device)
+    dist.all_to_all_single(out, t.contiguous(), output_split_sizes=list(recv_counts),
+                           input_split_sizes=list(send_counts), group=group)
+    return out
+
+
+def ep_forward(x, router, w_gate, w_up, w_down, E: int, k: int, norm_topk_prob: bool = True,
+               group=None, route_fn=None, experts_fn=None, combine_fn=None):
+    """One MoE layer with experts split across the ranks of ``group``.
+
+    x [N, H] bf16 (this rank's tokens), router [E, H] bf16 (all experts);
+    w_gate, w_up [E_r, I, H] and w_down [E_r, H, I]: this rank's experts.
+    Returns out [N, H] bf16."""
+    from sparse_moe_ffn_gb300 import binding
+
+    world = _world(group)
+    N, H = x.shape
+    if route_fn is None:
+        def route_fn(t):
+            w, ids, _, _ = binding.moe_route_raw(t, router, k, norm_topk_prob)
+            return w, ids
+    if experts_fn is None:
+        def experts_fn(rows, local_ids, weights):
+            return binding.moe_experts(rows, local_ids, weights, w_gate, w_up, w_down)[0]
+    if combine_fn is None:
+        def combine_fn(ypair, n, kk):
+            return binding.moe_combine(ypair, n, kk)
+
+    w, ids = route_fn(x)
+    order, dest, send_counts, E_local = ep_plan(ids, E, world)
+    send_x = x.index_select(0, order // k)
+    send_e = (ids.reshape(-1).long()[order] - dest[order] * E_local).to(torch.int32)
+    send_w = w.reshape(-1)[order].contiguous()
+    if world == 1:
+        recv_x, recv_e, recv_w = send_x, send_e, send_w
+    else:
+        # counts first (gloo carries CPU tensors, NCCL device tensors)
+        comm_dev = x.device if dist.get_backend(group) == "nccl" else torch.device("cpu")
+        sc = send_counts.to(torch.int32).to(comm_dev)
+        rc = torch.empty_like(sc)
+        dist.all_to_all_single(rc, sc, group=group)
+        send_list, recv_list = sc.tolist(), rc.tolist()
+        recv_x = _exchange(send_x.view(torch.int32), send_list, recv_list,
+                           group).view(torch.bfloat16)
+        recv_e = _exchange(send_e, send_list, recv_list, group)
+        recv_w = _exchange(send_w.view(torch.int32), send_list, recv_list,
+                           group).view(torch.float32)
+    y = experts_fn(recv_x, recv_e, recv_w)
+    if world == 1:
+        y_back = y
+    else:
+        y_back = _exchange(y.view(torch.int32), recv_list, send_list,
+                           group).view(torch.float16)
+    ypair = torch.empty((N * k, H), dtype=torch.float16, device=x.device)
+    ypair[order] = y_back
+    return combine_fn(ypair, N, k)

@@ -98,6 +98,35 @@ def test_forward_host_argument_errors(L):
     assert _fwd_host(L, N=0, x_host=None) == OK       # no-op, nothing enqueued
 
 
+def _experts(L, R=64, H=2048, E=16, I=768, x=FAKE, ids=FAKE, y=FAKE, ws=FAKE * 16,
+             ws_bytes=None):
+    if ws_bytes is None:
+        ws_bytes = L.moe_experts_workspace_bytes(R, H, E, I)
+    return L.moe_experts(x, ids, FAKE, R, H, E, I, FAKE, FAKE, FAKE, y, ws, ws_bytes, None)
+
+
+def test_experts_and_combine_argument_errors(L):
+    # the expert-parallel receiving side: one routed row per (row, expert)
+    assert L.moe_experts_workspace_bytes(64, 2048, 16, 768) == \
+        L.moe_forward_workspace_bytes(64, 2048, 16, 768, 1, 0)
+    assert _experts(L, R=-1) == INVALID
+    assert _experts(L, H=2044) == INVALID
+    assert _experts(L, I=0) == INVALID
+    assert _experts(L, E=0) == UNSUPPORTED
+    assert _experts(L, ids=None) == INVALID
+    assert _experts(L, y=FAKE + 2) == INVALID
+    assert _experts(L, ws=FAKE + 64) == INVALID
+    need = L.moe_experts_workspace_bytes(64, 2048, 16, 768)
+    assert _experts(L, ws_bytes=need - 1) == SMALL
+    assert _experts(L, R=0, x=None) == OK          # no-op, nothing launched
+    P = FAKE
+    assert L.moe_combine(P, None, 16, 2048, 0, P, None) == INVALID
+    assert L.moe_combine(P, None, 16, 2044, 2, P, None) == INVALID
+    assert L.moe_combine(None, None, 16, 2048, 2, P, None) == INVALID
+    assert L.moe_combine(P, P + 2, 16, 2048, 2, P, None) == INVALID
+    assert L.moe_combine(P, None, 0, 2048, 2, None, None) == OK
+
+
 def test_route_and_align_argument_errors(L):
     P = FAKE
     assert L.moe_route(P, P, None, 16, 64, 6, 7, 1, P, P, None, None, None, 0, None) == INVALID

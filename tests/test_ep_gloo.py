@@ -1,0 +1,102 @@
+"""Expert-parallel dispatch and combine (sparse_moe_ffn_gb300/ep.py) on CPU
+ranks: two gloo processes, each routing its own tokens, with stand-in
+compute steps (a per-pair function of the token row, the global expert id
+and the weight; a slot-order fp32 sum).  Every rank's output must equal the
+same stand-ins applied pair by pair without any exchange, bit for bit, also
+when E does not split evenly and when a rank receives no pairs."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+from sparse_moe_ffn_gb300.ep import ep_plan
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _pair_value(row, e, w):
+    """Stand-in for w * Expert_e(row): any function of all three inputs."""
+    return (w * (row.float() * (e + 1) + e)).to(torch.float16)
+
+
+def _combine(ypair, n, k):
+    return ypair.float().view(n, k, -1).sum(dim=1).to(torch.bfloat16)
+
+
+def _inputs(rank, N, H, E, k, all_to_rank0):
+    g = torch.Generator().manual_seed(100 + rank)
+    x = torch.randn(N, H, generator=g).to(torch.bfloat16)
+    scores = torch.rand(N, E, generator=g)
+    if all_to_rank0:  # only experts of rank 0 ever chosen
+        scores[:, (E + 1) // 2:] = -1.0
+    ids = scores.topk(k, dim=1).indices.to(torch.int32)
+    w = torch.rand(N, k, generator=g)
+    return x, ids, w
+
+
+def _worker(rank, world, port, q, N, H, E, k, all_to_rank0):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    from sparse_moe_ffn_gb300.ep import ep_forward
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        x, ids, w = _inputs(rank, N, H, E, k, all_to_rank0)
+        E_local = -(-E // world)
+        calls = []
+
+        def experts_fn(rows, local_ids, weights):
+            calls.append(rows.shape[0])
+            if local_ids.numel():
+                assert int(local_ids.min()) >= 0 and int(local_ids.max()) < E_local
+            ge = local_ids.long() + rank * E_local
+            return torch.stack([_pair_value(rows[i], int(ge[i]), float(weights[i]))
+                                for i in range(rows.shape[0])]) if rows.shape[0] else \
+                torch.empty((0, H), dtype=torch.float16)
+
+        out = ep_forward(x, None, None, None, None, E, k, group=None,
+                         route_fn=lambda t: (w, ids), experts_fn=experts_fn,
+                         combine_fn=_combine)
+        ref_pairs = torch.stack([_pair_value(x[p // k], int(ids.view(-1)[p]), float(w.view(-1)[p]))
+                                 for p in range(N * k)])
+        ref = _combine(ref_pairs, N, k)
+        q.put((rank, bool(torch.equal(out, ref)), calls[0]))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("N,H,E,k,all_to_rank0", [(12, 16, 6, 2, False), (9, 8, 5, 3, False),
+                                                  (7, 16, 6, 2, True)])
+def test_two_ranks_match_the_unsplit_layer(N, H, E, k, all_to_rank0):
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q, N, H, E, k, all_to_rank0))
+             for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+    assert all(p.exitcode == 0 for p in procs), [p.exitcode for p in procs]
+    got = dict((r, (ok, n)) for r, ok, n in (q.get(timeout=5) for _ in range(world)))
+    assert got[0][0] and got[1][0], got
+    if all_to_rank0:
+        assert got[1][1] == 0  # rank 1 received no pairs
+
+
+def test_plan_orders_pairs_by_destination_rank():
+    ids = torch.tensor([[4, 0], [1, 5], [2, 3]], dtype=torch.int32)
+    order, dest, counts, E_local = ep_plan(ids, E=6, world=2)
+    assert E_local == 3
+    assert dest.tolist() == [1, 0, 0, 1, 0, 1]
+    assert order.tolist() == [1, 2, 4, 0, 3, 5]  # stable within each rank
+    assert counts.tolist() == [3, 3]
+    with pytest.raises(ValueError):
+        ep_plan(torch.tensor([[6]], dtype=torch.int32), E=6, world=2)

@@ -1,0 +1,105 @@
+"""The expert-parallel compute steps on one GPU: moe_experts (the receiving
+side of dispatch) and moe_combine (the last step of the combine), and the
+whole exchange path of ep_forward with one rank, against moe_forward.  Each
+(token, slot) pair is computed by the same tile kernels whatever batch it
+sits in, so all of these agree with moe_forward bit for bit.
+
+Two ranks are emulated in one process by running moe_experts once per half
+of the experts, one call after the other; no kernel waits on another."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_cases import assert_close, prepare, prepared, run_forward, sample_rows
+from sparse_moe_ffn_gb300 import binding
+from sparse_moe_ffn_gb300.ep import ep_forward, ep_plan
+from sparse_moe_ffn_gb300.inputs import MoEShape
+
+pytestmark = pytest.mark.gpu
+
+
+def _pairs(shape, ws):
+    v = binding.workspace_views(ws, shape.N, shape.H, shape.E, shape.I, shape.k)
+    return v["topk_w"].reshape(-1).clone(), v["topk_ids"].reshape(-1).clone(), v["ypair"].clone()
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill"])
+def test_experts_rows_and_combine_match_forward(name):
+    shape, dev, _ = prepared(name)
+    out, ws = run_forward(shape, dev)
+    w, ids, ypair = _pairs(shape, ws)
+    rows = dev["x"].index_select(0, torch.arange(shape.N * shape.k, device="cuda") // shape.k)
+    y, ews = binding.moe_experts(rows, ids, w, dev["w_gate"], dev["w_up"], dev["w_down"])
+    torch.cuda.synchronize()
+    assert binding.moe_read_device_status(ews) == 0
+    assert torch.equal(y, ypair)
+    assert torch.equal(binding.moe_combine(ypair, shape.N, shape.k), out)
+
+
+@pytest.mark.parametrize("name", ["decode", "prefill"])
+def test_ep_forward_one_rank_equals_forward(name):
+    shape, dev, _ = prepared(name)
+    out, _ = run_forward(shape, dev)
+    got = ep_forward(dev["x"], dev["router"], dev["w_gate"], dev["w_up"], dev["w_down"],
+                     shape.E, shape.k, shape.norm_topk_prob)
+    assert torch.equal(got, out)
+
+
+@pytest.mark.parametrize("name,world", [("decode", 2), ("prefill", 2), ("prefill", 3),
+                                        ("tiny", 4)])
+def test_expert_slices_in_one_process_equal_forward(name, world):
+    """Each 'rank' holds a contiguous slice of the experts (the last one
+    smaller when E does not split evenly) and computes only the pairs routed
+    to it; scattered back to pair order and combined, the layer is unchanged."""
+    shape, dev, bits = prepared(name)
+    out, ws = run_forward(shape, dev)
+    w, ids, _ = _pairs(shape, ws)
+    order, dest, counts, E_loc = ep_plan(ids.view(shape.N, shape.k), shape.E, world)
+    ypair = torch.empty((shape.N * shape.k, shape.H), dtype=torch.float16, device="cuda")
+    start = 0
+    for r in range(world):
+        n_r = int(counts[r])
+        sel = order[start:start + n_r]
+        start += n_r
+        e0, e1 = r * E_loc, min(shape.E, (r + 1) * E_loc)
+        if n_r == 0:
+            continue
+        y, ews = binding.moe_experts(dev["x"].index_select(0, sel // shape.k),
+                                     (ids[sel].long() - e0).to(torch.int32), w[sel],
+                                     dev["w_gate"][e0:e1], dev["w_up"][e0:e1],
+                                     dev["w_down"][e0:e1])
+        torch.cuda.synchronize()
+        assert binding.moe_read_device_status(ews) == 0
+        ypair[sel] = y
+    got = binding.moe_combine(ypair, shape.N, shape.k)
+    assert torch.equal(got, out)
+    rows = sample_rows(shape.N, 64, seed=world)
+    ref = oracle.moe_forward(bits, shape.k, shape.norm_topk_prob, rows=rows)
+    assert_close(got[torch.from_numpy(rows).cuda()], ref, f"{name} world {world}")
+
+
+def test_experts_with_empty_experts_and_one_row():
+    """Rows routed to a few of many experts, down to a single row."""
+    shape, dev, _ = prepare(MoEShape("slice", N=1, H=256, E=40, k=1, I=192), seed=9)
+    for R in (1, 7, 130):
+        g = torch.Generator().manual_seed(R)
+        x = torch.randn(R, shape.H, generator=g).to(torch.bfloat16).cuda()
+        ids = torch.randint(0, 3, (R,), generator=g).to(torch.int32).cuda() * 13  # 0, 13, 26
+        w = torch.rand(R, generator=g).cuda()
+        y, ews = binding.moe_experts(x, ids, w, dev["w_gate"], dev["w_up"], dev["w_down"])
+        torch.cuda.synchronize()
+        assert binding.moe_read_device_status(ews) == 0
+        # reference: the oracle's E = k = 1 layer is expert e's SwiGLU with
+        # routing weight 1; scale by the row's weight afterwards
+        ids_h, w_h = ids.cpu().numpy(), w.cpu().numpy().astype(np.float64)
+        ref = np.zeros((R, shape.H))
+        for e in np.unique(ids_h):
+            sel = np.nonzero(ids_h == e)[0]
+            bits = {"x": oracle.bf16_bits(x[torch.from_numpy(sel).cuda()]),
+                    "router": np.zeros((1, shape.H), np.uint16),
+                    "w_gate": oracle.bf16_bits(dev["w_gate"][e:e + 1]),
+                    "w_up": oracle.bf16_bits(dev["w_up"][e:e + 1]),
+                    "w_down": oracle.bf16_bits(dev["w_down"][e:e + 1])}
+            ref[sel] = oracle.moe_forward(bits, 1, True) * w_h[sel, None]
+        assert_close(y, ref, f"R={R}")

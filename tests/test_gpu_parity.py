@@ -186,6 +186,21 @@ def test_forward_mixed_sparse_and_dense_row_blocks():
     assert_close(out, ref, shape.name)
 
 
+def test_forward_expert_indexed_tiles_with_passes_and_empty_experts():
+    """N <= 128 with fewer than 32 pairs per expert on average: gate/up tiles
+    are indexed by expert.  Skewed routing gives the 8 hot experts 45-52
+    pairs (two 32-row passes each) and 16 experts none (their tiles take no
+    pass)."""
+    shape, dev, bits = prepare(MoEShape("expert-tiles", N=128, H=256, E=24, k=3, I=128,
+                                        skew=True), seed=5)
+    out, ws = run_forward(shape, dev)
+    counts = binding.workspace_views(ws, shape.N, shape.H, shape.E, shape.I, shape.k)["counts"]
+    counts = counts.cpu()
+    assert int(counts.max()) > 32 and int((counts == 0).sum()) >= 10
+    ref = oracle.moe_forward(bits, shape.k, shape.norm_topk_prob)
+    assert_close(out, ref, shape.name)
+
+
 def test_batch_invariance_skewed():
     """A token computed alone equals the same token inside the skewed batch,
     bit for bit (routing, grouping position and GEMM order do not depend on
