@@ -52,6 +52,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 
 # ------------------------------------------------------------------ helpers
 
+
+def check_status(ws, what):
+    """A run whose kernels recorded a device-side failure reports no number."""
+    from sparse_moe_ffn_gb300 import binding
+    status = binding.moe_read_device_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the {what}: "
+                           f"{binding.moe_status_string(status)}")
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -243,7 +252,8 @@ def run_ours(args, world, rank, local):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     cpu = make_inputs(shape, seed=args.seed)
-    d = to_device(cpu, device)
+    # model load: weights to the device, down projections converted to fp16 once
+    d = binding.prepare_weights(to_device(cpu, device))
     shared = {n: d[n] for n in binding.SHARED_KEYS} if shape.I_s else None
     ws = binding.alloc_workspace(shape.N, shape.H, shape.E, shape.I, shape.k, shape.I_s, device)
     out = torch.empty((shape.N, shape.H), dtype=torch.bfloat16, device=device)
@@ -267,9 +277,7 @@ def run_ours(args, world, rank, local):
         step()
     binding.set_stage_events(None)
     torch.cuda.synchronize()
-    status = binding.moe_read_device_status(ws)
-    if status != 0:
-        raise RuntimeError(f"device status {status}: {binding.moe_status_string(status)}")
+    check_status(ws, "warm-up")
     probe_ms = {s: probe[j].elapsed_time(probe[j + 1]) for j, s in enumerate(STAGES)}
     dom = max(("route", "gate_up", "down", "shared", "combine"), key=lambda s: probe_ms[s])
     j_dom = STAGES.index(dom)
@@ -294,6 +302,7 @@ def run_ours(args, world, rank, local):
     barrier(world)
     launches = binding.moe_kernel_launch_count() - launches0
     clocks = ClockSampler.summarize(sampler.stop(), t0, t1)
+    check_status(ws, "timed region")
     ms = start.elapsed_time(end)
     ms_max = max_over_ranks(ms, world, device)
     # roofline pass: the same K steps, the dominant kernel bracketed by events
@@ -354,6 +363,7 @@ def run_ours(args, world, rank, local):
     e2.record()
     torch.cuda.synchronize()
     barrier(world)
+    check_status(ws, "end-to-end steps")
     e2e_ms = max_over_ranks(s2.elapsed_time(e2), world, device)
     e2e = {"value": round(shape.N * args.steps * world / (e2e_ms / 1e3), 1), "unit": UNIT,
            "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),

@@ -23,8 +23,15 @@
  * Conventions shared by every entry point
  *   - All tensors are dense, row-major, on the current CUDA device, unless a
  *     parameter says "host".  bf16 data is passed as moe_bf16_t (the raw
- *     IEEE bfloat16 bit pattern).  Pointers to bf16 matrices must be 16-byte
- *     aligned; H and I must be multiples of 8 (16-byte rows for TMA).
+ *     IEEE bfloat16 bit pattern), fp16 data as moe_f16_t (IEEE binary16).
+ *     Pointers to bf16 / fp16 matrices must be 16-byte aligned; H and I must
+ *     be multiples of 8 (16-byte rows for TMA).
+ *   - Down-projection weights (w_down, shared_down_proj) are taken in fp16,
+ *     made once from the model's bf16 weights by moe_convert_bf16_to_f16:
+ *     every bf16 value of magnitude 2^-14 or more converts exactly (fp16 has
+ *     more significand bits), smaller ones round to fp16's subnormal grid
+ *     (absolute error <= 2^-25).  The down GEMM then multiplies the fp16
+ *     activation by them on the fp16 tensor-core path.
  *   - The caller owns every buffer, including the workspace.  The library
  *     never allocates, frees or synchronises (except moe_read_device_status),
  *     and keeps no state between calls: calls on different streams with
@@ -52,6 +59,8 @@ extern "C" {
 
 /* IEEE bfloat16 bit pattern. */
 typedef uint16_t moe_bf16_t;
+/* IEEE binary16 (fp16) bit pattern. */
+typedef uint16_t moe_f16_t;
 
 typedef enum {
     MOE_OK = 0,
@@ -167,32 +176,33 @@ moe_status_t moe_align_noalloc(const int32_t *topk_ids, int64_t N, int k, int E,
  *   x                 [N, H] bf16
  *   router            [E, H] bf16
  *   w_gate, w_up      [E, I, H] bf16
- *   w_down            [E, H, I] bf16
+ *   w_down            [E, H, I] fp16 (moe_convert_bf16_to_f16 of the bf16 weights)
  *   shared_gate_proj  [I_s, H] bf16 \
  *   shared_up_proj    [I_s, H] bf16  | all four NULL: no shared expert
- *   shared_down_proj  [H, I_s] bf16  | (I_s ignored); all four set: shared
+ *   shared_down_proj  [H, I_s] fp16  | (I_s ignored); all four set: shared
  *   shared_gate       [1, H]   bf16 /  expert with I_s >= 8, I_s % 8 == 0
  *   out               [N, H] bf16 out (may not alias any input)
  *   workspace         >= moe_forward_workspace_bytes(...) bytes, 256-byte
  *                     aligned; holds the routing, grouping and intermediate
  *                     activations (layout: moe_forward_layout)
  * Precision: bf16 inputs, fp32 routing and accumulation; the gate/up
- * activation a = silu(g)*u is kept as the bf16 pair (hi, lo = a - hi), both
- * fed to the down GEMM (about 16 significant bits); each pair's weighted down projection (and the gated shared expert) is
- * stored in fp16 (same bytes as bf16, 8x finer rounding); the k
- * contributions and the shared term are summed in fp32 in slot order, and
- * out is rounded to bf16 once.  A pair output beyond the fp16 range
- * (|w * Expert(x)| > 65504) records MOE_ERR_DEVICE_CHECK.  The result does
+ * activation a = silu(g)*u is stored in fp16 (11 significant bits against
+ * bf16's 8) and multiplied by the fp16 down weights; each pair's weighted
+ * down projection (and the gated shared expert) is stored in fp16 (same
+ * bytes as bf16, 8x finer rounding); the k contributions and the shared
+ * term are summed in fp32 in slot order, and out is rounded to bf16 once.
+ * An activation or pair output beyond the fp16 range (65504) records
+ * MOE_ERR_DEVICE_CHECK.  The result does
  * not depend on the other tokens of the batch and is bitwise reproducible.
  * Limits: as moe_route, plus I % 8 == 0, N*k + E*128 < 2^31.
  * ---------------------------------------------------------------------- */
 size_t moe_forward_workspace_bytes(int64_t N, int H, int E, int I, int k, int I_s);
 moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router,
                          const moe_bf16_t *w_gate, const moe_bf16_t *w_up,
-                         const moe_bf16_t *w_down,
+                         const moe_f16_t *w_down,
                          const moe_bf16_t *shared_gate_proj,
                          const moe_bf16_t *shared_up_proj,
-                         const moe_bf16_t *shared_down_proj,
+                         const moe_f16_t *shared_down_proj,
                          const moe_bf16_t *shared_gate, int64_t N, int H, int E,
                          int I, int I_s, int k, int norm_topk_prob,
                          moe_bf16_t *out, void *workspace,
@@ -205,11 +215,11 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router,
  * (token, expert) table drives an all-to-all).  For every row r:
  *   y[r] = fp16(weights[r] * Expert_{ids[r]}(x_rows[r]))
  * with the arithmetic of moe_forward's per-pair outputs (grouping by expert,
- * gate/up with the hi/lo activation, down), so the bits equal the pair rows
+ * gate/up with the fp16 activation, down), so the bits equal the pair rows
  * moe_forward produces for the same (row, expert, weight).
  *   x_rows   [R, H] bf16      ids [R] int32 in [0, E)      weights [R] fp32
- *   w_gate, w_up [E, I, H], w_down [E, H, I] bf16: the experts this call
- *            serves (a rank's slice of the layer's experts)
+ *   w_gate, w_up [E, I, H] bf16, w_down [E, H, I] fp16: the experts this
+ *            call serves (a rank's slice of the layer's experts)
  *   y        [R, H] fp16 out
  *   workspace >= moe_experts_workspace_bytes(R, H, E, I) bytes, 256-byte
  *            aligned; its first 4 bytes are the status word
@@ -221,7 +231,7 @@ size_t moe_experts_workspace_bytes(int64_t R, int H, int E, int I);
 moe_status_t moe_experts(const moe_bf16_t *x_rows, const int32_t *ids,
                          const float *weights, int64_t R, int H, int E, int I,
                          const moe_bf16_t *w_gate, const moe_bf16_t *w_up,
-                         const moe_bf16_t *w_down, uint16_t *y, void *workspace,
+                         const moe_f16_t *w_down, moe_f16_t *y, void *workspace,
                          size_t workspace_bytes, cudaStream_t stream);
 
 /* -------------------------------------------------------------------------
@@ -232,8 +242,20 @@ moe_status_t moe_experts(const moe_bf16_t *x_rows, const int32_t *ids,
  * NULL, out [N, H] bf16; 16-byte aligned.  moe_forward ends with the same
  * kernel.
  * ---------------------------------------------------------------------- */
-moe_status_t moe_combine(const uint16_t *ypair, const uint16_t *yshared, int64_t N, int H,
+moe_status_t moe_combine(const moe_f16_t *ypair, const moe_f16_t *yshared, int64_t N, int H,
                          int k, moe_bf16_t *out, cudaStream_t stream);
+
+/* -------------------------------------------------------------------------
+ * moe_convert_bf16_to_f16 -- the load-time step that makes the fp16 down
+ * weights every entry point takes: dst[i] = fp16(src[i]) for i < n, round to
+ * nearest even (exact for |src| >= 2^-14 and for zero; below, the nearest
+ * fp16 subnormal).  src, dst: device, 16-byte aligned, not overlapping.
+ * device_status (nullable, int32 on the device) is set to
+ * MOE_ERR_DEVICE_CHECK if some |src[i]| exceeds fp16's range (65504; such
+ * a value becomes infinity) or is NaN; it is left untouched otherwise.
+ * ---------------------------------------------------------------------- */
+moe_status_t moe_convert_bf16_to_f16(const moe_bf16_t *src, moe_f16_t *dst, int64_t n,
+                                     int32_t *device_status, cudaStream_t stream);
 
 /* -------------------------------------------------------------------------
  * moe_forward_host -- moe_forward for activations that live in host memory:
@@ -252,10 +274,10 @@ moe_status_t moe_combine(const uint16_t *ypair, const uint16_t *yshared, int64_t
 moe_status_t moe_forward_host(const moe_bf16_t *x_host, moe_bf16_t *out_host,
                               moe_bf16_t *x_dev, moe_bf16_t *out_dev,
                               const moe_bf16_t *router, const moe_bf16_t *w_gate,
-                              const moe_bf16_t *w_up, const moe_bf16_t *w_down,
+                              const moe_bf16_t *w_up, const moe_f16_t *w_down,
                               const moe_bf16_t *shared_gate_proj,
                               const moe_bf16_t *shared_up_proj,
-                              const moe_bf16_t *shared_down_proj,
+                              const moe_f16_t *shared_down_proj,
                               const moe_bf16_t *shared_gate, int64_t N, int H, int E,
                               int I, int I_s, int k, int norm_topk_prob,
                               void *workspace, size_t workspace_bytes,
@@ -286,13 +308,13 @@ moe_status_t moe_add_rmsnorm(const moe_bf16_t *x, moe_bf16_t *residual,
  * Qwen3.5 walkthrough): out = (silu(x Wg^T) * (x Wu^T)) Wd^T, the layer with
  * E = k = 1, run on the same grouped GEMM kernels as one dense group.
  *
- *   x [N, H], w_gate / w_up [I, H], w_down [H, I], out [N, H]: bf16
+ *   x [N, H], w_gate / w_up [I, H], out [N, H]: bf16; w_down [H, I]: fp16
  *   workspace >= moe_dense_mlp_workspace_bytes(N, H, I), 256-byte aligned
  * Precision as moe_forward.  Limits: H % 8 == 0, I % 8 == 0.
  * ---------------------------------------------------------------------- */
 size_t moe_dense_mlp_workspace_bytes(int64_t N, int H, int I);
 moe_status_t moe_dense_mlp(const moe_bf16_t *x, const moe_bf16_t *w_gate,
-                           const moe_bf16_t *w_up, const moe_bf16_t *w_down,
+                           const moe_bf16_t *w_up, const moe_f16_t *w_down,
                            int64_t N, int H, int I, moe_bf16_t *out,
                            void *workspace, size_t workspace_bytes,
                            cudaStream_t stream);
@@ -312,11 +334,9 @@ typedef struct {
     size_t sorted_pair;   /* int32 [capacity]                                 */
     size_t block_expert;  /* int32 [capacity / 128]                           */
     size_t x_sorted;      /* bf16 [capacity, H]   x rows in expert order (dense blocks) */
-    size_t act;           /* bf16 [capacity, I]   a_hi = bf16(a), a = silu(x Wg^T) * (x Wu^T) */
-    size_t act_lo;        /* bf16 [capacity, I]   a_lo = bf16(a - a_hi)       */
+    size_t act;           /* fp16 [capacity, I]   a = silu(x Wg^T) * (x Wu^T)  */
     size_t ypair;         /* fp16 [N*k, H]        w * Expert(x), per pair     */
-    size_t act_shared;    /* bf16 [round_up(N,128), I_s] hi (shared only)     */
-    size_t act_shared_lo; /* bf16 [round_up(N,128), I_s] lo (shared only)     */
+    size_t act_shared;    /* fp16 [round_up(N,128), I_s] (shared only)        */
     size_t y_shared;      /* fp16 [N, H]  gamma * SharedMLP(x) (shared only)  */
     size_t total;         /* = moe_forward_workspace_bytes                    */
     int64_t capacity;     /* moe_align_capacity(N, k, E, 128)                 */

@@ -28,9 +28,8 @@ class MoEError(RuntimeError):
 class _Layout(ctypes.Structure):
     _fields_ = [(name, ctypes.c_size_t) for name in (
         "status", "topk_w", "topk_ids", "gamma", "counts", "offsets", "pad_offsets",
-        "num_padded", "align_scratch", "sorted_pair", "block_expert", "x_sorted", "act", "act_lo",
-        "ypair",
-        "act_shared", "act_shared_lo", "y_shared", "total")] + [("capacity", ctypes.c_int64)]
+        "num_padded", "align_scratch", "sorted_pair", "block_expert", "x_sorted", "act", "ypair",
+        "act_shared", "y_shared", "total")] + [("capacity", ctypes.c_int64)]
 
 
 _lib = None
@@ -59,6 +58,7 @@ def lib():
         "moe_experts_workspace_bytes": ([i64, i32, i32, i32], sz),
         "moe_experts": ([P, P, P, i64, i32, i32, i32, P, P, P, P, P, sz, P], i32),
         "moe_combine": ([P, P, i64, i32, i32, P, P], i32),
+        "moe_convert_bf16_to_f16": ([P, P, i64, P, P], i32),
         "moe_forward_layout": ([i64, i32, i32, i32, i32, i32, ctypes.POINTER(_Layout)], i32),
         "moe_read_device_status": ([P, P], i32),
         "moe_kernel_launch_count": ([], ctypes.c_uint64),
@@ -96,6 +96,15 @@ def _stream():
 def _bf16(t, name, shape=None):
     if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+def _f16(t, name, shape=None):
+    if t.dtype != torch.float16 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous fp16 CUDA tensor "
+                         "(convert the bf16 weights once with prepare_weights)")
     if shape is not None and tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
     return t
@@ -200,14 +209,16 @@ def alloc_workspace(N, H, E, I, k, I_s=0, device="cuda"):
 def moe_forward(x, router, w_gate, w_up, w_down, k: int, norm_topk_prob: bool = True,
                 shared=None, out=None, workspace=None):
     """The whole layer.  ``shared`` is None or a dict with shared_gate_proj,
-    shared_up_proj, shared_down_proj and shared_gate.  Returns out [N, H] bf16."""
+    shared_up_proj, shared_down_proj and shared_gate.  w_down and
+    shared_down_proj are fp16 (``prepare_weights``), every other tensor bf16.
+    Returns out [N, H] bf16."""
     N, H = x.shape
     E, I, _ = w_gate.shape
     _bf16(x, "x")
     _bf16(router, "router", (E, H))
     _bf16(w_gate, "w_gate", (E, I, H))
     _bf16(w_up, "w_up", (E, I, H))
-    _bf16(w_down, "w_down", (E, H, I))
+    _f16(w_down, "w_down", (E, H, I))
     sp = [None] * 4
     I_s = 0
     if shared is not None:
@@ -215,7 +226,7 @@ def moe_forward(x, router, w_gate, w_up, w_down, k: int, norm_topk_prob: bool = 
         I_s = sp[0].shape[0]
         _bf16(sp[0], "shared_gate_proj", (I_s, H))
         _bf16(sp[1], "shared_up_proj", (I_s, H))
-        _bf16(sp[2], "shared_down_proj", (H, I_s))
+        _f16(sp[2], "shared_down_proj", (H, I_s))
         _bf16(sp[3], "shared_gate", (1, H))
     if out is None:
         out = torch.empty((N, H), dtype=torch.bfloat16, device=x.device)
@@ -250,7 +261,7 @@ def moe_dense_mlp(x, w_gate, w_up, w_down, out=None, workspace=None):
     _bf16(x, "x")
     _bf16(w_gate, "w_gate", (I, H))
     _bf16(w_up, "w_up", (I, H))
-    _bf16(w_down, "w_down", (H, I))
+    _f16(w_down, "w_down", (H, I))
     if out is None:
         out = torch.empty((N, H), dtype=torch.bfloat16, device=x.device)
     _bf16(out, "out", (N, H))
@@ -271,7 +282,7 @@ def moe_experts(x_rows, ids, weights, w_gate, w_up, w_down, y=None, workspace=No
     _bf16(x_rows, "x_rows")
     _bf16(w_gate, "w_gate", (E, I, H))
     _bf16(w_up, "w_up", (E, I, H))
-    _bf16(w_down, "w_down", (E, H, I))
+    _f16(w_down, "w_down", (E, H, I))
     if ids.dtype != torch.int32 or not ids.is_cuda or tuple(ids.shape) != (R,):
         raise ValueError("ids must be a CUDA int32 tensor of shape [R]")
     if weights.dtype != torch.float32 or not weights.is_cuda or tuple(weights.shape) != (R,):
@@ -305,6 +316,40 @@ def moe_combine(ypair, N: int, k: int, yshared=None, out=None):
     return out
 
 
+def convert_bf16_to_f16(src, out=None, status=None):
+    """fp16 copy of a bf16 CUDA tensor (round to nearest even; exact for
+    |v| >= 2^-14).  ``status`` (int32 CUDA tensor, optional) receives
+    MOE_ERR_DEVICE_CHECK when a value exceeds fp16's range or is NaN."""
+    if src.dtype != torch.bfloat16 or not src.is_cuda or not src.is_contiguous():
+        raise ValueError("src must be a contiguous bf16 CUDA tensor")
+    if out is None:
+        out = torch.empty(src.shape, dtype=torch.float16, device=src.device)
+    _f16(out, "out", src.shape)
+    _check(lib().moe_convert_bf16_to_f16(_ptr(src), _ptr(out), src.numel(), _ptr(status),
+                                         _stream()), "moe_convert_bf16_to_f16")
+    return out
+
+
+DOWN_KEYS = ("w_down", "shared_down_proj")
+
+
+def prepare_weights(weights: dict) -> dict:
+    """The layer's weights in the form every entry point takes: the same dict
+    with the down projections (w_down, shared_down_proj) converted to fp16
+    once; bf16 entries pass through.  Raises if a down weight is outside
+    fp16's range."""
+    out = dict(weights)
+    dev = next(t.device for t in weights.values() if torch.is_tensor(t))
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    for name in DOWN_KEYS:
+        if name in weights and weights[name].dtype == torch.bfloat16:
+            out[name] = convert_bf16_to_f16(weights[name], status=status)
+    code = int(status.item())
+    if code != MOE_OK:
+        raise MoEError(code, "prepare_weights: a down-projection weight exceeds fp16's range")
+    return out
+
+
 def moe_forward_from_host(x_host, out_host, x_dev, out_dev, weights: dict, k: int,
                           norm_topk_prob: bool, workspace):
     """End-to-end call with host buffers through moe_forward_host: x (pinned
@@ -321,7 +366,10 @@ def moe_forward_from_host(x_host, out_host, x_dev, out_dev, weights: dict, k: in
         raise ValueError("x_host and out_host must be contiguous [N, H]")
     _bf16(x_dev, "x_dev", (N, H))
     _bf16(out_dev, "out_dev", (N, H))
+    _f16(weights["w_down"], "w_down", (E, H, I))
     shared = "shared_gate" in weights
+    if shared:
+        _f16(weights["shared_down_proj"], "shared_down_proj")
     sp = [weights[n] if shared else None for n in SHARED_KEYS]
     I_s = weights["shared_gate_proj"].shape[0] if shared else 0
     _check(lib().moe_forward_host(x_host.data_ptr(), out_host.data_ptr(), _ptr(x_dev),
@@ -403,15 +451,13 @@ def workspace_views(workspace, N, H, E, I, k, I_s=0) -> dict:
         "sorted_pair": view(lay["sorted_pair"], torch.int32, (cap,)),
         "block_expert": view(lay["block_expert"], torch.int32, (cap // MOE_BLOCK_M,)),
         "x_sorted": view(lay["x_sorted"], torch.bfloat16, (cap, H)),
-        "act": view(lay["act"], torch.bfloat16, (cap, I)),
-        "act_lo": view(lay["act_lo"], torch.bfloat16, (cap, I)),
+        "act": view(lay["act"], torch.float16, (cap, I)),
         "ypair": view(lay["ypair"], torch.float16, (P, H)),
     }
     if I_s:
         rows_s = -(-N // MOE_BLOCK_M) * MOE_BLOCK_M
         v["gamma"] = view(lay["gamma"], torch.float32, (N,))
-        v["act_shared"] = view(lay["act_shared"], torch.bfloat16, (rows_s, I_s))
-        v["act_shared_lo"] = view(lay["act_shared_lo"], torch.bfloat16, (rows_s, I_s))
+        v["act_shared"] = view(lay["act_shared"], torch.float16, (rows_s, I_s))
         v["y_shared"] = view(lay["y_shared"], torch.float16, (N, H))
     return v
 

@@ -65,8 +65,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
     return fn;
 }
 
-// bf16 matrix [rows, cols] (row stride `ld` elements), 128-byte swizzled box
-// of box_rows x box_cols (box_cols * 2 <= 128).  Out-of-range elements read 0.
+// 16-bit matrix [rows, cols] (row stride `ld` elements), 128-byte swizzled
+// box of box_rows x box_cols (box_cols * 2 <= 128).  Out-of-range elements
+// read 0.  Used for bf16 and fp16 data alike: the copy moves 16-bit elements
+// unchanged, and zero has the same bits in both formats.
 moe_status_t make_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows,
                       uint64_t ld, uint32_t box_cols, uint32_t box_rows, const char *what) {
     auto fn = encode_tiled();
@@ -274,10 +276,8 @@ moe_status_t forward_layout(int64_t N, int H, int E, int I, int k, int I_s,
     L->block_expert = take(sizeof(int32_t) * (cap / kBlockM));
     L->x_sorted = take(2 * static_cast<size_t>(cap) * H);
     L->act = take(2 * static_cast<size_t>(cap) * I);
-    L->act_lo = take(2 * static_cast<size_t>(cap) * I);
     L->ypair = take(2 * static_cast<size_t>(P) * H);  // fp16
     L->act_shared = take(shared ? 2 * static_cast<size_t>(round_up64(N, kBlockM)) * I_s : 0);
-    L->act_shared_lo = take(shared ? 2 * static_cast<size_t>(round_up64(N, kBlockM)) * I_s : 0);
     L->y_shared = take(shared ? 2 * static_cast<size_t>(N) * H : 0);  // fp16
     L->total = off;
     L->capacity = cap;
@@ -289,9 +289,9 @@ moe_status_t forward_layout(int64_t N, int H, int E, int I, int k, int I_s,
 // the workspace layout.
 moe_status_t check_forward_args(const moe_bf16_t *x, const moe_bf16_t *router,
                                 const moe_bf16_t *w_gate, const moe_bf16_t *w_up,
-                                const moe_bf16_t *w_down, const moe_bf16_t *shared_gate_proj,
+                                const moe_f16_t *w_down, const moe_bf16_t *shared_gate_proj,
                                 const moe_bf16_t *shared_up_proj,
-                                const moe_bf16_t *shared_down_proj, const moe_bf16_t *shared_gate,
+                                const moe_f16_t *shared_down_proj, const moe_bf16_t *shared_gate,
                                 int64_t N, int H, int E, int I, int I_s, int k,
                                 const moe_bf16_t *out, const void *workspace,
                                 size_t workspace_bytes, bool *shared_out,
@@ -337,7 +337,7 @@ moe_status_t check_forward_args(const moe_bf16_t *x, const moe_bf16_t *router,
 // is not reset here.  Records the align .. down stage events.
 moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const float *weights,
                              int64_t N, int k, int H, int E, int I, const moe_bf16_t *w_gate,
-                             const moe_bf16_t *w_up, const moe_bf16_t *w_down,
+                             const moe_bf16_t *w_up, const moe_f16_t *w_down,
                              const moe_forward_layout_t &L, uint8_t *ws, uint16_t *ypair,
                              cudaStream_t stream) {
     moe_status_t st;
@@ -345,7 +345,6 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
     int32_t *status = reinterpret_cast<int32_t *>(at(L.status));
     uint16_t *x_sorted = reinterpret_cast<uint16_t *>(at(L.x_sorted));
     uint16_t *act = reinterpret_cast<uint16_t *>(at(L.act));
-    uint16_t *act_lo = reinterpret_cast<uint16_t *>(at(L.act_lo));
     const int64_t P = N * k;
     const int64_t cap = L.capacity;
     const int sms = num_sms_of_current_device();
@@ -365,8 +364,7 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
     if (st != MOE_OK) return st;
 
     // K3: gathered gate/up GEMM + silu * up
-    CUtensorMap tm_xrows, tm_xsorted, tm_wg, tm_wu, tm_act, tm_act_lo, tm_act_box, tm_act_lo_box,
-        tm_wd;
+    CUtensorMap tm_xrows, tm_xsorted, tm_wg, tm_wu, tm_act, tm_act_box, tm_wd;
     if ((st = make_map(&tm_xrows, x, H, N, H, kBlockK, 1, "x rows")) != MOE_OK) return st;
     if ((st = make_map(&tm_xsorted, x_sorted, H, cap, H, kBlockK, kBlockM, "x_sorted")) != MOE_OK)
         return st;
@@ -394,7 +392,6 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
     g.n_out = I;
     g.w_rows = I;
     g.out = act;
-    g.out_lo = act_lo;
     g.out_ld = I;
     g.scale = nullptr;
     g.status = status;
@@ -423,7 +420,7 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
             g.max_tiles = E * ((I + bn_gu - 1) / bn_gu);
             g.grid = g.max_tiles < sms ? g.max_tiles : sms;
         }
-        MOE_CUDA(launch_sparse_gemm(kGateUp, bn_gu, tm_xrows, tm_xrows, tm_wg, tm_wu, g, stream),
+        MOE_CUDA(launch_sparse_gemm(kGateUp, bn_gu, tm_xrows, tm_wg, tm_wu, g, stream),
                  "gate/up kernel launch");
         g.expert_tiles = 0;
     } else if (pairs) {
@@ -438,12 +435,10 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
         const int max_pairs = static_cast<int>(cap / kBlockM);  // pairs <= blocks
         g.max_tiles = max_pairs * ((I + bn - 1) / bn);
         g.grid = 2 * (g.max_tiles < sms / 2 ? g.max_tiles : sms / 2);
-        MOE_CUDA(launch_pair_gemm(kGateUp, tm_xsorted, tm_xsorted, tm_wg_tile, tm_wu_tile, g,
-                                  stream),
+        MOE_CUDA(launch_pair_gemm(kGateUp, tm_xsorted, tm_wg_tile, tm_wu_tile, g, stream),
                  "gate/up kernel launch");
     } else {
-        MOE_CUDA(launch_gemm(kGateUp, bn_gu, tm_xrows, tm_xrows, tm_xsorted, tm_xsorted, tm_wg,
-                             tm_wu, g, stream),
+        MOE_CUDA(launch_gemm(kGateUp, bn_gu, tm_xrows, tm_xsorted, tm_wg, tm_wu, g, stream),
                  "gate/up kernel launch");
     }
     g_launches += 1;
@@ -451,11 +446,7 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
     // K4: down GEMM * routing weight, one row per pair
     if ((st = record_stage(MOE_STAGE_DOWN, stream)) != MOE_OK) return st;
     if ((st = make_map(&tm_act, act, I, cap, I, kBlockK, 1, "act rows")) != MOE_OK) return st;
-    if ((st = make_map(&tm_act_lo, act_lo, I, cap, I, kBlockK, 1, "act_lo rows")) != MOE_OK)
-        return st;
     if ((st = make_map(&tm_act_box, act, I, cap, I, kBlockK, kBlockM, "act")) != MOE_OK) return st;
-    if ((st = make_map(&tm_act_lo_box, act_lo, I, cap, I, kBlockK, kBlockM, "act_lo")) != MOE_OK)
-        return st;
     if ((st = make_map(&tm_wd, w_down, I, static_cast<uint64_t>(E) * H, I, kBlockK, kDownBN,
                        "w_down")) != MOE_OK)
         return st;
@@ -464,7 +455,6 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
     g.n_out = H;
     g.w_rows = H;
     g.out = ypair;
-    g.out_lo = nullptr;
     g.out_ld = H;
     g.scale = weights;
     {
@@ -473,7 +463,7 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
         g.grid = g.max_tiles < sms ? g.max_tiles : sms;
     }
     if (sparse) {
-        MOE_CUDA(launch_sparse_gemm(kDown, kDownBN, tm_act, tm_act_lo, tm_wd, tm_wd, g, stream),
+        MOE_CUDA(launch_sparse_gemm(kDown, kDownBN, tm_act, tm_wd, tm_wd, g, stream),
                  "down kernel launch");
     } else if (pairs) {
         const int bn = pair_gemm_block_n(kDown);
@@ -483,12 +473,10 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
             return st;
         g.max_tiles = static_cast<int>(cap / kBlockM) * ((H + bn - 1) / bn);
         g.grid = 2 * (g.max_tiles < sms / 2 ? g.max_tiles : sms / 2);
-        MOE_CUDA(launch_pair_gemm(kDown, tm_act_box, tm_act_lo_box, tm_wd_half, tm_wd_half, g,
-                                  stream),
+        MOE_CUDA(launch_pair_gemm(kDown, tm_act_box, tm_wd_half, tm_wd_half, g, stream),
                  "down kernel launch");
     } else {
-        MOE_CUDA(launch_gemm(kDown, kDownBN, tm_act, tm_act_lo, tm_act_box, tm_act_lo_box, tm_wd,
-                             tm_wd, g, stream),
+        MOE_CUDA(launch_gemm(kDown, kDownBN, tm_act, tm_act_box, tm_wd, tm_wd, g, stream),
                  "down kernel launch");
     }
     g_launches += 1;
@@ -612,9 +600,9 @@ size_t moe_forward_workspace_bytes(int64_t N, int H, int E, int I, int k, int I_
 }
 
 moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const moe_bf16_t *w_gate,
-                         const moe_bf16_t *w_up, const moe_bf16_t *w_down,
+                         const moe_bf16_t *w_up, const moe_f16_t *w_down,
                          const moe_bf16_t *shared_gate_proj, const moe_bf16_t *shared_up_proj,
-                         const moe_bf16_t *shared_down_proj, const moe_bf16_t *shared_gate,
+                         const moe_f16_t *shared_down_proj, const moe_bf16_t *shared_gate,
                          int64_t N, int H, int E, int I, int I_s, int k, int norm_topk_prob,
                          moe_bf16_t *out, void *workspace, size_t workspace_bytes,
                          cudaStream_t stream) {
@@ -653,10 +641,9 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
     uint16_t *y_shared = nullptr;
     if (shared) {
         uint16_t *act_s = reinterpret_cast<uint16_t *>(at(L.act_shared));
-        uint16_t *act_s_lo = reinterpret_cast<uint16_t *>(at(L.act_shared_lo));
         y_shared = reinterpret_cast<uint16_t *>(at(L.y_shared));
         const int64_t rows_s = round_up64(N, kBlockM);
-        CUtensorMap tm_sg, tm_su, tm_acts, tm_acts_lo, tm_sd, tm_xbox;
+        CUtensorMap tm_sg, tm_su, tm_acts, tm_sd, tm_xbox;
         const int bn_s = choose_gate_up_bn(static_cast<double>(rows_s / kBlockM),
                                            static_cast<double>(N), I_s, sms);
         if ((st = make_map(&tm_xbox, x, H, N, H, kBlockK, kBlockM, "x")) != MOE_OK) return st;
@@ -668,9 +655,6 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
             return st;
         if ((st = make_map(&tm_acts, act_s, I_s, rows_s, I_s, kBlockK, kBlockM,
                            "shared act rows")) != MOE_OK)
-            return st;
-        if ((st = make_map(&tm_acts_lo, act_s_lo, I_s, rows_s, I_s, kBlockK, kBlockM,
-                           "shared act_lo rows")) != MOE_OK)
             return st;
         if ((st = make_map(&tm_sd, shared_down_proj, I_s, H, I_s, kBlockK, kDownBN,
                            "shared_down_proj")) != MOE_OK)
@@ -690,7 +674,6 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
         s.n_out = I_s;
         s.w_rows = I_s;
         s.out = act_s;
-        s.out_lo = act_s_lo;
         s.out_ld = I_s;
         s.scale = nullptr;
         s.status = status;
@@ -712,18 +695,16 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
                 return st;
             s.max_tiles = static_cast<int>((rows_s / kBlockM + 1) / 2) * ((I_s + bn - 1) / bn);
             s.grid = 2 * (s.max_tiles < sms / 2 ? s.max_tiles : sms / 2);
-            MOE_CUDA(launch_pair_gemm(kGateUp, tm_xbox, tm_xbox, tm_sg2, tm_su2, s, stream),
+            MOE_CUDA(launch_pair_gemm(kGateUp, tm_xbox, tm_sg2, tm_su2, s, stream),
                      "shared gate/up kernel launch");
         } else {
-            MOE_CUDA(launch_gemm(kGateUp, bn_s, tm_xbox, tm_xbox, tm_xbox, tm_xbox, tm_sg, tm_su,
-                                 s, stream),
+            MOE_CUDA(launch_gemm(kGateUp, bn_s, tm_xbox, tm_xbox, tm_sg, tm_su, s, stream),
                      "shared gate/up kernel launch");
         }
         s.K = I_s;
         s.n_out = H;
         s.w_rows = H;
         s.out = y_shared;
-        s.out_lo = nullptr;
         s.out_ld = H;
         s.scale = gamma;
         {
@@ -739,11 +720,10 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
                 return st;
             s.max_tiles = static_cast<int>((rows_s / kBlockM + 1) / 2) * ((H + bn - 1) / bn);
             s.grid = 2 * (s.max_tiles < sms / 2 ? s.max_tiles : sms / 2);
-            MOE_CUDA(launch_pair_gemm(kDown, tm_acts, tm_acts_lo, tm_sd2, tm_sd2, s, stream),
+            MOE_CUDA(launch_pair_gemm(kDown, tm_acts, tm_sd2, tm_sd2, s, stream),
                      "shared down kernel launch");
         } else {
-            MOE_CUDA(launch_gemm(kDown, kDownBN, tm_acts, tm_acts_lo, tm_acts, tm_acts_lo, tm_sd,
-                                 tm_sd, s, stream),
+            MOE_CUDA(launch_gemm(kDown, kDownBN, tm_acts, tm_acts, tm_sd, tm_sd, s, stream),
                      "shared down kernel launch");
         }
         g_launches += 2;
@@ -763,7 +743,7 @@ size_t moe_experts_workspace_bytes(int64_t R, int H, int E, int I) {
 
 moe_status_t moe_experts(const moe_bf16_t *x_rows, const int32_t *ids, const float *weights,
                          int64_t R, int H, int E, int I, const moe_bf16_t *w_gate,
-                         const moe_bf16_t *w_up, const moe_bf16_t *w_down, uint16_t *y,
+                         const moe_bf16_t *w_up, const moe_f16_t *w_down, moe_f16_t *y,
                          void *workspace, size_t workspace_bytes, cudaStream_t stream) {
     g_last_error.clear();
     if (R < 0) return fail(MOE_ERR_INVALID_ARG, "R must be >= 0 (got %lld)", (long long)R);
@@ -792,8 +772,8 @@ moe_status_t moe_experts(const moe_bf16_t *x_rows, const int32_t *ids, const flo
                            stream);
 }
 
-moe_status_t moe_combine(const uint16_t *ypair, const uint16_t *yshared, int64_t N, int H, int k,
-                         moe_bf16_t *out, cudaStream_t stream) {
+moe_status_t moe_combine(const moe_f16_t *ypair, const moe_f16_t *yshared, int64_t N, int H,
+                         int k, moe_bf16_t *out, cudaStream_t stream) {
     g_last_error.clear();
     if (N < 0 || H < 8 || H % 8 || k < 1)
         return fail(MOE_ERR_INVALID_ARG, "need N >= 0, H a positive multiple of 8, k >= 1");
@@ -808,12 +788,31 @@ moe_status_t moe_combine(const uint16_t *ypair, const uint16_t *yshared, int64_t
     return MOE_OK;
 }
 
+moe_status_t moe_convert_bf16_to_f16(const moe_bf16_t *src, moe_f16_t *dst, int64_t n,
+                                     int32_t *device_status, cudaStream_t stream) {
+    g_last_error.clear();
+    if (n < 0) return fail(MOE_ERR_INVALID_ARG, "n must be >= 0 (got %lld)", (long long)n);
+    if (n == 0) return MOE_OK;
+    if (!src || !dst) return fail(MOE_ERR_INVALID_ARG, "src and dst must be non-null");
+    if (!aligned16(src) || !aligned16(dst))
+        return fail(MOE_ERR_INVALID_ARG, "src and dst must be 16-byte aligned");
+    const uintptr_t s0 = reinterpret_cast<uintptr_t>(src), d0 = reinterpret_cast<uintptr_t>(dst);
+    const uintptr_t bytes = static_cast<uintptr_t>(n) * 2;
+    if (s0 < d0 + bytes && d0 < s0 + bytes)
+        return fail(MOE_ERR_INVALID_ARG, "src and dst must not overlap");
+    MOE_CUDA(launch_convert_bf16_to_f16(src, dst, n, device_status, num_sms_of_current_device(),
+                                        stream),
+             "convert kernel launch");
+    g_launches += 1;
+    return MOE_OK;
+}
+
 moe_status_t moe_forward_host(const moe_bf16_t *x_host, moe_bf16_t *out_host, moe_bf16_t *x_dev,
                               moe_bf16_t *out_dev, const moe_bf16_t *router,
                               const moe_bf16_t *w_gate, const moe_bf16_t *w_up,
-                              const moe_bf16_t *w_down, const moe_bf16_t *shared_gate_proj,
+                              const moe_f16_t *w_down, const moe_bf16_t *shared_gate_proj,
                               const moe_bf16_t *shared_up_proj,
-                              const moe_bf16_t *shared_down_proj, const moe_bf16_t *shared_gate,
+                              const moe_f16_t *shared_down_proj, const moe_bf16_t *shared_gate,
                               int64_t N, int H, int E, int I, int I_s, int k, int norm_topk_prob,
                               void *workspace, size_t workspace_bytes, cudaStream_t stream) {
     g_last_error.clear();
@@ -863,11 +862,11 @@ moe_status_t moe_add_rmsnorm(const moe_bf16_t *x, moe_bf16_t *residual, const mo
 size_t moe_dense_mlp_workspace_bytes(int64_t N, int H, int I) {
     if (N < 0 || H < 1 || I < 1) return 0;
     const size_t rows = static_cast<size_t>(round_up64(N, kBlockM));
-    return kAlign + 2 * round_up(2 * rows * I, kAlign) + round_up(2 * static_cast<size_t>(N) * H, kAlign);
+    return kAlign + round_up(2 * rows * I, kAlign) + round_up(2 * static_cast<size_t>(N) * H, kAlign);
 }
 
 moe_status_t moe_dense_mlp(const moe_bf16_t *x, const moe_bf16_t *w_gate, const moe_bf16_t *w_up,
-                           const moe_bf16_t *w_down, int64_t N, int H, int I, moe_bf16_t *out,
+                           const moe_f16_t *w_down, int64_t N, int H, int I, moe_bf16_t *out,
                            void *workspace, size_t workspace_bytes, cudaStream_t stream) {
     g_last_error.clear();
     if (N < 0) return fail(MOE_ERR_INVALID_ARG, "N must be >= 0");
@@ -890,17 +889,15 @@ moe_status_t moe_dense_mlp(const moe_bf16_t *x, const moe_bf16_t *w_gate, const 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     int32_t *status = reinterpret_cast<int32_t *>(ws);
     uint16_t *act = reinterpret_cast<uint16_t *>(ws + kAlign);
-    uint16_t *act_lo = reinterpret_cast<uint16_t *>(ws + kAlign + round_up(2 * rows * I, kAlign));
-    uint16_t *y = reinterpret_cast<uint16_t *>(ws + kAlign + 2 * round_up(2 * rows * I, kAlign));
+    uint16_t *y = reinterpret_cast<uint16_t *>(ws + kAlign + round_up(2 * rows * I, kAlign));
     const int sms = num_sms_of_current_device();
     moe_status_t st;
-    CUtensorMap tm_x, tm_g, tm_u, tm_act, tm_act_lo, tm_d;
+    CUtensorMap tm_x, tm_g, tm_u, tm_act, tm_d;
     const int bn = choose_gate_up_bn(static_cast<double>(rows / kBlockM), static_cast<double>(N), I, sms);
     if ((st = make_map(&tm_x, x, H, N, H, kBlockK, kBlockM, "x")) != MOE_OK) return st;
     if ((st = make_map(&tm_g, w_gate, H, I, H, kBlockK, bn, "w_gate")) != MOE_OK) return st;
     if ((st = make_map(&tm_u, w_up, H, I, H, kBlockK, bn, "w_up")) != MOE_OK) return st;
     if ((st = make_map(&tm_act, act, I, rows, I, kBlockK, kBlockM, "act")) != MOE_OK) return st;
-    if ((st = make_map(&tm_act_lo, act_lo, I, rows, I, kBlockK, kBlockM, "act_lo")) != MOE_OK) return st;
     if ((st = make_map(&tm_d, w_down, I, H, I, kBlockK, kDownBN, "w_down")) != MOE_OK) return st;
     MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int32_t), stream), "status reset");
     // one dense group: every token row, weight 1
@@ -915,7 +912,6 @@ moe_status_t moe_dense_mlp(const moe_bf16_t *x, const moe_bf16_t *w_gate, const 
     g.n_out = I;
     g.w_rows = I;
     g.out = act;
-    g.out_lo = act_lo;
     g.out_ld = I;
     g.scale = nullptr;
     g.status = status;
@@ -932,17 +928,16 @@ moe_status_t moe_dense_mlp(const moe_bf16_t *x, const moe_bf16_t *w_gate, const 
             return st;
         g.max_tiles = static_cast<int>((rows / kBlockM + 1) / 2) * ((I + bnp - 1) / bnp);
         g.grid = 2 * (g.max_tiles < sms / 2 ? g.max_tiles : sms / 2);
-        MOE_CUDA(launch_pair_gemm(kGateUp, tm_x, tm_x, tm_g2, tm_u2, g, stream),
+        MOE_CUDA(launch_pair_gemm(kGateUp, tm_x, tm_g2, tm_u2, g, stream),
                  "dense gate/up kernel launch");
     } else {
-        MOE_CUDA(launch_gemm(kGateUp, bn, tm_x, tm_x, tm_x, tm_x, tm_g, tm_u, g, stream),
+        MOE_CUDA(launch_gemm(kGateUp, bn, tm_x, tm_x, tm_g, tm_u, g, stream),
                  "dense gate/up kernel launch");
     }
     g.K = I;
     g.n_out = H;
     g.w_rows = H;
     g.out = y;
-    g.out_lo = nullptr;
     g.out_ld = H;
     if (pairs) {
         const int bnp = pair_gemm_block_n(kDown);
@@ -951,13 +946,12 @@ moe_status_t moe_dense_mlp(const moe_bf16_t *x, const moe_bf16_t *w_gate, const 
             return st;
         g.max_tiles = static_cast<int>((rows / kBlockM + 1) / 2) * ((H + bnp - 1) / bnp);
         g.grid = 2 * (g.max_tiles < sms / 2 ? g.max_tiles : sms / 2);
-        MOE_CUDA(launch_pair_gemm(kDown, tm_act, tm_act_lo, tm_d2, tm_d2, g, stream),
+        MOE_CUDA(launch_pair_gemm(kDown, tm_act, tm_d2, tm_d2, g, stream),
                  "dense down kernel launch");
     } else {
         g.max_tiles = static_cast<int>(rows / kBlockM) * ((H + kDownBN - 1) / kDownBN);
         g.grid = g.max_tiles < sms ? g.max_tiles : sms;
-        MOE_CUDA(launch_gemm(kDown, kDownBN, tm_act, tm_act_lo, tm_act, tm_act_lo, tm_d, tm_d, g,
-                             stream),
+        MOE_CUDA(launch_gemm(kDown, kDownBN, tm_act, tm_act, tm_d, tm_d, g, stream),
                  "dense down kernel launch");
     }
     // fp16 rows -> bf16 out (the combine with one slot per token)

@@ -6,17 +6,17 @@
 //
 //   K3 (kGateUp): for the 128 rows of block b (expert e = block_expert[b]),
 //       A = x[token(q)] gathered row by row, B0 = Wg[e], B1 = Wu[e];
-//       a = silu(A B0^T) * (A B1^T) in fp32 (128-column tiles), stored as
-//       the pair act_hi = bf16(a), act_lo = bf16(a - act_hi)
-//   K4 (kDown): A = act_hi and act_lo rows of block b, B0 = Wd[e];
-//       y[q, :] = fp16(w[q] * (act_hi B0^T + act_lo B0^T))  (256-column tiles)
+//       a = silu(A B0^T) * (A B1^T) in fp32 (96- or 128-column tiles),
+//       stored as act = fp16(a)
+//   K4 (kDown): A = act rows of block b, B0 = Wd[e] held in fp16;
+//       y[q, :] = fp16(w[q] * act B0^T)  (256-column tiles, fp16 x fp16 MMAs)
 //       where w[q] is the routing weight of pair q (or the shared gate).
-//       Both MMAs accumulate into the same TMEM tile, so the activation
-//       reaches the down projection with ~16 significant bits instead of
-//       bf16's 8 (a bf16 activation alone costs ~1.6e-3 relative error per
-//       pair, more than the layer's output tolerance leaves over the final
-//       bf16 rounding).  The per-pair results are stored in fp16: the same
-//       bytes as bf16 with an 8x finer rounding step.  |y| > 65504 records
+//       fp16 gives the activation 11 significant bits instead of bf16's 8
+//       (a bf16 activation costs more relative error per pair than the
+//       layer's output tolerance leaves over the final bf16 rounding), and
+//       the bf16 down weights convert to fp16 exactly from 2^-14 up.  The
+//       per-pair results are stored in fp16 too: the same bytes as bf16 with
+//       an 8x finer rounding step.  A value past fp16's range records
 //       MOE_ERR_DEVICE_CHECK.
 // Padding rows (q >= q_limit) are computed by the MMA but never loaded from
 // memory nor stored.
@@ -66,15 +66,14 @@ struct GemmSmem {
 };
 
 // Tile shape: BN output columns per tile (gate/up: BN gate + BN up
-// columns), A_TILES activation tiles (the gathered x, or act_hi + act_lo) and
-// B_TILES weight tiles per K slice; as many stages as fit in ~200 KB.
+// columns), one activation tile (the gathered x, or act) and B_TILES weight
+// tiles per K slice; as many stages as fit in ~200 KB.
 template <int MODE, int BN_>
 struct Cfg {
     static constexpr int BN = BN_;
-    static constexpr int A_TILES = MODE == kGateUp ? 1 : 2;
     static constexpr int B_TILES = MODE == kGateUp ? 2 : 1;
     static constexpr int B_BYTES = B_TILES * BN * 128;
-    static constexpr int STAGE_BYTES = A_TILES * kATileBytes + B_BYTES;
+    static constexpr int STAGE_BYTES = kATileBytes + B_BYTES;
     static constexpr int STAGES = (200 * 1024 / STAGE_BYTES) < kMaxStages
                                       ? (200 * 1024 / STAGE_BYTES) : kMaxStages;
     static_assert(B_TILES * BN <= kAccCols, "accumulator wider than its TMEM slot");
@@ -83,16 +82,14 @@ struct Cfg {
 template <int MODE, int BN_>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
-                        const __grid_constant__ CUtensorMap tm_a_lo,
                         const __grid_constant__ CUtensorMap tm_a_box,
-                        const __grid_constant__ CUtensorMap tm_a_lo_box,
                         const __grid_constant__ CUtensorMap tm_b0,
                         const __grid_constant__ CUtensorMap tm_b1, const GemmArgs a) {
     using C = Cfg<MODE, BN_>;
     constexpr int BN = C::BN;
     constexpr int kStages = C::STAGES;
     constexpr int kStageBytes = C::STAGE_BYTES;
-    constexpr int kBOffset = C::A_TILES * kATileBytes;
+    constexpr int kBOffset = kATileBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *tiles = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -116,9 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensor_map(&tm_a);
         prefetch_tensor_map(&tm_b0);
         if (MODE == kGateUp) prefetch_tensor_map(&tm_b1);
-        if (MODE == kDown) prefetch_tensor_map(&tm_a_lo);
         prefetch_tensor_map(&tm_a_box);
-        if (MODE == kDown) prefetch_tensor_map(&tm_a_lo_box);
     }
     if (warp == 1) {
         tmem_alloc(&sm->tmem_base, kTmemCols);
@@ -178,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const uint32_t groups = dense ? 0u : __popc(__ballot_sync(0xffffffffu, any));
             const uint32_t a_bytes = dense ? kATileBytes : groups * 512;
-            const uint32_t tx = a_bytes * C::A_TILES + C::B_BYTES;
+            const uint32_t tx = a_bytes + C::B_BYTES;
             const int arow = blk * kBlockM;
             const int brow = static_cast<int>(static_cast<int64_t>(expert) * a.w_rows) + nt * BN;
             for (int kc = 0; kc < nk; ++kc, ++g) {
@@ -199,18 +194,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive_expect_tx(&sm->full[s], tx);
                 __syncwarp();
                 if (dense) {
-                    if (lane == 0) {
-                        tma_load_2d(st, &tm_a_box, &sm->full[s], kc * kBlockK, arow);
-                        if (MODE == kDown)
-                            tma_load_2d(st + kATileBytes, &tm_a_lo_box, &sm->full[s],
-                                        kc * kBlockK, arow);
-                    }
+                    if (lane == 0) tma_load_2d(st, &tm_a_box, &sm->full[s], kc * kBlockK, arow);
                 } else if (any) {
                     tma_gather4(st + lane * 512, &tm_a, &sm->full[s], kc * kBlockK, src[0],
                                 src[1], src[2], src[3]);
-                    if (MODE == kDown)
-                        tma_gather4(st + kATileBytes + lane * 512, &tm_a_lo, &sm->full[s],
-                                    kc * kBlockK, src[0], src[1], src[2], src[3]);
                 }
                 if (lane == 0) {
                     if (a.stream_weights) {
@@ -237,8 +224,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------ MMA issuer (1 thread)
         if (lane == 0) {
             // gate/up: the Wg and Wu tiles sit back to back in shared memory,
-            // so one MMA of N = 2 BN produces [gate | up] in the accumulator
-            constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, MODE == kGateUp ? 2 * BN : BN);
+            // so one MMA of N = 2 BN produces [gate | up] in the accumulator;
+            // bf16 x bf16.  down: fp16 act x fp16 Wd.
+            constexpr uint32_t idesc = MODE == kGateUp ? idesc_bf16_f32(kBlockM, 2 * BN)
+                                                       : idesc_f16_f32(kBlockM, BN);
             int g = 0, it = 0;
             bool failed = false;
             for (int tile = blockIdx.x; tile < total_tiles && !failed; tile += gridDim.x, ++it) {
@@ -263,11 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < kBlockK / 16; ++kk) {
                         const uint32_t accumulate = (kc | kk) != 0;
-                        mma_bf16(d, da + 2 * kk, db + 2 * kk, idesc, accumulate);
-                        if (MODE == kDown) {
-                            const uint64_t da_lo = sw128_kmajor_desc(smem_addr(st + kATileBytes));
-                            mma_bf16(d, da_lo + 2 * kk, db + 2 * kk, idesc, 1u);
-                        }
+                        mma_f16kind(d, da + 2 * kk, db + 2 * kk, idesc, accumulate);
                     }
                     mma_commit(&sm->empty[s]);
                 }
@@ -288,6 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int it = 0;
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
             const int acc = it & 1;
+            const TileRow r = tile_row<MODE>(a, tile / n_tiles, row);
             bool ok = true;
             if (lane == 0) ok = mbar_wait(&sm->acc_full[acc], (it >> 1) & 1, abort_flag);
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -300,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after_sync();
             const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kAccCols;
-            store_tile<MODE, BN>(a, taddr, tile / n_tiles, tile % n_tiles, row);
+            store_tile<MODE, BN>(a, taddr, r, tile % n_tiles);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm->acc_empty[acc]);
@@ -377,8 +363,7 @@ cudaError_t launch_gather_rows(const uint16_t *x, int H, int k, const int32_t *s
 }
 
 template <int MODE, int BN>
-cudaError_t launch_one(const CUtensorMap &tm_a, const CUtensorMap &tm_a_lo,
-                       const CUtensorMap &tm_a_box, const CUtensorMap &tm_a_lo_box,
+cudaError_t launch_one(const CUtensorMap &tm_a, const CUtensorMap &tm_a_box,
                        const CUtensorMap &tm_b0, const CUtensorMap &tm_b1, const GemmArgs &a,
                        cudaStream_t s) {
     using C = Cfg<MODE, BN>;
@@ -387,8 +372,8 @@ cudaError_t launch_one(const CUtensorMap &tm_a, const CUtensorMap &tm_a_lo,
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    return launch_pdl(kern, dim3(a.grid), dim3(kThreads), smem, s, 1, tm_a, tm_a_lo, tm_a_box,
-                      tm_a_lo_box, tm_b0, tm_b1, a);
+    return launch_pdl(kern, dim3(a.grid), dim3(kThreads), smem, s, 1, tm_a, tm_a_box, tm_b0,
+                      tm_b1, a);
 }
 
 bool gemm_block_n_supported(GemmMode mode, int bn) {
@@ -396,15 +381,14 @@ bool gemm_block_n_supported(GemmMode mode, int bn) {
 }
 
 cudaError_t launch_gemm(GemmMode mode, int bn, const CUtensorMap &tm_a,
-                        const CUtensorMap &tm_a_lo, const CUtensorMap &tm_a_box,
-                        const CUtensorMap &tm_a_lo_box, const CUtensorMap &tm_b0,
+                        const CUtensorMap &tm_a_box, const CUtensorMap &tm_b0,
                         const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s) {
     if (mode == kGateUp && bn == 96)
-        return launch_one<kGateUp, 96>(tm_a, tm_a_lo, tm_a_box, tm_a_lo_box, tm_b0, tm_b1, a, s);
+        return launch_one<kGateUp, 96>(tm_a, tm_a_box, tm_b0, tm_b1, a, s);
     if (mode == kGateUp && bn == 128)
-        return launch_one<kGateUp, 128>(tm_a, tm_a_lo, tm_a_box, tm_a_lo_box, tm_b0, tm_b1, a, s);
+        return launch_one<kGateUp, 128>(tm_a, tm_a_box, tm_b0, tm_b1, a, s);
     if (mode == kDown && bn == 256)
-        return launch_one<kDown, 256>(tm_a, tm_a_lo, tm_a_box, tm_a_lo_box, tm_b0, tm_b1, a, s);
+        return launch_one<kDown, 256>(tm_a, tm_a_box, tm_b0, tm_b1, a, s);
     return cudaErrorInvalidValue;
 }
 

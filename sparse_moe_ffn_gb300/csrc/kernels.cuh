@@ -97,8 +97,7 @@ struct GemmArgs {
     int K;              // reduction length (H for gate/up, I for down)
     int n_out;          // output columns (I for gate/up, H for down)
     int64_t w_rows;     // weight rows per expert (I or H)
-    uint16_t *out;      // act_hi [rows, I] (gate/up) or fp16 y [q_limit, H] (down)
-    uint16_t *out_lo;   // act_lo [rows, I] (gate/up only)
+    uint16_t *out;      // fp16 act [rows, I] (gate/up) or fp16 y [q_limit, H] (down)
     int64_t out_ld;
     const float *scale; // down: per-q weight (null: 1)
     int32_t *status;
@@ -122,14 +121,13 @@ struct GemmArgs {
 // Tile widths: gate/up 96 or 128 columns (of each of gate and up), down 256.
 // The width changes no output element's arithmetic, only the tile count.
 bool gemm_block_n_supported(GemmMode mode, int bn);
-// tm_a / tm_a_lo: 1-row boxes for gather4 of sparse blocks (x or act_hi;
-// act_lo, down only); tm_a_box / tm_a_lo_box: 128-row boxes over rows that
-// are contiguous per block (x_sorted or x for gate/up; act_hi / act_lo for
-// down); tm_b0/tm_b1: weight rows (Wg/Wu for gate/up, Wd for down), boxes of
-// bn rows
+// A operands: x (or x_sorted) rows in bf16 for gate/up, the fp16 activation
+// rows for down.  B operands: Wg / Wu (bf16) for gate/up, Wd (fp16) for down.
+// tm_a: 1-row boxes for gather4 of sparse blocks; tm_a_box: 128-row boxes over
+// rows that are contiguous per block; tm_b0 / tm_b1: weight rows, boxes of bn
+// rows.
 cudaError_t launch_gemm(GemmMode mode, int bn, const CUtensorMap &tm_a,
-                        const CUtensorMap &tm_a_lo, const CUtensorMap &tm_a_box,
-                        const CUtensorMap &tm_a_lo_box, const CUtensorMap &tm_b0,
+                        const CUtensorMap &tm_a_box, const CUtensorMap &tm_b0,
                         const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s);
 // x rows copied into expert order (x_sorted [cap, H]): the real rows of dense
 // blocks, or of every block when all_blocks is set
@@ -138,29 +136,36 @@ cudaError_t launch_gather_rows(const uint16_t *x, int H, int k, const int32_t *s
                                uint16_t *x_sorted, int all_blocks, int num_sms, cudaStream_t s);
 
 // CTA-pair grouped GEMM (cta_group::2, M = 256 over two row blocks of one
-// group): tm_a / tm_a_lo: 128-row boxes over A rows that are contiguous per
-// block (x_sorted for gate/up; act_hi / act_lo for down); tm_b0 / tm_b1:
-// weight rows, Wg / Wu in boxes of pair_gemm_block_n(kGateUp) rows for
-// gate/up, Wd in boxes of pair_gemm_block_n(kDown) / 2 rows for down.  a.grid
-// must be even (two CTAs per cluster).
+// group): tm_a: 128-row boxes over A rows that are contiguous per block
+// (x_sorted for gate/up, act for down); tm_b0 / tm_b1: weight rows, Wg / Wu
+// in boxes of pair_gemm_block_n(kGateUp) rows for gate/up, Wd in boxes of
+// pair_gemm_block_n(kDown) / 2 rows for down.  a.grid must be even (two CTAs
+// per cluster).
 int pair_gemm_block_n(GemmMode mode);
 
 // Grouped GEMM for blocks holding few real rows (decode): activation rows in
-// 32-row passes, gathered with tile::gather4 (tm_a / tm_a_lo: 1-row boxes of
-// x rows for gate/up, act_hi / act_lo rows for down), more weight stages in
-// flight; tm_b0 / tm_b1 as for launch_gemm (boxes of bn rows).  Needs the
-// routed block list (sorted_pair, block_expert, num_padded).
+// 32-row passes, gathered with tile::gather4 (tm_a: 1-row boxes of x rows for
+// gate/up, act rows for down), more weight stages in flight; tm_b0 / tm_b1 as
+// for launch_gemm (boxes of bn rows).  Needs the routed block list
+// (sorted_pair, block_expert, num_padded).
 cudaError_t launch_sparse_gemm(GemmMode mode, int bn, const CUtensorMap &tm_a,
-                               const CUtensorMap &tm_a_lo, const CUtensorMap &tm_b0,
-                               const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s);
-cudaError_t launch_pair_gemm(GemmMode mode, const CUtensorMap &tm_a, const CUtensorMap &tm_a_lo,
-                             const CUtensorMap &tm_b0, const CUtensorMap &tm_b1,
-                             const GemmArgs &a, cudaStream_t s);
+                               const CUtensorMap &tm_b0, const CUtensorMap &tm_b1,
+                               const GemmArgs &a, cudaStream_t s);
+cudaError_t launch_pair_gemm(GemmMode mode, const CUtensorMap &tm_a, const CUtensorMap &tm_b0,
+                             const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s);
 
 // ----------------------------------------------------------------- combine
 
 cudaError_t launch_combine(const uint16_t *ypair, const uint16_t *yshared, int64_t N, int H,
                            int k, uint16_t *out, int num_sms, cudaStream_t s);
+
+// ------------------------------------------- bf16 -> fp16 weight conversion
+
+// dst[i] = fp16(src[i]) (round to nearest even) for i < n; src and dst
+// 16-byte aligned; a magnitude above 65504 or a NaN records
+// MOE_ERR_DEVICE_CHECK in *status (nullable)
+cudaError_t launch_convert_bf16_to_f16(const uint16_t *src, uint16_t *dst, int64_t n,
+                                       int32_t *status, int num_sms, cudaStream_t s);
 
 // ------------------------------------------------- residual add + RMSNorm
 

@@ -22,8 +22,8 @@
 //   gate/up (BN = 128): 16 KB of x rows + 16 KB of weights, Wg rows in the
 //                       even CTA and Wu rows in the odd one, so that N = 256
 //                       spans [gate | up] (32 KB, 6 stages);
-//   down    (BN = 256): 16 KB act_hi + 16 KB act_lo + 16 KB of Wd (48 KB,
-//                       4 stages), two MMAs (hi and lo).
+//   down    (BN = 256): 16 KB of fp16 act rows + 16 KB of fp16 Wd rows
+//                       (32 KB, 6 stages), fp16 x fp16 MMAs.
 //
 // Roles (both CTAs run the same code):
 //   warp 0    producer: its CTA's A rows and weight rows, TMA copies whose
@@ -51,12 +51,11 @@ constexpr int kMaxGroups = MOE_MAX_EXPERTS;
 template <int MODE>
 struct PairCfg;
 
-// Per CTA and K slice: A_TILES 128-row activation tiles and B_ROWS weight
-// rows; the pair's MMA has N = MMA_N.
+// Per CTA and K slice: one 128-row activation tile and B_ROWS weight rows;
+// the pair's MMA has N = MMA_N.
 template <>
 struct PairCfg<kGateUp> {
     static constexpr int BN = 128;     // gate columns per tile (and as many up columns)
-    static constexpr int A_TILES = 1;
     static constexpr int B_ROWS = BN;  // Wg rows (even CTA) or Wu rows (odd CTA)
     static constexpr int MMA_N = 2 * BN;
     static constexpr int STAGE_BYTES = kATileBytes + B_ROWS * 128;
@@ -66,11 +65,10 @@ struct PairCfg<kGateUp> {
 template <>
 struct PairCfg<kDown> {
     static constexpr int BN = 256;
-    static constexpr int A_TILES = 2;      // act_hi, act_lo
     static constexpr int B_ROWS = BN / 2;  // this CTA's half of the Wd rows
     static constexpr int MMA_N = BN;
-    static constexpr int STAGE_BYTES = 2 * kATileBytes + B_ROWS * 128;
-    static constexpr int STAGES = 4;
+    static constexpr int STAGE_BYTES = kATileBytes + B_ROWS * 128;
+    static constexpr int STAGES = 6;
 };
 
 constexpr int kMaxPairStages = 6;
@@ -106,8 +104,12 @@ __device__ __forceinline__ uint32_t cluster_addr(const void *p, uint32_t rank) {
     return r;
 }
 
-__device__ __forceinline__ void arrive_cluster(uint32_t bar_cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+// Arrival on a barrier of a cluster CTA (a shared::cluster address), ordering
+// no memory accesses: the accumulator-empty barrier only says that this
+// warp's TMEM reads are complete (tcgen05.wait::ld has returned), and a
+// release would first drain the epilogue's global stores.
+__device__ __forceinline__ void arrive_cluster_relaxed(uint32_t bar_cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(
                      bar_cluster_addr)
                  : "memory");
 }
@@ -188,14 +190,13 @@ __device__ __forceinline__ PairTile pair_of(const PairSmem *sm, int j, uint32_t 
 template <int MODE>
 __global__ void __launch_bounds__(kPairThreads, 1)
     pair_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
-                     const __grid_constant__ CUtensorMap tm_a_lo,
                      const __grid_constant__ CUtensorMap tm_b0,
                      const __grid_constant__ CUtensorMap tm_b1, const GemmArgs a) {
     using C = PairCfg<MODE>;
     constexpr int BN = C::BN;
     constexpr int kStages = C::STAGES;
     constexpr int kStageBytes = C::STAGE_BYTES;
-    constexpr int kBOffset = C::A_TILES * kATileBytes;
+    constexpr int kBOffset = kATileBytes;
     constexpr int kBBytes = C::B_ROWS * 128;
     constexpr uint32_t kColsPerAcc = C::MMA_N;  // 256 either way
     extern __shared__ uint8_t smem_raw[];
@@ -221,7 +222,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         sm->abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         prefetch_tensor_map(&tm_a);
-        if (MODE == kDown) prefetch_tensor_map(&tm_a_lo);
         prefetch_tensor_map(&tm_b0);
         if (MODE == kGateUp) prefetch_tensor_map(&tm_b1);
     }
@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             for (int tile = pair_id; tile < total_tiles && !failed; tile += num_pairs) {
                 const PairTile pt = pair_of(sm, tile / n_tiles, rank);
                 const int nt = tile % n_tiles;
-                const uint32_t a_bytes = C::A_TILES * kATileBytes;
+                const uint32_t a_bytes = kATileBytes;
                 const uint32_t tx = 2 * kBBytes +
                                     a_bytes * ((pt.rows ? 1u : 0u) + (pt.peer_rows ? 1u : 0u));
                 const int arow = pt.block * kBlockM;
@@ -319,11 +319,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     uint8_t *st = tiles + s * kStageBytes;
                     const uint32_t bar = cluster_addr(&sm->full[s], 0);
                     if (leader) mbar_arrive_expect_tx(&sm->full[s], tx);
-                    if (pt.rows) {
-                        tma_load_pair(st, &tm_a, bar, kc * kBlockK, arow);
-                        if (MODE == kDown)
-                            tma_load_pair(st + kATileBytes, &tm_a_lo, bar, kc * kBlockK, arow);
-                    }
+                    if (pt.rows) tma_load_pair(st, &tm_a, bar, kc * kBlockK, arow);
                     tma_load_pair(st + kBOffset, tm_b, bar, kc * kBlockK, brow);
                 }
             }
@@ -337,7 +333,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (even CTA)
         if (leader && lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(2 * kBlockM, C::MMA_N);
+            // gate/up: bf16 x bf16; down: fp16 act x fp16 Wd
+            constexpr uint32_t idesc = MODE == kGateUp ? idesc_bf16_f32(2 * kBlockM, C::MMA_N)
+                                                       : idesc_f16_f32(2 * kBlockM, C::MMA_N);
             int g = 0, it = 0;
             bool failed = false;
             for (int tile = pair_id; tile < total_tiles && !failed; tile += num_pairs, ++it) {
@@ -363,10 +361,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     for (int kk = 0; kk < kBlockK / 16; ++kk) {
                         const uint32_t accumulate = (kc | kk) != 0;
                         mma_pair(d, da + 2 * kk, db + 2 * kk, idesc, accumulate);
-                        if (MODE == kDown) {
-                            const uint64_t da_lo = sw128_kmajor_desc(smem_addr(st + kATileBytes));
-                            mma_pair(d, da_lo + 2 * kk, db + 2 * kk, idesc, 1u);
-                        }
                     }
                     commit_pair(&sm->empty[s], 3);
                 }
@@ -389,6 +383,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         int it = 0;
         for (int tile = pair_id; tile < total_tiles; tile += num_pairs, ++it) {
             const int acc = it & 1;
+            const PairTile pt = pair_of(sm, tile / n_tiles, rank);
+            TileRow r = {};
+            if (pt.rows) r = tile_row<MODE>(a, pt.block, row);
             bool ok = true;
             if (lane == 0) ok = mbar_wait(&sm->acc_full[acc], (it >> 1) & 1, abort_flag);
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -400,15 +397,14 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 break;
             }
             tc_fence_after_sync();
-            const PairTile pt = pair_of(sm, tile / n_tiles, rank);
             if (pt.rows) {
                 const uint32_t taddr =
                     tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kColsPerAcc;
-                store_tile<MODE, BN>(a, taddr, pt.block, tile % n_tiles, row);
+                store_tile<MODE, BN>(a, taddr, r, tile % n_tiles);
             }
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) arrive_cluster(acc ? acc_empty1 : acc_empty0);
+            if (lane == 0) arrive_cluster_relaxed(acc ? acc_empty1 : acc_empty0);
         }
     }
 
@@ -422,17 +418,15 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 }
 
 template <int MODE>
-cudaError_t launch_pair_one(const CUtensorMap &tm_a, const CUtensorMap &tm_a_lo,
-                            const CUtensorMap &tm_b0, const CUtensorMap &tm_b1,
-                            const GemmArgs &a, cudaStream_t s) {
+cudaError_t launch_pair_one(const CUtensorMap &tm_a, const CUtensorMap &tm_b0,
+                            const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s) {
     using C = PairCfg<MODE>;
     const size_t smem = 1024 + static_cast<size_t>(C::STAGES) * C::STAGE_BYTES + sizeof(PairSmem);
     auto kern = pair_gemm_kernel<MODE>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    return launch_pdl(kern, dim3(a.grid), dim3(kPairThreads), smem, s, 2, tm_a, tm_a_lo, tm_b0,
-                      tm_b1, a);
+    return launch_pdl(kern, dim3(a.grid), dim3(kPairThreads), smem, s, 2, tm_a, tm_b0, tm_b1, a);
 }
 
 }  // namespace
@@ -440,14 +434,13 @@ cudaError_t launch_pair_one(const CUtensorMap &tm_a, const CUtensorMap &tm_a_lo,
 int pair_gemm_block_n(GemmMode mode) { return mode == kGateUp ? PairCfg<kGateUp>::BN
                                                               : PairCfg<kDown>::BN; }
 
-cudaError_t launch_pair_gemm(GemmMode mode, const CUtensorMap &tm_a, const CUtensorMap &tm_a_lo,
-                             const CUtensorMap &tm_b0, const CUtensorMap &tm_b1,
-                             const GemmArgs &a, cudaStream_t s) {
+cudaError_t launch_pair_gemm(GemmMode mode, const CUtensorMap &tm_a, const CUtensorMap &tm_b0,
+                             const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s) {
     if (a.grid < 2 || a.grid % 2) return cudaErrorInvalidValue;
     if (a.pad_offsets && (a.num_groups < 1 || a.num_groups > kMaxGroups))
         return cudaErrorInvalidValue;
-    if (mode == kGateUp) return launch_pair_one<kGateUp>(tm_a, tm_a_lo, tm_b0, tm_b1, a, s);
-    return launch_pair_one<kDown>(tm_a, tm_a_lo, tm_b0, tm_b1, a, s);
+    if (mode == kGateUp) return launch_pair_one<kGateUp>(tm_a, tm_b0, tm_b1, a, s);
+    return launch_pair_one<kDown>(tm_a, tm_b0, tm_b1, a, s);
 }
 
 }  // namespace moe

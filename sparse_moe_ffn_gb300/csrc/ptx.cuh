@@ -160,9 +160,10 @@ __device__ __forceinline__ void tc_fence_after_sync() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate; one thread.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate) {
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (A and B both bf16 or both
+// fp16, as idesc says), fp32 accumulate; one thread.
+__device__ __forceinline__ void mma_f16kind(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
@@ -226,6 +227,14 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
 
 // Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B, both K-major,
 // fp32 accumulator, M x N tile.
+// kind::f16 with fp16 A and B (the down projection: fp16 activation times
+// fp16 weights), fp32 accumulator
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+    return (1u << 4)                                   // D format: f32
+           | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8 (A, B format 0: f16)
+           | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
     return (1u << 4)                                   // D format: f32
            | (1u << 7)                                 // A format: bf16

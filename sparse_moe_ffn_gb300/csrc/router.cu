@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kRouterThreads, 1)
                 const uint64_t db = sw128_kmajor_desc(smem_addr(st + kATileBytes));
 #pragma unroll
                 for (int kk = 0; kk < kBlockK / 16; ++kk)
-                    mma_bf16(tmem, da + 2 * kk, db + 2 * kk, idesc, (i | kk) != 0);
+                    mma_f16kind(tmem, da + 2 * kk, db + 2 * kk, idesc, (i | kk) != 0);
                 mma_commit(&sm->empty[s]);
             }
             mma_commit(&sm->acc_full);

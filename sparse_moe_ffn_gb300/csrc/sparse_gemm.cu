@@ -6,12 +6,12 @@
 //
 // Such a GEMM streams every weight tile once and is bound by how many weight
 // bytes each SM keeps in flight.  The activation rows of a block are loaded
-// as 32-row sub-blocks into a 4 KB region per operand (instead of a 16 KB
-// 128-row tile), which leaves room for more weight stages:
+// as 32-row sub-blocks into a 4 KB region (instead of a 16 KB 128-row
+// tile), which leaves room for more weight stages:
 //   gate/up BN = 96: 4 KB + 24 KB per stage, 7 stages (168 KB of weights);
-//   gate/up BN = 128: 4 KB + 32 KB, 5 stages (160 KB);
-//   down BN = 256: 4 + 4 KB + 32 KB, 5 stages (160 KB; 96 KB with 128-row
-//   activation tiles).
+//   gate/up BN = 128: 4 KB + 32 KB, 6 stages (192 KB);
+//   down BN = 256: 4 KB of fp16 act + 32 KB of fp16 Wd, 6 stages (192 KB;
+//   144 KB with 128-row activation tiles).
 // The MMA is still M = 128: its A operand spans 16 KB from the region's
 // start, so rows 32-127 read whatever follows in the stage; they only feed
 // accumulator rows 32-127, which the epilogue never stores (and TMEM lanes
@@ -49,14 +49,12 @@ constexpr int kInfoReaders = 1 + 4;  // MMA warp + four epilogue warps
 template <int MODE, int BN_>
 struct SparseCfg {
     static constexpr int BN = BN_;
-    static constexpr int A_TILES = MODE == kGateUp ? 1 : 2;
     static constexpr int B_BYTES = (MODE == kGateUp ? 2 : 1) * BN * 128;
-    static constexpr int STAGE_BYTES = A_TILES * kSubTileBytes + B_BYTES;
-    static constexpr int STAGES = (200 * 1024 / STAGE_BYTES) < kSparseMaxStages
-                                      ? (200 * 1024 / STAGE_BYTES) : kSparseMaxStages;
-    // the MMA reads a 16 KB (128-row) A operand from each A region
-    static_assert(STAGE_BYTES >= (A_TILES - 1) * kSubTileBytes + kATileBytes,
-                  "a 128-row A read would leave the stage");
+    static constexpr int STAGE_BYTES = kSubTileBytes + B_BYTES;
+    static constexpr int STAGES = (216 * 1024 / STAGE_BYTES) < kSparseMaxStages
+                                      ? (216 * 1024 / STAGE_BYTES) : kSparseMaxStages;
+    // the MMA reads a 16 KB (128-row) A operand from the A region's start
+    static_assert(STAGE_BYTES >= kATileBytes, "a 128-row A read would leave the stage");
     static_assert((MODE == kGateUp ? 2 : 1) * BN <= kAccCols, "accumulator too wide");
 };
 
@@ -94,14 +92,13 @@ __device__ __forceinline__ int read_passes(SparseSmem *sm, int j, int lane,
 template <int MODE, int BN_>
 __global__ void __launch_bounds__(kSparseThreads, 1)
     sparse_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
-                       const __grid_constant__ CUtensorMap tm_a_lo,
                        const __grid_constant__ CUtensorMap tm_b0,
                        const __grid_constant__ CUtensorMap tm_b1, const GemmArgs a) {
     using C = SparseCfg<MODE, BN_>;
     constexpr int BN = C::BN;
     constexpr int kStages = C::STAGES;
     constexpr int kStageBytes = C::STAGE_BYTES;
-    constexpr int kBOffset = C::A_TILES * kSubTileBytes;
+    constexpr int kBOffset = kSubTileBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *tiles = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -127,7 +124,6 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
         sm->abort_flag = 0;
         fence_barrier_init();
         prefetch_tensor_map(&tm_a);
-        if (MODE == kDown) prefetch_tensor_map(&tm_a_lo);
         prefetch_tensor_map(&tm_b0);
         if (MODE == kGateUp) prefetch_tensor_map(&tm_b1);
     }
@@ -263,7 +259,7 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
             for (int p = 0; p < passes && !failed; ++p) {
                 const bool mine = lane / 8 == p && any;  // lanes 8p .. 8p+7 gather pass p
                 const uint32_t groups = __popc(__ballot_sync(0xffffffffu, mine));
-                const uint32_t tx = C::A_TILES * groups * 512 + C::B_BYTES;
+                const uint32_t tx = groups * 512 + C::B_BYTES;
                 for (int kc = 0; kc < nk; ++kc, ++g) {
                     const int s = g % kStages;
                     const uint32_t use = g / kStages;
@@ -285,9 +281,6 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
                         const int slot = lane % 8;
                         tma_gather4(st + slot * 512, &tm_a, &sm->full[s], kc * kBlockK, src[0],
                                     src[1], src[2], src[3]);
-                        if (MODE == kDown)
-                            tma_gather4(st + kSubTileBytes + slot * 512, &tm_a_lo, &sm->full[s],
-                                        kc * kBlockK, src[0], src[1], src[2], src[3]);
                     }
                     if (lane == 0) {
                         if (a.stream_weights) {
@@ -312,8 +305,10 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (1 thread)
-        // gate/up: Wg and Wu tiles are adjacent, one MMA of N = 2 BN
-        constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, MODE == kGateUp ? 2 * BN : BN);
+        // gate/up: Wg and Wu tiles are adjacent, one bf16 MMA of N = 2 BN;
+        // down: fp16 act x fp16 Wd
+        constexpr uint32_t idesc = MODE == kGateUp ? idesc_bf16_f32(kBlockM, 2 * BN)
+                                                   : idesc_f16_f32(kBlockM, BN);
         int g = 0, it = 0;
         bool failed = false;
         for (int tile = blockIdx.x, j = 0; tile < total_tiles && !failed; tile += gridDim.x, ++j) {
@@ -343,12 +338,7 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
                             const uint64_t db = sw128_kmajor_desc(smem_addr(st + kBOffset));
 #pragma unroll
                             for (int kk = 0; kk < kBlockK / 16; ++kk) {
-                                mma_bf16(d, da + 2 * kk, db + 2 * kk, idesc, (kc | kk) != 0);
-                                if (MODE == kDown) {
-                                    const uint64_t da_lo =
-                                        sw128_kmajor_desc(smem_addr(st + kSubTileBytes));
-                                    mma_bf16(d, da_lo + 2 * kk, db + 2 * kk, idesc, 1u);
-                                }
+                                mma_f16kind(d, da + 2 * kk, db + 2 * kk, idesc, (kc | kk) != 0);
                             }
                             mma_commit(&sm->empty[s]);
                         }
@@ -383,6 +373,8 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
             }
             for (int p = 0; p < passes; ++p, ++it) {
                 const int acc = it & 1;
+                TileRow r = {};
+                if (quarter == 0) r = tile_row<MODE>(a, block_of(tile), p * kSubRows + lane);
                 bool ok = true;
                 if (lane == 0) ok = mbar_wait(&sm->acc_full[acc], (it >> 1) & 1, abort_flag);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -395,9 +387,7 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                if (quarter == 0)
-                    store_tile<MODE, BN>(a, tmem + acc * kAccCols, block_of(tile), tile % n_tiles,
-                                         p * kSubRows + lane);
+                if (quarter == 0) store_tile<MODE, BN>(a, tmem + acc * kAccCols, r, tile % n_tiles);
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sm->acc_empty[acc]);
@@ -414,29 +404,26 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
 }
 
 template <int MODE, int BN>
-cudaError_t launch_sparse_one(const CUtensorMap &tm_a, const CUtensorMap &tm_a_lo,
-                              const CUtensorMap &tm_b0, const CUtensorMap &tm_b1,
-                              const GemmArgs &a, cudaStream_t s) {
+cudaError_t launch_sparse_one(const CUtensorMap &tm_a, const CUtensorMap &tm_b0,
+                              const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s) {
     using C = SparseCfg<MODE, BN>;
     const size_t smem = 1024 + static_cast<size_t>(C::STAGES) * C::STAGE_BYTES + sizeof(SparseSmem);
     auto kern = sparse_gemm_kernel<MODE, BN>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    return launch_pdl(kern, dim3(a.grid), dim3(kSparseThreads), smem, s, 1, tm_a, tm_a_lo, tm_b0,
-                      tm_b1, a);
+    return launch_pdl(kern, dim3(a.grid), dim3(kSparseThreads), smem, s, 1, tm_a, tm_b0, tm_b1, a);
 }
 
 }  // namespace
 
 cudaError_t launch_sparse_gemm(GemmMode mode, int bn, const CUtensorMap &tm_a,
-                               const CUtensorMap &tm_a_lo, const CUtensorMap &tm_b0,
-                               const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s) {
+                               const CUtensorMap &tm_b0, const CUtensorMap &tm_b1,
+                               const GemmArgs &a, cudaStream_t s) {
     if (!a.sorted_pair || !a.block_expert || !a.num_padded) return cudaErrorInvalidValue;
-    if (mode == kGateUp && bn == 96) return launch_sparse_one<kGateUp, 96>(tm_a, tm_a_lo, tm_b0, tm_b1, a, s);
-    if (mode == kGateUp && bn == 128)
-        return launch_sparse_one<kGateUp, 128>(tm_a, tm_a_lo, tm_b0, tm_b1, a, s);
-    if (mode == kDown && bn == 256) return launch_sparse_one<kDown, 256>(tm_a, tm_a_lo, tm_b0, tm_b1, a, s);
+    if (mode == kGateUp && bn == 96) return launch_sparse_one<kGateUp, 96>(tm_a, tm_b0, tm_b1, a, s);
+    if (mode == kGateUp && bn == 128) return launch_sparse_one<kGateUp, 128>(tm_a, tm_b0, tm_b1, a, s);
+    if (mode == kDown && bn == 256) return launch_sparse_one<kDown, 256>(tm_a, tm_b0, tm_b1, a, s);
     return cudaErrorInvalidValue;
 }
 

@@ -74,7 +74,8 @@ def ep_forward(x, router, w_gate, w_up, w_down, E: int, k: int, norm_topk_prob: 
     """One MoE layer with experts split across the ranks of ``group``.
 
     x [N, H] bf16 (this rank's tokens), router [E, H] bf16 (all experts);
-    w_gate, w_up [E_r, I, H] and w_down [E_r, H, I]: this rank's experts.
+    w_gate, w_up [E_r, I, H] bf16 and w_down [E_r, H, I] fp16 (see
+    binding.prepare_weights): this rank's experts.
     Returns out [N, H] bf16."""
     from sparse_moe_ffn_gb300 import binding
 

@@ -36,7 +36,8 @@ def prepare(shape: MoEShape, seed: int = 0):
         bits = {n: oracle.bf16_bits(t) for n, t in dev.items()}  # the GPU's cast
     else:
         bits = {n: oracle.bf16_bits(t) for n, t in cpu.items()}
-    return shape, dev, bits
+    # the oracle takes the model's bf16 weights; the library its fp16 down weights
+    return shape, binding.prepare_weights(dev), bits
 
 
 def shared_of(shape, dev):

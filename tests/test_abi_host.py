@@ -127,6 +127,15 @@ def test_experts_and_combine_argument_errors(L):
     assert L.moe_combine(P, None, 0, 2048, 2, None, None) == OK
 
 
+def test_convert_argument_errors(L):
+    P = FAKE
+    assert L.moe_convert_bf16_to_f16(P, P + 4096, -1, None, None) == INVALID
+    assert L.moe_convert_bf16_to_f16(None, P, 8, None, None) == INVALID
+    assert L.moe_convert_bf16_to_f16(P + 2, P + 4096, 8, None, None) == INVALID  # misaligned
+    assert L.moe_convert_bf16_to_f16(P, P + 16, 64, None, None) == INVALID       # overlap
+    assert L.moe_convert_bf16_to_f16(None, None, 0, None, None) == OK            # no-op
+
+
 def test_route_and_align_argument_errors(L):
     P = FAKE
     assert L.moe_route(P, P, None, 16, 64, 6, 7, 1, P, P, None, None, None, 0, None) == INVALID

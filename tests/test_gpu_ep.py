@@ -81,7 +81,7 @@ def test_expert_slices_in_one_process_equal_forward(name, world):
 
 def test_experts_with_empty_experts_and_one_row():
     """Rows routed to a few of many experts, down to a single row."""
-    shape, dev, _ = prepare(MoEShape("slice", N=1, H=256, E=40, k=1, I=192), seed=9)
+    shape, dev, wbits = prepare(MoEShape("slice", N=1, H=256, E=40, k=1, I=192), seed=9)
     for R in (1, 7, 130):
         g = torch.Generator().manual_seed(R)
         x = torch.randn(R, shape.H, generator=g).to(torch.bfloat16).cuda()
@@ -98,8 +98,7 @@ def test_experts_with_empty_experts_and_one_row():
             sel = np.nonzero(ids_h == e)[0]
             bits = {"x": oracle.bf16_bits(x[torch.from_numpy(sel).cuda()]),
                     "router": np.zeros((1, shape.H), np.uint16),
-                    "w_gate": oracle.bf16_bits(dev["w_gate"][e:e + 1]),
-                    "w_up": oracle.bf16_bits(dev["w_up"][e:e + 1]),
-                    "w_down": oracle.bf16_bits(dev["w_down"][e:e + 1])}
+                    "w_gate": wbits["w_gate"][e:e + 1], "w_up": wbits["w_up"][e:e + 1],
+                    "w_down": wbits["w_down"][e:e + 1]}
             ref[sel] = oracle.moe_forward(bits, 1, True) * w_h[sel, None]
         assert_close(y, ref, f"R={R}")
