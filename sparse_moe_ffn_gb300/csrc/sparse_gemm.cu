@@ -5,10 +5,11 @@
 // staging differs.
 //
 // Such a GEMM streams every weight tile once and is bound by how many weight
-// bytes each SM keeps in flight.  The activation rows of a block are loaded
+// bytes each SM keeps in flight (HBM3e under load answers in ~4 us, so ~190 KB
+// per SM is needed to approach the read bandwidth).  The activation rows of a block are loaded
 // as 32-row sub-blocks into a 4 KB region (instead of a 16 KB 128-row
 // tile), which leaves room for more weight stages:
-//   gate/up BN = 96: 4 KB + 24 KB per stage, 7 stages (168 KB of weights);
+//   gate/up BN = 96: 4 KB + 24 KB per stage, 8 stages (192 KB of weights);
 //   gate/up BN = 128: 4 KB + 32 KB, 6 stages (192 KB);
 //   down BN = 256: 4 KB of fp16 act + 32 KB of fp16 Wd, 6 stages (192 KB;
 //   144 KB with 128-row activation tiles).
@@ -51,10 +52,11 @@ struct SparseCfg {
     static constexpr int BN = BN_;
     static constexpr int B_BYTES = (MODE == kGateUp ? 2 : 1) * BN * 128;
     static constexpr int STAGE_BYTES = kSubTileBytes + B_BYTES;
-    static constexpr int STAGES = (216 * 1024 / STAGE_BYTES) < kSparseMaxStages
-                                      ? (216 * 1024 / STAGE_BYTES) : kSparseMaxStages;
+    static constexpr int STAGES = (224 * 1024 / STAGE_BYTES) < kSparseMaxStages
+                                      ? (224 * 1024 / STAGE_BYTES) : kSparseMaxStages;
     // the MMA reads a 16 KB (128-row) A operand from the A region's start
     static_assert(STAGE_BYTES >= kATileBytes, "a 128-row A read would leave the stage");
+    static_assert(STAGES * STAGE_BYTES + 1024 + 1024 <= 227 * 1024, "shared memory");
     static_assert((MODE == kGateUp ? 2 : 1) * BN <= kAccCols, "accumulator too wide");
 };
 
