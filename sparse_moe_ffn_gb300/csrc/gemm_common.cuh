@@ -31,13 +31,36 @@ struct TileRow {
     bool valid;
 };
 
+// The pair (or token) held by grouped row grow: one load, issued early.
+__device__ __forceinline__ int64_t row_pair(const GemmArgs &a, int64_t grow) {
+    return a.sorted_pair ? __ldcg(a.sorted_pair + grow) : grow;
+}
+
+// The TileRow of grouped row grow, whose pair q is already known; issues the
+// routing-weight load (down) without waiting for it.
+template <int MODE>
+__device__ __forceinline__ TileRow tile_row_of(const GemmArgs &a, int64_t grow, int64_t q) {
+    TileRow r;
+    r.grow = grow;
+    r.q = q;
+    r.valid = q >= 0 && q < a.q_limit;
+    r.w = (MODE == kDown && r.valid) ? (a.scale ? __ldcg(a.scale + q) : 1.f) : 0.f;
+    return r;
+}
+
 template <int MODE>
 __device__ __forceinline__ TileRow tile_row(const GemmArgs &a, int blk, int row) {
+    const int64_t grow = static_cast<int64_t>(blk) * kBlockM + row;
+    return tile_row_of<MODE>(a, grow, row_pair(a, grow));
+}
+
+// A tile row that stores nothing (its block holds no rows).
+__device__ __forceinline__ TileRow no_tile_row() {
     TileRow r;
-    r.grow = static_cast<int64_t>(blk) * kBlockM + row;
-    r.q = a.sorted_pair ? __ldcg(a.sorted_pair + r.grow) : r.grow;
-    r.valid = r.q >= 0 && r.q < a.q_limit;
-    r.w = (MODE == kDown && r.valid) ? (a.scale ? __ldcg(a.scale + r.q) : 1.f) : 0.f;
+    r.grow = 0;
+    r.q = -1;
+    r.w = 0.f;
+    r.valid = false;
     return r;
 }
 
@@ -53,11 +76,26 @@ __device__ __forceinline__ TileRow tile_row(const GemmArgs &a, int blk, int row)
 template <int MODE, int BN>
 __device__ __forceinline__ void store_tile(const GemmArgs &a, uint32_t taddr, const TileRow &r,
                                            int nt) {
+    static_assert(MODE == kGateUp || BN % 64 == 0, "down tiles are read 64 columns at a time");
     const int64_t grow = r.grow;
     const int64_t q = r.q;
     const bool valid = r.valid;
     const int col0 = nt * BN;
     float vmax = 0.f;
+    // 16 columns (32 bytes) per store when every output row starts on a
+    // 32-byte boundary, else 8 columns; stores never pass n_out (a multiple
+    // of 8)
+    const bool wide = (a.out_ld % 16) == 0 && (reinterpret_cast<uintptr_t>(a.out) % 32) == 0;
+    auto store16 = [&](uint16_t *dst, int col, const uint32_t (&pk)[8]) {
+        if (wide && col + 16 <= a.n_out) {
+            st_global_v8(dst, pk);
+        } else {
+            if (col + 8 <= a.n_out)
+                *reinterpret_cast<uint4 *>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            if (col + 16 <= a.n_out)
+                *reinterpret_cast<uint4 *>(dst + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+    };
     if (MODE == kGateUp) {
         uint16_t *dst = a.out + grow * a.out_ld + col0;
 #pragma unroll 1
@@ -68,50 +106,42 @@ __device__ __forceinline__ void store_tile(const GemmArgs &a, uint32_t taddr, co
             tmem_load_wait();
             if (valid) {
 #pragma unroll
-                for (int v8 = 0; v8 < 4; ++v8) {
-                    const int col = col0 + c * 32 + v8 * 8;
-                    if (col + 8 <= a.n_out) {
-                        uint32_t pk[4];
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t pk[8];
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const float a0 = silu_times(gv[v8 * 8 + 2 * i], uv[v8 * 8 + 2 * i]);
-                            const float a1 = silu_times(gv[v8 * 8 + 2 * i + 1],
-                                                        uv[v8 * 8 + 2 * i + 1]);
-                            vmax = fmaxf(vmax, fmaxf(fabsf(a0), fabsf(a1)));
-                            pk[i] = pack_f16x2(a0, a1);
-                        }
-                        *reinterpret_cast<uint4 *>(dst + c * 32 + v8 * 8) =
-                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    for (int i = 0; i < 8; ++i) {
+                        const int j = h * 16 + 2 * i;
+                        const float a0 = silu_times(gv[j], uv[j]);
+                        const float a1 = silu_times(gv[j + 1], uv[j + 1]);
+                        vmax = fmaxf(vmax, fmaxf(fabsf(a0), fabsf(a1)));
+                        pk[i] = pack_f16x2(a0, a1);
                     }
+                    store16(dst + c * 32 + h * 16, col0 + c * 32 + h * 16, pk);
                 }
             }
         }
     } else {
         const float w = r.w;
         uint16_t *dst = a.out + (valid ? q : 0) * a.out_ld + col0;
+        // 64 columns per TMEM round trip: two loads in flight, one wait
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-            float yv[32];
-            tmem_load32(taddr + c * 32, yv);
+        for (int c = 0; c < BN / 64; ++c) {
+            float yv[64];
+            tmem_load32(taddr + c * 64, *reinterpret_cast<float(*)[32]>(yv));
+            tmem_load32(taddr + c * 64 + 32, *reinterpret_cast<float(*)[32]>(yv + 32));
             tmem_load_wait();
             if (valid) {
 #pragma unroll
-                for (int v8 = 0; v8 < 4; ++v8) {
-                    const int col = col0 + c * 32 + v8 * 8;
-                    if (col + 8 <= a.n_out) {
-                        float t[8];
+                for (int h = 0; h < 4; ++h) {
+                    uint32_t pk[8];
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            t[i] = w * yv[v8 * 8 + i];
-                            vmax = fmaxf(vmax, fabsf(t[i]));
-                        }
-                        uint4 pk;
-                        pk.x = pack_f16x2(t[0], t[1]);
-                        pk.y = pack_f16x2(t[2], t[3]);
-                        pk.z = pack_f16x2(t[4], t[5]);
-                        pk.w = pack_f16x2(t[6], t[7]);
-                        *reinterpret_cast<uint4 *>(dst + c * 32 + v8 * 8) = pk;
+                    for (int i = 0; i < 8; ++i) {
+                        const float t0 = w * yv[h * 16 + 2 * i];
+                        const float t1 = w * yv[h * 16 + 2 * i + 1];
+                        vmax = fmaxf(vmax, fmaxf(fabsf(t0), fabsf(t1)));
+                        pk[i] = pack_f16x2(t0, t1);
                     }
+                    store16(dst + c * 64 + h * 16, col0 + c * 64 + h * 16, pk);
                 }
             }
         }

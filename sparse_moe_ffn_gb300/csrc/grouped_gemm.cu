@@ -271,9 +271,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp % 4;               // TMEM lanes this warp may read
         const int row = quarter * 32 + lane;        // tile row = TMEM lane
         int it = 0;
-        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
+        // row info runs ahead: the pair of a row two tiles ahead and its
+        // routing weight one tile ahead, so no L2 round trip delays a tile
+        const int step = gridDim.x;
+        auto grow_of = [&](int t) { return static_cast<int64_t>(t / n_tiles) * kBlockM + row; };
+        const int first = blockIdx.x;
+        TileRow cur = first < total_tiles ? tile_row<MODE>(a, first / n_tiles, row) : no_tile_row();
+        int64_t q_next = first + step < total_tiles ? row_pair(a, grow_of(first + step)) : -1;
+        for (int tile = first; tile < total_tiles; tile += step, ++it) {
             const int acc = it & 1;
-            const TileRow r = tile_row<MODE>(a, tile / n_tiles, row);
             bool ok = true;
             if (lane == 0) ok = mbar_wait(&sm->acc_full[acc], (it >> 1) & 1, abort_flag);
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -286,10 +292,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after_sync();
             const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kAccCols;
-            store_tile<MODE, BN>(a, taddr, r, tile % n_tiles);
+            const TileRow nxt = tile + step < total_tiles
+                                    ? tile_row_of<MODE>(a, grow_of(tile + step), q_next)
+                                    : no_tile_row();
+            q_next = tile + 2 * step < total_tiles ? row_pair(a, grow_of(tile + 2 * step)) : -1;
+            store_tile<MODE, BN>(a, taddr, cur, tile % n_tiles);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm->acc_empty[acc]);
+            cur = nxt;
         }
     }
 

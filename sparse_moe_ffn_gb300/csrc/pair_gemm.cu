@@ -381,11 +381,21 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         const uint32_t acc_empty0 = cluster_addr(&sm->acc_empty[0], 0);
         const uint32_t acc_empty1 = cluster_addr(&sm->acc_empty[1], 0);
         int it = 0;
-        for (int tile = pair_id; tile < total_tiles; tile += num_pairs, ++it) {
+        // row info runs ahead: the pair of a row two tiles ahead and its
+        // routing weight one tile ahead, so no L2 round trip delays a tile.
+        // grow -1: this CTA's block of the tile holds no rows.
+        const int step = num_pairs;
+        auto grow_of = [&](int t) -> int64_t {
+            if (t >= total_tiles) return -1;
+            const PairTile pt = pair_of(sm, t / n_tiles, rank);
+            return pt.rows ? static_cast<int64_t>(pt.block) * kBlockM + row : -1;
+        };
+        int64_t g_cur = grow_of(pair_id);
+        TileRow cur = g_cur >= 0 ? tile_row_of<MODE>(a, g_cur, row_pair(a, g_cur)) : no_tile_row();
+        int64_t g_next = grow_of(pair_id + step);
+        int64_t q_next = g_next >= 0 ? row_pair(a, g_next) : -1;
+        for (int tile = pair_id; tile < total_tiles; tile += step, ++it) {
             const int acc = it & 1;
-            const PairTile pt = pair_of(sm, tile / n_tiles, rank);
-            TileRow r = {};
-            if (pt.rows) r = tile_row<MODE>(a, pt.block, row);
             bool ok = true;
             if (lane == 0) ok = mbar_wait(&sm->acc_full[acc], (it >> 1) & 1, abort_flag);
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -397,11 +407,17 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 break;
             }
             tc_fence_after_sync();
-            if (pt.rows) {
+            const TileRow nxt = g_next >= 0 ? tile_row_of<MODE>(a, g_next, q_next) : no_tile_row();
+            const int64_t g_after = grow_of(tile + 2 * step);
+            q_next = g_after >= 0 ? row_pair(a, g_after) : -1;
+            if (g_cur >= 0) {  // CTA-uniform: the TMEM loads stay warp-wide
                 const uint32_t taddr =
                     tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kColsPerAcc;
-                store_tile<MODE, BN>(a, taddr, r, tile % n_tiles);
+                store_tile<MODE, BN>(a, taddr, cur, tile % n_tiles);
             }
+            cur = nxt;
+            g_cur = g_next;
+            g_next = g_after;
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) arrive_cluster_relaxed(acc ? acc_empty1 : acc_empty0);

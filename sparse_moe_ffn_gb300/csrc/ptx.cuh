@@ -273,6 +273,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// 32-byte store (8 words); p must be 32-byte aligned.  A thread that owns a
+// whole output row writes full 32-byte sectors this way, where 16-byte
+// stores to 32 different rows per warp leave every sector half written.
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t (&v)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]),
+                 "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
     __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&h);
