@@ -316,8 +316,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // blocks, or of every block when all_blocks is set (the CTA-pair kernel loads
 // every block with tiled boxes).  One CTA per row block (grid-stride): a
 // broadcast load of the block's row kSparseRows decides whether it is dense,
-// so sparse blocks (all of them at decode) cost one load.  Warp w copies rows w, w + 8, ... until the first padding row
-// (real rows come first), four 16-byte loads in flight per lane.  The stores
+// so sparse blocks (all of them at decode) cost one load.  Warp w copies rows
+// w, w + 8, ..., w + 120: their 16 row-map entries come with one load, then
+// two rows at a time are copied with all their 16-byte loads in flight before
+// the stores, until the first padding row (real rows come first).  The stores
 // are streaming (evict-first): the GEMM reads each x_sorted row once, while
 // each x row is read k times here and should stay in L2.
 constexpr int kGatherThreads = 256;
@@ -330,7 +332,8 @@ __global__ void __launch_bounds__(kGatherThreads)
     griddep_launch_dependents();
     griddep_wait();
     constexpr int kWarps = kGatherThreads / 32;
-    constexpr int kUnroll = 4;
+    constexpr int kRowsPerWarp = kBlockM / kWarps;  // 16
+    constexpr int kUnroll = 4;                      // 16-byte pieces per lane per row in flight
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     const int64_t nblocks = min(static_cast<int64_t>(__ldcg(num_padded)), cap) / kBlockM;
@@ -341,20 +344,34 @@ __global__ void __launch_bounds__(kGatherThreads)
             const int32_t probe = __ldcg(sorted_pair + base + kSparseRows);
             if (probe < 0 || probe >= P) continue;  // sparse block: its rows are gathered by TMA
         }
-        for (int r = warp; r < kBlockM; r += kWarps) {
-            const int32_t q = __ldcg(sorted_pair + base + r);
-            if (q < 0 || q >= P) break;  // padding from here on
-            const uint4 *src = reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(q / k) * H);
-            uint4 *dst = reinterpret_cast<uint4 *>(x_sorted + (base + r) * H);
+        const int32_t q_lane =
+            lane < kRowsPerWarp ? __ldcg(sorted_pair + base + warp + kWarps * lane) : -1;
+        for (int i = 0; i < kRowsPerWarp; i += 2) {
+            const int32_t q0 = __shfl_sync(0xffffffffu, q_lane, i);
+            const int32_t q1 = __shfl_sync(0xffffffffu, q_lane, i + 1);
+            const bool v0 = q0 >= 0 && q0 < P;
+            const bool v1 = v0 && q1 >= 0 && q1 < P;  // padding only after the real rows
+            if (!v0) break;
+            const uint4 *s0 = reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(q0 / k) * H);
+            const uint4 *s1 = reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(v1 ? q1 / k : 0) * H);
+            uint4 *d0 = reinterpret_cast<uint4 *>(x_sorted + (base + warp + kWarps * i) * H);
+            uint4 *d1 = reinterpret_cast<uint4 *>(x_sorted + (base + warp + kWarps * (i + 1)) * H);
             for (int c0 = lane; c0 < n16; c0 += 32 * kUnroll) {
-                uint4 v[kUnroll];
+                uint4 a0[kUnroll], a1[kUnroll];
 #pragma unroll
-                for (int u = 0; u < kUnroll; ++u)
-                    if (c0 + 32 * u < n16) v[u] = __ldcg(src + c0 + 32 * u);
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int c = c0 + 32 * u;
+                    if (c < n16) a0[u] = __ldcg(s0 + c);
+                    if (v1 && c < n16) a1[u] = __ldcg(s1 + c);
+                }
 #pragma unroll
-                for (int u = 0; u < kUnroll; ++u)
-                    if (c0 + 32 * u < n16) __stcs(dst + c0 + 32 * u, v[u]);
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int c = c0 + 32 * u;
+                    if (c < n16) __stcs(d0 + c, a0[u]);
+                    if (v1 && c < n16) __stcs(d1 + c, a1[u]);
+                }
             }
+            if (!v1) break;
         }
     }
 }
