@@ -228,9 +228,14 @@ __global__ void __launch_bounds__(kScanThreads)
                        int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
                        int32_t *__restrict__ pad_offsets, int32_t *__restrict__ num_padded,
                        int32_t *__restrict__ sorted_pair, int32_t *__restrict__ block_expert,
-                       int32_t *status) {
+                       int32_t *status, int32_t *__restrict__ expert_ready) {
     griddep_launch_dependents();
     griddep_wait();
+    // the hand-off counters of the decode GEMMs start from zero every call
+    // (the previous call's GEMMs are complete: this kernel follows routing,
+    // which followed the previous call's last kernel)
+    if (expert_ready)
+        for (int e = threadIdx.x; e < E; e += blockDim.x) expert_ready[e] = 0;
     __shared__ int32_t hist[kSmallMaxE];
     __shared__ int32_t pad_smem[kSmallMaxE + 1];
     __shared__ int32_t running[kSmallMaxE];
@@ -317,12 +322,14 @@ __global__ void __launch_bounds__(kScanThreads)
 
 }  // namespace
 
+bool align_is_single_cta(int64_t P, int E) { return P <= kSmallPairs && E <= kSmallMaxE; }
+
 cudaError_t launch_align(const AlignArgs &a, cudaStream_t s, int *launches) {
-    if (a.P <= kSmallPairs && a.E <= kSmallMaxE) {
+    if (align_is_single_cta(a.P, a.E)) {
         *launches += 1;
         return launch_pdl(align_small_kernel, dim3(1), dim3(kScanThreads), 0, s, 1, a.ids, a.P,
                           a.E, a.block_m, a.counts, a.offsets, a.pad_offsets, a.num_padded,
-                          a.sorted_pair, a.block_expert, a.status);
+                          a.sorted_pair, a.block_expert, a.status, a.expert_ready);
     }
     // the count and scatter kernels hold a chunk's ids in registers
     if (a.chunk != kAlignChunk) return cudaErrorInvalidValue;

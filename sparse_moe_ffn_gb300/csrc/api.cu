@@ -214,6 +214,7 @@ moe_status_t enqueue_route(const moe_bf16_t *x, const moe_bf16_t *router,
 struct AlignBuffers {
     int32_t *sorted_pair, *block_expert, *counts, *offsets, *pad_offsets, *num_padded, *scratch;
     int32_t *status;
+    int32_t *expert_ready = nullptr;
 };
 
 moe_status_t enqueue_align(const int32_t *ids, int64_t N, int k, int E, int block_m,
@@ -233,6 +234,7 @@ moe_status_t enqueue_align(const int32_t *ids, int64_t N, int k, int E, int bloc
     aa.sorted_pair = b.sorted_pair;
     aa.block_expert = b.block_expert;
     aa.status = b.status;
+    aa.expert_ready = b.expert_ready;
     int launches = 0;
     cudaError_t e = launch_align(aa, stream, &launches);
     g_launches += launches;
@@ -274,6 +276,7 @@ moe_status_t forward_layout(int64_t N, int H, int E, int I, int k, int I_s,
     L->align_scratch = take(sizeof(int32_t) * static_cast<size_t>(align_chunks(P)) * E);
     L->sorted_pair = take(sizeof(int32_t) * cap);
     L->block_expert = take(sizeof(int32_t) * (cap / kBlockM));
+    L->expert_ready = take(sizeof(int32_t) * E);
     L->x_sorted = take(2 * static_cast<size_t>(cap) * H);
     L->act = take(2 * static_cast<size_t>(cap) * I);
     L->ypair = take(2 * static_cast<size_t>(P) * H);  // fp16
@@ -349,6 +352,14 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
     const int64_t cap = L.capacity;
     const int sms = num_sms_of_current_device();
 
+    // Decode hand-off: with expert-indexed gate/up tiles (every expert owns
+    // at most one row block) and a single-CTA grouping kernel (which zeroes
+    // the counters), the down GEMM waits per expert for its activation rows
+    // instead of for the whole gate/up grid.
+    const bool handoff = !use_pair_tiles(P, E) && use_sparse_tiles(P, E) && N <= kBlockM &&
+                         align_is_single_cta(P, E);
+    int32_t *expert_ready = reinterpret_cast<int32_t *>(at(L.expert_ready));
+
     // K2: grouping
     if ((st = record_stage(MOE_STAGE_ALIGN, stream)) != MOE_OK) return st;
     AlignBuffers b;
@@ -360,6 +371,7 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
     b.num_padded = reinterpret_cast<int32_t *>(at(L.num_padded));
     b.scratch = reinterpret_cast<int32_t *>(at(L.align_scratch));
     b.status = status;
+    b.expert_ready = handoff ? expert_ready : nullptr;
     st = enqueue_align(ids, N, k, E, kBlockM, b, stream);
     if (st != MOE_OK) return st;
 
@@ -384,6 +396,8 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
     g.num_groups = E;
     g.expert_tiles = 0;
     g.w0 = g.w1 = nullptr;
+    g.act_ready = nullptr;
+    g.act_ready_count = 0;
     g.num_padded = b.num_padded;
     g.num_rows_host = cap;
     g.q_limit = P;
@@ -419,6 +433,10 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
             g.w1 = w_up;
             g.max_tiles = E * ((I + bn_gu - 1) / bn_gu);
             g.grid = g.max_tiles < sms ? g.max_tiles : sms;
+            if (handoff) {  // kept for the down GEMM below
+                g.act_ready = expert_ready;
+                g.act_ready_count = (I + bn_gu - 1) / bn_gu;
+            }
         }
         MOE_CUDA(launch_sparse_gemm(kGateUp, bn_gu, tm_xrows, tm_wg, tm_wu, g, stream),
                  "gate/up kernel launch");
@@ -670,6 +688,8 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
         s.num_groups = 0;
         s.expert_tiles = 0;
         s.w0 = s.w1 = nullptr;
+        s.act_ready = nullptr;
+        s.act_ready_count = 0;
         s.K = H;
         s.n_out = I_s;
         s.w_rows = I_s;

@@ -273,6 +273,25 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// Acquire load at GPU scope (pairs with red_release_gpu in another CTA).
+__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t *p) {
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Release add at GPU scope: every earlier write of this thread (and, through
+// a preceding warp barrier, of its warp) is visible before the new count.
+__device__ __forceinline__ void red_release_gpu(int32_t *p, int32_t v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Orders this thread's generic-proxy accesses to global memory with its
+// async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // 32-byte store (8 words); p must be 32-byte aligned.  A thread that owns a
 // whole output row writes full 32-byte sectors this way, where 16-byte
 // stores to 32 different rows per warp leave every sector half written.

@@ -140,7 +140,12 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
     volatile int *abort_flag = &sm->abort_flag;
     const int n_tiles = (a.n_out + BN - 1) / BN;
     const bool by_expert = a.expert_tiles != 0;
-    griddep_launch_dependents();
+    // decode hand-off (act_ready): the down GEMM launched after this one does
+    // not wait for this grid but for per-expert counts, and it reads the
+    // block list from the kernels before this one; so gate/up lets it launch
+    // only once every gate/up CTA has seen those kernels complete
+    const bool handoff = a.act_ready != nullptr;
+    if (!(MODE == kGateUp && handoff)) griddep_launch_dependents();
     // weights are inputs, not results of earlier kernels: with expert-indexed
     // tiles the first tile's weight rows are known now, and L2 fetches them
     // while memory is otherwise idle (routing)
@@ -157,7 +162,10 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
             if (MODE == kGateUp) prefetch_l2_bulk(static_cast<const uint8_t *>(a.w1) + off, bytes);
         }
     }
-    griddep_wait();  // the block list and the A rows come from earlier kernels
+    // the block list and the A rows come from earlier kernels (with the
+    // hand-off, down waits per expert for its A rows instead)
+    if (!(MODE == kDown && handoff)) griddep_wait();
+    if (MODE == kGateUp && handoff) griddep_launch_dependents();
 
     int total_tiles;
     if (by_expert) {
@@ -258,6 +266,27 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
             for (int i = 0; i < 4; ++i)
                 if (src[i] < 0) src[i] = first_valid;
             const int brow = static_cast<int>(static_cast<int64_t>(expert) * a.w_rows) + nt * BN;
+            if (MODE == kDown && handoff && passes > 0) {
+                // this expert's activation rows are complete once all its
+                // gate/up tiles are stored (bounded wait, warp-uniform)
+                const int32_t *count = a.act_ready + expert;
+                const uint64_t t0 = __shfl_sync(0xffffffffu, global_timer_ns(), 0);
+                bool ready = false;
+                while (true) {
+                    ready = __all_sync(0xffffffffu, ld_acquire_gpu(count) >= a.act_ready_count);
+                    if (ready || __any_sync(0xffffffffu, *abort_flag != 0)) break;
+                    if (__shfl_sync(0xffffffffu, global_timer_ns() - t0 > kWaitTimeoutNs, 0)) break;
+                }
+                if (!ready) {
+                    if (lane == 0) {
+                        record_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
+                        *abort_flag = 1;
+                    }
+                    failed = true;
+                    break;
+                }
+                fence_proxy_async_global();  // the TMA reads below see those rows
+            }
             for (int p = 0; p < passes && !failed; ++p) {
                 const bool mine = lane / 8 == p && any;  // lanes 8p .. 8p+7 gather pass p
                 const uint32_t groups = __popc(__ballot_sync(0xffffffffu, mine));
@@ -390,6 +419,12 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
                 }
                 tc_fence_after_sync();
                 if (quarter == 0) store_tile<MODE, BN>(a, tmem + acc * kAccCols, r, tile % n_tiles);
+                if (MODE == kGateUp && handoff && quarter == 0 && p == passes - 1) {
+                    // publish the tile: its rows' stores, then the count
+                    fence_proxy_async_global();
+                    __syncwarp();
+                    if (lane == 0) red_release_gpu(a.act_ready + expert_of(tile), 1);
+                }
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sm->acc_empty[acc]);
