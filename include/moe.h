@@ -333,7 +333,7 @@ typedef struct {
     size_t align_scratch; /* int32 [chunks, E]                                */
     size_t sorted_pair;   /* int32 [capacity]                                 */
     size_t block_expert;  /* int32 [capacity / 128]                           */
-    size_t expert_ready;  /* int32 [E] gate/up tiles stored per expert (decode) */
+    size_t ready;         /* int32 [max(E, capacity/128)] GEMM hand-off counts */
     size_t x_sorted;      /* bf16 [capacity, H]   x rows in expert order (dense blocks) */
     size_t act;           /* fp16 [capacity, I]   a = silu(x Wg^T) * (x Wu^T)  */
     size_t ypair;         /* fp16 [N*k, H]        w * Expert(x), per pair     */

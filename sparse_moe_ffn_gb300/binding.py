@@ -28,7 +28,7 @@ class MoEError(RuntimeError):
 class _Layout(ctypes.Structure):
     _fields_ = [(name, ctypes.c_size_t) for name in (
         "status", "topk_w", "topk_ids", "gamma", "counts", "offsets", "pad_offsets",
-        "num_padded", "align_scratch", "sorted_pair", "block_expert", "expert_ready", "x_sorted", "act", "ypair",
+        "num_padded", "align_scratch", "sorted_pair", "block_expert", "ready", "x_sorted", "act", "ypair",
         "act_shared", "y_shared", "total")] + [("capacity", ctypes.c_int64)]
 
 

@@ -106,7 +106,15 @@ __device__ __forceinline__ int owner_of(const int32_t *pad_off, int E, int64_t s
 
 // every padded slot gets the sentinel P, every row block its owner expert
 __device__ void fill_padded(const int32_t *pad_off_smem, int E, int block_m, int32_t num_padded,
-                            int64_t P, int32_t *sorted_pair, int32_t *block_expert) {
+                            int64_t P, int32_t *sorted_pair, int32_t *block_expert,
+                            int32_t *ready) {
+    // the GEMMs' hand-off counters (per expert or per block pair) start from
+    // zero every call; the previous call's GEMMs are complete, since this
+    // kernel follows routing, which followed the previous call's last kernel
+    if (ready) {
+        const int32_t n = E > num_padded / block_m ? E : num_padded / block_m;
+        for (int32_t i = threadIdx.x; i < n; i += blockDim.x) ready[i] = 0;
+    }
     for (int32_t i = threadIdx.x; i < num_padded; i += blockDim.x)
         sorted_pair[i] = static_cast<int32_t>(P);
     for (int32_t b = threadIdx.x; b < num_padded / block_m; b += blockDim.x)
@@ -117,7 +125,8 @@ __global__ void __launch_bounds__(kScanThreads)
     align_scan_kernel(int32_t *__restrict__ chunk_counts, int nchunks, int E, int block_m,
                       int64_t P, int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
                       int32_t *__restrict__ pad_offsets, int32_t *__restrict__ num_padded,
-                      int32_t *__restrict__ block_expert, int32_t *__restrict__ sorted_pair) {
+                      int32_t *__restrict__ block_expert, int32_t *__restrict__ sorted_pair,
+                      int32_t *__restrict__ ready) {
     griddep_launch_dependents();
     griddep_wait();
     __shared__ int32_t warp_sums[32];
@@ -162,7 +171,7 @@ __global__ void __launch_bounds__(kScanThreads)
     }
     __syncthreads();
     // the scatter kernel overwrites the real slots after this kernel ends
-    fill_padded(pad_smem, E, block_m, npad, P, sorted_pair, block_expert);
+    fill_padded(pad_smem, E, block_m, npad, P, sorted_pair, block_expert, ready);
 }
 
 __global__ void __launch_bounds__(kAlignThreads)
@@ -228,14 +237,9 @@ __global__ void __launch_bounds__(kScanThreads)
                        int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
                        int32_t *__restrict__ pad_offsets, int32_t *__restrict__ num_padded,
                        int32_t *__restrict__ sorted_pair, int32_t *__restrict__ block_expert,
-                       int32_t *status, int32_t *__restrict__ expert_ready) {
+                       int32_t *status, int32_t *__restrict__ ready) {
     griddep_launch_dependents();
     griddep_wait();
-    // the hand-off counters of the decode GEMMs start from zero every call
-    // (the previous call's GEMMs are complete: this kernel follows routing,
-    // which followed the previous call's last kernel)
-    if (expert_ready)
-        for (int e = threadIdx.x; e < E; e += blockDim.x) expert_ready[e] = 0;
     __shared__ int32_t hist[kSmallMaxE];
     __shared__ int32_t pad_smem[kSmallMaxE + 1];
     __shared__ int32_t running[kSmallMaxE];
@@ -288,7 +292,7 @@ __global__ void __launch_bounds__(kScanThreads)
         }
     }
     __syncthreads();
-    fill_padded(pad_smem, E, block_m, npad, P, sorted_pair, block_expert);
+    fill_padded(pad_smem, E, block_m, npad, P, sorted_pair, block_expert, ready);
     __syncthreads();  // sentinels first, then the real pairs over them
     const uint32_t lanes_below = (1u << lane) - 1u;
 #pragma unroll
@@ -322,14 +326,12 @@ __global__ void __launch_bounds__(kScanThreads)
 
 }  // namespace
 
-bool align_is_single_cta(int64_t P, int E) { return P <= kSmallPairs && E <= kSmallMaxE; }
-
 cudaError_t launch_align(const AlignArgs &a, cudaStream_t s, int *launches) {
-    if (align_is_single_cta(a.P, a.E)) {
+    if (a.P <= kSmallPairs && a.E <= kSmallMaxE) {
         *launches += 1;
         return launch_pdl(align_small_kernel, dim3(1), dim3(kScanThreads), 0, s, 1, a.ids, a.P,
                           a.E, a.block_m, a.counts, a.offsets, a.pad_offsets, a.num_padded,
-                          a.sorted_pair, a.block_expert, a.status, a.expert_ready);
+                          a.sorted_pair, a.block_expert, a.status, a.ready);
     }
     // the count and scatter kernels hold a chunk's ids in registers
     if (a.chunk != kAlignChunk) return cudaErrorInvalidValue;
@@ -340,7 +342,7 @@ cudaError_t launch_align(const AlignArgs &a, cudaStream_t s, int *launches) {
     if (err != cudaSuccess) return err;
     err = launch_pdl(align_scan_kernel, dim3(1), dim3(kScanThreads), 0, s, 1, a.chunk_counts,
                      a.nchunks, a.E, a.block_m, a.P, a.counts, a.offsets, a.pad_offsets,
-                     a.num_padded, a.block_expert, a.sorted_pair);
+                     a.num_padded, a.block_expert, a.sorted_pair, a.ready);
     if (err != cudaSuccess) return err;
     const size_t scatter_smem = sizeof(int32_t) * (a.E + kAlignWarps * a.E);
     if (scatter_smem > 48 * 1024) {

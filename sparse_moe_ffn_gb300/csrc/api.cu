@@ -214,7 +214,7 @@ moe_status_t enqueue_route(const moe_bf16_t *x, const moe_bf16_t *router,
 struct AlignBuffers {
     int32_t *sorted_pair, *block_expert, *counts, *offsets, *pad_offsets, *num_padded, *scratch;
     int32_t *status;
-    int32_t *expert_ready = nullptr;
+    int32_t *ready = nullptr;
 };
 
 moe_status_t enqueue_align(const int32_t *ids, int64_t N, int k, int E, int block_m,
@@ -234,7 +234,7 @@ moe_status_t enqueue_align(const int32_t *ids, int64_t N, int k, int E, int bloc
     aa.sorted_pair = b.sorted_pair;
     aa.block_expert = b.block_expert;
     aa.status = b.status;
-    aa.expert_ready = b.expert_ready;
+    aa.ready = b.ready;
     int launches = 0;
     cudaError_t e = launch_align(aa, stream, &launches);
     g_launches += launches;
@@ -276,7 +276,7 @@ moe_status_t forward_layout(int64_t N, int H, int E, int I, int k, int I_s,
     L->align_scratch = take(sizeof(int32_t) * static_cast<size_t>(align_chunks(P)) * E);
     L->sorted_pair = take(sizeof(int32_t) * cap);
     L->block_expert = take(sizeof(int32_t) * (cap / kBlockM));
-    L->expert_ready = take(sizeof(int32_t) * E);
+    L->ready = take(sizeof(int32_t) * (E > cap / kBlockM ? E : cap / kBlockM));
     L->x_sorted = take(2 * static_cast<size_t>(cap) * H);
     L->act = take(2 * static_cast<size_t>(cap) * I);
     L->ypair = take(2 * static_cast<size_t>(P) * H);  // fp16
@@ -353,12 +353,13 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
     const int sms = num_sms_of_current_device();
 
     // Decode hand-off: with expert-indexed gate/up tiles (every expert owns
-    // at most one row block) and a single-CTA grouping kernel (which zeroes
-    // the counters), the down GEMM waits per expert for its activation rows
-    // instead of for the whole gate/up grid.
-    const bool handoff = !use_pair_tiles(P, E) && use_sparse_tiles(P, E) && N <= kBlockM &&
-                         align_is_single_cta(P, E);
-    int32_t *expert_ready = reinterpret_cast<int32_t *>(at(L.expert_ready));
+    // at most one row block) the down GEMM waits per expert for its
+    // activation rows instead of for the whole gate/up grid (the grouping
+    // kernel zeroes the counters).
+    const bool handoff = !use_pair_tiles(P, E) && use_sparse_tiles(P, E) && N <= kBlockM;
+    // the same for the CTA-pair GEMMs (prefill), per block pair
+    const bool pair_handoff = use_pair_tiles(P, E);
+    int32_t *ready = reinterpret_cast<int32_t *>(at(L.ready));
 
     // K2: grouping
     if ((st = record_stage(MOE_STAGE_ALIGN, stream)) != MOE_OK) return st;
@@ -371,7 +372,7 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
     b.num_padded = reinterpret_cast<int32_t *>(at(L.num_padded));
     b.scratch = reinterpret_cast<int32_t *>(at(L.align_scratch));
     b.status = status;
-    b.expert_ready = handoff ? expert_ready : nullptr;
+    b.ready = handoff || pair_handoff ? ready : nullptr;
     st = enqueue_align(ids, N, k, E, kBlockM, b, stream);
     if (st != MOE_OK) return st;
 
@@ -434,7 +435,7 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
             g.max_tiles = E * ((I + bn_gu - 1) / bn_gu);
             g.grid = g.max_tiles < sms ? g.max_tiles : sms;
             if (handoff) {  // kept for the down GEMM below
-                g.act_ready = expert_ready;
+                g.act_ready = ready;
                 g.act_ready_count = (I + bn_gu - 1) / bn_gu;
             }
         }
@@ -453,6 +454,11 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
         const int max_pairs = static_cast<int>(cap / kBlockM);  // pairs <= blocks
         g.max_tiles = max_pairs * ((I + bn - 1) / bn);
         g.grid = 2 * (g.max_tiles < sms / 2 ? g.max_tiles : sms / 2);
+        if (pair_handoff) {  // kept for the down GEMM below
+            // one arrival per epilogue warp (4) of both CTAs per gate/up tile
+            g.act_ready = ready;
+            g.act_ready_count = 8 * ((I + bn - 1) / bn);
+        }
         MOE_CUDA(launch_pair_gemm(kGateUp, tm_xsorted, tm_wg_tile, tm_wu_tile, g, stream),
                  "gate/up kernel launch");
     } else {

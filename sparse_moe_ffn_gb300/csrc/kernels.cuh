@@ -76,14 +76,13 @@ struct AlignArgs {
     int32_t *counts, *offsets, *pad_offsets, *num_padded;
     int32_t *sorted_pair, *block_expert;
     int32_t *status;
-    int32_t *expert_ready;  // nullable: [E] counters zeroed for the sparse GEMMs' hand-off
+    // nullable: GEMM hand-off counters, ready[i] = 0 for i < max(E, padded
+    // rows / block_m) (per expert at decode, per block pair at prefill)
+    int32_t *ready;
 };
 
 constexpr int kAlignChunk = 2048;
 cudaError_t launch_align(const AlignArgs &a, cudaStream_t s, int *launches);
-// the grouping of P pairs over E experts runs as one CTA (which also zeroes
-// expert_ready); the other path leaves expert_ready untouched
-bool align_is_single_cta(int64_t P, int E);
 
 // ------------------------------------------------------------ grouped GEMM
 
@@ -118,10 +117,13 @@ struct GemmArgs {
     int expert_tiles;
     const void *w0;
     const void *w1;
-    // sparse kernel, decode hand-off: gate/up adds 1 to act_ready[e] when a
-    // tile of expert e is stored; down then waits, per tile, for
-    // act_ready[e] == act_ready_count instead of for the whole gate/up grid,
-    // so its CTAs start on the SMs that gate/up frees first (null: off)
+    // hand-off from gate/up to down (null: off).  Sparse kernel (decode):
+    // gate/up adds 1 to act_ready[e] when a tile of expert e is stored.
+    // CTA-pair kernel (prefill): each epilogue warp of both CTAs adds 1 to
+    // act_ready[j] when it has stored its rows of a tile of block pair j.
+    // Down then waits, per tile, for act_ready[e or j] == act_ready_count
+    // instead of for the whole gate/up grid, so its CTAs start on the SMs
+    // that gate/up frees first.
     int32_t *act_ready;
     int act_ready_count;
     int max_tiles;      // upper bound on tiles (sizes the persistent grid)

@@ -235,8 +235,14 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem = sm->tmem_base;
     volatile int *abort_flag = &sm->abort_flag;
-    griddep_launch_dependents();
-    griddep_wait();  // the block list and the A rows come from earlier kernels
+    // hand-off (act_ready): down waits per block pair for its A rows, not for
+    // the gate/up grid, and reads the block list from the kernels before
+    // gate/up; so gate/up lets it launch only after its own dependency wait
+    const bool handoff = a.act_ready != nullptr;
+    if (!(MODE == kGateUp && handoff)) griddep_launch_dependents();
+    // the block list and the A rows come from earlier kernels
+    if (!(MODE == kDown && handoff)) griddep_wait();
+    if (MODE == kGateUp && handoff) griddep_launch_dependents();
 
     // pair prefix over the groups (experts): warp 2 scans, 8 groups per lane
     if (warp == 2) {
@@ -297,6 +303,23 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             bool failed = false;
             for (int tile = pair_id; tile < total_tiles && !failed; tile += num_pairs) {
                 const PairTile pt = pair_of(sm, tile / n_tiles, rank);
+                if (MODE == kDown && handoff && pt.rows) {
+                    // this block pair's activation rows are complete once
+                    // every gate/up epilogue warp of both CTAs has stored
+                    // its rows of every gate/up tile of the pair (bounded)
+                    const int32_t *count = a.act_ready + tile / n_tiles;
+                    const uint64_t t0 = global_timer_ns();
+                    bool ready = ld_acquire_gpu(count) >= a.act_ready_count;
+                    while (!ready && *abort_flag == 0 && global_timer_ns() - t0 <= kWaitTimeoutNs)
+                        ready = ld_acquire_gpu(count) >= a.act_ready_count;
+                    if (!ready) {
+                        record_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
+                        *abort_flag = 1;
+                        failed = true;
+                        break;
+                    }
+                    fence_proxy_async_global();  // the TMA reads below see those rows
+                }
                 const int nt = tile % n_tiles;
                 const uint32_t a_bytes = kATileBytes;
                 const uint32_t tx = 2 * kBBytes +
@@ -414,6 +437,13 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 const uint32_t taddr =
                     tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kColsPerAcc;
                 store_tile<MODE, BN>(a, taddr, cur, tile % n_tiles);
+            }
+            if (MODE == kGateUp && handoff) {
+                // publish this warp's rows of the tile (a CTA without rows
+                // publishes too: the count is per warp of both CTAs)
+                fence_proxy_async_global();
+                __syncwarp();
+                if (lane == 0) red_release_gpu(a.act_ready + tile / n_tiles, 1);
             }
             cur = nxt;
             g_cur = g_next;
