@@ -23,6 +23,12 @@ Step 4 computes each pair as moe_forward does, and step 5 is moe_forward's
 own combine.  So the output equals moe_forward on the same tokens bit for
 bit, whatever the number of ranks.
 
+The shared expert (the talker layer) is dense: every rank holds its weights
+and applies it to its own tokens, with no exchange.  It runs as moe_experts
+with one expert, every row routed to it and the sigmoid gate as the row
+weight, which is moe_forward's shared term fp16(gamma * SharedMLP(x)); the
+combine adds it after the k slots.
+
 Transport: gloo and NCCL both carry int32, so bf16 and fp16 rows travel as
 their bit patterns viewed as int32 (H is even).  With one rank nothing is
 exchanged.  The three compute steps can be replaced (route_fn, experts_fn,
@@ -70,12 +76,16 @@ def _exchange(t: torch.Tensor, send_counts, recv_counts, group):
 
 
 def ep_forward(x, router, w_gate, w_up, w_down, E: int, k: int, norm_topk_prob: bool = True,
-               group=None, route_fn=None, experts_fn=None, combine_fn=None):
+               group=None, shared=None, route_fn=None, experts_fn=None, shared_fn=None,
+               combine_fn=None):
     """One MoE layer with experts split across the ranks of ``group``.
 
     x [N, H] bf16 (this rank's tokens), router [E, H] bf16 (all experts);
     w_gate, w_up [E_r, I, H] bf16 and w_down [E_r, H, I] fp16 (see
-    binding.prepare_weights): this rank's experts.
+    binding.prepare_weights): this rank's experts.  ``shared``: None or the
+    shared expert (binding.SHARED_KEYS, shared_down_proj in fp16), the same
+    on every rank.  route_fn(x) returns (weights, ids) or (weights, ids,
+    gamma); shared_fn(x, gamma) returns the fp16 shared term.
     Returns out [N, H] bf16."""
     from sparse_moe_ffn_gb300 import binding
 
@@ -83,16 +93,27 @@ def ep_forward(x, router, w_gate, w_up, w_down, E: int, k: int, norm_topk_prob: 
     N, H = x.shape
     if route_fn is None:
         def route_fn(t):
-            w, ids, _, _ = binding.moe_route_raw(t, router, k, norm_topk_prob)
-            return w, ids
+            gate = shared["shared_gate"] if shared is not None else None
+            w, ids, gamma, _ = binding.moe_route_raw(t, router, k, norm_topk_prob, gate)
+            return w, ids, gamma
     if experts_fn is None:
         def experts_fn(rows, local_ids, weights):
             return binding.moe_experts(rows, local_ids, weights, w_gate, w_up, w_down)[0]
+    if shared_fn is None and shared is not None:
+        def shared_fn(t, gamma):
+            zeros = torch.zeros(t.shape[0], dtype=torch.int32, device=t.device)
+            return binding.moe_experts(t, zeros, gamma, shared["shared_gate_proj"][None],
+                                       shared["shared_up_proj"][None],
+                                       shared["shared_down_proj"][None])[0]
     if combine_fn is None:
-        def combine_fn(ypair, n, kk):
-            return binding.moe_combine(ypair, n, kk)
+        def combine_fn(ypair, n, kk, yshared=None):
+            return binding.moe_combine(ypair, n, kk, yshared)
 
-    w, ids = route_fn(x)
+    routed = route_fn(x)
+    w, ids = routed[0], routed[1]
+    gamma = routed[2] if len(routed) > 2 else None
+    # the shared term needs no exchange: it can run before the dispatch
+    yshared = shared_fn(x, gamma) if shared_fn is not None else None
     order, dest, send_counts, E_local = ep_plan(ids, E, world)
     send_x = x.index_select(0, order // k)
     send_e = (ids.reshape(-1).long()[order] - dest[order] * E_local).to(torch.int32)
@@ -119,4 +140,6 @@ def ep_forward(x, router, w_gate, w_up, w_down, E: int, k: int, norm_topk_prob: 
                            group).view(torch.float16)
     ypair = torch.empty((N * k, H), dtype=torch.float16, device=x.device)
     ypair[order] = y_back
-    return combine_fn(ypair, N, k)
+    if yshared is None:
+        return combine_fn(ypair, N, k)
+    return combine_fn(ypair, N, k, yshared)

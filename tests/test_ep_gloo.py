@@ -26,8 +26,16 @@ def _pair_value(row, e, w):
     return (w * (row.float() * (e + 1) + e)).to(torch.float16)
 
 
-def _combine(ypair, n, k):
-    return ypair.float().view(n, k, -1).sum(dim=1).to(torch.bfloat16)
+def _combine(ypair, n, k, yshared=None):
+    acc = ypair.float().view(n, k, -1).sum(dim=1)
+    if yshared is not None:
+        acc = acc + yshared.float()
+    return acc.to(torch.bfloat16)
+
+
+def _shared_value(x, gamma):
+    """Stand-in for fp16(gamma * SharedMLP(x)), token-local."""
+    return (gamma[:, None] * (0.5 * x.float() - 1.0)).to(torch.float16)
 
 
 def _inputs(rank, N, H, E, k, all_to_rank0):
@@ -41,7 +49,7 @@ def _inputs(rank, N, H, E, k, all_to_rank0):
     return x, ids, w
 
 
-def _worker(rank, world, port, q, N, H, E, k, all_to_rank0):
+def _worker(rank, world, port, q, N, H, E, k, all_to_rank0, with_shared=False):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     import sys
     sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
@@ -61,24 +69,28 @@ def _worker(rank, world, port, q, N, H, E, k, all_to_rank0):
                                 for i in range(rows.shape[0])]) if rows.shape[0] else \
                 torch.empty((0, H), dtype=torch.float16)
 
+        gamma = torch.sigmoid(x.float()[:, 0]) if with_shared else None
         out = ep_forward(x, None, None, None, None, E, k, group=None,
-                         route_fn=lambda t: (w, ids), experts_fn=experts_fn,
+                         route_fn=lambda t: (w, ids, gamma), experts_fn=experts_fn,
+                         shared_fn=_shared_value if with_shared else None,
                          combine_fn=_combine)
         ref_pairs = torch.stack([_pair_value(x[p // k], int(ids.view(-1)[p]), float(w.view(-1)[p]))
                                  for p in range(N * k)])
-        ref = _combine(ref_pairs, N, k)
+        ref = _combine(ref_pairs, N, k, _shared_value(x, gamma) if with_shared else None)
         q.put((rank, bool(torch.equal(out, ref)), calls[0]))
     finally:
         dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("N,H,E,k,all_to_rank0", [(12, 16, 6, 2, False), (9, 8, 5, 3, False),
-                                                  (7, 16, 6, 2, True)])
-def test_two_ranks_match_the_unsplit_layer(N, H, E, k, all_to_rank0):
+@pytest.mark.parametrize("N,H,E,k,all_to_rank0,with_shared",
+                         [(12, 16, 6, 2, False, False), (9, 8, 5, 3, False, False),
+                          (7, 16, 6, 2, True, False), (10, 16, 6, 2, False, True)])
+def test_two_ranks_match_the_unsplit_layer(N, H, E, k, all_to_rank0, with_shared):
     world, port = 2, _free_port()
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
-    procs = [ctx.Process(target=_worker, args=(r, world, port, q, N, H, E, k, all_to_rank0))
+    procs = [ctx.Process(target=_worker,
+                         args=(r, world, port, q, N, H, E, k, all_to_rank0, with_shared))
              for r in range(world)]
     for p in procs:
         p.start()

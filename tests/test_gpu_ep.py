@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_cases import assert_close, prepare, prepared, run_forward, sample_rows
+from gpu_cases import assert_close, prepare, prepared, run_forward, sample_rows, shared_of
 from sparse_moe_ffn_gb300 import binding
 from sparse_moe_ffn_gb300.ep import ep_forward, ep_plan
 from sparse_moe_ffn_gb300.inputs import MoEShape
@@ -37,12 +37,14 @@ def test_experts_rows_and_combine_match_forward(name):
     assert torch.equal(binding.moe_combine(ypair, shape.N, shape.k), out)
 
 
-@pytest.mark.parametrize("name", ["decode", "prefill"])
+@pytest.mark.parametrize("name", ["decode", "prefill", "talker"])
 def test_ep_forward_one_rank_equals_forward(name):
+    """talker: the shared expert runs as a one-expert moe_experts call with
+    the sigmoid gate as the row weight, and matches moe_forward's term."""
     shape, dev, _ = prepared(name)
     out, _ = run_forward(shape, dev)
     got = ep_forward(dev["x"], dev["router"], dev["w_gate"], dev["w_up"], dev["w_down"],
-                     shape.E, shape.k, shape.norm_topk_prob)
+                     shape.E, shape.k, shape.norm_topk_prob, shared=shared_of(shape, dev))
     assert torch.equal(got, out)
 
 
