@@ -66,7 +66,7 @@ typedef enum {
     MOE_OK = 0,
     MOE_ERR_INVALID_ARG = 1,          /* null pointer, bad size, k > E, misalignment */
     MOE_ERR_WORKSPACE_TOO_SMALL = 2,  /* workspace_bytes below the *_workspace_bytes value */
-    MOE_ERR_UNSUPPORTED = 3,          /* valid but outside this build's limits (E > 256 ...) */
+    MOE_ERR_UNSUPPORTED = 3,          /* valid but outside the library's limits (E > 256 ...) */
     MOE_ERR_CUDA = 4,                 /* a CUDA runtime/driver call failed */
     MOE_ERR_DEVICE_CHECK = 5,         /* a kernel found a bad value (e.g. expert id >= E) */
     MOE_ERR_DEVICE_TIMEOUT = 6        /* a kernel's bounded wait ran out; it stopped early */
