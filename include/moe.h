@@ -353,8 +353,9 @@ moe_status_t moe_read_device_status(const void *workspace, cudaStream_t stream);
 
 /* Failure-detection self-check (not part of the layer; the pages have no
  * counterpart).  Enqueues a one-thread kernel that waits on a device barrier
- * nothing ever completes, through the same bounded wait the layer's kernels
- * use, giving up after limit_ns (0 < limit_ns <= 10 s).  The status word at
+ * nothing ever completes and then on a hand-off counter nothing ever
+ * increments, through the same bounded waits the layer's kernels use, each
+ * giving up after limit_ns (0 < limit_ns <= 10 s).  The status word at
  * the start of `workspace` (>= 4 bytes) then reads MOE_ERR_DEVICE_TIMEOUT and
  * the CUDA context stays usable. */
 moe_status_t moe_selftest_wait_timeout(void *workspace, size_t workspace_bytes,

@@ -307,12 +307,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     // this block pair's activation rows are complete once
                     // every gate/up epilogue warp of both CTAs has stored
                     // its rows of every gate/up tile of the pair (bounded)
-                    const int32_t *count = a.act_ready + tile / n_tiles;
-                    const uint64_t t0 = global_timer_ns();
-                    bool ready = ld_acquire_gpu(count) >= a.act_ready_count;
-                    while (!ready && *abort_flag == 0 && global_timer_ns() - t0 <= kWaitTimeoutNs)
-                        ready = ld_acquire_gpu(count) >= a.act_ready_count;
-                    if (!ready) {
+                    if (!wait_count_ns(a.act_ready + tile / n_tiles, a.act_ready_count,
+                                       abort_flag, kWaitTimeoutNs)) {
                         record_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
                         *abort_flag = 1;
                         failed = true;

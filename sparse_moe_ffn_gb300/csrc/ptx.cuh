@@ -286,6 +286,19 @@ __device__ __forceinline__ void red_release_gpu(int32_t *p, int32_t v) {
     asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Waits (one thread) until *count >= target, reading it with acquire loads.
+// Returns false if `abort_flag` became non-zero or `limit_ns` passed.
+__device__ __forceinline__ bool wait_count_ns(const int32_t *count, int32_t target,
+                                              volatile int *abort_flag, uint64_t limit_ns) {
+    if (ld_acquire_gpu(count) >= target) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (ld_acquire_gpu(count) >= target) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 // Orders this thread's generic-proxy accesses to global memory with its
 // async-proxy (TMA) accesses.
 __device__ __forceinline__ void fence_proxy_async_global() {

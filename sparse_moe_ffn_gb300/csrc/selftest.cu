@@ -1,13 +1,16 @@
 // selftest.cu -- device-side failure detection check: one thread waits on an
-// mbarrier that nothing ever completes, through the same bounded wait the
-// layer's kernels use; the wait must give up and record
-// MOE_ERR_DEVICE_TIMEOUT, and the kernel must return normally.
+// mbarrier that nothing ever completes, then on a hand-off counter that
+// nothing ever increments, through the same bounded waits the layer's kernels
+// use; both waits must give up, the kernel records MOE_ERR_DEVICE_TIMEOUT
+// (only when both did) and returns normally.
 #include "kernels.cuh"
 #include "ptx.cuh"
 
 namespace moe {
 
 namespace {
+
+__device__ int32_t g_never_counted = 0;  // no kernel ever adds to it
 
 __global__ void wait_timeout_probe(int32_t *status, uint64_t limit_ns) {
     __shared__ uint64_t bar;
@@ -18,7 +21,8 @@ __global__ void wait_timeout_probe(int32_t *status, uint64_t limit_ns) {
         fence_barrier_init();
     }
     __syncthreads();
-    if (threadIdx.x == 0 && !mbar_wait_ns(&bar, 0, &abort_flag, limit_ns))
+    if (threadIdx.x == 0 && !mbar_wait_ns(&bar, 0, &abort_flag, limit_ns) &&
+        !wait_count_ns(&g_never_counted, 1, &abort_flag, limit_ns))
         record_status(status, MOE_ERR_DEVICE_TIMEOUT);
 }
 

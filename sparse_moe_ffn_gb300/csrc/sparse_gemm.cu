@@ -268,15 +268,13 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
             const int brow = static_cast<int>(static_cast<int64_t>(expert) * a.w_rows) + nt * BN;
             if (MODE == kDown && handoff && passes > 0) {
                 // this expert's activation rows are complete once all its
-                // gate/up tiles are stored (bounded wait, warp-uniform)
-                const int32_t *count = a.act_ready + expert;
-                const uint64_t t0 = __shfl_sync(0xffffffffu, global_timer_ns(), 0);
+                // gate/up tiles are stored (bounded wait by lane 0; the warp
+                // barrier orders the other lanes' TMA copies after it)
                 bool ready = false;
-                while (true) {
-                    ready = __all_sync(0xffffffffu, ld_acquire_gpu(count) >= a.act_ready_count);
-                    if (ready || __any_sync(0xffffffffu, *abort_flag != 0)) break;
-                    if (__shfl_sync(0xffffffffu, global_timer_ns() - t0 > kWaitTimeoutNs, 0)) break;
-                }
+                if (lane == 0)
+                    ready = wait_count_ns(a.act_ready + expert, a.act_ready_count, abort_flag,
+                                          kWaitTimeoutNs);
+                ready = __shfl_sync(0xffffffffu, ready, 0);
                 if (!ready) {
                     if (lane == 0) {
                         record_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
