@@ -263,6 +263,9 @@ moe_status_t moe_convert_bf16_to_f16(const moe_bf16_t *src, moe_f16_t *dst, int6
  * have no counterpart; their layer works on device tensors).  Enqueued on
  * `stream`: copy x_host -> x_dev, the layer x_dev -> out_dev, copy out_dev ->
  * out_host.  The result is in out_host once the stream reaches that point.
+ * Pinned host buffers mapped into the device's address space (and 16-byte
+ * aligned) are copied by kernels on all SMs; other host memory by
+ * cudaMemcpyAsync.
  *   x_host, out_host  [N, H] bf16 host memory (pinned for asynchronous copies;
  *                     pageable memory makes the copies synchronous)
  *   x_dev, out_dev    [N, H] bf16 device buffers owned by the caller, 16-byte

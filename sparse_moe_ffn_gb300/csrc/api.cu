@@ -833,6 +833,31 @@ moe_status_t moe_convert_bf16_to_f16(const moe_bf16_t *src, moe_f16_t *dst, int6
     return MOE_OK;
 }
 
+}  // extern "C"
+
+namespace moe {
+// dst = src, bytes a multiple of 16, both 16-byte aligned device addresses
+// (one of them may be mapped pinned host memory); waits for the previous
+// kernel in the stream (convert.cu)
+cudaError_t launch_copy16(const void *src, void *dst, size_t bytes, int num_sms, cudaStream_t s);
+}  // namespace moe
+
+extern "C" {
+
+// The device address of pinned host memory mapped into the current device's
+// address space, 16-byte aligned; null for anything else (pageable memory,
+// unaligned buffers), which then takes cudaMemcpyAsync.
+static void *mapped_device_pointer(const void *host) {
+    if (!aligned16(host)) return nullptr;
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, host) != cudaSuccess) {
+        (void)cudaGetLastError();  // not a CUDA allocation: clear the error it left
+        return nullptr;
+    }
+    if (attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr) return nullptr;
+    return aligned16(attr.devicePointer) ? attr.devicePointer : nullptr;
+}
+
 moe_status_t moe_forward_host(const moe_bf16_t *x_host, moe_bf16_t *out_host, moe_bf16_t *x_dev,
                               moe_bf16_t *out_dev, const moe_bf16_t *router,
                               const moe_bf16_t *w_gate, const moe_bf16_t *w_up,
@@ -852,13 +877,29 @@ moe_status_t moe_forward_host(const moe_bf16_t *x_host, moe_bf16_t *out_host, mo
     if (!x_host || !out_host)
         return fail(MOE_ERR_INVALID_ARG, "x_host and out_host must be non-null");
     const size_t bytes = static_cast<size_t>(N) * H * sizeof(moe_bf16_t);
-    MOE_CUDA(cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, stream), "input copy");
+    // pinned, mapped host buffers are copied by kernels on all SMs over the
+    // CPU-GPU link; other host memory by the copy engines
+    const int sms = num_sms_of_current_device();
+    const void *x_map = mapped_device_pointer(x_host);
+    void *out_map = mapped_device_pointer(out_host);
+    if (x_map) {
+        MOE_CUDA(launch_copy16(x_map, x_dev, bytes, sms, stream), "input copy kernel launch");
+        g_launches += 1;
+    } else {
+        MOE_CUDA(cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, stream),
+                 "input copy");
+    }
     st = moe_forward(x_dev, router, w_gate, w_up, w_down, shared_gate_proj, shared_up_proj,
                      shared_down_proj, shared_gate, N, H, E, I, I_s, k, norm_topk_prob, out_dev,
                      workspace, workspace_bytes, stream);
     if (st != MOE_OK) return st;
-    MOE_CUDA(cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, stream),
-             "output copy");
+    if (out_map) {
+        MOE_CUDA(launch_copy16(out_dev, out_map, bytes, sms, stream), "output copy kernel launch");
+        g_launches += 1;
+    } else {
+        MOE_CUDA(cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, stream),
+                 "output copy");
+    }
     return MOE_OK;
 }
 

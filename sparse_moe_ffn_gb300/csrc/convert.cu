@@ -1,5 +1,7 @@
-// convert.cu -- the load-time conversion of the down-projection weights from
-// the model's bf16 to the fp16 operand format of the down GEMM.
+// convert.cu -- data movement around the layer: the load-time conversion of
+// the down-projection weights from the model's bf16 to the fp16 operand
+// format of the down GEMM, and the copies between pinned host buffers and
+// the device for moe_forward_host.
 //
 // bf16 -> fp32 is exact, and fp32 -> fp16 rounds to nearest even: a bf16
 // value carries 8 significant bits and fp16 11, so every value from 2^-14
@@ -49,7 +51,38 @@ __global__ void __launch_bounds__(kConvertThreads)
     if (bad) record_status(status, MOE_ERR_DEVICE_CHECK);
 }
 
+// dst[i] = src[i] over n16 16-byte words, one side being pinned host memory
+// mapped into the device's address space: all SMs read or write it over the
+// CPU-GPU link directly, four words per thread in flight.
+__global__ void __launch_bounds__(kConvertThreads)
+    copy16_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst, int64_t n16) {
+    griddep_launch_dependents();
+    griddep_wait();  // the source may be the previous kernel's output
+    constexpr int kUnroll = 4;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (int64_t i0 = tid; i0 < n16; i0 += stride * kUnroll) {
+        uint4 v[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+            if (i0 + u * stride < n16) v[u] = src[i0 + u * stride];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+            if (i0 + u * stride < n16) dst[i0 + u * stride] = v[u];
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_copy16(const void *src, void *dst, size_t bytes, int num_sms, cudaStream_t s) {
+    const int64_t n16 = static_cast<int64_t>(bytes / 16);
+    int64_t blocks = (n16 + kConvertThreads - 1) / kConvertThreads;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 4;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    return launch_pdl(copy16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kConvertThreads), 0,
+                      s, 1, static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), n16);
+}
 
 cudaError_t launch_convert_bf16_to_f16(const uint16_t *src, uint16_t *dst, int64_t n,
                                        int32_t *status, int num_sms, cudaStream_t s) {
