@@ -112,3 +112,24 @@ def test_plan_orders_pairs_by_destination_rank():
     assert counts.tolist() == [3, 3]
     with pytest.raises(ValueError):
         ep_plan(torch.tensor([[6]], dtype=torch.int32), E=6, world=2)
+
+
+@pytest.mark.parametrize("world", [1, 2, 3, 5, 8])
+def test_plan_properties_on_random_routing(world):
+    """For any routing table: the send order is a permutation of the pairs,
+    grouped by destination rank in rank order, in pair order within a rank;
+    every pair goes to the rank that owns its expert; counts add up."""
+    g = torch.Generator().manual_seed(world)
+    for N, k, E in [(1, 1, 1), (33, 4, 7), (64, 8, 128), (5, 3, 3)]:
+        ids = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(N)]).to(torch.int32)
+        order, dest, counts, E_local = ep_plan(ids, E, world)
+        flat = ids.reshape(-1).long()
+        assert E_local == -(-E // world)  # ceil(E / world); trailing ranks may own none
+        assert sorted(order.tolist()) == list(range(N * k))
+        assert torch.equal(dest, flat // E_local) and int(dest.max()) < world
+        d_sorted = dest[order]
+        assert torch.all(d_sorted[1:] >= d_sorted[:-1])
+        for r in range(world):
+            mine = order[d_sorted == r]
+            assert torch.all(mine[1:] > mine[:-1])  # stable: pair order within a rank
+        assert counts.tolist() == [int((dest == r).sum()) for r in range(world)]
