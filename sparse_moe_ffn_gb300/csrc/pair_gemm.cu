@@ -34,6 +34,10 @@
 //             accumulator barriers of both CTAs.
 //   warps 2-5 epilogue of the CTA's own 128 rows; each warp then arrives on
 //             the even CTA's accumulator-empty barrier (8 arrivals a round).
+// Hand-off (GemmArgs::act_ready): every gate/up epilogue warp of both CTAs
+// publishes its rows of a tile on the block pair's counter, and the down
+// GEMM, launched without waiting for the gate/up grid, loads a pair's
+// activation rows once all of the pair's arrivals are in.
 // Every wait is bounded; a CTA that gives up records MOE_ERR_DEVICE_TIMEOUT.
 #include <cuda_bf16.h>
 

@@ -26,6 +26,12 @@
 // and the epilogue never wait on a global load.  The next tile's row map
 // and expert are loaded while the current tile's stages are issued.
 //
+// Hand-off (GemmArgs::act_ready, decode with expert-indexed tiles): each
+// gate/up tile publishes itself on its expert's counter once its rows are
+// stored, and the down GEMM, launched without waiting for the gate/up grid,
+// waits per tile for its expert's count before gathering the activation
+// rows; down CTAs thus start on the SMs that gate/up frees first.
+//
 // Roles: warp 0 TMA producer (gather4 of the sub-block's real rows, lane 0
 // the weight tile(s)); warp 1 TMEM allocation and MMA issuer; warps 2-5
 // epilogue (warp 4, which owns TMEM lanes 0-31, stores; the others only
