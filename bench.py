@@ -1,12 +1,18 @@
 """Benchmark of the sparse MoE FFN layer (one step = one whole moe_forward:
-routing, grouping, grouped gate/up + SiLU, grouped down + weight, combine).
+routing, grouping, grouped gate/up + SiLU, grouped down + weight, combine),
+with the model's bf16 weights.
 
     python bench.py [--config decode] [--steps K] [--warmup W] [--gpus N]
     python bench.py --impl reference ...     # the fp64 CPU oracle, timed
 
 Prints ONE JSON line (rank 0).  Under torchrun every rank runs an independent
 replica of the same per-GPU workload (the layer has no cross-GPU step), and
-the value is the tokens of all ranks over the slowest rank's time.
+the value is the tokens of all ranks over the slowest rank's time; with
+--gpus N > 1 and no torchrun environment, bench.py starts the N ranks itself
+through torch.distributed.run.  The decode line also carries a "prefill"
+record: the prefill workload timed in the same run (its grouped GEMMs are
+the tensor-bound half of the metric), through moe_forward and through
+moe_forward_prepared (fp16 down weights made once at load).
 """
 from __future__ import annotations
 
@@ -245,6 +251,78 @@ def time_oracle(shape, bits, target_s: float):
 
 # ----------------------------------------------------------------- our arm
 
+def time_prefill(args, device, peaks):
+    """The prefill workload (N=8192) timed on this GPU through both forms of
+    the down weights: layer ms per call, and the grouped GEMMs (gate/up and
+    down, from the start of gate/up to the end of down, with no event
+    between them so that their hand-off overlap is kept) against the bf16
+    tensor peak."""
+    from sparse_moe_ffn_gb300 import binding
+
+    shape = CONFIGS["prefill"]
+    cpu = make_inputs(shape, seed=args.seed)
+    d_bf16 = to_device(cpu, device)
+    del cpu
+    ws = binding.alloc_workspace(shape.N, shape.H, shape.E, shape.I, shape.k, shape.I_s, device)
+    out = torch.empty((shape.N, shape.H), dtype=torch.bfloat16, device=device)
+    steps, warm = args.prefill_steps, 5
+    _, sflops, layer_flops, _ = algorithmic_work(shape, shape.E)
+    gemm_flops = sflops["gate_up"] + sflops["down"]
+    rec = {"workload": WORKLOADS["prefill"], "steps": steps, "warmup": warm}
+    for form, d in (("bf16_down", d_bf16), ("f16_down_prepared", None)):
+        if d is None:
+            d = binding.prepare_weights(d_bf16)
+
+        def step():
+            binding.moe_forward(d["x"], d["router"], d["w_gate"], d["w_up"], d["w_down"],
+                                shape.k, shape.norm_topk_prob, None, out=out, workspace=ws)
+
+        for _ in range(warm):
+            step()
+        torch.cuda.synchronize()
+        check_status(ws, f"prefill warm-up ({form})")
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record()
+        for _ in range(steps):
+            step()
+        s1.record()
+        torch.cuda.synchronize()
+        check_status(ws, f"prefill timed steps ({form})")
+        ms = s0.elapsed_time(s1) / steps
+        # grouped GEMMs: events before gate/up and after down only
+        evs = []
+        for _ in range(steps):
+            e = [None] * (len(STAGES) + 1)
+            e[STAGES.index("gate_up")] = torch.cuda.Event(enable_timing=True)
+            e[STAGES.index("shared")] = torch.cuda.Event(enable_timing=True)
+            evs.append(e)
+            binding.set_stage_events(e)
+            step()
+        binding.set_stage_events(None)
+        torch.cuda.synchronize()
+        gemm_ms = statistics.mean(e[STAGES.index("gate_up")].elapsed_time(e[STAGES.index("shared")])
+                                  for e in evs)
+        achieved = gemm_flops / (gemm_ms / 1e3) / 1e12
+        rec[form] = {
+            "entry": "moe_forward_prepared" if form.startswith("f16") else "moe_forward",
+            "ms_per_step": round(ms, 5), "tokens_per_s": round(shape.N / (ms / 1e3), 1),
+            "tflops": round(layer_flops / (ms / 1e3) / 1e12, 2),
+            "layer_frac_of_bf16_peak": round(layer_flops / (ms / 1e3) / 1e12
+                                             / peaks["bf16_tflops"], 4),
+            "roofline": {"bound": "tensor", "kernel": "gate_up+down", "achieved":
+                         round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": round(achieved / peaks["bf16_tflops"], 4),
+                         "kernel_ms": round(gemm_ms, 5), "algorithmic_per_launch": gemm_flops,
+                         "window": "CUDA events before the gate/up launch and after the down "
+                                   "launch, a separate pass of the same steps"},
+        }
+        if d is not d_bf16:
+            del d
+    del d_bf16, ws, out
+    torch.cuda.empty_cache()
+    return rec
+
+
 def run_ours(args, world, rank, local):
     from sparse_moe_ffn_gb300 import binding
 
@@ -252,8 +330,9 @@ def run_ours(args, world, rank, local):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     cpu = make_inputs(shape, seed=args.seed)
-    # model load: weights to the device, down projections converted to fp16 once
-    d = binding.prepare_weights(to_device(cpu, device))
+    # model load: the model's bf16 weights to the device (moe_forward takes
+    # them as they are)
+    d = to_device(cpu, device)
     shared = {n: d[n] for n in binding.SHARED_KEYS} if shape.I_s else None
     ws = binding.alloc_workspace(shape.N, shape.H, shape.E, shape.I, shape.k, shape.I_s, device)
     out = torch.empty((shape.N, shape.H), dtype=torch.bfloat16, device=device)
@@ -369,6 +448,55 @@ def run_ours(args, world, rank, local):
            "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
            "d2h_bytes_per_step": out_host.numel() * out_host.element_size()}
 
+    # the same steps through moe_forward_prepared (fp16 down weights made
+    # once at load; information next to the bf16 headline)
+    d16 = binding.prepare_weights(d)
+    shared16 = {n: d16[n] for n in binding.SHARED_KEYS} if shape.I_s else None
+    for _ in range(args.warmup):
+        binding.moe_forward(d16["x"], d16["router"], d16["w_gate"], d16["w_up"], d16["w_down"],
+                            shape.k, shape.norm_topk_prob, shared16, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record()
+    for _ in range(args.steps):
+        binding.moe_forward(d16["x"], d16["router"], d16["w_gate"], d16["w_up"], d16["w_down"],
+                            shape.k, shape.norm_topk_prob, shared16, out=out, workspace=ws)
+    p1.record()
+    torch.cuda.synchronize()
+    check_status(ws, "prepared-weight steps")
+    prep_ms = p0.elapsed_time(p1) / args.steps
+    prepared_rec = {"entry": "moe_forward_prepared", "ms_per_step": round(prep_ms, 5),
+                    "tokens_per_s": round(shape.N / (prep_ms / 1e3), 1)}
+    del d16, shared16
+
+    # the decode loop under CUDA-graph replay (buckets 1, 2, 4, ... 128; this
+    # workload's batch replays its own bucket), the step's activations copied
+    # into the captured input each step
+    graph_rec = None
+    if shape.N <= binding.DECODE_BUCKETS[-1]:
+        graphs = binding.ForwardGraphSet({n: t for n, t in d.items() if n != "x"}, shape.k,
+                                         shape.norm_topk_prob)
+        for _ in range(args.warmup):
+            graphs(d["x"])
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record()
+        for _ in range(args.steps):
+            graphs(d["x"])
+        g1.record()
+        torch.cuda.synchronize()
+        if graphs.read_device_status() != 0:
+            raise RuntimeError("device status after the graph-replay steps")
+        gms = g0.elapsed_time(g1) / args.steps
+        graph_rec = {"us_per_step": round(gms * 1e3, 2),
+                     "tokens_per_s": round(shape.N / (gms / 1e3), 1),
+                     "bucket": graphs.bucket_of(shape.N), "buckets": list(graphs.buckets)}
+        del graphs
+
+    prefill_rec = None
+    if rank == 0 and args.config == "decode" and not args.no_prefill:
+        prefill_rec = time_prefill(args, device, peaks)
+
     cpu_base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tps, threads, rows, el = time_oracle(shape, oracle_bits(cpu), args.cpu_seconds)
@@ -391,6 +519,9 @@ def run_ours(args, world, rank, local):
                          "inputs smaller than L2 (not flushed: latency-bound case)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "tflops": round(tflops, 2),
+        "entry": "moe_forward (bf16 weights, as the layer is defined)",
+        "prepared_down_weights": prepared_rec,
+        "graph_replay": graph_rec,
         "stage_ms_warmup_probe": {s: round(v, 5) for s, v in probe_ms.items()},
         "experts_touched": touched,
         "roofline": roof,
@@ -399,6 +530,8 @@ def run_ours(args, world, rank, local):
         "gpu_launches": launches,
         "clocks": clocks,
     }
+    if prefill_rec is not None:
+        line["prefill"] = prefill_rec
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -446,6 +579,19 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def spawn_ranks(n: int) -> int:
+    """Runs this script under torch.distributed.run with n local ranks (the
+    same arguments), and returns its exit code."""
+    import socket
+    with socket.socket() as sock:
+        sock.bind(("127.0.0.1", 0))
+        port = sock.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={n}", "--master-addr=127.0.0.1", f"--master-port={port}",
+           os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.call(cmd)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -456,9 +602,18 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill-steps", type=int, default=50)
+    ap.add_argument("--no-prefill", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # start the N ranks (one process per GPU) ourselves
+        sys.exit(spawn_ranks(args.gpus))
+    if args.gpus != int(os.environ.get("WORLD_SIZE", "1")):
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={os.environ.get('WORLD_SIZE', '1')}")
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, world, rank)

@@ -26,12 +26,16 @@
  *     IEEE bfloat16 bit pattern), fp16 data as moe_f16_t (IEEE binary16).
  *     Pointers to bf16 / fp16 matrices must be 16-byte aligned; H and I must
  *     be multiples of 8 (16-byte rows for TMA).
- *   - Down-projection weights (w_down, shared_down_proj) are taken in fp16,
- *     made once from the model's bf16 weights by moe_convert_bf16_to_f16:
+ *   - Every weight is taken in the model's bf16, as the pages define the
+ *     layer.  Each entry point that takes down-projection weights also has a
+ *     *_prepared twin taking an fp16 copy of them instead (w_down_f16,
+ *     shared_down_proj_f16), made once at load by moe_convert_bf16_to_f16:
  *     every bf16 value of magnitude 2^-14 or more converts exactly (fp16 has
  *     more significand bits), smaller ones round to fp16's subnormal grid
- *     (absolute error <= 2^-25).  The down GEMM then multiplies the fp16
- *     activation by them on the fp16 tensor-core path.
+ *     (absolute error <= 2^-25).  With bf16 down weights the gate/up
+ *     activation is kept as a bf16 pair hi + lo and the down GEMM issues two
+ *     MMAs per K step; with the fp16 copy it is kept in fp16 and one MMA per
+ *     K step suffices, which halves the down GEMM's tensor work.
  *   - The caller owns every buffer, including the workspace.  The library
  *     never allocates, frees or synchronises (except moe_read_device_status),
  *     and keeps no state between calls: calls on different streams with
@@ -154,11 +158,14 @@ moe_status_t moe_align(const int32_t *topk_ids, int64_t N, int k, int E,
  * exceed it return MOE_ERR_UNSUPPORTED (for E = 128 that is above ~4M pairs).
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current): make that first call
- * before any stream capture.  Every call shares the array, so calls whose
- * work overlaps on the GPU (other streams, other host threads) race; the
- * array needs no clearing between calls.  device_status (nullable, int32 on
- * the device) receives the call's status word (MOE_ERR_DEVICE_CHECK for an
- * id outside [0, E)) by an asynchronous copy on `stream`.
+ * before any stream capture.  The address is kept per device and CUDA
+ * context; a call made under a new context (after cudaDeviceReset, say)
+ * looks it up again, so that call too belongs before any capture.  Every
+ * call shares the array, so calls whose work overlaps on the GPU (other
+ * streams, other host threads) race; the array needs no clearing between
+ * calls.  device_status (nullable, int32 on the device) receives the call's
+ * status word (MOE_ERR_DEVICE_CHECK for an id outside [0, E); 0 for N = 0)
+ * by an asynchronous copy or memset on `stream`.
  * Arguments and outputs are those of moe_align.  Allocates nothing.
  * ---------------------------------------------------------------------- */
 #define MOE_ALIGN_NOALLOC_SCRATCH_BYTES (1u << 20)
@@ -176,51 +183,76 @@ moe_status_t moe_align_noalloc(const int32_t *topk_ids, int64_t N, int k, int E,
  *   x                 [N, H] bf16
  *   router            [E, H] bf16
  *   w_gate, w_up      [E, I, H] bf16
- *   w_down            [E, H, I] fp16 (moe_convert_bf16_to_f16 of the bf16 weights)
+ *   w_down            [E, H, I] bf16
  *   shared_gate_proj  [I_s, H] bf16 \
  *   shared_up_proj    [I_s, H] bf16  | all four NULL: no shared expert
- *   shared_down_proj  [H, I_s] fp16  | (I_s ignored); all four set: shared
+ *   shared_down_proj  [H, I_s] bf16  | (I_s ignored); all four set: shared
  *   shared_gate       [1, H]   bf16 /  expert with I_s >= 8, I_s % 8 == 0
  *   out               [N, H] bf16 out (may not alias any input)
  *   workspace         >= moe_forward_workspace_bytes(...) bytes, 256-byte
  *                     aligned; holds the routing, grouping and intermediate
  *                     activations (layout: moe_forward_layout)
  * Precision: bf16 inputs, fp32 routing and accumulation; the gate/up
- * activation a = silu(g)*u is stored in fp16 (11 significant bits against
- * bf16's 8) and multiplied by the fp16 down weights; each pair's weighted
- * down projection (and the gated shared expert) is stored in fp16 (same
- * bytes as bf16, 8x finer rounding); the k contributions and the shared
+ * activation a = silu(g)*u is kept as the bf16 pair hi = bf16(a),
+ * lo = bf16(a - hi) (16 significant bits) and both halves are multiplied by
+ * the bf16 down weights; each pair's weighted down projection (and the
+ * gated shared expert) is kept in fp32; the k contributions and the shared
  * term are summed in fp32 in slot order, and out is rounded to bf16 once.
- * An activation or pair output beyond the fp16 range (65504) records
- * MOE_ERR_DEVICE_CHECK.  The result does
- * not depend on the other tokens of the batch and is bitwise reproducible.
- * Limits: as moe_route, plus I % 8 == 0, N*k + E*128 < 2^31.
+ * A non-finite activation or pair output records MOE_ERR_DEVICE_CHECK.
+ * The result does not depend on the other tokens of the batch and is
+ * bitwise reproducible.
+ * Limits: as moe_route, plus I % 8 == 0, N*k + E*128 < 2^30.
  * ---------------------------------------------------------------------- */
 size_t moe_forward_workspace_bytes(int64_t N, int H, int E, int I, int k, int I_s);
 moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router,
                          const moe_bf16_t *w_gate, const moe_bf16_t *w_up,
-                         const moe_f16_t *w_down,
+                         const moe_bf16_t *w_down,
                          const moe_bf16_t *shared_gate_proj,
                          const moe_bf16_t *shared_up_proj,
-                         const moe_f16_t *shared_down_proj,
+                         const moe_bf16_t *shared_down_proj,
                          const moe_bf16_t *shared_gate, int64_t N, int H, int E,
                          int I, int I_s, int k, int norm_topk_prob,
                          moe_bf16_t *out, void *workspace,
                          size_t workspace_bytes, cudaStream_t stream);
 
 /* -------------------------------------------------------------------------
+ * moe_forward_prepared -- moe_forward with the down projections given as the
+ * fp16 copies moe_convert_bf16_to_f16 makes once at load (w_down_f16
+ * [E, H, I], shared_down_proj_f16 [H, I_s]; a load-time preparation the pages
+ * do not have).  The activation is then kept in fp16 (11 significant bits)
+ * and multiplied by the fp16 weights with one MMA per K step instead of two,
+ * which halves the down GEMM's tensor work at large N.  Everything else --
+ * arguments, workspace, routing, fp32 pair outputs, slot-order fp32 combine,
+ * limits, errors -- is moe_forward's.  The outputs differ from moe_forward's
+ * by the activation's rounding (both stay within the layer's tolerance).
+ * ---------------------------------------------------------------------- */
+moe_status_t moe_forward_prepared(const moe_bf16_t *x, const moe_bf16_t *router,
+                                  const moe_bf16_t *w_gate, const moe_bf16_t *w_up,
+                                  const moe_f16_t *w_down_f16,
+                                  const moe_bf16_t *shared_gate_proj,
+                                  const moe_bf16_t *shared_up_proj,
+                                  const moe_f16_t *shared_down_proj_f16,
+                                  const moe_bf16_t *shared_gate, int64_t N, int H,
+                                  int E, int I, int I_s, int k, int norm_topk_prob,
+                                  moe_bf16_t *out, void *workspace,
+                                  size_t workspace_bytes, cudaStream_t stream);
+
+/* -------------------------------------------------------------------------
  * moe_experts -- the per-expert half of the layer for rows whose expert and
  * weight are already chosen: the receiving side of expert-parallel dispatch
  * (M03 drill, level-3 follow-up on splitting experts across devices: the
  * (token, expert) table drives an all-to-all).  For every row r:
- *   y[r] = fp16(weights[r] * Expert_{ids[r]}(x_rows[r]))
+ *   y[r] = weights[r] * Expert_{ids[r]}(x_rows[r])   (fp32)
  * with the arithmetic of moe_forward's per-pair outputs (grouping by expert,
- * gate/up with the fp16 activation, down), so the bits equal the pair rows
- * moe_forward produces for the same (row, expert, weight).
+ * gate/up with the hi/lo activation, down), so the bits equal the pair rows
+ * moe_forward produces for the same (row, expert, weight);
+ * moe_experts_prepared does the same with fp16 down weights and equals
+ * moe_forward_prepared's pair rows.
  *   x_rows   [R, H] bf16      ids [R] int32 in [0, E)      weights [R] fp32
- *   w_gate, w_up [E, I, H] bf16, w_down [E, H, I] fp16: the experts this
- *            call serves (a rank's slice of the layer's experts)
- *   y        [R, H] fp16 out
+ *   w_gate, w_up [E, I, H] bf16, w_down [E, H, I] bf16 (w_down_f16: fp16):
+ *            the experts this call serves (a rank's slice of the layer's
+ *            experts)
+ *   y        [R, H] fp32 out
  *   workspace >= moe_experts_workspace_bytes(R, H, E, I) bytes, 256-byte
  *            aligned; its first 4 bytes are the status word
  *            (moe_read_device_status)
@@ -231,23 +263,29 @@ size_t moe_experts_workspace_bytes(int64_t R, int H, int E, int I);
 moe_status_t moe_experts(const moe_bf16_t *x_rows, const int32_t *ids,
                          const float *weights, int64_t R, int H, int E, int I,
                          const moe_bf16_t *w_gate, const moe_bf16_t *w_up,
-                         const moe_f16_t *w_down, moe_f16_t *y, void *workspace,
+                         const moe_bf16_t *w_down, float *y, void *workspace,
                          size_t workspace_bytes, cudaStream_t stream);
+moe_status_t moe_experts_prepared(const moe_bf16_t *x_rows, const int32_t *ids,
+                                  const float *weights, int64_t R, int H, int E,
+                                  int I, const moe_bf16_t *w_gate,
+                                  const moe_bf16_t *w_up, const moe_f16_t *w_down_f16,
+                                  float *y, void *workspace, size_t workspace_bytes,
+                                  cudaStream_t stream);
 
 /* -------------------------------------------------------------------------
  * moe_combine -- the weighted accumulation of the layer (M03 drill: each
  * token's outputs summed back, index_add_ in the pages' PyTorch form), done
  * without atomics: out[n] = bf16(sum_{j<k} ypair[n*k + j] (+ yshared[n])),
- * summed in fp32 in slot order.  ypair [N*k, H] fp16, yshared [N, H] fp16 or
+ * summed in fp32 in slot order.  ypair [N*k, H] fp32, yshared [N, H] fp32 or
  * NULL, out [N, H] bf16; 16-byte aligned.  moe_forward ends with the same
  * kernel.
  * ---------------------------------------------------------------------- */
-moe_status_t moe_combine(const moe_f16_t *ypair, const moe_f16_t *yshared, int64_t N, int H,
-                         int k, moe_bf16_t *out, cudaStream_t stream);
+moe_status_t moe_combine(const float *ypair, const float *yshared, int64_t N, int H, int k,
+                         moe_bf16_t *out, cudaStream_t stream);
 
 /* -------------------------------------------------------------------------
  * moe_convert_bf16_to_f16 -- the load-time step that makes the fp16 down
- * weights every entry point takes: dst[i] = fp16(src[i]) for i < n, round to
+ * weights the *_prepared entry points take: dst[i] = fp16(src[i]) for i < n, round to
  * nearest even (exact for |src| >= 2^-14 and for zero; below, the nearest
  * fp16 subnormal).  src, dst: device, 16-byte aligned, not overlapping.
  * device_status (nullable, int32 on the device) is set to
@@ -277,14 +315,24 @@ moe_status_t moe_convert_bf16_to_f16(const moe_bf16_t *src, moe_f16_t *dst, int6
 moe_status_t moe_forward_host(const moe_bf16_t *x_host, moe_bf16_t *out_host,
                               moe_bf16_t *x_dev, moe_bf16_t *out_dev,
                               const moe_bf16_t *router, const moe_bf16_t *w_gate,
-                              const moe_bf16_t *w_up, const moe_f16_t *w_down,
+                              const moe_bf16_t *w_up, const moe_bf16_t *w_down,
                               const moe_bf16_t *shared_gate_proj,
                               const moe_bf16_t *shared_up_proj,
-                              const moe_f16_t *shared_down_proj,
+                              const moe_bf16_t *shared_down_proj,
                               const moe_bf16_t *shared_gate, int64_t N, int H, int E,
                               int I, int I_s, int k, int norm_topk_prob,
                               void *workspace, size_t workspace_bytes,
                               cudaStream_t stream);
+/* moe_forward_host with fp16 down weights: the layer step is
+ * moe_forward_prepared. */
+moe_status_t moe_forward_host_prepared(
+    const moe_bf16_t *x_host, moe_bf16_t *out_host, moe_bf16_t *x_dev,
+    moe_bf16_t *out_dev, const moe_bf16_t *router, const moe_bf16_t *w_gate,
+    const moe_bf16_t *w_up, const moe_f16_t *w_down_f16,
+    const moe_bf16_t *shared_gate_proj, const moe_bf16_t *shared_up_proj,
+    const moe_f16_t *shared_down_proj_f16, const moe_bf16_t *shared_gate, int64_t N,
+    int H, int E, int I, int I_s, int k, int norm_topk_prob, void *workspace,
+    size_t workspace_bytes, cudaStream_t stream);
 
 /* -------------------------------------------------------------------------
  * moe_add_rmsnorm -- the decoder layer's step that feeds the MoE, in one
@@ -311,16 +359,23 @@ moe_status_t moe_add_rmsnorm(const moe_bf16_t *x, moe_bf16_t *residual,
  * Qwen3.5 walkthrough): out = (silu(x Wg^T) * (x Wu^T)) Wd^T, the layer with
  * E = k = 1, run on the same grouped GEMM kernels as one dense group.
  *
- *   x [N, H], w_gate / w_up [I, H], out [N, H]: bf16; w_down [H, I]: fp16
+ *   x [N, H], w_gate / w_up [I, H], w_down [H, I], out [N, H]: bf16
+ *   (moe_dense_mlp_prepared: w_down_f16 [H, I] fp16)
  *   workspace >= moe_dense_mlp_workspace_bytes(N, H, I), 256-byte aligned
- * Precision as moe_forward.  Limits: H % 8 == 0, I % 8 == 0.
+ * Precision as moe_forward (moe_forward_prepared).  Limits: H % 8 == 0,
+ * I % 8 == 0, N < 2^30.
  * ---------------------------------------------------------------------- */
 size_t moe_dense_mlp_workspace_bytes(int64_t N, int H, int I);
 moe_status_t moe_dense_mlp(const moe_bf16_t *x, const moe_bf16_t *w_gate,
-                           const moe_bf16_t *w_up, const moe_f16_t *w_down,
+                           const moe_bf16_t *w_up, const moe_bf16_t *w_down,
                            int64_t N, int H, int I, moe_bf16_t *out,
                            void *workspace, size_t workspace_bytes,
                            cudaStream_t stream);
+moe_status_t moe_dense_mlp_prepared(const moe_bf16_t *x, const moe_bf16_t *w_gate,
+                                    const moe_bf16_t *w_up, const moe_f16_t *w_down_f16,
+                                    int64_t N, int H, int I, moe_bf16_t *out,
+                                    void *workspace, size_t workspace_bytes,
+                                    cudaStream_t stream);
 
 /* Byte offsets of moe_forward's workspace sub-buffers (for inspecting the
  * intermediate results; every offset is 256-byte aligned). */
@@ -338,10 +393,13 @@ typedef struct {
     size_t block_expert;  /* int32 [capacity / 128]                           */
     size_t ready;         /* int32 [max(E, capacity/128)] GEMM hand-off counts */
     size_t x_sorted;      /* bf16 [capacity, H]   x rows in expert order (dense blocks) */
-    size_t act;           /* fp16 [capacity, I]   a = silu(x Wg^T) * (x Wu^T)  */
-    size_t ypair;         /* fp16 [N*k, H]        w * Expert(x), per pair     */
-    size_t act_shared;    /* fp16 [round_up(N,128), I_s] (shared only)        */
-    size_t y_shared;      /* fp16 [N, H]  gamma * SharedMLP(x) (shared only)  */
+    size_t act;           /* a = silu(x Wg^T) * (x Wu^T): bf16 hi [capacity, I]
+                             then bf16 lo [capacity, I] (moe_forward), or fp16
+                             [capacity, I] (moe_forward_prepared)           */
+    size_t ypair;         /* fp32 [N*k, H]        w * Expert(x), per pair     */
+    size_t act_shared;    /* as act, rows round_up(N,128), I_s columns
+                             (shared only)                                    */
+    size_t y_shared;      /* fp32 [N, H]  gamma * SharedMLP(x) (shared only)  */
     size_t total;         /* = moe_forward_workspace_bytes                    */
     int64_t capacity;     /* moe_align_capacity(N, k, E, 128)                 */
 } moe_forward_layout_t;

@@ -2,6 +2,11 @@
 include/moe.h.  Argument marshalling only: torch tensors supply device
 pointers and the current stream; every step of the layer runs in the
 library's CUDA kernels.  There is no fallback: a missing library raises.
+
+Down-projection weights may be the model's bf16 tensors or the fp16 copies
+``prepare_weights`` makes once at load; the wrappers pick the library entry
+point that takes that form (``moe_forward`` or ``moe_forward_prepared``, and
+likewise for the host, experts and dense-MLP calls).
 """
 from __future__ import annotations
 
@@ -54,9 +59,13 @@ def lib():
         "moe_align": ([P, i64, i32, i32, i32, P, P, P, P, P, P, sz, P], i32),
         "moe_forward_workspace_bytes": ([i64, i32, i32, i32, i32, i32], sz),
         "moe_forward": ([P] * 9 + [i64, i32, i32, i32, i32, i32, i32, P, P, sz, P], i32),
+        "moe_forward_prepared": ([P] * 9 + [i64, i32, i32, i32, i32, i32, i32, P, P, sz, P], i32),
         "moe_forward_host": ([P] * 12 + [i64, i32, i32, i32, i32, i32, i32, P, sz, P], i32),
+        "moe_forward_host_prepared": ([P] * 12 + [i64, i32, i32, i32, i32, i32, i32, P, sz, P],
+                                      i32),
         "moe_experts_workspace_bytes": ([i64, i32, i32, i32], sz),
         "moe_experts": ([P, P, P, i64, i32, i32, i32, P, P, P, P, P, sz, P], i32),
+        "moe_experts_prepared": ([P, P, P, i64, i32, i32, i32, P, P, P, P, P, sz, P], i32),
         "moe_combine": ([P, P, i64, i32, i32, P, P], i32),
         "moe_convert_bf16_to_f16": ([P, P, i64, P, P], i32),
         "moe_forward_layout": ([i64, i32, i32, i32, i32, i32, ctypes.POINTER(_Layout)], i32),
@@ -68,6 +77,7 @@ def lib():
         "moe_dense_mlp_workspace_bytes": ([i64, i32, i32], sz),
         "moe_add_rmsnorm": ([P, P, P, i64, i32, ctypes.c_float, i32, P, P], i32),
         "moe_dense_mlp": ([P, P, P, P, i64, i32, i32, P, P, sz, P], i32),
+        "moe_dense_mlp_prepared": ([P, P, P, P, i64, i32, i32, P, P, sz, P], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -108,6 +118,17 @@ def _f16(t, name, shape=None):
     if shape is not None and tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
     return t
+
+
+def _down(t, name, shape=None) -> bool:
+    """Checks a down-projection weight; True if it is the prepared fp16 copy."""
+    if t.dtype == torch.float16:
+        _f16(t, name, shape)
+        return True
+    if t.dtype != torch.bfloat16:
+        raise ValueError(f"{name} must be bf16 (or its fp16 copy from prepare_weights)")
+    _bf16(t, name, shape)
+    return False
 
 
 def moe_status_string(status: int) -> str:
@@ -209,16 +230,17 @@ def alloc_workspace(N, H, E, I, k, I_s=0, device="cuda"):
 def moe_forward(x, router, w_gate, w_up, w_down, k: int, norm_topk_prob: bool = True,
                 shared=None, out=None, workspace=None):
     """The whole layer.  ``shared`` is None or a dict with shared_gate_proj,
-    shared_up_proj, shared_down_proj and shared_gate.  w_down and
-    shared_down_proj are fp16 (``prepare_weights``), every other tensor bf16.
-    Returns out [N, H] bf16."""
+    shared_up_proj, shared_down_proj and shared_gate.  Every tensor is bf16,
+    except that w_down and shared_down_proj may instead be the fp16 copies
+    from ``prepare_weights`` (then moe_forward_prepared runs).  Returns out
+    [N, H] bf16."""
     N, H = x.shape
     E, I, _ = w_gate.shape
     _bf16(x, "x")
     _bf16(router, "router", (E, H))
     _bf16(w_gate, "w_gate", (E, I, H))
     _bf16(w_up, "w_up", (E, I, H))
-    _f16(w_down, "w_down", (E, H, I))
+    prepared = _down(w_down, "w_down", (E, H, I))
     sp = [None] * 4
     I_s = 0
     if shared is not None:
@@ -226,17 +248,19 @@ def moe_forward(x, router, w_gate, w_up, w_down, k: int, norm_topk_prob: bool = 
         I_s = sp[0].shape[0]
         _bf16(sp[0], "shared_gate_proj", (I_s, H))
         _bf16(sp[1], "shared_up_proj", (I_s, H))
-        _f16(sp[2], "shared_down_proj", (H, I_s))
+        if _down(sp[2], "shared_down_proj", (H, I_s)) != prepared:
+            raise ValueError("w_down and shared_down_proj must both be bf16 or both fp16")
         _bf16(sp[3], "shared_gate", (1, H))
     if out is None:
         out = torch.empty((N, H), dtype=torch.bfloat16, device=x.device)
     _bf16(out, "out", (N, H))
     if workspace is None:
         workspace = alloc_workspace(N, H, E, I, k, I_s, x.device)
-    _check(lib().moe_forward(_ptr(x), _ptr(router), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
-                             *[_ptr(t) for t in sp], N, H, E, I, I_s, k,
-                             int(bool(norm_topk_prob)), _ptr(out), _ptr(workspace),
-                             workspace.numel(), _stream()), "moe_forward")
+    fn = lib().moe_forward_prepared if prepared else lib().moe_forward
+    _check(fn(_ptr(x), _ptr(router), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
+              *[_ptr(t) for t in sp], N, H, E, I, I_s, k, int(bool(norm_topk_prob)), _ptr(out),
+              _ptr(workspace), workspace.numel(), _stream()),
+           "moe_forward_prepared" if prepared else "moe_forward")
     return out
 
 
@@ -255,13 +279,14 @@ def moe_add_rmsnorm(x, residual, weight, eps: float = 1e-6, gemma: bool = False,
 
 
 def moe_dense_mlp(x, w_gate, w_up, w_down, out=None, workspace=None):
-    """Dense SwiGLU MLP (silu(x Wg^T) * (x Wu^T)) Wd^T on the grouped GEMM kernels."""
+    """Dense SwiGLU MLP (silu(x Wg^T) * (x Wu^T)) Wd^T on the grouped GEMM
+    kernels; w_down bf16 (moe_dense_mlp) or its fp16 copy (_prepared)."""
     N, H = x.shape
     I = w_gate.shape[0]
     _bf16(x, "x")
     _bf16(w_gate, "w_gate", (I, H))
     _bf16(w_up, "w_up", (I, H))
-    _f16(w_down, "w_down", (H, I))
+    prepared = _down(w_down, "w_down", (H, I))
     if out is None:
         out = torch.empty((N, H), dtype=torch.bfloat16, device=x.device)
     _bf16(out, "out", (N, H))
@@ -269,45 +294,49 @@ def moe_dense_mlp(x, w_gate, w_up, w_down, out=None, workspace=None):
     if workspace is None:
         workspace = torch.empty(max(int(L.moe_dense_mlp_workspace_bytes(N, H, I)), 256),
                                 dtype=torch.uint8, device=x.device)
-    _check(L.moe_dense_mlp(_ptr(x), _ptr(w_gate), _ptr(w_up), _ptr(w_down), N, H, I, _ptr(out),
-                           _ptr(workspace), workspace.numel(), _stream()), "moe_dense_mlp")
+    fn = L.moe_dense_mlp_prepared if prepared else L.moe_dense_mlp
+    _check(fn(_ptr(x), _ptr(w_gate), _ptr(w_up), _ptr(w_down), N, H, I, _ptr(out),
+              _ptr(workspace), workspace.numel(), _stream()), "moe_dense_mlp")
     return out
 
 
 def moe_experts(x_rows, ids, weights, w_gate, w_up, w_down, y=None, workspace=None):
-    """Per-row expert outputs y[r] = fp16(weights[r] * Expert_{ids[r]}(x_rows[r]))
-    ([R, H] fp16): the receiving side of expert-parallel dispatch."""
+    """Per-row expert outputs y[r] = weights[r] * Expert_{ids[r]}(x_rows[r])
+    ([R, H] fp32): the receiving side of expert-parallel dispatch.  w_down
+    bf16 (moe_experts) or its fp16 copy (moe_experts_prepared)."""
     R, H = x_rows.shape
     E, I, _ = w_gate.shape
     _bf16(x_rows, "x_rows")
     _bf16(w_gate, "w_gate", (E, I, H))
     _bf16(w_up, "w_up", (E, I, H))
-    _f16(w_down, "w_down", (E, H, I))
+    prepared = _down(w_down, "w_down", (E, H, I))
     if ids.dtype != torch.int32 or not ids.is_cuda or tuple(ids.shape) != (R,):
         raise ValueError("ids must be a CUDA int32 tensor of shape [R]")
     if weights.dtype != torch.float32 or not weights.is_cuda or tuple(weights.shape) != (R,):
         raise ValueError("weights must be a CUDA float32 tensor of shape [R]")
     ids, weights = ids.contiguous(), weights.contiguous()
     if y is None:
-        y = torch.empty((R, H), dtype=torch.float16, device=x_rows.device)
-    if y.dtype != torch.float16 or tuple(y.shape) != (R, H) or not y.is_contiguous():
-        raise ValueError("y must be a contiguous float16 tensor of shape [R, H]")
+        y = torch.empty((R, H), dtype=torch.float32, device=x_rows.device)
+    if y.dtype != torch.float32 or tuple(y.shape) != (R, H) or not y.is_contiguous():
+        raise ValueError("y must be a contiguous float32 tensor of shape [R, H]")
     if workspace is None:
         workspace = torch.empty(max(lib().moe_experts_workspace_bytes(R, H, E, I), 256),
                                 dtype=torch.uint8, device=x_rows.device)
-    _check(lib().moe_experts(_ptr(x_rows), _ptr(ids), _ptr(weights), R, H, E, I, _ptr(w_gate),
-                             _ptr(w_up), _ptr(w_down), _ptr(y), _ptr(workspace),
-                             workspace.numel(), _stream()), "moe_experts")
+    fn = lib().moe_experts_prepared if prepared else lib().moe_experts
+    _check(fn(_ptr(x_rows), _ptr(ids), _ptr(weights), R, H, E, I, _ptr(w_gate), _ptr(w_up),
+              _ptr(w_down), _ptr(y), _ptr(workspace), workspace.numel(), _stream()),
+           "moe_experts")
     return y, workspace
 
 
 def moe_combine(ypair, N: int, k: int, yshared=None, out=None):
     """out[n] = bf16(sum_j ypair[n*k + j] (+ yshared[n])) in fp32, slot order."""
     H = ypair.shape[1]
-    if ypair.dtype != torch.float16 or tuple(ypair.shape) != (N * k, H) or not ypair.is_contiguous():
-        raise ValueError("ypair must be a contiguous float16 tensor of shape [N*k, H]")
-    if yshared is not None and (yshared.dtype != torch.float16 or tuple(yshared.shape) != (N, H)):
-        raise ValueError("yshared must be float16 of shape [N, H]")
+    if ypair.dtype != torch.float32 or tuple(ypair.shape) != (N * k, H) or not ypair.is_contiguous():
+        raise ValueError("ypair must be a contiguous float32 tensor of shape [N*k, H]")
+    if yshared is not None and (yshared.dtype != torch.float32 or tuple(yshared.shape) != (N, H)
+                                or not yshared.is_contiguous()):
+        raise ValueError("yshared must be a contiguous float32 tensor of shape [N, H]")
     if out is None:
         out = torch.empty((N, H), dtype=torch.bfloat16, device=ypair.device)
     _bf16(out, "out", (N, H))
@@ -334,10 +363,10 @@ DOWN_KEYS = ("w_down", "shared_down_proj")
 
 
 def prepare_weights(weights: dict) -> dict:
-    """The layer's weights in the form every entry point takes: the same dict
-    with the down projections (w_down, shared_down_proj) converted to fp16
-    once; bf16 entries pass through.  Raises if a down weight is outside
-    fp16's range."""
+    """The layer's weights in the form the *_prepared entry points take: the
+    same dict with the down projections (w_down, shared_down_proj) converted
+    to fp16 once; bf16 entries pass through.  Raises if a down weight is
+    outside fp16's range."""
     out = dict(weights)
     dev = next(t.device for t in weights.values() if torch.is_tensor(t))
     status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -366,18 +395,18 @@ def moe_forward_from_host(x_host, out_host, x_dev, out_dev, weights: dict, k: in
         raise ValueError("x_host and out_host must be contiguous [N, H]")
     _bf16(x_dev, "x_dev", (N, H))
     _bf16(out_dev, "out_dev", (N, H))
-    _f16(weights["w_down"], "w_down", (E, H, I))
+    prepared = _down(weights["w_down"], "w_down", (E, H, I))
     shared = "shared_gate" in weights
-    if shared:
-        _f16(weights["shared_down_proj"], "shared_down_proj")
+    if shared and _down(weights["shared_down_proj"], "shared_down_proj") != prepared:
+        raise ValueError("w_down and shared_down_proj must both be bf16 or both fp16")
     sp = [weights[n] if shared else None for n in SHARED_KEYS]
     I_s = weights["shared_gate_proj"].shape[0] if shared else 0
-    _check(lib().moe_forward_host(x_host.data_ptr(), out_host.data_ptr(), _ptr(x_dev),
-                                  _ptr(out_dev), _ptr(weights["router"]), _ptr(weights["w_gate"]),
-                                  _ptr(weights["w_up"]), _ptr(weights["w_down"]),
-                                  *[_ptr(t) for t in sp], N, H, E, I, I_s, k,
-                                  int(bool(norm_topk_prob)), _ptr(workspace), workspace.numel(),
-                                  _stream()), "moe_forward_host")
+    fn = lib().moe_forward_host_prepared if prepared else lib().moe_forward_host
+    _check(fn(x_host.data_ptr(), out_host.data_ptr(), _ptr(x_dev), _ptr(out_dev),
+              _ptr(weights["router"]), _ptr(weights["w_gate"]), _ptr(weights["w_up"]),
+              _ptr(weights["w_down"]), *[_ptr(t) for t in sp], N, H, E, I, I_s, k,
+              int(bool(norm_topk_prob)), _ptr(workspace), workspace.numel(), _stream()),
+           "moe_forward_host")
     return out_host
 
 
@@ -426,6 +455,96 @@ class ForwardGraph:
         return self.out[:n]
 
 
+DECODE_BUCKETS = (1, 2, 4, 8, 16, 32, 64, 128)
+
+
+class ForwardGraphSet:
+    """The layer captured once per token bucket (1, 2, 4, ... 128 by default)
+    and replayed for the smallest bucket that holds each step's batch: the
+    decode loop of a serving engine, whose batch size changes from step to
+    step, without per-step launch cost (the Nano-vLLM notes' model runner
+    captures its decode step for a ladder of batch sizes the same way).
+
+    Every bucket's graph reads the first b rows of one static input and
+    writes the first b rows of one static output, and all of them use one
+    workspace sized for the largest bucket: replays on one stream never
+    overlap, and each graph carries its own workspace layout.  A batch of
+    n tokens is copied into the input's first n rows (rows n..b-1 zeroed);
+    since every token's result is independent of the others, the first n
+    output rows equal an eager call on the n tokens bit for bit."""
+
+    def __init__(self, weights: dict, k: int, norm_topk_prob: bool,
+                 buckets=DECODE_BUCKETS):
+        self.buckets = tuple(sorted(set(int(b) for b in buckets)))
+        if not self.buckets or self.buckets[0] < 1:
+            raise ValueError("buckets must be positive token counts")
+        dev = weights["router"].device
+        H = weights["router"].shape[1]
+        E, I, _ = weights["w_gate"].shape
+        self.shared = ({n: weights[n] for n in SHARED_KEYS} if "shared_gate" in weights
+                       else None)
+        I_s = self.shared["shared_gate_proj"].shape[0] if self.shared else 0
+        self.w, self.k, self.norm = weights, k, norm_topk_prob
+        top = self.buckets[-1]
+        self.x = torch.zeros((top, H), dtype=torch.bfloat16, device=dev)
+        self.out = torch.empty((top, H), dtype=torch.bfloat16, device=dev)
+        self.ws = torch.empty(max(max(moe_forward_workspace_bytes(b, H, E, I, k, I_s)
+                                      for b in self.buckets), 256),
+                              dtype=torch.uint8, device=dev)
+        self.graphs = {}
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            for b in self.buckets:  # warm every shape once before capture
+                self._call(b)
+        torch.cuda.current_stream(dev).wait_stream(side)
+        for b in self.buckets:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self._call(b)
+            self.graphs[b] = g
+
+    def _call(self, b):
+        w = self.w
+        moe_forward(self.x[:b], w["router"], w["w_gate"], w["w_up"], w["w_down"], self.k,
+                    self.norm, self.shared, out=self.out[:b], workspace=self.ws)
+
+    def bucket_of(self, n: int) -> int:
+        for b in self.buckets:
+            if b >= n:
+                return b
+        raise ValueError(f"{n} tokens exceed the largest bucket ({self.buckets[-1]})")
+
+    def __call__(self, x):
+        """out[:n] for this step's x [n, H] (a view of the static output,
+        valid until the next call)."""
+        n = x.shape[0]
+        if n == 0:
+            return self.out[:0]
+        b = self.bucket_of(n)
+        self.x[:n].copy_(x)
+        if n < b:
+            self.x[n:b].zero_()
+        self.graphs[b].replay()
+        return self.out[:n]
+
+    def read_device_status(self) -> int:
+        """Status word of the last replay (synchronises the stream)."""
+        return moe_read_device_status(self.ws)
+
+
+def decode_loop(graphs: ForwardGraphSet, steps):
+    """Runs a multi-step decode: for each step's activations x_t [n_t, H]
+    (n_t may change from step to step), the MoE layer by graph replay.
+    Returns the per-step outputs (copies) and raises if a kernel recorded a
+    device-side failure."""
+    outs = [graphs(x).clone() for x in steps]
+    status = graphs.read_device_status()
+    if status != MOE_OK:
+        raise MoEError(status, f"decode loop: {moe_status_string(status)}")
+    return outs
+
+
 def workspace_views(workspace, N, H, E, I, k, I_s=0) -> dict:
     """Typed views of moe_forward's intermediate buffers inside ``workspace``."""
     lay = moe_forward_layout(N, H, E, I, k, I_s)
@@ -451,14 +570,17 @@ def workspace_views(workspace, N, H, E, I, k, I_s=0) -> dict:
         "sorted_pair": view(lay["sorted_pair"], torch.int32, (cap,)),
         "block_expert": view(lay["block_expert"], torch.int32, (cap // MOE_BLOCK_M,)),
         "x_sorted": view(lay["x_sorted"], torch.bfloat16, (cap, H)),
-        "act": view(lay["act"], torch.float16, (cap, I)),
-        "ypair": view(lay["ypair"], torch.float16, (P, H)),
+        # the activation: a bf16 hi/lo pair (bf16 down weights) or fp16
+        # (prepared fp16 down weights), in the same bytes
+        "act_hi": view(lay["act"], torch.bfloat16, (cap, I)),
+        "act_lo": view(lay["act"] + 2 * cap * I, torch.bfloat16, (cap, I)),
+        "act_f16": view(lay["act"], torch.float16, (cap, I)),
+        "ypair": view(lay["ypair"], torch.float32, (P, H)),
     }
     if I_s:
         rows_s = -(-N // MOE_BLOCK_M) * MOE_BLOCK_M
         v["gamma"] = view(lay["gamma"], torch.float32, (N,))
-        v["act_shared"] = view(lay["act_shared"], torch.float16, (rows_s, I_s))
-        v["y_shared"] = view(lay["y_shared"], torch.float16, (N, H))
+        v["y_shared"] = view(lay["y_shared"], torch.float32, (N, H))
     return v
 
 

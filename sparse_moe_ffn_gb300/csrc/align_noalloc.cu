@@ -13,11 +13,16 @@
 // library, held until the process exits.  Host code cannot use the array's
 // name as a device address, so the first call on each device looks the
 // address up with cudaGetSymbolAddress (with that device current) and caches
-// it; that first call should therefore come before any stream capture.  All
+// it; that first call should therefore come before any stream capture.  The
+// cache remembers the CUDA context the address belongs to, and looks it up
+// again when the device's current context has changed (after a
+// cudaDeviceReset the runtime makes a new one).  All
 // calls share the one array: calls whose work overlaps on the GPU (other
 // streams, other host threads) race with each other.  The scratch needs no
 // clearing between calls: moe_align resets the status word and writes every
 // chunk count before reading it.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "kernels.cuh"
@@ -32,19 +37,43 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratch
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 void *g_scratch_address[kMaxDevices] = {nullptr};
+CUcontext g_scratch_context[kMaxDevices] = {nullptr};
 
-// Device address of g_noalloc_scratch on the current device (looked up once).
+// The driver's cuCtxGetCurrent (looked up once through the runtime).
+PFN_cuCtxGetCurrent_v4000 ctx_get_current() {
+    static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    });
+    return fn;
+}
+
+// Device address of g_noalloc_scratch on the current device: looked up once
+// per device and context, with that device current.
 cudaError_t scratch_address(void **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    CUcontext ctx = nullptr;
+    auto get_ctx = ctx_get_current();
+    if (get_ctx && get_ctx(&ctx) != CUDA_SUCCESS) ctx = nullptr;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (g_scratch_address[dev] == nullptr) {
+    if (g_scratch_address[dev] == nullptr || ctx == nullptr || g_scratch_context[dev] != ctx) {
+        // (this also makes the device's primary context current if no
+        // context was yet)
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess) return e;
+        if (get_ctx && get_ctx(&ctx) != CUDA_SUCCESS) ctx = nullptr;
         g_scratch_address[dev] = p;
+        g_scratch_context[dev] = ctx;
     }
     *out = g_scratch_address[dev];
     return cudaSuccess;
@@ -67,7 +96,14 @@ extern "C" moe_status_t moe_align_noalloc(const int32_t *topk_ids, int64_t N, in
                             "static MOE_ALIGN_NOALLOC_SCRATCH_BYTES; use moe_align");
         return MOE_ERR_UNSUPPORTED;
     }
-    if (N == 0) return MOE_OK;
+    if (N == 0) {  // nothing to group: the status word still reports the call
+        if (device_status &&
+            cudaMemsetAsync(device_status, 0, sizeof(int32_t), stream) != cudaSuccess) {
+            moe::set_last_error("moe_align_noalloc: status reset failed");
+            return MOE_ERR_CUDA;
+        }
+        return MOE_OK;
+    }
     void *scratch = nullptr;
     if (scratch_address(&scratch) != cudaSuccess) {
         moe::set_last_error("moe_align_noalloc: cudaGetSymbolAddress of the static scratch failed");

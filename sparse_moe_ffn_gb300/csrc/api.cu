@@ -278,10 +278,12 @@ moe_status_t forward_layout(int64_t N, int H, int E, int I, int k, int I_s,
     L->block_expert = take(sizeof(int32_t) * (cap / kBlockM));
     L->ready = take(sizeof(int32_t) * (E > cap / kBlockM ? E : cap / kBlockM));
     L->x_sorted = take(2 * static_cast<size_t>(cap) * H);
-    L->act = take(2 * static_cast<size_t>(cap) * I);
-    L->ypair = take(2 * static_cast<size_t>(P) * H);  // fp16
-    L->act_shared = take(shared ? 2 * static_cast<size_t>(round_up64(N, kBlockM)) * I_s : 0);
-    L->y_shared = take(shared ? 2 * static_cast<size_t>(N) * H : 0);  // fp16
+    // the activation: fp16, or a bf16 hi/lo pair (4 bytes a value either way
+    // is reserved, so one workspace serves both forms of the down weights)
+    L->act = take(4 * static_cast<size_t>(cap) * I);
+    L->ypair = take(4 * static_cast<size_t>(P) * H);  // fp32
+    L->act_shared = take(shared ? 4 * static_cast<size_t>(round_up64(N, kBlockM)) * I_s : 0);
+    L->y_shared = take(shared ? 4 * static_cast<size_t>(N) * H : 0);  // fp32
     L->total = off;
     L->capacity = cap;
     return MOE_OK;
@@ -292,9 +294,9 @@ moe_status_t forward_layout(int64_t N, int H, int E, int I, int k, int I_s,
 // the workspace layout.
 moe_status_t check_forward_args(const moe_bf16_t *x, const moe_bf16_t *router,
                                 const moe_bf16_t *w_gate, const moe_bf16_t *w_up,
-                                const moe_f16_t *w_down, const moe_bf16_t *shared_gate_proj,
+                                const void *w_down, const moe_bf16_t *shared_gate_proj,
                                 const moe_bf16_t *shared_up_proj,
-                                const moe_f16_t *shared_down_proj, const moe_bf16_t *shared_gate,
+                                const void *shared_down_proj, const moe_bf16_t *shared_gate,
                                 int64_t N, int H, int E, int I, int I_s, int k,
                                 const moe_bf16_t *out, const void *workspace,
                                 size_t workspace_bytes, bool *shared_out,
@@ -324,8 +326,9 @@ moe_status_t check_forward_args(const moe_bf16_t *x, const moe_bf16_t *router,
         return fail(MOE_ERR_INVALID_ARG, "bf16 matrices must be 16-byte aligned");
     if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
         return fail(MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-    if (N * k + static_cast<int64_t>(E) * kBlockM >= (int64_t(1) << 31))
-        return fail(MOE_ERR_UNSUPPORTED, "N*k + E*128 must stay below 2^31");
+    // the hi and lo rows of a split activation share one row index space
+    if (N * k + static_cast<int64_t>(E) * kBlockM >= (int64_t(1) << 30))
+        return fail(MOE_ERR_UNSUPPORTED, "N*k + E*128 must stay below 2^30");
     forward_layout(N, H, E, I, k, I_s, L);
     if (workspace_bytes < L->total)
         return fail(MOE_ERR_WORKSPACE_TOO_SMALL, "forward workspace needs %zu bytes, got %zu",
@@ -335,13 +338,15 @@ moe_status_t check_forward_args(const moe_bf16_t *x, const moe_bf16_t *router,
 
 
 // Grouping, gate/up and down for N rows with k (expert, weight) slots each:
-// ypair[p] = fp16(weights[p] * Expert_{ids[p]}(x[p / k])), p = n * k + j.
-// The workspace follows moe_forward_layout(N, H, E, I, k, 0); its status word
-// is not reset here.  Records the align .. down stage events.
+// ypair[p] = weights[p] * Expert_{ids[p]}(x[p / k]) in fp32, p = n * k + j.
+// w_down is bf16 (down_f16 false: the activation kept as a bf16 hi/lo pair)
+// or its fp16 copy (down_f16 true: an fp16 activation).  The workspace
+// follows moe_forward_layout(N, H, E, I, k, 0); its status word is not reset
+// here.  Records the align .. down stage events.
 moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const float *weights,
                              int64_t N, int k, int H, int E, int I, const moe_bf16_t *w_gate,
-                             const moe_bf16_t *w_up, const moe_f16_t *w_down,
-                             const moe_forward_layout_t &L, uint8_t *ws, uint16_t *ypair,
+                             const moe_bf16_t *w_up, const void *w_down, bool down_f16,
+                             const moe_forward_layout_t &L, uint8_t *ws, float *ypair,
                              cudaStream_t stream) {
     moe_status_t st;
     auto at = [&](size_t off) { return ws + off; };
@@ -408,6 +413,7 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
     g.w_rows = I;
     g.out = act;
     g.out_ld = I;
+    g.lo_rows = down_f16 ? 0 : cap;  // bf16 down weights: hi/lo activation
     g.scale = nullptr;
     g.status = status;
     // fewer than a block of pairs per expert: every weight tile is read once
@@ -469,8 +475,11 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
 
     // K4: down GEMM * routing weight, one row per pair
     if ((st = record_stage(MOE_STAGE_DOWN, stream)) != MOE_OK) return st;
-    if ((st = make_map(&tm_act, act, I, cap, I, kBlockK, 1, "act rows")) != MOE_OK) return st;
-    if ((st = make_map(&tm_act_box, act, I, cap, I, kBlockK, kBlockM, "act")) != MOE_OK) return st;
+    const GemmMode down = down_f16 ? kDown : kDownSplit;
+    const int64_t act_rows = down_f16 ? cap : 2 * cap;  // split: hi rows, then lo rows
+    if ((st = make_map(&tm_act, act, I, act_rows, I, kBlockK, 1, "act rows")) != MOE_OK) return st;
+    if ((st = make_map(&tm_act_box, act, I, act_rows, I, kBlockK, kBlockM, "act")) != MOE_OK)
+        return st;
     if ((st = make_map(&tm_wd, w_down, I, static_cast<uint64_t>(E) * H, I, kBlockK, kDownBN,
                        "w_down")) != MOE_OK)
         return st;
@@ -487,20 +496,20 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
         g.grid = g.max_tiles < sms ? g.max_tiles : sms;
     }
     if (sparse) {
-        MOE_CUDA(launch_sparse_gemm(kDown, kDownBN, tm_act, tm_wd, tm_wd, g, stream),
+        MOE_CUDA(launch_sparse_gemm(down, kDownBN, tm_act, tm_wd, tm_wd, g, stream),
                  "down kernel launch");
     } else if (pairs) {
-        const int bn = pair_gemm_block_n(kDown);
+        const int bn = pair_gemm_block_n(down);
         CUtensorMap tm_wd_half;
         if ((st = make_map(&tm_wd_half, w_down, I, static_cast<uint64_t>(E) * H, I, kBlockK,
                            bn / 2, "w_down")) != MOE_OK)
             return st;
         g.max_tiles = static_cast<int>(cap / kBlockM) * ((H + bn - 1) / bn);
         g.grid = 2 * (g.max_tiles < sms / 2 ? g.max_tiles : sms / 2);
-        MOE_CUDA(launch_pair_gemm(kDown, tm_act_box, tm_wd_half, tm_wd_half, g, stream),
+        MOE_CUDA(launch_pair_gemm(down, tm_act_box, tm_wd_half, tm_wd_half, g, stream),
                  "down kernel launch");
     } else {
-        MOE_CUDA(launch_gemm(kDown, kDownBN, tm_act, tm_act_box, tm_wd, tm_wd, g, stream),
+        MOE_CUDA(launch_gemm(down, kDownBN, tm_act, tm_act_box, tm_wd, tm_wd, g, stream),
                  "down kernel launch");
     }
     g_launches += 1;
@@ -623,13 +632,16 @@ size_t moe_forward_workspace_bytes(int64_t N, int H, int E, int I, int k, int I_
     return L.total;
 }
 
-moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const moe_bf16_t *w_gate,
-                         const moe_bf16_t *w_up, const moe_f16_t *w_down,
-                         const moe_bf16_t *shared_gate_proj, const moe_bf16_t *shared_up_proj,
-                         const moe_f16_t *shared_down_proj, const moe_bf16_t *shared_gate,
-                         int64_t N, int H, int E, int I, int I_s, int k, int norm_topk_prob,
-                         moe_bf16_t *out, void *workspace, size_t workspace_bytes,
-                         cudaStream_t stream) {
+// The whole layer; w_down / shared_down_proj are bf16 (down_f16 false) or
+// their fp16 copies (down_f16 true).
+static moe_status_t forward_impl(const moe_bf16_t *x, const moe_bf16_t *router,
+                                 const moe_bf16_t *w_gate, const moe_bf16_t *w_up,
+                                 const void *w_down, const moe_bf16_t *shared_gate_proj,
+                                 const moe_bf16_t *shared_up_proj, const void *shared_down_proj,
+                                 const moe_bf16_t *shared_gate, int64_t N, int H, int E, int I,
+                                 int I_s, int k, int norm_topk_prob, bool down_f16,
+                                 moe_bf16_t *out, void *workspace, size_t workspace_bytes,
+                                 cudaStream_t stream) {
     g_last_error.clear();
     bool shared = false;
     moe_forward_layout_t L;
@@ -645,7 +657,7 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
     float *topk_w = reinterpret_cast<float *>(at(L.topk_w));
     int32_t *topk_ids = reinterpret_cast<int32_t *>(at(L.topk_ids));
     float *gamma = shared ? reinterpret_cast<float *>(at(L.gamma)) : nullptr;
-    uint16_t *ypair = reinterpret_cast<uint16_t *>(at(L.ypair));
+    float *ypair = reinterpret_cast<float *>(at(L.ypair));
     const int sms = num_sms_of_current_device();
 
     // K1: routing (its first CTA also clears the status word, so that no
@@ -656,17 +668,19 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
     if (st != MOE_OK) return st;
 
     // K2-K4: grouping, gate/up, down
-    if ((st = enqueue_experts(x, topk_ids, topk_w, N, k, H, E, I, w_gate, w_up, w_down, L, ws,
-                              ypair, stream)) != MOE_OK)
+    if ((st = enqueue_experts(x, topk_ids, topk_w, N, k, H, E, I, w_gate, w_up, w_down,
+                              down_f16, L, ws, ypair, stream)) != MOE_OK)
         return st;
 
     // shared expert: one dense group over all N tokens, weight sigmoid(x . g)
     if ((st = record_stage(MOE_STAGE_SHARED, stream)) != MOE_OK) return st;
-    uint16_t *y_shared = nullptr;
+    float *y_shared = nullptr;
     if (shared) {
         uint16_t *act_s = reinterpret_cast<uint16_t *>(at(L.act_shared));
-        y_shared = reinterpret_cast<uint16_t *>(at(L.y_shared));
+        y_shared = reinterpret_cast<float *>(at(L.y_shared));
         const int64_t rows_s = round_up64(N, kBlockM);
+        const GemmMode down = down_f16 ? kDown : kDownSplit;
+        const int64_t act_rows = down_f16 ? rows_s : 2 * rows_s;
         CUtensorMap tm_sg, tm_su, tm_acts, tm_sd, tm_xbox;
         const int bn_s = choose_gate_up_bn(static_cast<double>(rows_s / kBlockM),
                                            static_cast<double>(N), I_s, sms);
@@ -677,7 +691,7 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
         if ((st = make_map(&tm_su, shared_up_proj, H, I_s, H, kBlockK, bn_s,
                            "shared_up_proj")) != MOE_OK)
             return st;
-        if ((st = make_map(&tm_acts, act_s, I_s, rows_s, I_s, kBlockK, kBlockM,
+        if ((st = make_map(&tm_acts, act_s, I_s, act_rows, I_s, kBlockK, kBlockM,
                            "shared act rows")) != MOE_OK)
             return st;
         if ((st = make_map(&tm_sd, shared_down_proj, I_s, H, I_s, kBlockK, kDownBN,
@@ -701,6 +715,7 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
         s.w_rows = I_s;
         s.out = act_s;
         s.out_ld = I_s;
+        s.lo_rows = down_f16 ? 0 : rows_s;
         s.scale = nullptr;
         s.status = status;
         s.stream_weights = N <= kBlockM ? 1 : 0;
@@ -739,17 +754,17 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
             s.grid = s.max_tiles < sms ? s.max_tiles : sms;
         }
         if (pairs_s) {
-            const int bn = pair_gemm_block_n(kDown);
+            const int bn = pair_gemm_block_n(down);
             CUtensorMap tm_sd2;
             if ((st = make_map(&tm_sd2, shared_down_proj, I_s, H, I_s, kBlockK, bn / 2,
                                "shared_down_proj")) != MOE_OK)
                 return st;
             s.max_tiles = static_cast<int>((rows_s / kBlockM + 1) / 2) * ((H + bn - 1) / bn);
             s.grid = 2 * (s.max_tiles < sms / 2 ? s.max_tiles : sms / 2);
-            MOE_CUDA(launch_pair_gemm(kDown, tm_acts, tm_sd2, tm_sd2, s, stream),
+            MOE_CUDA(launch_pair_gemm(down, tm_acts, tm_sd2, tm_sd2, s, stream),
                      "shared down kernel launch");
         } else {
-            MOE_CUDA(launch_gemm(kDown, kDownBN, tm_acts, tm_acts, tm_sd, tm_sd, s, stream),
+            MOE_CUDA(launch_gemm(down, kDownBN, tm_acts, tm_acts, tm_sd, tm_sd, s, stream),
                      "shared down kernel launch");
         }
         g_launches += 2;
@@ -763,14 +778,41 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const mo
     return MOE_OK;
 }
 
+moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router, const moe_bf16_t *w_gate,
+                         const moe_bf16_t *w_up, const moe_bf16_t *w_down,
+                         const moe_bf16_t *shared_gate_proj, const moe_bf16_t *shared_up_proj,
+                         const moe_bf16_t *shared_down_proj, const moe_bf16_t *shared_gate,
+                         int64_t N, int H, int E, int I, int I_s, int k, int norm_topk_prob,
+                         moe_bf16_t *out, void *workspace, size_t workspace_bytes,
+                         cudaStream_t stream) {
+    return forward_impl(x, router, w_gate, w_up, w_down, shared_gate_proj, shared_up_proj,
+                        shared_down_proj, shared_gate, N, H, E, I, I_s, k, norm_topk_prob, false,
+                        out, workspace, workspace_bytes, stream);
+}
+
+moe_status_t moe_forward_prepared(const moe_bf16_t *x, const moe_bf16_t *router,
+                                  const moe_bf16_t *w_gate, const moe_bf16_t *w_up,
+                                  const moe_f16_t *w_down_f16,
+                                  const moe_bf16_t *shared_gate_proj,
+                                  const moe_bf16_t *shared_up_proj,
+                                  const moe_f16_t *shared_down_proj_f16,
+                                  const moe_bf16_t *shared_gate, int64_t N, int H, int E, int I,
+                                  int I_s, int k, int norm_topk_prob, moe_bf16_t *out,
+                                  void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return forward_impl(x, router, w_gate, w_up, w_down_f16, shared_gate_proj, shared_up_proj,
+                        shared_down_proj_f16, shared_gate, N, H, E, I, I_s, k, norm_topk_prob,
+                        true, out, workspace, workspace_bytes, stream);
+}
+
 size_t moe_experts_workspace_bytes(int64_t R, int H, int E, int I) {
     return moe_forward_workspace_bytes(R, H, E, I, 1, 0);
 }
 
-moe_status_t moe_experts(const moe_bf16_t *x_rows, const int32_t *ids, const float *weights,
-                         int64_t R, int H, int E, int I, const moe_bf16_t *w_gate,
-                         const moe_bf16_t *w_up, const moe_f16_t *w_down, moe_f16_t *y,
-                         void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+static moe_status_t experts_impl(const moe_bf16_t *x_rows, const int32_t *ids,
+                                 const float *weights, int64_t R, int H, int E, int I,
+                                 const moe_bf16_t *w_gate, const moe_bf16_t *w_up,
+                                 const void *w_down, bool down_f16, float *y, void *workspace,
+                                 size_t workspace_bytes, cudaStream_t stream) {
     g_last_error.clear();
     if (R < 0) return fail(MOE_ERR_INVALID_ARG, "R must be >= 0 (got %lld)", (long long)R);
     if (H < 8 || H % 8 || I < 8 || I % 8)
@@ -782,11 +824,11 @@ moe_status_t moe_experts(const moe_bf16_t *x_rows, const int32_t *ids, const flo
         return fail(MOE_ERR_INVALID_ARG, "every moe_experts pointer must be non-null");
     if (!aligned16(x_rows) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
         !aligned16(y))
-        return fail(MOE_ERR_INVALID_ARG, "bf16 / fp16 matrices must be 16-byte aligned");
+        return fail(MOE_ERR_INVALID_ARG, "matrices must be 16-byte aligned");
     if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
         return fail(MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-    if (R + static_cast<int64_t>(E) * kBlockM >= (int64_t(1) << 31))
-        return fail(MOE_ERR_UNSUPPORTED, "R + E*128 must stay below 2^31");
+    if (R + static_cast<int64_t>(E) * kBlockM >= (int64_t(1) << 30))
+        return fail(MOE_ERR_UNSUPPORTED, "R + E*128 must stay below 2^30");
     moe_forward_layout_t L;
     forward_layout(R, H, E, I, 1, 0, &L);
     if (workspace_bytes < L.total)
@@ -794,12 +836,29 @@ moe_status_t moe_experts(const moe_bf16_t *x_rows, const int32_t *ids, const flo
                     L.total, workspace_bytes);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     MOE_CUDA(cudaMemsetAsync(ws + L.status, 0, sizeof(int32_t), stream), "status reset");
-    return enqueue_experts(x_rows, ids, weights, R, 1, H, E, I, w_gate, w_up, w_down, L, ws, y,
-                           stream);
+    return enqueue_experts(x_rows, ids, weights, R, 1, H, E, I, w_gate, w_up, w_down, down_f16,
+                           L, ws, y, stream);
 }
 
-moe_status_t moe_combine(const moe_f16_t *ypair, const moe_f16_t *yshared, int64_t N, int H,
-                         int k, moe_bf16_t *out, cudaStream_t stream) {
+moe_status_t moe_experts(const moe_bf16_t *x_rows, const int32_t *ids, const float *weights,
+                         int64_t R, int H, int E, int I, const moe_bf16_t *w_gate,
+                         const moe_bf16_t *w_up, const moe_bf16_t *w_down, float *y,
+                         void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return experts_impl(x_rows, ids, weights, R, H, E, I, w_gate, w_up, w_down, false, y,
+                        workspace, workspace_bytes, stream);
+}
+
+moe_status_t moe_experts_prepared(const moe_bf16_t *x_rows, const int32_t *ids,
+                                  const float *weights, int64_t R, int H, int E, int I,
+                                  const moe_bf16_t *w_gate, const moe_bf16_t *w_up,
+                                  const moe_f16_t *w_down_f16, float *y, void *workspace,
+                                  size_t workspace_bytes, cudaStream_t stream) {
+    return experts_impl(x_rows, ids, weights, R, H, E, I, w_gate, w_up, w_down_f16, true, y,
+                        workspace, workspace_bytes, stream);
+}
+
+moe_status_t moe_combine(const float *ypair, const float *yshared, int64_t N, int H, int k,
+                         moe_bf16_t *out, cudaStream_t stream) {
     g_last_error.clear();
     if (N < 0 || H < 8 || H % 8 || k < 1)
         return fail(MOE_ERR_INVALID_ARG, "need N >= 0, H a positive multiple of 8, k >= 1");
@@ -858,14 +917,16 @@ static void *mapped_device_pointer(const void *host) {
     return aligned16(attr.devicePointer) ? attr.devicePointer : nullptr;
 }
 
-moe_status_t moe_forward_host(const moe_bf16_t *x_host, moe_bf16_t *out_host, moe_bf16_t *x_dev,
-                              moe_bf16_t *out_dev, const moe_bf16_t *router,
-                              const moe_bf16_t *w_gate, const moe_bf16_t *w_up,
-                              const moe_f16_t *w_down, const moe_bf16_t *shared_gate_proj,
-                              const moe_bf16_t *shared_up_proj,
-                              const moe_f16_t *shared_down_proj, const moe_bf16_t *shared_gate,
-                              int64_t N, int H, int E, int I, int I_s, int k, int norm_topk_prob,
-                              void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+static moe_status_t forward_host_impl(const moe_bf16_t *x_host, moe_bf16_t *out_host,
+                                      moe_bf16_t *x_dev, moe_bf16_t *out_dev,
+                                      const moe_bf16_t *router, const moe_bf16_t *w_gate,
+                                      const moe_bf16_t *w_up, const void *w_down,
+                                      const moe_bf16_t *shared_gate_proj,
+                                      const moe_bf16_t *shared_up_proj,
+                                      const void *shared_down_proj, const moe_bf16_t *shared_gate,
+                                      int64_t N, int H, int E, int I, int I_s, int k,
+                                      int norm_topk_prob, bool down_f16, void *workspace,
+                                      size_t workspace_bytes, cudaStream_t stream) {
     g_last_error.clear();
     bool shared = false;
     moe_forward_layout_t L;
@@ -889,9 +950,9 @@ moe_status_t moe_forward_host(const moe_bf16_t *x_host, moe_bf16_t *out_host, mo
         MOE_CUDA(cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, stream),
                  "input copy");
     }
-    st = moe_forward(x_dev, router, w_gate, w_up, w_down, shared_gate_proj, shared_up_proj,
-                     shared_down_proj, shared_gate, N, H, E, I, I_s, k, norm_topk_prob, out_dev,
-                     workspace, workspace_bytes, stream);
+    st = forward_impl(x_dev, router, w_gate, w_up, w_down, shared_gate_proj, shared_up_proj,
+                      shared_down_proj, shared_gate, N, H, E, I, I_s, k, norm_topk_prob, down_f16,
+                      out_dev, workspace, workspace_bytes, stream);
     if (st != MOE_OK) return st;
     if (out_map) {
         MOE_CUDA(launch_copy16(out_dev, out_map, bytes, sms, stream), "output copy kernel launch");
@@ -901,6 +962,33 @@ moe_status_t moe_forward_host(const moe_bf16_t *x_host, moe_bf16_t *out_host, mo
                  "output copy");
     }
     return MOE_OK;
+}
+
+moe_status_t moe_forward_host(const moe_bf16_t *x_host, moe_bf16_t *out_host, moe_bf16_t *x_dev,
+                              moe_bf16_t *out_dev, const moe_bf16_t *router,
+                              const moe_bf16_t *w_gate, const moe_bf16_t *w_up,
+                              const moe_bf16_t *w_down, const moe_bf16_t *shared_gate_proj,
+                              const moe_bf16_t *shared_up_proj,
+                              const moe_bf16_t *shared_down_proj, const moe_bf16_t *shared_gate,
+                              int64_t N, int H, int E, int I, int I_s, int k, int norm_topk_prob,
+                              void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return forward_host_impl(x_host, out_host, x_dev, out_dev, router, w_gate, w_up, w_down,
+                             shared_gate_proj, shared_up_proj, shared_down_proj, shared_gate, N,
+                             H, E, I, I_s, k, norm_topk_prob, false, workspace, workspace_bytes,
+                             stream);
+}
+
+moe_status_t moe_forward_host_prepared(
+    const moe_bf16_t *x_host, moe_bf16_t *out_host, moe_bf16_t *x_dev, moe_bf16_t *out_dev,
+    const moe_bf16_t *router, const moe_bf16_t *w_gate, const moe_bf16_t *w_up,
+    const moe_f16_t *w_down_f16, const moe_bf16_t *shared_gate_proj,
+    const moe_bf16_t *shared_up_proj, const moe_f16_t *shared_down_proj_f16,
+    const moe_bf16_t *shared_gate, int64_t N, int H, int E, int I, int I_s, int k,
+    int norm_topk_prob, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return forward_host_impl(x_host, out_host, x_dev, out_dev, router, w_gate, w_up, w_down_f16,
+                             shared_gate_proj, shared_up_proj, shared_down_proj_f16, shared_gate,
+                             N, H, E, I, I_s, k, norm_topk_prob, true, workspace,
+                             workspace_bytes, stream);
 }
 
 // ----------------------------------------------------- add + RMSNorm
@@ -929,12 +1017,15 @@ moe_status_t moe_add_rmsnorm(const moe_bf16_t *x, moe_bf16_t *residual, const mo
 size_t moe_dense_mlp_workspace_bytes(int64_t N, int H, int I) {
     if (N < 0 || H < 1 || I < 1) return 0;
     const size_t rows = static_cast<size_t>(round_up64(N, kBlockM));
-    return kAlign + round_up(2 * rows * I, kAlign) + round_up(2 * static_cast<size_t>(N) * H, kAlign);
+    // the activation (fp16, or a bf16 hi/lo pair: 4 bytes a value reserved),
+    // then the fp32 down projection
+    return kAlign + round_up(4 * rows * I, kAlign) + round_up(4 * static_cast<size_t>(N) * H, kAlign);
 }
 
-moe_status_t moe_dense_mlp(const moe_bf16_t *x, const moe_bf16_t *w_gate, const moe_bf16_t *w_up,
-                           const moe_f16_t *w_down, int64_t N, int H, int I, moe_bf16_t *out,
-                           void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+static moe_status_t dense_mlp_impl(const moe_bf16_t *x, const moe_bf16_t *w_gate,
+                                   const moe_bf16_t *w_up, const void *w_down, bool down_f16,
+                                   int64_t N, int H, int I, moe_bf16_t *out, void *workspace,
+                                   size_t workspace_bytes, cudaStream_t stream) {
     g_last_error.clear();
     if (N < 0) return fail(MOE_ERR_INVALID_ARG, "N must be >= 0");
     if (H < 8 || H % 8 || I < 8 || I % 8)
@@ -944,10 +1035,10 @@ moe_status_t moe_dense_mlp(const moe_bf16_t *x, const moe_bf16_t *w_gate, const 
         return fail(MOE_ERR_INVALID_ARG, "every moe_dense_mlp pointer must be non-null");
     if (!aligned16(x) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
         !aligned16(out))
-        return fail(MOE_ERR_INVALID_ARG, "bf16 matrices must be 16-byte aligned");
+        return fail(MOE_ERR_INVALID_ARG, "matrices must be 16-byte aligned");
     if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
         return fail(MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-    if (N >= (int64_t(1) << 31) - kBlockM) return fail(MOE_ERR_UNSUPPORTED, "N must stay below 2^31");
+    if (N >= (int64_t(1) << 30) - kBlockM) return fail(MOE_ERR_UNSUPPORTED, "N must stay below 2^30");
     const size_t need = moe_dense_mlp_workspace_bytes(N, H, I);
     if (workspace_bytes < need)
         return fail(MOE_ERR_WORKSPACE_TOO_SMALL, "dense MLP workspace needs %zu bytes, got %zu", need,
@@ -956,15 +1047,17 @@ moe_status_t moe_dense_mlp(const moe_bf16_t *x, const moe_bf16_t *w_gate, const 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     int32_t *status = reinterpret_cast<int32_t *>(ws);
     uint16_t *act = reinterpret_cast<uint16_t *>(ws + kAlign);
-    uint16_t *y = reinterpret_cast<uint16_t *>(ws + kAlign + round_up(2 * rows * I, kAlign));
+    float *y = reinterpret_cast<float *>(ws + kAlign + round_up(4 * rows * I, kAlign));
     const int sms = num_sms_of_current_device();
+    const GemmMode down = down_f16 ? kDown : kDownSplit;
+    const int64_t act_rows = down_f16 ? rows : 2 * rows;  // split: hi rows, then lo rows
     moe_status_t st;
     CUtensorMap tm_x, tm_g, tm_u, tm_act, tm_d;
     const int bn = choose_gate_up_bn(static_cast<double>(rows / kBlockM), static_cast<double>(N), I, sms);
     if ((st = make_map(&tm_x, x, H, N, H, kBlockK, kBlockM, "x")) != MOE_OK) return st;
     if ((st = make_map(&tm_g, w_gate, H, I, H, kBlockK, bn, "w_gate")) != MOE_OK) return st;
     if ((st = make_map(&tm_u, w_up, H, I, H, kBlockK, bn, "w_up")) != MOE_OK) return st;
-    if ((st = make_map(&tm_act, act, I, rows, I, kBlockK, kBlockM, "act")) != MOE_OK) return st;
+    if ((st = make_map(&tm_act, act, I, act_rows, I, kBlockK, kBlockM, "act")) != MOE_OK) return st;
     if ((st = make_map(&tm_d, w_down, I, H, I, kBlockK, kDownBN, "w_down")) != MOE_OK) return st;
     MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int32_t), stream), "status reset");
     // one dense group: every token row, weight 1
@@ -980,6 +1073,7 @@ moe_status_t moe_dense_mlp(const moe_bf16_t *x, const moe_bf16_t *w_gate, const 
     g.w_rows = I;
     g.out = act;
     g.out_ld = I;
+    g.lo_rows = down_f16 ? 0 : rows;
     g.scale = nullptr;
     g.status = status;
     g.stream_weights = N <= kBlockM ? 1 : 0;
@@ -1007,24 +1101,39 @@ moe_status_t moe_dense_mlp(const moe_bf16_t *x, const moe_bf16_t *w_gate, const 
     g.out = y;
     g.out_ld = H;
     if (pairs) {
-        const int bnp = pair_gemm_block_n(kDown);
+        const int bnp = pair_gemm_block_n(down);
         CUtensorMap tm_d2;
         if ((st = make_map(&tm_d2, w_down, I, H, I, kBlockK, bnp / 2, "w_down")) != MOE_OK)
             return st;
         g.max_tiles = static_cast<int>((rows / kBlockM + 1) / 2) * ((H + bnp - 1) / bnp);
         g.grid = 2 * (g.max_tiles < sms / 2 ? g.max_tiles : sms / 2);
-        MOE_CUDA(launch_pair_gemm(kDown, tm_act, tm_d2, tm_d2, g, stream),
+        MOE_CUDA(launch_pair_gemm(down, tm_act, tm_d2, tm_d2, g, stream),
                  "dense down kernel launch");
     } else {
         g.max_tiles = static_cast<int>(rows / kBlockM) * ((H + kDownBN - 1) / kDownBN);
         g.grid = g.max_tiles < sms ? g.max_tiles : sms;
-        MOE_CUDA(launch_gemm(kDown, kDownBN, tm_act, tm_act, tm_d, tm_d, g, stream),
+        MOE_CUDA(launch_gemm(down, kDownBN, tm_act, tm_act, tm_d, tm_d, g, stream),
                  "dense down kernel launch");
     }
-    // fp16 rows -> bf16 out (the combine with one slot per token)
+    // fp32 rows -> bf16 out (the combine with one slot per token)
     MOE_CUDA(launch_combine(y, nullptr, N, H, 1, out, sms, stream), "combine kernel launch");
     g_launches += 3;
     return MOE_OK;
+}
+
+moe_status_t moe_dense_mlp(const moe_bf16_t *x, const moe_bf16_t *w_gate, const moe_bf16_t *w_up,
+                           const moe_bf16_t *w_down, int64_t N, int H, int I, moe_bf16_t *out,
+                           void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return dense_mlp_impl(x, w_gate, w_up, w_down, false, N, H, I, out, workspace,
+                          workspace_bytes, stream);
+}
+
+moe_status_t moe_dense_mlp_prepared(const moe_bf16_t *x, const moe_bf16_t *w_gate,
+                                    const moe_bf16_t *w_up, const moe_f16_t *w_down_f16,
+                                    int64_t N, int H, int I, moe_bf16_t *out, void *workspace,
+                                    size_t workspace_bytes, cudaStream_t stream) {
+    return dense_mlp_impl(x, w_gate, w_up, w_down_f16, true, N, H, I, out, workspace,
+                          workspace_bytes, stream);
 }
 
 moe_status_t moe_selftest_wait_timeout(void *workspace, size_t workspace_bytes,

@@ -1,13 +1,17 @@
 // combine.cu -- K5: weighted accumulate of every token's k expert outputs.
 //
-// The scatter-add of the M03 "Sparse MoE" drill ("out.index_add_(0, toks,
-// y * w)": each token receives the sum of all k contributions, never just the
-// last one written) done without atomics: the down-projection epilogue stored
-// w * Expert(x) of pair p = n*k + j at row p of ypair, so token n's k
-// contributions are the k consecutive fp16 rows n*k .. n*k+k-1.  They are
-// summed in slot order in fp32, the shared-expert term gamma * SharedMLP(x) (same
-// page, talker line) is added last, and the result is rounded to bf16 once.
-// Bandwidth bound: one thread per 8 output columns, 16-byte loads and stores.
+// The scatter-add of the M03 "Sparse MoE" drill (each token receives the sum
+// of all k weighted expert outputs, an accumulation and never an assignment)
+// done without atomics: the down-projection epilogue stored w * Expert(x) of
+// pair p = n*k + j at row p of ypair in fp32, so token n's k contributions
+// are the k consecutive rows n*k .. n*k+k-1.  They are summed in slot order
+// in fp32, the shared-expert term gamma * SharedMLP(x) (same page, talker
+// line) is added last, and the result is rounded to bf16 once.  Keeping the
+// contributions in fp32 matters: the bf16 rounding of the exact result
+// already uses ~97% of the layer's max-error bound at prefill size, and an
+// fp16 rounding of each contribution pushed the largest outputs past it.
+// Bandwidth bound: one thread per 8 output columns, two 16-byte loads per
+// contribution and one 16-byte store.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -20,18 +24,22 @@ namespace {
 
 constexpr int kCombineThreads = 256;
 
-__device__ __forceinline__ void add_f16x8(float (&acc)[8], const uint4 &v) {
-    const __half2 *h = reinterpret_cast<const __half2 *>(&v);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 f = __half22float2(h[i]);
-        acc[2 * i] += f.x;
-        acc[2 * i + 1] += f.y;
-    }
+// acc[0..7] += the 8 floats at p (32-byte aligned), read through L2
+__device__ __forceinline__ void add_f32x8(float (&acc)[8], const float *p) {
+    const float4 a = __ldcg(reinterpret_cast<const float4 *>(p));
+    const float4 b = __ldcg(reinterpret_cast<const float4 *>(p + 4));
+    acc[0] += a.x;
+    acc[1] += a.y;
+    acc[2] += a.z;
+    acc[3] += a.w;
+    acc[4] += b.x;
+    acc[5] += b.y;
+    acc[6] += b.z;
+    acc[7] += b.w;
 }
 
 __global__ void __launch_bounds__(kCombineThreads)
-    combine_kernel(const uint16_t *__restrict__ ypair, const uint16_t *__restrict__ yshared,
+    combine_kernel(const float *__restrict__ ypair, const float *__restrict__ yshared,
                    int64_t N, int H, int k, uint16_t *__restrict__ out) {
     griddep_launch_dependents();
     griddep_wait();
@@ -42,11 +50,9 @@ __global__ void __launch_bounds__(kCombineThreads)
         const int64_t n = idx / groups;
         const int col = static_cast<int>(idx % groups) * 8;
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        const uint16_t *src = ypair + n * k * static_cast<int64_t>(H) + col;
-        for (int j = 0; j < k; ++j)
-            add_f16x8(acc, __ldcg(reinterpret_cast<const uint4 *>(src + static_cast<int64_t>(j) * H)));
-        if (yshared)
-            add_f16x8(acc, __ldcg(reinterpret_cast<const uint4 *>(yshared + n * H + col)));
+        const float *src = ypair + n * k * static_cast<int64_t>(H) + col;
+        for (int j = 0; j < k; ++j) add_f32x8(acc, src + static_cast<int64_t>(j) * H);
+        if (yshared) add_f32x8(acc, yshared + n * H + col);
         uint4 pk;
         pk.x = pack_bf16x2(acc[0], acc[1]);
         pk.y = pack_bf16x2(acc[2], acc[3]);
@@ -58,8 +64,8 @@ __global__ void __launch_bounds__(kCombineThreads)
 
 }  // namespace
 
-cudaError_t launch_combine(const uint16_t *ypair, const uint16_t *yshared, int64_t N, int H,
-                           int k, uint16_t *out, int num_sms, cudaStream_t s) {
+cudaError_t launch_combine(const float *ypair, const float *yshared, int64_t N, int H, int k,
+                           uint16_t *out, int num_sms, cudaStream_t s) {
     const int64_t total = N * (H / 8);
     int64_t blocks = (total + kCombineThreads - 1) / kCombineThreads;
     const int64_t cap = static_cast<int64_t>(num_sms) * 16;

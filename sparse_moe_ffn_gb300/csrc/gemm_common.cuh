@@ -14,6 +14,7 @@ constexpr int kATileBytes = kBlockM * 128;  // 128 rows x 64 bf16
 constexpr int kAccCols = 256;               // fp32 columns per accumulator
 constexpr uint32_t kTmemCols = 2 * kAccCols;
 constexpr float kF16Max = 65504.f;
+constexpr float kF32Max = 3.402823466e38f;
 constexpr int kSparseRows = 32;             // blocks with at most this many real rows gather
 
 __device__ __forceinline__ float silu_times(float g, float u) {
@@ -44,7 +45,7 @@ __device__ __forceinline__ TileRow tile_row_of(const GemmArgs &a, int64_t grow, 
     r.grow = grow;
     r.q = q;
     r.valid = q >= 0 && q < a.q_limit;
-    r.w = (MODE == kDown && r.valid) ? (a.scale ? __ldcg(a.scale + q) : 1.f) : 0.f;
+    r.w = (is_down(MODE) && r.valid) ? (a.scale ? __ldcg(a.scale + q) : 1.f) : 0.f;
     return r;
 }
 
@@ -68,11 +69,14 @@ __device__ __forceinline__ TileRow no_tile_row() {
 // output columns [nt * BN, nt * BN + BN) (gate/up: the accumulator holds BN
 // gate columns, then BN up columns).  taddr = this warp's TMEM lane quarter
 // and the tile's accumulator.
-//   gate/up: act = fp16(silu(g) * u), the down projection's A operand;
-//   down:    y[q] = fp16(w[q] * acc), the pair's weighted result.
-// fp16 keeps 11 significant bits; a value past its range (65504) is
-// reported as MOE_ERR_DEVICE_CHECK rather than silently turned into
-// infinity.
+//   gate/up: a = silu(g) * u in fp32, stored as the down projection's A
+//            operand: fp16(a) (a.lo_rows == 0), or the bf16 pair
+//            hi = bf16(a) at row grow and lo = bf16(a - hi) at row
+//            grow + a.lo_rows (hi + lo carries 16 significant bits);
+//   down:    y[q] = w[q] * acc in fp32, the pair's weighted result, kept in
+//            fp32 until the combine rounds the token's sum to bf16 once.
+// A value the stored format cannot hold (an fp16 activation past 65504, or
+// anything non-finite) is reported as MOE_ERR_DEVICE_CHECK.
 template <int MODE, int BN>
 __device__ __forceinline__ void store_tile(const GemmArgs &a, uint32_t taddr, const TileRow &r,
                                            int nt) {
@@ -82,22 +86,27 @@ __device__ __forceinline__ void store_tile(const GemmArgs &a, uint32_t taddr, co
     const bool valid = r.valid;
     const int col0 = nt * BN;
     float vmax = 0.f;
-    // 16 columns (32 bytes) per store when every output row starts on a
-    // 32-byte boundary, else 8 columns; stores never pass n_out (a multiple
-    // of 8)
-    const bool wide = (a.out_ld % 16) == 0 && (reinterpret_cast<uintptr_t>(a.out) % 32) == 0;
-    auto store16 = [&](uint16_t *dst, int col, const uint32_t (&pk)[8]) {
-        if (wide && col + 16 <= a.n_out) {
+    // 32 bytes per store when every output row starts on a 32-byte boundary,
+    // else 16; stores never pass n_out (a multiple of 8)
+    const int esize = MODE == kGateUp ? 2 : 4;
+    const bool wide = (a.out_ld * esize) % 32 == 0 && (reinterpret_cast<uintptr_t>(a.out) % 32) == 0;
+    // 32 bytes (pk) to dst, which holds elements [col, col + 32 / esize)
+    auto store32 = [&](void *dst, int col, const uint32_t (&pk)[8]) {
+        const int per16 = 16 / esize;
+        if (wide && col + 2 * per16 <= a.n_out) {
             st_global_v8(dst, pk);
         } else {
-            if (col + 8 <= a.n_out)
+            if (col + per16 <= a.n_out)
                 *reinterpret_cast<uint4 *>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            if (col + 16 <= a.n_out)
-                *reinterpret_cast<uint4 *>(dst + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            if (col + 2 * per16 <= a.n_out)
+                *reinterpret_cast<uint4 *>(static_cast<uint8_t *>(dst) + 16) =
+                    make_uint4(pk[4], pk[5], pk[6], pk[7]);
         }
     };
     if (MODE == kGateUp) {
-        uint16_t *dst = a.out + grow * a.out_ld + col0;
+        uint16_t *dst = static_cast<uint16_t *>(a.out) + grow * a.out_ld + col0;
+        const bool split = a.lo_rows != 0;
+        uint16_t *dst_lo = dst + a.lo_rows * a.out_ld;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
             float gv[32], uv[32];
@@ -107,22 +116,31 @@ __device__ __forceinline__ void store_tile(const GemmArgs &a, uint32_t taddr, co
             if (valid) {
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    uint32_t pk[8];
+                    uint32_t pk[8], pl[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const int j = h * 16 + 2 * i;
                         const float a0 = silu_times(gv[j], uv[j]);
                         const float a1 = silu_times(gv[j + 1], uv[j + 1]);
                         vmax = fmaxf(vmax, fmaxf(fabsf(a0), fabsf(a1)));
-                        pk[i] = pack_f16x2(a0, a1);
+                        if (split) {
+                            pk[i] = pack_bf16x2(a0, a1);
+                            const float2 hi = unpack_bf16x2(pk[i]);
+                            pl[i] = pack_bf16x2(a0 - hi.x, a1 - hi.y);
+                        } else {
+                            pk[i] = pack_f16x2(a0, a1);
+                        }
                     }
-                    store16(dst + c * 32 + h * 16, col0 + c * 32 + h * 16, pk);
+                    const int cc = c * 32 + h * 16;
+                    store32(dst + cc, col0 + cc, pk);
+                    if (split) store32(dst_lo + cc, col0 + cc, pl);
                 }
             }
         }
+        if (!(vmax <= (split ? kF32Max : kF16Max))) record_status(a.status, MOE_ERR_DEVICE_CHECK);
     } else {
         const float w = r.w;
-        uint16_t *dst = a.out + (valid ? q : 0) * a.out_ld + col0;
+        float *dst = static_cast<float *>(a.out) + (valid ? q : 0) * a.out_ld + col0;
         // 64 columns per TMEM round trip: two loads in flight, one wait
 #pragma unroll 1
         for (int c = 0; c < BN / 64; ++c) {
@@ -132,21 +150,21 @@ __device__ __forceinline__ void store_tile(const GemmArgs &a, uint32_t taddr, co
             tmem_load_wait();
             if (valid) {
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
+                for (int h = 0; h < 8; ++h) {
                     uint32_t pk[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const float t0 = w * yv[h * 16 + 2 * i];
-                        const float t1 = w * yv[h * 16 + 2 * i + 1];
-                        vmax = fmaxf(vmax, fmaxf(fabsf(t0), fabsf(t1)));
-                        pk[i] = pack_f16x2(t0, t1);
+                        const float t = w * yv[h * 8 + i];
+                        vmax = fmaxf(vmax, fabsf(t));
+                        pk[i] = __float_as_uint(t);
                     }
-                    store16(dst + c * 64 + h * 16, col0 + c * 64 + h * 16, pk);
+                    const int cc = c * 64 + h * 8;
+                    store32(dst + cc, col0 + cc, pk);
                 }
             }
         }
+        if (!(vmax <= kF32Max)) record_status(a.status, MOE_ERR_DEVICE_CHECK);
     }
-    if (!(vmax <= kF16Max)) record_status(a.status, MOE_ERR_DEVICE_CHECK);
 }
 
 }  // namespace moe

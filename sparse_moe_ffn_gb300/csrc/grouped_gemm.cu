@@ -8,16 +8,19 @@
 //       A = x[token(q)] gathered row by row, B0 = Wg[e], B1 = Wu[e];
 //       a = silu(A B0^T) * (A B1^T) in fp32 (96- or 128-column tiles),
 //       stored as act = fp16(a)
-//   K4 (kDown): A = act rows of block b, B0 = Wd[e] held in fp16;
-//       y[q, :] = fp16(w[q] * act B0^T)  (256-column tiles, fp16 x fp16 MMAs)
-//       where w[q] is the routing weight of pair q (or the shared gate).
-//       fp16 gives the activation 11 significant bits instead of bf16's 8
-//       (a bf16 activation costs more relative error per pair than the
-//       layer's output tolerance leaves over the final bf16 rounding), and
-//       the bf16 down weights convert to fp16 exactly from 2^-14 up.  The
-//       per-pair results are stored in fp16 too: the same bytes as bf16 with
-//       an 8x finer rounding step.  A value past fp16's range records
-//       MOE_ERR_DEVICE_CHECK.
+//   K4: A = act rows of block b, B0 = Wd[e];
+//       y[q, :] = w[q] * act B0^T in fp32 (256-column tiles), where w[q] is
+//       the routing weight of pair q (or the shared gate).  The activation
+//       needs more significant bits than bf16's 8 (a bf16 activation costs
+//       more relative error per pair than the layer's output tolerance
+//       leaves over the final bf16 rounding), so K4 takes it one of two ways:
+//         kDownSplit: act as a bf16 pair hi + lo (16 bits) against the
+//                     model's bf16 Wd, two MMAs per K step (hi, then lo);
+//         kDown:      act in fp16 (11 bits) against an fp16 copy of Wd made
+//                     once at load (exact for bf16 weights from 2^-14 up),
+//                     one MMA per K step.
+//       The per-pair results stay in fp32 until the combine.  A value the
+//       stored format cannot hold records MOE_ERR_DEVICE_CHECK.
 // Padding rows (q >= q_limit) are computed by the MMA but never loaded from
 // memory nor stored.
 //
@@ -66,14 +69,16 @@ struct GemmSmem {
 };
 
 // Tile shape: BN output columns per tile (gate/up: BN gate + BN up
-// columns), one activation tile (the gathered x, or act) and B_TILES weight
-// tiles per K slice; as many stages as fit in ~200 KB.
+// columns), A_TILES activation tiles (the gathered x, or act; the hi and lo
+// halves of a split activation) and B_TILES weight tiles per K slice; as
+// many stages as fit in ~200 KB.
 template <int MODE, int BN_>
 struct Cfg {
     static constexpr int BN = BN_;
+    static constexpr int A_TILES = MODE == kDownSplit ? 2 : 1;
     static constexpr int B_TILES = MODE == kGateUp ? 2 : 1;
     static constexpr int B_BYTES = B_TILES * BN * 128;
-    static constexpr int STAGE_BYTES = kATileBytes + B_BYTES;
+    static constexpr int STAGE_BYTES = A_TILES * kATileBytes + B_BYTES;
     static constexpr int STAGES = (200 * 1024 / STAGE_BYTES) < kMaxStages
                                       ? (200 * 1024 / STAGE_BYTES) : kMaxStages;
     static_assert(B_TILES * BN <= kAccCols, "accumulator wider than its TMEM slot");
@@ -89,7 +94,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int BN = C::BN;
     constexpr int kStages = C::STAGES;
     constexpr int kStageBytes = C::STAGE_BYTES;
-    constexpr int kBOffset = kATileBytes;
+    constexpr int kBOffset = C::A_TILES * kATileBytes;
+    constexpr bool kSplit = MODE == kDownSplit;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *tiles = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -172,7 +178,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (src[i] < 0) src[i] = first_valid;  // a real row; its result is dropped
             }
             const uint32_t groups = dense ? 0u : __popc(__ballot_sync(0xffffffffu, any));
-            const uint32_t a_bytes = dense ? kATileBytes : groups * 512;
+            const uint32_t a_bytes = C::A_TILES * (dense ? kATileBytes : groups * 512);
+            const int lo = static_cast<int>(a.lo_rows);  // split: rows of the lo half
             const uint32_t tx = a_bytes + C::B_BYTES;
             const int arow = blk * kBlockM;
             const int brow = static_cast<int>(static_cast<int64_t>(expert) * a.w_rows) + nt * BN;
@@ -194,10 +201,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive_expect_tx(&sm->full[s], tx);
                 __syncwarp();
                 if (dense) {
-                    if (lane == 0) tma_load_2d(st, &tm_a_box, &sm->full[s], kc * kBlockK, arow);
+                    if (lane == 0) {
+                        tma_load_2d(st, &tm_a_box, &sm->full[s], kc * kBlockK, arow);
+                        if (kSplit)
+                            tma_load_2d(st + kATileBytes, &tm_a_box, &sm->full[s], kc * kBlockK,
+                                        arow + lo);
+                    }
                 } else if (any) {
                     tma_gather4(st + lane * 512, &tm_a, &sm->full[s], kc * kBlockK, src[0],
                                 src[1], src[2], src[3]);
+                    if (kSplit)
+                        tma_gather4(st + kATileBytes + lane * 512, &tm_a, &sm->full[s],
+                                    kc * kBlockK, src[0] + lo, src[1] + lo, src[2] + lo,
+                                    src[3] + lo);
                 }
                 if (lane == 0) {
                     if (a.stream_weights) {
@@ -225,9 +241,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             // gate/up: the Wg and Wu tiles sit back to back in shared memory,
             // so one MMA of N = 2 BN produces [gate | up] in the accumulator;
-            // bf16 x bf16.  down: fp16 act x fp16 Wd.
+            // bf16 x bf16.  kDown: fp16 act x fp16 Wd.  kDownSplit: bf16 act
+            // hi x bf16 Wd, then act lo x the same Wd, per K step.
             constexpr uint32_t idesc = MODE == kGateUp ? idesc_bf16_f32(kBlockM, 2 * BN)
-                                                       : idesc_f16_f32(kBlockM, BN);
+                                       : MODE == kDown ? idesc_f16_f32(kBlockM, BN)
+                                                       : idesc_bf16_f32(kBlockM, BN);
             int g = 0, it = 0;
             bool failed = false;
             for (int tile = blockIdx.x; tile < total_tiles && !failed; tile += gridDim.x, ++it) {
@@ -248,11 +266,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after_sync();
                     const uint8_t *st = tiles + s * kStageBytes;
                     const uint64_t da = sw128_kmajor_desc(smem_addr(st));
+                    const uint64_t da_lo = sw128_kmajor_desc(smem_addr(st + kATileBytes));
                     const uint64_t db = sw128_kmajor_desc(smem_addr(st + kBOffset));
 #pragma unroll
                     for (int kk = 0; kk < kBlockK / 16; ++kk) {
                         const uint32_t accumulate = (kc | kk) != 0;
                         mma_f16kind(d, da + 2 * kk, db + 2 * kk, idesc, accumulate);
+                        if (kSplit) mma_f16kind(d, da_lo + 2 * kk, db + 2 * kk, idesc, 1);
                     }
                     mma_commit(&sm->empty[s]);
                 }
@@ -417,6 +437,8 @@ cudaError_t launch_gemm(GemmMode mode, int bn, const CUtensorMap &tm_a,
         return launch_one<kGateUp, 128>(tm_a, tm_a_box, tm_b0, tm_b1, a, s);
     if (mode == kDown && bn == 256)
         return launch_one<kDown, 256>(tm_a, tm_a_box, tm_b0, tm_b1, a, s);
+    if (mode == kDownSplit && bn == 256)
+        return launch_one<kDownSplit, 256>(tm_a, tm_a_box, tm_b0, tm_b1, a, s);
     return cudaErrorInvalidValue;
 }
 

@@ -86,7 +86,14 @@ cudaError_t launch_align(const AlignArgs &a, cudaStream_t s, int *launches);
 
 // ------------------------------------------------------------ grouped GEMM
 
-enum GemmMode { kGateUp = 0, kDown = 1 };
+// kDown multiplies an fp16 activation by fp16 down weights (one MMA per K
+// step); kDownSplit multiplies the activation, held as a bf16 pair
+// hi + lo, by the model's bf16 down weights (two MMAs per K step: hi, then
+// lo, into the same accumulator).  Both keep about 11 or more significant
+// bits of the activation, which the output tolerance needs.
+enum GemmMode { kGateUp = 0, kDown = 1, kDownSplit = 2 };
+
+__host__ __device__ constexpr bool is_down(int mode) { return mode != kGateUp; }
 
 struct GemmArgs {
     // row map: tile row r of block b holds q = sorted_pair[b*128 + r] (or
@@ -100,8 +107,14 @@ struct GemmArgs {
     int K;              // reduction length (H for gate/up, I for down)
     int n_out;          // output columns (I for gate/up, H for down)
     int64_t w_rows;     // weight rows per expert (I or H)
-    uint16_t *out;      // fp16 act [rows, I] (gate/up) or fp16 y [q_limit, H] (down)
+    // gate/up: act [rows, I], fp16, or bf16 hi with the bf16 lo rows lo_rows
+    // rows further on; down: fp32 y [q_limit, H]
+    void *out;
     int64_t out_ld;
+    // 0: fp16 activation.  Otherwise the activation is a bf16 pair: gate/up
+    // stores hi at row r and lo = bf16(a - hi) at row r + lo_rows; the
+    // kDownSplit GEMM reads its A lo rows lo_rows rows after the hi rows.
+    int64_t lo_rows;
     const float *scale; // down: per-q weight (null: 1)
     int32_t *status;
     int stream_weights; // weight tiles read once per call: load them evict-first
@@ -133,8 +146,10 @@ struct GemmArgs {
 // Tile widths: gate/up 96 or 128 columns (of each of gate and up), down 256.
 // The width changes no output element's arithmetic, only the tile count.
 bool gemm_block_n_supported(GemmMode mode, int bn);
-// A operands: x (or x_sorted) rows in bf16 for gate/up, the fp16 activation
-// rows for down.  B operands: Wg / Wu (bf16) for gate/up, Wd (fp16) for down.
+// A operands: x (or x_sorted) rows in bf16 for gate/up, the activation rows
+// for down (fp16, or the bf16 hi rows followed lo_rows later by the lo
+// rows).  B operands: Wg / Wu (bf16) for gate/up, Wd (fp16 for kDown, bf16
+// for kDownSplit) for down.
 // tm_a: 1-row boxes for gather4 of sparse blocks; tm_a_box: 128-row boxes over
 // rows that are contiguous per block; tm_b0 / tm_b1: weight rows, boxes of bn
 // rows.
@@ -168,8 +183,8 @@ cudaError_t launch_pair_gemm(GemmMode mode, const CUtensorMap &tm_a, const CUten
 
 // ----------------------------------------------------------------- combine
 
-cudaError_t launch_combine(const uint16_t *ypair, const uint16_t *yshared, int64_t N, int H,
-                           int k, uint16_t *out, int num_sms, cudaStream_t s);
+cudaError_t launch_combine(const float *ypair, const float *yshared, int64_t N, int H, int k,
+                           uint16_t *out, int num_sms, cudaStream_t s);
 
 // ------------------------------------------- bf16 -> fp16 weight conversion
 

@@ -23,7 +23,10 @@
 //                       even CTA and Wu rows in the odd one, so that N = 256
 //                       spans [gate | up] (32 KB, 6 stages);
 //   down    (BN = 256): 16 KB of fp16 act rows + 16 KB of fp16 Wd rows
-//                       (32 KB, 6 stages), fp16 x fp16 MMAs.
+//                       (32 KB, 6 stages), fp16 x fp16 MMAs (kDown); or
+//                       16 KB of bf16 act hi rows + 16 KB of their lo halves
+//                       + 16 KB of bf16 Wd rows (48 KB, 4 stages), two bf16
+//                       MMAs per K step, hi then lo (kDownSplit).
 //
 // Roles (both CTAs run the same code):
 //   warp 0    producer: its CTA's A rows and weight rows, TMA copies whose
@@ -62,6 +65,7 @@ struct PairCfg<kGateUp> {
     static constexpr int BN = 128;     // gate columns per tile (and as many up columns)
     static constexpr int B_ROWS = BN;  // Wg rows (even CTA) or Wu rows (odd CTA)
     static constexpr int MMA_N = 2 * BN;
+    static constexpr int A_TILES = 1;
     static constexpr int STAGE_BYTES = kATileBytes + B_ROWS * 128;
     static constexpr int STAGES = 6;
 };
@@ -71,8 +75,19 @@ struct PairCfg<kDown> {
     static constexpr int BN = 256;
     static constexpr int B_ROWS = BN / 2;  // this CTA's half of the Wd rows
     static constexpr int MMA_N = BN;
+    static constexpr int A_TILES = 1;
     static constexpr int STAGE_BYTES = kATileBytes + B_ROWS * 128;
     static constexpr int STAGES = 6;
+};
+
+template <>
+struct PairCfg<kDownSplit> {
+    static constexpr int BN = 256;
+    static constexpr int B_ROWS = BN / 2;
+    static constexpr int MMA_N = BN;
+    static constexpr int A_TILES = 2;  // act hi rows, then their lo halves
+    static constexpr int STAGE_BYTES = 2 * kATileBytes + B_ROWS * 128;
+    static constexpr int STAGES = 4;
 };
 
 constexpr int kMaxPairStages = 6;
@@ -200,8 +215,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     constexpr int BN = C::BN;
     constexpr int kStages = C::STAGES;
     constexpr int kStageBytes = C::STAGE_BYTES;
-    constexpr int kBOffset = kATileBytes;
+    constexpr int kBOffset = C::A_TILES * kATileBytes;
     constexpr int kBBytes = C::B_ROWS * 128;
+    constexpr bool kSplit = MODE == kDownSplit;
     constexpr uint32_t kColsPerAcc = C::MMA_N;  // 256 either way
     extern __shared__ uint8_t smem_raw[];
     uint8_t *tiles = reinterpret_cast<uint8_t *>(
@@ -245,7 +261,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     const bool handoff = a.act_ready != nullptr;
     if (!(MODE == kGateUp && handoff)) griddep_launch_dependents();
     // the block list and the A rows come from earlier kernels
-    if (!(MODE == kDown && handoff)) griddep_wait();
+    if (!(is_down(MODE) && handoff)) griddep_wait();
     if (MODE == kGateUp && handoff) griddep_launch_dependents();
 
     // pair prefix over the groups (experts): warp 2 scans, 8 groups per lane
@@ -307,7 +323,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             bool failed = false;
             for (int tile = pair_id; tile < total_tiles && !failed; tile += num_pairs) {
                 const PairTile pt = pair_of(sm, tile / n_tiles, rank);
-                if (MODE == kDown && handoff && pt.rows) {
+                if (is_down(MODE) && handoff && pt.rows) {
                     // this block pair's activation rows are complete once
                     // every gate/up epilogue warp of both CTAs has stored
                     // its rows of every gate/up tile of the pair (bounded)
@@ -321,14 +337,14 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     fence_proxy_async_global();  // the TMA reads below see those rows
                 }
                 const int nt = tile % n_tiles;
-                const uint32_t a_bytes = kATileBytes;
+                const uint32_t a_bytes = C::A_TILES * kATileBytes;
                 const uint32_t tx = 2 * kBBytes +
                                     a_bytes * ((pt.rows ? 1u : 0u) + (pt.peer_rows ? 1u : 0u));
                 const int arow = pt.block * kBlockM;
                 // gate/up: Wg rows (even CTA) or Wu rows (odd CTA) of N tile nt;
                 // down: this CTA's half of the Wd rows of N tile nt
                 const int brow = static_cast<int>(static_cast<int64_t>(pt.group) * a.w_rows) +
-                                 nt * BN + (MODE == kDown ? static_cast<int>(rank) * C::B_ROWS : 0);
+                                 nt * BN + (is_down(MODE) ? static_cast<int>(rank) * C::B_ROWS : 0);
                 const CUtensorMap *tm_b = (MODE == kGateUp && rank == 1) ? &tm_b1 : &tm_b0;
                 for (int kc = 0; kc < nk; ++kc, ++g) {
                     const int s = g % kStages;
@@ -342,7 +358,12 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     uint8_t *st = tiles + s * kStageBytes;
                     const uint32_t bar = cluster_addr(&sm->full[s], 0);
                     if (leader) mbar_arrive_expect_tx(&sm->full[s], tx);
-                    if (pt.rows) tma_load_pair(st, &tm_a, bar, kc * kBlockK, arow);
+                    if (pt.rows) {
+                        tma_load_pair(st, &tm_a, bar, kc * kBlockK, arow);
+                        if (kSplit)
+                            tma_load_pair(st + kATileBytes, &tm_a, bar, kc * kBlockK,
+                                          arow + static_cast<int>(a.lo_rows));
+                    }
                     tma_load_pair(st + kBOffset, tm_b, bar, kc * kBlockK, brow);
                 }
             }
@@ -356,9 +377,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (even CTA)
         if (leader && lane == 0) {
-            // gate/up: bf16 x bf16; down: fp16 act x fp16 Wd
-            constexpr uint32_t idesc = MODE == kGateUp ? idesc_bf16_f32(2 * kBlockM, C::MMA_N)
-                                                       : idesc_f16_f32(2 * kBlockM, C::MMA_N);
+            // gate/up: bf16 x bf16; kDown: fp16 act x fp16 Wd; kDownSplit:
+            // bf16 act hi x bf16 Wd, then act lo x the same Wd, per K step
+            constexpr uint32_t idesc = MODE == kDown ? idesc_f16_f32(2 * kBlockM, C::MMA_N)
+                                                     : idesc_bf16_f32(2 * kBlockM, C::MMA_N);
             int g = 0, it = 0;
             bool failed = false;
             for (int tile = pair_id; tile < total_tiles && !failed; tile += num_pairs, ++it) {
@@ -379,11 +401,13 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     tc_fence_after_sync();
                     const uint8_t *st = tiles + s * kStageBytes;
                     const uint64_t da = sw128_kmajor_desc(smem_addr(st));
+                    const uint64_t da_lo = sw128_kmajor_desc(smem_addr(st + kATileBytes));
                     const uint64_t db = sw128_kmajor_desc(smem_addr(st + kBOffset));
 #pragma unroll
                     for (int kk = 0; kk < kBlockK / 16; ++kk) {
                         const uint32_t accumulate = (kc | kk) != 0;
                         mma_pair(d, da + 2 * kk, db + 2 * kk, idesc, accumulate);
+                        if (kSplit) mma_pair(d, da_lo + 2 * kk, db + 2 * kk, idesc, 1);
                     }
                     commit_pair(&sm->empty[s], 3);
                 }
@@ -479,6 +503,7 @@ cudaError_t launch_pair_one(const CUtensorMap &tm_a, const CUtensorMap &tm_b0,
 
 int pair_gemm_block_n(GemmMode mode) { return mode == kGateUp ? PairCfg<kGateUp>::BN
                                                               : PairCfg<kDown>::BN; }
+static_assert(PairCfg<kDown>::BN == PairCfg<kDownSplit>::BN, "one down tile width");
 
 cudaError_t launch_pair_gemm(GemmMode mode, const CUtensorMap &tm_a, const CUtensorMap &tm_b0,
                              const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s) {
@@ -486,6 +511,7 @@ cudaError_t launch_pair_gemm(GemmMode mode, const CUtensorMap &tm_a, const CUten
     if (a.pad_offsets && (a.num_groups < 1 || a.num_groups > kMaxGroups))
         return cudaErrorInvalidValue;
     if (mode == kGateUp) return launch_pair_one<kGateUp>(tm_a, tm_b0, tm_b1, a, s);
+    if (mode == kDownSplit) return launch_pair_one<kDownSplit>(tm_a, tm_b0, tm_b1, a, s);
     return launch_pair_one<kDown>(tm_a, tm_b0, tm_b1, a, s);
 }
 

@@ -273,6 +273,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// The two bf16 values of a packed pair, widened exactly to fp32.
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t v) {
+    return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+}
+
 // Acquire load at GPU scope (pairs with red_release_gpu in another CTA).
 __device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t *p) {
     int32_t v;

@@ -11,15 +11,19 @@
 // tile), which leaves room for more weight stages:
 //   gate/up BN = 96: 4 KB + 24 KB per stage, 8 stages (192 KB of weights);
 //   gate/up BN = 128: 4 KB + 32 KB, 6 stages (192 KB);
-//   down BN = 256: 4 KB of fp16 act + 32 KB of fp16 Wd, 6 stages (192 KB;
-//   144 KB with 128-row activation tiles).
+//   down BN = 256: 4 KB of act + 32 KB of Wd, 6 stages (192 KB; 144 KB
+//   with 128-row activation tiles).  The fp16 activation (kDown) fills the
+//   4 KB with 32 rows; the bf16 hi/lo activation (kDownSplit) with 16 hi
+//   rows followed by the same 16 rows' lo halves, so its passes hold 16 rows
+//   and the weight bytes in flight stay the same.
 // The MMA is still M = 128: its A operand spans 16 KB from the region's
-// start, so rows 32-127 read whatever follows in the stage; they only feed
-// accumulator rows 32-127, which the epilogue never stores (and TMEM lanes
-// 0-31 belong to the first epilogue warp alone).  A block with more than 32
-// real rows is computed as several 32-row passes over K (rare at decode);
+// start (kDownSplit: from the start of the hi rows, then of the lo rows),
+// so the rows past a pass read whatever follows in the stage; they only
+// feed accumulator rows that the epilogue never stores (and TMEM lanes 0-31
+// belong to the first epilogue warp alone).  A block with more real rows
+// than a pass holds is computed as several passes over K (rare at decode);
 // real rows come first in a block, so a block with n real rows takes
-// ceil(n / 32) passes.
+// ceil(n / rows per pass) passes.
 //
 // The producer publishes each tile's pass count through a small ring of
 // shared-memory words (full/empty barriers per slot), so that the MMA issuer
@@ -46,8 +50,7 @@ namespace moe {
 
 namespace {
 
-constexpr int kSubRows = kSparseRows;          // rows per pass
-constexpr int kSubTileBytes = kSubRows * 128;  // 32 rows x 64 bf16
+constexpr int kSubTileBytes = kSparseRows * 128;  // A region: 32 rows x 64 16-bit values
 constexpr int kSparseMaxStages = 8;
 constexpr int kSparseThreads = 192;
 constexpr int kInfoSlots = 4;
@@ -56,12 +59,18 @@ constexpr int kInfoReaders = 1 + 4;  // MMA warp + four epilogue warps
 template <int MODE, int BN_>
 struct SparseCfg {
     static constexpr int BN = BN_;
+    // rows per pass, and the A copies per row (hi and lo for kDownSplit)
+    static constexpr int SUB_ROWS = MODE == kDownSplit ? kSparseRows / 2 : kSparseRows;
+    static constexpr int A_COPIES = MODE == kDownSplit ? 2 : 1;
+    static constexpr int LO_OFFSET = SUB_ROWS * 128;  // lo rows after the hi rows
     static constexpr int B_BYTES = (MODE == kGateUp ? 2 : 1) * BN * 128;
     static constexpr int STAGE_BYTES = kSubTileBytes + B_BYTES;
     static constexpr int STAGES = (224 * 1024 / STAGE_BYTES) < kSparseMaxStages
                                       ? (224 * 1024 / STAGE_BYTES) : kSparseMaxStages;
     // the MMA reads a 16 KB (128-row) A operand from the A region's start
-    static_assert(STAGE_BYTES >= kATileBytes, "a 128-row A read would leave the stage");
+    // (and, split, from the lo rows' start)
+    static_assert(STAGE_BYTES >= (A_COPIES - 1) * LO_OFFSET + kATileBytes,
+                  "a 128-row A read would leave the stage");
     static_assert(STAGES * STAGE_BYTES + 1024 + 1024 <= 227 * 1024, "shared memory");
     static_assert((MODE == kGateUp ? 2 : 1) * BN <= kAccCols, "accumulator too wide");
 };
@@ -107,6 +116,9 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
     constexpr int kStages = C::STAGES;
     constexpr int kStageBytes = C::STAGE_BYTES;
     constexpr int kBOffset = kSubTileBytes;
+    constexpr int kSubRows = C::SUB_ROWS;
+    constexpr int kLanesPerPass = kSubRows / 4;  // each lane gathers 4 rows
+    constexpr bool kSplit = MODE == kDownSplit;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *tiles = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -170,7 +182,7 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
     }
     // the block list and the A rows come from earlier kernels (with the
     // hand-off, down waits per expert for its A rows instead)
-    if (!(MODE == kDown && handoff)) griddep_wait();
+    if (!(is_down(MODE) && handoff)) griddep_wait();
     if (MODE == kGateUp && handoff) griddep_launch_dependents();
 
     int total_tiles;
@@ -262,8 +274,8 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
                     break;
                 }
             }
-            // a lane's 4 rows sit in sub-block lane / 8; padding rows copy a
-            // real row of the same group (their results are dropped)
+            // a lane's 4 rows sit in pass lane / kLanesPerPass; padding rows
+            // copy a real row of the same group (their results are dropped)
             int first_valid = -1;
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -272,10 +284,11 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
             for (int i = 0; i < 4; ++i)
                 if (src[i] < 0) src[i] = first_valid;
             const int brow = static_cast<int>(static_cast<int64_t>(expert) * a.w_rows) + nt * BN;
-            if (MODE == kDown && handoff && passes > 0) {
+            if (is_down(MODE) && handoff && passes > 0) {
                 // this expert's activation rows are complete once all its
                 // gate/up tiles are stored (bounded wait by lane 0; the warp
-                // barrier orders the other lanes' TMA copies after it)
+                // barrier after it orders the other lanes' accesses, and each
+                // lane's proxy fence its own TMA copies, after that acquire)
                 bool ready = false;
                 if (lane == 0)
                     ready = wait_count_ns(a.act_ready + expert, a.act_ready_count, abort_flag,
@@ -289,12 +302,14 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
                     failed = true;
                     break;
                 }
+                __syncwarp();
                 fence_proxy_async_global();  // the TMA reads below see those rows
             }
             for (int p = 0; p < passes && !failed; ++p) {
-                const bool mine = lane / 8 == p && any;  // lanes 8p .. 8p+7 gather pass p
+                // lanes kLanesPerPass * p .. kLanesPerPass * (p + 1) - 1 gather pass p
+                const bool mine = lane / kLanesPerPass == p && any;
                 const uint32_t groups = __popc(__ballot_sync(0xffffffffu, mine));
-                const uint32_t tx = groups * 512 + C::B_BYTES;
+                const uint32_t tx = groups * 512 * C::A_COPIES + C::B_BYTES;
                 for (int kc = 0; kc < nk; ++kc, ++g) {
                     const int s = g % kStages;
                     const uint32_t use = g / kStages;
@@ -313,9 +328,15 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
                     if (lane == 0) mbar_arrive_expect_tx(&sm->full[s], tx);
                     __syncwarp();
                     if (mine) {
-                        const int slot = lane % 8;
+                        const int slot = lane % kLanesPerPass;
                         tma_gather4(st + slot * 512, &tm_a, &sm->full[s], kc * kBlockK, src[0],
                                     src[1], src[2], src[3]);
+                        if (kSplit) {
+                            const int lo = static_cast<int>(a.lo_rows);
+                            tma_gather4(st + C::LO_OFFSET + slot * 512, &tm_a, &sm->full[s],
+                                        kc * kBlockK, src[0] + lo, src[1] + lo, src[2] + lo,
+                                        src[3] + lo);
+                        }
                     }
                     if (lane == 0) {
                         if (a.stream_weights) {
@@ -341,9 +362,11 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (1 thread)
         // gate/up: Wg and Wu tiles are adjacent, one bf16 MMA of N = 2 BN;
-        // down: fp16 act x fp16 Wd
+        // kDown: fp16 act x fp16 Wd; kDownSplit: bf16 act hi x bf16 Wd, then
+        // act lo x the same Wd, per K step
         constexpr uint32_t idesc = MODE == kGateUp ? idesc_bf16_f32(kBlockM, 2 * BN)
-                                                   : idesc_f16_f32(kBlockM, BN);
+                                   : MODE == kDown ? idesc_f16_f32(kBlockM, BN)
+                                                   : idesc_bf16_f32(kBlockM, BN);
         int g = 0, it = 0;
         bool failed = false;
         for (int tile = blockIdx.x, j = 0; tile < total_tiles && !failed; tile += gridDim.x, ++j) {
@@ -370,10 +393,12 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
                             tc_fence_after_sync();
                             const uint8_t *st = tiles + s * kStageBytes;
                             const uint64_t da = sw128_kmajor_desc(smem_addr(st));
+                            const uint64_t da_lo = sw128_kmajor_desc(smem_addr(st + C::LO_OFFSET));
                             const uint64_t db = sw128_kmajor_desc(smem_addr(st + kBOffset));
 #pragma unroll
                             for (int kk = 0; kk < kBlockK / 16; ++kk) {
                                 mma_f16kind(d, da + 2 * kk, db + 2 * kk, idesc, (kc | kk) != 0);
+                                if (kSplit) mma_f16kind(d, da_lo + 2 * kk, db + 2 * kk, idesc, 1);
                             }
                             mma_commit(&sm->empty[s]);
                         }
@@ -408,8 +433,9 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
             }
             for (int p = 0; p < passes; ++p, ++it) {
                 const int acc = it & 1;
-                TileRow r = {};
-                if (quarter == 0) r = tile_row<MODE>(a, block_of(tile), p * kSubRows + lane);
+                TileRow r = no_tile_row();
+                if (quarter == 0 && lane < kSubRows)
+                    r = tile_row<MODE>(a, block_of(tile), p * kSubRows + lane);
                 bool ok = true;
                 if (lane == 0) ok = mbar_wait(&sm->acc_full[acc], (it >> 1) & 1, abort_flag);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -465,6 +491,8 @@ cudaError_t launch_sparse_gemm(GemmMode mode, int bn, const CUtensorMap &tm_a,
     if (mode == kGateUp && bn == 96) return launch_sparse_one<kGateUp, 96>(tm_a, tm_b0, tm_b1, a, s);
     if (mode == kGateUp && bn == 128) return launch_sparse_one<kGateUp, 128>(tm_a, tm_b0, tm_b1, a, s);
     if (mode == kDown && bn == 256) return launch_sparse_one<kDown, 256>(tm_a, tm_b0, tm_b1, a, s);
+    if (mode == kDownSplit && bn == 256)
+        return launch_sparse_one<kDownSplit, 256>(tm_a, tm_b0, tm_b1, a, s);
     return cudaErrorInvalidValue;
 }
 

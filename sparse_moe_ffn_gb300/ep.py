@@ -14,7 +14,7 @@ and holds only their weights.  Per layer call, on every rank:
 3. dispatch: each pair's token row, its expert id local to the receiving
    rank and its routing weight travel with one all_to_all each;
 4. the receiving rank runs its experts on the rows it received
-   (moe_experts: y = fp16(w * Expert(x)));
+   (moe_experts: y = w * Expert(x) in fp32);
 5. combine: the results travel back with the reverse all_to_all and land in
    pair order (ypair[p]).  moe_combine then sums each token's k slots in slot
    order.
@@ -26,10 +26,10 @@ bit, whatever the number of ranks.
 The shared expert (the talker layer) is dense: every rank holds its weights
 and applies it to its own tokens, with no exchange.  It runs as moe_experts
 with one expert, every row routed to it and the sigmoid gate as the row
-weight, which is moe_forward's shared term fp16(gamma * SharedMLP(x)); the
+weight, which is moe_forward's shared term gamma * SharedMLP(x) in fp32; the
 combine adds it after the k slots.
 
-Transport: gloo and NCCL both carry int32, so bf16 and fp16 rows travel as
+Transport: gloo and NCCL both carry int32, so bf16 and fp32 rows travel as
 their bit patterns viewed as int32 (H is even).  With one rank nothing is
 exchanged.  The three compute steps can be replaced (route_fn, experts_fn,
 combine_fn), which is how the exchange logic is tested on CPU ranks.
@@ -81,11 +81,12 @@ def ep_forward(x, router, w_gate, w_up, w_down, E: int, k: int, norm_topk_prob: 
     """One MoE layer with experts split across the ranks of ``group``.
 
     x [N, H] bf16 (this rank's tokens), router [E, H] bf16 (all experts);
-    w_gate, w_up [E_r, I, H] bf16 and w_down [E_r, H, I] fp16 (see
-    binding.prepare_weights): this rank's experts.  ``shared``: None or the
-    shared expert (binding.SHARED_KEYS, shared_down_proj in fp16), the same
-    on every rank.  route_fn(x) returns (weights, ids) or (weights, ids,
-    gamma); shared_fn(x, gamma) returns the fp16 shared term.
+    w_gate, w_up [E_r, I, H] bf16 and w_down [E_r, H, I] (bf16, or the fp16
+    copy of binding.prepare_weights): this rank's experts.  ``shared``: None
+    or the shared expert (binding.SHARED_KEYS, shared_down_proj in the same
+    form as w_down), the same on every rank.  route_fn(x) returns (weights,
+    ids) or (weights, ids, gamma); shared_fn(x, gamma) returns the fp32
+    shared term.
     Returns out [N, H] bf16."""
     from sparse_moe_ffn_gb300 import binding
 
@@ -137,8 +138,8 @@ def ep_forward(x, router, w_gate, w_up, w_down, E: int, k: int, norm_topk_prob: 
         y_back = y
     else:
         y_back = _exchange(y.view(torch.int32), recv_list, send_list,
-                           group).view(torch.float16)
-    ypair = torch.empty((N * k, H), dtype=torch.float16, device=x.device)
+                           group).view(torch.float32)
+    ypair = torch.empty((N * k, H), dtype=torch.float32, device=x.device)
     ypair[order] = y_back
     if yshared is None:
         return combine_fn(ypair, N, k)

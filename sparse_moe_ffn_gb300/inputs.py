@@ -175,6 +175,29 @@ def make_inputs(shape: MoEShape, seed: int = 0, margin: float = MARGIN,
     return out
 
 
+def make_tokens(shape: MoEShape, router: torch.Tensor, n: int, seed: int,
+                margin: float = MARGIN, max_redraws: int = 1000) -> torch.Tensor:
+    """Fresh activations for one step of a decode loop over a layer whose
+    router is already drawn: x ~ N(0, 1) of shape [n, H] from a generator
+    seeded with ``seed``, the skew bias channel when ``shape.skew``, rounded
+    to bf16, with near-tie rows (against ``router``, bf16 [E, H]) redrawn as
+    in ``make_inputs``.  Returns a bf16 CPU tensor."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    x = _normal(g, (n, shape.H), 1.0)
+    _apply_skew_x(x, shape)
+    xb = _bf16(x)
+    router_b = router.to("cpu", torch.bfloat16)
+    for _ in range(max_redraws):
+        bad = _near_tie_rows(xb, router_b, shape.k, margin)
+        if bad.numel() == 0:
+            return xb
+        fresh = _normal(g, (bad.numel(), shape.H), 1.0)
+        _apply_skew_x(fresh, shape)
+        xb[bad] = _bf16(fresh)
+    raise RuntimeError(f"{shape.name}: near-tie rows remain after {max_redraws} redraws")
+
+
 def to_device(inputs: dict, device="cuda") -> dict:
     """Move inputs to ``device``; fp32 tensors are cast to bf16 there."""
     dev = {}

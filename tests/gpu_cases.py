@@ -1,9 +1,14 @@
 """Shared helpers of the GPU parity tests: seeded inputs on the device, their
-exact bf16 bits for the oracle, and the output tolerance.
+exact bf16 bits for the oracle, the oracle's full outputs (computed once per
+configuration), and the output tolerance.
 
 Output tolerance (bf16 outputs against the fp64 oracle), per token batch:
     max |out - ref| <= 2e-2 * rms(ref)   and   mean|out - ref| / mean|ref| <= 5e-3
 where rms(ref) = sqrt(mean(ref^2)) over every compared element.
+
+The layer runs with the model's bf16 down weights ("bf16": moe_forward, hi/lo
+activation) or with their fp16 copies ("f16": moe_forward_prepared); FORMS
+lists both, and the tests that hold for either run for both.
 """
 from __future__ import annotations
 
@@ -23,21 +28,48 @@ MEAN_REL_ERR = 5e-3
 WEIGHT_ATOL = 2e-5
 
 
+FORMS = ("bf16", "f16")
+ALL = ("tiny", "decode", "prefill", "talker", "skewed")
+
+
+@functools.lru_cache(maxsize=16)
+def prepared(name: str, seed: int = 0, form: str = "bf16"):
+    """(shape, device tensors, oracle bit arrays) of a named configuration;
+    form "f16" gives the down projections as their fp16 copies."""
+    shape, dev, bits = _prepared_bf16(name, seed)
+    return shape, with_form(dev, form), bits
+
+
 @functools.lru_cache(maxsize=5)
-def prepared(name: str, seed: int = 0):
-    """(shape, device tensors, oracle bit arrays) of a named configuration."""
+def _prepared_bf16(name: str, seed: int):
     return prepare(CONFIGS[name], seed)
 
 
-def prepare(shape: MoEShape, seed: int = 0):
+def prepare(shape: MoEShape, seed: int = 0, form: str = "bf16"):
     cpu = make_inputs(shape, seed)
     dev = to_device(cpu, "cuda")
     if shape.cast_on_gpu:
         bits = {n: oracle.bf16_bits(t) for n, t in dev.items()}  # the GPU's cast
     else:
         bits = {n: oracle.bf16_bits(t) for n, t in cpu.items()}
-    # the oracle takes the model's bf16 weights; the library its fp16 down weights
-    return shape, binding.prepare_weights(dev), bits
+    # the oracle takes the model's bf16 weights, as does moe_forward
+    return shape, with_form(dev, form), bits
+
+
+def with_form(dev: dict, form: str) -> dict:
+    """The device tensors with the down projections in the given form."""
+    if form == "bf16":
+        return dev
+    if form == "f16":
+        return binding.prepare_weights(dev)
+    raise ValueError(form)
+
+
+@functools.lru_cache(maxsize=5)
+def oracle_outputs(name: str, seed: int = 0) -> np.ndarray:
+    """The oracle's output for every token of a named configuration (fp64)."""
+    shape, _, bits = _prepared_bf16(name, seed)
+    return oracle.moe_forward(bits, shape.k, shape.norm_topk_prob)
 
 
 def shared_of(shape, dev):

@@ -2,6 +2,7 @@
 every entry point include/moe.h declares, sizes workspaces consistently, and
 rejects bad arguments before touching the device."""
 import ctypes
+import functools
 import os
 import re
 
@@ -50,35 +51,39 @@ def test_layout_is_consistent(L):
         N, H, E, I, k, _ = args
         cap = lay["capacity"]
         assert cap == L.moe_align_capacity(N, k, E, 128)
-        assert lay["ypair"] >= lay["act"] + 2 * cap * I
-        assert lay["total"] >= lay["ypair"] + 2 * N * k * H
+        assert lay["ypair"] >= lay["act"] + 4 * cap * I          # bf16 hi/lo or fp16 act
+        assert lay["total"] >= lay["ypair"] + 4 * N * k * H      # fp32 pair outputs
 
 
 def _fwd(L, N=64, H=2048, E=128, I=768, I_s=0, k=8, ws_bytes=None, shared=(None,) * 4,
-         x=FAKE, ws=FAKE * 16):
+         x=FAKE, ws=FAKE * 16, prepared=False):
     if ws_bytes is None:
         ws_bytes = L.moe_forward_workspace_bytes(N, H, E, I, k, I_s)
-    return L.moe_forward(x, FAKE, FAKE, FAKE, FAKE, *shared, N, H, E, I, I_s, k, 1, FAKE,
-                         ws, ws_bytes, None)
+    fn = L.moe_forward_prepared if prepared else L.moe_forward
+    return fn(x, FAKE, FAKE, FAKE, FAKE, *shared, N, H, E, I, I_s, k, 1, FAKE, ws, ws_bytes,
+              None)
 
 
-def test_forward_argument_errors(L):
-    assert _fwd(L, k=0) == INVALID
-    assert _fwd(L, k=129) == INVALID
-    assert _fwd(L, H=2044) == INVALID
-    assert _fwd(L, I=770) == INVALID
-    assert _fwd(L, N=-1) == INVALID
-    assert _fwd(L, x=None) == INVALID
-    assert _fwd(L, x=FAKE + 2) == INVALID          # misaligned bf16 matrix
-    assert _fwd(L, ws=FAKE + 64) == INVALID        # workspace not 256-byte aligned
-    assert _fwd(L, E=300, k=8) == UNSUPPORTED
-    assert _fwd(L, shared=(FAKE, None, None, None), I_s=64) == INVALID
-    assert _fwd(L, shared=(FAKE,) * 4, I_s=60) == INVALID
-    assert _fwd(L, E=256, shared=(FAKE,) * 4, I_s=64) == UNSUPPORTED
+@pytest.mark.parametrize("prepared", [False, True])
+def test_forward_argument_errors(L, prepared):
+    fwd = functools.partial(_fwd, prepared=prepared)  # both entry points share every check
+    assert fwd(L, k=0) == INVALID
+    assert fwd(L, k=129) == INVALID
+    assert fwd(L, H=2044) == INVALID
+    assert fwd(L, I=770) == INVALID
+    assert fwd(L, N=-1) == INVALID
+    assert fwd(L, x=None) == INVALID
+    assert fwd(L, x=FAKE + 2) == INVALID          # misaligned bf16 matrix
+    assert fwd(L, ws=FAKE + 64) == INVALID        # workspace not 256-byte aligned
+    assert fwd(L, E=300, k=8) == UNSUPPORTED
+    assert fwd(L, shared=(FAKE, None, None, None), I_s=64) == INVALID
+    assert fwd(L, shared=(FAKE,) * 4, I_s=60) == INVALID
+    assert fwd(L, E=256, shared=(FAKE,) * 4, I_s=64) == UNSUPPORTED
     need = L.moe_forward_workspace_bytes(64, 2048, 128, 768, 8, 0)
-    assert _fwd(L, ws_bytes=need - 1) == SMALL
+    assert fwd(L, ws_bytes=need - 1) == SMALL
     assert b"needs" in L.moe_last_error()
-    assert _fwd(L, N=0) == OK                      # no-op, nothing launched
+    assert fwd(L, N=0) == OK                      # no-op, nothing launched
+    assert fwd(L, N=1 << 27, k=8) == UNSUPPORTED  # N*k + E*128 beyond 2^30
 
 
 def _fwd_host(L, N=64, H=2048, E=128, I=768, k=8, x_host=FAKE, out_host=FAKE, x_dev=FAKE,
@@ -99,32 +104,47 @@ def test_forward_host_argument_errors(L):
 
 
 def _experts(L, R=64, H=2048, E=16, I=768, x=FAKE, ids=FAKE, y=FAKE, ws=FAKE * 16,
-             ws_bytes=None):
+             ws_bytes=None, prepared=False):
     if ws_bytes is None:
         ws_bytes = L.moe_experts_workspace_bytes(R, H, E, I)
-    return L.moe_experts(x, ids, FAKE, R, H, E, I, FAKE, FAKE, FAKE, y, ws, ws_bytes, None)
+    fn = L.moe_experts_prepared if prepared else L.moe_experts
+    return fn(x, ids, FAKE, R, H, E, I, FAKE, FAKE, FAKE, y, ws, ws_bytes, None)
 
 
-def test_experts_and_combine_argument_errors(L):
+@pytest.mark.parametrize("prepared", [False, True])
+def test_experts_and_combine_argument_errors(L, prepared):
+    experts = functools.partial(_experts, prepared=prepared)
+
     # the expert-parallel receiving side: one routed row per (row, expert)
     assert L.moe_experts_workspace_bytes(64, 2048, 16, 768) == \
         L.moe_forward_workspace_bytes(64, 2048, 16, 768, 1, 0)
-    assert _experts(L, R=-1) == INVALID
-    assert _experts(L, H=2044) == INVALID
-    assert _experts(L, I=0) == INVALID
-    assert _experts(L, E=0) == UNSUPPORTED
-    assert _experts(L, ids=None) == INVALID
-    assert _experts(L, y=FAKE + 2) == INVALID
-    assert _experts(L, ws=FAKE + 64) == INVALID
+    assert experts(L, R=-1) == INVALID
+    assert experts(L, H=2044) == INVALID
+    assert experts(L, I=0) == INVALID
+    assert experts(L, E=0) == UNSUPPORTED
+    assert experts(L, ids=None) == INVALID
+    assert experts(L, y=FAKE + 2) == INVALID
+    assert experts(L, ws=FAKE + 64) == INVALID
     need = L.moe_experts_workspace_bytes(64, 2048, 16, 768)
-    assert _experts(L, ws_bytes=need - 1) == SMALL
-    assert _experts(L, R=0, x=None) == OK          # no-op, nothing launched
+    assert experts(L, ws_bytes=need - 1) == SMALL
+    assert experts(L, R=0, x=None) == OK          # no-op, nothing launched
     P = FAKE
     assert L.moe_combine(P, None, 16, 2048, 0, P, None) == INVALID
     assert L.moe_combine(P, None, 16, 2044, 2, P, None) == INVALID
     assert L.moe_combine(None, None, 16, 2048, 2, P, None) == INVALID
     assert L.moe_combine(P, P + 2, 16, 2048, 2, P, None) == INVALID
     assert L.moe_combine(P, None, 0, 2048, 2, None, None) == OK
+
+
+def test_dense_mlp_argument_errors(L):
+    P = FAKE
+    need = L.moe_dense_mlp_workspace_bytes(300, 256, 192)
+    for fn in (L.moe_dense_mlp, L.moe_dense_mlp_prepared):
+        assert fn(P, P, P, P, 300, 250, 192, P, P * 16, need, None) == INVALID   # H % 8
+        assert fn(P, P, P, None, 300, 256, 192, P, P * 16, need, None) == INVALID
+        assert fn(P, P, P, P, 300, 256, 192, P, P * 16 + 64, need, None) == INVALID
+        assert fn(P, P, P, P, 300, 256, 192, P, P * 16, need - 1, None) == SMALL
+        assert fn(None, None, None, None, 0, 256, 192, None, None, 0, None) == OK
 
 
 def test_convert_argument_errors(L):

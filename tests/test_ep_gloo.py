@@ -23,7 +23,7 @@ def _free_port():
 
 def _pair_value(row, e, w):
     """Stand-in for w * Expert_e(row): any function of all three inputs."""
-    return (w * (row.float() * (e + 1) + e)).to(torch.float16)
+    return (w * (row.float() * (e + 1) + e)).to(torch.float32)
 
 
 def _combine(ypair, n, k, yshared=None):
@@ -34,8 +34,8 @@ def _combine(ypair, n, k, yshared=None):
 
 
 def _shared_value(x, gamma):
-    """Stand-in for fp16(gamma * SharedMLP(x)), token-local."""
-    return (gamma[:, None] * (0.5 * x.float() - 1.0)).to(torch.float16)
+    """Stand-in for gamma * SharedMLP(x) (fp32), token-local."""
+    return (gamma[:, None] * (0.5 * x.float() - 1.0)).to(torch.float32)
 
 
 def _inputs(rank, N, H, E, k, all_to_rank0):
@@ -67,7 +67,7 @@ def _worker(rank, world, port, q, N, H, E, k, all_to_rank0, with_shared=False):
             ge = local_ids.long() + rank * E_local
             return torch.stack([_pair_value(rows[i], int(ge[i]), float(weights[i]))
                                 for i in range(rows.shape[0])]) if rows.shape[0] else \
-                torch.empty((0, H), dtype=torch.float16)
+                torch.empty((0, H), dtype=torch.float32)
 
         gamma = torch.sigmoid(x.float()[:, 0]) if with_shared else None
         out = ep_forward(x, None, None, None, None, E, k, group=None,

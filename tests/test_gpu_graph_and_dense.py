@@ -5,9 +5,9 @@ import pytest
 import torch
 
 import oracle
-from gpu_cases import assert_close, prepare, prepared
+from gpu_cases import FORMS, assert_close, prepare, prepared
 from sparse_moe_ffn_gb300 import binding
-from sparse_moe_ffn_gb300.inputs import MoEShape, make_inputs
+from sparse_moe_ffn_gb300.inputs import MoEShape, make_inputs, make_tokens
 
 pytestmark = pytest.mark.gpu
 
@@ -29,11 +29,12 @@ def test_graph_replay_matches_eager(name):
         assert torch.equal(got, _eager(shape, dev, x)), f"seed {seed}"
 
 
+@pytest.mark.parametrize("form", FORMS)
 @pytest.mark.parametrize("name", ["decode", "talker"])
-def test_forward_host_buffers_match_device_call(name):
+def test_forward_host_buffers_match_device_call(name, form):
     """moe_forward_host (pinned host x in, pinned host out) equals the device
     call bit for bit."""
-    shape, dev, _ = prepared(name)
+    shape, dev, _ = prepared(name, form=form)
     weights = {n: t for n, t in dev.items() if n != "x"}
     x_host = dev["x"].cpu().pin_memory()
     out_host = torch.empty_like(x_host).pin_memory()
@@ -46,6 +47,31 @@ def test_forward_host_buffers_match_device_call(name):
     assert torch.equal(out_host, _eager(shape, dev, dev["x"]).cpu())
 
 
+@pytest.mark.parametrize("form", FORMS)
+def test_graph_set_decode_loop_matches_oracle(form):
+    """A multi-step decode loop under CUDA-graph replay: ten steps whose batch
+    sizes change from step to step (buckets 1, 4, 8, 32, 64 and 128 among
+    the captured 1, 2, 4, ... 128), each with fresh activations, every step's
+    output against the oracle over all its tokens and against an eager call
+    bit for bit."""
+    shape, dev, bits = prepared("decode", form=form)
+    weights = {n: t for n, t in dev.items() if n != "x"}
+    graphs = binding.ForwardGraphSet(weights, shape.k, shape.norm_topk_prob)
+    assert graphs.buckets == (1, 2, 4, 8, 16, 32, 64, 128)
+    sizes = [1, 3, 64, 8, 27, 128, 5, 64, 33, 2]
+    steps = [make_tokens(shape, dev["router"], n, seed=100 + i).cuda()
+             for i, n in enumerate(sizes)]
+    outs = binding.decode_loop(graphs, steps)
+    used = {graphs.bucket_of(n) for n in sizes}
+    assert len(used) >= 5, used
+    for i, (x, out) in enumerate(zip(steps, outs)):
+        assert out.shape == x.shape
+        step_bits = dict(bits, x=oracle.bf16_bits(x))
+        ref = oracle.moe_forward(step_bits, shape.k, shape.norm_topk_prob)
+        assert_close(out, ref, f"step {i} (n={x.shape[0]}, {form})")
+        assert torch.equal(out, _eager(shape, dev, x)), f"step {i}"
+
+
 def test_graph_bucket_padding_is_exact():
     shape, dev, _ = prepared("decode")
     weights = {n: t for n, t in dev.items() if n != "x"}
@@ -54,13 +80,13 @@ def test_graph_bucket_padding_is_exact():
     assert torch.equal(g(x), _eager(shape, dev, x))
 
 
+@pytest.mark.parametrize("form", FORMS)
 @pytest.mark.parametrize("N,H,I", [(300, 256, 192), (1, 128, 64), (129, 64, 200), (2048, 2048, 768)])
-def test_dense_mlp_matches_oracle(N, H, I):
-    shape, dev, bits = prepare(MoEShape("dense", N=N, H=H, E=1, k=1, I=I), seed=5)
+def test_dense_mlp_matches_oracle(N, H, I, form):
+    shape, dev, bits = prepare(MoEShape("dense", N=N, H=H, E=1, k=1, I=I), seed=5, form=form)
     out = binding.moe_dense_mlp(dev["x"], dev["w_gate"][0], dev["w_up"][0], dev["w_down"][0])
-    rows = np.arange(0, N, max(1, N // 256), dtype=np.int64)
-    ref = oracle.moe_forward(bits, 1, True, rows=rows)  # E = k = 1: the dense MLP
-    assert_close(out[torch.from_numpy(rows).cuda()], ref, f"dense N={N}")
+    ref = oracle.moe_forward(bits, 1, True)  # E = k = 1: the dense MLP
+    assert_close(out, ref, f"dense N={N} ({form})")
     # and it agrees with the layer's own E = k = 1 path bit for bit
     assert torch.equal(out, _eager(shape, dev, dev["x"]))
 

@@ -65,3 +65,18 @@ def test_prefill_router_is_near_uniform():
     counts = np.bincount(ids.reshape(-1), minlength=shp.E)
     mean = shp.pairs / shp.E
     assert counts.min() > 0.5 * mean and counts.max() < 1.6 * mean, (counts.min(), counts.max())
+
+
+def test_make_tokens_fresh_rows_without_near_ties():
+    """Fresh decode-step activations: seeded, bf16, the requested shape, and
+    no near-tie among each row's k+1 largest logits against the given router."""
+    from sparse_moe_ffn_gb300.inputs import MARGIN, make_tokens
+    shape = CONFIGS["decode"].with_tokens(4)
+    router = make_inputs(shape, seed=0)["router"]
+    a = make_tokens(shape, router, 37, seed=5)
+    b = make_tokens(shape, router, 37, seed=5)
+    assert a.dtype == torch.bfloat16 and a.shape == (37, shape.H)
+    assert torch.equal(a, b)
+    assert not torch.equal(a, make_tokens(shape, router, 37, seed=6))
+    top = torch.topk(a.double() @ router.double().T, shape.k + 1, dim=1).values
+    assert float((top[:, :-1] - top[:, 1:]).min()) >= MARGIN

@@ -47,3 +47,24 @@ def test_two_gloo_ranks_take_the_max():
     assert all(p.exitcode == 0 for p in procs), [p.exitcode for p in procs]
     got = dict(q.get(timeout=5) for _ in range(world))
     assert got == {0: 11.0, 1: 11.0}
+
+
+def test_bench_gpus_2_starts_two_ranks():
+    """`bench.py --gpus 2` without a torchrun environment starts the two
+    ranks itself (torch.distributed.run, gloo on CPU for the reference arm);
+    rank 0 alone prints one line, for the whole job."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2",
+                        "--impl", "reference", "--config", "tiny", "--steps", "1",
+                        "--warmup", "3"], capture_output=True, text=True, timeout=600, env=env,
+                       cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["n_gpus"] == 2

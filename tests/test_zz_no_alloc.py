@@ -13,7 +13,7 @@ import torch
 from sparse_moe_ffn_gb300 import binding
 from sparse_moe_ffn_gb300 import build as lib_build
 
-MOE_OK, MOE_ERR_UNSUPPORTED = 0, 3
+MOE_OK, MOE_ERR_UNSUPPORTED, MOE_ERR_DEVICE_CHECK = 0, 3, 5
 
 
 def _lib():
@@ -52,9 +52,13 @@ def _call_noalloc(L, ids, E, block_m):
 
 @pytest.mark.gpu
 def test_noalloc_matches_moe_align_on_two_calls_in_a_row():
+    """Three-kernel grouping (more than 4096 pairs) and the single-CTA one
+    (decode-sized: 64 tokens x 8 slots over 128 experts), each run twice in a
+    row through the shared static scratch."""
     L = _lib()
     rng = np.random.default_rng(2024)
-    for N, k, E, block_m in [(3000, 8, 128, 128), (700, 6, 64, 16)]:
+    for N, k, E, block_m in [(3000, 8, 128, 128), (700, 6, 64, 16), (3000, 8, 128, 128),
+                             (64, 8, 128, 128), (64, 8, 128, 128)]:
         ids_np = rng.integers(0, E, size=(N, k)).astype(np.int32)
         ids_np[ids_np == 5] = 6  # one expert without pairs
         ids = torch.from_numpy(ids_np).cuda()
@@ -69,3 +73,25 @@ def test_noalloc_matches_moe_align_on_two_calls_in_a_row():
         assert torch.equal(got["sorted_pair"][:npad], ref["sorted_pair"][:npad])
         assert torch.equal(got["block_expert"][:npad // block_m],
                            ref["block_expert"][:npad // block_m])
+
+
+@pytest.mark.gpu
+def test_noalloc_reports_bad_ids_and_zero_tokens():
+    """An id outside [0, E) is skipped and reported through device_status,
+    on both grouping paths; the next call (N = 0 included) reports 0 again."""
+    L = _lib()
+    for N, k, E in [(64, 8, 128), (1000, 8, 128)]:
+        ids = torch.randint(0, E, (N, k), dtype=torch.int32).cuda()
+        ids[3, 2] = E + 5
+        got = _call_noalloc(L, ids, E, 128)
+        torch.cuda.synchronize()
+        assert int(got["status"].item()) == MOE_ERR_DEVICE_CHECK
+        assert int(got["counts"].sum().item()) == N * k - 1
+        ids[3, 2] = 0
+        got = _call_noalloc(L, ids, E, 128)
+        torch.cuda.synchronize()
+        assert int(got["status"].item()) == 0
+    empty = torch.empty((0, 8), dtype=torch.int32, device="cuda")
+    got = _call_noalloc(L, empty, 128, 128)
+    torch.cuda.synchronize()
+    assert int(got["status"].item()) == 0  # written, not left at the -7 it held
