@@ -333,6 +333,8 @@ def run_ours(args, world, rank, local):
     # model load: the model's bf16 weights to the device (moe_forward takes
     # them as they are)
     d = to_device(cpu, device)
+    if args.down_weights == "f16":  # informational runs of moe_forward_prepared
+        d = binding.prepare_weights(d)
     shared = {n: d[n] for n in binding.SHARED_KEYS} if shape.I_s else None
     ws = binding.alloc_workspace(shape.N, shape.H, shape.E, shape.I, shape.k, shape.I_s, device)
     out = torch.empty((shape.N, shape.H), dtype=torch.bfloat16, device=device)
@@ -519,7 +521,8 @@ def run_ours(args, world, rank, local):
                          "inputs smaller than L2 (not flushed: latency-bound case)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "tflops": round(tflops, 2),
-        "entry": "moe_forward (bf16 weights, as the layer is defined)",
+        "entry": ("moe_forward (bf16 weights, as the layer is defined)" if args.down_weights ==
+                  "bf16" else "moe_forward_prepared (fp16 down weights made once at load)"),
         "prepared_down_weights": prepared_rec,
         "graph_replay": graph_rec,
         "stage_ms_warmup_probe": {s: round(v, 5) for s, v in probe_ms.items()},
@@ -604,6 +607,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill-steps", type=int, default=50)
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--down-weights", default="bf16", choices=["bf16", "f16"],
+                    help="form of the down weights of the timed steps: the model's bf16 "
+                         "(moe_forward) or fp16 copies made at load (moe_forward_prepared)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

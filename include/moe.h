@@ -196,8 +196,10 @@ moe_status_t moe_align_noalloc(const int32_t *topk_ids, int64_t N, int k, int E,
  * activation a = silu(g)*u is kept as the bf16 pair hi = bf16(a),
  * lo = bf16(a - hi) (16 significant bits) and both halves are multiplied by
  * the bf16 down weights; each pair's weighted down projection (and the
- * gated shared expert) is kept in fp32; the k contributions and the shared
- * term are summed in fp32 in slot order, and out is rounded to bf16 once.
+ * gated shared expert) is accumulated in fp32 and kept as a pair row (see
+ * "Pair rows" below: 16 significant bits in 3 bytes); the k contributions
+ * and the shared term are summed in fp32 in slot order, and out is rounded
+ * to bf16 once.
  * A non-finite activation or pair output records MOE_ERR_DEVICE_CHECK.
  * The result does not depend on the other tokens of the batch and is
  * bitwise reproducible.
@@ -222,7 +224,7 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router,
  * do not have).  The activation is then kept in fp16 (11 significant bits)
  * and multiplied by the fp16 weights with one MMA per K step instead of two,
  * which halves the down GEMM's tensor work at large N.  Everything else --
- * arguments, workspace, routing, fp32 pair outputs, slot-order fp32 combine,
+ * arguments, workspace, routing, pair rows, slot-order fp32 combine,
  * limits, errors -- is moe_forward's.  The outputs differ from moe_forward's
  * by the activation's rounding (both stay within the layer's tolerance).
  * ---------------------------------------------------------------------- */
@@ -238,11 +240,23 @@ moe_status_t moe_forward_prepared(const moe_bf16_t *x, const moe_bf16_t *router,
                                   size_t workspace_bytes, cudaStream_t stream);
 
 /* -------------------------------------------------------------------------
+ * Pair rows -- how the weighted per-pair outputs v = w * Expert(x) are held
+ * between the down projection and the combine (moe_experts writes them,
+ * moe_combine reads them; the pages have no counterpart).  Two planes of
+ * the same [rows, H] shape: hi = bf16(v) (round to nearest even) and an
+ * int8 residual r.  With f the 8-bit exponent field of hi (as an IEEE
+ * float), clamped to f >= 16:
+ *     r = clamp(round_even((v - hi) * 2^(142 - f)), -127, 127)
+ *     v' = hi + r * 2^(f - 142)
+ * so |v' - v| <= 2^-16 |v| (or <= 2^-127 for |v| < 2^-111).
+ * ---------------------------------------------------------------------- */
+
+/* -------------------------------------------------------------------------
  * moe_experts -- the per-expert half of the layer for rows whose expert and
  * weight are already chosen: the receiving side of expert-parallel dispatch
  * (M03 drill, level-3 follow-up on splitting experts across devices: the
  * (token, expert) table drives an all-to-all).  For every row r:
- *   y[r] = weights[r] * Expert_{ids[r]}(x_rows[r])   (fp32)
+ *   y[r] = weights[r] * Expert_{ids[r]}(x_rows[r])   (as pair rows)
  * with the arithmetic of moe_forward's per-pair outputs (grouping by expert,
  * gate/up with the hi/lo activation, down), so the bits equal the pair rows
  * moe_forward produces for the same (row, expert, weight);
@@ -252,7 +266,8 @@ moe_status_t moe_forward_prepared(const moe_bf16_t *x, const moe_bf16_t *router,
  *   w_gate, w_up [E, I, H] bf16, w_down [E, H, I] bf16 (w_down_f16: fp16):
  *            the experts this call serves (a rank's slice of the layer's
  *            experts)
- *   y        [R, H] fp32 out
+ *   y_hi     [R, H] bf16 out, y_res [R, H] int8 out: the pair rows of y
+ *            (both 16-byte aligned)
  *   workspace >= moe_experts_workspace_bytes(R, H, E, I) bytes, 256-byte
  *            aligned; its first 4 bytes are the status word
  *            (moe_read_device_status)
@@ -263,25 +278,27 @@ size_t moe_experts_workspace_bytes(int64_t R, int H, int E, int I);
 moe_status_t moe_experts(const moe_bf16_t *x_rows, const int32_t *ids,
                          const float *weights, int64_t R, int H, int E, int I,
                          const moe_bf16_t *w_gate, const moe_bf16_t *w_up,
-                         const moe_bf16_t *w_down, float *y, void *workspace,
-                         size_t workspace_bytes, cudaStream_t stream);
+                         const moe_bf16_t *w_down, moe_bf16_t *y_hi, int8_t *y_res,
+                         void *workspace, size_t workspace_bytes, cudaStream_t stream);
 moe_status_t moe_experts_prepared(const moe_bf16_t *x_rows, const int32_t *ids,
                                   const float *weights, int64_t R, int H, int E,
                                   int I, const moe_bf16_t *w_gate,
                                   const moe_bf16_t *w_up, const moe_f16_t *w_down_f16,
-                                  float *y, void *workspace, size_t workspace_bytes,
-                                  cudaStream_t stream);
+                                  moe_bf16_t *y_hi, int8_t *y_res, void *workspace,
+                                  size_t workspace_bytes, cudaStream_t stream);
 
 /* -------------------------------------------------------------------------
  * moe_combine -- the weighted accumulation of the layer (M03 drill: each
  * token's outputs summed back, index_add_ in the pages' PyTorch form), done
  * without atomics: out[n] = bf16(sum_{j<k} ypair[n*k + j] (+ yshared[n])),
- * summed in fp32 in slot order.  ypair [N*k, H] fp32, yshared [N, H] fp32 or
- * NULL, out [N, H] bf16; 16-byte aligned.  moe_forward ends with the same
- * kernel.
+ * the pair rows decoded and summed in fp32 in slot order.  ypair: pair rows
+ * [N*k, H] (ypair_hi bf16, ypair_res int8), yshared: pair rows [N, H] or
+ * both planes NULL, out [N, H] bf16; every plane 16-byte aligned.
+ * moe_forward ends with the same kernel.
  * ---------------------------------------------------------------------- */
-moe_status_t moe_combine(const float *ypair, const float *yshared, int64_t N, int H, int k,
-                         moe_bf16_t *out, cudaStream_t stream);
+moe_status_t moe_combine(const moe_bf16_t *ypair_hi, const int8_t *ypair_res,
+                         const moe_bf16_t *yshared_hi, const int8_t *yshared_res,
+                         int64_t N, int H, int k, moe_bf16_t *out, cudaStream_t stream);
 
 /* -------------------------------------------------------------------------
  * moe_convert_bf16_to_f16 -- the load-time step that makes the fp16 down
@@ -396,10 +413,12 @@ typedef struct {
     size_t act;           /* a = silu(x Wg^T) * (x Wu^T): bf16 hi [capacity, I]
                              then bf16 lo [capacity, I] (moe_forward), or fp16
                              [capacity, I] (moe_forward_prepared)           */
-    size_t ypair;         /* fp32 [N*k, H]        w * Expert(x), per pair     */
+    size_t ypair;         /* bf16 [N*k, H]  w * Expert(x) per pair: hi plane  */
+    size_t ypair_res;     /* int8 [N*k, H]  ... residual plane (pair rows)     */
     size_t act_shared;    /* as act, rows round_up(N,128), I_s columns
                              (shared only)                                    */
-    size_t y_shared;      /* fp32 [N, H]  gamma * SharedMLP(x) (shared only)  */
+    size_t y_shared;      /* bf16 [N, H]  gamma * SharedMLP(x), hi plane      */
+    size_t y_shared_res;  /* int8 [N, H]  ... residual plane (shared only)    */
     size_t total;         /* = moe_forward_workspace_bytes                    */
     int64_t capacity;     /* moe_align_capacity(N, k, E, 128)                 */
 } moe_forward_layout_t;

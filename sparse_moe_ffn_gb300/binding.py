@@ -33,8 +33,9 @@ class MoEError(RuntimeError):
 class _Layout(ctypes.Structure):
     _fields_ = [(name, ctypes.c_size_t) for name in (
         "status", "topk_w", "topk_ids", "gamma", "counts", "offsets", "pad_offsets",
-        "num_padded", "align_scratch", "sorted_pair", "block_expert", "ready", "x_sorted", "act", "ypair",
-        "act_shared", "y_shared", "total")] + [("capacity", ctypes.c_int64)]
+        "num_padded", "align_scratch", "sorted_pair", "block_expert", "ready", "x_sorted", "act",
+        "ypair", "ypair_res", "act_shared", "y_shared", "y_shared_res", "total")] + [
+        ("capacity", ctypes.c_int64)]
 
 
 _lib = None
@@ -64,9 +65,9 @@ def lib():
         "moe_forward_host_prepared": ([P] * 12 + [i64, i32, i32, i32, i32, i32, i32, P, sz, P],
                                       i32),
         "moe_experts_workspace_bytes": ([i64, i32, i32, i32], sz),
-        "moe_experts": ([P, P, P, i64, i32, i32, i32, P, P, P, P, P, sz, P], i32),
-        "moe_experts_prepared": ([P, P, P, i64, i32, i32, i32, P, P, P, P, P, sz, P], i32),
-        "moe_combine": ([P, P, i64, i32, i32, P, P], i32),
+        "moe_experts": ([P, P, P, i64, i32, i32, i32, P, P, P, P, P, P, sz, P], i32),
+        "moe_experts_prepared": ([P, P, P, i64, i32, i32, i32, P, P, P, P, P, P, sz, P], i32),
+        "moe_combine": ([P, P, P, P, i64, i32, i32, P, P], i32),
         "moe_convert_bf16_to_f16": ([P, P, i64, P, P], i32),
         "moe_forward_layout": ([i64, i32, i32, i32, i32, i32, ctypes.POINTER(_Layout)], i32),
         "moe_read_device_status": ([P, P], i32),
@@ -301,9 +302,11 @@ def moe_dense_mlp(x, w_gate, w_up, w_down, out=None, workspace=None):
 
 
 def moe_experts(x_rows, ids, weights, w_gate, w_up, w_down, y=None, workspace=None):
-    """Per-row expert outputs y[r] = weights[r] * Expert_{ids[r]}(x_rows[r])
-    ([R, H] fp32): the receiving side of expert-parallel dispatch.  w_down
-    bf16 (moe_experts) or its fp16 copy (moe_experts_prepared)."""
+    """Per-row expert outputs y[r] = weights[r] * Expert_{ids[r]}(x_rows[r]) as
+    pair rows (``(hi bf16 [R, H], res int8 [R, H])``, the format moe.h
+    describes): the receiving side of expert-parallel dispatch.  w_down bf16
+    (moe_experts) or its fp16 copy (moe_experts_prepared).  Returns (y,
+    workspace)."""
     R, H = x_rows.shape
     E, I, _ = w_gate.shape
     _bf16(x_rows, "x_rows")
@@ -316,32 +319,46 @@ def moe_experts(x_rows, ids, weights, w_gate, w_up, w_down, y=None, workspace=No
         raise ValueError("weights must be a CUDA float32 tensor of shape [R]")
     ids, weights = ids.contiguous(), weights.contiguous()
     if y is None:
-        y = torch.empty((R, H), dtype=torch.float32, device=x_rows.device)
-    if y.dtype != torch.float32 or tuple(y.shape) != (R, H) or not y.is_contiguous():
-        raise ValueError("y must be a contiguous float32 tensor of shape [R, H]")
+        y = alloc_pair_rows(R, H, x_rows.device)
+    _check_pair_rows(y, R, H, "y")
     if workspace is None:
         workspace = torch.empty(max(lib().moe_experts_workspace_bytes(R, H, E, I), 256),
                                 dtype=torch.uint8, device=x_rows.device)
     fn = lib().moe_experts_prepared if prepared else lib().moe_experts
     _check(fn(_ptr(x_rows), _ptr(ids), _ptr(weights), R, H, E, I, _ptr(w_gate), _ptr(w_up),
-              _ptr(w_down), _ptr(y), _ptr(workspace), workspace.numel(), _stream()),
-           "moe_experts")
+              _ptr(w_down), _ptr(y[0]), _ptr(y[1]), _ptr(workspace), workspace.numel(),
+              _stream()), "moe_experts")
     return y, workspace
 
 
+def alloc_pair_rows(R: int, H: int, device="cuda"):
+    """Empty pair rows of [R, H] values: (hi bf16 [R, H], res int8 [R, H])."""
+    return (torch.empty((R, H), dtype=torch.bfloat16, device=device),
+            torch.empty((R, H), dtype=torch.int8, device=device))
+
+
+def _check_pair_rows(y, R, H, name):
+    hi, res = y
+    if (hi.dtype != torch.bfloat16 or res.dtype != torch.int8 or tuple(hi.shape) != (R, H)
+            or tuple(res.shape) != (R, H) or not hi.is_contiguous() or not res.is_contiguous()
+            or not hi.is_cuda or not res.is_cuda):
+        raise ValueError(f"{name} must be pair rows: (bf16 [{R}, {H}], int8 [{R}, {H}]) "
+                         "contiguous CUDA tensors")
+
+
 def moe_combine(ypair, N: int, k: int, yshared=None, out=None):
-    """out[n] = bf16(sum_j ypair[n*k + j] (+ yshared[n])) in fp32, slot order."""
-    H = ypair.shape[1]
-    if ypair.dtype != torch.float32 or tuple(ypair.shape) != (N * k, H) or not ypair.is_contiguous():
-        raise ValueError("ypair must be a contiguous float32 tensor of shape [N*k, H]")
-    if yshared is not None and (yshared.dtype != torch.float32 or tuple(yshared.shape) != (N, H)
-                                or not yshared.is_contiguous()):
-        raise ValueError("yshared must be a contiguous float32 tensor of shape [N, H]")
+    """out[n] = bf16(sum_j ypair[n*k + j] (+ yshared[n])) in fp32, slot order;
+    ypair and yshared are pair rows (hi, res)."""
+    H = ypair[0].shape[1]
+    _check_pair_rows(ypair, N * k, H, "ypair")
+    if yshared is not None:
+        _check_pair_rows(yshared, N, H, "yshared")
+    sh = yshared if yshared is not None else (None, None)
     if out is None:
-        out = torch.empty((N, H), dtype=torch.bfloat16, device=ypair.device)
+        out = torch.empty((N, H), dtype=torch.bfloat16, device=ypair[0].device)
     _bf16(out, "out", (N, H))
-    _check(lib().moe_combine(_ptr(ypair), _ptr(yshared), N, H, k, _ptr(out), _stream()),
-           "moe_combine")
+    _check(lib().moe_combine(_ptr(ypair[0]), _ptr(ypair[1]), _ptr(sh[0]), _ptr(sh[1]), N, H, k,
+                             _ptr(out), _stream()), "moe_combine")
     return out
 
 
@@ -575,12 +592,14 @@ def workspace_views(workspace, N, H, E, I, k, I_s=0) -> dict:
         "act_hi": view(lay["act"], torch.bfloat16, (cap, I)),
         "act_lo": view(lay["act"] + 2 * cap * I, torch.bfloat16, (cap, I)),
         "act_f16": view(lay["act"], torch.float16, (cap, I)),
-        "ypair": view(lay["ypair"], torch.float32, (P, H)),
+        # pair rows (hi, res) of w * Expert(x), one row per pair
+        "ypair": (view(lay["ypair"], torch.bfloat16, (P, H)),
+                  view(lay["ypair_res"], torch.int8, (P, H))),
     }
     if I_s:
-        rows_s = -(-N // MOE_BLOCK_M) * MOE_BLOCK_M
         v["gamma"] = view(lay["gamma"], torch.float32, (N,))
-        v["y_shared"] = view(lay["y_shared"], torch.float32, (N, H))
+        v["y_shared"] = (view(lay["y_shared"], torch.bfloat16, (N, H)),
+                         view(lay["y_shared_res"], torch.int8, (N, H)))
     return v
 
 

@@ -281,9 +281,12 @@ moe_status_t forward_layout(int64_t N, int H, int E, int I, int k, int I_s,
     // the activation: fp16, or a bf16 hi/lo pair (4 bytes a value either way
     // is reserved, so one workspace serves both forms of the down weights)
     L->act = take(4 * static_cast<size_t>(cap) * I);
-    L->ypair = take(4 * static_cast<size_t>(P) * H);  // fp32
+    // pair rows: bf16 hi plane and int8 residual plane
+    L->ypair = take(2 * static_cast<size_t>(P) * H);
+    L->ypair_res = take(static_cast<size_t>(P) * H);
     L->act_shared = take(shared ? 4 * static_cast<size_t>(round_up64(N, kBlockM)) * I_s : 0);
-    L->y_shared = take(shared ? 4 * static_cast<size_t>(N) * H : 0);  // fp32
+    L->y_shared = take(shared ? 2 * static_cast<size_t>(N) * H : 0);
+    L->y_shared_res = take(shared ? static_cast<size_t>(N) * H : 0);
     L->total = off;
     L->capacity = cap;
     return MOE_OK;
@@ -346,8 +349,8 @@ moe_status_t check_forward_args(const moe_bf16_t *x, const moe_bf16_t *router,
 moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const float *weights,
                              int64_t N, int k, int H, int E, int I, const moe_bf16_t *w_gate,
                              const moe_bf16_t *w_up, const void *w_down, bool down_f16,
-                             const moe_forward_layout_t &L, uint8_t *ws, float *ypair,
-                             cudaStream_t stream) {
+                             const moe_forward_layout_t &L, uint8_t *ws, uint16_t *ypair,
+                             int8_t *ypair_res, cudaStream_t stream) {
     moe_status_t st;
     auto at = [&](size_t off) { return ws + off; };
     int32_t *status = reinterpret_cast<int32_t *>(at(L.status));
@@ -412,6 +415,7 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
     g.n_out = I;
     g.w_rows = I;
     g.out = act;
+    g.out_res = nullptr;
     g.out_ld = I;
     g.lo_rows = down_f16 ? 0 : cap;  // bf16 down weights: hi/lo activation
     g.scale = nullptr;
@@ -488,6 +492,7 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
     g.n_out = H;
     g.w_rows = H;
     g.out = ypair;
+    g.out_res = ypair_res;
     g.out_ld = H;
     g.scale = weights;
     {
@@ -657,7 +662,8 @@ static moe_status_t forward_impl(const moe_bf16_t *x, const moe_bf16_t *router,
     float *topk_w = reinterpret_cast<float *>(at(L.topk_w));
     int32_t *topk_ids = reinterpret_cast<int32_t *>(at(L.topk_ids));
     float *gamma = shared ? reinterpret_cast<float *>(at(L.gamma)) : nullptr;
-    float *ypair = reinterpret_cast<float *>(at(L.ypair));
+    uint16_t *ypair = reinterpret_cast<uint16_t *>(at(L.ypair));
+    int8_t *ypair_res = reinterpret_cast<int8_t *>(at(L.ypair_res));
     const int sms = num_sms_of_current_device();
 
     // K1: routing (its first CTA also clears the status word, so that no
@@ -669,15 +675,17 @@ static moe_status_t forward_impl(const moe_bf16_t *x, const moe_bf16_t *router,
 
     // K2-K4: grouping, gate/up, down
     if ((st = enqueue_experts(x, topk_ids, topk_w, N, k, H, E, I, w_gate, w_up, w_down,
-                              down_f16, L, ws, ypair, stream)) != MOE_OK)
+                              down_f16, L, ws, ypair, ypair_res, stream)) != MOE_OK)
         return st;
 
     // shared expert: one dense group over all N tokens, weight sigmoid(x . g)
     if ((st = record_stage(MOE_STAGE_SHARED, stream)) != MOE_OK) return st;
-    float *y_shared = nullptr;
+    uint16_t *y_shared = nullptr;
+    int8_t *y_shared_res = nullptr;
     if (shared) {
         uint16_t *act_s = reinterpret_cast<uint16_t *>(at(L.act_shared));
-        y_shared = reinterpret_cast<float *>(at(L.y_shared));
+        y_shared = reinterpret_cast<uint16_t *>(at(L.y_shared));
+        y_shared_res = reinterpret_cast<int8_t *>(at(L.y_shared_res));
         const int64_t rows_s = round_up64(N, kBlockM);
         const GemmMode down = down_f16 ? kDown : kDownSplit;
         const int64_t act_rows = down_f16 ? rows_s : 2 * rows_s;
@@ -714,6 +722,7 @@ static moe_status_t forward_impl(const moe_bf16_t *x, const moe_bf16_t *router,
         s.n_out = I_s;
         s.w_rows = I_s;
         s.out = act_s;
+        s.out_res = nullptr;
         s.out_ld = I_s;
         s.lo_rows = down_f16 ? 0 : rows_s;
         s.scale = nullptr;
@@ -746,6 +755,7 @@ static moe_status_t forward_impl(const moe_bf16_t *x, const moe_bf16_t *router,
         s.n_out = H;
         s.w_rows = H;
         s.out = y_shared;
+        s.out_res = y_shared_res;
         s.out_ld = H;
         s.scale = gamma;
         {
@@ -772,7 +782,8 @@ static moe_status_t forward_impl(const moe_bf16_t *x, const moe_bf16_t *router,
 
     // K5: out[n] = sum_j ypair[n*k + j] (+ shared)
     if ((st = record_stage(MOE_STAGE_COMBINE, stream)) != MOE_OK) return st;
-    MOE_CUDA(launch_combine(ypair, y_shared, N, H, k, out, sms, stream), "combine kernel launch");
+    MOE_CUDA(launch_combine(ypair, ypair_res, y_shared, y_shared_res, N, H, k, out, sms, stream),
+             "combine kernel launch");
     g_launches += 1;
     if ((st = record_stage(MOE_NUM_STAGES, stream)) != MOE_OK) return st;
     return MOE_OK;
@@ -811,8 +822,9 @@ size_t moe_experts_workspace_bytes(int64_t R, int H, int E, int I) {
 static moe_status_t experts_impl(const moe_bf16_t *x_rows, const int32_t *ids,
                                  const float *weights, int64_t R, int H, int E, int I,
                                  const moe_bf16_t *w_gate, const moe_bf16_t *w_up,
-                                 const void *w_down, bool down_f16, float *y, void *workspace,
-                                 size_t workspace_bytes, cudaStream_t stream) {
+                                 const void *w_down, bool down_f16, moe_bf16_t *y_hi,
+                                 int8_t *y_res, void *workspace, size_t workspace_bytes,
+                                 cudaStream_t stream) {
     g_last_error.clear();
     if (R < 0) return fail(MOE_ERR_INVALID_ARG, "R must be >= 0 (got %lld)", (long long)R);
     if (H < 8 || H % 8 || I < 8 || I % 8)
@@ -820,10 +832,11 @@ static moe_status_t experts_impl(const moe_bf16_t *x_rows, const int32_t *ids,
     if (E < 1 || E > MOE_MAX_EXPERTS)
         return fail(MOE_ERR_UNSUPPORTED, "E must be in [1, %d] (got %d)", MOE_MAX_EXPERTS, E);
     if (R == 0) return MOE_OK;
-    if (!x_rows || !ids || !weights || !w_gate || !w_up || !w_down || !y || !workspace)
+    if (!x_rows || !ids || !weights || !w_gate || !w_up || !w_down || !y_hi || !y_res ||
+        !workspace)
         return fail(MOE_ERR_INVALID_ARG, "every moe_experts pointer must be non-null");
     if (!aligned16(x_rows) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
-        !aligned16(y))
+        !aligned16(y_hi) || !aligned16(y_res))
         return fail(MOE_ERR_INVALID_ARG, "matrices must be 16-byte aligned");
     if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
         return fail(MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
@@ -837,37 +850,44 @@ static moe_status_t experts_impl(const moe_bf16_t *x_rows, const int32_t *ids,
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     MOE_CUDA(cudaMemsetAsync(ws + L.status, 0, sizeof(int32_t), stream), "status reset");
     return enqueue_experts(x_rows, ids, weights, R, 1, H, E, I, w_gate, w_up, w_down, down_f16,
-                           L, ws, y, stream);
+                           L, ws, y_hi, y_res, stream);
 }
 
 moe_status_t moe_experts(const moe_bf16_t *x_rows, const int32_t *ids, const float *weights,
                          int64_t R, int H, int E, int I, const moe_bf16_t *w_gate,
-                         const moe_bf16_t *w_up, const moe_bf16_t *w_down, float *y,
-                         void *workspace, size_t workspace_bytes, cudaStream_t stream) {
-    return experts_impl(x_rows, ids, weights, R, H, E, I, w_gate, w_up, w_down, false, y,
-                        workspace, workspace_bytes, stream);
+                         const moe_bf16_t *w_up, const moe_bf16_t *w_down, moe_bf16_t *y_hi,
+                         int8_t *y_res, void *workspace, size_t workspace_bytes,
+                         cudaStream_t stream) {
+    return experts_impl(x_rows, ids, weights, R, H, E, I, w_gate, w_up, w_down, false, y_hi,
+                        y_res, workspace, workspace_bytes, stream);
 }
 
 moe_status_t moe_experts_prepared(const moe_bf16_t *x_rows, const int32_t *ids,
                                   const float *weights, int64_t R, int H, int E, int I,
                                   const moe_bf16_t *w_gate, const moe_bf16_t *w_up,
-                                  const moe_f16_t *w_down_f16, float *y, void *workspace,
-                                  size_t workspace_bytes, cudaStream_t stream) {
-    return experts_impl(x_rows, ids, weights, R, H, E, I, w_gate, w_up, w_down_f16, true, y,
-                        workspace, workspace_bytes, stream);
+                                  const moe_f16_t *w_down_f16, moe_bf16_t *y_hi, int8_t *y_res,
+                                  void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return experts_impl(x_rows, ids, weights, R, H, E, I, w_gate, w_up, w_down_f16, true, y_hi,
+                        y_res, workspace, workspace_bytes, stream);
 }
 
-moe_status_t moe_combine(const float *ypair, const float *yshared, int64_t N, int H, int k,
-                         moe_bf16_t *out, cudaStream_t stream) {
+moe_status_t moe_combine(const moe_bf16_t *ypair_hi, const int8_t *ypair_res,
+                         const moe_bf16_t *yshared_hi, const int8_t *yshared_res, int64_t N,
+                         int H, int k, moe_bf16_t *out, cudaStream_t stream) {
     g_last_error.clear();
     if (N < 0 || H < 8 || H % 8 || k < 1)
         return fail(MOE_ERR_INVALID_ARG, "need N >= 0, H a positive multiple of 8, k >= 1");
     if (N == 0) return MOE_OK;
-    if (!ypair || !out) return fail(MOE_ERR_INVALID_ARG, "ypair and out must be non-null");
-    if (!aligned16(ypair) || !aligned16(out) || (yshared && !aligned16(yshared)))
-        return fail(MOE_ERR_INVALID_ARG, "ypair, yshared and out must be 16-byte aligned");
+    if (!ypair_hi || !ypair_res || !out)
+        return fail(MOE_ERR_INVALID_ARG, "ypair_hi, ypair_res and out must be non-null");
+    if ((yshared_hi == nullptr) != (yshared_res == nullptr))
+        return fail(MOE_ERR_INVALID_ARG, "give both planes of yshared or neither");
+    if (!aligned16(ypair_hi) || !aligned16(ypair_res) || !aligned16(out) ||
+        (yshared_hi && (!aligned16(yshared_hi) || !aligned16(yshared_res))))
+        return fail(MOE_ERR_INVALID_ARG, "pair planes and out must be 16-byte aligned");
     if (N > (int64_t(1) << 31) / k) return fail(MOE_ERR_UNSUPPORTED, "N*k must stay below 2^31");
-    MOE_CUDA(launch_combine(ypair, yshared, N, H, k, out, num_sms_of_current_device(), stream),
+    MOE_CUDA(launch_combine(ypair_hi, ypair_res, yshared_hi, yshared_res, N, H, k, out,
+                            num_sms_of_current_device(), stream),
              "combine kernel launch");
     g_launches += 1;
     return MOE_OK;
@@ -1018,8 +1038,9 @@ size_t moe_dense_mlp_workspace_bytes(int64_t N, int H, int I) {
     if (N < 0 || H < 1 || I < 1) return 0;
     const size_t rows = static_cast<size_t>(round_up64(N, kBlockM));
     // the activation (fp16, or a bf16 hi/lo pair: 4 bytes a value reserved),
-    // then the fp32 down projection
-    return kAlign + round_up(4 * rows * I, kAlign) + round_up(4 * static_cast<size_t>(N) * H, kAlign);
+    // then the down projection as pair rows (bf16 hi plane, int8 residual)
+    return kAlign + round_up(4 * rows * I, kAlign) + round_up(2 * static_cast<size_t>(N) * H, kAlign) +
+           round_up(static_cast<size_t>(N) * H, kAlign);
 }
 
 static moe_status_t dense_mlp_impl(const moe_bf16_t *x, const moe_bf16_t *w_gate,
@@ -1047,7 +1068,9 @@ static moe_status_t dense_mlp_impl(const moe_bf16_t *x, const moe_bf16_t *w_gate
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     int32_t *status = reinterpret_cast<int32_t *>(ws);
     uint16_t *act = reinterpret_cast<uint16_t *>(ws + kAlign);
-    float *y = reinterpret_cast<float *>(ws + kAlign + round_up(4 * rows * I, kAlign));
+    uint16_t *y = reinterpret_cast<uint16_t *>(ws + kAlign + round_up(4 * rows * I, kAlign));
+    int8_t *y_res = reinterpret_cast<int8_t *>(ws + kAlign + round_up(4 * rows * I, kAlign) +
+                                               round_up(2 * static_cast<size_t>(N) * H, kAlign));
     const int sms = num_sms_of_current_device();
     const GemmMode down = down_f16 ? kDown : kDownSplit;
     const int64_t act_rows = down_f16 ? rows : 2 * rows;  // split: hi rows, then lo rows
@@ -1072,6 +1095,7 @@ static moe_status_t dense_mlp_impl(const moe_bf16_t *x, const moe_bf16_t *w_gate
     g.n_out = I;
     g.w_rows = I;
     g.out = act;
+    g.out_res = nullptr;
     g.out_ld = I;
     g.lo_rows = down_f16 ? 0 : rows;
     g.scale = nullptr;
@@ -1099,6 +1123,7 @@ static moe_status_t dense_mlp_impl(const moe_bf16_t *x, const moe_bf16_t *w_gate
     g.n_out = H;
     g.w_rows = H;
     g.out = y;
+    g.out_res = y_res;
     g.out_ld = H;
     if (pairs) {
         const int bnp = pair_gemm_block_n(down);
@@ -1115,8 +1140,9 @@ static moe_status_t dense_mlp_impl(const moe_bf16_t *x, const moe_bf16_t *w_gate
         MOE_CUDA(launch_gemm(down, kDownBN, tm_act, tm_act, tm_d, tm_d, g, stream),
                  "dense down kernel launch");
     }
-    // fp32 rows -> bf16 out (the combine with one slot per token)
-    MOE_CUDA(launch_combine(y, nullptr, N, H, 1, out, sms, stream), "combine kernel launch");
+    // pair rows -> bf16 out (the combine with one slot per token)
+    MOE_CUDA(launch_combine(y, y_res, nullptr, nullptr, N, H, 1, out, sms, stream),
+             "combine kernel launch");
     g_launches += 3;
     return MOE_OK;
 }

@@ -3,19 +3,21 @@
 // The scatter-add of the M03 "Sparse MoE" drill (each token receives the sum
 // of all k weighted expert outputs, an accumulation and never an assignment)
 // done without atomics: the down-projection epilogue stored w * Expert(x) of
-// pair p = n*k + j at row p of ypair in fp32, so token n's k contributions
-// are the k consecutive rows n*k .. n*k+k-1.  They are summed in slot order
-// in fp32, the shared-expert term gamma * SharedMLP(x) (same page, talker
-// line) is added last, and the result is rounded to bf16 once.  Keeping the
-// contributions in fp32 matters: the bf16 rounding of the exact result
-// already uses ~97% of the layer's max-error bound at prefill size, and an
-// fp16 rounding of each contribution pushed the largest outputs past it.
-// Bandwidth bound: one thread per 8 output columns, two 16-byte loads per
-// contribution and one 16-byte store.
+// pair p = n*k + j at row p of ypair, so token n's k contributions are the k
+// consecutive rows n*k .. n*k+k-1.  They are decoded (pair_rows.cuh: bf16 hi
+// + int8 residual, 16 significant bits), summed in slot order in fp32, the
+// shared-expert term gamma * SharedMLP(x) (same page, talker line) is added
+// last, and the result is rounded to bf16 once.  The contributions need
+// those 16 bits: the bf16 rounding of the exact result already uses ~97% of
+// the layer's max-error bound at prefill size, and an fp16 rounding of each
+// contribution (11 bits) pushed the largest outputs past it.
+// Bandwidth bound: one thread per 8 output columns, a 16-byte and an 8-byte
+// load per contribution and one 16-byte store.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "kernels.cuh"
+#include "pair_rows.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -24,23 +26,30 @@ namespace {
 
 constexpr int kCombineThreads = 256;
 
-// acc[0..7] += the 8 floats at p (32-byte aligned), read through L2
-__device__ __forceinline__ void add_f32x8(float (&acc)[8], const float *p) {
-    const float4 a = __ldcg(reinterpret_cast<const float4 *>(p));
-    const float4 b = __ldcg(reinterpret_cast<const float4 *>(p + 4));
-    acc[0] += a.x;
-    acc[1] += a.y;
-    acc[2] += a.z;
-    acc[3] += a.w;
-    acc[4] += b.x;
-    acc[5] += b.y;
-    acc[6] += b.z;
-    acc[7] += b.w;
+// acc[0..7] += the 8 pair-row values of row offset o (hi 16 bytes, residual
+// 8 bytes), read through L2
+__device__ __forceinline__ void add_pair8(float (&acc)[8], const uint16_t *hi_plane,
+                                          const int8_t *res_plane, int64_t o) {
+    const uint4 h = __ldcg(reinterpret_cast<const uint4 *>(hi_plane + o));
+    const uint2 r = __ldcg(reinterpret_cast<const uint2 *>(res_plane + o));
+    const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
+    const uint32_t rw[2] = {r.x, r.y};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 hv = unpack_bf16x2(hw[i]);
+        const uint32_t rr = rw[i / 2] >> (16 * (i % 2));
+        const int r0 = static_cast<int8_t>(rr & 0xFFu);
+        const int r1 = static_cast<int8_t>((rr >> 8) & 0xFFu);
+        acc[2 * i] += pair_decode(hv.x, r0);
+        acc[2 * i + 1] += pair_decode(hv.y, r1);
+    }
 }
 
 __global__ void __launch_bounds__(kCombineThreads)
-    combine_kernel(const float *__restrict__ ypair, const float *__restrict__ yshared,
-                   int64_t N, int H, int k, uint16_t *__restrict__ out) {
+    combine_kernel(const uint16_t *__restrict__ ypair_hi, const int8_t *__restrict__ ypair_res,
+                   const uint16_t *__restrict__ yshared_hi,
+                   const int8_t *__restrict__ yshared_res, int64_t N, int H, int k,
+                   uint16_t *__restrict__ out) {
     griddep_launch_dependents();
     griddep_wait();
     const int groups = H / 8;
@@ -50,9 +59,10 @@ __global__ void __launch_bounds__(kCombineThreads)
         const int64_t n = idx / groups;
         const int col = static_cast<int>(idx % groups) * 8;
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        const float *src = ypair + n * k * static_cast<int64_t>(H) + col;
-        for (int j = 0; j < k; ++j) add_f32x8(acc, src + static_cast<int64_t>(j) * H);
-        if (yshared) add_f32x8(acc, yshared + n * H + col);
+        const int64_t o = n * k * static_cast<int64_t>(H) + col;
+        for (int j = 0; j < k; ++j)
+            add_pair8(acc, ypair_hi, ypair_res, o + static_cast<int64_t>(j) * H);
+        if (yshared_hi) add_pair8(acc, yshared_hi, yshared_res, n * H + col);
         uint4 pk;
         pk.x = pack_bf16x2(acc[0], acc[1]);
         pk.y = pack_bf16x2(acc[2], acc[3]);
@@ -64,14 +74,15 @@ __global__ void __launch_bounds__(kCombineThreads)
 
 }  // namespace
 
-cudaError_t launch_combine(const float *ypair, const float *yshared, int64_t N, int H, int k,
-                           uint16_t *out, int num_sms, cudaStream_t s) {
+cudaError_t launch_combine(const uint16_t *ypair_hi, const int8_t *ypair_res,
+                           const uint16_t *yshared_hi, const int8_t *yshared_res, int64_t N,
+                           int H, int k, uint16_t *out, int num_sms, cudaStream_t s) {
     const int64_t total = N * (H / 8);
     int64_t blocks = (total + kCombineThreads - 1) / kCombineThreads;
     const int64_t cap = static_cast<int64_t>(num_sms) * 16;
     if (blocks > cap) blocks = cap;
     return launch_pdl(combine_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kCombineThreads),
-                      0, s, 1, ypair, yshared, N, H, k, out);
+                      0, s, 1, ypair_hi, ypair_res, yshared_hi, yshared_res, N, H, k, out);
 }
 
 }  // namespace moe

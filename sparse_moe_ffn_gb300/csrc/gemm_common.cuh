@@ -6,6 +6,7 @@
 #include <cuda_bf16.h>
 
 #include "kernels.cuh"
+#include "pair_rows.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -73,8 +74,10 @@ __device__ __forceinline__ TileRow no_tile_row() {
 //            operand: fp16(a) (a.lo_rows == 0), or the bf16 pair
 //            hi = bf16(a) at row grow and lo = bf16(a - hi) at row
 //            grow + a.lo_rows (hi + lo carries 16 significant bits);
-//   down:    y[q] = w[q] * acc in fp32, the pair's weighted result, kept in
-//            fp32 until the combine rounds the token's sum to bf16 once.
+//   down:    y[q] = w[q] * acc in fp32, the pair's weighted result, stored
+//            as a pair row (pair_rows.cuh: bf16 hi + int8 residual, 16
+//            significant bits) until the combine rounds the token's sum to
+//            bf16 once.
 // A value the stored format cannot hold (an fp16 activation past 65504, or
 // anything non-finite) is reported as MOE_ERR_DEVICE_CHECK.
 template <int MODE, int BN>
@@ -88,7 +91,7 @@ __device__ __forceinline__ void store_tile(const GemmArgs &a, uint32_t taddr, co
     float vmax = 0.f;
     // 32 bytes per store when every output row starts on a 32-byte boundary,
     // else 16; stores never pass n_out (a multiple of 8)
-    const int esize = MODE == kGateUp ? 2 : 4;
+    const int esize = 2;  // bf16 / fp16 outputs
     const bool wide = (a.out_ld * esize) % 32 == 0 && (reinterpret_cast<uintptr_t>(a.out) % 32) == 0;
     // 32 bytes (pk) to dst, which holds elements [col, col + 32 / esize)
     auto store32 = [&](void *dst, int col, const uint32_t (&pk)[8]) {
@@ -140,7 +143,12 @@ __device__ __forceinline__ void store_tile(const GemmArgs &a, uint32_t taddr, co
         if (!(vmax <= (split ? kF32Max : kF16Max))) record_status(a.status, MOE_ERR_DEVICE_CHECK);
     } else {
         const float w = r.w;
-        float *dst = static_cast<float *>(a.out) + (valid ? q : 0) * a.out_ld + col0;
+        const int64_t row = (valid ? q : 0) * a.out_ld + col0;
+        uint16_t *dst = static_cast<uint16_t *>(a.out) + row;
+        int8_t *dst_res = a.out_res + row;
+        // residual plane: 16 bytes per 16 columns when its rows start on
+        // 16-byte boundaries, else 8
+        const bool res16 = a.out_ld % 16 == 0;
         // 64 columns per TMEM round trip: two loads in flight, one wait
 #pragma unroll 1
         for (int c = 0; c < BN / 64; ++c) {
@@ -150,16 +158,30 @@ __device__ __forceinline__ void store_tile(const GemmArgs &a, uint32_t taddr, co
             tmem_load_wait();
             if (valid) {
 #pragma unroll
-                for (int h = 0; h < 8; ++h) {
-                    uint32_t pk[8];
+                for (int h = 0; h < 4; ++h) {
+                    uint32_t pk[8], pr[4];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const float t = w * yv[h * 8 + i];
-                        vmax = fmaxf(vmax, fabsf(t));
-                        pk[i] = __float_as_uint(t);
+                        const float t0 = w * yv[h * 16 + 2 * i];
+                        const float t1 = w * yv[h * 16 + 2 * i + 1];
+                        vmax = fmaxf(vmax, fmaxf(fabsf(t0), fabsf(t1)));
+                        pk[i] = pack_bf16x2(t0, t1);
+                        const float2 hi = unpack_bf16x2(pk[i]);
+                        const uint32_t r2 = (static_cast<uint32_t>(pair_residual(t0, hi.x)) & 0xFFu) |
+                                            ((static_cast<uint32_t>(pair_residual(t1, hi.y)) & 0xFFu) << 8);
+                        if (i % 2 == 0) pr[i / 2] = r2;
+                        else pr[i / 2] |= r2 << 16;
                     }
-                    const int cc = c * 64 + h * 8;
+                    const int cc = c * 64 + h * 16;
                     store32(dst + cc, col0 + cc, pk);
+                    if (col0 + cc + 16 <= a.n_out && res16) {
+                        *reinterpret_cast<uint4 *>(dst_res + cc) = make_uint4(pr[0], pr[1], pr[2], pr[3]);
+                    } else {
+                        if (col0 + cc + 8 <= a.n_out)
+                            *reinterpret_cast<uint2 *>(dst_res + cc) = make_uint2(pr[0], pr[1]);
+                        if (col0 + cc + 16 <= a.n_out)
+                            *reinterpret_cast<uint2 *>(dst_res + cc + 8) = make_uint2(pr[2], pr[3]);
+                    }
                 }
             }
         }

@@ -108,8 +108,10 @@ struct GemmArgs {
     int n_out;          // output columns (I for gate/up, H for down)
     int64_t w_rows;     // weight rows per expert (I or H)
     // gate/up: act [rows, I], fp16, or bf16 hi with the bf16 lo rows lo_rows
-    // rows further on; down: fp32 y [q_limit, H]
+    // rows further on.  down: the pair rows y [q_limit, H] in the pair-row
+    // format (pair_rows.cuh): bf16 hi at out, int8 residual at out_res
     void *out;
+    int8_t *out_res;
     int64_t out_ld;
     // 0: fp16 activation.  Otherwise the activation is a bf16 pair: gate/up
     // stores hi at row r and lo = bf16(a - hi) at row r + lo_rows; the
@@ -183,8 +185,10 @@ cudaError_t launch_pair_gemm(GemmMode mode, const CUtensorMap &tm_a, const CUten
 
 // ----------------------------------------------------------------- combine
 
-cudaError_t launch_combine(const float *ypair, const float *yshared, int64_t N, int H, int k,
-                           uint16_t *out, int num_sms, cudaStream_t s);
+// ypair / yshared: pair rows (bf16 hi plane, int8 residual plane)
+cudaError_t launch_combine(const uint16_t *ypair_hi, const int8_t *ypair_res,
+                           const uint16_t *yshared_hi, const int8_t *yshared_res, int64_t N,
+                           int H, int k, uint16_t *out, int num_sms, cudaStream_t s);
 
 // ------------------------------------------- bf16 -> fp16 weight conversion
 

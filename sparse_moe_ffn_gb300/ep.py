@@ -14,7 +14,8 @@ and holds only their weights.  Per layer call, on every rank:
 3. dispatch: each pair's token row, its expert id local to the receiving
    rank and its routing weight travel with one all_to_all each;
 4. the receiving rank runs its experts on the rows it received
-   (moe_experts: y = w * Expert(x) in fp32);
+   (moe_experts: y = w * Expert(x) as pair rows, a bf16 plane and an int8
+   residual plane);
 5. combine: the results travel back with the reverse all_to_all and land in
    pair order (ypair[p]).  moe_combine then sums each token's k slots in slot
    order.
@@ -26,11 +27,11 @@ bit, whatever the number of ranks.
 The shared expert (the talker layer) is dense: every rank holds its weights
 and applies it to its own tokens, with no exchange.  It runs as moe_experts
 with one expert, every row routed to it and the sigmoid gate as the row
-weight, which is moe_forward's shared term gamma * SharedMLP(x) in fp32; the
-combine adds it after the k slots.
+weight, which is moe_forward's shared term gamma * SharedMLP(x); the combine
+adds it after the k slots.
 
-Transport: gloo and NCCL both carry int32, so bf16 and fp32 rows travel as
-their bit patterns viewed as int32 (H is even).  With one rank nothing is
+Transport: gloo and NCCL both carry int32, so bf16 rows and int8 residual
+rows travel as their bit patterns viewed as int32 (H is a multiple of 8).  With one rank nothing is
 exchanged.  The three compute steps can be replaced (route_fn, experts_fn,
 combine_fn), which is how the exchange logic is tested on CPU ranks.
 """
@@ -85,8 +86,8 @@ def ep_forward(x, router, w_gate, w_up, w_down, E: int, k: int, norm_topk_prob: 
     copy of binding.prepare_weights): this rank's experts.  ``shared``: None
     or the shared expert (binding.SHARED_KEYS, shared_down_proj in the same
     form as w_down), the same on every rank.  route_fn(x) returns (weights,
-    ids) or (weights, ids, gamma); shared_fn(x, gamma) returns the fp32
-    shared term.
+    ids) or (weights, ids, gamma); experts_fn and shared_fn return pair rows
+    (hi bf16, res int8), each [rows, H].
     Returns out [N, H] bf16."""
     from sparse_moe_ffn_gb300 import binding
 
@@ -137,10 +138,14 @@ def ep_forward(x, router, w_gate, w_up, w_down, E: int, k: int, norm_topk_prob: 
     if world == 1:
         y_back = y
     else:
-        y_back = _exchange(y.view(torch.int32), recv_list, send_list,
-                           group).view(torch.float32)
-    ypair = torch.empty((N * k, H), dtype=torch.float32, device=x.device)
-    ypair[order] = y_back
+        y_back = (_exchange(y[0].view(torch.int32), recv_list, send_list,
+                            group).view(torch.bfloat16),
+                  _exchange(y[1].view(torch.int32), recv_list, send_list,
+                            group).view(torch.int8))
+    ypair = (torch.empty((N * k, H), dtype=torch.bfloat16, device=x.device),
+             torch.empty((N * k, H), dtype=torch.int8, device=x.device))
+    ypair[0][order] = y_back[0]
+    ypair[1][order] = y_back[1]
     if yshared is None:
         return combine_fn(ypair, N, k)
     return combine_fn(ypair, N, k, yshared)

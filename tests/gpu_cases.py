@@ -89,6 +89,15 @@ def run_forward(shape, dev, x=None, workspace=None):
     return out, workspace
 
 
+def decode_pair_rows(y) -> np.ndarray:
+    """The values held by pair rows (hi bf16, res int8), as moe.h defines the
+    format: v = hi + res * 2^(f - 142), f = max(16, exponent field of hi)."""
+    hi = y[0].float().cpu()
+    res = y[1].cpu().to(torch.float64)
+    f = ((hi.view(torch.int32) >> 23) & 0xFF).clamp(min=16).to(torch.float64)
+    return (hi.double() + res * torch.pow(2.0, f - 142)).numpy()
+
+
 def error_stats(out, ref):
     got = out.float().cpu().numpy().astype(np.float64) if torch.is_tensor(out) else out
     err = np.abs(got - ref)

@@ -52,7 +52,8 @@ def test_layout_is_consistent(L):
         cap = lay["capacity"]
         assert cap == L.moe_align_capacity(N, k, E, 128)
         assert lay["ypair"] >= lay["act"] + 4 * cap * I          # bf16 hi/lo or fp16 act
-        assert lay["total"] >= lay["ypair"] + 4 * N * k * H      # fp32 pair outputs
+        assert lay["ypair_res"] >= lay["ypair"] + 2 * N * k * H  # pair rows: bf16 plane,
+        assert lay["total"] >= lay["ypair_res"] + N * k * H      # then the int8 plane
 
 
 def _fwd(L, N=64, H=2048, E=128, I=768, I_s=0, k=8, ws_bytes=None, shared=(None,) * 4,
@@ -108,7 +109,7 @@ def _experts(L, R=64, H=2048, E=16, I=768, x=FAKE, ids=FAKE, y=FAKE, ws=FAKE * 1
     if ws_bytes is None:
         ws_bytes = L.moe_experts_workspace_bytes(R, H, E, I)
     fn = L.moe_experts_prepared if prepared else L.moe_experts
-    return fn(x, ids, FAKE, R, H, E, I, FAKE, FAKE, FAKE, y, ws, ws_bytes, None)
+    return fn(x, ids, FAKE, R, H, E, I, FAKE, FAKE, FAKE, y, FAKE, ws, ws_bytes, None)
 
 
 @pytest.mark.parametrize("prepared", [False, True])
@@ -129,11 +130,13 @@ def test_experts_and_combine_argument_errors(L, prepared):
     assert experts(L, ws_bytes=need - 1) == SMALL
     assert experts(L, R=0, x=None) == OK          # no-op, nothing launched
     P = FAKE
-    assert L.moe_combine(P, None, 16, 2048, 0, P, None) == INVALID
-    assert L.moe_combine(P, None, 16, 2044, 2, P, None) == INVALID
-    assert L.moe_combine(None, None, 16, 2048, 2, P, None) == INVALID
-    assert L.moe_combine(P, P + 2, 16, 2048, 2, P, None) == INVALID
-    assert L.moe_combine(P, None, 0, 2048, 2, None, None) == OK
+    assert L.moe_combine(P, P, None, None, 16, 2048, 0, P, None) == INVALID
+    assert L.moe_combine(P, P, None, None, 16, 2044, 2, P, None) == INVALID
+    assert L.moe_combine(None, P, None, None, 16, 2048, 2, P, None) == INVALID
+    assert L.moe_combine(P, None, None, None, 16, 2048, 2, P, None) == INVALID
+    assert L.moe_combine(P, P, P, None, 16, 2048, 2, P, None) == INVALID   # one shared plane
+    assert L.moe_combine(P, P, P + 2, P, 16, 2048, 2, P, None) == INVALID  # misaligned
+    assert L.moe_combine(P, P, None, None, 0, 2048, 2, None, None) == OK
 
 
 def test_dense_mlp_argument_errors(L):

@@ -21,21 +21,31 @@ def _free_port():
         return s.getsockname()[1]
 
 
+def _rows(v):
+    """Stand-in pair rows of values v: a bf16 plane and an int8 plane that
+    both depend on v (the exchange must carry both bit for bit)."""
+    hi = v.to(torch.bfloat16)
+    res = ((v - hi.float()) * 4096).round().clamp(-127, 127).to(torch.int8)
+    return hi, res
+
+
 def _pair_value(row, e, w):
     """Stand-in for w * Expert_e(row): any function of all three inputs."""
     return (w * (row.float() * (e + 1) + e)).to(torch.float32)
 
 
 def _combine(ypair, n, k, yshared=None):
-    acc = ypair.float().view(n, k, -1).sum(dim=1)
+    def val(y):
+        return y[0].float() + y[1].float() / 4096
+    acc = val(ypair).view(n, k, -1).sum(dim=1)
     if yshared is not None:
-        acc = acc + yshared.float()
+        acc = acc + val(yshared)
     return acc.to(torch.bfloat16)
 
 
 def _shared_value(x, gamma):
-    """Stand-in for gamma * SharedMLP(x) (fp32), token-local."""
-    return (gamma[:, None] * (0.5 * x.float() - 1.0)).to(torch.float32)
+    """Stand-in for gamma * SharedMLP(x), token-local."""
+    return _rows((gamma[:, None] * (0.5 * x.float() - 1.0)).to(torch.float32))
 
 
 def _inputs(rank, N, H, E, k, all_to_rank0):
@@ -65,17 +75,17 @@ def _worker(rank, world, port, q, N, H, E, k, all_to_rank0, with_shared=False):
             if local_ids.numel():
                 assert int(local_ids.min()) >= 0 and int(local_ids.max()) < E_local
             ge = local_ids.long() + rank * E_local
-            return torch.stack([_pair_value(rows[i], int(ge[i]), float(weights[i]))
-                                for i in range(rows.shape[0])]) if rows.shape[0] else \
-                torch.empty((0, H), dtype=torch.float32)
+            return _rows(torch.stack([_pair_value(rows[i], int(ge[i]), float(weights[i]))
+                                      for i in range(rows.shape[0])]) if rows.shape[0] else
+                         torch.empty((0, H), dtype=torch.float32))
 
         gamma = torch.sigmoid(x.float()[:, 0]) if with_shared else None
         out = ep_forward(x, None, None, None, None, E, k, group=None,
                          route_fn=lambda t: (w, ids, gamma), experts_fn=experts_fn,
                          shared_fn=_shared_value if with_shared else None,
                          combine_fn=_combine)
-        ref_pairs = torch.stack([_pair_value(x[p // k], int(ids.view(-1)[p]), float(w.view(-1)[p]))
-                                 for p in range(N * k)])
+        ref_pairs = _rows(torch.stack([_pair_value(x[p // k], int(ids.view(-1)[p]),
+                                                   float(w.view(-1)[p])) for p in range(N * k)]))
         ref = _combine(ref_pairs, N, k, _shared_value(x, gamma) if with_shared else None)
         q.put((rank, bool(torch.equal(out, ref)), calls[0]))
     finally:

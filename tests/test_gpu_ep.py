@@ -11,8 +11,8 @@ import pytest
 import torch
 
 import oracle
-from gpu_cases import (FORMS, assert_close, oracle_outputs, prepare, prepared, run_forward,
-                       shared_of)
+from gpu_cases import (FORMS, assert_close, decode_pair_rows, oracle_outputs, prepare, prepared,
+                       run_forward, shared_of)
 from sparse_moe_ffn_gb300 import binding
 from sparse_moe_ffn_gb300.ep import ep_forward, ep_plan
 from sparse_moe_ffn_gb300.inputs import MoEShape
@@ -22,7 +22,8 @@ pytestmark = pytest.mark.gpu
 
 def _pairs(shape, ws):
     v = binding.workspace_views(ws, shape.N, shape.H, shape.E, shape.I, shape.k)
-    return v["topk_w"].reshape(-1).clone(), v["topk_ids"].reshape(-1).clone(), v["ypair"].clone()
+    return (v["topk_w"].reshape(-1).clone(), v["topk_ids"].reshape(-1).clone(),
+            tuple(t.clone() for t in v["ypair"]))
 
 
 @pytest.mark.parametrize("form", FORMS)
@@ -35,7 +36,7 @@ def test_experts_rows_and_combine_match_forward(name, form):
     y, ews = binding.moe_experts(rows, ids, w, dev["w_gate"], dev["w_up"], dev["w_down"])
     torch.cuda.synchronize()
     assert binding.moe_read_device_status(ews) == 0
-    assert torch.equal(y, ypair)
+    assert torch.equal(y[0], ypair[0]) and torch.equal(y[1], ypair[1])
     assert torch.equal(binding.moe_combine(ypair, shape.N, shape.k), out)
 
 
@@ -61,7 +62,7 @@ def test_expert_slices_in_one_process_equal_forward(name, world):
     out, ws = run_forward(shape, dev)
     w, ids, _ = _pairs(shape, ws)
     order, dest, counts, E_loc = ep_plan(ids.view(shape.N, shape.k), shape.E, world)
-    ypair = torch.empty((shape.N * shape.k, shape.H), dtype=torch.float32, device="cuda")
+    ypair = binding.alloc_pair_rows(shape.N * shape.k, shape.H)
     start = 0
     for r in range(world):
         n_r = int(counts[r])
@@ -76,7 +77,8 @@ def test_expert_slices_in_one_process_equal_forward(name, world):
                                      dev["w_down"][e0:e1])
         torch.cuda.synchronize()
         assert binding.moe_read_device_status(ews) == 0
-        ypair[sel] = y
+        ypair[0][sel] = y[0]
+        ypair[1][sel] = y[1]
     got = binding.moe_combine(ypair, shape.N, shape.k)
     assert torch.equal(got, out)
     assert_close(got, oracle_outputs(name), f"{name} world {world}")
@@ -104,4 +106,4 @@ def test_experts_with_empty_experts_and_one_row():
                     "w_gate": wbits["w_gate"][e:e + 1], "w_up": wbits["w_up"][e:e + 1],
                     "w_down": wbits["w_down"][e:e + 1]}
             ref[sel] = oracle.moe_forward(bits, 1, True) * w_h[sel, None]
-        assert_close(y, ref, f"R={R}")
+        assert_close(decode_pair_rows(y), ref, f"R={R}")
