@@ -49,10 +49,10 @@ BOUND = {"tiny": "hbm", "decode": "hbm", "talker": "hbm", "prefill": "tensor", "
 STAGES = ("route", "align", "gather", "gate_up", "down", "shared", "combine")
 # kernel sources behind each stage (the GEMM stages run the one-CTA, the
 # sparse-block or the CTA-pair kernel depending on the batch)
-GEMM_SOURCES = ("grouped_gemm.cu", "sparse_gemm.cu", "pair_gemm.cu", "gemm_common.cuh")
+GEMM_SOURCES = ("grouped_gemm.cu", "sparse_gemm.cu", "pair_gemm.cu", "gemm_common.cuh", "pair_rows.cuh")
 SOURCES = {"route": ("router.cu",), "align": ("align.cu",), "gather": ("grouped_gemm.cu",),
            "gate_up": GEMM_SOURCES, "down": GEMM_SOURCES, "shared": GEMM_SOURCES,
-           "combine": ("combine.cu",)}
+           "combine": ("combine.cu", "pair_rows.cuh")}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 
 
@@ -253,42 +253,51 @@ def time_oracle(shape, bits, target_s: float):
 
 def time_prefill(args, device, peaks):
     """The prefill workload (N=8192) timed on this GPU through both forms of
-    the down weights: layer ms per call, and the grouped GEMMs (gate/up and
-    down, from the start of gate/up to the end of down, with no event
-    between them so that their hand-off overlap is kept) against the bf16
-    tensor peak."""
+    the down weights: layer ms per call (median of three rounds that
+    alternate the two forms, so that a clock or thermal drift hits both
+    alike), and the grouped GEMMs (gate/up and down, from the start of
+    gate/up to the end of down, with no event between them so that their
+    hand-off overlap is kept) against the bf16 tensor peak."""
     from sparse_moe_ffn_gb300 import binding
 
     shape = CONFIGS["prefill"]
     cpu = make_inputs(shape, seed=args.seed)
     d_bf16 = to_device(cpu, device)
     del cpu
+    forms = {"bf16_down": d_bf16, "f16_down_prepared": binding.prepare_weights(d_bf16)}
     ws = binding.alloc_workspace(shape.N, shape.H, shape.E, shape.I, shape.k, shape.I_s, device)
     out = torch.empty((shape.N, shape.H), dtype=torch.bfloat16, device=device)
-    steps, warm = args.prefill_steps, 5
+    steps, warm, rounds = args.prefill_steps, 5, 3
     _, sflops, layer_flops, _ = algorithmic_work(shape, shape.E)
     gemm_flops = sflops["gate_up"] + sflops["down"]
-    rec = {"workload": WORKLOADS["prefill"], "steps": steps, "warmup": warm}
-    for form, d in (("bf16_down", d_bf16), ("f16_down_prepared", None)):
-        if d is None:
-            d = binding.prepare_weights(d_bf16)
+    rec = {"workload": WORKLOADS["prefill"], "steps": steps, "warmup": warm, "rounds": rounds}
 
-        def step():
-            binding.moe_forward(d["x"], d["router"], d["w_gate"], d["w_up"], d["w_down"],
-                                shape.k, shape.norm_topk_prob, None, out=out, workspace=ws)
+    def step(d):
+        binding.moe_forward(d["x"], d["router"], d["w_gate"], d["w_up"], d["w_down"], shape.k,
+                            shape.norm_topk_prob, None, out=out, workspace=ws)
 
+    for form, d in forms.items():
         for _ in range(warm):
-            step()
-        torch.cuda.synchronize()
-        check_status(ws, f"prefill warm-up ({form})")
-        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s0.record()
-        for _ in range(steps):
-            step()
-        s1.record()
-        torch.cuda.synchronize()
-        check_status(ws, f"prefill timed steps ({form})")
-        ms = s0.elapsed_time(s1) / steps
+            step(d)
+    torch.cuda.synchronize()
+    check_status(ws, "prefill warm-up")
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    sampler.start()
+    t0 = time.time()
+    times = {form: [] for form in forms}
+    for _ in range(rounds):
+        for form, d in forms.items():
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record()
+            for _ in range(steps):
+                step(d)
+            s1.record()
+            torch.cuda.synchronize()
+            times[form].append(s0.elapsed_time(s1) / steps)
+    t1 = time.time()
+    check_status(ws, "prefill timed steps")
+    for form, d in forms.items():
+        ms = statistics.median(times[form])
         # grouped GEMMs: events before gate/up and after down only
         evs = []
         for _ in range(steps):
@@ -297,7 +306,7 @@ def time_prefill(args, device, peaks):
             e[STAGES.index("shared")] = torch.cuda.Event(enable_timing=True)
             evs.append(e)
             binding.set_stage_events(e)
-            step()
+            step(d)
         binding.set_stage_events(None)
         torch.cuda.synchronize()
         gemm_ms = statistics.mean(e[STAGES.index("gate_up")].elapsed_time(e[STAGES.index("shared")])
@@ -305,7 +314,8 @@ def time_prefill(args, device, peaks):
         achieved = gemm_flops / (gemm_ms / 1e3) / 1e12
         rec[form] = {
             "entry": "moe_forward_prepared" if form.startswith("f16") else "moe_forward",
-            "ms_per_step": round(ms, 5), "tokens_per_s": round(shape.N / (ms / 1e3), 1),
+            "ms_per_step": round(ms, 5), "ms_per_round": [round(t, 5) for t in times[form]],
+            "tokens_per_s": round(shape.N / (ms / 1e3), 1),
             "tflops": round(layer_flops / (ms / 1e3) / 1e12, 2),
             "layer_frac_of_bf16_peak": round(layer_flops / (ms / 1e3) / 1e12
                                              / peaks["bf16_tflops"], 4),
@@ -316,9 +326,9 @@ def time_prefill(args, device, peaks):
                          "window": "CUDA events before the gate/up launch and after the down "
                                    "launch, a separate pass of the same steps"},
         }
-        if d is not d_bf16:
-            del d
-    del d_bf16, ws, out
+    check_status(ws, "prefill GEMM pass")
+    rec["clocks"] = ClockSampler.summarize(sampler.stop(), t0, t1)
+    del forms, d_bf16, ws, out
     torch.cuda.empty_cache()
     return rec
 

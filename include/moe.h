@@ -300,6 +300,47 @@ moe_status_t moe_combine(const moe_bf16_t *ypair_hi, const int8_t *ypair_res,
                          const moe_bf16_t *yshared_hi, const int8_t *yshared_res,
                          int64_t N, int H, int k, moe_bf16_t *out, cudaStream_t stream);
 
+/* moe_combine over pair rows held in another order: pair p = n*k + j reads
+ * row row_index[p] of yrows ([num_rows, H] pair rows; the order in which
+ * expert-parallel results come back, moe_ep_dispatch's inv_order).  An index
+ * outside [0, num_rows) (a pair that was never sent) contributes nothing.
+ * row_index: [N*k] int32 on the device. */
+moe_status_t moe_combine_indexed(const moe_bf16_t *yrows_hi, const int8_t *yrows_res,
+                                 int64_t num_rows, const int32_t *row_index,
+                                 const moe_bf16_t *yshared_hi, const int8_t *yshared_res,
+                                 int64_t N, int H, int k, moe_bf16_t *out,
+                                 cudaStream_t stream);
+
+/* -------------------------------------------------------------------------
+ * moe_ep_dispatch -- the sending side of expert-parallel dispatch (M03 drill,
+ * level-3 follow-up: the (token, expert) table drives an all-to-all), on the
+ * device.  The layer's E experts are split over `world` ranks, rank r owning
+ * [r*E_r, (r+1)*E_r) with E_r = ceil(E / world).  For this rank's routed
+ * tokens:
+ *   send_counts [world] int32 out: pairs whose expert rank r owns
+ *   send rows i = 0 .. N*k-1 (those with a valid id) in rank order, pairs
+ *     in ascending p = n*k + j within a rank:
+ *     send_x   [N*k, H] bf16 out: x[p / k]
+ *     send_ids [N*k] int32 out: the expert id local to its rank, id - r*E_r
+ *     send_w   [N*k] fp32 out: topk_w[p]
+ *   inv_order [N*k] int32 out: the send row of pair p (-1 for an id outside
+ *     [0, E), which is also recorded as MOE_ERR_DEVICE_CHECK), i.e. the row
+ *     index moe_combine_indexed takes once the results come back in send
+ *     order
+ *   x [N, H] bf16, topk_ids / topk_w [N, k] (moe_route's outputs)
+ *   workspace >= moe_ep_dispatch_workspace_bytes(N, k, world), 256-byte
+ *     aligned; its first 4 bytes are the status word
+ * The grouping is moe_align's, with `world` groups and blocks of one row.
+ * Limits: 1 <= world <= 1024, N*k < 2^30.
+ * ---------------------------------------------------------------------- */
+size_t moe_ep_dispatch_workspace_bytes(int64_t N, int k, int world);
+moe_status_t moe_ep_dispatch(const moe_bf16_t *x, const int32_t *topk_ids,
+                             const float *topk_w, int64_t N, int H, int k, int E,
+                             int world, moe_bf16_t *send_x, int32_t *send_ids,
+                             float *send_w, int32_t *send_counts, int32_t *inv_order,
+                             void *workspace, size_t workspace_bytes,
+                             cudaStream_t stream);
+
 /* -------------------------------------------------------------------------
  * moe_convert_bf16_to_f16 -- the load-time step that makes the fp16 down
  * weights the *_prepared entry points take: dst[i] = fp16(src[i]) for i < n, round to

@@ -9,7 +9,8 @@ import importlib
 from .inputs import CONFIGS, MoEShape, make_inputs, to_device  # noqa: F401
 
 _BINDING_NAMES = ("moe_route", "moe_route_raw", "moe_align", "moe_align_noalloc", "moe_forward",
-                  "moe_forward_from_host", "moe_experts", "moe_combine", "alloc_pair_rows", "moe_dense_mlp",
+                  "moe_forward_from_host", "moe_experts", "moe_combine", "moe_combine_indexed",
+                  "moe_ep_dispatch", "alloc_pair_rows", "moe_dense_mlp",
                   "moe_add_rmsnorm", "prepare_weights", "convert_bf16_to_f16", "ForwardGraph",
                   "ForwardGraphSet", "decode_loop", "DECODE_BUCKETS",
                   "moe_status_string", "moe_forward_workspace_bytes", "moe_forward_layout",

@@ -68,6 +68,9 @@ def lib():
         "moe_experts": ([P, P, P, i64, i32, i32, i32, P, P, P, P, P, P, sz, P], i32),
         "moe_experts_prepared": ([P, P, P, i64, i32, i32, i32, P, P, P, P, P, P, sz, P], i32),
         "moe_combine": ([P, P, P, P, i64, i32, i32, P, P], i32),
+        "moe_combine_indexed": ([P, P, i64, P, P, P, i64, i32, i32, P, P], i32),
+        "moe_ep_dispatch_workspace_bytes": ([i64, i32, i32], sz),
+        "moe_ep_dispatch": ([P, P, P, i64, i32, i32, i32, i32, P, P, P, P, P, P, sz, P], i32),
         "moe_convert_bf16_to_f16": ([P, P, i64, P, P], i32),
         "moe_forward_layout": ([i64, i32, i32, i32, i32, i32, ctypes.POINTER(_Layout)], i32),
         "moe_read_device_status": ([P, P], i32),
@@ -360,6 +363,57 @@ def moe_combine(ypair, N: int, k: int, yshared=None, out=None):
     _check(lib().moe_combine(_ptr(ypair[0]), _ptr(ypair[1]), _ptr(sh[0]), _ptr(sh[1]), N, H, k,
                              _ptr(out), _stream()), "moe_combine")
     return out
+
+
+def moe_combine_indexed(yrows, row_index, N: int, k: int, yshared=None, out=None):
+    """moe_combine over pair rows in another order: pair p reads row
+    row_index[p] of yrows (pair rows (hi, res), [R, H]); an index outside
+    [0, R) contributes nothing."""
+    R, H = yrows[0].shape
+    _check_pair_rows(yrows, R, H, "yrows")
+    if (row_index.dtype != torch.int32 or tuple(row_index.shape) != (N * k,) or
+            not row_index.is_cuda or not row_index.is_contiguous()):
+        raise ValueError("row_index must be a contiguous int32 CUDA tensor of shape [N*k]")
+    if yshared is not None:
+        _check_pair_rows(yshared, N, H, "yshared")
+    sh = yshared if yshared is not None else (None, None)
+    if out is None:
+        out = torch.empty((N, H), dtype=torch.bfloat16, device=row_index.device)
+    _bf16(out, "out", (N, H))
+    _check(lib().moe_combine_indexed(_ptr(yrows[0]), _ptr(yrows[1]), R, _ptr(row_index),
+                                     _ptr(sh[0]), _ptr(sh[1]), N, H, k, _ptr(out), _stream()),
+           "moe_combine_indexed")
+    return out
+
+
+def moe_ep_dispatch(x, topk_ids, topk_w, E: int, world: int):
+    """The sending side of expert-parallel dispatch on the device (moe.h):
+    returns a dict with send_x [N*k, H] bf16, send_ids [N*k] int32 (local
+    expert ids), send_w [N*k] fp32, send_counts [world] int32 (device),
+    inv_order [N*k] int32 and the workspace (status word first)."""
+    N, H = x.shape
+    _bf16(x, "x")
+    k = topk_ids.shape[1]
+    if topk_ids.dtype != torch.int32 or tuple(topk_ids.shape) != (N, k) or not topk_ids.is_cuda:
+        raise ValueError("topk_ids must be an int32 CUDA tensor of shape [N, k]")
+    if topk_w.dtype != torch.float32 or tuple(topk_w.shape) != (N, k) or not topk_w.is_cuda:
+        raise ValueError("topk_w must be a float32 CUDA tensor of shape [N, k]")
+    topk_ids, topk_w = topk_ids.contiguous(), topk_w.contiguous()
+    dev = x.device
+    P = N * k
+    r = {"send_x": torch.empty((P, H), dtype=torch.bfloat16, device=dev),
+         "send_ids": torch.empty(P, dtype=torch.int32, device=dev),
+         "send_w": torch.empty(P, dtype=torch.float32, device=dev),
+         "send_counts": torch.zeros(world, dtype=torch.int32, device=dev),
+         "inv_order": torch.empty(P, dtype=torch.int32, device=dev)}
+    L = lib()
+    wsb = int(L.moe_ep_dispatch_workspace_bytes(N, k, world))
+    r["workspace"] = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
+    _check(L.moe_ep_dispatch(_ptr(x), _ptr(topk_ids), _ptr(topk_w), N, H, k, E, world,
+                             _ptr(r["send_x"]), _ptr(r["send_ids"]), _ptr(r["send_w"]),
+                             _ptr(r["send_counts"]), _ptr(r["inv_order"]), _ptr(r["workspace"]),
+                             r["workspace"].numel(), _stream()), "moe_ep_dispatch")
+    return r
 
 
 def convert_bf16_to_f16(src, out=None, status=None):

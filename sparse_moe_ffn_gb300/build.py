@@ -21,7 +21,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libsparse_moe_ffn.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["api.cu", "router.cu", "align.cu", "grouped_gemm.cu", "pair_gemm.cu", "sparse_gemm.cu", "combine.cu", "selftest.cu",
-           "align_noalloc.cu", "rmsnorm.cu", "convert.cu"]
+           "align_noalloc.cu", "rmsnorm.cu", "convert.cu", "ep.cu"]
 
 
 def nvcc() -> str:

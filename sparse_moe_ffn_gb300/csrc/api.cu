@@ -782,7 +782,8 @@ static moe_status_t forward_impl(const moe_bf16_t *x, const moe_bf16_t *router,
 
     // K5: out[n] = sum_j ypair[n*k + j] (+ shared)
     if ((st = record_stage(MOE_STAGE_COMBINE, stream)) != MOE_OK) return st;
-    MOE_CUDA(launch_combine(ypair, ypair_res, y_shared, y_shared_res, N, H, k, out, sms, stream),
+    MOE_CUDA(launch_combine(ypair, ypair_res, nullptr, N * k, y_shared, y_shared_res, N, H, k, out,
+                            sms, stream),
              "combine kernel launch");
     g_launches += 1;
     if ((st = record_stage(MOE_NUM_STAGES, stream)) != MOE_OK) return st;
@@ -871,9 +872,10 @@ moe_status_t moe_experts_prepared(const moe_bf16_t *x_rows, const int32_t *ids,
                         y_res, workspace, workspace_bytes, stream);
 }
 
-moe_status_t moe_combine(const moe_bf16_t *ypair_hi, const int8_t *ypair_res,
-                         const moe_bf16_t *yshared_hi, const int8_t *yshared_res, int64_t N,
-                         int H, int k, moe_bf16_t *out, cudaStream_t stream) {
+static moe_status_t combine_impl(const moe_bf16_t *ypair_hi, const int8_t *ypair_res,
+                                 const int32_t *row_index, int64_t rows,
+                                 const moe_bf16_t *yshared_hi, const int8_t *yshared_res,
+                                 int64_t N, int H, int k, moe_bf16_t *out, cudaStream_t stream) {
     g_last_error.clear();
     if (N < 0 || H < 8 || H % 8 || k < 1)
         return fail(MOE_ERR_INVALID_ARG, "need N >= 0, H a positive multiple of 8, k >= 1");
@@ -886,9 +888,121 @@ moe_status_t moe_combine(const moe_bf16_t *ypair_hi, const int8_t *ypair_res,
         (yshared_hi && (!aligned16(yshared_hi) || !aligned16(yshared_res))))
         return fail(MOE_ERR_INVALID_ARG, "pair planes and out must be 16-byte aligned");
     if (N > (int64_t(1) << 31) / k) return fail(MOE_ERR_UNSUPPORTED, "N*k must stay below 2^31");
-    MOE_CUDA(launch_combine(ypair_hi, ypair_res, yshared_hi, yshared_res, N, H, k, out,
-                            num_sms_of_current_device(), stream),
+    if (rows < 0) return fail(MOE_ERR_INVALID_ARG, "num_rows must be >= 0");
+    MOE_CUDA(launch_combine(ypair_hi, ypair_res, row_index, rows, yshared_hi, yshared_res, N, H, k,
+                            out, num_sms_of_current_device(), stream),
              "combine kernel launch");
+    g_launches += 1;
+    return MOE_OK;
+}
+
+moe_status_t moe_combine(const moe_bf16_t *ypair_hi, const int8_t *ypair_res,
+                         const moe_bf16_t *yshared_hi, const int8_t *yshared_res, int64_t N,
+                         int H, int k, moe_bf16_t *out, cudaStream_t stream) {
+    return combine_impl(ypair_hi, ypair_res, nullptr, N * k, yshared_hi, yshared_res, N, H, k,
+                        out, stream);
+}
+
+moe_status_t moe_combine_indexed(const moe_bf16_t *yrows_hi, const int8_t *yrows_res,
+                                 int64_t num_rows, const int32_t *row_index,
+                                 const moe_bf16_t *yshared_hi, const int8_t *yshared_res,
+                                 int64_t N, int H, int k, moe_bf16_t *out, cudaStream_t stream) {
+    g_last_error.clear();
+    if (N > 0 && !row_index) return fail(MOE_ERR_INVALID_ARG, "row_index must be non-null");
+    if (N > 0 && num_rows > 0 && (!yrows_hi || !yrows_res))
+        return fail(MOE_ERR_INVALID_ARG, "yrows_hi and yrows_res must be non-null");
+    // nothing was sent (num_rows = 0): no row is read, so any aligned
+    // stand-in address passes the checks below
+    alignas(16) static const uint8_t kNone[16] = {};
+    const moe_bf16_t *hi = num_rows > 0 ? yrows_hi : reinterpret_cast<const moe_bf16_t *>(kNone);
+    const int8_t *res = num_rows > 0 ? yrows_res : reinterpret_cast<const int8_t *>(kNone);
+    return combine_impl(hi, res, row_index, num_rows, yshared_hi, yshared_res, N, H, k, out,
+                        stream);
+}
+
+// ------------------------------------------------- expert-parallel dispatch
+
+// workspace: status | dest [P] | pad_offsets [R+1] | align scratch |
+// order [P] | block owners [P] | offsets [R+1] | row count [1]
+struct EpLayout {
+    size_t status, dest, pad_offsets, scratch, order, owners, offsets, num_rows, total;
+};
+
+static EpLayout ep_layout(int64_t N, int k, int world) {
+    const int64_t P = N * k;
+    EpLayout L;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = round_up(off + bytes, kAlign);
+        return at;
+    };
+    L.status = take(4);
+    L.dest = take(sizeof(int32_t) * P);
+    L.pad_offsets = take(sizeof(int32_t) * (world + 1));
+    L.scratch = take(sizeof(int32_t) * static_cast<size_t>(align_chunks(P)) * world);
+    L.order = take(sizeof(int32_t) * P);
+    L.owners = take(sizeof(int32_t) * P);
+    L.offsets = take(sizeof(int32_t) * (world + 1));
+    L.num_rows = take(sizeof(int32_t));
+    L.total = off;
+    return L;
+}
+
+size_t moe_ep_dispatch_workspace_bytes(int64_t N, int k, int world) {
+    if (N < 0 || k < 1 || world < 1) return 0;
+    return ep_layout(N, k, world).total;
+}
+
+moe_status_t moe_ep_dispatch(const moe_bf16_t *x, const int32_t *topk_ids, const float *topk_w,
+                             int64_t N, int H, int k, int E, int world, moe_bf16_t *send_x,
+                             int32_t *send_ids, float *send_w, int32_t *send_counts,
+                             int32_t *inv_order, void *workspace, size_t workspace_bytes,
+                             cudaStream_t stream) {
+    g_last_error.clear();
+    if (N < 0 || H < 8 || H % 8 || k < 1 || E < 1 || world < 1)
+        return fail(MOE_ERR_INVALID_ARG, "need N >= 0, H a positive multiple of 8, k, E, world >= 1");
+    if (world > 1024) return fail(MOE_ERR_UNSUPPORTED, "world must be <= 1024");
+    if (N > (int64_t(1) << 30) / k) return fail(MOE_ERR_UNSUPPORTED, "N*k must stay below 2^30");
+    if (N == 0) return MOE_OK;
+    if (!x || !topk_ids || !topk_w || !send_x || !send_ids || !send_w || !send_counts ||
+        !inv_order || !workspace)
+        return fail(MOE_ERR_INVALID_ARG, "every moe_ep_dispatch pointer must be non-null");
+    if (!aligned16(x) || !aligned16(send_x))
+        return fail(MOE_ERR_INVALID_ARG, "x and send_x must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
+        return fail(MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    const EpLayout L = ep_layout(N, k, world);
+    if (workspace_bytes < L.total)
+        return fail(MOE_ERR_WORKSPACE_TOO_SMALL, "dispatch workspace needs %zu bytes, got %zu",
+                    L.total, workspace_bytes);
+    const int64_t P = N * k;
+    const int e_local = (E + world - 1) / world;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    int32_t *status = reinterpret_cast<int32_t *>(ws + L.status);
+    int32_t *dest = reinterpret_cast<int32_t *>(ws + L.dest);
+    const int sms = num_sms_of_current_device();
+    MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int32_t), stream), "status reset");
+    MOE_CUDA(launch_ep_dest(topk_ids, P, E, e_local, dest, inv_order, status, sms, stream),
+             "dispatch kernel launch");
+    g_launches += 1;
+    // group the pairs by destination rank: moe_align's kernels with `world`
+    // groups and blocks of one row (no padding: the grouped order is the
+    // send order, the counts are the send counts)
+    AlignBuffers b;
+    b.sorted_pair = reinterpret_cast<int32_t *>(ws + L.order);
+    b.block_expert = reinterpret_cast<int32_t *>(ws + L.owners);
+    b.counts = send_counts;
+    b.offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
+    b.pad_offsets = reinterpret_cast<int32_t *>(ws + L.pad_offsets);
+    b.num_padded = reinterpret_cast<int32_t *>(ws + L.num_rows);
+    b.scratch = reinterpret_cast<int32_t *>(ws + L.scratch);
+    b.status = status;
+    moe_status_t st = enqueue_align(dest, P, 1, world, 1, b, stream);
+    if (st != MOE_OK) return st;
+    MOE_CUDA(launch_ep_pack(x, topk_ids, topk_w, b.sorted_pair, b.num_padded, P, H, k, e_local,
+                            send_x, send_ids, send_w, inv_order, sms, stream),
+             "dispatch pack kernel launch");
     g_launches += 1;
     return MOE_OK;
 }
@@ -1141,7 +1255,7 @@ static moe_status_t dense_mlp_impl(const moe_bf16_t *x, const moe_bf16_t *w_gate
                  "dense down kernel launch");
     }
     // pair rows -> bf16 out (the combine with one slot per token)
-    MOE_CUDA(launch_combine(y, y_res, nullptr, nullptr, N, H, 1, out, sms, stream),
+    MOE_CUDA(launch_combine(y, y_res, nullptr, N, nullptr, nullptr, N, H, 1, out, sms, stream),
              "combine kernel launch");
     g_launches += 3;
     return MOE_OK;

@@ -47,6 +47,7 @@ __device__ __forceinline__ void add_pair8(float (&acc)[8], const uint16_t *hi_pl
 
 __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(const uint16_t *__restrict__ ypair_hi, const int8_t *__restrict__ ypair_res,
+                   const int32_t *__restrict__ row_index, int64_t rows,
                    const uint16_t *__restrict__ yshared_hi,
                    const int8_t *__restrict__ yshared_res, int64_t N, int H, int k,
                    uint16_t *__restrict__ out) {
@@ -59,9 +60,12 @@ __global__ void __launch_bounds__(kCombineThreads)
         const int64_t n = idx / groups;
         const int col = static_cast<int>(idx % groups) * 8;
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        const int64_t o = n * k * static_cast<int64_t>(H) + col;
-        for (int j = 0; j < k; ++j)
-            add_pair8(acc, ypair_hi, ypair_res, o + static_cast<int64_t>(j) * H);
+        for (int j = 0; j < k; ++j) {
+            const int64_t p = n * k + j;
+            const int64_t row = row_index ? static_cast<int64_t>(__ldcg(row_index + p)) : p;
+            if (row < 0 || row >= rows) continue;  // a pair that was never sent
+            add_pair8(acc, ypair_hi, ypair_res, row * H + col);
+        }
         if (yshared_hi) add_pair8(acc, yshared_hi, yshared_res, n * H + col);
         uint4 pk;
         pk.x = pack_bf16x2(acc[0], acc[1]);
@@ -75,14 +79,16 @@ __global__ void __launch_bounds__(kCombineThreads)
 }  // namespace
 
 cudaError_t launch_combine(const uint16_t *ypair_hi, const int8_t *ypair_res,
-                           const uint16_t *yshared_hi, const int8_t *yshared_res, int64_t N,
-                           int H, int k, uint16_t *out, int num_sms, cudaStream_t s) {
+                           const int32_t *row_index, int64_t rows, const uint16_t *yshared_hi,
+                           const int8_t *yshared_res, int64_t N, int H, int k, uint16_t *out,
+                           int num_sms, cudaStream_t s) {
     const int64_t total = N * (H / 8);
     int64_t blocks = (total + kCombineThreads - 1) / kCombineThreads;
     const int64_t cap = static_cast<int64_t>(num_sms) * 16;
     if (blocks > cap) blocks = cap;
     return launch_pdl(combine_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kCombineThreads),
-                      0, s, 1, ypair_hi, ypair_res, yshared_hi, yshared_res, N, H, k, out);
+                      0, s, 1, ypair_hi, ypair_res, row_index, rows, yshared_hi, yshared_res, N,
+                      H, k, out);
 }
 
 }  // namespace moe

@@ -143,6 +143,12 @@ struct GemmArgs {
     int act_ready_count;
     int max_tiles;      // upper bound on tiles (sizes the persistent grid)
     int grid;           // persistent CTAs
+    // CTA-pair kernel: weight_streaming (set by the host) asks for a deep
+    // weight ring and a shallow activation ring (experts with few row
+    // blocks, whose weights stream from HBM); ring_a / ring_b are the ring
+    // depths launch_pair_gemm derives from it
+    int weight_streaming;
+    int ring_a, ring_b;
 };
 
 // Tile widths: gate/up 96 or 128 columns (of each of gate and up), down 256.
@@ -185,10 +191,27 @@ cudaError_t launch_pair_gemm(GemmMode mode, const CUtensorMap &tm_a, const CUten
 
 // ----------------------------------------------------------------- combine
 
-// ypair / yshared: pair rows (bf16 hi plane, int8 residual plane)
+// ypair / yshared: pair rows (bf16 hi plane, int8 residual plane); pair p's
+// row is row_index[p] when row_index is given (the order in which
+// expert-parallel results come back; an index outside [0, rows) adds
+// nothing), else p
 cudaError_t launch_combine(const uint16_t *ypair_hi, const int8_t *ypair_res,
-                           const uint16_t *yshared_hi, const int8_t *yshared_res, int64_t N,
-                           int H, int k, uint16_t *out, int num_sms, cudaStream_t s);
+                           const int32_t *row_index, int64_t rows, const uint16_t *yshared_hi,
+                           const int8_t *yshared_res, int64_t N, int H, int k, uint16_t *out,
+                           int num_sms, cudaStream_t s);
+
+// ------------------------------------------- expert-parallel dispatch plan
+
+// dest[p] = ids[p] / e_local (-1 and MOE_ERR_DEVICE_CHECK for an id outside
+// [0, E)); inv[p] = -1
+cudaError_t launch_ep_dest(const int32_t *ids, int64_t P, int E, int e_local, int32_t *dest,
+                           int32_t *inv, int32_t *status, int num_sms, cudaStream_t s);
+// send row i <- pair order[i] (i < *num_rows): x row, local expert id,
+// weight; inv[order[i]] = i
+cudaError_t launch_ep_pack(const uint16_t *x, const int32_t *ids, const float *weights,
+                           const int32_t *order, const int32_t *num_rows, int64_t P, int H, int k,
+                           int e_local, uint16_t *send_x, int32_t *send_ids, float *send_w,
+                           int32_t *inv, int num_sms, cudaStream_t s);
 
 // ------------------------------------------- bf16 -> fp16 weight conversion
 

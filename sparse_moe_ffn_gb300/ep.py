@@ -8,17 +8,20 @@ Rank r owns experts [r * E_local, (r + 1) * E_local), E_local = ceil(E / R),
 and holds only their weights.  Per layer call, on every rank:
 
 1. route its N tokens over all E experts (moe_route: fp32 weights, ids);
-2. plan: pair p = n*k + j goes to rank ids[p] // E_local.  Pairs are sent
-   grouped by destination rank and in pair order within a rank (a stable
-   sort); the per-rank counts are exchanged first;
-3. dispatch: each pair's token row, its expert id local to the receiving
-   rank and its routing weight travel with one all_to_all each;
+2. dispatch plan, on the device (moe_ep_dispatch): pair p = n*k + j goes to
+   rank ids[p] // E_local; the pairs are grouped by destination rank, in
+   pair order within a rank (moe_align's grouping kernels with R groups),
+   and packed in that order: token rows, expert ids local to the receiving
+   rank, routing weights, the per-rank counts, and each pair's send row;
+3. exchange: the counts first (the one host synchronisation: all_to_all
+   needs the split sizes on the host), then the rows, ids and weights with
+   one all_to_all each;
 4. the receiving rank runs its experts on the rows it received
    (moe_experts: y = w * Expert(x) as pair rows, a bf16 plane and an int8
    residual plane);
-5. combine: the results travel back with the reverse all_to_all and land in
-   pair order (ypair[p]).  moe_combine then sums each token's k slots in slot
-   order.
+5. combine: the results travel back with the reverse all_to_all, in send
+   order, and moe_combine_indexed sums each token's k slots in slot order,
+   reading pair p's row at its send row.
 
 Step 4 computes each pair as moe_forward does, and step 5 is moe_forward's
 own combine.  So the output equals moe_forward on the same tokens bit for
@@ -31,9 +34,12 @@ weight, which is moe_forward's shared term gamma * SharedMLP(x); the combine
 adds it after the k slots.
 
 Transport: gloo and NCCL both carry int32, so bf16 rows and int8 residual
-rows travel as their bit patterns viewed as int32 (H is a multiple of 8).  With one rank nothing is
-exchanged.  The three compute steps can be replaced (route_fn, experts_fn,
-combine_fn), which is how the exchange logic is tested on CPU ranks.
+rows travel as their bit patterns viewed as int32 (H is a multiple of 8).
+With one rank nothing is exchanged.  The compute steps can be replaced
+(route_fn, dispatch_fn, experts_fn, shared_fn, combine_fn), which is how the
+exchange logic is tested on CPU ranks; ``ep_dispatch_reference`` is the
+dispatch plan written with host tensor operations for that purpose (and the
+reference the device plan is tested against).
 """
 from __future__ import annotations
 
@@ -60,6 +66,20 @@ def ep_plan(ids: torch.Tensor, E: int, world: int):
     return order, dest, send_counts, E_local
 
 
+def ep_dispatch_reference(x, ids, w, E: int, world: int):
+    """The dispatch plan of step 2 with torch operations (CPU ranks, tests):
+    returns (send_x, send_ids, send_w, send_counts, inv_order) as
+    moe_ep_dispatch defines them."""
+    order, dest, send_counts, E_local = ep_plan(ids, E, world)
+    k = ids.shape[1]
+    send_x = x.index_select(0, order // k)
+    send_e = (ids.reshape(-1).long()[order] - dest[order] * E_local).to(torch.int32)
+    send_w = w.reshape(-1)[order].contiguous()
+    inv = torch.empty_like(order)
+    inv[order] = torch.arange(order.numel(), device=order.device)
+    return send_x, send_e, send_w, send_counts.to(torch.int32), inv.to(torch.int32)
+
+
 def _world(group):
     if not dist.is_available() or not dist.is_initialized():
         return 1
@@ -77,8 +97,8 @@ def _exchange(t: torch.Tensor, send_counts, recv_counts, group):
 
 
 def ep_forward(x, router, w_gate, w_up, w_down, E: int, k: int, norm_topk_prob: bool = True,
-               group=None, shared=None, route_fn=None, experts_fn=None, shared_fn=None,
-               combine_fn=None):
+               group=None, shared=None, route_fn=None, dispatch_fn=None, experts_fn=None,
+               shared_fn=None, combine_fn=None):
     """One MoE layer with experts split across the ranks of ``group``.
 
     x [N, H] bf16 (this rank's tokens), router [E, H] bf16 (all experts);
@@ -86,8 +106,10 @@ def ep_forward(x, router, w_gate, w_up, w_down, E: int, k: int, norm_topk_prob: 
     copy of binding.prepare_weights): this rank's experts.  ``shared``: None
     or the shared expert (binding.SHARED_KEYS, shared_down_proj in the same
     form as w_down), the same on every rank.  route_fn(x) returns (weights,
-    ids) or (weights, ids, gamma); experts_fn and shared_fn return pair rows
-    (hi bf16, res int8), each [rows, H].
+    ids) or (weights, ids, gamma); dispatch_fn(x, ids, w, E, world) returns
+    (send_x, send_ids, send_w, send_counts, inv_order); experts_fn and
+    shared_fn return pair rows (hi bf16, res int8), each [rows, H];
+    combine_fn(yrows, inv_order, N, k, yshared) returns the output.
     Returns out [N, H] bf16."""
     from sparse_moe_ffn_gb300 import binding
 
@@ -107,19 +129,20 @@ def ep_forward(x, router, w_gate, w_up, w_down, E: int, k: int, norm_topk_prob: 
             return binding.moe_experts(t, zeros, gamma, shared["shared_gate_proj"][None],
                                        shared["shared_up_proj"][None],
                                        shared["shared_down_proj"][None])[0]
+    if dispatch_fn is None:
+        def dispatch_fn(t, ids_, w_, E_, world_):
+            d = binding.moe_ep_dispatch(t, ids_, w_, E_, world_)
+            return d["send_x"], d["send_ids"], d["send_w"], d["send_counts"], d["inv_order"]
     if combine_fn is None:
-        def combine_fn(ypair, n, kk, yshared=None):
-            return binding.moe_combine(ypair, n, kk, yshared)
+        def combine_fn(yrows, inv, n, kk, yshared=None):
+            return binding.moe_combine_indexed(yrows, inv, n, kk, yshared)
 
     routed = route_fn(x)
     w, ids = routed[0], routed[1]
     gamma = routed[2] if len(routed) > 2 else None
     # the shared term needs no exchange: it can run before the dispatch
     yshared = shared_fn(x, gamma) if shared_fn is not None else None
-    order, dest, send_counts, E_local = ep_plan(ids, E, world)
-    send_x = x.index_select(0, order // k)
-    send_e = (ids.reshape(-1).long()[order] - dest[order] * E_local).to(torch.int32)
-    send_w = w.reshape(-1)[order].contiguous()
+    send_x, send_e, send_w, send_counts, inv = dispatch_fn(x, ids, w, E, world)
     if world == 1:
         recv_x, recv_e, recv_w = send_x, send_e, send_w
     else:
@@ -129,10 +152,11 @@ def ep_forward(x, router, w_gate, w_up, w_down, E: int, k: int, norm_topk_prob: 
         rc = torch.empty_like(sc)
         dist.all_to_all_single(rc, sc, group=group)
         send_list, recv_list = sc.tolist(), rc.tolist()
-        recv_x = _exchange(send_x.view(torch.int32), send_list, recv_list,
+        n_send = sum(send_list)
+        recv_x = _exchange(send_x[:n_send].view(torch.int32), send_list, recv_list,
                            group).view(torch.bfloat16)
-        recv_e = _exchange(send_e, send_list, recv_list, group)
-        recv_w = _exchange(send_w.view(torch.int32), send_list, recv_list,
+        recv_e = _exchange(send_e[:n_send], send_list, recv_list, group)
+        recv_w = _exchange(send_w[:n_send].view(torch.int32), send_list, recv_list,
                            group).view(torch.float32)
     y = experts_fn(recv_x, recv_e, recv_w)
     if world == 1:
@@ -142,10 +166,4 @@ def ep_forward(x, router, w_gate, w_up, w_down, E: int, k: int, norm_topk_prob: 
                             group).view(torch.bfloat16),
                   _exchange(y[1].view(torch.int32), recv_list, send_list,
                             group).view(torch.int8))
-    ypair = (torch.empty((N * k, H), dtype=torch.bfloat16, device=x.device),
-             torch.empty((N * k, H), dtype=torch.int8, device=x.device))
-    ypair[0][order] = y_back[0]
-    ypair[1][order] = y_back[1]
-    if yshared is None:
-        return combine_fn(ypair, N, k)
-    return combine_fn(ypair, N, k, yshared)
+    return combine_fn(y_back, inv, N, k, yshared)

@@ -178,3 +178,26 @@ def test_stage_events_argument_check(L):
     assert L.moe_set_stage_events(None, 0) == OK
     arr = (ctypes.c_void_p * 3)()
     assert L.moe_set_stage_events(arr, 3) == INVALID
+
+
+def test_dispatch_and_indexed_combine_argument_errors(L):
+    P = FAKE
+    need = L.moe_ep_dispatch_workspace_bytes(64, 8, 2)
+    assert need > 0 and L.moe_ep_dispatch_workspace_bytes(-1, 8, 2) == 0
+
+    def disp(N=64, H=2048, k=8, E=128, world=2, x=P, ws=P * 16, ws_bytes=need):
+        return L.moe_ep_dispatch(x, P, P, N, H, k, E, world, P, P, P, P, P, ws, ws_bytes, None)
+
+    assert disp(world=0) == INVALID
+    assert disp(H=2044) == INVALID
+    assert disp(world=2000) == UNSUPPORTED
+    assert disp(x=None) == INVALID
+    assert disp(x=P + 2) == INVALID
+    assert disp(ws=P * 16 + 64) == INVALID
+    assert disp(ws_bytes=need - 1) == SMALL
+    assert disp(N=0, x=None) == OK
+    # indexed combine: row_index required, both shared planes or neither
+    assert L.moe_combine_indexed(P, P, 10, None, None, None, 4, 2048, 2, P, None) == INVALID
+    assert L.moe_combine_indexed(P, P, 10, P, P, None, 4, 2048, 2, P, None) == INVALID
+    assert L.moe_combine_indexed(P, P, -1, P, None, None, 4, 2048, 2, P, None) == INVALID
+    assert L.moe_combine_indexed(None, None, 0, None, None, None, 0, 2048, 2, None, None) == OK

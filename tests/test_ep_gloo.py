@@ -12,7 +12,7 @@ import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
 
-from sparse_moe_ffn_gb300.ep import ep_plan
+from sparse_moe_ffn_gb300.ep import ep_dispatch_reference, ep_plan
 
 
 def _free_port():
@@ -43,6 +43,12 @@ def _combine(ypair, n, k, yshared=None):
     return acc.to(torch.bfloat16)
 
 
+def _combine_rows(yrows, inv, n, k, yshared=None):
+    """Stand-in combine over rows in send order: pair p reads row inv[p]."""
+    idx = inv.long()
+    return _combine((yrows[0][idx], yrows[1][idx]), n, k, yshared)
+
+
 def _shared_value(x, gamma):
     """Stand-in for gamma * SharedMLP(x), token-local."""
     return _rows((gamma[:, None] * (0.5 * x.float() - 1.0)).to(torch.float32))
@@ -63,7 +69,7 @@ def _worker(rank, world, port, q, N, H, E, k, all_to_rank0, with_shared=False):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     import sys
     sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
-    from sparse_moe_ffn_gb300.ep import ep_forward
+    from sparse_moe_ffn_gb300.ep import ep_dispatch_reference, ep_forward
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
         x, ids, w = _inputs(rank, N, H, E, k, all_to_rank0)
@@ -83,7 +89,7 @@ def _worker(rank, world, port, q, N, H, E, k, all_to_rank0, with_shared=False):
         out = ep_forward(x, None, None, None, None, E, k, group=None,
                          route_fn=lambda t: (w, ids, gamma), experts_fn=experts_fn,
                          shared_fn=_shared_value if with_shared else None,
-                         combine_fn=_combine)
+                         dispatch_fn=ep_dispatch_reference, combine_fn=_combine_rows)
         ref_pairs = _rows(torch.stack([_pair_value(x[p // k], int(ids.view(-1)[p]),
                                                    float(w.view(-1)[p])) for p in range(N * k)]))
         ref = _combine(ref_pairs, N, k, _shared_value(x, gamma) if with_shared else None)
@@ -143,3 +149,23 @@ def test_plan_properties_on_random_routing(world):
             mine = order[d_sorted == r]
             assert torch.all(mine[1:] > mine[:-1])  # stable: pair order within a rank
         assert counts.tolist() == [int((dest == r).sum()) for r in range(world)]
+
+
+def test_reference_dispatch_packs_rows_in_send_order():
+    """The host reference of the dispatch plan: send row i is pair order[i]
+    (its token row, local expert id and weight), and inv_order inverts the
+    order, so reading row inv[p] gives pair p back."""
+    g = torch.Generator().manual_seed(7)
+    N, H, E, k, world = 9, 8, 7, 3, 3
+    x = torch.randn(N, H, generator=g).to(torch.bfloat16)
+    ids = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(N)]).to(torch.int32)
+    w = torch.rand(N, k, generator=g)
+    send_x, send_e, send_w, counts, inv = ep_dispatch_reference(x, ids, w, E, world)
+    order, dest, _, E_local = ep_plan(ids, E, world)
+    assert counts.tolist() == [int((dest == r).sum()) for r in range(world)]
+    for p in range(N * k):
+        i = int(inv[p])
+        assert int(order[i]) == p
+        assert torch.equal(send_x[i], x[p // k])
+        assert int(send_e[i]) == int(ids.view(-1)[p]) - int(dest[p]) * E_local
+        assert float(send_w[i]) == float(w.view(-1)[p])

@@ -14,7 +14,7 @@ import oracle
 from gpu_cases import (FORMS, assert_close, decode_pair_rows, oracle_outputs, prepare, prepared,
                        run_forward, shared_of)
 from sparse_moe_ffn_gb300 import binding
-from sparse_moe_ffn_gb300.ep import ep_forward, ep_plan
+from sparse_moe_ffn_gb300.ep import ep_dispatch_reference, ep_forward, ep_plan
 from sparse_moe_ffn_gb300.inputs import MoEShape
 
 pytestmark = pytest.mark.gpu
@@ -56,32 +56,76 @@ def test_ep_forward_one_rank_equals_forward(name, form):
                                         ("tiny", 4)])
 def test_expert_slices_in_one_process_equal_forward(name, world):
     """Each 'rank' holds a contiguous slice of the experts (the last one
-    smaller when E does not split evenly) and computes only the pairs routed
-    to it; scattered back to pair order and combined, the layer is unchanged."""
+    smaller when E does not split evenly) and computes only the pairs the
+    device dispatch plan sends it; the results, concatenated in send order
+    and combined through each pair's send row, leave the layer unchanged."""
     shape, dev, bits = prepared(name)
     out, ws = run_forward(shape, dev)
     w, ids, _ = _pairs(shape, ws)
-    order, dest, counts, E_loc = ep_plan(ids.view(shape.N, shape.k), shape.E, world)
-    ypair = binding.alloc_pair_rows(shape.N * shape.k, shape.H)
+    ids2, w2 = ids.view(shape.N, shape.k), w.view(shape.N, shape.k)
+    d = binding.moe_ep_dispatch(dev["x"], ids2, w2, shape.E, world)
+    counts = d["send_counts"].cpu().tolist()
+    E_loc = -(-shape.E // world)
+    ys_hi, ys_res = [], []
     start = 0
     for r in range(world):
-        n_r = int(counts[r])
-        sel = order[start:start + n_r]
-        start += n_r
+        n_r = counts[r]
         e0, e1 = r * E_loc, min(shape.E, (r + 1) * E_loc)
         if n_r == 0:
             continue
-        y, ews = binding.moe_experts(dev["x"].index_select(0, sel // shape.k),
-                                     (ids[sel].long() - e0).to(torch.int32), w[sel],
+        sl = slice(start, start + n_r)
+        start += n_r
+        y, ews = binding.moe_experts(d["send_x"][sl], d["send_ids"][sl], d["send_w"][sl],
                                      dev["w_gate"][e0:e1], dev["w_up"][e0:e1],
                                      dev["w_down"][e0:e1])
         torch.cuda.synchronize()
         assert binding.moe_read_device_status(ews) == 0
-        ypair[0][sel] = y[0]
-        ypair[1][sel] = y[1]
-    got = binding.moe_combine(ypair, shape.N, shape.k)
+        ys_hi.append(y[0])
+        ys_res.append(y[1])
+    y_back = (torch.cat(ys_hi), torch.cat(ys_res))
+    got = binding.moe_combine_indexed(y_back, d["inv_order"], shape.N, shape.k)
     assert torch.equal(got, out)
     assert_close(got, oracle_outputs(name), f"{name} world {world}")
+
+
+@pytest.mark.parametrize("N,k,E,world", [(1, 1, 1, 1), (64, 8, 128, 2), (700, 6, 64, 3),
+                                         (5000, 8, 128, 8), (33, 4, 7, 5)])
+def test_device_dispatch_matches_reference(N, k, E, world):
+    """moe_ep_dispatch against the host reference plan, bit for bit: send
+    rows (token rows, local ids, weights), counts and each pair's send row;
+    the grouping runs the single-CTA path (<= 4096 pairs) and the
+    three-kernel one."""
+    g = torch.Generator().manual_seed(N + E + world)
+    H = 64
+    x = torch.randn(N, H, generator=g).to(torch.bfloat16)
+    ids = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(N)]).to(torch.int32)
+    w = torch.rand(N, k, generator=g)
+    d = binding.moe_ep_dispatch(x.cuda(), ids.cuda(), w.cuda(), E, world)
+    torch.cuda.synchronize()
+    assert binding.moe_read_device_status(d["workspace"]) == 0
+    ref = ep_dispatch_reference(x, ids, w, E, world)
+    for name, r in zip(("send_x", "send_ids", "send_w", "send_counts", "inv_order"), ref):
+        assert torch.equal(d[name].cpu(), r), name
+
+
+def test_device_dispatch_flags_a_bad_id():
+    """An expert id outside [0, E) is not sent (its send row is -1), is
+    reported as MOE_ERR_DEVICE_CHECK, and the indexed combine skips it."""
+    N, H, E, k, world = 6, 64, 8, 2, 2
+    x = torch.randn(N, H).to(torch.bfloat16).cuda()
+    ids = torch.tensor([[0, 5], [1, 2], [9, 3], [4, 6], [7, 0], [2, 1]], dtype=torch.int32).cuda()
+    w = torch.rand(N, k).cuda()
+    d = binding.moe_ep_dispatch(x, ids, w, E, world)
+    assert binding.moe_read_device_status(d["workspace"]) == 5  # MOE_ERR_DEVICE_CHECK
+    assert int(d["inv_order"][4].item()) == -1                   # pair (2, 0) holds id 9
+    assert int(d["send_counts"].sum().item()) == N * k - 1
+    n_rows = N * k - 1
+    rows = binding.alloc_pair_rows(n_rows, H)
+    rows[0].fill_(1.0)
+    rows[1].zero_()
+    out = binding.moe_combine_indexed(rows, d["inv_order"], N, k)
+    sums = out.float().sum(dim=1).cpu() / H
+    assert sums.tolist() == [2.0, 2.0, 1.0, 2.0, 2.0, 2.0]
 
 
 def test_experts_with_empty_experts_and_one_row():
