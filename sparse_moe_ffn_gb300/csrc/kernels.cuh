@@ -143,12 +143,6 @@ struct GemmArgs {
     int act_ready_count;
     int max_tiles;      // upper bound on tiles (sizes the persistent grid)
     int grid;           // persistent CTAs
-    // CTA-pair kernel: weight_streaming (set by the host) asks for a deep
-    // weight ring and a shallow activation ring (experts with few row
-    // blocks, whose weights stream from HBM); ring_a / ring_b are the ring
-    // depths launch_pair_gemm derives from it
-    int weight_streaming;
-    int ring_a, ring_b;
 };
 
 // Tile widths: gate/up 96 or 128 columns (of each of gate and up), down 256.
