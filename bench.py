@@ -101,25 +101,29 @@ def measured_traffic(stage, config):
 
 def algorithmic_work(shape: MoEShape, touched: int):
     """Per-stage algorithmic bytes and FLOPs of one layer call (padding rows,
-    re-reads and the act/ypair intermediates are overheads, not work)."""
+    re-reads and the act/ypair intermediates are overheads, not work).  The
+    shared expert runs inside the gate/up and down launches (its chunks are
+    virtual experts), so its work is counted there; the shared stage has no
+    launches of its own."""
     N, H, E, k, I, Is = shape.N, shape.H, shape.E, shape.k, shape.I, shape.I_s
     P = N * k
     b = {
         "route": E * H * 2 + N * H * 2 + P * 8,
         "align": P * 4 + P * 4,
         "gather": 0,  # x rows copied into expert order: an intermediate, not work
-        "gate_up": touched * 2 * I * H * 2 + N * H * 2 + P * I * 2,
-        "down": touched * H * I * 2 + P * I * 2 + P * H * 2 + P * 4,
-        "shared": (3 * Is * H * 2 + N * H * 2 + 2 * N * Is * 2 + N * H * 2) if Is else 0,
+        "gate_up": touched * 2 * I * H * 2 + N * H * 2 + P * I * 2 + 2 * Is * H * 2 + N * Is * 2,
+        "down": (touched * H * I * 2 + P * I * 2 + P * H * 2 + P * 4
+                 + Is * H * 2 + N * Is * 2 + N * H * 2),
+        "shared": 0,
         "combine": P * H * 2 + N * H * 2 + (N * H * 2 if Is else 0),
     }
     f = {
         "route": 2 * N * H * (E + (1 if Is else 0)),
         "align": 0,
         "gather": 0,
-        "gate_up": 4 * H * I * P,
-        "down": 2 * H * I * P,
-        "shared": 6 * H * Is * N if Is else 0,
+        "gate_up": 4 * H * I * P + 4 * H * Is * N,
+        "down": 2 * H * I * P + 2 * H * Is * N,
+        "shared": 0,
         "combine": 0,
     }
     layer_flops = 2 * N * H * E + 6 * H * I * P + (N * (6 * H * Is + 2 * H) if Is else 0)
@@ -405,8 +409,9 @@ def run_ours(args, world, rank, local):
     dom_ms = statistics.mean(ev[i][j_dom].elapsed_time(ev[i][j_dom + 1])
                              for i in range(args.steps))
 
+    # routed experts that received rows (the shared expert's chunks follow them)
     touched = int((binding.workspace_views(ws, shape.N, shape.H, shape.E, shape.I, shape.k,
-                                           shape.I_s)["counts"] > 0).sum().item())
+                                           shape.I_s)["counts"][:shape.E] > 0).sum().item())
     sbytes, sflops, layer_flops, layer_bytes = algorithmic_work(shape, touched)
     ms_step = ms_max / args.steps
     value = shape.N * args.steps * world / (ms_max / 1e3)

@@ -195,15 +195,19 @@ moe_status_t moe_align_noalloc(const int32_t *topk_ids, int64_t N, int k, int E,
  * Precision: bf16 inputs, fp32 routing and accumulation; the gate/up
  * activation a = silu(g)*u is kept as the bf16 pair hi = bf16(a),
  * lo = bf16(a - hi) (16 significant bits) and both halves are multiplied by
- * the bf16 down weights; each pair's weighted down projection (and the
- * gated shared expert) is accumulated in fp32 and kept as a pair row (see
- * "Pair rows" below: 16 significant bits in 3 bytes); the k contributions
- * and the shared term are summed in fp32 in slot order, and out is rounded
- * to bf16 once.
+ * the bf16 down weights; each pair's weighted down projection is
+ * accumulated in fp32 and kept as a pair row (see "Pair rows" below: 16
+ * significant bits in 3 bytes); the k contributions are summed in fp32 in
+ * slot order, and out is rounded to bf16 once.
+ * The shared expert runs in the same grouped GEMMs as C = ceil(I_s / I)
+ * virtual experts of I intermediate rows each (see moe_forward_layout_t):
+ * gamma * SharedMLP(x) arrives as C partial sums over disjoint intermediate
+ * rows, each a pair row with weight gamma, added after the k routed slots.
  * A non-finite activation or pair output records MOE_ERR_DEVICE_CHECK.
  * The result does not depend on the other tokens of the batch and is
  * bitwise reproducible.
- * Limits: as moe_route, plus I % 8 == 0, N*k + E*128 < 2^30.
+ * Limits: as moe_route, plus I % 8 == 0, E + C <= 256 and
+ * N*(k + C) + (E + C)*128 < 2^30 (C = 0 without the shared expert).
  * ---------------------------------------------------------------------- */
 size_t moe_forward_workspace_bytes(int64_t N, int H, int E, int I, int k, int I_s);
 moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *router,
@@ -288,17 +292,61 @@ moe_status_t moe_experts_prepared(const moe_bf16_t *x_rows, const int32_t *ids,
                                   size_t workspace_bytes, cudaStream_t stream);
 
 /* -------------------------------------------------------------------------
+ * moe_shared_expert -- the gated shared expert of the talker layer on its own
+ * (vLLM Qwen3.5 walkthrough, "2.5B Sparse MoE": gamma * SharedMLP(x) with
+ * gamma = sigmoid(x . g)), computed exactly as moe_forward computes it: its
+ * I_s intermediate rows cut into C = moe_shared_chunks(I, I_s) = ceil(I_s / I)
+ * chunks of I rows (I: the routed experts' intermediate size; the last chunk
+ * padded with zero weights), chunk c a virtual expert with weight gamma.
+ * For every token n and chunk c (row n*C + c of y):
+ *   y[n*C + c] = gamma[n] * Wd[:, chunk c] (silu(Wg[chunk c] x) * (Wu[chunk c] x))
+ * as pair rows, bit for bit the rows moe_forward holds in slots k .. k+C-1;
+ * moe_combine / moe_combine_indexed add them with shared_slots = C.  This is
+ * the expert-parallel layer's local shared term (it needs no exchange).
+ *   x [N, H] bf16; shared_gamma [N] fp32 (moe_route's output)
+ *   shared_gate_proj, shared_up_proj [I_s, H] bf16; shared_down_proj [H, I_s]
+ *     bf16 (moe_shared_expert_prepared: its fp16 copy, as in
+ *     moe_forward_prepared)
+ *   y_hi [N*C, H] bf16 out, y_res [N*C, H] int8 out (16-byte aligned)
+ *   workspace >= moe_shared_expert_workspace_bytes(N, H, I, I_s) bytes,
+ *     256-byte aligned; its first 4 bytes are the status word
+ * Limits: H, I, I_s positive multiples of 8, C <= 256, N*C + C*128 < 2^30.
+ * ---------------------------------------------------------------------- */
+int moe_shared_chunks(int I, int I_s);
+size_t moe_shared_expert_workspace_bytes(int64_t N, int H, int I, int I_s);
+moe_status_t moe_shared_expert(const moe_bf16_t *x, const float *shared_gamma,
+                               int64_t N, int H, int I, int I_s,
+                               const moe_bf16_t *shared_gate_proj,
+                               const moe_bf16_t *shared_up_proj,
+                               const moe_bf16_t *shared_down_proj, moe_bf16_t *y_hi,
+                               int8_t *y_res, void *workspace, size_t workspace_bytes,
+                               cudaStream_t stream);
+moe_status_t moe_shared_expert_prepared(const moe_bf16_t *x, const float *shared_gamma,
+                                        int64_t N, int H, int I, int I_s,
+                                        const moe_bf16_t *shared_gate_proj,
+                                        const moe_bf16_t *shared_up_proj,
+                                        const moe_f16_t *shared_down_proj_f16,
+                                        moe_bf16_t *y_hi, int8_t *y_res,
+                                        void *workspace, size_t workspace_bytes,
+                                        cudaStream_t stream);
+
+/* -------------------------------------------------------------------------
  * moe_combine -- the weighted accumulation of the layer (M03 drill: each
  * token's outputs summed back, index_add_ in the pages' PyTorch form), done
- * without atomics: out[n] = bf16(sum_{j<k} ypair[n*k + j] (+ yshared[n])),
- * the pair rows decoded and summed in fp32 in slot order.  ypair: pair rows
- * [N*k, H] (ypair_hi bf16, ypair_res int8), yshared: pair rows [N, H] or
- * both planes NULL, out [N, H] bf16; every plane 16-byte aligned.
- * moe_forward ends with the same kernel.
+ * without atomics:
+ *   out[n] = bf16(sum_{j<k} ypair[n*k + j] + sum_{c<S} yshared[n*S + c]),
+ * the pair rows decoded and summed in fp32 in slot order, then the shared
+ * expert's S = shared_slots chunk rows in chunk order.  ypair: pair rows
+ * [N*k, H] (ypair_hi bf16, ypair_res int8); yshared: pair rows [N*S, H]
+ * (moe_shared_expert's output, S = moe_shared_chunks(I, I_s)) with
+ * 1 <= S <= 256, or both planes NULL (shared_slots ignored); out [N, H]
+ * bf16; every plane 16-byte aligned.  moe_forward ends with the same
+ * kernel, its k + C slots per token all in ypair.
  * ---------------------------------------------------------------------- */
 moe_status_t moe_combine(const moe_bf16_t *ypair_hi, const int8_t *ypair_res,
                          const moe_bf16_t *yshared_hi, const int8_t *yshared_res,
-                         int64_t N, int H, int k, moe_bf16_t *out, cudaStream_t stream);
+                         int shared_slots, int64_t N, int H, int k, moe_bf16_t *out,
+                         cudaStream_t stream);
 
 /* moe_combine over pair rows held in another order: pair p = n*k + j reads
  * row row_index[p] of yrows ([num_rows, H] pair rows; the order in which
@@ -308,8 +356,8 @@ moe_status_t moe_combine(const moe_bf16_t *ypair_hi, const int8_t *ypair_res,
 moe_status_t moe_combine_indexed(const moe_bf16_t *yrows_hi, const int8_t *yrows_res,
                                  int64_t num_rows, const int32_t *row_index,
                                  const moe_bf16_t *yshared_hi, const int8_t *yshared_res,
-                                 int64_t N, int H, int k, moe_bf16_t *out,
-                                 cudaStream_t stream);
+                                 int shared_slots, int64_t N, int H, int k,
+                                 moe_bf16_t *out, cudaStream_t stream);
 
 /* -------------------------------------------------------------------------
  * moe_ep_dispatch -- the sending side of expert-parallel dispatch (M03 drill,
@@ -436,32 +484,38 @@ moe_status_t moe_dense_mlp_prepared(const moe_bf16_t *x, const moe_bf16_t *w_gat
                                     cudaStream_t stream);
 
 /* Byte offsets of moe_forward's workspace sub-buffers (for inspecting the
- * intermediate results; every offset is 256-byte aligned). */
+ * intermediate results; every offset is 256-byte aligned).
+ *
+ * With the shared expert (I_s > 0) the layer runs it inside the grouped
+ * GEMMs: its intermediate rows are cut into C = ceil(I_s / I) chunks of I
+ * rows (the last one padded with zero weights), and chunk c is a virtual
+ * expert E + c that every token uses with weight gamma = sigmoid(x . g).
+ * Every token then has `slots` = k + C (expert, weight) slots, the routed
+ * ones first, grouped over `groups` = E + C experts; the sizes below that
+ * name k and E mean `slots` and `groups`. */
 typedef struct {
     size_t status;        /* int32 device status word (a moe_status_t)       */
-    size_t topk_w;        /* fp32 [N, k]                                      */
-    size_t topk_ids;      /* int32 [N, k]                                     */
+    size_t topk_w;        /* fp32 [N, slots]: routed weights, then gamma      */
+    size_t topk_ids;      /* int32 [N, slots]: routed experts, then E + c     */
     size_t gamma;         /* fp32 [N] (shared expert only)                    */
-    size_t counts;        /* int32 [E]                                        */
-    size_t offsets;       /* int32 [E+1]                                      */
-    size_t pad_offsets;   /* int32 [E+1]                                      */
+    size_t counts;        /* int32 [groups]                                   */
+    size_t offsets;       /* int32 [groups+1]                                 */
+    size_t pad_offsets;   /* int32 [groups+1]                                 */
     size_t num_padded;    /* int32 [1]                                        */
-    size_t align_scratch; /* int32 [chunks, E]                                */
+    size_t align_scratch; /* int32 [chunks, groups]                           */
     size_t sorted_pair;   /* int32 [capacity]                                 */
     size_t block_expert;  /* int32 [capacity / 128]                           */
-    size_t ready;         /* int32 [max(E, capacity/128)] GEMM hand-off counts */
+    size_t ready;         /* int32 [max(groups, capacity/128)] GEMM hand-off counts */
     size_t x_sorted;      /* bf16 [capacity, H]   x rows in expert order (dense blocks) */
     size_t act;           /* a = silu(x Wg^T) * (x Wu^T): bf16 hi [capacity, I]
                              then bf16 lo [capacity, I] (moe_forward), or fp16
                              [capacity, I] (moe_forward_prepared)           */
-    size_t ypair;         /* bf16 [N*k, H]  w * Expert(x) per pair: hi plane  */
-    size_t ypair_res;     /* int8 [N*k, H]  ... residual plane (pair rows)     */
-    size_t act_shared;    /* as act, rows round_up(N,128), I_s columns
-                             (shared only)                                    */
-    size_t y_shared;      /* bf16 [N, H]  gamma * SharedMLP(x), hi plane      */
-    size_t y_shared_res;  /* int8 [N, H]  ... residual plane (shared only)    */
+    size_t ypair;         /* bf16 [N*slots, H]  w * Expert(x) per slot: hi plane */
+    size_t ypair_res;     /* int8 [N*slots, H]  ... residual plane (pair rows)   */
     size_t total;         /* = moe_forward_workspace_bytes                    */
-    int64_t capacity;     /* moe_align_capacity(N, k, E, 128)                 */
+    int64_t capacity;     /* moe_align_capacity(N, slots, groups, 128)        */
+    int slots;            /* k + C (k without the shared expert)              */
+    int groups;           /* E + C (E without the shared expert)              */
 } moe_forward_layout_t;
 
 moe_status_t moe_forward_layout(int64_t N, int H, int E, int I, int k, int I_s,

@@ -34,8 +34,8 @@ class _Layout(ctypes.Structure):
     _fields_ = [(name, ctypes.c_size_t) for name in (
         "status", "topk_w", "topk_ids", "gamma", "counts", "offsets", "pad_offsets",
         "num_padded", "align_scratch", "sorted_pair", "block_expert", "ready", "x_sorted", "act",
-        "ypair", "ypair_res", "act_shared", "y_shared", "y_shared_res", "total")] + [
-        ("capacity", ctypes.c_int64)]
+        "ypair", "ypair_res", "total")] + [
+        ("capacity", ctypes.c_int64), ("slots", ctypes.c_int), ("groups", ctypes.c_int)]
 
 
 _lib = None
@@ -67,8 +67,13 @@ def lib():
         "moe_experts_workspace_bytes": ([i64, i32, i32, i32], sz),
         "moe_experts": ([P, P, P, i64, i32, i32, i32, P, P, P, P, P, P, sz, P], i32),
         "moe_experts_prepared": ([P, P, P, i64, i32, i32, i32, P, P, P, P, P, P, sz, P], i32),
-        "moe_combine": ([P, P, P, P, i64, i32, i32, P, P], i32),
-        "moe_combine_indexed": ([P, P, i64, P, P, P, i64, i32, i32, P, P], i32),
+        "moe_combine": ([P, P, P, P, i32, i64, i32, i32, P, P], i32),
+        "moe_combine_indexed": ([P, P, i64, P, P, P, i32, i64, i32, i32, P, P], i32),
+        "moe_shared_chunks": ([i32, i32], i32),
+        "moe_shared_expert_workspace_bytes": ([i64, i32, i32, i32], sz),
+        "moe_shared_expert": ([P, P, i64, i32, i32, i32, P, P, P, P, P, P, sz, P], i32),
+        "moe_shared_expert_prepared": ([P, P, i64, i32, i32, i32, P, P, P, P, P, P, sz, P],
+                                       i32),
         "moe_ep_dispatch_workspace_bytes": ([i64, i32, i32], sz),
         "moe_ep_dispatch": ([P, P, P, i64, i32, i32, i32, i32, P, P, P, P, P, P, sz, P], i32),
         "moe_convert_bf16_to_f16": ([P, P, i64, P, P], i32),
@@ -349,19 +354,30 @@ def _check_pair_rows(y, R, H, name):
                          "contiguous CUDA tensors")
 
 
+def _shared_rows(yshared, N, H):
+    """(planes, S) of the shared expert's pair rows [N*S, H] (S rows per
+    token, moe_shared_expert's output), or ((None, None), 0)."""
+    if yshared is None:
+        return (None, None), 0
+    rows = yshared[0].shape[0]
+    if N == 0 or rows % N or rows == 0:
+        raise ValueError("yshared must hold S >= 1 rows per token ([N*S, H])")
+    _check_pair_rows(yshared, rows, H, "yshared")
+    return yshared, rows // N
+
+
 def moe_combine(ypair, N: int, k: int, yshared=None, out=None):
-    """out[n] = bf16(sum_j ypair[n*k + j] (+ yshared[n])) in fp32, slot order;
-    ypair and yshared are pair rows (hi, res)."""
+    """out[n] = bf16(sum_j ypair[n*k + j] + sum_c yshared[n*S + c]) in fp32,
+    slot order; ypair and yshared are pair rows (hi, res), yshared (optional)
+    with S rows per token (moe_shared_expert's chunks)."""
     H = ypair[0].shape[1]
     _check_pair_rows(ypair, N * k, H, "ypair")
-    if yshared is not None:
-        _check_pair_rows(yshared, N, H, "yshared")
-    sh = yshared if yshared is not None else (None, None)
+    sh, S = _shared_rows(yshared, N, H)
     if out is None:
         out = torch.empty((N, H), dtype=torch.bfloat16, device=ypair[0].device)
     _bf16(out, "out", (N, H))
-    _check(lib().moe_combine(_ptr(ypair[0]), _ptr(ypair[1]), _ptr(sh[0]), _ptr(sh[1]), N, H, k,
-                             _ptr(out), _stream()), "moe_combine")
+    _check(lib().moe_combine(_ptr(ypair[0]), _ptr(ypair[1]), _ptr(sh[0]), _ptr(sh[1]), S, N, H,
+                             k, _ptr(out), _stream()), "moe_combine")
     return out
 
 
@@ -374,16 +390,49 @@ def moe_combine_indexed(yrows, row_index, N: int, k: int, yshared=None, out=None
     if (row_index.dtype != torch.int32 or tuple(row_index.shape) != (N * k,) or
             not row_index.is_cuda or not row_index.is_contiguous()):
         raise ValueError("row_index must be a contiguous int32 CUDA tensor of shape [N*k]")
-    if yshared is not None:
-        _check_pair_rows(yshared, N, H, "yshared")
-    sh = yshared if yshared is not None else (None, None)
+    sh, S = _shared_rows(yshared, N, H)
     if out is None:
         out = torch.empty((N, H), dtype=torch.bfloat16, device=row_index.device)
     _bf16(out, "out", (N, H))
     _check(lib().moe_combine_indexed(_ptr(yrows[0]), _ptr(yrows[1]), R, _ptr(row_index),
-                                     _ptr(sh[0]), _ptr(sh[1]), N, H, k, _ptr(out), _stream()),
+                                     _ptr(sh[0]), _ptr(sh[1]), S, N, H, k, _ptr(out),
+                                     _stream()),
            "moe_combine_indexed")
     return out
+
+
+def moe_shared_chunks(I: int, I_s: int) -> int:
+    """C = ceil(I_s / I): the chunks (virtual experts) of the shared expert."""
+    return int(lib().moe_shared_chunks(I, I_s))
+
+
+def moe_shared_expert(x, gamma, I: int, shared_gate_proj, shared_up_proj, shared_down_proj,
+                      y=None, workspace=None):
+    """The gated shared expert on its own, as moe_forward computes it: pair
+    rows [N*C, H], row n*C + c = gamma[n] * (chunk c of SharedMLP)(x[n]), C =
+    ceil(I_s / I) with I the routed experts' intermediate size (moe.h).
+    shared_down_proj bf16 or its fp16 copy.  Returns (y, workspace)."""
+    N, H = x.shape
+    I_s = shared_gate_proj.shape[0]
+    _bf16(x, "x")
+    _bf16(shared_gate_proj, "shared_gate_proj", (I_s, H))
+    _bf16(shared_up_proj, "shared_up_proj", (I_s, H))
+    prepared = _down(shared_down_proj, "shared_down_proj", (H, I_s))
+    if gamma.dtype != torch.float32 or not gamma.is_cuda or tuple(gamma.shape) != (N,):
+        raise ValueError("gamma must be a CUDA float32 tensor of shape [N]")
+    gamma = gamma.contiguous()
+    C = moe_shared_chunks(I, I_s)
+    if y is None:
+        y = alloc_pair_rows(N * C, H, x.device)
+    _check_pair_rows(y, N * C, H, "y")
+    if workspace is None:
+        workspace = torch.empty(max(lib().moe_shared_expert_workspace_bytes(N, H, I, I_s), 256),
+                                dtype=torch.uint8, device=x.device)
+    fn = lib().moe_shared_expert_prepared if prepared else lib().moe_shared_expert
+    _check(fn(_ptr(x), _ptr(gamma), N, H, I, I_s, _ptr(shared_gate_proj), _ptr(shared_up_proj),
+              _ptr(shared_down_proj), _ptr(y[0]), _ptr(y[1]), _ptr(workspace), workspace.numel(),
+              _stream()), "moe_shared_expert")
+    return y, workspace
 
 
 def moe_ep_dispatch(x, topk_ids, topk_w, E: int, world: int):
@@ -617,10 +666,16 @@ def decode_loop(graphs: ForwardGraphSet, steps):
 
 
 def workspace_views(workspace, N, H, E, I, k, I_s=0) -> dict:
-    """Typed views of moe_forward's intermediate buffers inside ``workspace``."""
+    """Typed views of moe_forward's intermediate buffers inside ``workspace``.
+
+    With the shared expert every token has ``slots`` = k + C slots (the
+    routed ones, then the shared expert's C chunks as virtual experts E + c)
+    grouped over ``groups`` = E + C experts; topk_w / topk_ids / ypair hold
+    all slots, ``routed_w`` / ``routed_ids`` only the first k."""
     lay = moe_forward_layout(N, H, E, I, k, I_s)
     cap = lay["capacity"]
-    P = N * k
+    slots, groups = lay["slots"], lay["groups"]
+    P = N * slots
     base = workspace
 
     def view(off, dtype, shape):
@@ -631,12 +686,14 @@ def workspace_views(workspace, N, H, E, I, k, I_s=0) -> dict:
         return base[off:off + nbytes].view(dtype).view(shape)
 
     v = {
+        "slots": slots,
+        "groups": groups,
         "status": view(lay["status"], torch.int32, (1,)),
-        "topk_w": view(lay["topk_w"], torch.float32, (N, k)),
-        "topk_ids": view(lay["topk_ids"], torch.int32, (N, k)),
-        "counts": view(lay["counts"], torch.int32, (E,)),
-        "offsets": view(lay["offsets"], torch.int32, (E + 1,)),
-        "pad_offsets": view(lay["pad_offsets"], torch.int32, (E + 1,)),
+        "topk_w": view(lay["topk_w"], torch.float32, (N, slots)),
+        "topk_ids": view(lay["topk_ids"], torch.int32, (N, slots)),
+        "counts": view(lay["counts"], torch.int32, (groups,)),
+        "offsets": view(lay["offsets"], torch.int32, (groups + 1,)),
+        "pad_offsets": view(lay["pad_offsets"], torch.int32, (groups + 1,)),
         "num_padded": view(lay["num_padded"], torch.int32, (1,)),
         "sorted_pair": view(lay["sorted_pair"], torch.int32, (cap,)),
         "block_expert": view(lay["block_expert"], torch.int32, (cap // MOE_BLOCK_M,)),
@@ -646,14 +703,14 @@ def workspace_views(workspace, N, H, E, I, k, I_s=0) -> dict:
         "act_hi": view(lay["act"], torch.bfloat16, (cap, I)),
         "act_lo": view(lay["act"] + 2 * cap * I, torch.bfloat16, (cap, I)),
         "act_f16": view(lay["act"], torch.float16, (cap, I)),
-        # pair rows (hi, res) of w * Expert(x), one row per pair
+        # pair rows (hi, res) of w * Expert(x), one row per slot
         "ypair": (view(lay["ypair"], torch.bfloat16, (P, H)),
                   view(lay["ypair_res"], torch.int8, (P, H))),
     }
+    v["routed_w"] = v["topk_w"][:, :k]
+    v["routed_ids"] = v["topk_ids"][:, :k]
     if I_s:
         v["gamma"] = view(lay["gamma"], torch.float32, (N,))
-        v["y_shared"] = (view(lay["y_shared"], torch.bfloat16, (N, H)),
-                         view(lay["y_shared_res"], torch.int8, (N, H)))
     return v
 
 

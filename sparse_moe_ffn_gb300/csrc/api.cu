@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -179,7 +180,7 @@ moe_status_t enqueue_route(const moe_bf16_t *x, const moe_bf16_t *router,
                            const moe_bf16_t *shared_gate, int64_t N, int H, int E, int k,
                            int norm, float *topk_w, int32_t *topk_ids, moe_bf16_t *topk_w_bf16,
                            float *gamma, int32_t *status, bool reset_status,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, int virt_slots = 0) {
     const bool shared = shared_gate != nullptr;
     RouterArgs ra;
     ra.N = N;
@@ -196,6 +197,9 @@ moe_status_t enqueue_route(const moe_bf16_t *x, const moe_bf16_t *router,
     ra.topk_w_bf16 = topk_w_bf16;
     ra.gamma = gamma;
     ra.status = status;
+    ra.out_ld = k + virt_slots;
+    ra.virt_slots = virt_slots;
+    ra.virt_base = E;
     CUtensorMap tm_x, tm_r, tm_g;
     moe_status_t st;
     if ((st = make_map(&tm_x, x, H, N, H, kBlockK, kBlockM, "x")) != MOE_OK) return st;
@@ -254,10 +258,19 @@ bool use_pair_tiles(int64_t P, int E) { return P >= static_cast<int64_t>(kBlockM
 // rows in 32-row passes keep more weight bytes in flight.
 bool use_sparse_tiles(int64_t P, int E) { return P < 32 * static_cast<int64_t>(E); }
 
-moe_status_t forward_layout(int64_t N, int H, int E, int I, int k, int I_s,
+// The shared expert runs as shared_chunks(I, I_s) virtual experts E, E+1, ...
+// of I intermediate rows each (the last one padded with zero weights by the
+// TMA fill), which every token uses with the shared gate as its weight: its
+// slots k, k+1, ... of the routing and grouping.
+int shared_chunks(int I, int I_s) { return I_s > 0 ? (I_s + I - 1) / I : 0; }
+
+moe_status_t forward_layout(int64_t N, int H, int E_routed, int I, int k_routed, int I_s,
                             moe_forward_layout_t *L) {
-    const int64_t P = N * k;
     const bool shared = I_s > 0;
+    const int C = shared_chunks(I, I_s);
+    const int k = k_routed + C;  // slots per token, routed then shared chunks
+    const int E = E_routed + C;  // groups: the experts, then the shared chunks
+    const int64_t P = N * k;
     const int64_t cap = moe_align_capacity(N, k, E, kBlockM);
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -284,11 +297,10 @@ moe_status_t forward_layout(int64_t N, int H, int E, int I, int k, int I_s,
     // pair rows: bf16 hi plane and int8 residual plane
     L->ypair = take(2 * static_cast<size_t>(P) * H);
     L->ypair_res = take(static_cast<size_t>(P) * H);
-    L->act_shared = take(shared ? 4 * static_cast<size_t>(round_up64(N, kBlockM)) * I_s : 0);
-    L->y_shared = take(shared ? 2 * static_cast<size_t>(N) * H : 0);
-    L->y_shared_res = take(shared ? static_cast<size_t>(N) * H : 0);
     L->total = off;
     L->capacity = cap;
+    L->slots = k;
+    L->groups = E;
     return MOE_OK;
 }
 
@@ -330,9 +342,14 @@ moe_status_t check_forward_args(const moe_bf16_t *x, const moe_bf16_t *router,
     if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
         return fail(MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
     // the hi and lo rows of a split activation share one row index space
-    if (N * k + static_cast<int64_t>(E) * kBlockM >= (int64_t(1) << 30))
-        return fail(MOE_ERR_UNSUPPORTED, "N*k + E*128 must stay below 2^30");
-    forward_layout(N, H, E, I, k, I_s, L);
+    const int C = shared_chunks(I, shared ? I_s : 0);
+    if (E + C > MOE_MAX_EXPERTS)
+        return fail(MOE_ERR_UNSUPPORTED,
+                    "E + ceil(I_s / I) (the shared expert's chunks) must be <= %d (got %d)",
+                    MOE_MAX_EXPERTS, E + C);
+    if (N * (k + C) + static_cast<int64_t>(E + C) * kBlockM >= (int64_t(1) << 30))
+        return fail(MOE_ERR_UNSUPPORTED, "N*(k + chunks) + (E + chunks)*128 must stay below 2^30");
+    forward_layout(N, H, E, I, k, shared ? I_s : 0, L);
     if (workspace_bytes < L->total)
         return fail(MOE_ERR_WORKSPACE_TOO_SMALL, "forward workspace needs %zu bytes, got %zu",
                     L->total, workspace_bytes);
@@ -346,11 +363,21 @@ moe_status_t check_forward_args(const moe_bf16_t *x, const moe_bf16_t *router,
 // or its fp16 copy (down_f16 true: an fp16 activation).  The workspace
 // follows moe_forward_layout(N, H, E, I, k, 0); its status word is not reset
 // here.  Records the align .. down stage events.
+// The shared expert folded into the grouped GEMMs (see shared_chunks):
+// groups from E_routed on read these weights.
+struct SharedWeights {
+    const moe_bf16_t *gate_proj, *up_proj;  // [I_s, H]
+    const void *down_proj;                  // [H, I_s], bf16 or fp16 as w_down
+    int I_s;
+    int E_routed;
+};
+
 moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const float *weights,
                              int64_t N, int k, int H, int E, int I, const moe_bf16_t *w_gate,
                              const moe_bf16_t *w_up, const void *w_down, bool down_f16,
                              const moe_forward_layout_t &L, uint8_t *ws, uint16_t *ypair,
-                             int8_t *ypair_res, cudaStream_t stream) {
+                             int8_t *ypair_res, cudaStream_t stream,
+                             const SharedWeights *sh = nullptr) {
     moe_status_t st;
     auto at = [&](size_t off) { return ws + off; };
     int32_t *status = reinterpret_cast<int32_t *>(at(L.status));
@@ -390,12 +417,45 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
     if ((st = make_map(&tm_xsorted, x_sorted, H, cap, H, kBlockK, kBlockM, "x_sorted")) != MOE_OK)
         return st;
     const int bn_gu = choose_gate_up_bn(expected_blocks(P, E), static_cast<double>(P) / E, I, sms);
-    if ((st = make_map(&tm_wg, w_gate, H, static_cast<uint64_t>(E) * I, H, kBlockK, bn_gu,
-                       "w_gate")) != MOE_OK)
+    // the routed experts' weights; the shared expert's chunks (groups from
+    // E_routed on) read the shared maps
+    const int E_map = sh ? sh->E_routed : E;
+    // no routed experts (the shared expert on its own): the routed maps are
+    // never read, so they describe the shared weights
+    const bool all_virtual = sh && sh->E_routed == 0;
+    if (all_virtual) {
+        w_gate = sh->gate_proj;
+        w_up = sh->up_proj;
+        w_down = sh->down_proj;
+    }
+    const uint64_t gu_rows = all_virtual ? sh->I_s : static_cast<uint64_t>(E_map) * I;
+    const uint64_t down_rows = all_virtual ? H : static_cast<uint64_t>(E_map) * H;
+    if ((st = make_map(&tm_wg, w_gate, H, gu_rows, H, kBlockK, bn_gu, "w_gate")) != MOE_OK)
         return st;
-    if ((st = make_map(&tm_wu, w_up, H, static_cast<uint64_t>(E) * I, H, kBlockK, bn_gu,
-                       "w_up")) != MOE_OK)
+    if ((st = make_map(&tm_wu, w_up, H, gu_rows, H, kBlockK, bn_gu, "w_up")) != MOE_OK)
         return st;
+    CUtensorMap tm_sg, tm_su, tm_sd;
+    const CUtensorMap *psg = nullptr, *psu = nullptr, *psd = nullptr;
+    auto shared_gate_up_maps = [&](int box_rows) -> moe_status_t {
+        if (!sh) return MOE_OK;
+        moe_status_t r;
+        if ((r = make_map(&tm_sg, sh->gate_proj, H, sh->I_s, H, kBlockK, box_rows,
+                          "shared_gate_proj")) != MOE_OK ||
+            (r = make_map(&tm_su, sh->up_proj, H, sh->I_s, H, kBlockK, box_rows,
+                          "shared_up_proj")) != MOE_OK)
+            return r;
+        psg = &tm_sg;
+        psu = &tm_su;
+        return MOE_OK;
+    };
+    auto shared_down_map = [&](int box_rows) -> moe_status_t {
+        if (!sh) return MOE_OK;
+        moe_status_t r = make_map(&tm_sd, sh->down_proj, sh->I_s, H, sh->I_s, kBlockK, box_rows,
+                                  "shared_down_proj");
+        if (r != MOE_OK) return r;
+        psd = &tm_sd;
+        return MOE_OK;
+    };
     const bool pairs = use_pair_tiles(P, E);
     const bool sparse = !pairs && use_sparse_tiles(P, E);
     GemmArgs g;
@@ -407,6 +467,8 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
     g.w0 = g.w1 = nullptr;
     g.act_ready = nullptr;
     g.act_ready_count = 0;
+    g.virt_base = sh ? sh->E_routed : INT_MAX;
+    g.virt_chunk = I;
     g.num_padded = b.num_padded;
     g.num_rows_host = cap;
     g.q_limit = P;
@@ -449,18 +511,18 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
                 g.act_ready_count = (I + bn_gu - 1) / bn_gu;
             }
         }
-        MOE_CUDA(launch_sparse_gemm(kGateUp, bn_gu, tm_xrows, tm_wg, tm_wu, g, stream),
+        if ((st = shared_gate_up_maps(bn_gu)) != MOE_OK) return st;
+        MOE_CUDA(launch_sparse_gemm(kGateUp, bn_gu, tm_xrows, tm_wg, tm_wu, g, stream, psg, psu),
                  "gate/up kernel launch");
         g.expert_tiles = 0;
     } else if (pairs) {
         const int bn = pair_gemm_block_n(kGateUp);
         CUtensorMap tm_wg_tile, tm_wu_tile;
-        if ((st = make_map(&tm_wg_tile, w_gate, H, static_cast<uint64_t>(E) * I, H, kBlockK, bn,
-                           "w_gate")) != MOE_OK)
+        if ((st = make_map(&tm_wg_tile, w_gate, H, gu_rows, H, kBlockK, bn, "w_gate")) != MOE_OK)
             return st;
-        if ((st = make_map(&tm_wu_tile, w_up, H, static_cast<uint64_t>(E) * I, H, kBlockK, bn,
-                           "w_up")) != MOE_OK)
+        if ((st = make_map(&tm_wu_tile, w_up, H, gu_rows, H, kBlockK, bn, "w_up")) != MOE_OK)
             return st;
+        if ((st = shared_gate_up_maps(bn)) != MOE_OK) return st;
         const int max_pairs = static_cast<int>(cap / kBlockM);  // pairs <= blocks
         g.max_tiles = max_pairs * ((I + bn - 1) / bn);
         g.grid = 2 * (g.max_tiles < sms / 2 ? g.max_tiles : sms / 2);
@@ -469,10 +531,13 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
             g.act_ready = ready;
             g.act_ready_count = 8 * ((I + bn - 1) / bn);
         }
-        MOE_CUDA(launch_pair_gemm(kGateUp, tm_xsorted, tm_wg_tile, tm_wu_tile, g, stream),
+        MOE_CUDA(launch_pair_gemm(kGateUp, tm_xsorted, tm_wg_tile, tm_wu_tile, g, stream, psg,
+                                  psu),
                  "gate/up kernel launch");
     } else {
-        MOE_CUDA(launch_gemm(kGateUp, bn_gu, tm_xrows, tm_xsorted, tm_wg, tm_wu, g, stream),
+        if ((st = shared_gate_up_maps(bn_gu)) != MOE_OK) return st;
+        MOE_CUDA(launch_gemm(kGateUp, bn_gu, tm_xrows, tm_xsorted, tm_wg, tm_wu, g, stream, psg,
+                             psu),
                  "gate/up kernel launch");
     }
     g_launches += 1;
@@ -484,7 +549,8 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
     if ((st = make_map(&tm_act, act, I, act_rows, I, kBlockK, 1, "act rows")) != MOE_OK) return st;
     if ((st = make_map(&tm_act_box, act, I, act_rows, I, kBlockK, kBlockM, "act")) != MOE_OK)
         return st;
-    if ((st = make_map(&tm_wd, w_down, I, static_cast<uint64_t>(E) * H, I, kBlockK, kDownBN,
+    const uint64_t down_cols = all_virtual ? sh->I_s : I;
+    if ((st = make_map(&tm_wd, w_down, down_cols, down_rows, down_cols, kBlockK, kDownBN,
                        "w_down")) != MOE_OK)
         return st;
     g.k_div = 1;
@@ -501,20 +567,24 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
         g.grid = g.max_tiles < sms ? g.max_tiles : sms;
     }
     if (sparse) {
-        MOE_CUDA(launch_sparse_gemm(down, kDownBN, tm_act, tm_wd, tm_wd, g, stream),
+        if ((st = shared_down_map(kDownBN)) != MOE_OK) return st;
+        MOE_CUDA(launch_sparse_gemm(down, kDownBN, tm_act, tm_wd, tm_wd, g, stream, psd, psd),
                  "down kernel launch");
     } else if (pairs) {
         const int bn = pair_gemm_block_n(down);
         CUtensorMap tm_wd_half;
-        if ((st = make_map(&tm_wd_half, w_down, I, static_cast<uint64_t>(E) * H, I, kBlockK,
-                           bn / 2, "w_down")) != MOE_OK)
+        if ((st = make_map(&tm_wd_half, w_down, down_cols, down_rows, down_cols, kBlockK, bn / 2,
+                           "w_down")) != MOE_OK)
             return st;
+        if ((st = shared_down_map(bn / 2)) != MOE_OK) return st;
         g.max_tiles = static_cast<int>(cap / kBlockM) * ((H + bn - 1) / bn);
         g.grid = 2 * (g.max_tiles < sms / 2 ? g.max_tiles : sms / 2);
-        MOE_CUDA(launch_pair_gemm(down, tm_act_box, tm_wd_half, tm_wd_half, g, stream),
+        MOE_CUDA(launch_pair_gemm(down, tm_act_box, tm_wd_half, tm_wd_half, g, stream, psd, psd),
                  "down kernel launch");
     } else {
-        MOE_CUDA(launch_gemm(down, kDownBN, tm_act, tm_act_box, tm_wd, tm_wd, g, stream),
+        if ((st = shared_down_map(kDownBN)) != MOE_OK) return st;
+        MOE_CUDA(launch_gemm(down, kDownBN, tm_act, tm_act_box, tm_wd, tm_wd, g, stream, psd,
+                             psd),
                  "down kernel launch");
     }
     g_launches += 1;
@@ -667,123 +737,29 @@ static moe_status_t forward_impl(const moe_bf16_t *x, const moe_bf16_t *router,
     const int sms = num_sms_of_current_device();
 
     // K1: routing (its first CTA also clears the status word, so that no
-    // memset node breaks the chain of programmatically serialized launches)
+    // memset node breaks the chain of programmatically serialized launches);
+    // with the shared expert every token also gets its chunks' slots
+    const int C = L.slots - k;
     if ((st = record_stage(MOE_STAGE_ROUTE, stream)) != MOE_OK) return st;
     st = enqueue_route(x, router, shared ? shared_gate : nullptr, N, H, E, k, norm_topk_prob,
-                       topk_w, topk_ids, nullptr, gamma, status, true, stream);
+                       topk_w, topk_ids, nullptr, gamma, status, true, stream, C);
     if (st != MOE_OK) return st;
 
-    // K2-K4: grouping, gate/up, down
-    if ((st = enqueue_experts(x, topk_ids, topk_w, N, k, H, E, I, w_gate, w_up, w_down,
-                              down_f16, L, ws, ypair, ypair_res, stream)) != MOE_OK)
+    // K2-K4: grouping, gate/up, down over the routed experts and the shared
+    // expert's chunks together
+    SharedWeights sw{shared_gate_proj, shared_up_proj, shared_down_proj, I_s, E};
+    if ((st = enqueue_experts(x, topk_ids, topk_w, N, L.slots, H, L.groups, I, w_gate, w_up,
+                              w_down, down_f16, L, ws, ypair, ypair_res, stream,
+                              shared ? &sw : nullptr)) != MOE_OK)
         return st;
-
-    // shared expert: one dense group over all N tokens, weight sigmoid(x . g)
+    // (the shared stage has no launches of its own any more)
     if ((st = record_stage(MOE_STAGE_SHARED, stream)) != MOE_OK) return st;
-    uint16_t *y_shared = nullptr;
-    int8_t *y_shared_res = nullptr;
-    if (shared) {
-        uint16_t *act_s = reinterpret_cast<uint16_t *>(at(L.act_shared));
-        y_shared = reinterpret_cast<uint16_t *>(at(L.y_shared));
-        y_shared_res = reinterpret_cast<int8_t *>(at(L.y_shared_res));
-        const int64_t rows_s = round_up64(N, kBlockM);
-        const GemmMode down = down_f16 ? kDown : kDownSplit;
-        const int64_t act_rows = down_f16 ? rows_s : 2 * rows_s;
-        CUtensorMap tm_sg, tm_su, tm_acts, tm_sd, tm_xbox;
-        const int bn_s = choose_gate_up_bn(static_cast<double>(rows_s / kBlockM),
-                                           static_cast<double>(N), I_s, sms);
-        if ((st = make_map(&tm_xbox, x, H, N, H, kBlockK, kBlockM, "x")) != MOE_OK) return st;
-        if ((st = make_map(&tm_sg, shared_gate_proj, H, I_s, H, kBlockK, bn_s,
-                           "shared_gate_proj")) != MOE_OK)
-            return st;
-        if ((st = make_map(&tm_su, shared_up_proj, H, I_s, H, kBlockK, bn_s,
-                           "shared_up_proj")) != MOE_OK)
-            return st;
-        if ((st = make_map(&tm_acts, act_s, I_s, act_rows, I_s, kBlockK, kBlockM,
-                           "shared act rows")) != MOE_OK)
-            return st;
-        if ((st = make_map(&tm_sd, shared_down_proj, I_s, H, I_s, kBlockK, kDownBN,
-                           "shared_down_proj")) != MOE_OK)
-            return st;
-        GemmArgs s;
-        s.sorted_pair = nullptr;
-        s.block_expert = nullptr;
-        s.num_padded = nullptr;
-        s.num_rows_host = N;
-        s.q_limit = N;
-        s.k_div = 1;
-        s.pad_offsets = nullptr;
-        s.num_groups = 0;
-        s.expert_tiles = 0;
-        s.w0 = s.w1 = nullptr;
-        s.act_ready = nullptr;
-        s.act_ready_count = 0;
-        s.K = H;
-        s.n_out = I_s;
-        s.w_rows = I_s;
-        s.out = act_s;
-        s.out_res = nullptr;
-        s.out_ld = I_s;
-        s.lo_rows = down_f16 ? 0 : rows_s;
-        s.scale = nullptr;
-        s.status = status;
-        s.stream_weights = N <= kBlockM ? 1 : 0;
-        {
-            const int nt = (I_s + bn_s - 1) / bn_s;
-            s.max_tiles = static_cast<int>(rows_s / kBlockM) * nt;
-            s.grid = s.max_tiles < sms ? s.max_tiles : sms;
-        }
-        // more than one row block: two-CTA tiles over consecutive blocks
-        const bool pairs_s = rows_s >= 2 * kBlockM;
-        if (pairs_s) {
-            const int bn = pair_gemm_block_n(kGateUp);
-            CUtensorMap tm_sg2, tm_su2;
-            if ((st = make_map(&tm_sg2, shared_gate_proj, H, I_s, H, kBlockK, bn,
-                               "shared_gate_proj")) != MOE_OK ||
-                (st = make_map(&tm_su2, shared_up_proj, H, I_s, H, kBlockK, bn,
-                               "shared_up_proj")) != MOE_OK)
-                return st;
-            s.max_tiles = static_cast<int>((rows_s / kBlockM + 1) / 2) * ((I_s + bn - 1) / bn);
-            s.grid = 2 * (s.max_tiles < sms / 2 ? s.max_tiles : sms / 2);
-            MOE_CUDA(launch_pair_gemm(kGateUp, tm_xbox, tm_sg2, tm_su2, s, stream),
-                     "shared gate/up kernel launch");
-        } else {
-            MOE_CUDA(launch_gemm(kGateUp, bn_s, tm_xbox, tm_xbox, tm_sg, tm_su, s, stream),
-                     "shared gate/up kernel launch");
-        }
-        s.K = I_s;
-        s.n_out = H;
-        s.w_rows = H;
-        s.out = y_shared;
-        s.out_res = y_shared_res;
-        s.out_ld = H;
-        s.scale = gamma;
-        {
-            const int nt = (H + kDownBN - 1) / kDownBN;
-            s.max_tiles = static_cast<int>(rows_s / kBlockM) * nt;
-            s.grid = s.max_tiles < sms ? s.max_tiles : sms;
-        }
-        if (pairs_s) {
-            const int bn = pair_gemm_block_n(down);
-            CUtensorMap tm_sd2;
-            if ((st = make_map(&tm_sd2, shared_down_proj, I_s, H, I_s, kBlockK, bn / 2,
-                               "shared_down_proj")) != MOE_OK)
-                return st;
-            s.max_tiles = static_cast<int>((rows_s / kBlockM + 1) / 2) * ((H + bn - 1) / bn);
-            s.grid = 2 * (s.max_tiles < sms / 2 ? s.max_tiles : sms / 2);
-            MOE_CUDA(launch_pair_gemm(down, tm_acts, tm_sd2, tm_sd2, s, stream),
-                     "shared down kernel launch");
-        } else {
-            MOE_CUDA(launch_gemm(down, kDownBN, tm_acts, tm_acts, tm_sd, tm_sd, s, stream),
-                     "shared down kernel launch");
-        }
-        g_launches += 2;
-    }
 
-    // K5: out[n] = sum_j ypair[n*k + j] (+ shared)
+    // K5: out[n] = sum_j ypair[n*slots + j], the routed slots then the
+    // shared expert's chunks
     if ((st = record_stage(MOE_STAGE_COMBINE, stream)) != MOE_OK) return st;
-    MOE_CUDA(launch_combine(ypair, ypair_res, nullptr, N * k, y_shared, y_shared_res, N, H, k, out,
-                            sms, stream),
+    MOE_CUDA(launch_combine(ypair, ypair_res, nullptr, N * L.slots, nullptr, nullptr, 0, N, H,
+                            L.slots, out, sms, stream),
              "combine kernel launch");
     g_launches += 1;
     if ((st = record_stage(MOE_NUM_STAGES, stream)) != MOE_OK) return st;
@@ -816,8 +792,17 @@ moe_status_t moe_forward_prepared(const moe_bf16_t *x, const moe_bf16_t *router,
                         true, out, workspace, workspace_bytes, stream);
 }
 
+// what moe_experts and moe_shared_expert use of moe_forward's layout: all but
+// the pair-row planes, which they write to the caller's y
+static size_t experts_workspace(int64_t N, int H, int E, int I, int k, int I_s) {
+    moe_forward_layout_t L;
+    forward_layout(N, H, E, I, k, I_s, &L);
+    return L.ypair;
+}
+
 size_t moe_experts_workspace_bytes(int64_t R, int H, int E, int I) {
-    return moe_forward_workspace_bytes(R, H, E, I, 1, 0);
+    if (R < 0 || H < 1 || E < 1 || I < 1) return 0;
+    return experts_workspace(R, H, E, I, 1, 0);
 }
 
 static moe_status_t experts_impl(const moe_bf16_t *x_rows, const int32_t *ids,
@@ -845,9 +830,9 @@ static moe_status_t experts_impl(const moe_bf16_t *x_rows, const int32_t *ids,
         return fail(MOE_ERR_UNSUPPORTED, "R + E*128 must stay below 2^30");
     moe_forward_layout_t L;
     forward_layout(R, H, E, I, 1, 0, &L);
-    if (workspace_bytes < L.total)
+    if (workspace_bytes < L.ypair)
         return fail(MOE_ERR_WORKSPACE_TOO_SMALL, "experts workspace needs %zu bytes, got %zu",
-                    L.total, workspace_bytes);
+                    L.ypair, workspace_bytes);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     MOE_CUDA(cudaMemsetAsync(ws + L.status, 0, sizeof(int32_t), stream), "status reset");
     return enqueue_experts(x_rows, ids, weights, R, 1, H, E, I, w_gate, w_up, w_down, down_f16,
@@ -872,10 +857,85 @@ moe_status_t moe_experts_prepared(const moe_bf16_t *x_rows, const int32_t *ids,
                         y_res, workspace, workspace_bytes, stream);
 }
 
+int moe_shared_chunks(int I, int I_s) { return I >= 1 && I_s >= 1 ? shared_chunks(I, I_s) : 0; }
+
+size_t moe_shared_expert_workspace_bytes(int64_t N, int H, int I, int I_s) {
+    if (N < 0 || H < 1 || I < 1 || I_s < 1) return 0;
+    return experts_workspace(N, H, 0, I, 0, I_s);
+}
+
+static moe_status_t shared_expert_impl(const moe_bf16_t *x, const float *shared_gamma, int64_t N,
+                                       int H, int I, int I_s, const moe_bf16_t *shared_gate_proj,
+                                       const moe_bf16_t *shared_up_proj,
+                                       const void *shared_down_proj, bool down_f16,
+                                       moe_bf16_t *y_hi, int8_t *y_res, void *workspace,
+                                       size_t workspace_bytes, cudaStream_t stream) {
+    g_last_error.clear();
+    if (N < 0) return fail(MOE_ERR_INVALID_ARG, "N must be >= 0 (got %lld)", (long long)N);
+    if (H < 8 || H % 8 || I < 8 || I % 8 || I_s < 8 || I_s % 8)
+        return fail(MOE_ERR_INVALID_ARG,
+                    "H, I and I_s must be positive multiples of 8 (H=%d, I=%d, I_s=%d)", H, I, I_s);
+    const int C = shared_chunks(I, I_s);
+    if (C > MOE_MAX_EXPERTS)
+        return fail(MOE_ERR_UNSUPPORTED, "ceil(I_s / I) must be <= %d (got %d)", MOE_MAX_EXPERTS,
+                    C);
+    if (N == 0) return MOE_OK;
+    if (!x || !shared_gamma || !shared_gate_proj || !shared_up_proj || !shared_down_proj ||
+        !y_hi || !y_res || !workspace)
+        return fail(MOE_ERR_INVALID_ARG, "every moe_shared_expert pointer must be non-null");
+    if (!aligned16(x) || !aligned16(shared_gate_proj) || !aligned16(shared_up_proj) ||
+        !aligned16(shared_down_proj) || !aligned16(y_hi) || !aligned16(y_res))
+        return fail(MOE_ERR_INVALID_ARG, "matrices must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
+        return fail(MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    if (N * C + static_cast<int64_t>(C) * kBlockM >= (int64_t(1) << 30))
+        return fail(MOE_ERR_UNSUPPORTED, "N*C + C*128 must stay below 2^30");
+    moe_forward_layout_t L;
+    forward_layout(N, H, 0, I, 0, I_s, &L);
+    if (workspace_bytes < L.ypair)
+        return fail(MOE_ERR_WORKSPACE_TOO_SMALL, "shared expert workspace needs %zu bytes, got %zu",
+                    L.ypair, workspace_bytes);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    int32_t *ids = reinterpret_cast<int32_t *>(ws + L.topk_ids);
+    float *w = reinterpret_cast<float *>(ws + L.topk_w);
+    MOE_CUDA(cudaMemsetAsync(ws + L.status, 0, sizeof(int32_t), stream), "status reset");
+    MOE_CUDA(launch_shared_slots(shared_gamma, N, C, ids, w, num_sms_of_current_device(), stream),
+             "shared slots kernel launch");
+    g_launches += 1;
+    SharedWeights sw{shared_gate_proj, shared_up_proj, shared_down_proj, I_s, 0};
+    return enqueue_experts(x, ids, w, N, C, H, C, I, shared_gate_proj, shared_up_proj,
+                           shared_down_proj, down_f16, L, ws, reinterpret_cast<uint16_t *>(y_hi),
+                           y_res, stream, &sw);
+}
+
+moe_status_t moe_shared_expert(const moe_bf16_t *x, const float *shared_gamma, int64_t N, int H,
+                               int I, int I_s, const moe_bf16_t *shared_gate_proj,
+                               const moe_bf16_t *shared_up_proj,
+                               const moe_bf16_t *shared_down_proj, moe_bf16_t *y_hi,
+                               int8_t *y_res, void *workspace, size_t workspace_bytes,
+                               cudaStream_t stream) {
+    return shared_expert_impl(x, shared_gamma, N, H, I, I_s, shared_gate_proj, shared_up_proj,
+                              shared_down_proj, false, y_hi, y_res, workspace, workspace_bytes,
+                              stream);
+}
+
+moe_status_t moe_shared_expert_prepared(const moe_bf16_t *x, const float *shared_gamma,
+                                        int64_t N, int H, int I, int I_s,
+                                        const moe_bf16_t *shared_gate_proj,
+                                        const moe_bf16_t *shared_up_proj,
+                                        const moe_f16_t *shared_down_proj_f16, moe_bf16_t *y_hi,
+                                        int8_t *y_res, void *workspace, size_t workspace_bytes,
+                                        cudaStream_t stream) {
+    return shared_expert_impl(x, shared_gamma, N, H, I, I_s, shared_gate_proj, shared_up_proj,
+                              shared_down_proj_f16, true, y_hi, y_res, workspace,
+                              workspace_bytes, stream);
+}
+
 static moe_status_t combine_impl(const moe_bf16_t *ypair_hi, const int8_t *ypair_res,
                                  const int32_t *row_index, int64_t rows,
                                  const moe_bf16_t *yshared_hi, const int8_t *yshared_res,
-                                 int64_t N, int H, int k, moe_bf16_t *out, cudaStream_t stream) {
+                                 int shared_slots, int64_t N, int H, int k, moe_bf16_t *out,
+                                 cudaStream_t stream) {
     g_last_error.clear();
     if (N < 0 || H < 8 || H % 8 || k < 1)
         return fail(MOE_ERR_INVALID_ARG, "need N >= 0, H a positive multiple of 8, k >= 1");
@@ -884,29 +944,37 @@ static moe_status_t combine_impl(const moe_bf16_t *ypair_hi, const int8_t *ypair
         return fail(MOE_ERR_INVALID_ARG, "ypair_hi, ypair_res and out must be non-null");
     if ((yshared_hi == nullptr) != (yshared_res == nullptr))
         return fail(MOE_ERR_INVALID_ARG, "give both planes of yshared or neither");
+    if (yshared_hi && (shared_slots < 1 || shared_slots > MOE_MAX_EXPERTS))
+        return fail(MOE_ERR_INVALID_ARG, "shared_slots must be in [1, %d] with yshared (got %d)",
+                    MOE_MAX_EXPERTS, shared_slots);
     if (!aligned16(ypair_hi) || !aligned16(ypair_res) || !aligned16(out) ||
         (yshared_hi && (!aligned16(yshared_hi) || !aligned16(yshared_res))))
         return fail(MOE_ERR_INVALID_ARG, "pair planes and out must be 16-byte aligned");
     if (N > (int64_t(1) << 31) / k) return fail(MOE_ERR_UNSUPPORTED, "N*k must stay below 2^31");
     if (rows < 0) return fail(MOE_ERR_INVALID_ARG, "num_rows must be >= 0");
-    MOE_CUDA(launch_combine(ypair_hi, ypair_res, row_index, rows, yshared_hi, yshared_res, N, H, k,
-                            out, num_sms_of_current_device(), stream),
+    if (yshared_hi && N > (int64_t(1) << 31) / shared_slots)
+        return fail(MOE_ERR_UNSUPPORTED, "N*shared_slots must stay below 2^31");
+    MOE_CUDA(launch_combine(ypair_hi, ypair_res, row_index, rows, yshared_hi, yshared_res,
+                            yshared_hi ? shared_slots : 0, N, H, k, out,
+                            num_sms_of_current_device(), stream),
              "combine kernel launch");
     g_launches += 1;
     return MOE_OK;
 }
 
 moe_status_t moe_combine(const moe_bf16_t *ypair_hi, const int8_t *ypair_res,
-                         const moe_bf16_t *yshared_hi, const int8_t *yshared_res, int64_t N,
-                         int H, int k, moe_bf16_t *out, cudaStream_t stream) {
-    return combine_impl(ypair_hi, ypair_res, nullptr, N * k, yshared_hi, yshared_res, N, H, k,
-                        out, stream);
+                         const moe_bf16_t *yshared_hi, const int8_t *yshared_res,
+                         int shared_slots, int64_t N, int H, int k, moe_bf16_t *out,
+                         cudaStream_t stream) {
+    return combine_impl(ypair_hi, ypair_res, nullptr, N * k, yshared_hi, yshared_res,
+                        shared_slots, N, H, k, out, stream);
 }
 
 moe_status_t moe_combine_indexed(const moe_bf16_t *yrows_hi, const int8_t *yrows_res,
                                  int64_t num_rows, const int32_t *row_index,
                                  const moe_bf16_t *yshared_hi, const int8_t *yshared_res,
-                                 int64_t N, int H, int k, moe_bf16_t *out, cudaStream_t stream) {
+                                 int shared_slots, int64_t N, int H, int k, moe_bf16_t *out,
+                                 cudaStream_t stream) {
     g_last_error.clear();
     if (N > 0 && !row_index) return fail(MOE_ERR_INVALID_ARG, "row_index must be non-null");
     if (N > 0 && num_rows > 0 && (!yrows_hi || !yrows_res))
@@ -916,8 +984,8 @@ moe_status_t moe_combine_indexed(const moe_bf16_t *yrows_hi, const int8_t *yrows
     alignas(16) static const uint8_t kNone[16] = {};
     const moe_bf16_t *hi = num_rows > 0 ? yrows_hi : reinterpret_cast<const moe_bf16_t *>(kNone);
     const int8_t *res = num_rows > 0 ? yrows_res : reinterpret_cast<const int8_t *>(kNone);
-    return combine_impl(hi, res, row_index, num_rows, yshared_hi, yshared_res, N, H, k, out,
-                        stream);
+    return combine_impl(hi, res, row_index, num_rows, yshared_hi, yshared_res, shared_slots, N, H,
+                        k, out, stream);
 }
 
 // ------------------------------------------------- expert-parallel dispatch
@@ -1199,6 +1267,7 @@ static moe_status_t dense_mlp_impl(const moe_bf16_t *x, const moe_bf16_t *w_gate
     MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int32_t), stream), "status reset");
     // one dense group: every token row, weight 1
     GemmArgs g = {};
+    g.virt_base = INT_MAX;  // no virtual experts
     g.sorted_pair = nullptr;
     g.block_expert = nullptr;
     g.num_padded = nullptr;
@@ -1255,7 +1324,7 @@ static moe_status_t dense_mlp_impl(const moe_bf16_t *x, const moe_bf16_t *w_gate
                  "dense down kernel launch");
     }
     // pair rows -> bf16 out (the combine with one slot per token)
-    MOE_CUDA(launch_combine(y, y_res, nullptr, N, nullptr, nullptr, N, H, 1, out, sms, stream),
+    MOE_CUDA(launch_combine(y, y_res, nullptr, N, nullptr, nullptr, 0, N, H, 1, out, sms, stream),
              "combine kernel launch");
     g_launches += 3;
     return MOE_OK;

@@ -6,8 +6,9 @@
 // pair p = n*k + j at row p of ypair, so token n's k contributions are the k
 // consecutive rows n*k .. n*k+k-1.  They are decoded (pair_rows.cuh: bf16 hi
 // + int8 residual, 16 significant bits), summed in slot order in fp32, the
-// shared-expert term gamma * SharedMLP(x) (same page, talker line) is added
-// last, and the result is rounded to bf16 once.  The contributions need
+// shared-expert term gamma * SharedMLP(x) (same page, talker line), given as
+// shared_slots partial rows per token (its chunks of intermediate rows), is
+// added last in chunk order, and the result is rounded to bf16 once.  The contributions need
 // those 16 bits: the bf16 rounding of the exact result already uses ~97% of
 // the layer's max-error bound at prefill size, and an fp16 rounding of each
 // contribution (11 bits) pushed the largest outputs past it.
@@ -49,8 +50,8 @@ __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(const uint16_t *__restrict__ ypair_hi, const int8_t *__restrict__ ypair_res,
                    const int32_t *__restrict__ row_index, int64_t rows,
                    const uint16_t *__restrict__ yshared_hi,
-                   const int8_t *__restrict__ yshared_res, int64_t N, int H, int k,
-                   uint16_t *__restrict__ out) {
+                   const int8_t *__restrict__ yshared_res, int shared_slots, int64_t N,
+                   int H, int k, uint16_t *__restrict__ out) {
     griddep_launch_dependents();
     griddep_wait();
     const int groups = H / 8;
@@ -66,7 +67,8 @@ __global__ void __launch_bounds__(kCombineThreads)
             if (row < 0 || row >= rows) continue;  // a pair that was never sent
             add_pair8(acc, ypair_hi, ypair_res, row * H + col);
         }
-        if (yshared_hi) add_pair8(acc, yshared_hi, yshared_res, n * H + col);
+        for (int c = 0; c < shared_slots; ++c)
+            add_pair8(acc, yshared_hi, yshared_res, (n * shared_slots + c) * H + col);
         uint4 pk;
         pk.x = pack_bf16x2(acc[0], acc[1]);
         pk.y = pack_bf16x2(acc[2], acc[3]);
@@ -80,15 +82,15 @@ __global__ void __launch_bounds__(kCombineThreads)
 
 cudaError_t launch_combine(const uint16_t *ypair_hi, const int8_t *ypair_res,
                            const int32_t *row_index, int64_t rows, const uint16_t *yshared_hi,
-                           const int8_t *yshared_res, int64_t N, int H, int k, uint16_t *out,
-                           int num_sms, cudaStream_t s) {
+                           const int8_t *yshared_res, int shared_slots, int64_t N, int H, int k,
+                           uint16_t *out, int num_sms, cudaStream_t s) {
     const int64_t total = N * (H / 8);
     int64_t blocks = (total + kCombineThreads - 1) / kCombineThreads;
     const int64_t cap = static_cast<int64_t>(num_sms) * 16;
     if (blocks > cap) blocks = cap;
     return launch_pdl(combine_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kCombineThreads),
-                      0, s, 1, ypair_hi, ypair_res, row_index, rows, yshared_hi, yshared_res, N,
-                      H, k, out);
+                      0, s, 1, ypair_hi, ypair_res, row_index, rows, yshared_hi, yshared_res,
+                      yshared_hi ? shared_slots : 0, N, H, k, out);
 }
 
 }  // namespace moe

@@ -74,6 +74,22 @@ __global__ void __launch_bounds__(kEpThreads)
     }
 }
 
+// The shared expert run on its own (a rank's local term): every token n
+// gets C slots p = n C + c, slot c being chunk c (virtual expert c) with
+// the shared gate gamma[n] as its weight.
+__global__ void __launch_bounds__(kEpThreads)
+    shared_slots_kernel(const float *__restrict__ gamma, int64_t N, int C,
+                        int32_t *__restrict__ ids, float *__restrict__ w) {
+    griddep_launch_dependents();
+    griddep_wait();  // gamma may come from the routing kernel just before
+    const int64_t P = N * C;
+    for (int64_t p = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; p < P;
+         p += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        ids[p] = static_cast<int32_t>(p % C);
+        w[p] = __ldcg(gamma + p / C);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_ep_dest(const int32_t *ids, int64_t P, int E, int e_local, int32_t *dest,
@@ -98,6 +114,16 @@ cudaError_t launch_ep_pack(const uint16_t *x, const int32_t *ids, const float *w
     return launch_pdl(ep_pack_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kEpThreads), 0, s,
                       1, x, ids, weights, order, num_rows, P, H, k, e_local, send_x, send_ids,
                       send_w, inv);
+}
+
+cudaError_t launch_shared_slots(const float *gamma, int64_t N, int C, int32_t *ids, float *w,
+                                int num_sms, cudaStream_t s) {
+    int64_t blocks = (N * C + kEpThreads - 1) / kEpThreads;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 4;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    return launch_pdl(shared_slots_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kEpThreads),
+                      0, s, 1, gamma, N, C, ids, w);
 }
 
 }  // namespace moe

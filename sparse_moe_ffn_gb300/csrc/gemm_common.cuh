@@ -22,6 +22,34 @@ __device__ __forceinline__ float silu_times(float g, float u) {
     return g / (1.f + __expf(-g)) * u;
 }
 
+// Where the weight rows of N tile nt of group (expert) `expert` are: the
+// routed weights (row expert * w_rows + n0 + extra, K from 0), or, for a
+// virtual expert of the folded shared expert, the shared weights (gate/up:
+// row v * virt_chunk + n0; down: row n0 + extra, K from v * virt_chunk).
+struct WeightCoord {
+    bool shared;
+    int row;
+    int k0;
+};
+
+template <int MODE>
+__device__ __forceinline__ WeightCoord weight_coord(const GemmArgs &a, int expert, int n0,
+                                                    int extra) {
+    WeightCoord c;
+    c.shared = expert >= a.virt_base;
+    if (!c.shared) {
+        c.row = static_cast<int>(static_cast<int64_t>(expert) * a.w_rows) + n0 + extra;
+        c.k0 = 0;
+    } else if (MODE == kGateUp) {
+        c.row = (expert - a.virt_base) * a.virt_chunk + n0 + extra;
+        c.k0 = 0;
+    } else {
+        c.row = n0 + extra;
+        c.k0 = (expert - a.virt_base) * a.virt_chunk;
+    }
+    return c;
+}
+
 // One row of a tile: grouped row `grow`, the pair (or token) q it holds,
 // whether it is real, and the down projection's scale.  Loaded before the
 // tile's accumulator is ready, so that the two dependent L2 reads overlap

@@ -89,7 +89,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                         const __grid_constant__ CUtensorMap tm_a_box,
                         const __grid_constant__ CUtensorMap tm_b0,
-                        const __grid_constant__ CUtensorMap tm_b1, const GemmArgs a) {
+                        const __grid_constant__ CUtensorMap tm_b1,
+                        const __grid_constant__ CUtensorMap tm_s0,
+                        const __grid_constant__ CUtensorMap tm_s1, const GemmArgs a) {
     using C = Cfg<MODE, BN_>;
     constexpr int BN = C::BN;
     constexpr int kStages = C::STAGES;
@@ -182,7 +184,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int lo = static_cast<int>(a.lo_rows);  // split: rows of the lo half
             const uint32_t tx = a_bytes + C::B_BYTES;
             const int arow = blk * kBlockM;
-            const int brow = static_cast<int>(static_cast<int64_t>(expert) * a.w_rows) + nt * BN;
+            const WeightCoord wc = weight_coord<MODE>(a, expert, nt * BN, 0);
+            const CUtensorMap *mb0 = wc.shared ? &tm_s0 : &tm_b0;
+            const CUtensorMap *mb1 = wc.shared ? &tm_s1 : &tm_b1;
             for (int kc = 0; kc < nk; ++kc, ++g) {
                 const int s = g % kStages;
                 const uint32_t use = g / kStages;
@@ -216,17 +220,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     src[3] + lo);
                 }
                 if (lane == 0) {
+                    const int kx = wc.k0 + kc * kBlockK;
                     if (a.stream_weights) {
-                        tma_load_2d_hint(st + kBOffset, &tm_b0, &sm->full[s], kc * kBlockK, brow,
-                                         wpol);
+                        tma_load_2d_hint(st + kBOffset, mb0, &sm->full[s], kx, wc.row, wpol);
                         if (MODE == kGateUp)
-                            tma_load_2d_hint(st + kBOffset + BN * 128, &tm_b1, &sm->full[s],
-                                             kc * kBlockK, brow, wpol);
+                            tma_load_2d_hint(st + kBOffset + BN * 128, mb1, &sm->full[s], kx,
+                                             wc.row, wpol);
                     } else {
-                        tma_load_2d(st + kBOffset, &tm_b0, &sm->full[s], kc * kBlockK, brow);
+                        tma_load_2d(st + kBOffset, mb0, &sm->full[s], kx, wc.row);
                         if (MODE == kGateUp)
-                            tma_load_2d(st + kBOffset + BN * 128, &tm_b1, &sm->full[s],
-                                        kc * kBlockK, brow);
+                            tma_load_2d(st + kBOffset + BN * 128, mb1, &sm->full[s], kx, wc.row);
                     }
                 }
             }
@@ -412,7 +415,8 @@ cudaError_t launch_gather_rows(const uint16_t *x, int H, int k, const int32_t *s
 
 template <int MODE, int BN>
 cudaError_t launch_one(const CUtensorMap &tm_a, const CUtensorMap &tm_a_box,
-                       const CUtensorMap &tm_b0, const CUtensorMap &tm_b1, const GemmArgs &a,
+                       const CUtensorMap &tm_b0, const CUtensorMap &tm_b1,
+                       const CUtensorMap &tm_s0, const CUtensorMap &tm_s1, const GemmArgs &a,
                        cudaStream_t s) {
     using C = Cfg<MODE, BN>;
     const size_t smem = 1024 + static_cast<size_t>(C::STAGES) * C::STAGE_BYTES + sizeof(GemmSmem);
@@ -421,7 +425,7 @@ cudaError_t launch_one(const CUtensorMap &tm_a, const CUtensorMap &tm_a_box,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
     return launch_pdl(kern, dim3(a.grid), dim3(kThreads), smem, s, 1, tm_a, tm_a_box, tm_b0,
-                      tm_b1, a);
+                      tm_b1, tm_s0, tm_s1, a);
 }
 
 bool gemm_block_n_supported(GemmMode mode, int bn) {
@@ -430,15 +434,18 @@ bool gemm_block_n_supported(GemmMode mode, int bn) {
 
 cudaError_t launch_gemm(GemmMode mode, int bn, const CUtensorMap &tm_a,
                         const CUtensorMap &tm_a_box, const CUtensorMap &tm_b0,
-                        const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s) {
+                        const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s,
+                        const CUtensorMap *tm_s0, const CUtensorMap *tm_s1) {
+    const CUtensorMap &s0 = tm_s0 ? *tm_s0 : tm_b0;
+    const CUtensorMap &s1 = tm_s1 ? *tm_s1 : tm_b1;
     if (mode == kGateUp && bn == 96)
-        return launch_one<kGateUp, 96>(tm_a, tm_a_box, tm_b0, tm_b1, a, s);
+        return launch_one<kGateUp, 96>(tm_a, tm_a_box, tm_b0, tm_b1, s0, s1, a, s);
     if (mode == kGateUp && bn == 128)
-        return launch_one<kGateUp, 128>(tm_a, tm_a_box, tm_b0, tm_b1, a, s);
+        return launch_one<kGateUp, 128>(tm_a, tm_a_box, tm_b0, tm_b1, s0, s1, a, s);
     if (mode == kDown && bn == 256)
-        return launch_one<kDown, 256>(tm_a, tm_a_box, tm_b0, tm_b1, a, s);
+        return launch_one<kDown, 256>(tm_a, tm_a_box, tm_b0, tm_b1, s0, s1, a, s);
     if (mode == kDownSplit && bn == 256)
-        return launch_one<kDownSplit, 256>(tm_a, tm_a_box, tm_b0, tm_b1, a, s);
+        return launch_one<kDownSplit, 256>(tm_a, tm_a_box, tm_b0, tm_b1, s0, s1, a, s);
     return cudaErrorInvalidValue;
 }
 

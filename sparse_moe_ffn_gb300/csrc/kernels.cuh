@@ -57,6 +57,13 @@ struct RouterArgs {
     uint16_t *topk_w_bf16;
     float *gamma;
     int32_t *status;
+    // row stride of topk_w / topk_ids / topk_w_bf16 (k, or k + virt_slots)
+    int out_ld;
+    // > 0: after its k routed slots every token gets virt_slots more, the
+    // shared expert's chunks as virtual experts virt_base, virt_base + 1, ...,
+    // each with weight sigmoid(x . g) (the shared gate)
+    int virt_slots;
+    int virt_base;
 };
 
 int router_split(int H);  // 1, 2, 4 or 8: depends on H only (batch invariance)
@@ -143,6 +150,14 @@ struct GemmArgs {
     int act_ready_count;
     int max_tiles;      // upper bound on tiles (sizes the persistent grid)
     int grid;           // persistent CTAs
+    // the shared expert folded in as virtual experts: groups (experts) from
+    // virt_base on are its chunks of virt_chunk intermediate rows, whose
+    // weights come from the shared maps (tm_s0 / tm_s1 of the launchers):
+    // gate/up, chunk v: rows v * virt_chunk + n0 of shared gate_proj /
+    // up_proj; down, chunk v: K columns from v * virt_chunk of shared
+    // down_proj.  Rows or columns past I_s read as zero (TMA fill).
+    int virt_base;      // INT_MAX without a shared expert
+    int virt_chunk;
 };
 
 // Tile widths: gate/up 96 or 128 columns (of each of gate and up), down 256.
@@ -155,9 +170,12 @@ bool gemm_block_n_supported(GemmMode mode, int bn);
 // tm_a: 1-row boxes for gather4 of sparse blocks; tm_a_box: 128-row boxes over
 // rows that are contiguous per block; tm_b0 / tm_b1: weight rows, boxes of bn
 // rows.
+// tm_s0 / tm_s1 (nullable): the shared expert's weight maps (see
+// GemmArgs::virt_base), boxes as tm_b0 / tm_b1
 cudaError_t launch_gemm(GemmMode mode, int bn, const CUtensorMap &tm_a,
                         const CUtensorMap &tm_a_box, const CUtensorMap &tm_b0,
-                        const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s);
+                        const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s,
+                        const CUtensorMap *tm_s0 = nullptr, const CUtensorMap *tm_s1 = nullptr);
 // x rows copied into expert order (x_sorted [cap, H]): the real rows of dense
 // blocks, or of every block when all_blocks is set
 cudaError_t launch_gather_rows(const uint16_t *x, int H, int k, const int32_t *sorted_pair,
@@ -179,20 +197,25 @@ int pair_gemm_block_n(GemmMode mode);
 // (sorted_pair, block_expert, num_padded).
 cudaError_t launch_sparse_gemm(GemmMode mode, int bn, const CUtensorMap &tm_a,
                                const CUtensorMap &tm_b0, const CUtensorMap &tm_b1,
-                               const GemmArgs &a, cudaStream_t s);
+                               const GemmArgs &a, cudaStream_t s,
+                               const CUtensorMap *tm_s0 = nullptr,
+                               const CUtensorMap *tm_s1 = nullptr);
 cudaError_t launch_pair_gemm(GemmMode mode, const CUtensorMap &tm_a, const CUtensorMap &tm_b0,
-                             const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s);
+                             const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s,
+                             const CUtensorMap *tm_s0 = nullptr,
+                             const CUtensorMap *tm_s1 = nullptr);
 
 // ----------------------------------------------------------------- combine
 
 // ypair / yshared: pair rows (bf16 hi plane, int8 residual plane); pair p's
 // row is row_index[p] when row_index is given (the order in which
 // expert-parallel results come back; an index outside [0, rows) adds
-// nothing), else p
+// nothing), else p; yshared (nullable): shared_slots rows per token, row
+// n * shared_slots + c, added after the k slots in chunk order
 cudaError_t launch_combine(const uint16_t *ypair_hi, const int8_t *ypair_res,
                            const int32_t *row_index, int64_t rows, const uint16_t *yshared_hi,
-                           const int8_t *yshared_res, int64_t N, int H, int k, uint16_t *out,
-                           int num_sms, cudaStream_t s);
+                           const int8_t *yshared_res, int shared_slots, int64_t N, int H, int k,
+                           uint16_t *out, int num_sms, cudaStream_t s);
 
 // ------------------------------------------- expert-parallel dispatch plan
 
@@ -206,6 +229,10 @@ cudaError_t launch_ep_pack(const uint16_t *x, const int32_t *ids, const float *w
                            const int32_t *order, const int32_t *num_rows, int64_t P, int H, int k,
                            int e_local, uint16_t *send_x, int32_t *send_ids, float *send_w,
                            int32_t *inv, int num_sms, cudaStream_t s);
+// ids[n*C + c] = c, w[n*C + c] = gamma[n]: the slots of the shared expert's
+// C chunks when it runs on its own
+cudaError_t launch_shared_slots(const float *gamma, int64_t N, int C, int32_t *ids, float *w,
+                                int num_sms, cudaStream_t s);
 
 // ------------------------------------------- bf16 -> fp16 weight conversion
 

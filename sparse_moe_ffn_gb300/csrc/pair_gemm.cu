@@ -210,7 +210,9 @@ template <int MODE>
 __global__ void __launch_bounds__(kPairThreads, 1)
     pair_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                      const __grid_constant__ CUtensorMap tm_b0,
-                     const __grid_constant__ CUtensorMap tm_b1, const GemmArgs a) {
+                     const __grid_constant__ CUtensorMap tm_b1,
+                     const __grid_constant__ CUtensorMap tm_s0,
+                     const __grid_constant__ CUtensorMap tm_s1, const GemmArgs a) {
     using C = PairCfg<MODE>;
     constexpr int BN = C::BN;
     constexpr int kStages = C::STAGES;
@@ -343,9 +345,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 const int arow = pt.block * kBlockM;
                 // gate/up: Wg rows (even CTA) or Wu rows (odd CTA) of N tile nt;
                 // down: this CTA's half of the Wd rows of N tile nt
-                const int brow = static_cast<int>(static_cast<int64_t>(pt.group) * a.w_rows) +
-                                 nt * BN + (is_down(MODE) ? static_cast<int>(rank) * C::B_ROWS : 0);
-                const CUtensorMap *tm_b = (MODE == kGateUp && rank == 1) ? &tm_b1 : &tm_b0;
+                const WeightCoord wc = weight_coord<MODE>(
+                    a, pt.group, nt * BN, is_down(MODE) ? static_cast<int>(rank) * C::B_ROWS : 0);
+                const CUtensorMap *tm_b = (MODE == kGateUp && rank == 1)
+                                              ? (wc.shared ? &tm_s1 : &tm_b1)
+                                              : (wc.shared ? &tm_s0 : &tm_b0);
                 for (int kc = 0; kc < nk; ++kc, ++g) {
                     const int s = g % kStages;
                     const uint32_t use = g / kStages;
@@ -364,7 +368,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                             tma_load_pair(st + kATileBytes, &tm_a, bar, kc * kBlockK,
                                           arow + static_cast<int>(a.lo_rows));
                     }
-                    tma_load_pair(st + kBOffset, tm_b, bar, kc * kBlockK, brow);
+                    tma_load_pair(st + kBOffset, tm_b, bar, wc.k0 + kc * kBlockK, wc.row);
                 }
             }
             // the even CTA's stage barriers count both CTAs' bytes: it waits
@@ -489,14 +493,16 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 
 template <int MODE>
 cudaError_t launch_pair_one(const CUtensorMap &tm_a, const CUtensorMap &tm_b0,
-                            const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s) {
+                            const CUtensorMap &tm_b1, const CUtensorMap &tm_s0,
+                            const CUtensorMap &tm_s1, const GemmArgs &a, cudaStream_t s) {
     using C = PairCfg<MODE>;
     const size_t smem = 1024 + static_cast<size_t>(C::STAGES) * C::STAGE_BYTES + sizeof(PairSmem);
     auto kern = pair_gemm_kernel<MODE>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    return launch_pdl(kern, dim3(a.grid), dim3(kPairThreads), smem, s, 2, tm_a, tm_b0, tm_b1, a);
+    return launch_pdl(kern, dim3(a.grid), dim3(kPairThreads), smem, s, 2, tm_a, tm_b0, tm_b1,
+                      tm_s0, tm_s1, a);
 }
 
 }  // namespace
@@ -506,13 +512,16 @@ int pair_gemm_block_n(GemmMode mode) { return mode == kGateUp ? PairCfg<kGateUp>
 static_assert(PairCfg<kDown>::BN == PairCfg<kDownSplit>::BN, "one down tile width");
 
 cudaError_t launch_pair_gemm(GemmMode mode, const CUtensorMap &tm_a, const CUtensorMap &tm_b0,
-                             const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s) {
+                             const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s,
+                             const CUtensorMap *tm_s0, const CUtensorMap *tm_s1) {
     if (a.grid < 2 || a.grid % 2) return cudaErrorInvalidValue;
     if (a.pad_offsets && (a.num_groups < 1 || a.num_groups > kMaxGroups))
         return cudaErrorInvalidValue;
-    if (mode == kGateUp) return launch_pair_one<kGateUp>(tm_a, tm_b0, tm_b1, a, s);
-    if (mode == kDownSplit) return launch_pair_one<kDownSplit>(tm_a, tm_b0, tm_b1, a, s);
-    return launch_pair_one<kDown>(tm_a, tm_b0, tm_b1, a, s);
+    const CUtensorMap &s0 = tm_s0 ? *tm_s0 : tm_b0;
+    const CUtensorMap &s1 = tm_s1 ? *tm_s1 : tm_b1;
+    if (mode == kGateUp) return launch_pair_one<kGateUp>(tm_a, tm_b0, tm_b1, s0, s1, a, s);
+    if (mode == kDownSplit) return launch_pair_one<kDownSplit>(tm_a, tm_b0, tm_b1, s0, s1, a, s);
+    return launch_pair_one<kDown>(tm_a, tm_b0, tm_b1, s0, s1, a, s);
 }
 
 }  // namespace moe

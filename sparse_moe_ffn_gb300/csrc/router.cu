@@ -275,7 +275,12 @@ __global__ void __launch_bounds__(kRouterThreads, 1)
 #pragma unroll
             for (int j = 0; j < PL; ++j)
                 if (j == jg) lgate = lg[j];
-            a.gamma[n] = 1.f / (1.f + expf(-lgate));
+            const float gam = 1.f / (1.f + expf(-lgate));
+            a.gamma[n] = gam;
+            for (int c = 0; c < a.virt_slots; ++c) {  // the shared expert's chunks
+                a.topk_w[n * a.out_ld + a.k + c] = gam;
+                a.topk_ids[n * a.out_ld + a.k + c] = a.virt_base + c;
+            }
         }
 #pragma unroll
         for (int j = 0; j < PL; ++j) {
@@ -346,11 +351,11 @@ __global__ void __launch_bounds__(kRouterThreads, 1)
             const float inv = a.norm ? 1.f / wsum : 1.f;
             for (int r = sub; r < a.k; r += kLanesPerRow) {
                 const float w = slot_w[rl * a.k + r] * inv;
-                a.topk_w[n * a.k + r] = w;
-                a.topk_ids[n * a.k + r] = slot_e[rl * a.k + r];
+                a.topk_w[n * a.out_ld + r] = w;
+                a.topk_ids[n * a.out_ld + r] = slot_e[rl * a.k + r];
                 if (a.topk_w_bf16) {
                     __nv_bfloat16 h = __float2bfloat16_rn(w);
-                    a.topk_w_bf16[n * a.k + r] = *reinterpret_cast<uint16_t *>(&h);
+                    a.topk_w_bf16[n * a.out_ld + r] = *reinterpret_cast<uint16_t *>(&h);
                 }
             }
         }

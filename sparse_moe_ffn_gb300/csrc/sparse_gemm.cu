@@ -110,7 +110,9 @@ template <int MODE, int BN_>
 __global__ void __launch_bounds__(kSparseThreads, 1)
     sparse_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                        const __grid_constant__ CUtensorMap tm_b0,
-                       const __grid_constant__ CUtensorMap tm_b1, const GemmArgs a) {
+                       const __grid_constant__ CUtensorMap tm_b1,
+                       const __grid_constant__ CUtensorMap tm_s0,
+                       const __grid_constant__ CUtensorMap tm_s1, const GemmArgs a) {
     using C = SparseCfg<MODE, BN_>;
     constexpr int BN = C::BN;
     constexpr int kStages = C::STAGES;
@@ -169,7 +171,8 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
     // while memory is otherwise idle (routing)
     // (half of the tile's rows: the same gain as the whole tile in a timed
     // decode loop, with half the L2 footprint)
-    if (by_expert && threadIdx.x == 0 && static_cast<int>(blockIdx.x) < a.num_groups * n_tiles) {
+    if (by_expert && threadIdx.x == 0 && static_cast<int>(blockIdx.x) < a.num_groups * n_tiles &&
+        static_cast<int>(blockIdx.x) / n_tiles < a.virt_base) {
         const int64_t e = blockIdx.x / n_tiles;
         const int64_t r0 = static_cast<int64_t>(blockIdx.x % n_tiles) * BN;
         const int64_t nrows = min(static_cast<int64_t>(BN), a.w_rows - r0) / 2;
@@ -283,7 +286,9 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
 #pragma unroll
             for (int i = 0; i < 4; ++i)
                 if (src[i] < 0) src[i] = first_valid;
-            const int brow = static_cast<int>(static_cast<int64_t>(expert) * a.w_rows) + nt * BN;
+            const WeightCoord wc = weight_coord<MODE>(a, expert, nt * BN, 0);
+            const CUtensorMap *mb0 = wc.shared ? &tm_s0 : &tm_b0;
+            const CUtensorMap *mb1 = wc.shared ? &tm_s1 : &tm_b1;
             if (is_down(MODE) && handoff && passes > 0) {
                 // this expert's activation rows are complete once all its
                 // gate/up tiles are stored (bounded wait by lane 0; the warp
@@ -339,17 +344,17 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
                         }
                     }
                     if (lane == 0) {
+                        const int kx = wc.k0 + kc * kBlockK;
                         if (a.stream_weights) {
-                            tma_load_2d_hint(st + kBOffset, &tm_b0, &sm->full[s], kc * kBlockK,
-                                             brow, wpol);
+                            tma_load_2d_hint(st + kBOffset, mb0, &sm->full[s], kx, wc.row, wpol);
                             if (MODE == kGateUp)
-                                tma_load_2d_hint(st + kBOffset + BN * 128, &tm_b1, &sm->full[s],
-                                                 kc * kBlockK, brow, wpol);
+                                tma_load_2d_hint(st + kBOffset + BN * 128, mb1, &sm->full[s], kx,
+                                                 wc.row, wpol);
                         } else {
-                            tma_load_2d(st + kBOffset, &tm_b0, &sm->full[s], kc * kBlockK, brow);
+                            tma_load_2d(st + kBOffset, mb0, &sm->full[s], kx, wc.row);
                             if (MODE == kGateUp)
-                                tma_load_2d(st + kBOffset + BN * 128, &tm_b1, &sm->full[s],
-                                            kc * kBlockK, brow);
+                                tma_load_2d(st + kBOffset + BN * 128, mb1, &sm->full[s], kx,
+                                            wc.row);
                         }
                     }
                 }
@@ -472,27 +477,35 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
 
 template <int MODE, int BN>
 cudaError_t launch_sparse_one(const CUtensorMap &tm_a, const CUtensorMap &tm_b0,
-                              const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s) {
+                              const CUtensorMap &tm_b1, const CUtensorMap &tm_s0,
+                              const CUtensorMap &tm_s1, const GemmArgs &a, cudaStream_t s) {
     using C = SparseCfg<MODE, BN>;
     const size_t smem = 1024 + static_cast<size_t>(C::STAGES) * C::STAGE_BYTES + sizeof(SparseSmem);
     auto kern = sparse_gemm_kernel<MODE, BN>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    return launch_pdl(kern, dim3(a.grid), dim3(kSparseThreads), smem, s, 1, tm_a, tm_b0, tm_b1, a);
+    return launch_pdl(kern, dim3(a.grid), dim3(kSparseThreads), smem, s, 1, tm_a, tm_b0, tm_b1,
+                      tm_s0, tm_s1, a);
 }
 
 }  // namespace
 
 cudaError_t launch_sparse_gemm(GemmMode mode, int bn, const CUtensorMap &tm_a,
                                const CUtensorMap &tm_b0, const CUtensorMap &tm_b1,
-                               const GemmArgs &a, cudaStream_t s) {
+                               const GemmArgs &a, cudaStream_t s, const CUtensorMap *tm_s0,
+                               const CUtensorMap *tm_s1) {
     if (!a.sorted_pair || !a.block_expert || !a.num_padded) return cudaErrorInvalidValue;
-    if (mode == kGateUp && bn == 96) return launch_sparse_one<kGateUp, 96>(tm_a, tm_b0, tm_b1, a, s);
-    if (mode == kGateUp && bn == 128) return launch_sparse_one<kGateUp, 128>(tm_a, tm_b0, tm_b1, a, s);
-    if (mode == kDown && bn == 256) return launch_sparse_one<kDown, 256>(tm_a, tm_b0, tm_b1, a, s);
+    const CUtensorMap &s0 = tm_s0 ? *tm_s0 : tm_b0;
+    const CUtensorMap &s1 = tm_s1 ? *tm_s1 : tm_b1;
+    if (mode == kGateUp && bn == 96)
+        return launch_sparse_one<kGateUp, 96>(tm_a, tm_b0, tm_b1, s0, s1, a, s);
+    if (mode == kGateUp && bn == 128)
+        return launch_sparse_one<kGateUp, 128>(tm_a, tm_b0, tm_b1, s0, s1, a, s);
+    if (mode == kDown && bn == 256)
+        return launch_sparse_one<kDown, 256>(tm_a, tm_b0, tm_b1, s0, s1, a, s);
     if (mode == kDownSplit && bn == 256)
-        return launch_sparse_one<kDownSplit, 256>(tm_a, tm_b0, tm_b1, a, s);
+        return launch_sparse_one<kDownSplit, 256>(tm_a, tm_b0, tm_b1, s0, s1, a, s);
     return cudaErrorInvalidValue;
 }
 

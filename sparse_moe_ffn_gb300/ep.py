@@ -28,10 +28,11 @@ own combine.  So the output equals moe_forward on the same tokens bit for
 bit, whatever the number of ranks.
 
 The shared expert (the talker layer) is dense: every rank holds its weights
-and applies it to its own tokens, with no exchange.  It runs as moe_experts
-with one expert, every row routed to it and the sigmoid gate as the row
-weight, which is moe_forward's shared term gamma * SharedMLP(x); the combine
-adds it after the k slots.
+and applies it to its own tokens, with no exchange.  It runs as
+moe_shared_expert, which computes moe_forward's shared term gamma *
+SharedMLP(x) the same way (its intermediate rows in chunks of the routed
+experts' I, one pair row per chunk); the combine adds the chunk rows after
+the k slots.
 
 Transport: gloo and NCCL both carry int32, so bf16 rows and int8 residual
 rows travel as their bit patterns viewed as int32 (H is a multiple of 8).
@@ -108,8 +109,9 @@ def ep_forward(x, router, w_gate, w_up, w_down, E: int, k: int, norm_topk_prob: 
     form as w_down), the same on every rank.  route_fn(x) returns (weights,
     ids) or (weights, ids, gamma); dispatch_fn(x, ids, w, E, world) returns
     (send_x, send_ids, send_w, send_counts, inv_order); experts_fn and
-    shared_fn return pair rows (hi bf16, res int8), each [rows, H];
-    combine_fn(yrows, inv_order, N, k, yshared) returns the output.
+    shared_fn return pair rows (hi bf16, res int8), each [rows, H] (the
+    shared term: S rows per token); combine_fn(yrows, inv_order, N, k,
+    yshared) returns the output.
     Returns out [N, H] bf16."""
     from sparse_moe_ffn_gb300 import binding
 
@@ -125,10 +127,9 @@ def ep_forward(x, router, w_gate, w_up, w_down, E: int, k: int, norm_topk_prob: 
             return binding.moe_experts(rows, local_ids, weights, w_gate, w_up, w_down)[0]
     if shared_fn is None and shared is not None:
         def shared_fn(t, gamma):
-            zeros = torch.zeros(t.shape[0], dtype=torch.int32, device=t.device)
-            return binding.moe_experts(t, zeros, gamma, shared["shared_gate_proj"][None],
-                                       shared["shared_up_proj"][None],
-                                       shared["shared_down_proj"][None])[0]
+            return binding.moe_shared_expert(t, gamma, w_gate.shape[1],
+                                             shared["shared_gate_proj"], shared["shared_up_proj"],
+                                             shared["shared_down_proj"])[0]
     if dispatch_fn is None:
         def dispatch_fn(t, ids_, w_, E_, world_):
             d = binding.moe_ep_dispatch(t, ids_, w_, E_, world_)

@@ -46,9 +46,13 @@ def test_layout_is_consistent(L):
     for args in [(64, 2048, 128, 768, 8, 0), (2048, 2048, 64, 768, 6, 2048), (16, 64, 6, 128, 2, 0)]:
         lay = binding.moe_forward_layout(*args)
         assert lay["total"] == binding.moe_forward_workspace_bytes(*args)
-        offs = [v for k, v in lay.items() if k not in ("total", "capacity")]
+        offs = [v for k, v in lay.items() if k not in ("total", "capacity", "slots", "groups")]
         assert all(o % 256 == 0 for o in offs)
-        N, H, E, I, k, _ = args
+        N, H, E, I, k0, I_s = args
+        # the shared expert adds ceil(I_s / I) slots per token and as many groups
+        C = -(-I_s // I)
+        assert lay["slots"] == k0 + C and lay["groups"] == E + C
+        k, E = k0 + C, E + C
         cap = lay["capacity"]
         assert cap == L.moe_align_capacity(N, k, E, 128)
         assert lay["ypair"] >= lay["act"] + 4 * cap * I          # bf16 hi/lo or fp16 act
@@ -80,6 +84,8 @@ def test_forward_argument_errors(L, prepared):
     assert fwd(L, shared=(FAKE, None, None, None), I_s=64) == INVALID
     assert fwd(L, shared=(FAKE,) * 4, I_s=60) == INVALID
     assert fwd(L, E=256, shared=(FAKE,) * 4, I_s=64) == UNSUPPORTED
+    # the shared expert's chunks count as experts: 248 + ceil(72 / 8) > 256
+    assert fwd(L, E=248, I=8, shared=(FAKE,) * 4, I_s=72) == UNSUPPORTED
     need = L.moe_forward_workspace_bytes(64, 2048, 128, 768, 8, 0)
     assert fwd(L, ws_bytes=need - 1) == SMALL
     assert b"needs" in L.moe_last_error()
@@ -117,8 +123,10 @@ def test_experts_and_combine_argument_errors(L, prepared):
     experts = functools.partial(_experts, prepared=prepared)
 
     # the expert-parallel receiving side: one routed row per (row, expert)
+    # moe_forward's layout with one slot per row, without the pair-row planes
+    # (the outputs go to the caller's y)
     assert L.moe_experts_workspace_bytes(64, 2048, 16, 768) == \
-        L.moe_forward_workspace_bytes(64, 2048, 16, 768, 1, 0)
+        binding.moe_forward_layout(64, 2048, 16, 768, 1, 0)["ypair"]
     assert experts(L, R=-1) == INVALID
     assert experts(L, H=2044) == INVALID
     assert experts(L, I=0) == INVALID
@@ -130,13 +138,15 @@ def test_experts_and_combine_argument_errors(L, prepared):
     assert experts(L, ws_bytes=need - 1) == SMALL
     assert experts(L, R=0, x=None) == OK          # no-op, nothing launched
     P = FAKE
-    assert L.moe_combine(P, P, None, None, 16, 2048, 0, P, None) == INVALID
-    assert L.moe_combine(P, P, None, None, 16, 2044, 2, P, None) == INVALID
-    assert L.moe_combine(None, P, None, None, 16, 2048, 2, P, None) == INVALID
-    assert L.moe_combine(P, None, None, None, 16, 2048, 2, P, None) == INVALID
-    assert L.moe_combine(P, P, P, None, 16, 2048, 2, P, None) == INVALID   # one shared plane
-    assert L.moe_combine(P, P, P + 2, P, 16, 2048, 2, P, None) == INVALID  # misaligned
-    assert L.moe_combine(P, P, None, None, 0, 2048, 2, None, None) == OK
+    assert L.moe_combine(P, P, None, None, 0, 16, 2048, 0, P, None) == INVALID
+    assert L.moe_combine(P, P, None, None, 0, 16, 2044, 2, P, None) == INVALID
+    assert L.moe_combine(None, P, None, None, 0, 16, 2048, 2, P, None) == INVALID
+    assert L.moe_combine(P, None, None, None, 0, 16, 2048, 2, P, None) == INVALID
+    assert L.moe_combine(P, P, P, None, 1, 16, 2048, 2, P, None) == INVALID   # one shared plane
+    assert L.moe_combine(P, P, P + 2, P, 1, 16, 2048, 2, P, None) == INVALID  # misaligned
+    assert L.moe_combine(P, P, P, P, 0, 16, 2048, 2, P, None) == INVALID      # no shared slots
+    assert L.moe_combine(P, P, P, P, 257, 16, 2048, 2, P, None) == INVALID
+    assert L.moe_combine(P, P, None, None, 0, 0, 2048, 2, None, None) == OK
 
 
 def test_dense_mlp_argument_errors(L):
@@ -197,7 +207,39 @@ def test_dispatch_and_indexed_combine_argument_errors(L):
     assert disp(ws_bytes=need - 1) == SMALL
     assert disp(N=0, x=None) == OK
     # indexed combine: row_index required, both shared planes or neither
-    assert L.moe_combine_indexed(P, P, 10, None, None, None, 4, 2048, 2, P, None) == INVALID
-    assert L.moe_combine_indexed(P, P, 10, P, P, None, 4, 2048, 2, P, None) == INVALID
-    assert L.moe_combine_indexed(P, P, -1, P, None, None, 4, 2048, 2, P, None) == INVALID
-    assert L.moe_combine_indexed(None, None, 0, None, None, None, 0, 2048, 2, None, None) == OK
+    assert L.moe_combine_indexed(P, P, 10, None, None, None, 0, 4, 2048, 2, P, None) == INVALID
+    assert L.moe_combine_indexed(P, P, 10, P, P, None, 1, 4, 2048, 2, P, None) == INVALID
+    assert L.moe_combine_indexed(P, P, -1, P, None, None, 0, 4, 2048, 2, P, None) == INVALID
+    assert L.moe_combine_indexed(P, P, 10, P, P, P, 0, 4, 2048, 2, P, None) == INVALID
+    assert L.moe_combine_indexed(None, None, 0, None, None, None, 0, 0, 2048, 2, None,
+                                 None) == OK
+
+
+def _shared(L, N=64, H=2048, I=768, I_s=2048, x=FAKE, gamma=FAKE, y=FAKE, ws=FAKE * 16,
+            ws_bytes=None, prepared=False):
+    if ws_bytes is None:
+        ws_bytes = L.moe_shared_expert_workspace_bytes(N, H, I, I_s)
+    fn = L.moe_shared_expert_prepared if prepared else L.moe_shared_expert
+    return fn(x, gamma, N, H, I, I_s, FAKE, FAKE, FAKE, y, FAKE, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("prepared", [False, True])
+def test_shared_expert_argument_errors(L, prepared):
+    shared = functools.partial(_shared, L, prepared=prepared)
+    assert L.moe_shared_chunks(768, 2048) == 3
+    assert L.moe_shared_chunks(768, 768) == 1
+    assert L.moe_shared_chunks(64, 8) == 1
+    # the layout of moe_forward with no routed experts and C chunk slots
+    lay = binding.moe_forward_layout(64, 2048, 1, 768, 1, 2048)
+    assert L.moe_shared_expert_workspace_bytes(64, 2048, 768, 2048) <= lay["total"]
+    assert shared(N=-1) == INVALID
+    assert shared(H=2044) == INVALID
+    assert shared(I=0) == INVALID
+    assert shared(I_s=60) == INVALID
+    assert shared(I=8, I_s=8 * 257) == UNSUPPORTED   # 257 chunks
+    assert shared(gamma=None) == INVALID
+    assert shared(y=FAKE + 2) == INVALID
+    assert shared(ws=FAKE + 64) == INVALID
+    need = L.moe_shared_expert_workspace_bytes(64, 2048, 768, 2048)
+    assert shared(ws_bytes=need - 1) == SMALL
+    assert shared(N=0, x=None) == OK

@@ -43,13 +43,48 @@ def test_experts_rows_and_combine_match_forward(name, form):
 @pytest.mark.parametrize("form", FORMS)
 @pytest.mark.parametrize("name", ["decode", "prefill", "talker"])
 def test_ep_forward_one_rank_equals_forward(name, form):
-    """talker: the shared expert runs as a one-expert moe_experts call with
-    the sigmoid gate as the row weight, and matches moe_forward's term."""
+    """talker: the shared expert runs as moe_shared_expert (chunk rows, no
+    exchange), and matches moe_forward's shared slots."""
     shape, dev, _ = prepared(name, form=form)
     out, _ = run_forward(shape, dev)
     got = ep_forward(dev["x"], dev["router"], dev["w_gate"], dev["w_up"], dev["w_down"],
                      shape.E, shape.k, shape.norm_topk_prob, shared=shared_of(shape, dev))
     assert torch.equal(got, out)
+
+
+SHARED_CASES = {
+    "talker": None,  # I_s = 2048 in three chunks of I = 768 (the last one 512 rows)
+    "three-chunks": MoEShape("three-chunks", N=200, H=128, E=8, k=2, I=64, I_s=160,
+                             norm_topk_prob=False),
+}
+
+
+@pytest.mark.parametrize("form", FORMS)
+@pytest.mark.parametrize("case", list(SHARED_CASES))
+def test_shared_expert_rows_equal_forward_slots(case, form):
+    """moe_shared_expert's chunk rows equal the pair rows moe_forward holds in
+    slots k .. k+C-1 bit for bit, and combining the routed slots with them
+    gives the layer's output."""
+    if SHARED_CASES[case] is None:
+        shape, dev, _ = prepared(case, form=form)
+    else:
+        shape, dev, _ = prepare(SHARED_CASES[case], seed=8, form=form)
+    out, ws = run_forward(shape, dev)
+    v = binding.workspace_views(ws, shape.N, shape.H, shape.E, shape.I, shape.k, shape.I_s)
+    slots, k, H = v["slots"], shape.k, shape.H
+    C = slots - k
+    assert C == binding.moe_shared_chunks(shape.I, shape.I_s)
+    y, sws = binding.moe_shared_expert(dev["x"], v["gamma"].clone(), shape.I,
+                                       dev["shared_gate_proj"], dev["shared_up_proj"],
+                                       dev["shared_down_proj"])
+    torch.cuda.synchronize()
+    assert binding.moe_read_device_status(sws) == 0
+    hi = v["ypair"][0].view(shape.N, slots, H)
+    res = v["ypair"][1].view(shape.N, slots, H)
+    assert torch.equal(y[0], hi[:, k:].reshape(-1, H))
+    assert torch.equal(y[1], res[:, k:].reshape(-1, H))
+    routed = (hi[:, :k].reshape(-1, H).contiguous(), res[:, :k].reshape(-1, H).contiguous())
+    assert torch.equal(binding.moe_combine(routed, shape.N, k, yshared=y), out)
 
 
 @pytest.mark.parametrize("name,world", [("decode", 2), ("prefill", 2), ("prefill", 3),

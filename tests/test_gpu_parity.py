@@ -115,8 +115,16 @@ def test_forward_matches_oracle(name, form):
     # the stages inside the workspace: routing and grouping bit-exact
     v = binding.workspace_views(ws, shape.N, shape.H, shape.E, shape.I, shape.k, shape.I_s)
     _, _, _, ids_ref = oracle.route(bits["x"], bits["router"], shape.k, shape.norm_topk_prob)
-    assert np.array_equal(v["topk_ids"].cpu().numpy(), ids_ref)
-    al = oracle.align(ids_ref, shape.E, 128)
+    assert np.array_equal(v["routed_ids"].cpu().numpy(), ids_ref)
+    # the shared expert's chunks: virtual experts E, E+1, ... in the slots
+    # after the routed ones, for every token
+    C = v["slots"] - shape.k
+    assert C == (-(-shape.I_s // shape.I) if shape.I_s else 0)
+    all_ids = np.concatenate(
+        [ids_ref, np.tile(np.arange(shape.E, shape.E + C, dtype=ids_ref.dtype), (shape.N, 1))],
+        axis=1)
+    assert np.array_equal(v["topk_ids"].cpu().numpy(), all_ids)
+    al = oracle.align(all_ids, shape.E + C, 128)
     npad = int(v["num_padded"].item())
     assert npad == al["num_padded"]
     assert np.array_equal(v["counts"].cpu().numpy(), al["counts"])
@@ -185,6 +193,11 @@ EDGE = [
     ("pairs-ragged-H-I", 700, 200, 5, 3, 200, 0, False),
     ("pairs-E1-k1", 520, 128, 1, 1, 128, 0, True),
     ("pairs-shared", 600, 128, 4, 2, 128, 64, True),
+    # the shared expert cut into three chunks of I rows, the last one partly
+    # zero padding: one-CTA tiles, CTA pairs, expert-indexed sparse tiles
+    ("shared-3-chunks", 200, 128, 8, 2, 64, 160, False),
+    ("pairs-shared-3-chunks", 600, 128, 4, 2, 96, 200, True),
+    ("sparse-shared-3-chunks", 24, 128, 16, 2, 64, 136, False),
 ]
 
 
