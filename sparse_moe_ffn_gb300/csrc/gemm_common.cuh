@@ -188,18 +188,22 @@ __device__ __forceinline__ void store_tile(const GemmArgs &a, uint32_t taddr, co
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
                     uint32_t pk[8], pr[4];
+                    float tv[16], hv[16];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const float t0 = w * yv[h * 16 + 2 * i];
-                        const float t1 = w * yv[h * 16 + 2 * i + 1];
-                        vmax = fmaxf(vmax, fmaxf(fabsf(t0), fabsf(t1)));
-                        pk[i] = pack_bf16x2(t0, t1);
+                        tv[2 * i] = w * yv[h * 16 + 2 * i];
+                        tv[2 * i + 1] = w * yv[h * 16 + 2 * i + 1];
+                        vmax = fmaxf(vmax, fmaxf(fabsf(tv[2 * i]), fabsf(tv[2 * i + 1])));
+                        pk[i] = pack_bf16x2(tv[2 * i], tv[2 * i + 1]);
                         const float2 hi = unpack_bf16x2(pk[i]);
-                        const uint32_t r2 = (static_cast<uint32_t>(pair_residual(t0, hi.x)) & 0xFFu) |
-                                            ((static_cast<uint32_t>(pair_residual(t1, hi.y)) & 0xFFu) << 8);
-                        if (i % 2 == 0) pr[i / 2] = r2;
-                        else pr[i / 2] |= r2 << 16;
+                        hv[2 * i] = hi.x;
+                        hv[2 * i + 1] = hi.y;
                     }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        pr[i] = pair_residual4(tv[4 * i], hv[4 * i], tv[4 * i + 1], hv[4 * i + 1],
+                                               tv[4 * i + 2], hv[4 * i + 2], tv[4 * i + 3],
+                                               hv[4 * i + 3]);
                     const int cc = c * 64 + h * 16;
                     store32(dst + cc, col0 + cc, pk);
                     if (col0 + cc + 16 <= a.n_out && res16) {

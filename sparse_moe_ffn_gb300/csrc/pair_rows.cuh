@@ -41,6 +41,32 @@ __device__ __forceinline__ int pair_residual(float v, float hi) {
     return static_cast<int>(r);
 }
 
+// Four residuals (of v[i] against hi[i]) packed as bytes 0..3 of a word,
+// with the arithmetic kept off the conversion pipe: (v - hi) * 2^(142 - f)
+// is exact (a difference of v and its own rounding, times a power of two)
+// and lies within [-128, 128], so one fused add of 1.5 * 2^23 rounds it to
+// the nearest integer, ties to even, exactly as rint does, and leaves that
+// integer in the low mantissa bits (1.5 * 2^23 has a zero low byte); the
+// clamp to [-127, 127] is taken on the sum, and the low bytes are gathered
+// with byte permutes.  Equal, byte for byte, to pair_residual.
+__device__ __forceinline__ uint32_t pair_residual_sum_bits(float v, float hi) {
+    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+    const int f = pair_exp_field(hi);
+    const float up = __uint_as_float(static_cast<uint32_t>(269 - f) << 23);  // 2^(142 - f)
+    float t = fmaf(v - hi, up, kMagic);
+    t = fminf(fmaxf(t, kMagic - 127.f), kMagic + 127.f);
+    return __float_as_uint(t);
+}
+
+__device__ __forceinline__ uint32_t pair_residual4(float v0, float h0, float v1, float h1,
+                                                   float v2, float h2, float v3, float h3) {
+    const uint32_t a = __byte_perm(pair_residual_sum_bits(v0, h0), pair_residual_sum_bits(v1, h1),
+                                   0x0040);
+    const uint32_t b = __byte_perm(pair_residual_sum_bits(v2, h2), pair_residual_sum_bits(v3, h3),
+                                   0x0040);
+    return __byte_perm(a, b, 0x5410);
+}
+
 // hi + r * 2^(f - 142): the decoded value.
 __device__ __forceinline__ float pair_decode(float hi, int r) {
     const int f = pair_exp_field(hi);
