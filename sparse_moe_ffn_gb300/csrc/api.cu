@@ -469,6 +469,7 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
     g.act_ready_count = 0;
     g.virt_base = sh ? sh->E_routed : INT_MAX;
     g.virt_chunk = I;
+    g.a_from_x = 0;
     g.num_padded = b.num_padded;
     g.num_rows_host = cap;
     g.q_limit = P;
@@ -490,9 +491,13 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
         g.grid = g.max_tiles < sms ? g.max_tiles : sms;
     }
     if ((st = record_stage(MOE_STAGE_GATHER, stream)) != MOE_OK) return st;
+    // the CTA-pair gate/up loads the shared expert's rows (x in token order)
+    // from x itself; its blocks are not gathered
+    const bool shared_from_x = pairs && sh != nullptr;
     if (!sparse) {  // the sparse GEMM gathers its x rows itself
+        const int skip_slot = shared_from_x ? k - (E - sh->E_routed) : INT_MAX;
         MOE_CUDA(launch_gather_rows(x, H, k, b.sorted_pair, b.num_padded, P, cap, x_sorted,
-                                    pairs ? 1 : 0, sms, stream),
+                                    pairs ? 1 : 0, skip_slot, sms, stream),
                  "gather kernel launch");
         g_launches += 1;
     }
@@ -531,9 +536,15 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
             g.act_ready = ready;
             g.act_ready_count = 8 * ((I + bn - 1) / bn);
         }
+        CUtensorMap tm_xv;
+        if (shared_from_x) {
+            if ((st = make_map(&tm_xv, x, H, N, H, kBlockK, kBlockM, "x")) != MOE_OK) return st;
+            g.a_from_x = 1;
+        }
         MOE_CUDA(launch_pair_gemm(kGateUp, tm_xsorted, tm_wg_tile, tm_wu_tile, g, stream, psg,
-                                  psu),
+                                  psu, shared_from_x ? &tm_xv : nullptr),
                  "gate/up kernel launch");
+        g.a_from_x = 0;
     } else {
         if ((st = shared_gate_up_maps(bn_gu)) != MOE_OK) return st;
         MOE_CUDA(launch_gemm(kGateUp, bn_gu, tm_xrows, tm_xsorted, tm_wg, tm_wu, g, stream, psg,

@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(kGatherThreads)
     gather_rows_kernel(const uint16_t *__restrict__ x, int H, int k,
                        const int32_t *__restrict__ sorted_pair,
                        const int32_t *__restrict__ num_padded, int64_t P, int64_t cap,
-                       uint16_t *__restrict__ x_sorted, int all_blocks) {
+                       uint16_t *__restrict__ x_sorted, int all_blocks, int skip_slot) {
     griddep_launch_dependents();
     griddep_wait();
     constexpr int kWarps = kGatherThreads / 32;
@@ -366,6 +366,12 @@ __global__ void __launch_bounds__(kGatherThreads)
         if (!all_blocks) {
             const int32_t probe = __ldcg(sorted_pair + base + kSparseRows);
             if (probe < 0 || probe >= P) continue;  // sparse block: its rows are gathered by TMA
+        }
+        if (skip_slot < k) {
+            // a block of the shared expert's chunks (slots >= skip_slot): its
+            // rows are x itself, in token order, loaded from x by the GEMM
+            const int32_t first = __ldcg(sorted_pair + base);
+            if (first >= 0 && first < P && first % k >= skip_slot) continue;
         }
         const int32_t q_lane =
             lane < kRowsPerWarp ? __ldcg(sorted_pair + base + warp + kWarps * lane) : -1;
@@ -403,14 +409,15 @@ __global__ void __launch_bounds__(kGatherThreads)
 
 cudaError_t launch_gather_rows(const uint16_t *x, int H, int k, const int32_t *sorted_pair,
                                const int32_t *num_padded, int64_t P, int64_t cap,
-                               uint16_t *x_sorted, int all_blocks, int num_sms, cudaStream_t s) {
+                               uint16_t *x_sorted, int all_blocks, int skip_slot, int num_sms,
+                               cudaStream_t s) {
     int64_t blocks = cap / kBlockM;  // one CTA per row block, at most 4 per SM
     const int64_t limit = static_cast<int64_t>(num_sms) * 4;
     if (blocks > limit) blocks = limit;
     if (blocks < 1) blocks = 1;
     return launch_pdl(gather_rows_kernel, dim3(static_cast<unsigned>(blocks)),
                       dim3(kGatherThreads), 0, s, 1,
-                      x, H, k, sorted_pair, num_padded, P, cap, x_sorted, all_blocks);
+                      x, H, k, sorted_pair, num_padded, P, cap, x_sorted, all_blocks, skip_slot);
 }
 
 template <int MODE, int BN>

@@ -158,6 +158,8 @@ struct GemmArgs {
     // down_proj.  Rows or columns past I_s read as zero (TMA fill).
     int virt_base;      // INT_MAX without a shared expert
     int virt_chunk;
+    // CTA-pair gate/up: the shared expert's blocks load x directly (tm_xv)
+    int a_from_x;
 };
 
 // Tile widths: gate/up 96 or 128 columns (of each of gate and up), down 256.
@@ -178,9 +180,12 @@ cudaError_t launch_gemm(GemmMode mode, int bn, const CUtensorMap &tm_a,
                         const CUtensorMap *tm_s0 = nullptr, const CUtensorMap *tm_s1 = nullptr);
 // x rows copied into expert order (x_sorted [cap, H]): the real rows of dense
 // blocks, or of every block when all_blocks is set
+// Blocks whose pairs sit in slots >= skip_slot (the shared expert's chunks,
+// whose rows are x in token order) are skipped; skip_slot >= k skips none.
 cudaError_t launch_gather_rows(const uint16_t *x, int H, int k, const int32_t *sorted_pair,
                                const int32_t *num_padded, int64_t P, int64_t cap,
-                               uint16_t *x_sorted, int all_blocks, int num_sms, cudaStream_t s);
+                               uint16_t *x_sorted, int all_blocks, int skip_slot, int num_sms,
+                               cudaStream_t s);
 
 // CTA-pair grouped GEMM (cta_group::2, M = 256 over two row blocks of one
 // group): tm_a: 128-row boxes over A rows that are contiguous per block
@@ -200,10 +205,15 @@ cudaError_t launch_sparse_gemm(GemmMode mode, int bn, const CUtensorMap &tm_a,
                                const GemmArgs &a, cudaStream_t s,
                                const CUtensorMap *tm_s0 = nullptr,
                                const CUtensorMap *tm_s1 = nullptr);
+// tm_xv (nullable, gate/up): 128-row boxes over x; the row blocks of the
+// shared expert's chunks (groups >= a.virt_base) then load their A rows
+// from x directly, block j of a chunk being tokens [128 j, 128 j + 128)
+// (the grouping keeps pairs in token order), instead of from tm_a
 cudaError_t launch_pair_gemm(GemmMode mode, const CUtensorMap &tm_a, const CUtensorMap &tm_b0,
                              const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s,
                              const CUtensorMap *tm_s0 = nullptr,
-                             const CUtensorMap *tm_s1 = nullptr);
+                             const CUtensorMap *tm_s1 = nullptr,
+                             const CUtensorMap *tm_xv = nullptr);
 
 // ----------------------------------------------------------------- combine
 

@@ -212,7 +212,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                      const __grid_constant__ CUtensorMap tm_b0,
                      const __grid_constant__ CUtensorMap tm_b1,
                      const __grid_constant__ CUtensorMap tm_s0,
-                     const __grid_constant__ CUtensorMap tm_s1, const GemmArgs a) {
+                     const __grid_constant__ CUtensorMap tm_s1,
+                     const __grid_constant__ CUtensorMap tm_xv, const GemmArgs a) {
     using C = PairCfg<MODE>;
     constexpr int BN = C::BN;
     constexpr int kStages = C::STAGES;
@@ -350,6 +351,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 const CUtensorMap *tm_b = (MODE == kGateUp && rank == 1)
                                               ? (wc.shared ? &tm_s1 : &tm_b1)
                                               : (wc.shared ? &tm_s0 : &tm_b0);
+                // a shared-expert chunk's block j holds tokens 128 j .. (x
+                // itself, rows past N read as zero)
+                const bool a_from_x = MODE == kGateUp && a.a_from_x && wc.shared;
+                const CUtensorMap *tm_arows = a_from_x ? &tm_xv : &tm_a;
+                const int arow_src = a_from_x ? (pt.block - sm->block0[pt.group]) * kBlockM : arow;
                 for (int kc = 0; kc < nk; ++kc, ++g) {
                     const int s = g % kStages;
                     const uint32_t use = g / kStages;
@@ -363,7 +369,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     const uint32_t bar = cluster_addr(&sm->full[s], 0);
                     if (leader) mbar_arrive_expect_tx(&sm->full[s], tx);
                     if (pt.rows) {
-                        tma_load_pair(st, &tm_a, bar, kc * kBlockK, arow);
+                        tma_load_pair(st, tm_arows, bar, kc * kBlockK, arow_src);
                         if (kSplit)
                             tma_load_pair(st + kATileBytes, &tm_a, bar, kc * kBlockK,
                                           arow + static_cast<int>(a.lo_rows));
@@ -494,7 +500,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 template <int MODE>
 cudaError_t launch_pair_one(const CUtensorMap &tm_a, const CUtensorMap &tm_b0,
                             const CUtensorMap &tm_b1, const CUtensorMap &tm_s0,
-                            const CUtensorMap &tm_s1, const GemmArgs &a, cudaStream_t s) {
+                            const CUtensorMap &tm_s1, const CUtensorMap &tm_xv, const GemmArgs &a,
+                            cudaStream_t s) {
     using C = PairCfg<MODE>;
     const size_t smem = 1024 + static_cast<size_t>(C::STAGES) * C::STAGE_BYTES + sizeof(PairSmem);
     auto kern = pair_gemm_kernel<MODE>;
@@ -502,7 +509,7 @@ cudaError_t launch_pair_one(const CUtensorMap &tm_a, const CUtensorMap &tm_b0,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
     return launch_pdl(kern, dim3(a.grid), dim3(kPairThreads), smem, s, 2, tm_a, tm_b0, tm_b1,
-                      tm_s0, tm_s1, a);
+                      tm_s0, tm_s1, tm_xv, a);
 }
 
 }  // namespace
@@ -513,15 +520,19 @@ static_assert(PairCfg<kDown>::BN == PairCfg<kDownSplit>::BN, "one down tile widt
 
 cudaError_t launch_pair_gemm(GemmMode mode, const CUtensorMap &tm_a, const CUtensorMap &tm_b0,
                              const CUtensorMap &tm_b1, const GemmArgs &a, cudaStream_t s,
-                             const CUtensorMap *tm_s0, const CUtensorMap *tm_s1) {
+                             const CUtensorMap *tm_s0, const CUtensorMap *tm_s1,
+                             const CUtensorMap *tm_xv) {
     if (a.grid < 2 || a.grid % 2) return cudaErrorInvalidValue;
     if (a.pad_offsets && (a.num_groups < 1 || a.num_groups > kMaxGroups))
         return cudaErrorInvalidValue;
     const CUtensorMap &s0 = tm_s0 ? *tm_s0 : tm_b0;
     const CUtensorMap &s1 = tm_s1 ? *tm_s1 : tm_b1;
-    if (mode == kGateUp) return launch_pair_one<kGateUp>(tm_a, tm_b0, tm_b1, s0, s1, a, s);
-    if (mode == kDownSplit) return launch_pair_one<kDownSplit>(tm_a, tm_b0, tm_b1, s0, s1, a, s);
-    return launch_pair_one<kDown>(tm_a, tm_b0, tm_b1, s0, s1, a, s);
+    if (a.a_from_x && (!tm_xv || mode != kGateUp)) return cudaErrorInvalidValue;
+    const CUtensorMap &xv = tm_xv ? *tm_xv : tm_a;
+    if (mode == kGateUp) return launch_pair_one<kGateUp>(tm_a, tm_b0, tm_b1, s0, s1, xv, a, s);
+    if (mode == kDownSplit)
+        return launch_pair_one<kDownSplit>(tm_a, tm_b0, tm_b1, s0, s1, xv, a, s);
+    return launch_pair_one<kDown>(tm_a, tm_b0, tm_b1, s0, s1, xv, a, s);
 }
 
 }  // namespace moe
