@@ -527,14 +527,7 @@ def run_ours(args, world, rank, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights, random init)",
-        "config": {"workload": WORKLOADS[args.config], "N": shape.N, "H": shape.H,
-                   "E": shape.E, "k": shape.k, "I": shape.I, "I_s": shape.I_s,
-                   "norm_topk_prob": shape.norm_topk_prob, "seed": args.seed,
-                   "l2": "inputs larger than L2 (expert weights "
-                         f"{3 * shape.E * shape.H * shape.I * 2 / 1e9:.2f} GB > 129 MB)"
-                         if shape.E * shape.H * shape.I * 6 > 129e6 else
-                         "inputs smaller than L2 (not flushed: latency-bound case)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": workload_config(args, shape, world),
         "tflops": round(tflops, 2),
         "entry": ("moe_forward (bf16 weights, as the layer is defined)" if args.down_weights ==
                   "bf16" else "moe_forward_prepared (fp16 down weights made once at load)"),
@@ -555,6 +548,18 @@ def run_ours(args, world, rank, local):
 
 
 # ------------------------------------------------------------ reference arm
+
+def workload_config(args, shape, world) -> dict:
+    """The `config` object of both arms' JSON lines (the same workload)."""
+    return {"workload": WORKLOADS[args.config], "N": shape.N, "H": shape.H, "E": shape.E,
+            "k": shape.k, "I": shape.I, "I_s": shape.I_s,
+            "norm_topk_prob": shape.norm_topk_prob, "seed": args.seed,
+            "l2": "inputs larger than L2 (expert weights "
+                  f"{3 * shape.E * shape.H * shape.I * 2 / 1e9:.2f} GB > 129 MB)"
+                  if shape.E * shape.H * shape.I * 6 > 129e6 else
+                  "inputs smaller than L2 (not flushed: latency-bound case)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
 
 def run_reference(args, world, rank):
     """The fp64 CPU oracle as the reference arm (host cores, bounded samples)."""
@@ -587,8 +592,7 @@ def run_reference(args, world, rank):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOADS[args.config], "N": shape.N, "H": shape.H, "E": shape.E,
-                   "k": shape.k, "I": shape.I, "I_s": shape.I_s, "seed": args.seed},
+        "config": workload_config(args, shape, world),
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": threads,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
