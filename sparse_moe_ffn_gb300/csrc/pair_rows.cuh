@@ -51,8 +51,10 @@ __device__ __forceinline__ int pair_residual(float v, float hi) {
 // with byte permutes.  Equal, byte for byte, to pair_residual.
 __device__ __forceinline__ uint32_t pair_residual_sum_bits(float v, float hi) {
     constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
-    const int f = pair_exp_field(hi);
-    const float up = __uint_as_float(static_cast<uint32_t>(269 - f) << 23);  // 2^(142 - f)
+    // 2^(142 - f) built from hi's exponent bits in place: (269 << 23) minus
+    // max(exponent bits, 16 << 23), the same value as pair_residual's
+    const uint32_t e_bits = max(__float_as_uint(hi) & 0x7F800000u, 16u << 23);
+    const float up = __uint_as_float((269u << 23) - e_bits);
     float t = fmaf(v - hi, up, kMagic);
     t = fminf(fmaxf(t, kMagic - 127.f), kMagic + 127.f);
     return __float_as_uint(t);
