@@ -22,6 +22,15 @@ __device__ __forceinline__ float silu_times(float g, float u) {
     return g / (1.f + __expf(-g)) * u;
 }
 
+// max(a, |b|, |c|) that returns NaN when any operand is NaN (fmaxf drops a
+// NaN operand), so that the stored-range checks below see NaN outputs too
+__device__ __forceinline__ float max_abs_nan(float a, float b, float c) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(fabsf(b)), "f"(fabsf(c)));
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(r), "f"(a));
+    return r;
+}
+
 // Where the weight rows of N tile nt of group (expert) `expert` are: the
 // routed weights (row expert * w_rows + n0 + extra, K from 0), or, for a
 // virtual expert of the folded shared expert, the shared weights (gate/up:
@@ -153,7 +162,7 @@ __device__ __forceinline__ void store_tile(const GemmArgs &a, uint32_t taddr, co
                         const int j = h * 16 + 2 * i;
                         const float a0 = silu_times(gv[j], uv[j]);
                         const float a1 = silu_times(gv[j + 1], uv[j + 1]);
-                        vmax = fmaxf(vmax, fmaxf(fabsf(a0), fabsf(a1)));
+                        vmax = max_abs_nan(vmax, a0, a1);
                         if (split) {
                             pk[i] = pack_bf16x2(a0, a1);
                             const float2 hi = unpack_bf16x2(pk[i]);
@@ -193,7 +202,7 @@ __device__ __forceinline__ void store_tile(const GemmArgs &a, uint32_t taddr, co
                     for (int i = 0; i < 8; ++i) {
                         tv[2 * i] = w * yv[h * 16 + 2 * i];
                         tv[2 * i + 1] = w * yv[h * 16 + 2 * i + 1];
-                        vmax = fmaxf(vmax, fmaxf(fabsf(tv[2 * i]), fabsf(tv[2 * i + 1])));
+                        vmax = max_abs_nan(vmax, tv[2 * i], tv[2 * i + 1]);
                         pk[i] = pack_bf16x2(tv[2 * i], tv[2 * i + 1]);
                         const float2 hi = unpack_bf16x2(pk[i]);
                         hv[2 * i] = hi.x;

@@ -212,6 +212,54 @@ def test_forward_edge_shapes(case, form):
     assert_close(out, ref, f"{name} ({form})")
 
 
+def _forward_status(shape, dev, x):
+    ws = binding.alloc_workspace(x.shape[0], shape.H, shape.E, shape.I, shape.k, shape.I_s)
+    out = binding.moe_forward(x, dev["router"], dev["w_gate"], dev["w_up"], dev["w_down"],
+                              shape.k, shape.norm_topk_prob, shared_of(shape, dev),
+                              workspace=ws)
+    return out, binding.moe_read_device_status(ws)
+
+
+@pytest.mark.parametrize("form", FORMS)
+@pytest.mark.parametrize("bad", ["nan", "inf"])
+@pytest.mark.parametrize("N", [40, 300, 600])  # 32-row passes, one-CTA tiles, CTA pairs
+def test_non_finite_token_is_reported(form, bad, N):
+    """A token whose x row holds a NaN or an infinity gives non-finite
+    activations and pair outputs: the layer records MOE_ERR_DEVICE_CHECK,
+    its ids stay in [0, E), and every other token's output still matches the
+    oracle (tokens do not mix)."""
+    shape, dev, bits = prepare(MoEShape("non-finite", N=N, H=128, E=8, k=2, I=64, I_s=64,
+                                        norm_topk_prob=False), seed=9, form=form)
+    x = dev["x"].clone()
+    x[7, 5] = float("nan") if bad == "nan" else float("inf")
+    out, status = _forward_status(shape, dev, x)
+    assert status == 5  # MOE_ERR_DEVICE_CHECK
+    keep = np.array([n for n in range(N) if n != 7])
+    ref = oracle.moe_forward(bits, shape.k, shape.norm_topk_prob)
+    assert_close(out[torch.from_numpy(keep).cuda()], ref[keep], f"{bad} token, other rows")
+
+
+@pytest.mark.parametrize("form", FORMS)
+def test_activation_range(form):
+    """One token scaled by 2^12 gives activations of ~1e5-1e6: past fp16's
+    65504, so the prepared path (fp16 activation) records
+    MOE_ERR_DEVICE_CHECK, while the bf16 hi/lo activation holds them and the
+    layer stays within the tolerance of the oracle."""
+    shape, dev, bits = prepare(MoEShape("range", N=40, H=128, E=8, k=2, I=64), seed=10,
+                               form=form)
+    x = dev["x"].clone()
+    x[3] *= 4096.0
+    out, status = _forward_status(shape, dev, x)
+    assert status == (5 if form == "f16" else 0)
+    if form == "bf16":
+        big = dict(bits)
+        big["x"] = oracle.bf16_bits(x)
+        ref = oracle.moe_forward(big, shape.k, shape.norm_topk_prob)
+        assert_close(out[3:4], ref[3:4], "scaled token")
+        rest = np.array([n for n in range(shape.N) if n != 3])
+        assert_close(out[torch.from_numpy(rest).cuda()], ref[rest], "other tokens")
+
+
 @pytest.mark.parametrize("form", FORMS)
 def test_forward_mixed_sparse_and_dense_row_blocks(form):
     """Skewed routing at a small size with top-10: each token takes the 8 hot
