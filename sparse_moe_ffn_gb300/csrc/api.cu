@@ -176,11 +176,18 @@ moe_status_t check_route_args(const void *x, const void *router, const void *sha
     return MOE_OK;
 }
 
+struct AlignBuffers {
+    int32_t *sorted_pair, *block_expert, *counts, *offsets, *pad_offsets, *num_padded, *scratch;
+    int32_t *status;
+    int32_t *ready = nullptr;
+};
+
 moe_status_t enqueue_route(const moe_bf16_t *x, const moe_bf16_t *router,
                            const moe_bf16_t *shared_gate, int64_t N, int H, int E, int k,
                            int norm, float *topk_w, int32_t *topk_ids, moe_bf16_t *topk_w_bf16,
                            float *gamma, int32_t *status, bool reset_status,
-                           cudaStream_t stream, int virt_slots = 0) {
+                           cudaStream_t stream, int virt_slots = 0,
+                           const AlignBuffers *fused = nullptr, int ready_n = 0) {
     const bool shared = shared_gate != nullptr;
     RouterArgs ra;
     ra.N = N;
@@ -200,6 +207,17 @@ moe_status_t enqueue_route(const moe_bf16_t *x, const moe_bf16_t *router,
     ra.out_ld = k + virt_slots;
     ra.virt_slots = virt_slots;
     ra.virt_base = E;
+    // the grouping done by the routing cluster itself (one cluster routes
+    // every token): moe_align's outputs for 128-row blocks
+    ra.fuse_align = fused ? 1 : 0;
+    ra.sorted_pair = fused ? fused->sorted_pair : nullptr;
+    ra.block_expert = fused ? fused->block_expert : nullptr;
+    ra.counts = fused ? fused->counts : nullptr;
+    ra.offsets = fused ? fused->offsets : nullptr;
+    ra.pad_offsets = fused ? fused->pad_offsets : nullptr;
+    ra.num_padded = fused ? fused->num_padded : nullptr;
+    ra.ready = fused ? fused->ready : nullptr;
+    ra.ready_n = fused ? ready_n : 0;
     CUtensorMap tm_x, tm_r, tm_g;
     moe_status_t st;
     if ((st = make_map(&tm_x, x, H, N, H, kBlockK, kBlockM, "x")) != MOE_OK) return st;
@@ -215,11 +233,6 @@ moe_status_t enqueue_route(const moe_bf16_t *x, const moe_bf16_t *router,
     return MOE_OK;
 }
 
-struct AlignBuffers {
-    int32_t *sorted_pair, *block_expert, *counts, *offsets, *pad_offsets, *num_padded, *scratch;
-    int32_t *status;
-    int32_t *ready = nullptr;
-};
 
 moe_status_t enqueue_align(const int32_t *ids, int64_t N, int k, int E, int block_m,
                            const AlignBuffers &b, cudaStream_t stream) {
@@ -372,12 +385,39 @@ struct SharedWeights {
     int E_routed;
 };
 
+// moe_align's outputs inside a forward workspace
+AlignBuffers align_buffers_of(const moe_forward_layout_t &L, uint8_t *ws) {
+    AlignBuffers b;
+    b.sorted_pair = reinterpret_cast<int32_t *>(ws + L.sorted_pair);
+    b.block_expert = reinterpret_cast<int32_t *>(ws + L.block_expert);
+    b.counts = reinterpret_cast<int32_t *>(ws + L.counts);
+    b.offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
+    b.pad_offsets = reinterpret_cast<int32_t *>(ws + L.pad_offsets);
+    b.num_padded = reinterpret_cast<int32_t *>(ws + L.num_padded);
+    b.scratch = reinterpret_cast<int32_t *>(ws + L.align_scratch);
+    b.status = reinterpret_cast<int32_t *>(ws + L.status);
+    b.ready = reinterpret_cast<int32_t *>(ws + L.ready);
+    return b;
+}
+
+// hand-off counters in a forward workspace (max(E, capacity / 128))
+int ready_count_of(const moe_forward_layout_t &L) {
+    const int blocks = static_cast<int>(L.capacity / kBlockM);
+    return L.groups > blocks ? L.groups : blocks;
+}
+
+// Routing can group the pairs itself when one cluster routes every token
+// and no shared-expert slots follow the routed ones.
+bool route_groups(int64_t N, int E, bool shared) {
+    return N <= kBlockM && E <= 256 && !shared;
+}
+
 moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const float *weights,
                              int64_t N, int k, int H, int E, int I, const moe_bf16_t *w_gate,
                              const moe_bf16_t *w_up, const void *w_down, bool down_f16,
                              const moe_forward_layout_t &L, uint8_t *ws, uint16_t *ypair,
                              int8_t *ypair_res, cudaStream_t stream,
-                             const SharedWeights *sh = nullptr) {
+                             const SharedWeights *sh = nullptr, bool grouped = false) {
     moe_status_t st;
     auto at = [&](size_t off) { return ws + off; };
     int32_t *status = reinterpret_cast<int32_t *>(at(L.status));
@@ -398,18 +438,12 @@ moe_status_t enqueue_experts(const moe_bf16_t *x, const int32_t *ids, const floa
 
     // K2: grouping
     if ((st = record_stage(MOE_STAGE_ALIGN, stream)) != MOE_OK) return st;
-    AlignBuffers b;
-    b.sorted_pair = reinterpret_cast<int32_t *>(at(L.sorted_pair));
-    b.block_expert = reinterpret_cast<int32_t *>(at(L.block_expert));
-    b.counts = reinterpret_cast<int32_t *>(at(L.counts));
-    b.offsets = reinterpret_cast<int32_t *>(at(L.offsets));
-    b.pad_offsets = reinterpret_cast<int32_t *>(at(L.pad_offsets));
-    b.num_padded = reinterpret_cast<int32_t *>(at(L.num_padded));
-    b.scratch = reinterpret_cast<int32_t *>(at(L.align_scratch));
-    b.status = status;
+    AlignBuffers b = align_buffers_of(L, ws);
     b.ready = handoff || pair_handoff ? ready : nullptr;
-    st = enqueue_align(ids, N, k, E, kBlockM, b, stream);
-    if (st != MOE_OK) return st;
+    if (!grouped) {  // (else the routing kernel has grouped the pairs)
+        st = enqueue_align(ids, N, k, E, kBlockM, b, stream);
+        if (st != MOE_OK) return st;
+    }
 
     // K3: gathered gate/up GEMM + silu * up
     CUtensorMap tm_xrows, tm_xsorted, tm_wg, tm_wu, tm_act, tm_act_box, tm_wd;
@@ -752,8 +786,11 @@ static moe_status_t forward_impl(const moe_bf16_t *x, const moe_bf16_t *router,
     // with the shared expert every token also gets its chunks' slots
     const int C = L.slots - k;
     if ((st = record_stage(MOE_STAGE_ROUTE, stream)) != MOE_OK) return st;
+    const bool grouped = route_groups(N, E, shared);
+    const AlignBuffers ab = align_buffers_of(L, ws);
     st = enqueue_route(x, router, shared ? shared_gate : nullptr, N, H, E, k, norm_topk_prob,
-                       topk_w, topk_ids, nullptr, gamma, status, true, stream, C);
+                       topk_w, topk_ids, nullptr, gamma, status, true, stream, C,
+                       grouped ? &ab : nullptr, ready_count_of(L));
     if (st != MOE_OK) return st;
 
     // K2-K4: grouping, gate/up, down over the routed experts and the shared
@@ -761,7 +798,7 @@ static moe_status_t forward_impl(const moe_bf16_t *x, const moe_bf16_t *router,
     SharedWeights sw{shared_gate_proj, shared_up_proj, shared_down_proj, I_s, E};
     if ((st = enqueue_experts(x, topk_ids, topk_w, N, L.slots, H, L.groups, I, w_gate, w_up,
                               w_down, down_f16, L, ws, ypair, ypair_res, stream,
-                              shared ? &sw : nullptr)) != MOE_OK)
+                              shared ? &sw : nullptr, grouped)) != MOE_OK)
         return st;
     // (the shared stage has no launches of its own any more)
     if ((st = record_stage(MOE_STAGE_SHARED, stream)) != MOE_OK) return st;

@@ -64,10 +64,24 @@ struct RouterArgs {
     // each with weight sigmoid(x . g) (the shared gate)
     int virt_slots;
     int virt_base;
+    // grouping fused into the routing kernel (set only when one cluster
+    // routes every token: N <= 128, and no virtual slots): the cluster
+    // writes what moe_align writes for block size 128 -- sorted_pair,
+    // block_expert, counts, offsets, pad_offsets, num_padded -- and zeroes
+    // the GEMMs' hand-off counters ready[0 .. ready_n)
+    int fuse_align;
+    int32_t *sorted_pair;
+    int32_t *block_expert;
+    int32_t *counts;
+    int32_t *offsets;
+    int32_t *pad_offsets;
+    int32_t *num_padded;
+    int32_t *ready;
+    int ready_n;
 };
 
 int router_split(int H);  // 1, 2, 4 or 8: depends on H only (batch invariance)
-size_t router_smem_bytes(int e_pad, int k);
+size_t router_smem_bytes(int e_pad, int k, int table_bytes);
 cudaError_t launch_router(const CUtensorMap &tm_x, const CUtensorMap &tm_router,
                           const CUtensorMap &tm_gate, const RouterArgs &a, cudaStream_t s);
 

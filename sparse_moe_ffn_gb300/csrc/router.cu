@@ -83,6 +83,180 @@ __device__ __forceinline__ void key_max(float &v, int &e, float ov, int oe) {
     }
 }
 
+// Exclusive scan over the CTA (128 threads) of two consecutive values per
+// thread (v0, v1 at positions 2t, 2t+1); returns the prefix of v0 and sets
+// *total.  `sums` holds 4 ints of shared memory.
+__device__ __forceinline__ int32_t cta_scan2(int32_t v0, int32_t v1, int32_t *sums,
+                                             int32_t *total) {
+    const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+    const int32_t own = v0 + v1;
+    int32_t incl = own;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int32_t t = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += t;
+    }
+    if (lane == 31) sums[warp] = incl;
+    __syncthreads();
+    int32_t before = 0, all = 0;
+#pragma unroll
+    for (int w = 0; w < kRouterThreads / 32; ++w) {
+        if (w < warp) before += sums[w];
+        all += sums[w];
+    }
+    __syncthreads();
+    *total = all;
+    return before + incl - own;
+}
+
+// The grouping of moe_align (block size 128) done by the routing cluster
+// when it routes every token (N <= 128), instead of by another launch.
+// Definition (M03 "serving way": bincount, prefix offsets, stable order):
+// counts[e] = pairs with expert e; offsets = exclusive prefix of counts;
+// each expert with pairs owns one 128-row block (counts <= N <= 128), in
+// expert order (pad_offsets); its pairs fill the block in ascending
+// p = n*k + j, then the sentinel P; block_expert[b] = the block's expert.
+// CTA r of the cluster routed tokens [r*rows, (r+1)*rows), i.e. pairs
+// [r*rows*k, (r+1)*rows*k) in p order, so a pair's row in its block is
+// (its expert's pairs in the CTAs before r) + (those before it in CTA r):
+//   1. each CTA counts its pairs per expert and pushes the counts into the
+//      table `tbl` [split][E] of every CTA of the cluster (DSMEM stores);
+//   2. after a cluster barrier each CTA scans the table itself (no second
+//      exchange), and places its own pairs with warp match + per-warp counts;
+//   3. CTA r writes the per-expert outputs of experts e = r mod split, CTA 0
+//      the totals, and every CTA zeroes its share of the hand-off counters.
+// An id outside [0, E) (only a broken routing could write one) is skipped
+// and reported as MOE_ERR_DEVICE_CHECK.
+// local_ids: this CTA's ids in shared memory (pair i of the CTA at [i]) when
+// one 16-row pass routed all its rows, else null (read back from topk_ids).
+__device__ __noinline__ void cluster_group(const RouterArgs &a, uint32_t crank, int rows_per_cta,
+                                           int32_t *tbl, int32_t *scratch,
+                                           const int32_t *local_ids) {
+    const int E = a.E;
+    const int k = a.k;
+    const int tid = threadIdx.x;
+    const int lane = tid % 32, warp = tid / 32;
+    constexpr int kWarps = kRouterThreads / 32;
+    const int64_t P = a.N * k;
+    const int64_t row0 = static_cast<int64_t>(crank) * rows_per_cta;
+    const int64_t live = a.N > row0 ? min(static_cast<int64_t>(rows_per_cta), a.N - row0) : 0;
+    const int64_t p0 = row0 * k;
+    const int np = static_cast<int>(live) * k;
+    // scratch (this CTA's partial rows are no longer read): per-expert
+    // counts, totals, running positions, per-warp counts of a chunk
+    int32_t *hist = scratch;                 // [256]
+    int32_t *tot = hist + 256;               // [256]
+    int32_t *run = tot + 256;                // [256]
+    int32_t *padv = run + 256;               // [256]
+    int32_t *warp_cnt = padv + 256;          // [kWarps][256]
+    int32_t *sums = warp_cnt + kWarps * 256; // [4]
+    for (int e = tid; e < 256; e += kRouterThreads) hist[e] = 0;
+    for (int i = tid; i < kWarps * 256; i += kRouterThreads) warp_cnt[i] = 0;
+    __syncthreads();
+    bool bad = false;
+    auto id_of = [&](int i) -> int32_t {
+        return local_ids ? local_ids[i] : __ldcg(a.topk_ids + p0 + i);
+    };
+    for (int i = tid; i < np; i += kRouterThreads) {
+        const int32_t e = id_of(i);
+        if (e < 0 || e >= E) bad = true;
+        else atomicAdd(&hist[e], 1);
+    }
+    if (bad) record_status(a.status, MOE_ERR_DEVICE_CHECK);
+    __syncthreads();
+    // 1. this CTA's counts into slot [crank] of every CTA's table
+    for (int e = tid; e < E; e += kRouterThreads) {
+        const int32_t v = hist[e];
+        for (int r = 0; r < a.split; ++r)
+            asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(
+                             dsmem_addr(&tbl[crank * E + e], static_cast<uint32_t>(r))),
+                         "r"(v)
+                         : "memory");
+    }
+    cluster_sync();  // every table is complete
+    // 2. totals, prefix offsets, padded offsets and this CTA's start rows
+    int32_t c2[2], before2[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int e = 2 * tid + u;
+        int32_t c = 0, b = 0;
+        if (e < E)
+            for (int r = 0; r < a.split; ++r) {
+                const int32_t v = tbl[r * E + e];
+                c += v;
+                if (r < static_cast<int>(crank)) b += v;
+            }
+        c2[u] = c;
+        before2[u] = b;
+    }
+    int32_t total_pairs, total_pad;
+    const int32_t off0 = cta_scan2(c2[0], c2[1], sums, &total_pairs);
+    const int32_t seg0 = c2[0] > 0 ? kBlockM : 0, seg1 = c2[1] > 0 ? kBlockM : 0;
+    const int32_t pad0 = cta_scan2(seg0, seg1, sums, &total_pad);
+    const int32_t offs[2] = {off0, off0 + c2[0]};
+    const int32_t pads[2] = {pad0, pad0 + seg0};
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int e = 2 * tid + u;
+        if (e >= E) continue;
+        tot[e] = c2[u];
+        padv[e] = pads[u];
+        run[e] = pads[u] + before2[u];
+        // 3. experts of this CTA's share: counts, offsets, blocks, sentinels
+        if (e % a.split == static_cast<int>(crank)) {
+            a.counts[e] = c2[u];
+            a.offsets[e] = offs[u];
+            a.pad_offsets[e] = pads[u];
+            if (c2[u] > 0) a.block_expert[pads[u] / kBlockM] = e;
+        }
+    }
+    if (crank == 0 && tid == 0) {
+        a.offsets[E] = total_pairs;
+        a.pad_offsets[E] = total_pad;
+        *a.num_padded = total_pad;
+    }
+    // the hand-off counters start from zero every call (the previous call's
+    // GEMMs are complete: routing waited for them)
+    for (int i = static_cast<int>(crank) * kRouterThreads + tid; i < a.ready_n;
+         i += a.split * kRouterThreads)
+        a.ready[i] = 0;
+    __syncthreads();
+    // sentinels: the rows of each block past its pairs (experts of this
+    // CTA's share, 128 rows each, spread over the threads)
+    const int share = (E - static_cast<int>(crank) + a.split - 1) / a.split;
+    for (int idx = tid; idx < share * kBlockM; idx += kRouterThreads) {
+        const int e = static_cast<int>(crank) + a.split * (idx / kBlockM);
+        const int r = idx % kBlockM;
+        if (tot[e] > 0 && r >= tot[e]) a.sorted_pair[padv[e] + r] = static_cast<int32_t>(P);
+    }
+    // stable placement of this CTA's pairs, 128 at a time in p order
+    const uint32_t lanes_below = (1u << lane) - 1u;
+    for (int c0 = 0; c0 < np; c0 += kRouterThreads) {
+        const int i = c0 + tid;
+        const int32_t e = i < np ? id_of(i) : -1;
+        const bool valid = e >= 0 && e < E;
+        const uint32_t peers = __match_any_sync(0xffffffffu, valid ? e : E + lane);
+        const int rank = __popc(peers & lanes_below);
+        if (valid && rank == 0) warp_cnt[warp * 256 + e] = __popc(peers);
+        __syncthreads();
+        if (valid) {
+            int32_t before = 0;
+            for (int w = 0; w < warp; ++w) before += warp_cnt[w * 256 + e];
+            a.sorted_pair[run[e] + before + rank] = static_cast<int32_t>(p0 + i);
+        }
+        __syncthreads();
+        for (int x = tid; x < E; x += kRouterThreads) {
+            int32_t t = 0;
+            for (int w = 0; w < kWarps; ++w) {
+                t += warp_cnt[w * 256 + x];
+                warp_cnt[w * 256 + x] = 0;
+            }
+            run[x] += t;
+        }
+        __syncthreads();
+    }
+}
+
 // PL: logits per lane (e_pad / 8 rounded up to 4, 16 or 32), a compile-time
 // bound so that the per-round scans cover only the columns that exist.
 template <int PL>
@@ -97,8 +271,14 @@ __global__ void __launch_bounds__(kRouterThreads, 1)
     const int stage_bytes = kATileBytes + b_tile_bytes;
     const int ring_bytes = kRouterStages * stage_bytes;
     const int part_bytes = kBlockM * (a.e_pad + 4) * 4 + kRowsPerPass * a.k * 8;
+    // fused grouping: every CTA's expert histogram, pushed into every CTA
+    // of the cluster; kept clear of the partial rows, which peers may still
+    // be reading while a fast CTA pushes its histogram
+    const int tbl_off = (part_bytes + 15) / 16 * 16;
+    const int tbl_bytes = a.fuse_align ? a.split * a.E * 4 : 0;
+    const int body_bytes = tbl_off + tbl_bytes > ring_bytes ? tbl_off + tbl_bytes : ring_bytes;
     RouterSmem *sm = reinterpret_cast<RouterSmem *>(
-        tiles + (ring_bytes > part_bytes ? ring_bytes : part_bytes));
+        tiles + (body_bytes > part_bytes ? body_bytes : part_bytes));
     float *partial = reinterpret_cast<float *>(tiles);  // reuses the ring once it is idle
     const int ld = a.e_pad + 4;                          // row stride of the partial tile
 
@@ -362,6 +542,10 @@ __global__ void __launch_bounds__(kRouterThreads, 1)
         __syncwarp();
     }
     __syncthreads();
+    if (a.fuse_align)
+        cluster_group(a, crank, rows_per_cta, reinterpret_cast<int32_t *>(tiles + tbl_off),
+                      reinterpret_cast<int32_t *>(tiles),
+                      rows_per_cta == kRowsPerPass ? slot_e : nullptr);
     if (warp == 0) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, tmem_cols);
@@ -380,17 +564,22 @@ int router_per_lane(int e_pad) {
     return pl <= 4 ? 4 : (pl <= 16 ? 16 : 32);
 }
 
-size_t router_smem_bytes(int e_pad, int k) {
+size_t router_smem_bytes(int e_pad, int k, int table_bytes) {
     const size_t ring = static_cast<size_t>(kRouterStages) * (kATileBytes + e_pad * 128);
-    // the partial tile, then the slot results of one 16-row pass
+    // the partial tile, then the slot results of one 16-row pass; the fused
+    // grouping's table after them (the kernel's layout)
     const size_t part = static_cast<size_t>(kBlockM) * (e_pad + 4) * sizeof(float) +
                         static_cast<size_t>(kRowsPerPass) * k * 8;
-    return 1024 + (ring > part ? ring : part) + sizeof(RouterSmem);
+    const size_t table_end = (part + 15) / 16 * 16 + static_cast<size_t>(table_bytes);
+    const size_t body = table_end > ring ? table_end : ring;
+    return 1024 + (body > part ? body : part) + sizeof(RouterSmem);
 }
 
 cudaError_t launch_router(const CUtensorMap &tm_x, const CUtensorMap &tm_router,
                           const CUtensorMap &tm_gate, const RouterArgs &a, cudaStream_t s) {
-    const size_t smem = router_smem_bytes(a.e_pad, a.k);
+    if (a.fuse_align && (a.N > kBlockM || a.E > 256 || a.virt_slots != 0 || a.out_ld != a.k))
+        return cudaErrorInvalidValue;
+    const size_t smem = router_smem_bytes(a.e_pad, a.k, a.fuse_align ? a.split * a.E * 4 : 0);
     const int pl = router_per_lane(a.e_pad);
     auto kern = pl == 4 ? router_kernel<4> : (pl == 16 ? router_kernel<16> : router_kernel<32>);
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
