@@ -257,7 +257,7 @@ def time_oracle(shape, bits, target_s: float):
 
 def time_prefill(args, device, peaks):
     """The prefill workload (N=8192) timed on this GPU through both forms of
-    the down weights: layer ms per call (median of three rounds that
+    the down weights: layer ms per call (median of five rounds that
     alternate the two forms, so that a clock or thermal drift hits both
     alike), and the grouped GEMMs (gate/up and down, from the start of
     gate/up to the end of down, with no event between them so that their
@@ -271,7 +271,7 @@ def time_prefill(args, device, peaks):
     forms = {"bf16_down": d_bf16, "f16_down_prepared": binding.prepare_weights(d_bf16)}
     ws = binding.alloc_workspace(shape.N, shape.H, shape.E, shape.I, shape.k, shape.I_s, device)
     out = torch.empty((shape.N, shape.H), dtype=torch.bfloat16, device=device)
-    steps, warm, rounds = args.prefill_steps, 5, 3
+    steps, warm, rounds = args.prefill_steps, 5, 5
     _, sflops, layer_flops, _ = algorithmic_work(shape, shape.E)
     gemm_flops = sflops["gate_up"] + sflops["down"]
     rec = {"workload": WORKLOADS["prefill"], "steps": steps, "warmup": warm, "rounds": rounds}
