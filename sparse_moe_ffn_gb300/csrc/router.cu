@@ -74,15 +74,6 @@ __device__ __forceinline__ void st_dsmem_f4(uint32_t addr, float4 v) {
                  : "memory");
 }
 
-// the larger of two (logit, expert) keys: larger logit, then lower expert;
-// an expert of -1 means "none"
-__device__ __forceinline__ void key_max(float &v, int &e, float ov, int oe) {
-    if (oe >= 0 && (e < 0 || ov > v || (ov == v && oe < e))) {
-        v = ov;
-        e = oe;
-    }
-}
-
 // Exclusive scan over the CTA (128 threads) of two consecutive values per
 // thread (v0, v1 at positions 2t, 2t+1); returns the prefix of v0 and sets
 // *total.  `sums` holds 4 ints of shared memory.
@@ -487,38 +478,44 @@ __global__ void __launch_bounds__(kRouterThreads, 1)
         const float inv_den = 1.f / den;
         // k arg-max rounds; exp is monotone, so this is the top-k of the
         // probabilities.  A lane's candidates are reduced as a tournament
-        // (log2(PL) levels of key_max instead of a PL-long dependent chain);
-        // a selected expert's index becomes -1, so it never wins again.
-        int le[PL];
+        // (log2(PL) levels of max instead of a PL-long dependent chain),
+        // then across the row's 8 lanes; a selected key becomes 0, so it
+        // never wins again.  Each candidate is one 64-bit key: the logit mapped to an unsigned
+        // integer of the same order (its sign bit flipped, or all bits for
+        // a negative value; -0 first made +0, which compares equal), then
+        // 255 - e, so that an equal logit ranks the lower expert first; 0
+        // means "none" (past E, or already taken).  The keys order the
+        // candidates exactly as (larger logit, then lower expert).
+        uint64_t key[PL];
 #pragma unroll
         for (int j = 0; j < PL; ++j) {
             const int e = 32 * (j / 4) + 4 * sub + j % 4;
-            le[j] = e < a.E ? e : -1;
+            const uint32_t u = __float_as_uint(lg[j] + 0.f);
+            const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+            key[j] = e < a.E ? (static_cast<uint64_t>(ord) << 32) | static_cast<uint32_t>(255 - e)
+                             : 0ull;
         }
         float wsum = 0.f;
         for (int r = 0; r < a.k; ++r) {
-            float tv[PL];
-            int te[PL];
+            uint64_t t[PL];
 #pragma unroll
-            for (int j = 0; j < PL; ++j) {
-                tv[j] = lg[j];
-                te[j] = le[j];
-            }
+            for (int j = 0; j < PL; ++j) t[j] = key[j];
 #pragma unroll
             for (int w = PL / 2; w > 0; w >>= 1)
 #pragma unroll
-                for (int j = 0; j < w; ++j) key_max(tv[j], te[j], tv[j + w], te[j + w]);
-            float bv = tv[0];
-            int be = te[0];
+                for (int j = 0; j < w; ++j) t[j] = t[j] > t[j + w] ? t[j] : t[j + w];
+            uint64_t best = t[0];
 #pragma unroll
             for (int d = kLanesPerRow / 2; d > 0; d >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, d, kLanesPerRow);
-                const int oe = __shfl_xor_sync(0xffffffffu, be, d, kLanesPerRow);
-                key_max(bv, be, ov, oe);
+                const uint64_t o = __shfl_xor_sync(0xffffffffu, best, d, kLanesPerRow);
+                best = o > best ? o : best;
             }
 #pragma unroll
             for (int j = 0; j < PL; ++j)
-                if (le[j] == be) le[j] = -1;
+                if (key[j] == best) key[j] = 0ull;
+            const int be = 255 - static_cast<int>(best & 0xFFu);
+            const uint32_t ord = static_cast<uint32_t>(best >> 32);
+            const float bv = __uint_as_float((ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord);
             const float p = __expf(bv - mx) * inv_den;
             wsum += p;
             if (sub == 0) {
