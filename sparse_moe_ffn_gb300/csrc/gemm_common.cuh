@@ -18,8 +18,13 @@ constexpr float kF16Max = 65504.f;
 constexpr float kF32Max = 3.402823466e38f;
 constexpr int kSparseRows = 32;             // blocks with at most this many real rows gather
 
+// silu(g) * u = g / (1 + e^-g) * u, with the fast division (a reciprocal
+// and a multiply, ~2 ulp; the activation is rounded to 11 or 16 bits after
+// it).  The exponent is capped at 80 so that the divisor stays below 2^126,
+// the fast division's range; for g < -80 silu is below 1e-33 in magnitude
+// either way.
 __device__ __forceinline__ float silu_times(float g, float u) {
-    return g / (1.f + __expf(-g)) * u;
+    return __fdividef(g, 1.f + __expf(fminf(-g, 80.f))) * u;
 }
 
 // max(a, |b|, |c|) that returns NaN when any operand is NaN (fmaxf drops a
