@@ -543,11 +543,13 @@ moe_status_t moe_selftest_wait_timeout(void *workspace, size_t workspace_bytes,
 /* Stages of moe_forward, in launch order. */
 enum {
     MOE_STAGE_ROUTE = 0,
-    MOE_STAGE_ALIGN = 1,
+    MOE_STAGE_ALIGN = 1,   /* empty when routing groups the pairs itself (N <= 128,
+                              no shared expert) */
     MOE_STAGE_GATHER = 2,  /* x rows of full row blocks copied into expert order */
     MOE_STAGE_GATE_UP = 3,
     MOE_STAGE_DOWN = 4,
-    MOE_STAGE_SHARED = 5, /* shared expert gate/up + down (empty without one) */
+    MOE_STAGE_SHARED = 5, /* always empty: the shared expert runs inside the
+                             gate/up and down stages (kept for the layout) */
     MOE_STAGE_COMBINE = 6,
     MOE_NUM_STAGES = 7
 };
