@@ -12,11 +12,13 @@
 // outputs:
 //   count:   CTA c histograms pairs [c*chunk, (c+1)*chunk) in shared memory
 //   scan:    one CTA: per-expert exclusive scan over chunks (in place),
-//            counts, offsets, padded offsets, then block owners and the
-//            sentinel in every padded slot (coalesced, all threads)
+//            counts, offsets, padded offsets
 //   scatter: CTA c ranks each of its pairs among the same-expert pairs before
 //            it (warp match + per-warp tallies), so pair p lands at
-//            pad_off[e] + #{p' < p : expert(p') = e}: a stable order.
+//            pad_off[e] + #{p' < p : expert(p') = e}: a stable order; CTA c
+//            also writes the sentinel into the padding rows of experts
+//            e = c (mod CTAs) and their blocks' owner, spreading that work
+//            over all CTAs instead of the scan's single one.
 // Small P (decode): the same steps inside one 1024-thread CTA, one launch.
 #include "kernels.cuh"
 #include "ptx.cuh"
@@ -123,9 +125,8 @@ __device__ void fill_padded(const int32_t *pad_off_smem, int E, int block_m, int
 
 __global__ void __launch_bounds__(kScanThreads)
     align_scan_kernel(int32_t *__restrict__ chunk_counts, int nchunks, int E, int block_m,
-                      int64_t P, int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+                      int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
                       int32_t *__restrict__ pad_offsets, int32_t *__restrict__ num_padded,
-                      int32_t *__restrict__ block_expert, int32_t *__restrict__ sorted_pair,
                       int32_t *__restrict__ ready) {
     griddep_launch_dependents();
     griddep_wait();
@@ -155,13 +156,11 @@ __global__ void __launch_bounds__(kScanThreads)
     const int32_t seg = (cnt + block_m - 1) / block_m * block_m;
     const int32_t off = block_exclusive_scan(cnt, warp_sums, &total);
     const int32_t pad = block_exclusive_scan(seg, warp_sums, &total);
-    __shared__ int32_t pad_smem[1024 + 1];
     __shared__ int32_t npad;
     if (e < E) {
         counts[e] = cnt;
         offsets[e] = off;
         pad_offsets[e] = pad;
-        pad_smem[e] = pad;
         if (e == E - 1) {
             offsets[E] = off + cnt;
             pad_offsets[E] = pad + seg;
@@ -170,17 +169,34 @@ __global__ void __launch_bounds__(kScanThreads)
         }
     }
     __syncthreads();
-    // the scatter kernel overwrites the real slots after this kernel ends
-    fill_padded(pad_smem, E, block_m, npad, P, sorted_pair, block_expert, ready);
+    // the GEMMs' hand-off counters start from zero every call (see
+    // fill_padded); the sentinels and block owners are written by the
+    // scatter kernel's CTAs, expert by expert, next to the real pairs
+    if (ready) {
+        const int32_t n = E > npad / block_m ? E : npad / block_m;
+        for (int32_t i = threadIdx.x; i < n; i += blockDim.x) ready[i] = 0;
+    }
 }
 
 __global__ void __launch_bounds__(kAlignThreads)
     align_scatter_kernel(const int32_t *__restrict__ ids, int64_t P, int E, int chunk,
                          const int32_t *__restrict__ chunk_base,
                          const int32_t *__restrict__ pad_offsets,
-                         int32_t *__restrict__ sorted_pair) {
+                         const int32_t *__restrict__ counts, int block_m,
+                         int32_t *__restrict__ sorted_pair, int32_t *__restrict__ block_expert) {
     griddep_launch_dependents();
     griddep_wait();
+    // experts e = blockIdx.x (mod gridDim.x): the sentinel P in the rows of
+    // their blocks past their pairs, and the blocks' owner (positions the
+    // real pairs below never take, so no ordering is needed)
+    for (int e = blockIdx.x; e < E; e += gridDim.x) {
+        const int32_t p0 = __ldcg(pad_offsets + e), p1 = __ldcg(pad_offsets + e + 1);
+        const int32_t c = __ldcg(counts + e);
+        for (int32_t i = p0 + c + threadIdx.x; i < p1; i += blockDim.x)
+            sorted_pair[i] = static_cast<int32_t>(P);
+        for (int32_t b = p0 / block_m + threadIdx.x; b < p1 / block_m; b += blockDim.x)
+            block_expert[b] = e;
+    }
     extern __shared__ int32_t sh[];
     int32_t *running = sh;                 // [E] next destination of each expert
     int32_t *warp_cnt = sh + E;            // [kAlignWarps][E]
@@ -341,8 +357,8 @@ cudaError_t launch_align(const AlignArgs &a, cudaStream_t s, int *launches) {
                                  a.status);
     if (err != cudaSuccess) return err;
     err = launch_pdl(align_scan_kernel, dim3(1), dim3(kScanThreads), 0, s, 1, a.chunk_counts,
-                     a.nchunks, a.E, a.block_m, a.P, a.counts, a.offsets, a.pad_offsets,
-                     a.num_padded, a.block_expert, a.sorted_pair, a.ready);
+                     a.nchunks, a.E, a.block_m, a.counts, a.offsets, a.pad_offsets,
+                     a.num_padded, a.ready);
     if (err != cudaSuccess) return err;
     const size_t scatter_smem = sizeof(int32_t) * (a.E + kAlignWarps * a.E);
     if (scatter_smem > 48 * 1024) {
@@ -355,7 +371,9 @@ cudaError_t launch_align(const AlignArgs &a, cudaStream_t s, int *launches) {
     return launch_pdl(align_scatter_kernel, dim3(a.nchunks), dim3(kAlignThreads), scatter_smem,
                       s, 1, a.ids, a.P, a.E, a.chunk,
                       static_cast<const int32_t *>(a.chunk_counts),
-                      static_cast<const int32_t *>(a.pad_offsets), a.sorted_pair);
+                      static_cast<const int32_t *>(a.pad_offsets),
+                      static_cast<const int32_t *>(a.counts), a.block_m, a.sorted_pair,
+                      a.block_expert);
 }
 
 }  // namespace moe
