@@ -27,12 +27,9 @@ namespace {
 
 constexpr int kCombineThreads = 256;
 
-// acc[0..7] += the 8 pair-row values of row offset o (hi 16 bytes, residual
-// 8 bytes), read through L2
-__device__ __forceinline__ void add_pair8(float (&acc)[8], const uint16_t *hi_plane,
-                                          const int8_t *res_plane, int64_t o) {
-    const uint4 h = __ldcg(reinterpret_cast<const uint4 *>(hi_plane + o));
-    const uint2 r = __ldcg(reinterpret_cast<const uint2 *>(res_plane + o));
+// acc[0..7] += the 8 pair-row values held in h (16 bytes of the bf16
+// plane) and r (8 bytes of the residual plane)
+__device__ __forceinline__ void add_loaded8(float (&acc)[8], uint4 h, uint2 r) {
     const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
     const uint32_t rw[2] = {r.x, r.y};
 #pragma unroll
@@ -46,6 +43,28 @@ __device__ __forceinline__ void add_pair8(float (&acc)[8], const uint16_t *hi_pl
     }
 }
 
+// acc[0..7] += the 8 pair-row values of row offset o, read through L2
+__device__ __forceinline__ void add_pair8(float (&acc)[8], const uint16_t *hi_plane,
+                                          const int8_t *res_plane, int64_t o) {
+    const uint4 h = __ldcg(reinterpret_cast<const uint4 *>(hi_plane + o));
+    const uint2 r = __ldcg(reinterpret_cast<const uint2 *>(res_plane + o));
+    add_loaded8(acc, h, r);
+}
+
+// The row of slot j of token n (-1: a pair that was never sent).
+__device__ __forceinline__ int64_t slot_row(const int32_t *row_index, int64_t rows, int64_t n,
+                                            int k, int j) {
+    const int64_t p = n * k + j;
+    const int64_t row = row_index ? static_cast<int64_t>(__ldcg(row_index + p)) : p;
+    return row < 0 || row >= rows ? -1 : row;
+}
+
+// HOIST (k <= kHoistSlots, small batches): every slot's loads are issued
+// before the first add, one round trip to memory instead of k; the adds
+// run in the same slot order either way, so both forms give the same bits.
+constexpr int kHoistSlots = 8;
+
+template <bool HOIST>
 __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(const uint16_t *__restrict__ ypair_hi, const int8_t *__restrict__ ypair_res,
                    const int32_t *__restrict__ row_index, int64_t rows,
@@ -61,11 +80,28 @@ __global__ void __launch_bounds__(kCombineThreads)
         const int64_t n = idx / groups;
         const int col = static_cast<int>(idx % groups) * 8;
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int j = 0; j < k; ++j) {
-            const int64_t p = n * k + j;
-            const int64_t row = row_index ? static_cast<int64_t>(__ldcg(row_index + p)) : p;
-            if (row < 0 || row >= rows) continue;  // a pair that was never sent
-            add_pair8(acc, ypair_hi, ypair_res, row * H + col);
+        if (HOIST) {
+            uint4 h[kHoistSlots];
+            uint2 r[kHoistSlots];
+            bool live[kHoistSlots];
+#pragma unroll
+            for (int j = 0; j < kHoistSlots; ++j) {
+                const int64_t row = j < k ? slot_row(row_index, rows, n, k, j) : -1;
+                live[j] = row >= 0;
+                if (live[j]) {
+                    h[j] = __ldcg(reinterpret_cast<const uint4 *>(ypair_hi + row * H + col));
+                    r[j] = __ldcg(reinterpret_cast<const uint2 *>(ypair_res + row * H + col));
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kHoistSlots; ++j)
+                if (live[j]) add_loaded8(acc, h[j], r[j]);
+        } else {
+            for (int j = 0; j < k; ++j) {
+                const int64_t row = slot_row(row_index, rows, n, k, j);
+                if (row < 0) continue;  // a pair that was never sent
+                add_pair8(acc, ypair_hi, ypair_res, row * H + col);
+            }
         }
         for (int c = 0; c < shared_slots; ++c)
             add_pair8(acc, yshared_hi, yshared_res, (n * shared_slots + c) * H + col);
@@ -88,8 +124,13 @@ cudaError_t launch_combine(const uint16_t *ypair_hi, const int8_t *ypair_res,
     int64_t blocks = (total + kCombineThreads - 1) / kCombineThreads;
     const int64_t cap = static_cast<int64_t>(num_sms) * 16;
     if (blocks > cap) blocks = cap;
-    return launch_pdl(combine_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kCombineThreads),
-                      0, s, 1, ypair_hi, ypair_res, row_index, rows, yshared_hi, yshared_res,
+    // few tokens: latency-bound, so every slot's loads go out at once; many
+    // tokens: bandwidth-bound, where the hoisted form's registers would cost
+    // occupancy
+    const bool hoist = k <= kHoistSlots && N <= 256;
+    return launch_pdl(hoist ? combine_kernel<true> : combine_kernel<false>,
+                      dim3(static_cast<unsigned>(blocks)), dim3(kCombineThreads), 0, s, 1,
+                      ypair_hi, ypair_res, row_index, rows, yshared_hi, yshared_res,
                       yshared_hi ? shared_slots : 0, N, H, k, out);
 }
 
