@@ -56,6 +56,9 @@ SHARED_CASES = {
     "talker": None,  # I_s = 2048 in three chunks of I = 768 (the last one 512 rows)
     "three-chunks": MoEShape("three-chunks", N=200, H=128, E=8, k=2, I=64, I_s=160,
                              norm_topk_prob=False),
+    # decode-sized: the 32-row-pass GEMMs with expert-indexed tiles
+    "sparse-chunks": MoEShape("sparse-chunks", N=24, H=128, E=16, k=2, I=64, I_s=136,
+                              norm_topk_prob=True),
 }
 
 

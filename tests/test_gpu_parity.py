@@ -96,6 +96,32 @@ def test_align_random(N, k, E, block_m):
     _align_vs_oracle(ids, E, block_m)
 
 
+@pytest.mark.parametrize("N,H,E,k", [(1, 2048, 128, 8), (7, 64, 6, 2), (64, 2048, 128, 8),
+                                     (100, 200, 32, 12), (127, 128, 256, 4), (128, 512, 16, 16)])
+def test_routing_kernel_grouping(N, H, E, k):
+    """One cluster routes every token (N <= 128, no shared expert): the
+    routing kernel groups the pairs itself, and what it writes into the
+    forward workspace equals moe_align's result on the same ids, bit for bit,
+    and the oracle's grouping (H spans cluster sizes 1, 2, 4 and 8; k = 12
+    and 16 place more pairs per CTA than one pass)."""
+    shape, dev, _ = prepare(MoEShape("grouped-in-router", N=N, H=H, E=E, k=k, I=64), seed=11)
+    out, ws = run_forward(shape, dev)
+    v = binding.workspace_views(ws, N, H, E, 64, k)
+    ids = v["topk_ids"].clone()
+    ref = oracle.align(ids.cpu().numpy(), E, 128)
+    npad = int(v["num_padded"].item())
+    assert npad == ref["num_padded"]
+    assert np.array_equal(v["counts"].cpu().numpy(), ref["counts"])
+    assert np.array_equal(v["offsets"].cpu().numpy(), ref["offsets"])
+    assert np.array_equal(v["sorted_pair"][:npad].cpu().numpy(), ref["sorted_pair"])
+    assert np.array_equal(v["block_expert"][:npad // 128].cpu().numpy(), ref["block_expert"])
+    r = binding.moe_align(ids, E, 128)
+    torch.cuda.synchronize()
+    assert np.array_equal(r["sorted_pair"][:npad].cpu().numpy(),
+                          v["sorted_pair"][:npad].cpu().numpy())
+    assert np.array_equal(r["counts"].cpu().numpy(), v["counts"].cpu().numpy())
+
+
 def test_align_flags_bad_ids():
     """An id outside [0, E) is skipped and recorded in the status word."""
     ids = torch.tensor([[0, 1], [7, 2]], dtype=torch.int32, device="cuda")
