@@ -238,6 +238,37 @@ def test_forward_edge_shapes(case, form):
     assert_close(out, ref, f"{name} ({form})")
 
 
+def _random_shapes(n, seed):
+    """Seeded random layer shapes spanning the three GEMM tilings, ragged H
+    and I (multiples of 8), k up to E, and the shared expert in one or
+    several chunks."""
+    rng = np.random.default_rng(seed)
+    shapes = []
+    for i in range(n):
+        E = int(rng.choice([1, 3, 8, 24, 64, 160]))
+        k = int(rng.integers(1, min(E, 10) + 1))
+        N = int(rng.choice([1, 5, 37, 128, 129, 300, 900]))
+        H = int(rng.integers(1, 40)) * 8
+        I = int(rng.integers(1, 33)) * 8
+        I_s = int(rng.integers(1, 50)) * 8 if (E + 8 <= 240 and rng.random() < 0.4) else 0
+        shapes.append(MoEShape(f"fuzz{i}", N=N, H=H, E=E, k=k, I=I, I_s=I_s,
+                               norm_topk_prob=bool(rng.random() < 0.5)))
+    return shapes
+
+
+FUZZ = _random_shapes(16, 2024)
+
+
+@pytest.mark.parametrize("form", FORMS)
+@pytest.mark.parametrize("shape", FUZZ, ids=[f"{s.name}-N{s.N}-H{s.H}-E{s.E}-k{s.k}-I{s.I}-Is{s.I_s}"
+                                              for s in FUZZ])
+def test_forward_random_shapes(shape, form):
+    """Random shapes (seeded) against the oracle, every output element."""
+    shape, dev, bits = prepare(shape, seed=12, form=form)
+    out, _ = run_forward(shape, dev)
+    assert_close(out, oracle.moe_forward(bits, shape.k, shape.norm_topk_prob), shape.name)
+
+
 def _forward_status(shape, dev, x):
     ws = binding.alloc_workspace(x.shape[0], shape.H, shape.E, shape.I, shape.k, shape.I_s)
     out = binding.moe_forward(x, dev["router"], dev["w_gate"], dev["w_up"], dev["w_down"],
