@@ -90,6 +90,23 @@ def test_shared_expert_rows_equal_forward_slots(case, form):
     assert torch.equal(binding.moe_combine(routed, shape.N, k, yshared=y), out)
 
 
+def _fuzz_shapes():
+    from test_gpu_parity import FUZZ
+    return FUZZ
+
+
+@pytest.mark.parametrize("shape", _fuzz_shapes(), ids=lambda s: s.name)
+def test_ep_forward_one_rank_random_shapes(shape):
+    """ep_forward with one rank (device dispatch plan, moe_experts,
+    moe_shared_expert, indexed combine) equals moe_forward bit for bit on the
+    seeded random shapes."""
+    shape, dev, _ = prepare(shape, seed=12)
+    out, _ = run_forward(shape, dev)
+    got = ep_forward(dev["x"], dev["router"], dev["w_gate"], dev["w_up"], dev["w_down"],
+                     shape.E, shape.k, shape.norm_topk_prob, shared=shared_of(shape, dev))
+    assert torch.equal(got, out)
+
+
 @pytest.mark.parametrize("name,world", [("decode", 2), ("prefill", 2), ("prefill", 3),
                                         ("tiny", 4)])
 def test_expert_slices_in_one_process_equal_forward(name, world):
