@@ -369,14 +369,9 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
         // gate/up: Wg and Wu tiles are adjacent, one bf16 MMA of N = 2 BN;
         // kDown: fp16 act x fp16 Wd; kDownSplit: bf16 act hi x bf16 Wd, then
         // act lo x the same Wd, per K step
-        // the hi/lo down GEMM's passes hold 16 rows: an M = 64 MMA covers them
-        // at half the tensor work of M = 128.  Its rows 0-15 land in TMEM lanes
-        // 0-15, read by the lane-0-31 epilogue warp; rows 16-31 do not land in
-        // lanes 16-31 (the 32-row passes keep M = 128: a run with M = 64 there
-        // failed the parity tests)
         constexpr uint32_t idesc = MODE == kGateUp ? idesc_bf16_f32(kBlockM, 2 * BN)
                                    : MODE == kDown ? idesc_f16_f32(kBlockM, BN)
-                                                   : idesc_bf16_f32(64, BN);
+                                                   : idesc_bf16_f32(kBlockM, BN);
         int g = 0, it = 0;
         bool failed = false;
         for (int tile = blockIdx.x, j = 0; tile < total_tiles && !failed; tile += gridDim.x, ++j) {
