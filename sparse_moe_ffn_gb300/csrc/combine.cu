@@ -51,6 +51,46 @@ __device__ __forceinline__ void add_pair8(float (&acc)[8], const uint16_t *hi_pl
     add_loaded8(acc, h, r);
 }
 
+// 32 bytes of the bf16 plane in one load, through L2
+__device__ __forceinline__ void ld_cg_v8(const void *p, uint32_t (&v)[8]) {
+    asm volatile("ld.global.cg.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
+                   "=r"(v[6]), "=r"(v[7])
+                 : "l"(p));
+}
+
+// acc[0..15] += the 16 pair-row values of row offset o (32 bytes of the bf16
+// plane, 16 of the residual plane)
+__device__ __forceinline__ void add_pair16(float (&acc)[16], const uint16_t *hi_plane,
+                                           const int8_t *res_plane, int64_t o) {
+    uint32_t h[8];
+    ld_cg_v8(hi_plane + o, h);
+    const uint4 r = __ldcg(reinterpret_cast<const uint4 *>(res_plane + o));
+    float a0[8], a1[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        a0[i] = acc[i];
+        a1[i] = acc[8 + i];
+    }
+    add_loaded8(a0, make_uint4(h[0], h[1], h[2], h[3]), make_uint2(r.x, r.y));
+    add_loaded8(a1, make_uint4(h[4], h[5], h[6], h[7]), make_uint2(r.z, r.w));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        acc[i] = a0[i];
+        acc[8 + i] = a1[i];
+    }
+}
+
+// 16 output columns per thread (H % 16 == 0, large batches): one 32-byte and
+// one 16-byte load per slot; the same adds in the same order as the 8-column
+// form, so the same bits.
+__global__ void __launch_bounds__(kCombineThreads)
+    combine16_kernel(const uint16_t *__restrict__ ypair_hi, const int8_t *__restrict__ ypair_res,
+                     const int32_t *__restrict__ row_index, int64_t rows,
+                     const uint16_t *__restrict__ yshared_hi,
+                     const int8_t *__restrict__ yshared_res, int shared_slots, int64_t N,
+                     int H, int k, uint16_t *__restrict__ out);
+
 // The row of slot j of token n (-1: a pair that was never sent).
 __device__ __forceinline__ int64_t slot_row(const int32_t *row_index, int64_t rows, int64_t n,
                                             int k, int j) {
@@ -114,6 +154,37 @@ __global__ void __launch_bounds__(kCombineThreads)
     }
 }
 
+__global__ void __launch_bounds__(kCombineThreads)
+    combine16_kernel(const uint16_t *__restrict__ ypair_hi, const int8_t *__restrict__ ypair_res,
+                     const int32_t *__restrict__ row_index, int64_t rows,
+                     const uint16_t *__restrict__ yshared_hi,
+                     const int8_t *__restrict__ yshared_res, int shared_slots, int64_t N,
+                     int H, int k, uint16_t *__restrict__ out) {
+    griddep_launch_dependents();
+    griddep_wait();
+    const int groups = H / 16;
+    const int64_t total = N * groups;
+    for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t n = idx / groups;
+        const int col = static_cast<int>(idx % groups) * 16;
+        float acc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+        for (int j = 0; j < k; ++j) {
+            const int64_t row = slot_row(row_index, rows, n, k, j);
+            if (row < 0) continue;  // a pair that was never sent
+            add_pair16(acc, ypair_hi, ypair_res, row * H + col);
+        }
+        for (int c = 0; c < shared_slots; ++c)
+            add_pair16(acc, yshared_hi, yshared_res, (n * shared_slots + c) * H + col);
+        uint32_t pk[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+        st_global_v8(out + n * H + col, pk);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_combine(const uint16_t *ypair_hi, const int8_t *ypair_res,
@@ -128,6 +199,18 @@ cudaError_t launch_combine(const uint16_t *ypair_hi, const int8_t *ypair_res,
     // tokens: bandwidth-bound, where the hoisted form's registers would cost
     // occupancy
     const bool hoist = k <= kHoistSlots && N <= 256;
+    // 32-byte accesses need 32-byte aligned planes and output
+    const bool al32 = ((reinterpret_cast<uintptr_t>(ypair_hi) |
+                        reinterpret_cast<uintptr_t>(yshared_hi) |
+                        reinterpret_cast<uintptr_t>(out)) & 31u) == 0;
+    if (!hoist && H % 16 == 0 && al32) {
+        const int64_t total16 = N * (H / 16);
+        int64_t b16 = (total16 + kCombineThreads - 1) / kCombineThreads;
+        if (b16 > cap) b16 = cap;
+        return launch_pdl(combine16_kernel, dim3(static_cast<unsigned>(b16)),
+                          dim3(kCombineThreads), 0, s, 1, ypair_hi, ypair_res, row_index, rows,
+                          yshared_hi, yshared_res, yshared_hi ? shared_slots : 0, N, H, k, out);
+    }
     return launch_pdl(hoist ? combine_kernel<true> : combine_kernel<false>,
                       dim3(static_cast<unsigned>(blocks)), dim3(kCombineThreads), 0, s, 1,
                       ypair_hi, ypair_res, row_index, rows, yshared_hi, yshared_res,
