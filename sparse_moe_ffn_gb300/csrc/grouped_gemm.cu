@@ -341,7 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // broadcast load of the block's row kSparseRows decides whether it is dense,
 // so sparse blocks (all of them at decode) cost one load.  Warp w copies rows
 // w, w + 8, ..., w + 120: their 16 row-map entries come with one load, then
-// two rows at a time are copied with all their 16-byte loads in flight before
+// two rows at a time are copied with all their 16-byte loads (8 per lane and
+// row) in flight before
 // the stores, until the first padding row (real rows come first).  The stores
 // are streaming (evict-first): the GEMM reads each x_sorted row once, while
 // each x row is read k times here and should stay in L2.
@@ -356,7 +357,7 @@ __global__ void __launch_bounds__(kGatherThreads)
     griddep_wait();
     constexpr int kWarps = kGatherThreads / 32;
     constexpr int kRowsPerWarp = kBlockM / kWarps;  // 16
-    constexpr int kUnroll = 4;                      // 16-byte pieces per lane per row in flight
+    constexpr int kUnroll = 8;                      // 16-byte pieces per lane per row in flight
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     const int64_t nblocks = min(static_cast<int64_t>(__ldcg(num_padded)), cap) / kBlockM;
