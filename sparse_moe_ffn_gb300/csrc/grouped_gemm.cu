@@ -342,8 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // so sparse blocks (all of them at decode) cost one load.  Warp w copies rows
 // w, w + 8, ..., w + 120: their 16 row-map entries come with one load, then
 // two rows at a time are copied with all their 16-byte loads (8 per lane and
-// row) in flight before
-// the stores, until the first padding row (real rows come first).  The stores
+// row) in flight before the stores, until the first padding row (real rows
+// come first).  The stores
 // are streaming (evict-first): the GEMM reads each x_sorted row once, while
 // each x row is read k times here and should stay in L2.
 constexpr int kGatherThreads = 256;
