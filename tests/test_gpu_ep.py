@@ -40,6 +40,40 @@ def test_experts_rows_and_combine_match_forward(name, form):
     assert torch.equal(binding.moe_combine(ypair, shape.N, shape.k), out)
 
 
+def _shifted(t, elems):
+    """A contiguous copy of t whose data starts `elems` elements into a fresh
+    buffer (16 bytes in: 16-byte but not 32-byte aligned)."""
+    buf = torch.empty(t.numel() + elems, dtype=t.dtype, device=t.device)
+    view = buf[elems:].view(t.shape)
+    view.copy_(t)
+    return view
+
+
+@pytest.mark.parametrize("name", ["prefill", "talker"])
+def test_combine_forms_agree_on_unaligned_planes(name):
+    """Large batches sum 16 columns per thread with 32-byte loads when the
+    planes and the output are 32-byte aligned, else 8 columns per thread;
+    both add the same values in the same order, so the bits agree."""
+    shape, dev, _ = prepared(name)
+    out, ws = run_forward(shape, dev)
+    v = binding.workspace_views(ws, shape.N, shape.H, shape.E, shape.I, shape.k, shape.I_s)
+    slots, k, H = v["slots"], shape.k, shape.H
+    hi = v["ypair"][0].view(shape.N, slots, H)
+    res = v["ypair"][1].view(shape.N, slots, H)
+    routed = (hi[:, :k].reshape(-1, H).contiguous(), res[:, :k].reshape(-1, H).contiguous())
+    shared = None
+    if slots > k:
+        shared = (hi[:, k:].reshape(-1, H).contiguous(), res[:, k:].reshape(-1, H).contiguous())
+    aligned = binding.moe_combine(routed, shape.N, k, yshared=shared)
+    assert torch.equal(aligned, out)
+    moved = (_shifted(routed[0], 8), _shifted(routed[1], 16))
+    moved_shared = None if shared is None else (_shifted(shared[0], 8), _shifted(shared[1], 16))
+    target = _shifted(torch.zeros_like(out), 8)
+    assert target.data_ptr() % 32 == 16 and moved[0].data_ptr() % 32 == 16
+    got = binding.moe_combine(moved, shape.N, k, yshared=moved_shared, out=target)
+    assert torch.equal(got, out)
+
+
 @pytest.mark.parametrize("form", FORMS)
 @pytest.mark.parametrize("name", ["decode", "prefill", "talker"])
 def test_ep_forward_one_rank_equals_forward(name, form):
