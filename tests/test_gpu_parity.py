@@ -224,6 +224,9 @@ EDGE = [
     ("shared-3-chunks", 200, 128, 8, 2, 64, 160, False),
     ("pairs-shared-3-chunks", 600, 128, 4, 2, 96, 200, True),
     ("sparse-shared-3-chunks", 24, 128, 16, 2, 64, 136, False),
+    # the limit on experts: routed experts plus shared chunks at exactly
+    # 256 (E + C, C = 2)
+    ("shared-at-expert-limit", 40, 64, 254, 4, 32, 64, False),
 ]
 
 
@@ -236,6 +239,35 @@ def test_forward_edge_shapes(case, form):
     out, _ = run_forward(shape, dev)
     ref = oracle.moe_forward(bits, k, norm)
     assert_close(out, ref, f"{name} ({form})")
+
+
+@pytest.mark.parametrize("form", FORMS)
+def test_forward_every_expert_per_token(form):
+    """The largest top-k: k = E = 256, every token routed to every expert.
+    Random logits over 256 experts leave gaps below the near-tie margin, so
+    column 0 spreads them instead: x[:, 0] = 4 and router[e, 0] = (e - 128)
+    / 64 put expert e's logit near (e - 128) / 16, the rest of the router
+    scaled down to noise (std ~0.01), so the descending order of all 256 is
+    unambiguous.  Ids bit for bit, outputs within the tolerance."""
+    from sparse_moe_ffn_gb300.inputs import MARGIN, _near_tie_rows, make_inputs, to_device
+    shape = MoEShape("k-equals-E-256", N=3, H=64, E=256, k=256, I=32, norm_topk_prob=True)
+    cpu = make_inputs(MoEShape("k-equals-E-256-draw", N=3, H=64, E=256, k=1, I=32), seed=13)
+    x = cpu["x"].float()
+    router = cpu["router"].float() * 0.05
+    x[:, 0] = 4.0
+    router[:, 0] = (torch.arange(256, dtype=torch.float32) - 128.0) / 64.0
+    cpu["x"], cpu["router"] = x.to(torch.bfloat16), router.to(torch.bfloat16)
+    assert _near_tie_rows(cpu["x"], cpu["router"], shape.k, MARGIN).numel() == 0
+    bits = {n: oracle.bf16_bits(t) for n, t in cpu.items()}
+    dev = to_device(cpu, "cuda")
+    if form == "f16":
+        dev = binding.prepare_weights(dev)
+    out, ws = run_forward(shape, dev)
+    _, _, _, ids_ref = oracle.route(bits["x"], bits["router"], shape.k, True)
+    ids = binding.workspace_views(ws, shape.N, shape.H, shape.E, shape.I, shape.k)["topk_ids"]
+    assert np.array_equal(ids.cpu().numpy(), ids_ref)
+    assert np.array_equal(ids_ref[:, 0], np.full(3, 255))  # descending: expert 255 first
+    assert_close(out, oracle.moe_forward(bits, shape.k, True), shape.name)
 
 
 def _random_shapes(n, seed):
