@@ -16,14 +16,22 @@
 //   4 KB with 32 rows; the bf16 hi/lo activation (kDownSplit) with 16 hi
 //   rows followed by the same 16 rows' lo halves, so its passes hold 16 rows
 //   and the weight bytes in flight stay the same.
-// The MMA is still M = 128: its A operand spans 16 KB from the region's
-// start (kDownSplit: from the start of the hi rows, then of the lo rows),
-// so the rows past a pass read whatever follows in the stage; they only
-// feed accumulator rows that the epilogue never stores (and TMEM lanes 0-31
-// belong to the first epilogue warp alone).  A block with more real rows
-// than a pass holds is computed as several passes over K (rare at decode);
-// real rows come first in a block, so a block with n real rows takes
-// ceil(n / rows per pass) passes.
+// Gate/up: the MMA is still M = 128: its A operand spans 16 KB from the
+// region's start, so the rows past a pass read whatever follows in the
+// stage; they only feed accumulator rows that the epilogue never stores
+// (and TMEM lanes 0-31 belong to the first epilogue warp alone).
+// Down: the operands swap roles, so that the MMA's M side is the weights'
+// and its N side the pass's rows: D^T = Wd * act^T as two M = 128 MMAs
+// (weight rows 0-127 and 128-255 of the tile) of N = rows per pass (32, or
+// 16 for kDownSplit, whose lo MMAs read the lo rows), K = 16 each.  An M =
+// 128 MMA over 16 real rows did 8x the tensor work of this form, and with
+// the hi/lo pair kept the tensor pipe ~60% busy in a kernel that should
+// only stream weights.  Each product and each K step's sum reach an output
+// element in the same order either way.  The epilogue then holds one output
+// column per thread (TMEM lane = weight row) for the pass's rows.
+// A block with more real rows than a pass holds is computed as several
+// passes over K (rare at decode); real rows come first in a block, so a
+// block with n real rows takes ceil(n / rows per pass) passes.
 //
 // The producer publishes each tile's pass count through a small ring of
 // shared-memory words (full/empty barriers per slot), so that the MMA issuer
@@ -38,8 +46,9 @@
 //
 // Roles: warp 0 TMA producer (gather4 of the sub-block's real rows, lane 0
 // the weight tile(s)); warp 1 TMEM allocation and MMA issuer; warps 2-5
-// epilogue (warp 4, which owns TMEM lanes 0-31, stores; the others only
-// release the accumulator).  Every wait is bounded.
+// epilogue (gate/up: warp 4, which owns TMEM lanes 0-31, stores and the
+// others only release the accumulator; down: each warp stores the output
+// columns of its 32 TMEM lanes).  Every wait is bounded.
 #include <cuda_bf16.h>
 
 #include "gemm_common.cuh"
@@ -104,6 +113,47 @@ __device__ __forceinline__ int read_passes(SparseSmem *sm, int j, int lane,
         }
     }
     return __shfl_sync(0xffffffffu, n, 0);
+}
+
+// Down epilogue of the swapped MMA, for the thread that owns TMEM lane
+// (weight row) t of its warp's quarter: taddr = that quarter's lanes and the
+// accumulator; h0 = t's output column in the tile's first 128 (the second
+// half's is h0 + 128).  Columns [0, ROWS) of the lane hold the first half's
+// values for the pass's rows 0 .. ROWS-1, [ROWS, 2 ROWS) the second half's.
+// Lane i of the warp holds row i's TileRow (pair q, routing weight w); real
+// rows come first.  Per value the arithmetic of store_tile's down branch: y
+// = w * acc in fp32, stored as a pair row (bf16 hi at out, int8 residual at
+// out_res, row q), so every tiling stores the same bits.
+template <int ROWS>
+__device__ __forceinline__ void store_tile_swapped(const GemmArgs &a, uint32_t taddr,
+                                                   const TileRow &r, int h0, int lane) {
+    static_assert(ROWS == 16 || ROWS == 32, "rows per pass");
+    float v[2 * ROWS];
+    tmem_load32(taddr, *reinterpret_cast<float(*)[32]>(v));
+    if (ROWS == 32) tmem_load32(taddr + 32, *reinterpret_cast<float(*)[32]>(v + 32));
+    tmem_load_wait();
+    const int32_t q_lane = r.valid ? static_cast<int32_t>(r.q) : -1;
+    uint16_t *hi_plane = static_cast<uint16_t *>(a.out);
+    float vmax = 0.f;
+#pragma unroll
+    for (int j = 0; j < ROWS; ++j) {
+        const int32_t q = __shfl_sync(0xffffffffu, q_lane, j);
+        const float w = __shfl_sync(0xffffffffu, r.w, j);
+        if (q < 0) break;  // warp-uniform: the rest of the pass is padding
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int h = h0 + half * kBlockM;
+            const float y = w * v[half * ROWS + j];
+            if (h < a.n_out) {
+                vmax = max_abs_nan(vmax, y, y);
+                const __nv_bfloat16 hb = __float2bfloat16_rn(y);
+                const int64_t o = static_cast<int64_t>(q) * a.out_ld + h;
+                hi_plane[o] = __bfloat16_as_ushort(hb);
+                a.out_res[o] = static_cast<int8_t>(pair_residual(y, __bfloat162float(hb)));
+            }
+        }
+    }
+    if (!(vmax <= kF32Max)) record_status(a.status, MOE_ERR_DEVICE_CHECK);
 }
 
 template <int MODE, int BN_>
@@ -369,9 +419,11 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
         // gate/up: Wg and Wu tiles are adjacent, one bf16 MMA of N = 2 BN;
         // kDown: fp16 act x fp16 Wd; kDownSplit: bf16 act hi x bf16 Wd, then
         // act lo x the same Wd, per K step
+        // down (swapped): A = 128 weight rows, B = the pass's kSubRows rows
         constexpr uint32_t idesc = MODE == kGateUp ? idesc_bf16_f32(kBlockM, 2 * BN)
-                                   : MODE == kDown ? idesc_f16_f32(kBlockM, BN)
-                                                   : idesc_bf16_f32(kBlockM, BN);
+                                   : MODE == kDown ? idesc_f16_f32(kBlockM, kSubRows)
+                                                   : idesc_bf16_f32(kBlockM, kSubRows);
+        static_assert(!is_down(MODE) || BN == 2 * kBlockM, "down tiles: two 128-row halves");
         int g = 0, it = 0;
         bool failed = false;
         for (int tile = blockIdx.x, j = 0; tile < total_tiles && !failed; tile += gridDim.x, ++j) {
@@ -400,10 +452,25 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
                             const uint64_t da = sw128_kmajor_desc(smem_addr(st));
                             const uint64_t da_lo = sw128_kmajor_desc(smem_addr(st + C::LO_OFFSET));
                             const uint64_t db = sw128_kmajor_desc(smem_addr(st + kBOffset));
+                            const uint64_t db1 =
+                                sw128_kmajor_desc(smem_addr(st + kBOffset + kATileBytes));
 #pragma unroll
                             for (int kk = 0; kk < kBlockK / 16; ++kk) {
-                                mma_f16kind(d, da + 2 * kk, db + 2 * kk, idesc, (kc | kk) != 0);
-                                if (kSplit) mma_f16kind(d, da_lo + 2 * kk, db + 2 * kk, idesc, 1);
+                                const uint32_t acc_on = (kc | kk) != 0;
+                                if (MODE == kGateUp) {
+                                    mma_f16kind(d, da + 2 * kk, db + 2 * kk, idesc, acc_on);
+                                } else {
+                                    // columns [0, kSubRows): weight rows 0-127;
+                                    // [kSubRows, 2 kSubRows): rows 128-255
+                                    mma_f16kind(d, db + 2 * kk, da + 2 * kk, idesc, acc_on);
+                                    mma_f16kind(d + kSubRows, db1 + 2 * kk, da + 2 * kk, idesc,
+                                                acc_on);
+                                    if (kSplit) {
+                                        mma_f16kind(d, db + 2 * kk, da_lo + 2 * kk, idesc, 1);
+                                        mma_f16kind(d + kSubRows, db1 + 2 * kk, da_lo + 2 * kk,
+                                                    idesc, 1);
+                                    }
+                                }
                             }
                             mma_commit(&sm->empty[s]);
                         }
@@ -439,7 +506,9 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
             for (int p = 0; p < passes; ++p, ++it) {
                 const int acc = it & 1;
                 TileRow r = no_tile_row();
-                if (quarter == 0 && lane < kSubRows)
+                // gate/up: lane i of warp 4 holds row i; down: lane i of every
+                // epilogue warp holds row i (column i of the swapped result)
+                if ((is_down(MODE) || quarter == 0) && lane < kSubRows)
                     r = tile_row<MODE>(a, block_of(tile), p * kSubRows + lane);
                 bool ok = true;
                 if (lane == 0) ok = mbar_wait(&sm->acc_full[acc], (it >> 1) & 1, abort_flag);
@@ -453,7 +522,13 @@ __global__ void __launch_bounds__(kSparseThreads, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                if (quarter == 0) store_tile<MODE, BN>(a, tmem + acc * kAccCols, r, tile % n_tiles);
+                if (MODE == kGateUp) {
+                    if (quarter == 0) store_tile<MODE, BN>(a, tmem + acc * kAccCols, r, tile % n_tiles);
+                } else {
+                    store_tile_swapped<kSubRows>(
+                        a, tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kAccCols, r,
+                        (tile % n_tiles) * BN + quarter * 32 + lane, lane);
+                }
                 if (MODE == kGateUp && handoff && quarter == 0 && p == passes - 1) {
                     // publish the tile: its rows' stores, then the count
                     fence_proxy_async_global();

@@ -224,9 +224,9 @@ EDGE = [
     ("shared-3-chunks", 200, 128, 8, 2, 64, 160, False),
     ("pairs-shared-3-chunks", 600, 128, 4, 2, 96, 200, True),
     ("sparse-shared-3-chunks", 24, 128, 16, 2, 64, 136, False),
-    # the limit on experts: routed experts plus shared chunks at exactly
-    # 256 (E + C, C = 2)
-    ("shared-at-expert-limit", 40, 64, 254, 4, 32, 64, False),
+    # the limits on experts with a shared expert: E = 248 (the shared gate's
+    # router column follows E rounded up to 8) and E + C = 256 (C = 8 chunks)
+    ("shared-at-expert-limit", 40, 64, 248, 4, 32, 256, False),
 ]
 
 
