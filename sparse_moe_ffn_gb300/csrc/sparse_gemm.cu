@@ -23,11 +23,11 @@
 // Down: the operands swap roles, so that the MMA's M side is the weights'
 // and its N side the pass's rows: D^T = Wd * act^T as two M = 128 MMAs
 // (weight rows 0-127 and 128-255 of the tile) of N = rows per pass (32, or
-// 16 for kDownSplit, whose lo MMAs read the lo rows), K = 16 each.  An M =
-// 128 MMA over 16 real rows did 8x the tensor work of this form, and with
-// the hi/lo pair kept the tensor pipe ~60% busy in a kernel that should
-// only stream weights.  Each product and each K step's sum reach an output
-// element in the same order either way.  The epilogue then holds one output
+// 16 for kDownSplit, whose lo MMAs read the lo rows), K = 16 each: no
+// padding row is read or multiplied (an M = 128 MMA over 16 real rows does
+// 8x the tensor work).  The kernel's time is set by its weight stream either
+// way.  Each product and each K step's sum reach an output element in the
+// same order as in the other tilings.  The epilogue then holds one output
 // column per thread (TMEM lane = weight row) for the pass's rows.
 // A block with more real rows than a pass holds is computed as several
 // passes over K (rare at decode); real rows come first in a block, so a
@@ -76,8 +76,8 @@ struct SparseCfg {
     static constexpr int STAGE_BYTES = kSubTileBytes + B_BYTES;
     static constexpr int STAGES = (224 * 1024 / STAGE_BYTES) < kSparseMaxStages
                                       ? (224 * 1024 / STAGE_BYTES) : kSparseMaxStages;
-    // the MMA reads a 16 KB (128-row) A operand from the A region's start
-    // (and, split, from the lo rows' start)
+    // gate/up's MMA reads a 16 KB (128-row) A operand from the A region's
+    // start (down's swapped MMAs read only the pass's rows)
     static_assert(STAGE_BYTES >= (A_COPIES - 1) * LO_OFFSET + kATileBytes,
                   "a 128-row A read would leave the stage");
     static_assert(STAGES * STAGE_BYTES + 1024 + 1024 <= 227 * 1024, "shared memory");
