@@ -340,8 +340,10 @@ moe_status_t moe_shared_expert_prepared(const moe_bf16_t *x, const float *shared
  * [N*k, H] (ypair_hi bf16, ypair_res int8); yshared: pair rows [N*S, H]
  * (moe_shared_expert's output, S = moe_shared_chunks(I, I_s)) with
  * 1 <= S <= 256, or both planes NULL (shared_slots ignored); out [N, H]
- * bf16; every plane 16-byte aligned.  moe_forward ends with the same
- * kernel, its k + C slots per token all in ypair.
+ * bf16; every plane 16-byte aligned (with 32-byte aligned planes and
+ * H % 16 == 0, large batches read 32 bytes at a time; every form adds the
+ * same values in the same order).  moe_forward ends with the same kernels,
+ * its k + C slots per token all in ypair.
  * ---------------------------------------------------------------------- */
 moe_status_t moe_combine(const moe_bf16_t *ypair_hi, const int8_t *ypair_res,
                          const moe_bf16_t *yshared_hi, const int8_t *yshared_res,
