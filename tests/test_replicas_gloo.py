@@ -68,3 +68,17 @@ def test_bench_gpus_2_starts_two_ranks():
     assert len(lines) == 1, r.stdout
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference" and rec["n_gpus"] == 2
+    # the line the driver parses: every key of the bench contract, with the
+    # reference arm's own e2e (no host copies) and its cpu_baseline
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in rec, key
+    assert rec["steps"] == 1 and rec["warmup"] == 3 and rec["higher_is_better"] is True
+    assert rec["scaling"] == "weak" and rec["vs_baseline"] is None
+    assert rec["value"] > 0 and rec["ms_per_step"] > 0
+    assert "workload" in rec["config"] and "N=16" in rec["config"]["workload"]
+    cb = rec["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == rec["value"] and cb["cores"] >= 1
+    assert rec["e2e"] == {"value": rec["value"], "unit": rec["unit"],
+                          "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
