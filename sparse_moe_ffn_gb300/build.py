@@ -7,6 +7,7 @@ sparse_moe_ffn_gb300.build`` (or ``__graft_entry__.build()``).
 """
 from __future__ import annotations
 
+import fcntl
 import os
 import shutil
 import subprocess
@@ -44,8 +45,19 @@ def _stale(target: str, deps) -> bool:
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile the library if any source or header changed; returns its path."""
+    """Compile the library if any source or header changed; returns its path.
+
+    Processes that build at the same time (one per GPU under torchrun) take
+    turns on a lock file; the later ones find everything up to date.  Each
+    object and the library are written to a temporary name and renamed, so
+    an interrupted compile never leaves a truncated file that looks fresh."""
     os.makedirs(BUILD, exist_ok=True)
+    with open(os.path.join(BUILD, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        return _build_locked(force, verbose, ptxas_info)
+
+
+def _build_locked(force: bool, verbose: bool, ptxas_info: bool) -> str:
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     headers.append(os.path.join(INCLUDE, "moe.h"))
     objs = []
@@ -56,10 +68,13 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         objs.append(o)
         if force or _stale(o, [s, *headers]):
             extra = ["-Xptxas", "-v"] if ptxas_info else []
-            jobs.append([nvcc(), *_flags(extra), "-c", s, "-o", o])
+            jobs.append(([nvcc(), *_flags(extra), "-c", s, "-o", o + f".tmp{os.getpid()}"], o))
 
-    def run(cmd):
+    def run(job):
+        cmd, o = job
         r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode == 0:
+            os.replace(cmd[-1], o)
         return cmd, r
 
     with ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 4))) as ex:
