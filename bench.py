@@ -113,7 +113,7 @@ def algorithmic_work(shape: MoEShape, touched: int):
         "gather": 0,  # x rows copied into expert order: an intermediate, not work
         "gate_up": touched * 2 * I * H * 2 + N * H * 2 + P * I * 2 + 2 * Is * H * 2 + N * Is * 2,
         "down": (touched * H * I * 2 + P * I * 2 + P * H * 2 + P * 4
-                 + Is * H * 2 + N * Is * 2 + N * H * 2),
+                 + ((Is * H * 2 + N * Is * 2 + N * H * 2) if Is else 0)),
         "shared": 0,
         "combine": P * H * 2 + N * H * 2 + (N * H * 2 if Is else 0),
     }
