@@ -243,3 +243,15 @@ def test_shared_expert_argument_errors(L, prepared):
     need = L.moe_shared_expert_workspace_bytes(64, 2048, 768, 2048)
     assert shared(ws_bytes=need - 1) == SMALL
     assert shared(N=0, x=None) == OK
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """No CPU fallback: with the library absent, the binding raises instead
+    of computing anything."""
+    from sparse_moe_ffn_gb300 import binding
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "LIB", str(tmp_path / "libsparse_moe_ffn.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        binding.lib()
+    with pytest.raises(RuntimeError, match="missing"):
+        binding.moe_shared_chunks(768, 2048)
